@@ -1,0 +1,443 @@
+"""Throughput of the scaled FP8 linear layer on one GB300 (and N replicas).
+
+Workload: the Llama-2-7B-shaped linears of one transformer block, forward +
+dgrad + wgrad, per-tensor delayed scaling (amax history 16, margin 0,
+"max"): tokens M = 8192, d = 4096 -> QKV 4096x12288, O 4096x4096,
+gate/up 4096x11008, down 11008x4096; X ~ N(0,1) with outlier channels,
+W ~ N(0, 0.02^2), dY ~ N(0, (1e-3)^2); E4M3 forward operands, E5M2
+gradients, FP32 wgrad buffer.  One step = fp8_linear_fwd + fp8_linear_bwd of
+all five linears (every quantiser, GEMM and scale update of the path).
+
+value       = sum over linears of 6*M*N*K / step time (TFLOP/s), inputs
+              resident in HBM, L2 flushed (256 MiB write) before each step.
+e2e         = the same through the public API with pinned host buffers:
+              H2D of X, W, dY and D2H of Y, dX, dW inside the timed region.
+roofline    = the dominant kernel (the FP8 GEMM): GEMM FLOPs / GEMM time,
+              from CUDA events around each GEMM of a component-wise pass of
+              the same steps, against 2x the measured bf16 dense peak.
+quantize    = the quantiser kernels' algorithmic bytes / their time against
+              the measured HBM copy bandwidth.
+cpu_baseline= the CPU oracle on a bounded sample of the same step.
+
+`--impl reference` times the CPU oracle (the only reference this method has)
+on the same workload; see the module docstring of oracle/.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+TOKENS = 8192
+LINEARS = [("qkv", 4096, 12288), ("o", 4096, 4096), ("gate", 4096, 11008),
+           ("up", 4096, 11008), ("down", 11008, 4096)]
+WORKLOAD = ("llama2-7b block linears fwd+dgrad+wgrad, per-tensor delayed scaling "
+            "(history 16, margin 0, max), tokens 8192")
+METRIC = "FP8 linear fwd+bwd TFLOP/s and quantize GB/s, as fraction of GB300 peak"
+FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _flops_step():
+    return sum(6.0 * TOKENS * n * k for _, k, n in LINEARS)
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import scaled_fp8_linear_gb300 as F
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    F.lib()
+    hbm_gbs, bf16_burst, bf16_sust, peak_kind = _peaks()
+    fp8_peak = 2.0 * bf16_sust   # FP8 dense = 2x bf16 dense (nominal ratio), sustained figure
+
+    recipe = F.Recipe(F.SCALING_DELAYED, history_len=16, margin=0, amax_algo=F.AMAX_MAX)
+    layers, Ws, Xs, dYs, Ys, dXs, dWs = [], [], [], [], [], [], []
+    for li, (name, K, N) in enumerate(LINEARS):
+        layers.append(F.Fp8Linear(TOKENS, N, K, recipe, device=dev))
+        Ws.append(synthetic.normal((N, K), 0.02, seed=1000 + li, device=dev))
+        n_out = 43 if K == 11008 else 16
+        Xs.append([synthetic.with_outlier_channels((TOKENS, K), 1.0, n_out, 50.0,
+                                                    seed=10 * li + s, device=dev) for s in range(2)])
+        dYs.append([synthetic.normal((TOKENS, N), 1e-3, seed=500 + 10 * li + s, device=dev)
+                    for s in range(2)])
+        Ys.append(torch.empty(TOKENS, N, dtype=torch.bfloat16, device=dev))
+        dXs.append(torch.empty(TOKENS, K, dtype=torch.bfloat16, device=dev))
+        dWs.append(torch.zeros(N, K, dtype=torch.float32, device=dev))
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(s):
+        for li in range(len(LINEARS)):
+            L = layers[li]
+            L.forward(Xs[li][s % 2], Ws[li], Y=Ys[li])
+            L.backward(dYs[li][s % 2], dX=dXs[li], dW=dWs[li], accumulate_dW=True)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for s in range(args.warmup):
+        step(s)
+    barrier()
+
+    clocks = Clocks(local)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier()
+    for s in range(args.steps):
+        flush.fill_(float(s))                       # evict L2 between steps (untimed)
+        ev[s][0].record(stream)
+        step(args.warmup + s)
+        ev[s][1].record(stream)
+    barrier()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    clk = clocks.stop()
+    assert F.fp8_device_status() == 0, "a kernel reported a timeout"
+    t_ms = sum(ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([t_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_ms = t.item()
+    flops = _flops_step() * args.steps * world
+    value = flops / (t_ms * 1e-3) / 1e12
+
+    # component-wise pass of the same steps: events around each kernel group
+    comp = component_pass(F, layers, Xs, dYs, Ws, Ys, dXs, dWs, flush, args, stream)
+
+    e2e = e2e_pass(F, recipe, dev, args, stream) if rank == 0 else None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+    if rank != 0:
+        return
+    gemm_tflops = comp["gemm_flops"] / (comp["gemm_ms"] * 1e-3) / 1e12
+    quant_gbs = comp["quant_bytes"] / (comp["quant_ms"] * 1e-3) / 1e9
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8(e4m3/e5m2)xfp8->fp32acc", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": TOKENS,
+                   "linears": {n: [k, n_] for n, k, n_ in LINEARS},
+                   "recipe": "HYBRID delayed, history 16, margin 0, amax max",
+                   "l2": "flushed (256 MiB write) before every timed step",
+                   "parallelism": "replicas" if world > 1 else "single-gpu"},
+        "roofline": {"bound": "tensor", "kernel": "gemm_tensor_kernel (tcgen05 kind::f8f6f4)",
+                     "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
+                     "peak_source": f"{peak_kind}: 2 x bf16_tflops_sustained (FP8/BF16 nominal 2x)",
+                     "traffic": None},
+        "quantize": {"achieved_gbs": round(quant_gbs, 1), "peak_gbs": hbm_gbs,
+                     "frac": round(quant_gbs / hbm_gbs, 4), "peak_source": f"{peak_kind} hbm_gbs"},
+        "kernels_ms_per_step": {k: round(v / args.steps, 4) for k, v in comp["by_kind"].items()},
+        "component_pass_ms_per_step": round(comp["total_ms"] / args.steps, 4),
+        "gpu_launches": 8 * len(LINEARS) * args.steps,
+        "e2e": e2e,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args)
+    print(json.dumps(out))
+
+
+def component_pass(F, layers, Xs, dYs, Ws, Ys, dXs, dWs, flush, args, stream):
+    """The steps of fp8_linear_fwd/bwd issued as the individual C-ABI calls
+    (same kernels, same order) with CUDA events around each call, to split
+    the step time between GEMMs, quantisers and scale updates."""
+    by_kind = {"gemm": 0.0, "quantize": 0.0, "update_scale": 0.0}
+    gemm_flops = quant_bytes = 0.0
+    total = 0.0
+    pending = []
+
+    def timed(kind, fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        pending.append((kind, a, b))
+
+    for s in range(args.steps):
+        flush.fill_(float(s))
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for li, (name, K, N) in enumerate(LINEARS):
+            L = layers[li]
+            M = TOKENS
+            X, W, dY = Xs[li][s % 2], Ws[li], dYs[li][s % 2]
+            am = L.amax
+            timed("quantize", lambda: F.fp8_quantize(X, F.E4M3, scale=L.scale[0:1], q=L.x_q,
+                                                     q_t=L.x_qt, amax_out=am[0:1]))
+            timed("quantize", lambda: F.fp8_quantize(W, F.E4M3, scale=L.scale[1:2], q=L.w_q,
+                                                     q_t=L.w_qt, amax_out=am[1:2]))
+            timed("gemm", lambda: F.fp8_gemm(L.x_q, F.E4M3, L.w_q, F.E4M3, L.scale_inv[0:1],
+                                             L.scale_inv[1:2], D=Ys[li]))
+            timed("update_scale", lambda: [F.fp8_update_scale(
+                am[r:r + 1], L.history[r], L.pos[r:r + 1], 16, F.AMAX_MAX, F.E4M3, 0, False,
+                L.scale[r:r + 1], L.scale_inv[r:r + 1]) for r in (0, 1)])
+            dyq = L.workspace[:M * N].view(M, N)
+            dyqt = L.workspace[L.workspace.numel() // 2:][:M * N].view(N, M)
+            timed("quantize", lambda: F.fp8_quantize(dY, F.E5M2, scale=L.scale[2:3], q=dyq,
+                                                     q_t=dyqt, amax_out=am[2:3]))
+            timed("gemm", lambda: F.fp8_gemm(dyq, F.E5M2, L.w_qt, F.E4M3, L.scale_inv[2:3],
+                                             L.scale_inv[1:2], D=dXs[li]))
+            timed("gemm", lambda: F.fp8_gemm(dyqt, F.E5M2, L.x_qt, F.E4M3, L.scale_inv[2:3],
+                                             L.scale_inv[0:1], out=F.OUT_F32, D=dWs[li],
+                                             accumulate=True))
+            timed("update_scale", lambda: F.fp8_update_scale(
+                am[2:3], L.history[2], L.pos[2:3], 16, F.AMAX_MAX, F.E5M2, 0, False,
+                L.scale[2:3], L.scale_inv[2:3]))
+            gemm_flops += 6.0 * M * N * K
+            # quantiser bytes: bf16 read (2 B) + q and q_t writes (1 B + 1 B) per element
+            quant_bytes += 4.0 * (M * K + N * K + M * N)
+        t1.record(stream)
+        pending.append(("__step", t0, t1))
+    torch.cuda.synchronize()
+    for kind, a, b in pending:
+        ms = a.elapsed_time(b)
+        if kind == "__step":
+            total += ms
+        else:
+            by_kind[kind] += ms
+    return {"by_kind": by_kind, "gemm_ms": by_kind["gemm"], "quant_ms": by_kind["quantize"],
+            "gemm_flops": gemm_flops, "quant_bytes": quant_bytes, "total_ms": total}
+
+
+def e2e_pass(F, recipe, dev, args, stream):
+    """Public API with host buffers: per step H2D of X, W, dY (pinned), the
+    five linears' fwd+bwd, D2H of Y, dX, dW; timed with events on the stream."""
+    hX, hW, hdY, dX_, dW_, dY_, hY, hdX, hdW, layers, dXd, dWd, dYd = ([] for _ in range(13))
+    for li, (name, K, N) in enumerate(LINEARS):
+        hX.append(synthetic.with_outlier_channels((TOKENS, K), 1.0, 16, 50.0, seed=li).pin_memory())
+        hW.append(synthetic.normal((N, K), 0.02, seed=1000 + li).pin_memory())
+        hdY.append(synthetic.normal((TOKENS, N), 1e-3, seed=500 + li).pin_memory())
+        hY.append(torch.empty(TOKENS, N, dtype=torch.bfloat16).pin_memory())
+        hdX.append(torch.empty(TOKENS, K, dtype=torch.bfloat16).pin_memory())
+        hdW.append(torch.empty(N, K, dtype=torch.float32).pin_memory())
+        layers.append(F.Fp8Linear(TOKENS, N, K, recipe, device=dev))
+        dX_.append(torch.empty(TOKENS, K, dtype=torch.bfloat16, device=dev))
+        dW_.append(torch.empty(N, K, dtype=torch.bfloat16, device=dev))   # device copy of W
+        dY_.append(torch.empty(TOKENS, N, dtype=torch.bfloat16, device=dev))
+        dXd.append(torch.empty(TOKENS, K, dtype=torch.bfloat16, device=dev))  # device copy of X
+        dWd.append(torch.zeros(N, K, dtype=torch.float32, device=dev))
+        dYd.append(torch.empty(TOKENS, N, dtype=torch.bfloat16, device=dev))
+    h2d = sum(t.numel() * t.element_size() for t in hX + hW + hdY)
+    d2h = sum(t.numel() * t.element_size() for t in hY + hdX + hdW)
+    Ydev = [torch.empty(TOKENS, n, dtype=torch.bfloat16, device=dev) for _, _, n in LINEARS]
+
+    def one():
+        for li in range(len(LINEARS)):
+            dXd[li].copy_(hX[li], non_blocking=True)
+            dW_[li].copy_(hW[li], non_blocking=True)
+            dYd[li].copy_(hdY[li], non_blocking=True)
+            L = layers[li]
+            L.forward(dXd[li], dW_[li], Y=Ydev[li])
+            L.backward(dYd[li], dX=dX_[li], dW=dWd[li], accumulate_dW=False)
+            hY[li].copy_(Ydev[li], non_blocking=True)
+            hdX[li].copy_(dX_[li], non_blocking=True)
+            hdW[li].copy_(dWd[li], non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        one()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 5))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    return {"value": round(_flops_step() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 3), "steps": n, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def _oracle_sample_step(rows_per_gemm, inputs, states):
+    """One step of the oracle on a bounded sample: whole-tensor amax, scale
+    update and quantisation of X, W, dY for every linear (the oracle's
+    linear_fwd / linear_bwd), and `rows_per_gemm` full output rows of each
+    of the 15 GEMMs.  Returns the FLOPs of the sampled GEMM rows."""
+    import numpy as np
+    import oracle
+    flops = 0.0
+    for li, (name, K, N) in enumerate(LINEARS):
+        bx, bw, bdy = inputs[li]
+        st, rec = states[li]
+        rows = np.arange(rows_per_gemm)
+        oracle.linear_fwd(bx, bw, rec, st, rows=rows)
+        oracle.linear_bwd(bdy, rec, st, rows_dx=rows, rows_dw=rows)
+        flops += 2.0 * rows_per_gemm * (N * K + K * N + K * TOKENS)
+    return flops
+
+
+def _oracle_inputs():
+    import oracle
+    inputs, states = [], []
+    rec = oracle.Recipe(scaling=oracle.SCALING_DELAYED, history_len=16)
+    for li, (name, K, N) in enumerate(LINEARS):
+        n_out = 43 if K == 11008 else 16
+        X = synthetic.with_outlier_channels((TOKENS, K), 1.0, n_out, 50.0, seed=10 * li)
+        W = synthetic.normal((N, K), 0.02, seed=1000 + li)
+        dY = synthetic.normal((TOKENS, N), 1e-3, seed=500 + 10 * li)
+        inputs.append((synthetic.bf16_bits(X), synthetic.bf16_bits(W), synthetic.bf16_bits(dY)))
+        states.append((oracle.LinearState(rec), rec))
+    return inputs, states
+
+
+def cpu_baseline(args):
+    import oracle
+    inputs, states = _oracle_inputs()
+    rows = args.cpu_rows
+    t0 = time.perf_counter()
+    flops = _oracle_sample_step(rows, inputs, states)
+    dt = time.perf_counter() - t0
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": (f"one step: whole-tensor amax/scale/quantise(+transpose) of X, W, dY of the "
+                       f"5 linears, and {rows} full output rows of each of the 15 GEMMs "
+                       f"(fp64 accumulation); value = sampled GEMM FLOPs / wall time")}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    inputs, states = _oracle_inputs()
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        _oracle_sample_step(rows, inputs, states)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(args.steps):
+        flops += _oracle_sample_step(rows, inputs, states)
+    dt = time.perf_counter() - t0
+    v = flops / dt / 1e12
+    sample = (f"per step: whole-tensor amax/scale/quantise(+transpose) of X, W, dY of the 5 "
+              f"linears and {rows} full output rows of each of the 15 GEMMs; value = sampled "
+              f"GEMM FLOPs / wall time")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": TOKENS,
+                   "linears": {n: [k, n_] for n, k, n_ in LINEARS}},
+        "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=32)
+    ap.add_argument("--ref-rows", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,207 @@
+/*
+ * fp8linear.h -- C ABI of the scaled FP8 linear layer for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the FP8 linear layer of mixed-precision LLM training as
+ * "Mixed Precision LLM Training: The Complete Guide" describes it:
+ *   forward   Y  = X . W^T            X [M x K], W [N x K] cast to E4M3
+ *   dgrad     dX = dY . W             dY [M x N] cast to E5M2
+ *   wgrad     dW (+)= dY^T . X        FP32 result, accumulated across calls
+ * with FP32 accumulation inside every GEMM ("Skipping the BAcc accumulator
+ * promotion"; "DeepSeek FP8 training recipe" > "Mixed-precision
+ * accumulation"), per-tensor scales ("Transformer Engine internals" >
+ * "Per-tensor scaling"), either current (dynamic) or delayed from an amax
+ * history ("Delayed scaling", "History-based scaling"), or block-wise scales
+ * ("DeepSeek FP8 training recipe" > "Block-wise scaling at 128
+ * granularity").  Power-of-two scales follow the per-tensor "scaling bias"
+ * of "Training and inference of large language models using 8-bit floating
+ * point".
+ *
+ * Conventions shared by every call:
+ *   - Tensor arguments are DEVICE pointers owned by the caller.  Matrices are
+ *     row-major and densely packed; bf16 tensors are passed as void*.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t, NULL = the
+ *     legacy default stream) and does no host synchronisation.  Scales,
+ *     amaxes and histories stay in device memory; a call that reads a scale
+ *     sees the value left by earlier work on the same stream.
+ *   - The library allocates no device memory.  Calls that need scratch take
+ *     a caller-owned `workspace` of at least fp8_workspace_size() bytes.
+ *   - Return value: FP8_OK, or a negative status; on failure nothing was
+ *     launched, except for FP8_ERR_CUDA, and fp8_last_error() returns a
+ *     message (thread-local).
+ *   - A tensor with no elements may be passed as NULL.
+ *   - FP8 codes are round-to-nearest-even with saturation to the largest
+ *     finite value (448 for E4M3, 57344 for E5M2); NaN becomes the code 0x7F.
+ */
+#ifndef FP8LINEAR_H
+#define FP8LINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ----------------------------------------------------------------- status */
+#define FP8_OK               0
+#define FP8_ERR_INVALID_ARG (-1)  /* null pointer, unknown enum, value out of range */
+#define FP8_ERR_SHAPE       (-2)  /* a dimension violates the call's multiple-of rule */
+#define FP8_ERR_ALIGN       (-3)  /* a pointer is not 16-byte aligned */
+#define FP8_ERR_CUDA        (-4)  /* a CUDA call failed; see fp8_last_error() */
+#define FP8_ERR_TIMEOUT     (-5)  /* a kernel's bounded wait gave up (device status) */
+#define FP8_ERR_UNSUPPORTED (-6)  /* valid combination that this build does not run */
+
+/* ------------------------------------------------------------------ enums */
+typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format_t;
+typedef enum { FP8_OUT_BF16 = 0, FP8_OUT_F32 = 1 } fp8_out_t;
+typedef enum { FP8_AMAX_MAX = 0, FP8_AMAX_MOST_RECENT = 1 } fp8_amax_algo_t;
+typedef enum {
+    FP8_GRAN_TENSOR = 0,     /* one scale for the tensor                    */
+    FP8_GRAN_1x128 = 1,      /* one scale per 128 consecutive row elements  */
+    FP8_GRAN_128x128 = 2     /* one scale per 128 x 128 tile                */
+} fp8_gran_t;
+typedef enum {
+    FP8_LAYOUT_TN = 0        /* A [M x K] and B [N x K], both K-contiguous   */
+} fp8_layout_t;
+typedef enum {
+    FP8_SCALING_DELAYED = 0, /* per-tensor, scale from the amax history      */
+    FP8_SCALING_DYNAMIC = 1, /* per-tensor, scale from the tensor's own amax */
+    FP8_SCALING_BLOCK = 2    /* 1x128 activations, 128x128 weights           */
+} fp8_scaling_t;
+
+/* Recipe of one linear layer ("Calibration deep dive" > "Dynamic
+ * calibration": margin, amax_history_len, amax_compute_algo; "The HYBRID
+ * recipe": E4M3 forward, E5M2 backward). */
+typedef struct {
+    int32_t scaling;      /* fp8_scaling_t                                   */
+    int32_t margin;       /* 0..64: scale = fp8_max / amax / 2^margin        */
+    int32_t history_len;  /* 1..1024, delayed scaling only                   */
+    int32_t amax_algo;    /* fp8_amax_algo_t, delayed scaling only           */
+    int32_t pow2;         /* nonzero: round scales down to powers of two     */
+    int32_t fwd_format;   /* format of X and W (FP8_E4M3 for HYBRID)         */
+    int32_t bwd_format;   /* format of dY (FP8_E5M2 for HYBRID)              */
+} fp8_recipe_t;
+
+/* Caller-owned device state of one linear layer.  Role r indexes the
+ * per-tensor arrays: 0 = X (forward activation), 1 = W (forward weight),
+ * 2 = dY (backward gradient) -- one scale per (tensor, format) pair
+ * ("Transformer Engine internals" > "Per-tensor scaling").  Everything here
+ * is plain device memory, so checkpointing the layer means copying it. */
+typedef struct {
+    float*   scale;      /* [3] quantisation scales, initialise to 1           */
+    float*   scale_inv;  /* [3] 1/scale, initialise to 1                       */
+    float*   amax;       /* [3] out: max|x| of the last tensor of each role    */
+    float*   history;    /* [3][H] amax history (H = history_len, 1 for        */
+                         /*   dynamic), initialise to 0                        */
+    int32_t* pos;        /* [3] next history slot, initialise to 0             */
+    uint8_t* x_q;        /* [M][K] written by fwd                              */
+    uint8_t* x_qt;       /* [K][M] written by fwd (per-tensor modes)           */
+    uint8_t* w_q;        /* [N][K] written by fwd                              */
+    uint8_t* w_qt;       /* [K][N] written by fwd (per-tensor modes)           */
+    float*   x_sinv;     /* [M][K/128] written by fwd (block mode)             */
+    float*   w_sinv;     /* [N/128][K/128] written by fwd (block mode)         */
+    float*   qscale_inv; /* [2] out: dequantisation factors that x_q/x_qt (0)  */
+                         /*   and w_q/w_qt (1) were cast with; written by fwd  */
+                         /*   (per-tensor modes), read by bwd                  */
+} fp8_linear_state_t;
+
+/* ---------------------------------------------------------------- calls */
+
+/* amax = max |x| over n bf16 values ("Per-tensor scaling": the scale is set
+ * from the tensor's max absolute value).  Computed as an integer max over
+ * the |bf16| bit patterns: exact and independent of order; any NaN gives
+ * NaN.  x: 16-byte aligned, n >= 0 (n = 0 gives 0).  amax: one float,
+ * overwritten. */
+int fp8_amax(const void* x, int64_t n, float* amax, void* stream);
+
+/* One step of the scale update ("Delayed scaling", "History-based scaling";
+ * "torch.compile and FP8" for the all-zero skip):
+ *   history[*pos] = *amax;  *pos = (*pos + 1) % history_len;
+ *   a = (algo == FP8_AMAX_MAX) ? max(history) : *amax;
+ *   if a is 0 or not finite: *scale and *scale_inv are left unchanged;
+ *   else  s = fp8_max(format) / a            (fp32, round to nearest)
+ *         s = s * 2^-margin                  (fp32)
+ *         s = min(max(s, FLT_MIN), FLT_MAX)
+ *         if pow2: s = 2^floor(log2 s)
+ *         *scale = s;  *scale_inv = 1 / s    (fp32, round to nearest).
+ * amax values are magnitudes (>= 0 or NaN).  history_len 1..1024, margin
+ * 0..64.  Dynamic scaling is history_len = 1.  All pointers device. */
+int fp8_update_scale(const float* amax, float* history, int32_t* pos, int history_len,
+                     int algo, int format, int margin, int pow2, float* scale,
+                     float* scale_inv, void* stream);
+
+/* Cast a bf16 matrix x [rows x cols] to FP8.
+ * granularity FP8_GRAN_TENSOR: q = fp8(fp32(x) * (*scale)), one fp32 multiply
+ *   then the saturating round-to-nearest-even cast ("Per-tensor scaling").
+ *   q_t (nullable) receives the transpose [cols x rows] in the same launch;
+ *   amax_out (nullable) receives max|x| (fused reduction, overwritten).
+ *   Shape rule: rows*cols any when q_t is NULL; with q_t, rows and cols must
+ *   be multiples of 16.
+ * granularity FP8_GRAN_1x128 / FP8_GRAN_128x128: each 1x128 row segment or
+ *   128x128 tile gets its own scale fp8_max/amax_block (margin 0; 1 for an
+ *   all-zero or non-finite block; rounded down to a power of two if pow2),
+ *   and scale_inv_blocks receives 1/scale as [rows/b][cols/128] (b = 1 or
+ *   128) ("Block-wise scaling at 128 granularity").  scale, q_t and amax_out
+ *   must be NULL.  cols must be a multiple of 128 (and rows, for 128x128).
+ * x, q, q_t: 16-byte aligned.  format: FP8_E4M3 or FP8_E5M2. */
+int fp8_quantize(const void* x, int64_t rows, int64_t cols, int format, int granularity,
+                 const float* scale, int pow2, uint8_t* q, uint8_t* q_t,
+                 float* scale_inv_blocks, float* amax_out, void* stream);
+
+/* Scaled FP8 GEMM, layout FP8_LAYOUT_TN:
+ *   D[m][n] = sum_k sa(m,k) * sb(n,k) * A[m][k] * B[n][k]
+ * with FP32 accumulation on the tensor cores.  sa, sb are DEQUANTISATION
+ * factors (scale_inv = 1/scale, device memory):
+ *   FP8_GRAN_TENSOR   scale_inv[0]
+ *   FP8_GRAN_1x128    scale_inv[row][k/128]            (A only)
+ *   FP8_GRAN_128x128  scale_inv[row/128][k/128]
+ * Per-tensor factors multiply the FP32 result once; block factors scale each
+ * 128-deep partial sum before it is added ("applied during the matmul").
+ * out FP8_OUT_BF16: D is bf16 [M x N], rounded to nearest even.
+ * out FP8_OUT_F32:  D is fp32 [M x N]; accumulate != 0 adds to D.
+ * Shape rule: M >= 0; N, K multiples of 16 (multiples of 128 when either
+ * operand uses block scales).  A, B, D: 16-byte aligned.
+ * fa, fb: FP8_E4M3 / FP8_E5M2 in any combination. */
+int fp8_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
+             int64_t K, int layout, int ga, const float* scale_inv_a, int gb,
+             const float* scale_inv_b, void* D, int out, int accumulate, void* stream);
+
+/* Bytes of workspace that fp8_linear_fwd / fp8_linear_bwd need for a layer
+ * of this shape and recipe (0 if none).  Returns 0 for an invalid recipe. */
+size_t fp8_workspace_size(int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe);
+
+/* Forward pass Y [M x N] (bf16) = X [M x K] . W [N x K]^T.
+ *   delayed: quantise X and W with the current scales (fusing their amax and
+ *            transposes), GEMM, then update the X and W scales (the new
+ *            scales take effect on the next call: one-step lag);
+ *   dynamic: amax, scale update and quantisation of X and W, then GEMM;
+ *   block:   1x128 quantisation of X, 128x128 of W, block-scaled GEMM.
+ * Writes state->x_q/x_qt/w_q/w_qt (or x_q/w_q/x_sinv/w_sinv) for the
+ * backward pass.  Shape rule: M, N, K multiples of 16 (128 for block). */
+int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K,
+                   const fp8_recipe_t* recipe, const fp8_linear_state_t* state, void* Y,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward pass after fp8_linear_fwd on the same state:
+ *   dX [M x K] (bf16) = dY . W,   dW [N x K] (fp32) = dY^T . X  (+ dW if
+ *   accumulate_dW).  dY is cast to the recipe's bwd_format with the dY
+ *   role's scale (delayed: current scale, then update; dynamic: its own
+ *   amax).  The quantised dY and its transpose live in the workspace.
+ * Block scaling has no backward in this build (FP8_ERR_UNSUPPORTED). */
+int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K,
+                   const fp8_recipe_t* recipe, const fp8_linear_state_t* state, void* dX,
+                   float* dW, int accumulate_dW, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char* fp8_last_error(void);
+
+/* Read (and, if clear != 0, reset) the device status word that kernels set
+ * when a bounded wait gives up (bit 0: timeout).  Synchronises the device.
+ * Returns FP8_OK and *status = 0 when every kernel finished normally. */
+int fp8_device_status(int* status, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8LINEAR_H */

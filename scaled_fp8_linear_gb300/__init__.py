@@ -1,0 +1,304 @@
+"""Scaled FP8 linear layer for NVIDIA GB300 (sm_103a).
+
+A thin Python binding of the C-ABI library ``libfp8linear.so`` (declared in
+``include/fp8linear.h``).  The functions here carry the C names and only
+marshal arguments: torch tensors supply device memory and the current CUDA
+stream, and every step of the computation runs in the library's kernels.
+There is no fallback: if the library has not been built (``build()``), or
+no GPU is present, every call raises.
+
+The method is the FP8 linear layer of "Mixed Precision LLM Training: The
+Complete Guide": E4M3 forward operands, E5M2 gradients, FP32 accumulation,
+per-tensor (dynamic or delayed/history) or block-wise (1x128 / 128x128)
+scales.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "E4M3", "E5M2", "OUT_BF16", "OUT_F32", "AMAX_MAX", "AMAX_MOST_RECENT",
+    "GRAN_TENSOR", "GRAN_1x128", "GRAN_128x128", "LAYOUT_TN",
+    "SCALING_DELAYED", "SCALING_DYNAMIC", "SCALING_BLOCK",
+    "Fp8Error", "Recipe", "LinearStateC", "Fp8Linear", "build", "lib", "library_path",
+    "fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_gemm", "fp8_workspace_size",
+    "fp8_linear_fwd", "fp8_linear_bwd", "fp8_last_error", "fp8_device_status",
+]
+
+E4M3, E5M2 = 0, 1
+OUT_BF16, OUT_F32 = 0, 1
+AMAX_MAX, AMAX_MOST_RECENT = 0, 1
+GRAN_TENSOR, GRAN_1x128, GRAN_128x128 = 0, 1, 2
+LAYOUT_TN = 0
+SCALING_DELAYED, SCALING_DYNAMIC, SCALING_BLOCK = 0, 1, 2
+
+_STATUS = {0: "FP8_OK", -1: "FP8_ERR_INVALID_ARG", -2: "FP8_ERR_SHAPE", -3: "FP8_ERR_ALIGN",
+           -4: "FP8_ERR_CUDA", -5: "FP8_ERR_TIMEOUT", -6: "FP8_ERR_UNSUPPORTED"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "_build", "libfp8linear.so")
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library in-tree (nvcc, sm_103a)."""
+    from . import nvcc_build
+    return nvcc_build.build(force=force)
+
+
+class Fp8Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class Recipe(ctypes.Structure):
+    """fp8_recipe_t: HYBRID recipe (E4M3 forward, E5M2 backward) by default."""
+    _fields_ = [("scaling", ctypes.c_int32), ("margin", ctypes.c_int32),
+                ("history_len", ctypes.c_int32), ("amax_algo", ctypes.c_int32),
+                ("pow2", ctypes.c_int32), ("fwd_format", ctypes.c_int32),
+                ("bwd_format", ctypes.c_int32)]
+
+    def __init__(self, scaling=SCALING_DELAYED, margin=0, history_len=16, amax_algo=AMAX_MAX,
+                 pow2=False, fwd_format=E4M3, bwd_format=E5M2):
+        super().__init__(scaling, margin, history_len, amax_algo, int(bool(pow2)), fwd_format,
+                         bwd_format)
+
+
+_vp = ctypes.c_void_p
+
+
+class LinearStateC(ctypes.Structure):
+    """fp8_linear_state_t: device pointers of one layer's scaling state."""
+    _fields_ = [("scale", _vp), ("scale_inv", _vp), ("amax", _vp), ("history", _vp),
+                ("pos", _vp), ("x_q", _vp), ("x_qt", _vp), ("w_q", _vp), ("w_qt", _vp),
+                ("x_sinv", _vp), ("w_sinv", _vp), ("qscale_inv", _vp)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfp8linear.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build the CUDA library first "
+                           "(scaled_fp8_linear_gb300.build())")
+    L = ctypes.CDLL(path)
+    i, i64, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    L.fp8_amax.argtypes = [_vp, i64, _vp, _vp]
+    L.fp8_update_scale.argtypes = [_vp, _vp, _vp, i, i, i, i, i, _vp, _vp, _vp]
+    L.fp8_quantize.argtypes = [_vp, i64, i64, i, i, _vp, i, _vp, _vp, _vp, _vp, _vp]
+    L.fp8_gemm.argtypes = [_vp, i, _vp, i, i64, i64, i64, i, i, _vp, i, _vp, _vp, i, i, _vp]
+    L.fp8_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(Recipe)]
+    L.fp8_workspace_size.restype = sz
+    L.fp8_linear_fwd.argtypes = [_vp, _vp, i64, i64, i64, ctypes.POINTER(Recipe),
+                                 ctypes.POINTER(LinearStateC), _vp, _vp, sz, _vp]
+    L.fp8_linear_bwd.argtypes = [_vp, i64, i64, i64, ctypes.POINTER(Recipe),
+                                 ctypes.POINTER(LinearStateC), _vp, _vp, i, _vp, sz, _vp]
+    L.fp8_last_error.restype = ctypes.c_char_p
+    L.fp8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i]
+    for name in ("fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_gemm", "fp8_linear_fwd",
+                 "fp8_linear_bwd", "fp8_device_status"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def fp8_last_error() -> str:
+    return lib().fp8_last_error().decode()
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise Fp8Error(status, fp8_last_error())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t, what, dtype=None, device=True):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what}: expected a tensor")
+    if device and not t.is_cuda:
+        raise ValueError(f"{what}: must be a CUDA tensor")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{what}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: must be contiguous")
+    return t.data_ptr()
+
+
+_U8 = (torch.uint8, torch.float8_e4m3fn, torch.float8_e5m2)
+
+
+# ------------------------------------------------------------------ raw calls
+
+def fp8_amax(x: torch.Tensor, amax: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """max |x| of a bf16 tensor into a 1-element fp32 device tensor."""
+    if amax is None:
+        amax = torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(lib().fp8_amax(_ptr(x, "x", torch.bfloat16), x.numel(),
+                          _ptr(amax, "amax", torch.float32), _stream(stream)))
+    return amax
+
+
+def fp8_update_scale(amax, history, pos, history_len, algo, fmt, margin, pow2, scale,
+                     scale_inv, stream=None) -> None:
+    """One scale-update step on device state (see include/fp8linear.h)."""
+    _check(lib().fp8_update_scale(
+        _ptr(amax, "amax", torch.float32), _ptr(history, "history", torch.float32),
+        _ptr(pos, "pos", torch.int32), int(history_len), int(algo), int(fmt), int(margin),
+        int(bool(pow2)), _ptr(scale, "scale", torch.float32),
+        _ptr(scale_inv, "scale_inv", torch.float32), _stream(stream)))
+
+
+def fp8_quantize(x: torch.Tensor, fmt: int, granularity: int = GRAN_TENSOR, scale=None,
+                 pow2: bool = False, q=None, q_t=None, transpose: bool = False,
+                 scale_inv_blocks=None, amax_out=None, want_amax: bool = False, stream=None):
+    """Cast a 2-D bf16 tensor to FP8 codes (uint8).  Returns
+    (q, q_t or None, scale_inv_blocks or None, amax or None)."""
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D")
+    rows, cols = x.shape
+    dev = x.device
+    if q is None:
+        q = torch.empty(rows, cols, dtype=torch.uint8, device=dev)
+    if transpose and q_t is None:
+        q_t = torch.empty(cols, rows, dtype=torch.uint8, device=dev)
+    if granularity != GRAN_TENSOR and scale_inv_blocks is None:
+        br = 1 if granularity == GRAN_1x128 else 128
+        scale_inv_blocks = torch.empty(rows // br, cols // 128, dtype=torch.float32, device=dev)
+    if want_amax and amax_out is None:
+        amax_out = torch.empty(1, dtype=torch.float32, device=dev)
+    _check(lib().fp8_quantize(
+        _ptr(x, "x", torch.bfloat16), rows, cols, int(fmt), int(granularity),
+        _ptr(scale, "scale", torch.float32), int(bool(pow2)), _ptr(q, "q", _U8),
+        _ptr(q_t, "q_t", _U8), _ptr(scale_inv_blocks, "scale_inv_blocks", torch.float32),
+        _ptr(amax_out, "amax_out", torch.float32), _stream(stream)))
+    return q, q_t, scale_inv_blocks, amax_out
+
+
+def fp8_gemm(A: torch.Tensor, fa: int, B: torch.Tensor, fb: int, scale_inv_a, scale_inv_b,
+             ga: int = GRAN_TENSOR, gb: int = GRAN_TENSOR, out: int = OUT_BF16, D=None,
+             accumulate: bool = False, layout: int = LAYOUT_TN, stream=None) -> torch.Tensor:
+    """D = (A . B^T) with dequantisation factors; A [M,K], B [N,K] FP8 codes."""
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("A and B disagree on K")
+    if D is None:
+        D = torch.empty(M, N, dtype=torch.bfloat16 if out == OUT_BF16 else torch.float32,
+                        device=A.device)
+    _check(lib().fp8_gemm(
+        _ptr(A, "A", _U8), int(fa), _ptr(B, "B", _U8), int(fb), M, N, K, int(layout), int(ga),
+        _ptr(scale_inv_a, "scale_inv_a", torch.float32), int(gb),
+        _ptr(scale_inv_b, "scale_inv_b", torch.float32),
+        _ptr(D, "D", torch.bfloat16 if out == OUT_BF16 else torch.float32), int(out),
+        int(bool(accumulate)), _stream(stream)))
+    return D
+
+
+def fp8_workspace_size(M: int, N: int, K: int, recipe: Recipe) -> int:
+    return int(lib().fp8_workspace_size(M, N, K, ctypes.byref(recipe)))
+
+
+def fp8_linear_fwd(X, W, recipe: Recipe, state: "LinearStateC", Y, workspace=None,
+                   stream=None) -> None:
+    M, K = X.shape
+    N = W.shape[0]
+    _check(lib().fp8_linear_fwd(
+        _ptr(X, "X", torch.bfloat16), _ptr(W, "W", torch.bfloat16), M, N, K,
+        ctypes.byref(recipe), ctypes.byref(state), _ptr(Y, "Y", torch.bfloat16),
+        _ptr(workspace, "workspace"), 0 if workspace is None else workspace.numel(),
+        _stream(stream)))
+
+
+def fp8_linear_bwd(dY, M, N, K, recipe: Recipe, state: "LinearStateC", dX, dW,
+                   accumulate_dW: bool, workspace, stream=None) -> None:
+    _check(lib().fp8_linear_bwd(
+        _ptr(dY, "dY", torch.bfloat16), M, N, K, ctypes.byref(recipe), ctypes.byref(state),
+        _ptr(dX, "dX", torch.bfloat16), _ptr(dW, "dW", torch.float32), int(bool(accumulate_dW)),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
+
+
+def fp8_device_status(clear: bool = True) -> int:
+    st = ctypes.c_int(0)
+    _check(lib().fp8_device_status(ctypes.byref(st), int(bool(clear))))
+    return st.value
+
+
+# ------------------------------------------------------------- layer object
+
+class Fp8Linear:
+    """One FP8 linear layer's device state (scales, histories, quantised
+    operands, workspace), allocated with torch on `device`, plus fwd/bwd
+    calls into the library.  `state_dict()` / `load_state_dict()` copy the
+    scaling state for checkpoints."""
+
+    def __init__(self, M: int, N: int, K: int, recipe: Recipe | None = None, device="cuda"):
+        self.M, self.N, self.K = M, N, K
+        self.recipe = recipe or Recipe()
+        dev = torch.device(device)
+        H = self.recipe.history_len if self.recipe.scaling == SCALING_DELAYED else 1
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.scale = torch.ones(3, **f32)
+        self.scale_inv = torch.ones(3, **f32)
+        self.amax = torch.zeros(3, **f32)
+        self.history = torch.zeros(3, H, **f32)
+        self.pos = torch.zeros(3, dtype=torch.int32, device=dev)
+        self.qscale_inv = torch.ones(2, **f32)
+        u8 = dict(dtype=torch.uint8, device=dev)
+        self.x_q = torch.empty(M, K, **u8)
+        self.w_q = torch.empty(N, K, **u8)
+        block = self.recipe.scaling == SCALING_BLOCK
+        self.x_qt = None if block else torch.empty(K, M, **u8)
+        self.w_qt = None if block else torch.empty(K, N, **u8)
+        self.x_sinv = torch.empty(M, K // 128, **f32) if block else None
+        self.w_sinv = torch.empty(N // 128, K // 128, **f32) if block else None
+        ws = fp8_workspace_size(M, N, K, self.recipe)
+        self.workspace = torch.empty(max(ws, 16), **u8)
+        p = lambda t: None if t is None else t.data_ptr()
+        self.c_state = LinearStateC(p(self.scale), p(self.scale_inv), p(self.amax),
+                                    p(self.history), p(self.pos), p(self.x_q), p(self.x_qt),
+                                    p(self.w_q), p(self.w_qt), p(self.x_sinv), p(self.w_sinv),
+                                    p(self.qscale_inv))
+
+    def forward(self, X: torch.Tensor, W: torch.Tensor, Y=None, stream=None) -> torch.Tensor:
+        if Y is None:
+            Y = torch.empty(self.M, self.N, dtype=torch.bfloat16, device=X.device)
+        fp8_linear_fwd(X, W, self.recipe, self.c_state, Y, None, stream)
+        return Y
+
+    def backward(self, dY: torch.Tensor, dX=None, dW=None, accumulate_dW: bool = False,
+                 stream=None):
+        if dX is None:
+            dX = torch.empty(self.M, self.K, dtype=torch.bfloat16, device=dY.device)
+        if dW is None:
+            dW = torch.zeros(self.N, self.K, dtype=torch.float32, device=dY.device)
+        fp8_linear_bwd(dY, self.M, self.N, self.K, self.recipe, self.c_state, dX, dW,
+                       accumulate_dW, self.workspace, stream)
+        return dX, dW
+
+    def state_dict(self) -> dict:
+        return {k: getattr(self, k).clone()
+                for k in ("scale", "scale_inv", "amax", "history", "pos", "qscale_inv")}
+
+    def load_state_dict(self, sd: dict) -> None:
+        for k, v in sd.items():
+            getattr(self, k).copy_(v)

@@ -1,0 +1,333 @@
+// api.cu -- the extern "C" boundary (include/fp8linear.h): argument checks,
+// the composition of the linear layer's forward and backward passes out of
+// the quantiser and GEMM launchers, and error reporting.
+//
+// Forward / backward composition ("Mixed Precision LLM Training: The
+// Complete Guide", "Transformer Engine internals" > "Delayed scaling" and
+// "The HYBRID recipe"; "FP8 and gradient accumulation"):
+//   fwd delayed:  q(X), q(W) with the current scales, fused amax + transpose
+//                 -> GEMM -> scale update of X and W (used from the next call)
+//   fwd dynamic:  amax(X), amax(W) -> scale update -> q(X), q(W) -> GEMM
+//   fwd block:    1x128 q(X), 128x128 q(W) -> block-scaled GEMM
+//   bwd:          q(dY) (E5M2) + transpose -> dgrad GEMM dY . W
+//                 -> wgrad GEMM dY^T . X into the FP32 buffer -> dY scale update
+// Every step is one kernel launch on the caller's stream; nothing waits on
+// the host.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "../../include/fp8linear.h"
+#include "internal.h"
+
+namespace fp8 {
+
+namespace {
+thread_local std::string g_last_error;
+}
+
+int set_error(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool valid_format(int f) { return f == FP8_E4M3 || f == FP8_E5M2; }
+bool valid_gran(int g) { return g >= FP8_GRAN_TENSOR && g <= FP8_GRAN_128x128; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+int cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return FP8_OK;
+    return set_error(FP8_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define FP8_CHECK(expr)                  \
+    do {                                 \
+        const int st_ = (expr);          \
+        if (st_ != FP8_OK) return st_;   \
+    } while (0)
+
+int check_recipe(const fp8_recipe_t* r) {
+    if (!r) return set_error(FP8_ERR_INVALID_ARG, "recipe is NULL");
+    if (r->scaling < FP8_SCALING_DELAYED || r->scaling > FP8_SCALING_BLOCK)
+        return set_error(FP8_ERR_INVALID_ARG, "unknown scaling mode %d", r->scaling);
+    if (r->margin < 0 || r->margin > 64)
+        return set_error(FP8_ERR_INVALID_ARG, "margin %d outside 0..64", r->margin);
+    if (r->scaling == FP8_SCALING_DELAYED && (r->history_len < 1 || r->history_len > 1024))
+        return set_error(FP8_ERR_INVALID_ARG, "history_len %d outside 1..1024", r->history_len);
+    if (r->amax_algo != FP8_AMAX_MAX && r->amax_algo != FP8_AMAX_MOST_RECENT)
+        return set_error(FP8_ERR_INVALID_ARG, "unknown amax_algo %d", r->amax_algo);
+    if (!valid_format(r->fwd_format) || !valid_format(r->bwd_format))
+        return set_error(FP8_ERR_INVALID_ARG, "unknown FP8 format");
+    return FP8_OK;
+}
+
+int history_len_of(const fp8_recipe_t* r) {
+    return r->scaling == FP8_SCALING_DELAYED ? r->history_len : 1;
+}
+
+int check_gemm_args(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
+                    int64_t K, int layout, int ga, const float* sa, int gb, const float* sb,
+                    const void* D, int out, int accumulate) {
+    if (!sa || !sb) return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: NULL scale pointer");
+    if ((!A && M > 0 && K > 0) || (!B && N > 0 && K > 0) || (!D && M > 0 && N > 0))
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: NULL pointer");
+    if (!valid_format(fa) || !valid_format(fb))
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: unknown FP8 format");
+    if (layout != FP8_LAYOUT_TN) return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: unknown layout %d", layout);
+    if (!valid_gran(ga) || !valid_gran(gb))
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: unknown scale granularity");
+    if (out != FP8_OUT_BF16 && out != FP8_OUT_F32)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: unknown output type %d", out);
+    if (accumulate && out != FP8_OUT_F32)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: accumulate needs FP32 output");
+    if (M < 0 || N < 0 || K < 0 || M > (1ll << 31) || N > (1ll << 31) || K > (1ll << 31))
+        return set_error(FP8_ERR_SHAPE, "fp8_gemm: dimensions out of range");
+    if (N % 16 || K % 16) return set_error(FP8_ERR_SHAPE, "fp8_gemm: N and K must be multiples of 16");
+    const bool block = ga != FP8_GRAN_TENSOR || gb != FP8_GRAN_TENSOR;
+    if (block) {
+        if (gb == FP8_GRAN_1x128)
+            return set_error(FP8_ERR_UNSUPPORTED, "fp8_gemm: 1x128 scales on B are not supported");
+        if (K % 128 || N % 128)
+            return set_error(FP8_ERR_SHAPE, "fp8_gemm: block scales need N and K multiples of 128");
+        if (ga == FP8_GRAN_128x128 && M % 128)
+            return set_error(FP8_ERR_SHAPE, "fp8_gemm: 128x128 scales on A need M multiple of 128");
+    }
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D))
+        return set_error(FP8_ERR_ALIGN, "fp8_gemm: A, B and D must be 16-byte aligned");
+    return FP8_OK;
+}
+
+int check_quantize_args(const void* x, int64_t rows, int64_t cols, int format, int gran,
+                        const float* scale, uint8_t* q, uint8_t* q_t, float* sinv, float* amax_out) {
+    if ((!x || !q) && rows > 0 && cols > 0)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: NULL pointer");
+    if (!valid_format(format)) return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: unknown format");
+    if (!valid_gran(gran)) return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: unknown granularity");
+    if (rows < 0 || cols < 0) return set_error(FP8_ERR_SHAPE, "fp8_quantize: negative dimension");
+    if (gran == FP8_GRAN_TENSOR) {
+        if (!scale) return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: scale is NULL");
+        if (q_t && (rows % 16 || cols % 16))
+            return set_error(FP8_ERR_SHAPE, "fp8_quantize: the transpose needs rows and cols multiples of 16");
+    } else {
+        if (!sinv) return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: scale_inv_blocks is NULL");
+        if (q_t || amax_out || scale)
+            return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: block modes take no scale, q_t or amax_out");
+        if (cols % 128) return set_error(FP8_ERR_SHAPE, "fp8_quantize: block modes need cols multiple of 128");
+        if (gran == FP8_GRAN_128x128 && rows % 128)
+            return set_error(FP8_ERR_SHAPE, "fp8_quantize: 128x128 blocks need rows multiple of 128");
+    }
+    if (!aligned16(x) || !aligned16(q) || (q_t && !aligned16(q_t)))
+        return set_error(FP8_ERR_ALIGN, "fp8_quantize: x, q and q_t must be 16-byte aligned");
+    return FP8_OK;
+}
+
+int check_linear_shape(int64_t M, int64_t N, int64_t K, const fp8_recipe_t* r) {
+    if (M < 0 || N < 0 || K < 0 || M > (1ll << 31) || N > (1ll << 31) || K > (1ll << 31))
+        return set_error(FP8_ERR_SHAPE, "linear: dimensions out of range");
+    const int64_t mult = r->scaling == FP8_SCALING_BLOCK ? 128 : 16;
+    if (N % mult || K % mult || (r->scaling != FP8_SCALING_BLOCK && M % mult))
+        return set_error(FP8_ERR_SHAPE, "linear: M, N, K must be multiples of %lld", (long long)mult);
+    return FP8_OK;
+}
+
+int check_state_scales(const fp8_linear_state_t* s) {
+    if (!s) return set_error(FP8_ERR_INVALID_ARG, "linear: state is NULL");
+    if (!s->scale || !s->scale_inv || !s->amax || !s->history || !s->pos || !s->qscale_inv)
+        return set_error(FP8_ERR_INVALID_ARG, "linear: state scale arrays must be set");
+    return FP8_OK;
+}
+
+size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+}  // namespace fp8
+
+using namespace fp8;
+
+extern "C" {
+
+const char* fp8_last_error(void) { return g_last_error.c_str(); }
+
+int fp8_amax(const void* x, int64_t n, float* amax, void* stream) {
+    if (!amax || (!x && n > 0)) return set_error(FP8_ERR_INVALID_ARG, "fp8_amax: NULL pointer");
+    if (n < 0) return set_error(FP8_ERR_SHAPE, "fp8_amax: negative size");
+    if (!aligned16(x)) return set_error(FP8_ERR_ALIGN, "fp8_amax: x must be 16-byte aligned");
+    return cuda_status(launch_amax(x, n, amax, as_stream(stream)), "fp8_amax");
+}
+
+int fp8_update_scale(const float* amax, float* history, int32_t* pos, int history_len, int algo,
+                     int format, int margin, int pow2, float* scale, float* scale_inv,
+                     void* stream) {
+    if (!amax || !history || !pos || !scale || !scale_inv)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_update_scale: NULL pointer");
+    if (history_len < 1 || history_len > 1024)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_update_scale: history_len %d outside 1..1024", history_len);
+    if (algo != FP8_AMAX_MAX && algo != FP8_AMAX_MOST_RECENT)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_update_scale: unknown algo %d", algo);
+    if (!valid_format(format)) return set_error(FP8_ERR_INVALID_ARG, "fp8_update_scale: unknown format");
+    if (margin < 0 || margin > 64)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_update_scale: margin %d outside 0..64", margin);
+    return cuda_status(launch_update_scale(amax, history, pos, history_len, algo, format, margin,
+                                           pow2 != 0, scale, scale_inv, 1, as_stream(stream)),
+                       "fp8_update_scale");
+}
+
+int fp8_quantize(const void* x, int64_t rows, int64_t cols, int format, int granularity,
+                 const float* scale, int pow2, uint8_t* q, uint8_t* q_t, float* scale_inv_blocks,
+                 float* amax_out, void* stream) {
+    FP8_CHECK(check_quantize_args(x, rows, cols, format, granularity, scale, q, q_t,
+                                  scale_inv_blocks, amax_out));
+    if (granularity == FP8_GRAN_TENSOR)
+        return cuda_status(launch_quantize_tensor(x, rows, cols, format, scale, q, q_t, amax_out,
+                                                  as_stream(stream)),
+                           "fp8_quantize");
+    return cuda_status(launch_quantize_block(x, rows, cols, format, granularity, pow2 != 0, q,
+                                             scale_inv_blocks, as_stream(stream)),
+                       "fp8_quantize");
+}
+
+int fp8_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N, int64_t K,
+             int layout, int ga, const float* scale_inv_a, int gb, const float* scale_inv_b,
+             void* D, int out, int accumulate, void* stream) {
+    FP8_CHECK(check_gemm_args(A, fa, B, fb, M, N, K, layout, ga, scale_inv_a, gb, scale_inv_b, D,
+                              out, accumulate));
+    return launch_gemm(A, fa, B, fb, M, N, K, ga, scale_inv_a, gb, scale_inv_b, D, out,
+                       accumulate != 0, as_stream(stream));
+}
+
+size_t fp8_workspace_size(int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe) {
+    (void)K;
+    if (check_recipe(recipe) != FP8_OK || M < 0 || N < 0) return 0;
+    if (recipe->scaling == FP8_SCALING_BLOCK) return 0;
+    // backward: dY quantised [M x N] and its transpose [N x M]
+    return 2 * align256(static_cast<size_t>(M) * static_cast<size_t>(N));
+}
+
+int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K,
+                   const fp8_recipe_t* recipe, const fp8_linear_state_t* s, void* Y,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    FP8_CHECK(check_recipe(recipe));
+    FP8_CHECK(check_linear_shape(M, N, K, recipe));
+    if (!X || !W || !Y || !s) return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_fwd: NULL pointer");
+    if (!s->x_q || !s->w_q) return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_fwd: state->x_q / w_q must be set");
+    if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(s->x_q) || !aligned16(s->w_q) ||
+        (s->x_qt && !aligned16(s->x_qt)) || (s->w_qt && !aligned16(s->w_qt)))
+        return set_error(FP8_ERR_ALIGN, "fp8_linear_fwd: tensors must be 16-byte aligned");
+    cudaStream_t st = as_stream(stream);
+    const int f = recipe->fwd_format;
+
+    if (recipe->scaling == FP8_SCALING_BLOCK) {
+        if (!s->x_sinv || !s->w_sinv)
+            return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_fwd: block mode needs x_sinv and w_sinv");
+        FP8_CHECK(cuda_status(launch_quantize_block(X, M, K, f, FP8_GRAN_1x128, recipe->pow2 != 0,
+                                                    s->x_q, s->x_sinv, st), "quantize X"));
+        FP8_CHECK(cuda_status(launch_quantize_block(W, N, K, f, FP8_GRAN_128x128, recipe->pow2 != 0,
+                                                    s->w_q, s->w_sinv, st), "quantize W"));
+        return launch_gemm(s->x_q, f, s->w_q, f, M, N, K, FP8_GRAN_1x128, s->x_sinv,
+                           FP8_GRAN_128x128, s->w_sinv, Y, FP8_OUT_BF16, 0, st);
+    }
+
+    FP8_CHECK(check_state_scales(s));
+    const int H = history_len_of(recipe);
+    if (recipe->scaling == FP8_SCALING_DYNAMIC) {
+        FP8_CHECK(cuda_status(launch_amax(X, M * K, s->amax + 0, st), "amax X"));
+        FP8_CHECK(cuda_status(launch_amax(W, N * K, s->amax + 1, st), "amax W"));
+        FP8_CHECK(cuda_status(launch_update_scale(s->amax, s->history, s->pos, H, FP8_AMAX_MOST_RECENT,
+                                                  f, recipe->margin, recipe->pow2 != 0, s->scale,
+                                                  s->scale_inv, 2, st, s->qscale_inv, 1),
+                              "update scales"));
+        FP8_CHECK(cuda_status(launch_quantize_tensor(X, M, K, f, s->scale + 0, s->x_q, s->x_qt,
+                                                     nullptr, st), "quantize X"));
+        FP8_CHECK(cuda_status(launch_quantize_tensor(W, N, K, f, s->scale + 1, s->w_q, s->w_qt,
+                                                     nullptr, st), "quantize W"));
+        return launch_gemm(s->x_q, f, s->w_q, f, M, N, K, FP8_GRAN_TENSOR, s->scale_inv + 0,
+                           FP8_GRAN_TENSOR, s->scale_inv + 1, Y, FP8_OUT_BF16, 0, st);
+    }
+
+    // delayed: cast with the scales of earlier steps, fold this step's amax in afterwards
+    FP8_CHECK(cuda_status(launch_quantize_tensor(X, M, K, f, s->scale + 0, s->x_q, s->x_qt,
+                                                 s->amax + 0, st), "quantize X"));
+    FP8_CHECK(cuda_status(launch_quantize_tensor(W, N, K, f, s->scale + 1, s->w_q, s->w_qt,
+                                                 s->amax + 1, st), "quantize W"));
+    FP8_CHECK(launch_gemm(s->x_q, f, s->w_q, f, M, N, K, FP8_GRAN_TENSOR, s->scale_inv + 0,
+                          FP8_GRAN_TENSOR, s->scale_inv + 1, Y, FP8_OUT_BF16, 0, st));
+    return cuda_status(launch_update_scale(s->amax, s->history, s->pos, H, recipe->amax_algo, f,
+                                           recipe->margin, recipe->pow2 != 0, s->scale,
+                                           s->scale_inv, 2, st, s->qscale_inv, 0),
+                       "update scales");
+}
+
+int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe,
+                   const fp8_linear_state_t* s, void* dX, float* dW, int accumulate_dW,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+    FP8_CHECK(check_recipe(recipe));
+    if (recipe->scaling == FP8_SCALING_BLOCK)
+        return set_error(FP8_ERR_UNSUPPORTED, "fp8_linear_bwd: block-wise backward is not built");
+    FP8_CHECK(check_linear_shape(M, N, K, recipe));
+    if (!dY || !dX || !dW || !s || !workspace)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: NULL pointer");
+    FP8_CHECK(check_state_scales(s));
+    if (!s->x_qt || !s->w_qt)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: the forward pass must keep x_qt and w_qt");
+    const size_t need = fp8_workspace_size(M, N, K, recipe);
+    if (workspace_bytes < need)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: workspace of %zu bytes, %zu needed",
+                         workspace_bytes, need);
+    if (!aligned16(dY) || !aligned16(dX) || !aligned16(dW) || !aligned16(workspace) ||
+        !aligned16(s->x_qt) || !aligned16(s->w_qt))
+        return set_error(FP8_ERR_ALIGN, "fp8_linear_bwd: tensors must be 16-byte aligned");
+    cudaStream_t st = as_stream(stream);
+    const int fb = recipe->bwd_format, ff = recipe->fwd_format;
+    const int H = history_len_of(recipe);
+    uint8_t* dy_q = static_cast<uint8_t*>(workspace);
+    uint8_t* dy_qt = dy_q + align256(static_cast<size_t>(M) * static_cast<size_t>(N));
+    float* h2 = s->history + 2 * static_cast<int64_t>(H);
+
+    if (recipe->scaling == FP8_SCALING_DYNAMIC) {
+        FP8_CHECK(cuda_status(launch_amax(dY, M * N, s->amax + 2, st), "amax dY"));
+        FP8_CHECK(cuda_status(launch_update_scale(s->amax + 2, h2, s->pos + 2, H, FP8_AMAX_MOST_RECENT,
+                                                  fb, recipe->margin, recipe->pow2 != 0, s->scale + 2,
+                                                  s->scale_inv + 2, 1, st), "update dY scale"));
+        FP8_CHECK(cuda_status(launch_quantize_tensor(dY, M, N, fb, s->scale + 2, dy_q, dy_qt, nullptr, st),
+                              "quantize dY"));
+    } else {
+        FP8_CHECK(cuda_status(launch_quantize_tensor(dY, M, N, fb, s->scale + 2, dy_q, dy_qt,
+                                                     s->amax + 2, st), "quantize dY"));
+    }
+    // dgrad: dX [M x K] = dY_q [M x N] . (W_q^T [K x N])^T
+    FP8_CHECK(launch_gemm(dy_q, fb, s->w_qt, ff, M, K, N, FP8_GRAN_TENSOR, s->scale_inv + 2,
+                          FP8_GRAN_TENSOR, s->qscale_inv + 1, dX, FP8_OUT_BF16, 0, st));
+    // wgrad: dW [N x K] (+)= dY_q^T [N x M] . (X_q^T [K x M])^T
+    FP8_CHECK(launch_gemm(dy_qt, fb, s->x_qt, ff, N, K, M, FP8_GRAN_TENSOR, s->scale_inv + 2,
+                          FP8_GRAN_TENSOR, s->qscale_inv + 0, dW, FP8_OUT_F32, accumulate_dW != 0, st));
+    if (recipe->scaling == FP8_SCALING_DELAYED)
+        return cuda_status(launch_update_scale(s->amax + 2, h2, s->pos + 2, H, recipe->amax_algo, fb,
+                                               recipe->margin, recipe->pow2 != 0, s->scale + 2,
+                                               s->scale_inv + 2, 1, st), "update dY scale");
+    return FP8_OK;
+}
+
+int fp8_device_status(int* status, int clear) {
+    if (!status) return set_error(FP8_ERR_INVALID_ARG, "fp8_device_status: NULL pointer");
+    unsigned v = 0;
+    FP8_CHECK(read_device_status(&v, clear != 0));
+    *status = static_cast<int>(v);
+    return FP8_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,595 @@
+// gemm.cu -- the compute-bound half of the scaled FP8 linear: FP8 x FP8 GEMMs
+// on the sm_103a tensor cores (tcgen05.mma kind::f8f6f4), fed by TMA through
+// a shared-memory ring, accumulating in TMEM (FP32), with the dequantisation
+// fused into the epilogue.
+//
+// Method ("Mixed Precision LLM Training: The Complete Guide"):
+//   "Transformer Engine internals" > "Per-tensor scaling": the matmul result
+//     is multiplied by the inverse scales of both operands;
+//   "Skipping the BAcc accumulator promotion", "DeepSeek FP8 training
+//     recipe" > "Mixed-precision accumulation": FP8 multiplicands, FP32
+//     accumulation, BF16 (or FP32) result;
+//   "DeepSeek FP8 training recipe" > "Block-wise scaling at 128 granularity":
+//     block scales applied inside the matmul -- every 128-deep partial sum
+//     is scaled by its blocks' factors and added to an FP32 accumulator.
+//
+// Kernel structure (one persistent CTA per SM, warp-specialised):
+//   warp 0      TMA producer: A and B tiles (128 B of K per row, 128-byte
+//               swizzle) into a STAGES-deep ring guarded by full/empty
+//               mbarriers;
+//   warp 1      MMA issuer: one thread issues 4 tcgen05.mma (K = 32 each)
+//               per 128-deep stage into a TMEM accumulator and releases the
+//               stage with tcgen05.commit;
+//   warp 2      TMEM allocation / release;
+//   warps 4..   epilogue: tcgen05.ld of the accumulator (thread = row),
+//               scale, convert, store to global memory.
+// Per-tensor kernel: BM x BN = 128 x 256, two TMEM accumulators (512
+// columns) so the epilogue of one tile overlaps the mainloop of the next.
+// Block-scaled kernel: BM x BN = 128 x 128, four TMEM partial-sum buffers
+// rotated per 128-deep K block; 8 epilogue warps promote them into FP32
+// registers.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fp8linear.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8 {
+
+__device__ unsigned int g_device_status = 0;
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 128;      // bytes = FP8 elements of K per stage
+constexpr int UMMA_K = 32;   // K of one kind::f8f6f4 instruction
+
+struct GemmParams {
+    int64_t M, N, K;
+    int num_m, num_n, num_kb;
+    int fa, fb;
+    int ga, gb;
+    const float* sa;
+    const float* sb;
+    void* D;
+    int out;          // FP8_OUT_BF16 / FP8_OUT_F32
+    int accumulate;
+};
+
+// Grouped rasterisation: walk GROUP consecutive M-blocks down each N-column
+// so that the CTAs resident at one time share A and B panels in L2.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk,
+                                            int& n_blk) {
+    constexpr int GROUP = 8;
+    const int per_group = GROUP * num_n;
+    const int g = tile / per_group;
+    const int first_m = g * GROUP;
+    const int gsize = min(num_m - first_m, GROUP);
+    const int in_g = tile - g * per_group;
+    m_blk = first_m + in_g % gsize;
+    n_blk = in_g / gsize;
+}
+
+template <int BN, int STAGES>
+struct Layout {
+    static constexpr int A_BYTES = BM * BK;
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES = RING_BYTES + BAR_BYTES + 1024;  // + alignment slack
+};
+
+// Producer role: stream the A / B tiles of every K block of every tile of
+// this CTA through the ring.  On exit, waits for its own copies in flight.
+template <int BN, int STAGES>
+__device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t* ring,
+                         uint64_t* full, uint64_t* empty, const GemmParams& p,
+                         volatile uint32_t* abort_flag) {
+    using L = Layout<BN, STAGES>;
+    const int num_tiles = p.num_m * p.num_n;
+    uint32_t stage = 0, phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        int m_blk, n_blk;
+        tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+            uint8_t* sa = ring + stage * L::STAGE_BYTES;
+            ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+            ptx::tma_load_2d(sa, tmA, &full[stage], kb * BK, m_blk * BM);
+            ptx::tma_load_2d(sa + L::A_BYTES, tmB, &full[stage], kb * BK, n_blk * BN);
+            ++issued;
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+    }
+    // drain: the last copy issued into each slot must have landed
+    uint32_t never = 0;
+    for (int s = 0; s < STAGES; ++s) {
+        if (issued <= s && issued < STAGES) break;
+        const uint32_t par = (static_cast<uint32_t>(s) < stage) ? phase : (phase ^ 1u);
+        ptx::mbar_wait(&full[s], par, &never);
+    }
+}
+
+// --------------------------------------------------------- per-tensor kernel
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(256, 1)
+    gemm_tensor_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    using L = Layout<BN, STAGES>;
+    constexpr uint32_t TMEM_COLS = 2 * BN;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + L::RING_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* done = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(&tfull[a], 1);
+            ptx::mbar_init(&tempty[a], 4);
+        }
+        ptx::mbar_init(done, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::tma_prefetch_desc(&tmA);
+        ptx::tma_prefetch_desc(&tmB);
+    }
+    if (warp == 2) {
+        ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int num_tiles = p.num_m * p.num_n;
+
+    if (warp == 0) {
+        if (lane == 0) producer<BN, STAGES>(&tmA, &tmB, ring, full, empty, p, abort_flag);
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = ptx::idesc_f8f6f4(p.fa, p.fb, BM, BN);
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) break;
+                ptx::tc_fence_after();
+                const uint32_t d = tmem_base + acc * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    uint8_t* sa = ring + stage * L::STAGE_BYTES;
+                    const uint64_t ad = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa));
+                    const uint64_t bd = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa + L::A_BYTES));
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k)
+                        ptx::mma_f8f6f4(d, ad + (k * UMMA_K >> 4), bd + (k * UMMA_K >> 4), idesc,
+                                        (kb | k) != 0);
+                    ptx::mma_commit(&empty[stage]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                ptx::mma_commit(&tfull[acc]);
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            // every MMA issued by this thread must finish before TMEM is released
+            uint32_t never = 0;
+            ptx::mma_commit(done);
+            ptx::mbar_wait(done, 0, &never);
+        }
+    } else if (warp >= 4) {
+        const int qd = warp & 3;  // TMEM lane quadrant this warp may access
+        const int row = qd * 32 + lane;
+        const float alpha = __fmul_rn(p.sa[0], p.sb[0]);
+        uint32_t acc = 0, acc_phase = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            int m_blk, n_blk;
+            tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+            bool ok = (lane == 0) ? ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag) : false;
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            __syncwarp();
+            ptx::tc_fence_after();
+            const int64_t m = static_cast<int64_t>(m_blk) * BM + row;
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + acc * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(tbase + c * 32, r);
+                ptx::tmem_wait_ld();
+                const int64_t n0 = static_cast<int64_t>(n_blk) * BN + c * 32;
+                if (m < p.M) {
+                    if (p.out == FP8_OUT_BF16) {
+                        __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.D) + m * p.N;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 8) {
+                            if (n0 + j < p.N) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const __nv_bfloat162 h = __floats2bfloat162_rn(
+                                        __fmul_rn(__uint_as_float(r[j + 2 * e]), alpha),
+                                        __fmul_rn(__uint_as_float(r[j + 2 * e + 1]), alpha));
+                                    w[e] = *reinterpret_cast<const uint32_t*>(&h);
+                                }
+                                *reinterpret_cast<uint4*>(drow + n0 + j) =
+                                    make_uint4(w[0], w[1], w[2], w[3]);
+                            }
+                        }
+                    } else {
+                        float* drow = static_cast<float*>(p.D) + m * p.N;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            if (n0 + j < p.N) {
+                                float4 v = make_float4(__fmul_rn(__uint_as_float(r[j]), alpha),
+                                                       __fmul_rn(__uint_as_float(r[j + 1]), alpha),
+                                                       __fmul_rn(__uint_as_float(r[j + 2]), alpha),
+                                                       __fmul_rn(__uint_as_float(r[j + 3]), alpha));
+                                float4* dst = reinterpret_cast<float4*>(drow + n0 + j);
+                                if (p.accumulate) {
+                                    const float4 o = *dst;
+                                    v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+                                }
+                                *dst = v;
+                            }
+                        }
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_device_status, 1u);
+}
+
+// --------------------------------------------------------- block-scaled kernel
+
+// Dequantisation factor of row r (of A or B) for K block kb.
+__device__ __forceinline__ float block_factor(const float* s, int gran, int64_t r, int kb,
+                                              int KB) {
+    if (gran == FP8_GRAN_TENSOR) return s[0];
+    if (gran == FP8_GRAN_1x128) return s[r * KB + kb];
+    return s[(r >> 7) * KB + kb];
+}
+
+template <int STAGES>
+__global__ void __launch_bounds__(384, 1)
+    gemm_block_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    constexpr int BN = 128;
+    constexpr int NBUF = 4;
+    using L = Layout<BN, STAGES>;
+    constexpr uint32_t TMEM_COLS = NBUF * BN;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + L::RING_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + NBUF;
+    uint64_t* done = tempty + NBUF;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < NBUF; ++a) {
+            ptx::mbar_init(&tfull[a], 1);
+            ptx::mbar_init(&tempty[a], 8);
+        }
+        ptx::mbar_init(done, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::tma_prefetch_desc(&tmA);
+        ptx::tma_prefetch_desc(&tmB);
+    }
+    if (warp == 2) {
+        ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int num_tiles = p.num_m * p.num_n;
+
+    if (warp == 0) {
+        if (lane == 0) producer<BN, STAGES>(&tmA, &tmB, ring, full, empty, p, abort_flag);
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = ptx::idesc_f8f6f4(p.fa, p.fb, BM, BN);
+            uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!ptx::mbar_wait(&tempty[buf], buf_phase ^ 1u, abort_flag)) { ok = false; break; }
+                    if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    uint8_t* sa = ring + stage * L::STAGE_BYTES;
+                    const uint64_t ad = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa));
+                    const uint64_t bd = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa + L::A_BYTES));
+                    const uint32_t d = tmem_base + buf * BN;
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k)
+                        ptx::mma_f8f6f4(d, ad + (k * UMMA_K >> 4), bd + (k * UMMA_K >> 4), idesc,
+                                        k != 0);
+                    ptx::mma_commit(&empty[stage]);
+                    ptx::mma_commit(&tfull[buf]);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    if (++buf == NBUF) { buf = 0; buf_phase ^= 1u; }
+                }
+            }
+            uint32_t never = 0;
+            ptx::mma_commit(done);
+            ptx::mbar_wait(done, 0, &never);
+        }
+    } else if (warp >= 4) {
+        const int qd = warp & 3;
+        const int half = (warp - 4) >> 2;  // which 64 of the 128 columns
+        const int row = qd * 32 + lane;
+        const int KB = p.num_kb;
+        uint32_t buf = 0, buf_phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            int m_blk, n_blk;
+            tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+            const int64_t m = static_cast<int64_t>(m_blk) * BM + row;
+            const int64_t m_safe = m < p.M ? m : p.M - 1;
+            const int64_t n_row = static_cast<int64_t>(n_blk) * BN;  // a row of B in this tile
+            float acc[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+            float f_next = __fmul_rn(block_factor(p.sa, p.ga, m_safe, 0, KB),
+                                     block_factor(p.sb, p.gb, n_row, 0, KB));
+            for (int kb = 0; kb < KB; ++kb) {
+                const float f = f_next;
+                if (kb + 1 < KB)
+                    f_next = __fmul_rn(block_factor(p.sa, p.ga, m_safe, kb + 1, KB),
+                                       block_factor(p.sb, p.gb, n_row, kb + 1, KB));
+                ok = (lane == 0) ? ptx::mbar_wait(&tfull[buf], buf_phase, abort_flag) : false;
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                if (!ok) break;
+                __syncwarp();
+                ptx::tc_fence_after();
+                const uint32_t tb = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + buf * BN +
+                                    half * 64;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(tb + c * 32, r);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), f, acc[c * 32 + j]);
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
+                if (++buf == NBUF) { buf = 0; buf_phase ^= 1u; }
+            }
+            if (!ok) break;
+            if (m < p.M) {
+                const int64_t n0 = n_row + half * 64;
+                if (p.out == FP8_OUT_BF16) {
+                    __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.D) + m * p.N;
+#pragma unroll
+                    for (int j = 0; j < 64; j += 8) {
+                        if (n0 + j < p.N) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const __nv_bfloat162 h =
+                                    __floats2bfloat162_rn(acc[j + 2 * e], acc[j + 2 * e + 1]);
+                                w[e] = *reinterpret_cast<const uint32_t*>(&h);
+                            }
+                            *reinterpret_cast<uint4*>(drow + n0 + j) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                } else {
+                    float* drow = static_cast<float*>(p.D) + m * p.N;
+#pragma unroll
+                    for (int j = 0; j < 64; j += 4) {
+                        if (n0 + j < p.N) {
+                            float4 v = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                            float4* dst = reinterpret_cast<float4*>(drow + n0 + j);
+                            if (p.accumulate) {
+                                const float4 o = *dst;
+                                v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+                            }
+                            *dst = v;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_device_status, 1u);
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Tensor map of a K-contiguous FP8 matrix [rows x K]: boxes of 128 bytes of K
+// by box_rows rows, 128-byte swizzle, zero fill outside the matrix.
+int make_kmajor_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K,
+                    uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return set_error(FP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(FP8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%lld x %lld]",
+                         static_cast<int>(r), static_cast<long long>(rows),
+                         static_cast<long long>(K));
+    return FP8_OK;
+}
+
+constexpr int kTensorBN = 256, kTensorStages = 4;
+constexpr int kBlockStages = 6;
+
+template <typename Kernel>
+int ensure_smem(Kernel k, int bytes, int kernel_id) {
+    static std::mutex mu;
+    static bool done[64][4] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev][kernel_id]) return FP8_OK;
+    const cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess)
+        return set_error(FP8_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    done[dev][kernel_id] = true;
+    return FP8_OK;
+}
+
+}  // namespace
+
+int num_sms() {
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
+                int64_t K, int ga, const float* sa, int gb, const float* sb, void* D, int out,
+                int accumulate, cudaStream_t stream) {
+    if (M == 0 || N == 0) return FP8_OK;
+    if (K == 0) {
+        if (out == FP8_OUT_F32 && accumulate) return FP8_OK;
+        const size_t bytes = static_cast<size_t>(M) * N * (out == FP8_OUT_F32 ? 4 : 2);
+        const cudaError_t e = cudaMemsetAsync(D, 0, bytes, stream);
+        return e == cudaSuccess ? FP8_OK
+                                : set_error(FP8_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+    }
+    const bool block = ga != FP8_GRAN_TENSOR || gb != FP8_GRAN_TENSOR;
+    const int BN = block ? 128 : kTensorBN;
+    GemmParams p;
+    p.M = M; p.N = N; p.K = K;
+    p.num_m = static_cast<int>((M + BM - 1) / BM);
+    p.num_n = static_cast<int>((N + BN - 1) / BN);
+    p.num_kb = static_cast<int>((K + BK - 1) / BK);
+    p.fa = fa; p.fb = fb; p.ga = ga; p.gb = gb; p.sa = sa; p.sb = sb;
+    p.D = D; p.out = out; p.accumulate = accumulate;
+
+    CUtensorMap tmA, tmB;
+    int st = make_kmajor_map(&tmA, A, M, K, BM);
+    if (st != FP8_OK) return st;
+    st = make_kmajor_map(&tmB, B, N, K, BN);
+    if (st != FP8_OK) return st;
+
+    const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
+    const int grid = static_cast<int>(tiles < num_sms() ? tiles : num_sms());
+    if (!block) {
+        using L = Layout<kTensorBN, kTensorStages>;
+        auto k = gemm_tensor_kernel<kTensorBN, kTensorStages>;
+        if ((st = ensure_smem(k, L::SMEM_BYTES, 0)) != FP8_OK) return st;
+        k<<<grid, 256, L::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    } else {
+        using L = Layout<128, kBlockStages>;
+        auto k = gemm_block_kernel<kBlockStages>;
+        if ((st = ensure_smem(k, L::SMEM_BYTES, 1)) != FP8_OK) return st;
+        k<<<grid, 384, L::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(FP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+    return FP8_OK;
+}
+
+int read_device_status(unsigned* status, bool clear) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return set_error(FP8_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
+    e = cudaMemcpyFromSymbol(status, g_device_status, sizeof(unsigned));
+    if (e != cudaSuccess)
+        return set_error(FP8_ERR_CUDA, "reading device status: %s", cudaGetErrorString(e));
+    if (clear) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(unsigned));
+        if (e != cudaSuccess)
+            return set_error(FP8_ERR_CUDA, "clearing device status: %s", cudaGetErrorString(e));
+    }
+    return FP8_OK;
+}
+
+}  // namespace fp8

@@ -1,0 +1,48 @@
+// internal.h -- launchers shared between the C-ABI layer (api.cu) and the
+// kernel translation units.  Arguments are validated by the caller; these
+// functions only configure and enqueue kernels on `stream`.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace fp8 {
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+// max|x| over n bf16 values into *amax (zeroed first, then atomically raised).
+cudaError_t launch_amax(const void* x, int64_t n, float* amax, cudaStream_t stream);
+
+// Scale update for `nroles` consecutive roles of a state laid out as
+// amax[r], history[r * H + i], pos[r], scale[r], scale_inv[r].  `saved`
+// (nullable) receives scale_inv[r] from before (save_after = 0) or after
+// (save_after = 1) the update.
+cudaError_t launch_update_scale(const float* amax, float* history, int32_t* pos, int H,
+                                int algo, int fmt, int margin, int pow2, float* scale,
+                                float* scale_inv, int nroles, cudaStream_t stream,
+                                float* saved = nullptr, int save_after = 0);
+
+// Per-tensor cast of x [rows x cols]; q_t and amax may be null.  With q_t,
+// rows and cols are multiples of 16.
+cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, int fmt,
+                                   const float* scale, uint8_t* q, uint8_t* q_t, float* amax,
+                                   cudaStream_t stream);
+
+// Block cast: gran 1 (1x128) or 2 (128x128); writes q and 1/scale per block.
+cudaError_t launch_quantize_block(const void* x, int64_t rows, int64_t cols, int fmt, int gran,
+                                  int pow2, uint8_t* q, float* scale_inv, cudaStream_t stream);
+
+// Scaled FP8 GEMM, TN layout.  Returns 0 or a negative fp8 status code
+// (tensor-map encoding can fail); launch errors come back as FP8_ERR_CUDA.
+int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
+                int64_t K, int ga, const float* sa, int gb, const float* sb, void* D, int out,
+                int accumulate, cudaStream_t stream);
+
+// Device status word (bit 0: a bounded wait timed out).
+int read_device_status(unsigned* status, bool clear);
+
+// Record a message for fp8_last_error() and return `code`.
+int set_error(int code, const char* fmt, ...);
+
+}  // namespace fp8

@@ -1,0 +1,445 @@
+// quantize.cu -- the memory-bound half of the scaled FP8 linear: amax
+// reduction, scale update and the bf16 -> FP8 casts (per-tensor, with an
+// optional fused transpose and fused amax; 1x128 and 128x128 block-wise).
+//
+// Method ("Mixed Precision LLM Training: The Complete Guide"):
+//   "Transformer Engine internals" > "Per-tensor scaling": q = fp8(x * s)
+//     with s chosen so that max|x| lands at the top of the FP8 range;
+//   "Delayed scaling" / "History-based scaling": s comes from the max over
+//     an amax history and is applied one step late;
+//   "DeepSeek FP8 training recipe" > "Block-wise scaling at 128
+//     granularity": one scale per 1x128 row segment or 128x128 tile.
+//
+// Every kernel streams bf16 in 16-byte vectors and writes FP8 in 8- or
+// 16-byte vectors.  amax is an integer max over |bf16| bit patterns
+// (sign bit cleared), reduced with warp max-reductions and one atomicMax
+// per CTA on the fp32 bit pattern, which orders like the value for
+// non-negative floats: the result is exact and independent of order.
+#include <cfloat>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace fp8 {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <int FMT>
+struct Fp8Traits;
+template <>
+struct Fp8Traits<0> {
+    static constexpr __nv_fp8_interpretation_t kind = __NV_E4M3;
+    static constexpr float max_finite = 448.0f;
+};
+template <>
+struct Fp8Traits<1> {
+    static constexpr __nv_fp8_interpretation_t kind = __NV_E5M2;
+    static constexpr float max_finite = 57344.0f;
+};
+
+// Two packed bf16 (element 0 in the low half) times s, cast to two FP8
+// codes (element 0 in the low byte), saturating, round to nearest even.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt2(uint32_t w, float s) {
+    const float lo = __fmul_rn(__uint_as_float(w << 16), s);
+    const float hi = __fmul_rn(__uint_as_float(w & 0xFFFF0000u), s);
+    return static_cast<uint32_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, Fp8Traits<FMT>::kind));
+}
+
+// Four bf16 (two words) -> four FP8 codes in one word.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt4(uint32_t w0, uint32_t w1, float s) {
+    return cvt2<FMT>(w0, s) | (cvt2<FMT>(w1, s) << 16);
+}
+
+// Running per-halfword max of |bf16| bit patterns.
+__device__ __forceinline__ uint32_t absmax2(uint32_t m, uint32_t w) {
+    return __vmaxu2(m, w & 0x7FFF7FFFu);
+}
+
+__device__ __forceinline__ uint32_t absmax_vec(uint32_t m, const uint4& v) {
+    m = absmax2(m, v.x);
+    m = absmax2(m, v.y);
+    m = absmax2(m, v.z);
+    return absmax2(m, v.w);
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Reduce a per-thread |bf16| max (packed or not) over the CTA and raise
+// *amax_bits to it (fp32 bit pattern = bf16 bits << 16).
+__device__ __forceinline__ void cta_amax_commit(uint32_t m2, unsigned* amax_bits) {
+    __shared__ uint32_t warp_max[kThreads / 32];
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) warp_max[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t v = lane < (int)(blockDim.x >> 5) ? warp_max[lane] : 0u;
+        v = __reduce_max_sync(0xFFFFFFFFu, v);
+        if (lane == 0 && v != 0) atomicMax(amax_bits, v << 16);
+    }
+}
+
+// Scale of one block from its amax: fp8_max / amax, clamped to the normal
+// fp32 range, optionally rounded down to a power of two; 1 for an all-zero
+// or non-finite block.
+template <int FMT>
+__device__ __forceinline__ float block_scale(float amax, int pow2) {
+    if (!(amax > 0.0f) || !isfinite(amax)) return 1.0f;
+    float s = __fdiv_rn(Fp8Traits<FMT>::max_finite, amax);
+    if (!(s <= FLT_MAX)) s = FLT_MAX;
+    if (s < FLT_MIN) s = FLT_MIN;
+    if (pow2) s = __uint_as_float(__float_as_uint(s) & 0xFF800000u);
+    return s;
+}
+
+// ------------------------------------------------------------------ amax
+
+__global__ void __launch_bounds__(kThreads) amax_kernel(const uint4* __restrict__ x,
+                                                        int64_t nvec,
+                                                        const uint16_t* __restrict__ tail,
+                                                        int tail_n, unsigned* amax_bits) {
+    uint32_t m = 0;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < nvec; i += 4 * stride) {
+        const uint4 a = ldg_stream(x + i), b = ldg_stream(x + i + stride);
+        const uint4 c = ldg_stream(x + i + 2 * stride), d = ldg_stream(x + i + 3 * stride);
+        m = absmax_vec(m, a);
+        m = absmax_vec(m, b);
+        m = absmax_vec(m, c);
+        m = absmax_vec(m, d);
+    }
+    for (; i < nvec; i += stride) m = absmax_vec(m, ldg_stream(x + i));
+    if (blockIdx.x == 0 && threadIdx.x < tail_n) m = max(m, (uint32_t)(tail[threadIdx.x] & 0x7FFFu));
+    cta_amax_commit(m, amax_bits);
+}
+
+// ---------------------------------------------------------- scale update
+
+// One warp per role.  history[pos] = amax; pos = (pos + 1) % H;
+// a = max(history) or amax; if 0 < a < inf: s = fp8_max / a * 2^-margin,
+// clamped to [FLT_MIN, FLT_MAX], optionally rounded down to 2^k; scale = s,
+// scale_inv = 1 / s.  Otherwise scale and scale_inv are left unchanged.
+// `saved` (nullable) receives scale_inv[r] as it was before the update
+// (save_after = 0) or after it (save_after = 1): the dequantisation factor of
+// the operand that the same pass cast with the old or the new scale.
+__global__ void update_scale_kernel(const float* __restrict__ amax, float* __restrict__ history,
+                                    int32_t* __restrict__ pos, int H, int algo, float fmax,
+                                    int margin, int pow2, float* __restrict__ scale,
+                                    float* __restrict__ scale_inv, float* __restrict__ saved,
+                                    int save_after) {
+    const int r = blockIdx.x, lane = threadIdx.x;
+    float* hist = history + static_cast<int64_t>(r) * H;
+    const float a = amax[r];
+    const int p = pos[r];
+    // NaN-dominant max over the history with the new value in slot p
+    float eff = -INFINITY;
+    if (algo == 0) {
+        for (int i = lane; i < H; i += 32) {
+            const float h = (i == p) ? a : hist[i];
+            if (isnan(h) || h > eff) eff = h;
+        }
+        for (int off = 16; off > 0; off >>= 1) {
+            const float o = __shfl_xor_sync(0xFFFFFFFFu, eff, off);
+            if (isnan(o) || o > eff) eff = o;
+        }
+    } else {
+        eff = a;
+    }
+    __syncwarp();
+    if (lane == 0) {
+        if (saved && !save_after) saved[r] = scale_inv[r];
+        hist[p] = a;
+        pos[r] = (p + 1 == H) ? 0 : p + 1;
+        if (eff > 0.0f && isfinite(eff)) {
+            float s = __fdiv_rn(fmax, eff);
+            s = __fmul_rn(s, __uint_as_float(static_cast<uint32_t>(127 - margin) << 23));
+            if (!(s <= FLT_MAX)) s = FLT_MAX;
+            if (s < FLT_MIN) s = FLT_MIN;
+            if (pow2) s = __uint_as_float(__float_as_uint(s) & 0xFF800000u);
+            scale[r] = s;
+            scale_inv[r] = __fdiv_rn(1.0f, s);
+        }
+        if (saved && save_after) saved[r] = scale_inv[r];
+    }
+}
+
+// ------------------------------------------------------- per-tensor cast
+
+// Flat cast, 16 elements (32 B in, 16 B out) per thread per step.
+template <int FMT, bool AMAX>
+__global__ void __launch_bounds__(kThreads)
+    quantize_flat_kernel(const uint4* __restrict__ x, int64_t n16, const uint16_t* __restrict__ xt,
+                         int tail_n, const float* __restrict__ scale_p, uint4* __restrict__ q,
+                         uint8_t* __restrict__ qtail, unsigned* amax_bits) {
+    const float s = *scale_p;
+    uint32_t m = 0;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; i + stride < n16; i += 2 * stride) {
+        const uint4 a0 = ldg_stream(x + 2 * i), b0 = ldg_stream(x + 2 * i + 1);
+        const uint4 a1 = ldg_stream(x + 2 * (i + stride)), b1 = ldg_stream(x + 2 * (i + stride) + 1);
+        if (AMAX) m = absmax_vec(absmax_vec(absmax_vec(absmax_vec(m, a0), b0), a1), b1);
+        q[i] = make_uint4(cvt4<FMT>(a0.x, a0.y, s), cvt4<FMT>(a0.z, a0.w, s),
+                          cvt4<FMT>(b0.x, b0.y, s), cvt4<FMT>(b0.z, b0.w, s));
+        q[i + stride] = make_uint4(cvt4<FMT>(a1.x, a1.y, s), cvt4<FMT>(a1.z, a1.w, s),
+                                   cvt4<FMT>(b1.x, b1.y, s), cvt4<FMT>(b1.z, b1.w, s));
+    }
+    for (; i < n16; i += stride) {
+        const uint4 a = ldg_stream(x + 2 * i), b = ldg_stream(x + 2 * i + 1);
+        if (AMAX) m = absmax_vec(absmax_vec(m, a), b);
+        q[i] = make_uint4(cvt4<FMT>(a.x, a.y, s), cvt4<FMT>(a.z, a.w, s), cvt4<FMT>(b.x, b.y, s),
+                          cvt4<FMT>(b.z, b.w, s));
+    }
+    if (blockIdx.x == 0 && threadIdx.x < tail_n) {
+        const uint32_t w = xt[threadIdx.x];
+        if (AMAX) m = max(m, w & 0x7FFFu);
+        qtail[threadIdx.x] = static_cast<uint8_t>(cvt2<FMT>(w, s) & 0xFFu);
+    }
+    if (AMAX) cta_amax_commit(m, amax_bits);
+}
+
+// Cast with fused transpose.  One CTA per 128 x 128 tile:
+//  phase 1: each thread reads 16 consecutive bf16 of a row (2 x 16 B), writes
+//           16 FP8 codes of q (16 B) and keeps them in shared memory;
+//  phase 2: each thread gathers 4 x 4 byte blocks from shared memory,
+//           transposes them with byte permutes and writes 4 codes to each of
+//           4 rows of q_t (a warp covers 128 contiguous bytes per row).
+// Shared-memory rows of 32 words are XOR-swizzled in groups of 4 words so
+// that phase 1 stores stay 16-byte vectors and phase 2 reads spread over
+// 8 banks.  rows and cols are multiples of 16.
+__device__ __forceinline__ int tr_swz(int row) { return ((row >> 2) & 7) << 2; }
+
+template <int FMT, bool AMAX>
+__global__ void __launch_bounds__(kThreads)
+    quantize_transpose_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
+                              int64_t tiles_c, const float* __restrict__ scale_p,
+                              uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
+                              unsigned* amax_bits) {
+    __shared__ __align__(16) uint32_t S[128 * 32];
+    const int64_t tile = blockIdx.x;
+    const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
+    const float s = *scale_p;
+    const int t = threadIdx.x;
+    uint32_t m = 0;
+
+    const int cg = t & 7;
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int rl = it * 32 + (t >> 3);
+        const int64_t r = r0 + rl, c = c0 + cg * 16;
+        uint4 out = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows && c < cols) {
+            const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + c);
+            const uint4 a = ldg_stream(src), b = ldg_stream(src + 1);
+            if (AMAX) m = absmax_vec(absmax_vec(m, a), b);
+            out = make_uint4(cvt4<FMT>(a.x, a.y, s), cvt4<FMT>(a.z, a.w, s),
+                             cvt4<FMT>(b.x, b.y, s), cvt4<FMT>(b.z, b.w, s));
+            *reinterpret_cast<uint4*>(q + r * cols + c) = out;
+        }
+        *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = out;
+    }
+    __syncthreads();
+
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int b = it * kThreads + t;
+        const int br = b & 31, bc = b >> 5;
+        const int R = 4 * br;
+        const uint32_t w0 = S[(R + 0) * 32 + (bc ^ tr_swz(R + 0))];
+        const uint32_t w1 = S[(R + 1) * 32 + (bc ^ tr_swz(R + 1))];
+        const uint32_t w2 = S[(R + 2) * 32 + (bc ^ tr_swz(R + 2))];
+        const uint32_t w3 = S[(R + 3) * 32 + (bc ^ tr_swz(R + 3))];
+        const uint32_t lo01 = __byte_perm(w0, w1, 0x5140), hi01 = __byte_perm(w0, w1, 0x7362);
+        const uint32_t lo23 = __byte_perm(w2, w3, 0x5140), hi23 = __byte_perm(w2, w3, 0x7362);
+        const uint32_t o[4] = {__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo01, lo23, 0x7632),
+                               __byte_perm(hi01, hi23, 0x5410), __byte_perm(hi01, hi23, 0x7632)};
+        const int64_t r = r0 + R, c = c0 + 4 * bc;
+        if (r < rows) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (c + k < cols) *reinterpret_cast<uint32_t*>(qt + (c + k) * rows + r) = o[k];
+        }
+    }
+    if (AMAX) cta_amax_commit(m, amax_bits);
+}
+
+// ----------------------------------------------------------- block casts
+
+// 1x128: a half-warp per row segment (16 lanes x 8 elements); the segment's
+// amax is a max-reduction over the 16 lanes.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads)
+    quantize_1x128_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int pow2,
+                          uint8_t* __restrict__ q, float* __restrict__ scale_inv) {
+    const int64_t KB = cols / 128;
+    const int64_t nseg = rows * KB;
+    const int64_t npairs = (nseg + 1) / 2;
+    const int lane = threadIdx.x & 31, sub = lane & 15;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t p = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         p < npairs; p += warps) {
+        const int64_t seg = 2 * p + (lane >> 4);
+        const bool valid = seg < nseg;
+        const int64_t row = seg / KB, kb = seg - row * KB;
+        const int64_t off = row * cols + kb * 128 + sub * 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) v = ldg_stream(reinterpret_cast<const uint4*>(x + off));
+        uint32_t m2 = absmax_vec(0u, v);
+        uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        const float s = block_scale<FMT>(__uint_as_float(m << 16), pow2);
+        if (valid) {
+            *reinterpret_cast<uint2*>(q + off) =
+                make_uint2(cvt4<FMT>(v.x, v.y, s), cvt4<FMT>(v.z, v.w, s));
+            if (sub == 0) scale_inv[seg] = __fdiv_rn(1.0f, s);
+        }
+    }
+}
+
+// 128x128: one CTA per tile; each thread holds 64 elements in registers
+// while the CTA reduces the tile's amax.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads)
+    quantize_128x128_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int pow2,
+                            uint8_t* __restrict__ q, float* __restrict__ scale_inv) {
+    __shared__ uint32_t warp_max[kThreads / 32];
+    const int64_t KB = cols / 128;
+    const int64_t br = blockIdx.x / KB, bc = blockIdx.x % KB;
+    const int t = threadIdx.x;
+    uint4 v[8];
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t r = br * 128 + i * 16 + (t >> 4), c = bc * 128 + (t & 15) * 8;
+        v[i] = ldg_stream(reinterpret_cast<const uint4*>(x + r * cols + c));
+        m2 = absmax_vec(m2, v[i]);
+    }
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((t & 31) == 0) warp_max[t >> 5] = m;
+    __syncthreads();
+    m = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) m = max(m, warp_max[w]);
+    const float s = block_scale<FMT>(__uint_as_float(m << 16), pow2);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t r = br * 128 + i * 16 + (t >> 4), c = bc * 128 + (t & 15) * 8;
+        *reinterpret_cast<uint2*>(q + r * cols + c) =
+            make_uint2(cvt4<FMT>(v[i].x, v[i].y, s), cvt4<FMT>(v[i].z, v[i].w, s));
+    }
+    if (t == 0) scale_inv[br * KB + bc] = __fdiv_rn(1.0f, s);
+}
+
+int grid_for(int64_t work_items, int per_cta) {
+    const int64_t need = (work_items + per_cta - 1) / per_cta;
+    const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+    return static_cast<int>(need < 1 ? 1 : (need < cap ? need : cap));
+}
+
+}  // namespace
+
+cudaError_t launch_amax(const void* x, int64_t n, float* amax, cudaStream_t stream) {
+    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), stream);
+    if (e != cudaSuccess || n == 0) return e;
+    const int64_t nvec = n / 8;
+    const int tail_n = static_cast<int>(n - nvec * 8);
+    const uint16_t* tail = static_cast<const uint16_t*>(x) + nvec * 8;
+    amax_kernel<<<grid_for(nvec + 1, kThreads * 4), kThreads, 0, stream>>>(
+        static_cast<const uint4*>(x), nvec, tail, tail_n, reinterpret_cast<unsigned*>(amax));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_update_scale(const float* amax, float* history, int32_t* pos, int H, int algo,
+                                int fmt, int margin, int pow2, float* scale, float* scale_inv,
+                                int nroles, cudaStream_t stream, float* saved, int save_after) {
+    const float fmax = fmt == 0 ? 448.0f : 57344.0f;
+    update_scale_kernel<<<nroles, 32, 0, stream>>>(amax, history, pos, H, algo, fmax, margin,
+                                                   pow2, scale, scale_inv, saved, save_after);
+    return cudaGetLastError();
+}
+
+template <int FMT, bool AMAX>
+static void launch_flat(const void* x, int64_t n, const float* scale, uint8_t* q, float* amax,
+                        cudaStream_t stream) {
+    const int64_t n16 = n / 16;
+    const int tail_n = static_cast<int>(n - n16 * 16);
+    quantize_flat_kernel<FMT, AMAX><<<grid_for(n16 + 1, kThreads * 2), kThreads, 0, stream>>>(
+        static_cast<const uint4*>(x), n16, static_cast<const uint16_t*>(x) + n16 * 16, tail_n,
+        scale, reinterpret_cast<uint4*>(q), q + n16 * 16, reinterpret_cast<unsigned*>(amax));
+}
+
+template <int FMT, bool AMAX>
+static void launch_transpose(const void* x, int64_t rows, int64_t cols, const float* scale,
+                             uint8_t* q, uint8_t* qt, float* amax, cudaStream_t stream) {
+    const int64_t tiles_c = (cols + 127) / 128, tiles_r = (rows + 127) / 128;
+    quantize_transpose_kernel<FMT, AMAX><<<static_cast<unsigned>(tiles_r * tiles_c), kThreads, 0,
+                                           stream>>>(static_cast<const uint16_t*>(x), rows, cols,
+                                                     tiles_c, scale, q, qt,
+                                                     reinterpret_cast<unsigned*>(amax));
+}
+
+cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, int fmt,
+                                   const float* scale, uint8_t* q, uint8_t* q_t, float* amax,
+                                   cudaStream_t stream) {
+    const int64_t n = rows * cols;
+    if (amax) {
+        cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), stream);
+        if (e != cudaSuccess) return e;
+    }
+    if (n == 0) return cudaSuccess;
+    const bool A = amax != nullptr;
+    if (q_t) {
+        if (fmt == 0) {
+            if (A) launch_transpose<0, true>(x, rows, cols, scale, q, q_t, amax, stream);
+            else launch_transpose<0, false>(x, rows, cols, scale, q, q_t, amax, stream);
+        } else {
+            if (A) launch_transpose<1, true>(x, rows, cols, scale, q, q_t, amax, stream);
+            else launch_transpose<1, false>(x, rows, cols, scale, q, q_t, amax, stream);
+        }
+    } else {
+        if (fmt == 0) {
+            if (A) launch_flat<0, true>(x, n, scale, q, amax, stream);
+            else launch_flat<0, false>(x, n, scale, q, amax, stream);
+        } else {
+            if (A) launch_flat<1, true>(x, n, scale, q, amax, stream);
+            else launch_flat<1, false>(x, n, scale, q, amax, stream);
+        }
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_block(const void* x, int64_t rows, int64_t cols, int fmt, int gran,
+                                  int pow2, uint8_t* q, float* scale_inv, cudaStream_t stream) {
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    const uint16_t* xs = static_cast<const uint16_t*>(x);
+    if (gran == 1) {
+        const int64_t pairs = (rows * (cols / 128) + 1) / 2;
+        const int grid = grid_for(pairs, kThreads / 32);
+        if (fmt == 0) quantize_1x128_kernel<0><<<grid, kThreads, 0, stream>>>(xs, rows, cols, pow2, q, scale_inv);
+        else quantize_1x128_kernel<1><<<grid, kThreads, 0, stream>>>(xs, rows, cols, pow2, q, scale_inv);
+    } else {
+        const unsigned tiles = static_cast<unsigned>((rows / 128) * (cols / 128));
+        if (fmt == 0) quantize_128x128_kernel<0><<<tiles, kThreads, 0, stream>>>(xs, rows, cols, pow2, q, scale_inv);
+        else quantize_128x128_kernel<1><<<tiles, kThreads, 0, stream>>>(xs, rows, cols, pow2, q, scale_inv);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace fp8

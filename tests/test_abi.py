@@ -1,0 +1,104 @@
+"""The C-ABI library loads here (no GPU needed), exports every call that
+include/fp8linear.h declares, and rejects invalid arguments on the host,
+before any CUDA call, with the documented status codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import scaled_fp8_linear_gb300 as F
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(fp8_\w+)\s*\(", src, flags=re.M))
+    return names
+
+
+def test_library_exports_every_declared_call():
+    F.build()
+    lib = F.lib()
+    names = _declared()
+    assert {"fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_gemm", "fp8_linear_fwd",
+            "fp8_linear_bwd", "fp8_workspace_size", "fp8_last_error",
+            "fp8_device_status"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+FAKE = 0x10000  # a 16-byte-aligned address that is never dereferenced: every call below fails validation
+
+
+def test_gemm_argument_checks():
+    L = F.lib()
+    one = ctypes.c_void_p(FAKE)
+    ok = dict(A=one, fa=0, B=one, fb=0, M=128, N=128, K=128, layout=0, ga=0, sa=one, gb=0,
+              sb=one, D=one, out=0, acc=0, s=None)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return L.fp8_gemm(a["A"], a["fa"], a["B"], a["fb"], a["M"], a["N"], a["K"], a["layout"],
+                          a["ga"], a["sa"], a["gb"], a["sb"], a["D"], a["out"], a["acc"], a["s"])
+
+    assert call(A=None) == -1
+    assert call(fa=7) == -1
+    assert call(layout=3) == -1
+    assert call(out=5) == -1
+    assert call(acc=1) == -1                      # accumulate needs fp32 output
+    assert call(N=120) == -2 and call(K=40) == -2  # not multiples of 16
+    assert call(M=-1) == -2
+    assert call(ga=1, K=144) == -2                 # block scales need K % 128 == 0
+    assert call(ga=1, gb=1) == -6                  # 1x128 on B: not built
+    assert call(D=ctypes.c_void_p(FAKE + 4)) == -3
+    assert "16-byte" in F.fp8_last_error()
+
+
+def test_quantize_update_amax_argument_checks():
+    L = F.lib()
+    p = ctypes.c_void_p(FAKE)
+    assert L.fp8_quantize(None, 4, 4, 0, 0, p, 0, p, None, None, None, None) == -1
+    assert L.fp8_quantize(p, 4, 4, 9, 0, p, 0, p, None, None, None, None) == -1
+    assert L.fp8_quantize(p, 4, 4, 0, 0, None, 0, p, None, None, None, None) == -1  # no scale
+    assert L.fp8_quantize(p, 24, 16, 0, 0, p, 0, p, p, None, None, None) == -2      # transpose rule
+    assert L.fp8_quantize(p, 4, 100, 0, 1, None, 0, p, None, p, None, None) == -2   # cols % 128
+    assert L.fp8_quantize(p, 100, 128, 0, 2, None, 0, p, None, p, None, None) == -2  # rows % 128
+    assert L.fp8_quantize(p, 128, 128, 0, 1, p, 0, p, None, p, None, None) == -1    # scale in block mode
+    assert L.fp8_quantize(ctypes.c_void_p(FAKE + 2), 4, 4, 0, 0, p, 0, p, None, None, None, None) == -3
+    assert L.fp8_update_scale(p, p, p, 0, 0, 0, 0, 0, p, p, None) == -1
+    assert L.fp8_update_scale(p, p, p, 16, 0, 0, 65, 0, p, p, None) == -1
+    assert L.fp8_update_scale(p, p, p, 16, 2, 0, 0, 0, p, p, None) == -1
+    assert L.fp8_amax(p, -1, p, None) == -2
+    assert L.fp8_amax(None, 4, p, None) == -1
+
+
+def test_workspace_size_and_recipe_checks():
+    r = F.Recipe()
+    assert F.fp8_workspace_size(8192, 4096, 4096, r) == 2 * 8192 * 4096
+    assert F.fp8_workspace_size(16, 16, 16, r) == 2 * 256
+    assert F.fp8_workspace_size(256, 256, 256, F.Recipe(scaling=F.SCALING_BLOCK)) == 0
+    assert F.fp8_workspace_size(16, 16, 16, F.Recipe(history_len=0)) == 0
+    assert F.fp8_workspace_size(16, 16, 16, F.Recipe(margin=-1)) == 0
+    L = F.lib()
+    p = ctypes.c_void_p(FAKE)
+    st = F.LinearStateC()
+    bad = F.Recipe(history_len=2000)
+    assert L.fp8_linear_fwd(p, p, 16, 16, 16, ctypes.byref(bad), ctypes.byref(st), p, None, 0, None) == -1
+    blk = F.Recipe(scaling=F.SCALING_BLOCK)
+    assert L.fp8_linear_fwd(p, p, 16, 16, 16, ctypes.byref(blk), ctypes.byref(st), p, None, 0, None) == -2
+    assert L.fp8_linear_bwd(p, 128, 128, 128, ctypes.byref(blk), ctypes.byref(st), p, p, 0, p, 0, None) == -6
+    r = F.Recipe()
+    assert L.fp8_linear_fwd(p, p, 16, 16, 16, ctypes.byref(r), ctypes.byref(st), p, None, 0, None) == -1
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(4, 4, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        F.fp8_amax(x)

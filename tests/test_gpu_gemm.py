@@ -1,0 +1,144 @@
+"""GPU parity of the tcgen05 FP8 GEMMs (per-tensor and block-scaled) against
+the CPU oracle's fp64 GEMM: within |gpu - oracle| <= 2e-3 * sum|a b| s_a s_b
+per element, and exactly equal where every partial sum is representable."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scaled_fp8_linear_gb300 as F
+from tests.helpers import assert_gemm_bound
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    F.build()
+    F.lib()
+    yield
+    torch.cuda.synchronize()
+    assert F.fp8_device_status() == 0
+
+
+def _codes(rng, shape, fmt, std=1.0):
+    """Realistic FP8 operand: N(0, std^2) values cast with a per-tensor scale."""
+    v = rng.standard_normal(shape).astype(np.float32) * std
+    b = (v.view(np.uint32) >> 16).astype(np.uint16)
+    s = np.float32(oracle.fp8_max(fmt)) / oracle.amax(b)
+    q, _ = oracle.quantize(b, fmt, s)
+    return q, np.float32(1) / s
+
+
+def _t(a, dtype=torch.uint8):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _s(v):
+    return torch.tensor(np.asarray(v, np.float32).reshape(-1), device=DEV)
+
+
+SHAPES = [(128, 256, 128), (200, 336, 304), (1, 16, 16), (384, 512, 1024), (129, 272, 4000),
+          (256, 768, 2048), (640, 1280, 256)]
+FORMATS = [(F.E4M3, F.E4M3), (F.E5M2, F.E4M3), (F.E4M3, F.E5M2), (F.E5M2, F.E5M2)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("fa,fb", FORMATS)
+def test_tensor_scaled_bf16(M, N, K, fa, fb):
+    rng = np.random.default_rng(M + 7 * N + 13 * K + fa * 3 + fb)
+    A, sa = _codes(rng, (M, K), fa)
+    B, sb = _codes(rng, (N, K), fb, 0.02)
+    D = F.fp8_gemm(_t(A), fa, _t(B), fb, _s(sa), _s(sb))
+    Do, Dabs = oracle.gemm(A, fa, B, fb, sa, sb)
+    assert_gemm_bound(D, Do, Dabs, what=f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 336, 304), (256, 512, 2048), (1000, 272, 640)])
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_tensor_scaled_f32_accumulate(M, N, K, accumulate):
+    rng = np.random.default_rng(M * N + K)
+    A, sa = _codes(rng, (M, K), F.E5M2)
+    B, sb = _codes(rng, (N, K), F.E4M3)
+    prev = rng.standard_normal((M, N)).astype(np.float32)
+    D = _t(prev, torch.float32)
+    F.fp8_gemm(_t(A), F.E5M2, _t(B), F.E4M3, _s(sa), _s(sb), out=F.OUT_F32, D=D,
+               accumulate=accumulate)
+    Do, Dabs = oracle.gemm(A, F.E5M2, B, F.E4M3, sa, sb)
+    if accumulate:
+        assert_gemm_bound(D, Do + prev, Dabs, prev=prev)
+    else:
+        assert_gemm_bound(D, Do, Dabs)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (300, 512, 4096), (64, 48, 1040)])
+def test_exact_integer_products(M, N, K):
+    """Small-integer codes and power-of-two scales: every partial sum is an
+    integer below 2^24, so the FP32 result must equal the oracle exactly."""
+    rng = np.random.default_rng(K)
+    ai = rng.integers(-4, 5, size=(M, K)).astype(np.float32)
+    bi = rng.integers(-4, 5, size=(N, K)).astype(np.float32)
+    A = oracle.encode(ai, F.E4M3)
+    B = oracle.encode(bi, F.E5M2)
+    D = F.fp8_gemm(_t(A), F.E4M3, _t(B), F.E5M2, _s(0.5), _s(4.0), out=F.OUT_F32)
+    want = (ai.astype(np.int64) @ bi.astype(np.int64).T).astype(np.float64) * 2.0
+    assert np.array_equal(D.cpu().numpy().astype(np.float64), want)
+
+
+def test_degenerate_shapes():
+    A = torch.zeros(0, 64, dtype=torch.uint8, device=DEV)
+    B = torch.zeros(32, 64, dtype=torch.uint8, device=DEV)
+    D = F.fp8_gemm(A, F.E4M3, B, F.E4M3, _s(1.0), _s(1.0))
+    assert D.shape == (0, 32)
+    A = torch.zeros(16, 0, dtype=torch.uint8, device=DEV)
+    B = torch.zeros(32, 0, dtype=torch.uint8, device=DEV)
+    D = torch.full((16, 32), 7.0, dtype=torch.float32, device=DEV)
+    F.fp8_gemm(A, F.E4M3, B, F.E4M3, _s(1.0), _s(1.0), out=F.OUT_F32, D=D)
+    assert (D == 0).all()
+    D.fill_(7.0)
+    F.fp8_gemm(A, F.E4M3, B, F.E4M3, _s(1.0), _s(1.0), out=F.OUT_F32, D=D, accumulate=True)
+    assert (D == 7).all()
+
+
+def _block_operand(rng, shape, fmt, gran, std=1.0):
+    v = rng.standard_normal(shape).astype(np.float32) * std
+    v *= np.abs(rng.standard_t(3, size=(shape[0], 1))).astype(np.float32)
+    b = (v.view(np.uint32) >> 16).astype(np.uint16)
+    if gran == F.GRAN_TENSOR:
+        s = np.float32(oracle.fp8_max(fmt)) / oracle.amax(b)
+        return oracle.quantize(b, fmt, s)[0], np.array([1 / s], np.float32)
+    return oracle.block_quantize(b, fmt, 1 if gran == F.GRAN_1x128 else 128)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 512), (200, 384, 1024), (128, 128, 128),
+                                   (512, 640, 2048)])
+@pytest.mark.parametrize("ga,gb", [(F.GRAN_1x128, F.GRAN_128x128),
+                                   (F.GRAN_128x128, F.GRAN_128x128),
+                                   (F.GRAN_TENSOR, F.GRAN_128x128),
+                                   (F.GRAN_1x128, F.GRAN_TENSOR)])
+def test_block_scaled(M, N, K, ga, gb):
+    if ga == F.GRAN_128x128 and M % 128:
+        pytest.skip("128x128 scales on A need M % 128 == 0")
+    rng = np.random.default_rng(M + N + K + ga * 10 + gb)
+    A, sa = _block_operand(rng, (M, K), F.E4M3, ga)
+    B, sb = _block_operand(rng, (N, K), F.E4M3, gb, 0.02)
+    for out in (F.OUT_BF16, F.OUT_F32):
+        D = F.fp8_gemm(_t(A), F.E4M3, _t(B), F.E4M3, _s(sa), _s(sb), ga, gb, out=out)
+        Do, Dabs = oracle.gemm(A, F.E4M3, B, F.E4M3, sa, sb, ga, gb)
+        assert_gemm_bound(D, Do, Dabs, what=f"block {M}x{N}x{K} out={out}")
+
+
+def test_block_scaled_exact():
+    """Integer codes with power-of-two block factors: exact in FP32."""
+    rng = np.random.default_rng(3)
+    M, N, K = 256, 384, 1024
+    ai = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
+    bi = rng.integers(-3, 4, size=(N, K)).astype(np.float32)
+    sa = (2.0 ** rng.integers(-3, 4, size=(M, K // 128))).astype(np.float32)
+    sb = (2.0 ** rng.integers(-3, 4, size=(N // 128, K // 128))).astype(np.float32)
+    A, B = oracle.encode(ai, F.E4M3), oracle.encode(bi, F.E4M3)
+    D = F.fp8_gemm(_t(A), F.E4M3, _t(B), F.E4M3, _s(sa), _s(sb), F.GRAN_1x128, F.GRAN_128x128,
+                   out=F.OUT_F32)
+    Do, _ = oracle.gemm(A, F.E4M3, B, F.E4M3, sa, sb, F.GRAN_1x128, F.GRAN_128x128)
+    assert np.array_equal(D.cpu().numpy().astype(np.float64), Do)

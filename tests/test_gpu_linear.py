@@ -1,0 +1,173 @@
+"""GPU parity of the composed linear layer (fp8_linear_fwd / fp8_linear_bwd)
+against the oracle's own state machine: quantised operands, amaxes, scales
+and histories bit-exact at every step; Y, dX, dW within the GEMM bound.
+The last tests run the full-size workload shapes and check sampled rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scaled_fp8_linear_gb300 as F
+import synthetic
+from tests.helpers import assert_gemm_bound, bits, f32bits, u8
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    F.build()
+    F.lib()
+    yield
+    torch.cuda.synchronize()
+    assert F.fp8_device_status() == 0
+
+
+def _orecipe(r: F.Recipe) -> oracle.Recipe:
+    return oracle.Recipe(scaling=r.scaling, margin=r.margin, history_len=r.history_len,
+                         algo=r.amax_algo, pow2=bool(r.pow2))
+
+
+def _check_state(layer, ost, roles=(0, 1, 2)):
+    for r in roles:
+        rs = ost.roles[r]
+        assert f32bits(layer.scale[r].cpu().numpy()) == f32bits(rs.scale[0]), r
+        assert f32bits(layer.scale_inv[r].cpu().numpy()) == f32bits(rs.scale_inv[0]), r
+        assert np.array_equal(f32bits(layer.history[r].cpu().numpy()), f32bits(rs.history)), r
+        assert layer.pos[r].item() == rs.pos[0]
+
+
+@pytest.mark.parametrize("recipe", [
+    F.Recipe(F.SCALING_DELAYED, history_len=16),
+    F.Recipe(F.SCALING_DELAYED, history_len=4, amax_algo=F.AMAX_MOST_RECENT, margin=1),
+    F.Recipe(F.SCALING_DELAYED, history_len=16, pow2=True),
+    F.Recipe(F.SCALING_DYNAMIC)], ids=["delayed16", "delayed4_recent_m1", "delayed16_pow2", "dynamic"])
+def test_training_steps(recipe):
+    """20 steps (wrapping a 16-long history), fresh seeded X, dY each step,
+    fixed W; wgrad accumulated over pairs of steps (two micro-batches)."""
+    M, N, K = 256, 384, 512
+    layer = F.Fp8Linear(M, N, K, recipe, device=DEV)
+    orec = _orecipe(recipe)
+    ost = oracle.LinearState(orec)
+    W = synthetic.normal((N, K), 0.02, seed=1000)
+    dW = torch.zeros(N, K, dtype=torch.float32, device=DEV)
+    dW_o = np.zeros((N, K))
+    for step in range(20):
+        X = synthetic.with_outlier_channels((M, K), 1.0, 4, 50.0 if step % 5 else 200.0, seed=step)
+        dY = synthetic.normal((M, N), 1e-3 * (1 + step % 3), seed=100 + step)
+        if step == 7:
+            dY.zero_()                        # all-zero gradient: its scale update is skipped
+        acc = step % 2 == 1
+        Y = layer.forward(X.to(DEV), W.to(DEV))
+        dX, _ = layer.backward(dY.to(DEV), dW=dW, accumulate_dW=acc)
+        Yo, Yabs = oracle.linear_fwd(bits(X), bits(W), orec, ost)
+        prev = dW_o.copy()
+        (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(bits(dY), orec, ost,
+                                                       dW_prev=prev if acc else None)
+        assert np.array_equal(u8(layer.x_q), ost.x_q), step
+        assert np.array_equal(u8(layer.w_qt), ost.w_qt), step
+        assert np.array_equal(u8(layer.x_qt), ost.x_qt), step
+        assert np.array_equal(f32bits(layer.amax.cpu().numpy()), f32bits(ost.last_amax)), step
+        assert np.array_equal(f32bits(layer.qscale_inv.cpu().numpy()),
+                              f32bits(np.concatenate(ost.sinv_fwd))), step
+        _check_state(layer, ost)
+        assert_gemm_bound(Y, Yo, Yabs, what=f"Y step {step}")
+        assert_gemm_bound(dX, dXo, dXabs, what=f"dX step {step}")
+        assert_gemm_bound(dW, dWo, dWabs, prev=prev if acc else None, what=f"dW step {step}")
+        dW_o = dW.cpu().numpy().astype(np.float64)   # next step accumulates onto the GPU buffer
+
+
+def test_block_forward():
+    M, N, K = 300, 512, 768
+    rec = F.Recipe(F.SCALING_BLOCK)
+    layer = F.Fp8Linear(M, N, K, rec, device=DEV)
+    X = synthetic.student_t_rows((M, K), 1.0, 3, seed=5)
+    W = synthetic.student_t_rows((N, K), 0.02, 3, seed=6)
+    Y = layer.forward(X.to(DEV), W.to(DEV))
+    ost = oracle.LinearState(_orecipe(rec))
+    Yo, Yabs = oracle.linear_fwd(bits(X), bits(W), _orecipe(rec), ost)
+    assert np.array_equal(u8(layer.x_q), ost.x_q)
+    assert np.array_equal(u8(layer.w_q), ost.w_q)
+    assert np.array_equal(f32bits(layer.x_sinv.cpu().numpy()), f32bits(ost.x_sinv))
+    assert np.array_equal(f32bits(layer.w_sinv.cpu().numpy()), f32bits(ost.w_sinv))
+    assert_gemm_bound(Y, Yo, Yabs)
+
+
+def test_checkpoint_restore_gives_identical_next_step():
+    M, N, K = 128, 256, 256
+    rec = F.Recipe(F.SCALING_DELAYED, history_len=16)
+    a = F.Fp8Linear(M, N, K, rec, device=DEV)
+    W = synthetic.normal((N, K), 0.02, seed=1).to(DEV)
+    for s in range(5):
+        a.forward(synthetic.normal((M, K), 1.0 + s, seed=s).to(DEV), W)
+        a.backward(synthetic.normal((M, N), 1e-3, seed=50 + s).to(DEV))
+    sd = a.state_dict()
+    b = F.Fp8Linear(M, N, K, rec, device=DEV)
+    b.load_state_dict(sd)
+    X = synthetic.normal((M, K), 9.0, seed=99).to(DEV)
+    ya, yb = a.forward(X, W), b.forward(X, W)
+    assert torch.equal(ya, yb)
+    assert torch.equal(a.scale, b.scale) and torch.equal(a.history, b.history)
+
+
+# ----------------------------------------------------------- full-size shapes
+
+def _sample_rows(n, k, seed):
+    rng = np.random.default_rng(seed)
+    return np.sort(np.concatenate([[0, n - 1], rng.choice(n, k, replace=False)]))
+
+
+@pytest.mark.parametrize("name,M,N,K,recipe", [
+    ("llama2-7b qkv, delayed", 8192, 12288, 4096, F.Recipe(F.SCALING_DELAYED, history_len=16)),
+    ("llama2-7b down, delayed", 8192, 4096, 11008, F.Recipe(F.SCALING_DELAYED, history_len=16)),
+    ("llama2-70b gate, dynamic", 4096, 28672, 8192, F.Recipe(F.SCALING_DYNAMIC)),
+    ("llama2-70b down, dynamic", 4096, 8192, 28672, F.Recipe(F.SCALING_DYNAMIC))])
+def test_full_size_linear_sampled(name, M, N, K, recipe):
+    layer = F.Fp8Linear(M, N, K, recipe, device=DEV)
+    X = synthetic.with_outlier_channels((M, K), 1.0, max(1, K // 256), 50.0, seed=1, device=DEV)
+    W = synthetic.normal((N, K), 0.02, seed=2, device=DEV)
+    dY = synthetic.normal((M, N), 1e-3, seed=3, device=DEV)
+    Y = layer.forward(X, W)
+    dX, dW = layer.backward(dY)
+    torch.cuda.synchronize()
+    orec = _orecipe(recipe)
+    ost = oracle.LinearState(orec)
+    bx, bw, bdy = bits(X), bits(W), bits(dY)
+    # scales (whole-tensor amax) and quantised operands, bit-exact
+    rows_y = _sample_rows(M, 6, 1)
+    rows_dw = _sample_rows(N, 6, 2)
+    Yo, Yabs = oracle.linear_fwd(bx, bw, orec, ost, rows=rows_y)
+    (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(bdy, orec, ost, rows_dx=rows_y, rows_dw=rows_dw)
+    assert np.array_equal(u8(layer.x_q), ost.x_q)
+    assert np.array_equal(u8(layer.w_qt), ost.w_qt)
+    _check_state(layer, ost)
+    ry, rw = torch.as_tensor(rows_y, device=DEV), torch.as_tensor(rows_dw, device=DEV)
+    assert_gemm_bound(Y[ry], Yo, Yabs, what=name + " Y")
+    assert_gemm_bound(dX[ry], dXo, dXabs, what=name + " dX")
+    assert_gemm_bound(dW[rw], dWo, dWabs, what=name + " dW")
+
+
+@pytest.mark.parametrize("M,N,K", [(16384, 18432, 7168), (16384, 7168, 18432)])
+def test_full_size_block_gemm_sampled(M, N, K):
+    """Block-wise scaled forward at the DeepSeek-style shapes."""
+    layer = F.Fp8Linear(M, N, K, F.Recipe(F.SCALING_BLOCK), device=DEV)
+    X = synthetic.student_t_rows((M, K), 1.0, 3, seed=11, device=DEV)
+    W = synthetic.student_t_rows((N, K), 0.02, 3, seed=12, device=DEV)
+    Y = layer.forward(X, W)
+    torch.cuda.synchronize()
+    rows = _sample_rows(M, 8, 3)
+    x_q, x_s = layer.x_q.cpu().numpy(), layer.x_sinv.cpu().numpy()
+    # the quantised rows and their scales against the oracle's block cast of those rows
+    qo, so = oracle.block_quantize(bits(X[torch.as_tensor(rows, device=DEV)]), F.E4M3, 1)
+    assert np.array_equal(x_q[rows], qo)
+    assert np.array_equal(f32bits(x_s[rows]), f32bits(so))
+    wq, ws = oracle.block_quantize(bits(W), F.E4M3, 128)
+    assert np.array_equal(u8(layer.w_q), wq)
+    assert np.array_equal(f32bits(layer.w_sinv.cpu().numpy()), f32bits(ws))
+    ii = np.repeat(rows, N)
+    jj = np.tile(np.arange(N), rows.shape[0])
+    D, Dabs = oracle.gemm_entries(x_q, F.E4M3, wq, F.E4M3, x_s, ws, ii, jj, F.GRAN_1x128,
+                                  F.GRAN_128x128)
+    assert_gemm_bound(Y[torch.as_tensor(rows, device=DEV)], D.reshape(len(rows), N),
+                      Dabs.reshape(len(rows), N))
