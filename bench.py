@@ -86,7 +86,7 @@ class Clocks:
                  "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -169,6 +169,7 @@ def run_gpu(args):
 
     clocks = Clocks(local)
     clocks.start()
+    time.sleep(0.5)                                 # let the sampler start before the region
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     barrier()
@@ -183,10 +184,8 @@ def run_gpu(args):
     assert F.fp8_device_status() == 0, "a kernel reported a timeout"
     t_ms = sum(ms)
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([t_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_ms = t.item()
+        from scaled_fp8_linear_gb300.distributed import max_over_ranks
+        t_ms = max_over_ranks(t_ms, device=dev)
     flops = _flops_step() * args.steps * world
     value = flops / (t_ms * 1e-3) / 1e12
 
@@ -219,8 +218,8 @@ def run_gpu(args):
                      "traffic": None},
         "quantize": {"achieved_gbs": round(quant_gbs, 1), "peak_gbs": hbm_gbs,
                      "frac": round(quant_gbs / hbm_gbs, 4), "peak_source": f"{peak_kind} hbm_gbs"},
-        "kernels_ms_per_step": {k: round(v / args.steps, 4) for k, v in comp["by_kind"].items()},
-        "component_pass_ms_per_step": round(comp["total_ms"] / args.steps, 4),
+        "kernels_ms_per_step": {k: round(v / comp["steps"], 4) for k, v in comp["by_kind"].items()},
+        "component_pass_ms_per_step": round(comp["total_ms"] / comp["steps"], 4),
         "gpu_launches": 8 * len(LINEARS) * args.steps,
         "e2e": e2e,
         "clocks": clk,
@@ -246,7 +245,8 @@ def component_pass(F, layers, Xs, dYs, Ws, Ys, dXs, dWs, flush, args, stream):
         b.record(stream)
         pending.append((kind, a, b))
 
-    for s in range(args.steps):
+    n_steps = min(args.steps, 20)
+    for s in range(n_steps):
         flush.fill_(float(s))
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
@@ -289,7 +289,8 @@ def component_pass(F, layers, Xs, dYs, Ws, Ys, dXs, dWs, flush, args, stream):
         else:
             by_kind[kind] += ms
     return {"by_kind": by_kind, "gemm_ms": by_kind["gemm"], "quant_ms": by_kind["quantize"],
-            "gemm_flops": gemm_flops, "quant_bytes": quant_bytes, "total_ms": total}
+            "gemm_flops": gemm_flops, "quant_bytes": quant_bytes, "total_ms": total,
+            "steps": n_steps}
 
 
 def e2e_pass(F, recipe, dev, args, stream):
@@ -424,7 +425,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-rows", type=int, default=32)
