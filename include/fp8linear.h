@@ -193,6 +193,30 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K,
                    float* dW, int accumulate_dW, void* workspace, size_t workspace_bytes,
                    void* stream);
 
+/* Size of the built-in device scratch of fp8_linear_bwd_noalloc: 32 MiB. */
+#define FP8_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* fp8_linear_bwd for callers that cannot allocate device memory -- e.g. an
+ * operator inside a host framework whose memory planner owns every device
+ * buffer and passes it only its inputs and outputs, a latency-critical caller
+ * that must avoid cudaMalloc's implicit synchronisation, or a process whose
+ * caching allocator has reserved almost all device memory.  (The pages have
+ * no counterpart: this is a property of the library, not of the method.)
+ * Same arguments and results as fp8_linear_bwd, minus the workspace: the
+ * quantised gradient and its transpose go to a fixed device array of
+ * FP8_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library holds until the process exits.  Shapes whose
+ * fp8_workspace_size() exceeds it (2*M*N > 32 MiB, e.g. more than 4096 x
+ * 4096) are rejected with FP8_ERR_SHAPE and a message naming the limit.
+ * Calls no allocating routine.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Every call on a device
+ * shares the array and leaves its contents behind; calls whose work overlaps
+ * on the GPU race on it, so order them on one stream. */
+int fp8_linear_bwd_noalloc(const void* dY, int64_t M, int64_t N, int64_t K,
+                           const fp8_recipe_t* recipe, const fp8_linear_state_t* state,
+                           void* dX, float* dW, int accumulate_dW, void* stream);
+
 /* Message of the last failing call on this host thread ("" if none). */
 const char* fp8_last_error(void);
 

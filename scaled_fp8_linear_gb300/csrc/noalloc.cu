@@ -1,0 +1,83 @@
+// noalloc.cu -- fp8_linear_bwd_noalloc: the backward pass for callers that
+// cannot allocate device memory.
+//
+// fp8_linear_bwd needs 2 x M x N bytes of scratch for the quantised gradient
+// and its transpose, and asks the caller for it as a workspace.  Some callers
+// have no way to provide one: a custom operator inside a host framework whose
+// memory planner owns every device buffer and hands the operator only its
+// inputs and outputs; a latency-critical caller that must not pay for
+// cudaMalloc's implicit device synchronisation; a process whose caching
+// allocator has already reserved nearly all device memory, so that a raw
+// cudaMalloc fails although the pool has room.  For them the scratch lives in
+// this file's own device array, sized once when the library is loaded.
+//
+// The array is shared by every call on a device and keeps the last call's
+// contents.  Nothing in it has to start at zero: the gradient cast writes
+// every byte of both layouts before the GEMMs read them.  Calls whose work
+// overlaps on the GPU (e.g. issued on two streams without ordering) race on
+// the array and must be serialised by the caller.
+#include <cstddef>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/fp8linear.h"
+#include "internal.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = FP8_NOALLOC_SCRATCH_BYTES;
+
+// Held by every GPU that loads the library, until the process exits.
+static __device__ __align__(256) uint8_t g_bwd_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_bwd_scratch on the current device.  The host-side
+// symbol is only a stand-in, so the address is looked up once per device
+// (with that device current) and cached.
+int scratch_on_current_device(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fp8::set_error(FP8_ERR_CUDA, "fp8_linear_bwd_noalloc: cudaGetDevice: %s",
+                              cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices)
+        return fp8::set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd_noalloc: device %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_bwd_scratch);
+        if (e != cudaSuccess || !p)
+            return fp8::set_error(FP8_ERR_CUDA,
+                                  "fp8_linear_bwd_noalloc: cudaGetSymbolAddress: %s",
+                                  cudaGetErrorString(e));
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return FP8_OK;
+}
+
+}  // namespace
+
+extern "C" int fp8_linear_bwd_noalloc(const void* dY, int64_t M, int64_t N, int64_t K,
+                                      const fp8_recipe_t* recipe,
+                                      const fp8_linear_state_t* state, void* dX, float* dW,
+                                      int accumulate_dW, void* stream) {
+    const size_t need = fp8_workspace_size(M, N, K, recipe);
+    if (need > kScratchBytes)
+        return fp8::set_error(FP8_ERR_SHAPE,
+                              "fp8_linear_bwd_noalloc: M x N = %lld x %lld needs %zu bytes of "
+                              "scratch; the built-in scratch holds %zu bytes "
+                              "(2 x M x N <= %zu)",
+                              static_cast<long long>(M), static_cast<long long>(N), need,
+                              kScratchBytes, kScratchBytes);
+    void* scratch = nullptr;
+    const int st = scratch_on_current_device(&scratch);
+    if (st != FP8_OK) return st;
+    return fp8_linear_bwd(dY, M, N, K, recipe, state, dX, dW, accumulate_dW, scratch,
+                          kScratchBytes, stream);
+}

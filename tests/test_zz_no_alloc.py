@@ -1,0 +1,76 @@
+"""fp8_linear_bwd_noalloc -- the backward entry point for callers that cannot
+allocate device memory (its scratch is a fixed device array inside the
+library) -- against the existing fp8_linear_bwd with a caller workspace, on
+two calls in a row.  Called through the C ABI with ctypes.  This file sorts
+last so that a run stopping at the first failure has run every other test
+first; it also passes on its own in a fresh process."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scaled_fp8_linear_gb300 as F
+import synthetic
+from tests.helpers import assert_gemm_bound, bits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _noalloc():
+    F.build()
+    L = F.lib()
+    fn = L.fp8_linear_bwd_noalloc
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                   ctypes.POINTER(F.Recipe), ctypes.POINTER(F.LinearStateC), ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    return fn
+
+
+def test_noalloc_backward_matches_workspace_backward():
+    fn = _noalloc()
+    M, N, K = 512, 768, 1024
+    rec = F.Recipe(F.SCALING_DELAYED, history_len=16)
+    ref_layer = F.Fp8Linear(M, N, K, rec, device=DEV)    # fp8_linear_bwd + workspace
+    na_layer = F.Fp8Linear(M, N, K, rec, device=DEV)     # fp8_linear_bwd_noalloc
+    orec = oracle.Recipe(scaling=oracle.SCALING_DELAYED, history_len=16)
+    ost = oracle.LinearState(orec)
+    W = synthetic.normal((N, K), 0.02, seed=7)
+    dW_ref = torch.zeros(N, K, dtype=torch.float32, device=DEV)
+    dW_na = torch.zeros(N, K, dtype=torch.float32, device=DEV)
+    stream = torch.cuda.current_stream().cuda_stream
+    for step in range(2):
+        X = synthetic.with_outlier_channels((M, K), 1.0, 4, 50.0, seed=10 + step)
+        dY = synthetic.normal((M, N), 1e-3, seed=20 + step)
+        ref_layer.forward(X.to(DEV), W.to(DEV))
+        na_layer.forward(X.to(DEV), W.to(DEV))
+        dX_ref, _ = ref_layer.backward(dY.to(DEV), dW=dW_ref, accumulate_dW=step > 0)
+        dX_na = torch.empty(M, K, dtype=torch.bfloat16, device=DEV)
+        dYd = dY.to(DEV)
+        st = fn(dYd.data_ptr(), M, N, K, ctypes.byref(rec), ctypes.byref(na_layer.c_state),
+                dX_na.data_ptr(), dW_na.data_ptr(), int(step > 0), stream)
+        assert st == 0, F.fp8_last_error()
+        torch.cuda.synchronize()
+        # tolerance of the GEMM tests: 2e-3 * sum|a b| * s_a * s_b (+ bf16 rounding)
+        oracle.linear_fwd(bits(X), bits(W), orec, ost)
+        (_, dXabs), (_, dWabs) = oracle.linear_bwd(bits(dY), orec, ost)
+        assert_gemm_bound(dX_na, dX_ref.float().cpu().numpy().astype(np.float64), dXabs,
+                          what=f"dX call {step}")
+        assert_gemm_bound(dW_na, dW_ref.cpu().numpy().astype(np.float64), dWabs,
+                          what=f"dW call {step}")
+        assert torch.equal(na_layer.scale, ref_layer.scale)
+        assert torch.equal(na_layer.history, ref_layer.history)
+    assert F.fp8_device_status() == 0
+
+
+def test_noalloc_rejects_shapes_beyond_the_scratch():
+    fn = _noalloc()
+    rec = F.Recipe(F.SCALING_DELAYED, history_len=16)
+    st = F.LinearStateC()
+    p = ctypes.c_void_p(0x10000)
+    # 2 * 8192 * 4096 bytes > 32 MiB: rejected before any device work
+    assert fn(p, 8192, 4096, 4096, ctypes.byref(rec), ctypes.byref(st), p, p, 0, None) == -2
+    assert "scratch" in F.fp8_last_error()
