@@ -294,43 +294,85 @@ def component_pass(F, layers, Xs, dYs, Ws, Ys, dXs, dWs, flush, args, stream):
 
 
 def e2e_pass(F, recipe, dev, args, stream):
-    """Public API with host buffers: per step H2D of X, W, dY (pinned), the
-    five linears' fwd+bwd, D2H of Y, dX, dW; timed with events on the stream."""
-    hX, hW, hdY, dX_, dW_, dY_, hY, hdX, hdW, layers, dXd, dWd, dYd = ([] for _ in range(13))
+    """Public API with host buffers.  Per step and linear: H2D of X, W, dY from
+    pinned memory, fp8_linear_fwd + fp8_linear_bwd, D2H of Y, dX, dW -- all
+    inside the timed region.  Copies run on their own streams so that the
+    next linear's inputs arrive and the previous one's results leave while
+    the current linear computes (two device buffer sets, event-ordered)."""
+    nl = len(LINEARS)
+    h_in, h_out, layers = [], [], []
     for li, (name, K, N) in enumerate(LINEARS):
-        hX.append(synthetic.with_outlier_channels((TOKENS, K), 1.0, 16, 50.0, seed=li).pin_memory())
-        hW.append(synthetic.normal((N, K), 0.02, seed=1000 + li).pin_memory())
-        hdY.append(synthetic.normal((TOKENS, N), 1e-3, seed=500 + li).pin_memory())
-        hY.append(torch.empty(TOKENS, N, dtype=torch.bfloat16).pin_memory())
-        hdX.append(torch.empty(TOKENS, K, dtype=torch.bfloat16).pin_memory())
-        hdW.append(torch.empty(N, K, dtype=torch.float32).pin_memory())
+        n_out = 43 if K == 11008 else 16
+        h_in.append((synthetic.with_outlier_channels((TOKENS, K), 1.0, n_out, 50.0, seed=li).pin_memory(),
+                     synthetic.normal((N, K), 0.02, seed=1000 + li).pin_memory(),
+                     synthetic.normal((TOKENS, N), 1e-3, seed=500 + li).pin_memory()))
+        h_out.append((torch.empty(TOKENS, N, dtype=torch.bfloat16).pin_memory(),
+                      torch.empty(TOKENS, K, dtype=torch.bfloat16).pin_memory(),
+                      torch.empty(N, K, dtype=torch.float32).pin_memory()))
         layers.append(F.Fp8Linear(TOKENS, N, K, recipe, device=dev))
-        dX_.append(torch.empty(TOKENS, K, dtype=torch.bfloat16, device=dev))
-        dW_.append(torch.empty(N, K, dtype=torch.bfloat16, device=dev))   # device copy of W
-        dY_.append(torch.empty(TOKENS, N, dtype=torch.bfloat16, device=dev))
-        dXd.append(torch.empty(TOKENS, K, dtype=torch.bfloat16, device=dev))  # device copy of X
-        dWd.append(torch.zeros(N, K, dtype=torch.float32, device=dev))
-        dYd.append(torch.empty(TOKENS, N, dtype=torch.bfloat16, device=dev))
-    h2d = sum(t.numel() * t.element_size() for t in hX + hW + hdY)
-    d2h = sum(t.numel() * t.element_size() for t in hY + hdX + hdW)
-    Ydev = [torch.empty(TOKENS, n, dtype=torch.bfloat16, device=dev) for _, _, n in LINEARS]
+    kmax = max(k for _, k, _ in LINEARS)
+    nmax = max(n for _, _, n in LINEARS)
+    nk = max(n * k for _, k, n in LINEARS)
+
+    def dbuf():
+        return {"X": torch.empty(TOKENS * kmax, dtype=torch.bfloat16, device=dev),
+                "W": torch.empty(nk, dtype=torch.bfloat16, device=dev),
+                "dY": torch.empty(TOKENS * nmax, dtype=torch.bfloat16, device=dev),
+                "Y": torch.empty(TOKENS * nmax, dtype=torch.bfloat16, device=dev),
+                "dX": torch.empty(TOKENS * kmax, dtype=torch.bfloat16, device=dev),
+                "dW": torch.empty(nk, dtype=torch.float32, device=dev)}
+
+    bufs = [dbuf(), dbuf()]
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    h2d = sum(t.numel() * t.element_size() for tr in h_in for t in tr)
+    d2h = sum(t.numel() * t.element_size() for tr in h_out for t in tr)
 
     def one():
-        for li in range(len(LINEARS)):
-            dXd[li].copy_(hX[li], non_blocking=True)
-            dW_[li].copy_(hW[li], non_blocking=True)
-            dYd[li].copy_(hdY[li], non_blocking=True)
+        loaded = [torch.cuda.Event() for _ in range(nl)]
+        computed = [torch.cuda.Event() for _ in range(nl)]
+        drained = [torch.cuda.Event() for _ in range(nl)]
+        h2d_s.wait_stream(stream)        # previous step's readers of both buffer sets are done
+
+        def load(li):
+            _, K, N = LINEARS[li]
+            b = bufs[li % 2]
+            with torch.cuda.stream(h2d_s):
+                if li >= 2:
+                    h2d_s.wait_event(computed[li - 2])   # the buffer set's last reader
+                hx, hw, hdy = h_in[li]
+                b["X"][:TOKENS * K].view(TOKENS, K).copy_(hx, non_blocking=True)
+                b["W"][:N * K].view(N, K).copy_(hw, non_blocking=True)
+                b["dY"][:TOKENS * N].view(TOKENS, N).copy_(hdy, non_blocking=True)
+                loaded[li].record(h2d_s)
+
+        load(0)
+        for li, (name, K, N) in enumerate(LINEARS):
+            if li + 1 < nl:
+                load(li + 1)
+            b = bufs[li % 2]
+            stream.wait_event(loaded[li])
+            if li >= 2:
+                stream.wait_event(drained[li - 2])       # outputs of this set have left
+            Y = b["Y"][:TOKENS * N].view(TOKENS, N)
+            dX = b["dX"][:TOKENS * K].view(TOKENS, K)
+            dW = b["dW"][:N * K].view(N, K)
             L = layers[li]
-            L.forward(dXd[li], dW_[li], Y=Ydev[li])
-            L.backward(dYd[li], dX=dX_[li], dW=dWd[li], accumulate_dW=False)
-            hY[li].copy_(Ydev[li], non_blocking=True)
-            hdX[li].copy_(dX_[li], non_blocking=True)
-            hdW[li].copy_(dWd[li], non_blocking=True)
+            L.forward(b["X"][:TOKENS * K].view(TOKENS, K), b["W"][:N * K].view(N, K), Y=Y)
+            L.backward(b["dY"][:TOKENS * N].view(TOKENS, N), dX=dX, dW=dW, accumulate_dW=False)
+            computed[li].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(computed[li])
+                hy, hdx, hdw = h_out[li]
+                hy.copy_(Y, non_blocking=True)
+                hdx.copy_(dX, non_blocking=True)
+                hdw.copy_(dW, non_blocking=True)
+                drained[li].record(d2h_s)
+        stream.wait_stream(d2h_s)
 
     for _ in range(max(1, min(args.warmup, 3))):
         one()
     torch.cuda.synchronize()
-    n = max(1, min(args.steps, 5))
+    n = max(1, min(args.steps, 10))
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for _ in range(n):
@@ -340,7 +382,8 @@ def e2e_pass(F, recipe, dev, args, stream):
     ms = a.elapsed_time(b) / n
     return {"value": round(_flops_step() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "steps": n, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+            "d2h_bytes_per_step": d2h,
+            "copies": "pinned host <-> device on two copy streams, overlapped with compute"}
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -422,6 +465,74 @@ def run_reference(args):
                 "d2h_bytes_per_step": 0}}))
 
 
+def run_kernel(args):
+    """Time one kernel of the path on one shape (not the headline number):
+    gemm (per-tensor, E4M3 or E5M2 x E4M3, bf16 out), block_gemm (1x128 x
+    128x128 scales, bf16 out) or quantize (fused amax + cast + transpose,
+    stale scale).  L2 is flushed before every timed launch."""
+    import scaled_fp8_linear_gb300 as F
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    F.lib()
+    hbm_gbs, bf16_burst, _, peak_kind = _peaks()
+    dims = [int(v) for v in args.shape.split(",")]
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    fa = F.E5M2 if args.fmt == "e5m2" else F.E4M3
+
+    def codes(r, c):
+        # random finite FP8 codes: magnitude codes 0x00..0x7B (finite in both formats) | sign
+        v = torch.randint(0, 0x7C, (r, c), generator=g, device=dev, dtype=torch.int32)
+        v |= torch.randint(0, 2, (r, c), generator=g, device=dev, dtype=torch.int32) << 7
+        return v.to(torch.uint8)
+
+    if args.kernel in ("gemm", "block_gemm"):
+        M, N, K = dims
+        A, B = codes(M, K), codes(N, K)
+        D = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        if args.kernel == "gemm":
+            one = torch.ones(1, dtype=torch.float32, device=dev)
+            call = lambda: F.fp8_gemm(A, fa, B, F.E4M3, one, one, D=D)
+        else:
+            sa = torch.rand(M, K // 128, generator=g, device=dev) + 0.5
+            sb = torch.rand(N // 128, K // 128, generator=g, device=dev) + 0.5
+            call = lambda: F.fp8_gemm(A, F.E4M3, B, F.E4M3, sa, sb, F.GRAN_1x128,
+                                      F.GRAN_128x128, D=D)
+        work, unit, peak = 2.0 * M * N * K, "TFLOP/s", 2.0 * bf16_burst
+    else:
+        R, C = dims
+        x = synthetic.student_t((R, C), 3, 1.0, seed=1, device=dev)
+        q = torch.empty(R, C, dtype=torch.uint8, device=dev)
+        qt = torch.empty(C, R, dtype=torch.uint8, device=dev)
+        am = torch.empty(1, dtype=torch.float32, device=dev)
+        one = torch.ones(1, dtype=torch.float32, device=dev)
+        call = lambda: F.fp8_quantize(x, fa, scale=one, q=q, q_t=qt, amax_out=am)
+        work, unit, peak = 4.0 * R * C, "GB/s", hbm_gbs
+    for _ in range(args.warmup):
+        call()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.iters)]
+    for i in range(args.iters):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert F.fp8_device_status() == 0
+    ms = sorted(a.elapsed_time(b) for a, b in ev)
+    med = ms[len(ms) // 2]
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    ach = work / (med * 1e-3) / scale
+    print(json.dumps({"kernel": args.kernel, "shape": dims, "format": args.fmt,
+                      "median_ms": round(med, 4), "min_ms": round(ms[0], 4),
+                      "achieved": round(ach, 1), "unit": unit, "peak": round(peak, 1),
+                      "frac": round(ach / peak, 4),
+                      "peak_source": f"{peak_kind} ({'2 x bf16 burst' if unit == 'TFLOP/s' else 'hbm_gbs'})",
+                      "iters": args.iters, "l2": "flushed before every launch"}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -431,10 +542,17 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=32)
     ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["gemm", "block_gemm", "quantize"],
+                    help="time one kernel on --shape instead of the layer step")
+    ap.add_argument("--shape", default="8192,12288,4096")
+    ap.add_argument("--fmt", choices=["e4m3", "e5m2"], default="e4m3")
+    ap.add_argument("--iters", type=int, default=20)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.kernel:
+        run_kernel(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

@@ -120,6 +120,58 @@ __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t
     }
 }
 
+// Epilogue of one 32-column chunk of an accumulator row: scale by alpha, then
+// round to bf16 or (optionally) add into the FP32 buffer; 16-byte stores.
+__device__ __forceinline__ void store_chunk(const uint32_t (&r)[32], int64_t m, int64_t n0,
+                                            const GemmParams& p, float alpha, bool rmw) {
+    if (p.out == FP8_OUT_BF16) {
+        __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.D) + m * p.N;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+            if (n0 + j < p.N) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __nv_bfloat162 h =
+                        __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[j + 2 * e]), alpha),
+                                              __fmul_rn(__uint_as_float(r[j + 2 * e + 1]), alpha));
+                    w[e] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+                *reinterpret_cast<uint4*>(drow + n0 + j) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    } else {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.D) + m * p.N + n0);
+        // all loads of the chunk first, so that their latencies overlap
+        float4 o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            o[j] = (rmw && n0 + 4 * j < p.N) ? dst[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (n0 + 4 * j < p.N) {
+                float4 v = make_float4(__fmul_rn(__uint_as_float(r[4 * j]), alpha),
+                                       __fmul_rn(__uint_as_float(r[4 * j + 1]), alpha),
+                                       __fmul_rn(__uint_as_float(r[4 * j + 2]), alpha),
+                                       __fmul_rn(__uint_as_float(r[4 * j + 3]), alpha));
+                if (rmw) {
+                    v.x += o[j].x; v.y += o[j].y; v.z += o[j].z; v.w += o[j].w;
+                }
+                dst[j] = v;
+            }
+        }
+    }
+}
+
+// The FP32 accumulation rows that an epilogue thread will read for a tile:
+// pulled into L2 while the tensor cores work, so the read-modify-write hits L2.
+__device__ __forceinline__ void prefetch_row(int64_t m, int64_t n0, int width,
+                                             const GemmParams& p) {
+    if (m >= p.M) return;
+    const int64_t cols = p.N - n0 < width ? p.N - n0 : width;
+    ptx::prefetch_l2(static_cast<const float*>(p.D) + m * p.N + n0, static_cast<uint32_t>(cols * 4));
+}
+
 // --------------------------------------------------------- per-tensor kernel
 
 template <int BN, int STAGES>
@@ -206,9 +258,13 @@ __global__ void __launch_bounds__(256, 1)
         const int row = qd * 32 + lane;
         const float alpha = __fmul_rn(p.sa[0], p.sb[0]);
         uint32_t acc = 0, acc_phase = 0;
+        const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             int m_blk, n_blk;
             tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+            if (rmw)
+                prefetch_row(static_cast<int64_t>(m_blk) * BM + row, static_cast<int64_t>(n_blk) * BN,
+                             BN, p);
             bool ok = (lane == 0) ? ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag) : false;
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
@@ -222,43 +278,7 @@ __global__ void __launch_bounds__(256, 1)
                 ptx::tmem_ld_32x32b_x32(tbase + c * 32, r);
                 ptx::tmem_wait_ld();
                 const int64_t n0 = static_cast<int64_t>(n_blk) * BN + c * 32;
-                if (m < p.M) {
-                    if (p.out == FP8_OUT_BF16) {
-                        __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.D) + m * p.N;
-#pragma unroll
-                        for (int j = 0; j < 32; j += 8) {
-                            if (n0 + j < p.N) {
-                                uint32_t w[4];
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const __nv_bfloat162 h = __floats2bfloat162_rn(
-                                        __fmul_rn(__uint_as_float(r[j + 2 * e]), alpha),
-                                        __fmul_rn(__uint_as_float(r[j + 2 * e + 1]), alpha));
-                                    w[e] = *reinterpret_cast<const uint32_t*>(&h);
-                                }
-                                *reinterpret_cast<uint4*>(drow + n0 + j) =
-                                    make_uint4(w[0], w[1], w[2], w[3]);
-                            }
-                        }
-                    } else {
-                        float* drow = static_cast<float*>(p.D) + m * p.N;
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            if (n0 + j < p.N) {
-                                float4 v = make_float4(__fmul_rn(__uint_as_float(r[j]), alpha),
-                                                       __fmul_rn(__uint_as_float(r[j + 1]), alpha),
-                                                       __fmul_rn(__uint_as_float(r[j + 2]), alpha),
-                                                       __fmul_rn(__uint_as_float(r[j + 3]), alpha));
-                                float4* dst = reinterpret_cast<float4*>(drow + n0 + j);
-                                if (p.accumulate) {
-                                    const float4 o = *dst;
-                                    v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
-                                }
-                                *dst = v;
-                            }
-                        }
-                    }
-                }
+                if (m < p.M) store_chunk(r, m, n0, p, alpha, rmw);
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -273,6 +293,178 @@ __global__ void __launch_bounds__(256, 1)
     if (warp == 2) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_device_status, 1u);
+}
+
+// ------------------------------------------------------- CTA-pair kernel
+
+// A cluster of two CTAs (on the two SMs of a TPC) computes a 256 x 256 tile
+// with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 32):
+//   - CTA r loads rows [r*128, r*128+128) of the tile's A panel and of its B
+//     panel into its own ring (16 + 16 KiB per stage), so each SM streams
+//     half the B bytes that a 128 x 256 single-CTA tile needs;
+//   - both CTAs' TMA completions count on the even CTA's `full` barrier, whose
+//     MMA thread issues the pair MMAs; each CTA's TMEM receives its 128 rows
+//     of the 256 x 256 FP32 accumulator (two accumulators, 512 columns);
+//   - MMA completion is multicast to both CTAs' `empty` and `tfull` barriers;
+//     both CTAs' epilogue warps arrive on the even CTA's `tempty` barrier.
+template <int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    constexpr int HALF = 128;              // rows of A and of B held by each CTA
+    constexpr int TILE = 2 * HALF;         // pair tile: 256 x 256
+    constexpr int A_BYTES = HALF * BK, B_BYTES = HALF * BK;
+    constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    constexpr uint32_t TMEM_COLS = 2 * TILE;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + STAGES * STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* done = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const bool leader = rank == 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(&tfull[a], 1);
+            ptx::mbar_init(&tempty[a], 8);      // 4 epilogue warps x 2 CTAs
+        }
+        ptx::mbar_init(done, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::tma_prefetch_desc(&tmA);
+        ptx::tma_prefetch_desc(&tmB);
+    }
+    if (warp == 2) {
+        ptx::tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    ptx::cluster_sync();   // the peer's barriers exist before any remote arrival
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int num_tiles = p.num_m * p.num_n;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
+                int m_blk, n_blk;
+                tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+                const int ya = m_blk * TILE + static_cast<int>(rank) * HALF;
+                const int yb = n_blk * TILE + static_cast<int>(rank) * HALF;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+                    uint8_t* sa = ring + stage * STAGE_BYTES;
+                    const uint32_t bar = ptx::cluster_addr(&full[stage], 0);
+                    if (leader) ptx::mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
+                    ptx::tma_load_2d_pair(sa, &tmA, bar, kb * BK, ya);
+                    ptx::tma_load_2d_pair(sa + A_BYTES, &tmB, bar, kb * BK, yb);
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            uint32_t never = 0;
+            if (leader) {
+                // drain: the last copies into each slot (both CTAs' bytes) have landed
+                for (int s = 0; s < STAGES; ++s) {
+                    if (issued <= s && issued < STAGES) break;
+                    const uint32_t par = (static_cast<uint32_t>(s) < stage) ? phase : (phase ^ 1u);
+                    ptx::mbar_wait(&full[s], par, &never);
+                }
+            } else if (!ok) {
+                // copies signal the peer's barriers: after an abort, give those in
+                // flight a bounded grace period to land before this CTA moves on
+                const uint64_t t0 = ptx::globaltimer();
+                while (ptx::globaltimer() - t0 < 1000000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            const uint32_t idesc = ptx::idesc_f8f6f4(p.fa, p.fb, TILE, TILE);
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
+                if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) break;
+                ptx::tc_fence_after();
+                const uint32_t d = tmem_base + acc * TILE;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    uint8_t* sa = ring + stage * STAGE_BYTES;
+                    const uint64_t ad = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa));
+                    const uint64_t bd = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa + A_BYTES));
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k)
+                        ptx::mma_f8f6f4_pair(d, ad + (k * UMMA_K >> 4), bd + (k * UMMA_K >> 4),
+                                             idesc, (kb | k) != 0);
+                    ptx::mma_commit_pair(&empty[stage], 0x3);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                ptx::mma_commit_pair(&tfull[acc], 0x3);
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            uint32_t never = 0;
+            ptx::mma_commit_pair(done, 0x1);
+            ptx::mbar_wait(done, 0, &never);
+        }
+    } else if (warp >= 4) {
+        const int qd = warp & 3;
+        const int row = qd * 32 + lane;
+        const float alpha = __fmul_rn(p.sa[0], p.sb[0]);
+        const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
+        uint32_t acc = 0, acc_phase = 0;
+        for (int tile = pair; tile < num_tiles; tile += npairs) {
+            int m_blk, n_blk;
+            tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+            const int64_t m = static_cast<int64_t>(m_blk) * TILE + rank * HALF + row;
+            if (rmw) prefetch_row(m, static_cast<int64_t>(n_blk) * TILE, TILE, p);
+            bool ok = (lane == 0) ? ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag) : false;
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            __syncwarp();
+            ptx::tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + acc * TILE;
+#pragma unroll 1
+            for (int c = 0; c < TILE / 32; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(tbase + c * 32, r);
+                ptx::tmem_wait_ld();
+                if (m < p.M) store_chunk(r, m, static_cast<int64_t>(n_blk) * TILE + c * 32, p, alpha, rmw);
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(ptx::cluster_addr(&tempty[acc], 0));
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    ptx::tc_fence_before();
+    ptx::cluster_sync();   // the pair's MMAs, copies and remote arrivals are all done
+    if (warp == 2) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
     if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_device_status, 1u);
 }
@@ -377,6 +569,9 @@ __global__ void __launch_bounds__(384, 1)
             const int64_t m = static_cast<int64_t>(m_blk) * BM + row;
             const int64_t m_safe = m < p.M ? m : p.M - 1;
             const int64_t n_row = static_cast<int64_t>(n_blk) * BN;  // a row of B in this tile
+            const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
+            if (rmw && m < p.M)
+                ptx::prefetch_l2(static_cast<const float*>(p.D) + m * p.N + n_row + half * 64, 64 * 4);
             float acc[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
@@ -428,17 +623,22 @@ __global__ void __launch_bounds__(384, 1)
                         }
                     }
                 } else {
-                    float* drow = static_cast<float*>(p.D) + m * p.N;
+                    // block mode has N % 128 == 0: all 64 columns of this half exist
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.D) + m * p.N + n0);
 #pragma unroll
-                    for (int j = 0; j < 64; j += 4) {
-                        if (n0 + j < p.N) {
-                            float4 v = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-                            float4* dst = reinterpret_cast<float4*>(drow + n0 + j);
-                            if (p.accumulate) {
-                                const float4 o = *dst;
-                                v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+                    for (int h = 0; h < 2; ++h) {
+                        float4 o[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            o[j] = rmw ? dst[h * 8 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int c = (h * 8 + j) * 4;
+                            float4 v = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+                            if (rmw) {
+                                v.x += o[j].x; v.y += o[j].y; v.z += o[j].z; v.w += o[j].w;
                             }
-                            *dst = v;
+                            dst[h * 8 + j] = v;
                         }
                     }
                 }
@@ -498,6 +698,10 @@ int make_kmajor_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K,
 }
 
 constexpr int kTensorBN = 256, kTensorStages = 4;
+constexpr int kPairStages = 6;
+constexpr int kPairSmemBytes = kPairStages * 2 * 128 * BK + 256 + 1024;
+// Problems with at least this many rows use the CTA-pair kernel.
+constexpr int64_t kPairMinRows = INT64_MAX;  // (pair kernel not yet selected)
 constexpr int kBlockStages = 6;
 
 template <typename Kernel>
@@ -514,6 +718,29 @@ int ensure_smem(Kernel k, int bytes, int kernel_id) {
         return set_error(FP8_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     done[dev][kernel_id] = true;
     return FP8_OK;
+}
+
+// How many 2-CTA clusters of the pair kernel fit on the device at once (the
+// persistent grid size); cached per device.
+int pair_clusters(const void* func) {
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * 1024, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.dynamicSmemBytes = kPairSmemBytes;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess || n <= 0) {
+            (void)cudaGetLastError();
+            n = num_sms() / 2;
+        }
+        cache[dev] = n;
+    }
+    return cache[dev];
 }
 
 }  // namespace
@@ -543,10 +770,12 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
                                 : set_error(FP8_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
     }
     const bool block = ga != FP8_GRAN_TENSOR || gb != FP8_GRAN_TENSOR;
+    const bool pair = !block && M >= kPairMinRows;
     const int BN = block ? 128 : kTensorBN;
+    const int TM = pair ? 256 : BM;   // rows of C per tile
     GemmParams p;
     p.M = M; p.N = N; p.K = K;
-    p.num_m = static_cast<int>((M + BM - 1) / BM);
+    p.num_m = static_cast<int>((M + TM - 1) / TM);
     p.num_n = static_cast<int>((N + BN - 1) / BN);
     p.num_kb = static_cast<int>((K + BK - 1) / BK);
     p.fa = fa; p.fb = fb; p.ga = ga; p.gb = gb; p.sa = sa; p.sb = sb;
@@ -555,12 +784,18 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
     CUtensorMap tmA, tmB;
     int st = make_kmajor_map(&tmA, A, M, K, BM);
     if (st != FP8_OK) return st;
-    st = make_kmajor_map(&tmB, B, N, K, BN);
+    st = make_kmajor_map(&tmB, B, N, K, pair ? 128 : BN);
     if (st != FP8_OK) return st;
 
     const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
     const int grid = static_cast<int>(tiles < num_sms() ? tiles : num_sms());
-    if (!block) {
+    if (pair) {
+        auto k = gemm_pair_kernel<kPairStages>;
+        if ((st = ensure_smem(k, kPairSmemBytes, 2)) != FP8_OK) return st;
+        const int64_t clusters = pair_clusters(reinterpret_cast<const void*>(k));
+        const int pgrid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
+        k<<<pgrid, 256, kPairSmemBytes, stream>>>(tmA, tmB, p);
+    } else if (!block) {
         using L = Layout<kTensorBN, kTensorStages>;
         auto k = gemm_tensor_kernel<kTensorBN, kTensorStages>;
         if ((st = ensure_smem(k, L::SMEM_BYTES, 0)) != FP8_OK) return st;
