@@ -701,7 +701,7 @@ constexpr int kTensorBN = 256, kTensorStages = 4;
 constexpr int kPairStages = 6;
 constexpr int kPairSmemBytes = kPairStages * 2 * 128 * BK + 256 + 1024;
 // Problems with at least this many rows use the CTA-pair kernel.
-constexpr int64_t kPairMinRows = INT64_MAX;  // (pair kernel not yet selected)
+constexpr int64_t kPairMinRows = 256;
 constexpr int kBlockStages = 6;
 
 template <typename Kernel>
