@@ -62,6 +62,16 @@ def _flops_step():
     return sum(6.0 * TOKENS * n * k for _, k, n in LINEARS)
 
 
+def _gemm_alg_bytes():
+    """Mean algorithmic DRAM bytes per GEMM launch of the step: both FP8
+    operands read once, the output written once (FP32 accumulation: read
+    and written)."""
+    tot = 0.0
+    for _, M, N, K, _, out in step_gemms():
+        tot += M * K + N * K + (2 * M * N if out == "bf16" else 8 * M * N)
+    return tot / len(step_gemms())
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -211,11 +221,13 @@ def run_gpu(args):
                    "recipe": "HYBRID delayed, history 16, margin 0, amax max",
                    "l2": "flushed (256 MiB write) before every timed step",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
-        "roofline": {"bound": "tensor", "kernel": "gemm_tensor_kernel (tcgen05 kind::f8f6f4)",
+        "roofline": {"bound": "tensor", "kernel": "gemm_pair_kernel (tcgen05.mma.cta_group::2 kind::f8f6f4)",
                      "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
                      "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
                      "peak_source": f"{peak_kind}: 2 x bf16_tflops_sustained (FP8/BF16 nominal 2x)",
-                     "traffic": None},
+                     "traffic": _gemm_traffic(),
+                     "traffic_unit": "DRAM bytes per GEMM launch (ncu, mean of the step's 15)",
+                     "algorithmic_bytes_per_launch": round(_gemm_alg_bytes())},
         "quantize": {"achieved_gbs": round(quant_gbs, 1), "peak_gbs": hbm_gbs,
                      "frac": round(quant_gbs / hbm_gbs, 4), "peak_source": f"{peak_kind} hbm_gbs"},
         "kernels_ms_per_step": {k: round(v / comp["steps"], 4) for k, v in comp["by_kind"].items()},
@@ -487,6 +499,8 @@ def run_kernel(args):
         v |= torch.randint(0, 2, (r, c), generator=g, device=dev, dtype=torch.int32) << 7
         return v.to(torch.uint8)
 
+    if args.kernel == "gemm_step":
+        return run_gemm_step(F, args, dev, codes, flush)
     if args.kernel in ("gemm", "block_gemm"):
         M, N, K = dims
         A, B = codes(M, K), codes(N, K)
@@ -533,6 +547,65 @@ def run_kernel(args):
                       "iters": args.iters, "l2": "flushed before every launch"}))
 
 
+def step_gemms():
+    """The 15 GEMMs of one layer step: (name, M, N, K, A format, output)."""
+    out = []
+    for name, K, N in LINEARS:
+        out.append((name + ".fwd", TOKENS, N, K, "e4m3", "bf16"))
+        out.append((name + ".dgrad", TOKENS, K, N, "e5m2", "bf16"))
+        out.append((name + ".wgrad", N, K, TOKENS, "e5m2", "f32acc"))
+    return out
+
+
+def run_gemm_step(F, args, dev, codes, flush):
+    """The step's 15 GEMMs with their shapes, formats and output types, each on
+    random codes, run once as warm-up and once timed (in that order), with
+    the operands of one GEMM on the device at a time."""
+    gemms = step_gemms()
+    one = torch.ones(1, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    times = []
+    for rep in range(2):
+        for name, M, N, K, fa, out in gemms:
+            A, B = codes(M, K), codes(N, K)
+            if out == "bf16":
+                D = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            else:
+                D = torch.zeros(M, N, dtype=torch.float32, device=dev)
+            flush.fill_(float(rep))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            F.fp8_gemm(A, F.E5M2 if fa == "e5m2" else F.E4M3, B, F.E4M3, one, one,
+                       out=F.OUT_BF16 if out == "bf16" else F.OUT_F32, D=D,
+                       accumulate=out == "f32acc")
+            b.record(stream)
+            torch.cuda.synchronize()
+            if rep == 1:
+                times.append(a.elapsed_time(b))
+            del A, B, D
+    assert F.fp8_device_status() == 0
+    flops = sum(2.0 * M * N * K for _, M, N, K, _, _ in gemms)
+    print(json.dumps({"kernel": "gemm_step", "gemms": [g[0] for g in gemms],
+                      "ms": [round(t, 4) for t in times], "total_ms": round(sum(times), 4),
+                      "achieved": round(flops / (sum(times) * 1e-3) / 1e12, 1),
+                      "unit": "TFLOP/s"}))
+
+
+def _gemm_traffic():
+    """DRAM bytes per GEMM launch of the step (mean over its 15 GEMMs), as
+    measured by ncu and recorded in profiles/ together with a hash of the
+    GEMM source it was measured on; None if the source has changed since."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "gemm_step_traffic.json")) as f:
+            rec = json.load(f)
+        with open(os.path.join(ROOT, "scaled_fp8_linear_gb300", "csrc", "gemm.cu"), "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()
+        return rec["bytes_per_launch"] if rec.get("gemm_cu_sha256") == h else None
+    except Exception:
+        return None
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -542,7 +615,7 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=32)
     ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["gemm", "block_gemm", "quantize"],
+    ap.add_argument("--kernel", choices=["gemm", "block_gemm", "quantize", "gemm_step"],
                     help="time one kernel on --shape instead of the layer step")
     ap.add_argument("--shape", default="8192,12288,4096")
     ap.add_argument("--fmt", choices=["e4m3", "e5m2"], default="e4m3")

@@ -103,6 +103,9 @@ typedef struct {
     float*   qscale_inv; /* [2] out: dequantisation factors that x_q/x_qt (0)  */
                          /*   and w_q/w_qt (1) were cast with; written by fwd  */
                          /*   (per-tensor modes), read by bwd                  */
+    float*   x_sinv_t;   /* [K][M/128] block mode: scales of x_qt, the 1x128   */
+                         /*   block cast of X^T (blocks run along the tokens)  */
+    float*   w_sinv_t;   /* [K/128][N/128] block mode: scales of w_qt = W_q^T  */
 } fp8_linear_state_t;
 
 /* ---------------------------------------------------------------- calls */
@@ -141,20 +144,29 @@ int fp8_update_scale(const float* amax, float* history, int32_t* pos, int histor
  *   128x128 tile gets its own scale fp8_max/amax_block (margin 0; 1 for an
  *   all-zero or non-finite block; rounded down to a power of two if pow2),
  *   and scale_inv_blocks receives 1/scale as [rows/b][cols/128] (b = 1 or
- *   128) ("Block-wise scaling at 128 granularity").  scale, q_t and amax_out
- *   must be NULL.  cols must be a multiple of 128 (and rows, for 128x128).
+ *   128) ("Block-wise scaling at 128 granularity").  scale and amax_out must
+ *   be NULL.  cols must be a multiple of 128 (and rows, for 128x128).
+ *   q_t (nullable; rows a multiple of 128; with scale_inv_blocks_t) gets, in
+ *   the same pass,
+ *     1x128:   the 1x128 block cast of x^T [cols x rows] -- blocks of 128
+ *              consecutive rows of one column of x -- with scale_inv_blocks_t
+ *              [cols][rows/128] (the operand layout of the wgrad GEMM);
+ *     128x128: the transposed codes (a 128x128 block keeps its scale) with
+ *              the transposed scales scale_inv_blocks_t [cols/128][rows/128].
  * x, q, q_t: 16-byte aligned.  format: FP8_E4M3 or FP8_E5M2. */
 int fp8_quantize(const void* x, int64_t rows, int64_t cols, int format, int granularity,
                  const float* scale, int pow2, uint8_t* q, uint8_t* q_t,
-                 float* scale_inv_blocks, float* amax_out, void* stream);
+                 float* scale_inv_blocks, float* scale_inv_blocks_t, float* amax_out,
+                 void* stream);
 
 /* Scaled FP8 GEMM, layout FP8_LAYOUT_TN:
  *   D[m][n] = sum_k sa(m,k) * sb(n,k) * A[m][k] * B[n][k]
  * with FP32 accumulation on the tensor cores.  sa, sb are DEQUANTISATION
  * factors (scale_inv = 1/scale, device memory):
  *   FP8_GRAN_TENSOR   scale_inv[0]
- *   FP8_GRAN_1x128    scale_inv[row][k/128]            (A only)
+ *   FP8_GRAN_1x128    scale_inv[row][k/128]
  *   FP8_GRAN_128x128  scale_inv[row/128][k/128]
+ * (a row of B is a column n of D: 1x128 scales on B scale D column-wise).
  * Per-tensor factors multiply the FP32 result once; block factors scale each
  * 128-deep partial sum before it is added ("applied during the matmul").
  * out FP8_OUT_BF16: D is bf16 [M x N], rounded to nearest even.
@@ -175,9 +187,13 @@ size_t fp8_workspace_size(int64_t M, int64_t N, int64_t K, const fp8_recipe_t* r
  *            transposes), GEMM, then update the X and W scales (the new
  *            scales take effect on the next call: one-step lag);
  *   dynamic: amax, scale update and quantisation of X and W, then GEMM;
- *   block:   1x128 quantisation of X, 128x128 of W, block-scaled GEMM.
- * Writes state->x_q/x_qt/w_q/w_qt (or x_q/w_q/x_sinv/w_sinv) for the
- * backward pass.  Shape rule: M, N, K multiples of 16 (128 for block). */
+ *   block:   1x128 quantisation of X, 128x128 of W, block-scaled GEMM; with
+ *            state->x_qt and w_qt set (training) the same passes also write
+ *            the 1x128 block cast of X^T (x_qt, x_sinv_t) and W_q^T (w_qt,
+ *            w_sinv_t) for the backward pass, which needs M % 128 == 0.
+ * Writes state->x_q/x_qt/w_q/w_qt (and the block scale arrays) for the
+ * backward pass.  Shape rule: M, N, K multiples of 16 (N, K multiples of 128
+ * for block). */
 int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K,
                    const fp8_recipe_t* recipe, const fp8_linear_state_t* state, void* Y,
                    void* workspace, size_t workspace_bytes, void* stream);
@@ -187,7 +203,13 @@ int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K
  *   accumulate_dW).  dY is cast to the recipe's bwd_format with the dY
  *   role's scale (delayed: current scale, then update; dynamic: its own
  *   amax).  The quantised dY and its transpose live in the workspace.
- * Block scaling has no backward in this build (FP8_ERR_UNSUPPORTED). */
+ * Block scaling ("DeepSeek FP8 training recipe" > "Block-wise scaling at
+ *   128 granularity"): dY is cast once into 1x128 blocks along N (dgrad
+ *   operand) and 1x128 blocks along the tokens of dY^T (wgrad operand);
+ *   dgrad = block GEMM with W_q^T's 128x128 scales; wgrad = block GEMM of
+ *   dY^T and X^T, both with 1x128 scales along the tokens.  Needs the
+ *   forward pass to have kept x_qt/x_sinv_t and w_qt/w_sinv_t, and
+ *   M % 128 == 0.  Workspace: 2*M*N code bytes + 8*M*N/128 scale bytes. */
 int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K,
                    const fp8_recipe_t* recipe, const fp8_linear_state_t* state, void* dX,
                    float* dW, int accumulate_dW, void* workspace, size_t workspace_bytes,

@@ -245,8 +245,15 @@ def _per_tensor_operand(st: LinearState, role: int, x_bits, fmt: int, recipe: Re
 def linear_fwd(X_bits, W_bits, recipe: Recipe, st: LinearState, rows=None):
     """Y = X . W^T.  Returns (Y, Yabs) fp64 (all rows, or the listed rows)."""
     if recipe.scaling == SCALING_BLOCK:
-        st.x_q, st.x_sinv = block_quantize(X_bits, E4M3, 1, recipe.pow2)
+        X = np.ascontiguousarray(X_bits, dtype=np.uint16)
+        st.x_q, st.x_sinv = block_quantize(X, E4M3, 1, recipe.pow2)
         st.w_q, st.w_sinv = block_quantize(W_bits, E4M3, 128, recipe.pow2)
+        if X.shape[0] % 128 == 0:
+            # backward operands: X^T cast in 1x128 blocks along the tokens, and
+            # W_q^T, whose 128x128 blocks keep their scales
+            st.xt_q, st.xt_sinv = block_quantize(np.ascontiguousarray(X.T), E4M3, 1, recipe.pow2)
+            st.wt_q = np.ascontiguousarray(st.w_q.T)
+            st.wt_sinv = np.ascontiguousarray(st.w_sinv.T)
         return _gemm_rows(st.x_q, E4M3, st.w_q, E4M3, st.x_sinv, st.w_sinv, rows,
                           GRAN_1x128, GRAN_128x128)
     st.x_q, st.x_qt, sx = _per_tensor_operand(st, ROLE_X, X_bits, E4M3, recipe)
@@ -259,11 +266,31 @@ def linear_bwd(dY_bits, recipe: Recipe, st: LinearState, dW_prev=None, rows_dx=N
                rows_dw=None):
     """dX = dY . W  and  dW (+)= dY^T . X, E5M2 gradient, FP32 wgrad buffer.
     Returns ((dX, dXabs), (dW, dWabs)); dW includes dW_prev when given."""
-    assert recipe.scaling != SCALING_BLOCK, "block-wise backward is not part of this path"
+    if recipe.scaling == SCALING_BLOCK:
+        return _linear_bwd_block(dY_bits, recipe, st, dW_prev, rows_dx, rows_dw)
     sx, sw = st.sinv_fwd
     dy_q, dy_qt, sdy = _per_tensor_operand(st, ROLE_DY, dY_bits, E5M2, recipe)
     dX = _gemm_rows(dy_q, E5M2, st.w_qt, E4M3, sdy, sw, rows_dx)
     dW, dWabs = _gemm_rows(dy_qt, E5M2, st.x_qt, E4M3, sdy, sx, rows_dw)
+    if dW_prev is not None:
+        prev = np.asarray(dW_prev, np.float64)
+        dW = dW + (prev if rows_dw is None else prev[np.asarray(rows_dw)])
+    return dX, (dW, dWabs)
+
+
+def _linear_bwd_block(dY_bits, recipe: Recipe, st: LinearState, dW_prev, rows_dx, rows_dw):
+    """Block-wise backward ("DeepSeek FP8 training recipe" > "Block-wise
+    scaling at 128 granularity"): dY in 1x128 blocks along N for dgrad (with
+    W^T's 128x128 blocks), dY^T and X^T in 1x128 blocks along the tokens for
+    wgrad; every 128-deep partial sum is scaled by its blocks' factors."""
+    dY = np.ascontiguousarray(dY_bits, dtype=np.uint16)
+    dy_q, dy_s = block_quantize(dY, E5M2, 1, recipe.pow2)
+    dyt_q, dyt_s = block_quantize(np.ascontiguousarray(dY.T), E5M2, 1, recipe.pow2)
+    st.dy_q, st.dy_s, st.dyt_q, st.dyt_s = dy_q, dy_s, dyt_q, dyt_s
+    dX = _gemm_rows(dy_q, E5M2, st.wt_q, E4M3, dy_s, st.wt_sinv, rows_dx, GRAN_1x128,
+                    GRAN_128x128)
+    dW, dWabs = _gemm_rows(dyt_q, E5M2, st.xt_q, E4M3, dyt_s, st.xt_sinv, rows_dw, GRAN_1x128,
+                           GRAN_1x128)
     if dW_prev is not None:
         prev = np.asarray(dW_prev, np.float64)
         dW = dW + (prev if rows_dw is None else prev[np.asarray(rows_dw)])

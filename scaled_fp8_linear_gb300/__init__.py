@@ -24,7 +24,8 @@ __all__ = [
     "GRAN_TENSOR", "GRAN_1x128", "GRAN_128x128", "LAYOUT_TN",
     "SCALING_DELAYED", "SCALING_DYNAMIC", "SCALING_BLOCK",
     "Fp8Error", "Recipe", "LinearStateC", "Fp8Linear", "build", "lib", "library_path",
-    "fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_gemm", "fp8_workspace_size",
+    "fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_quantize_blocks", "fp8_gemm",
+    "fp8_workspace_size",
     "fp8_linear_fwd", "fp8_linear_bwd", "fp8_last_error", "fp8_device_status",
 ]
 
@@ -77,7 +78,8 @@ class LinearStateC(ctypes.Structure):
     """fp8_linear_state_t: device pointers of one layer's scaling state."""
     _fields_ = [("scale", _vp), ("scale_inv", _vp), ("amax", _vp), ("history", _vp),
                 ("pos", _vp), ("x_q", _vp), ("x_qt", _vp), ("w_q", _vp), ("w_qt", _vp),
-                ("x_sinv", _vp), ("w_sinv", _vp), ("qscale_inv", _vp)]
+                ("x_sinv", _vp), ("w_sinv", _vp), ("qscale_inv", _vp), ("x_sinv_t", _vp),
+                ("w_sinv_t", _vp)]
 
 
 _lib = None
@@ -96,7 +98,7 @@ def lib() -> ctypes.CDLL:
     i, i64, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
     L.fp8_amax.argtypes = [_vp, i64, _vp, _vp]
     L.fp8_update_scale.argtypes = [_vp, _vp, _vp, i, i, i, i, i, _vp, _vp, _vp]
-    L.fp8_quantize.argtypes = [_vp, i64, i64, i, i, _vp, i, _vp, _vp, _vp, _vp, _vp]
+    L.fp8_quantize.argtypes = [_vp, i64, i64, i, i, _vp, i, _vp, _vp, _vp, _vp, _vp, _vp]
     L.fp8_gemm.argtypes = [_vp, i, _vp, i, i64, i64, i64, i, i, _vp, i, _vp, _vp, i, i, _vp]
     L.fp8_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(Recipe)]
     L.fp8_workspace_size.restype = sz
@@ -170,9 +172,13 @@ def fp8_update_scale(amax, history, pos, history_len, algo, fmt, margin, pow2, s
 
 def fp8_quantize(x: torch.Tensor, fmt: int, granularity: int = GRAN_TENSOR, scale=None,
                  pow2: bool = False, q=None, q_t=None, transpose: bool = False,
-                 scale_inv_blocks=None, amax_out=None, want_amax: bool = False, stream=None):
+                 scale_inv_blocks=None, amax_out=None, want_amax: bool = False,
+                 scale_inv_blocks_t=None, stream=None):
     """Cast a 2-D bf16 tensor to FP8 codes (uint8).  Returns
-    (q, q_t or None, scale_inv_blocks or None, amax or None)."""
+    (q, q_t or None, scale_inv_blocks or None, amax or None); in block modes
+    with transpose=True the transposed block scales are in
+    `scale_inv_blocks_t` (allocated here if not given) -- see
+    fp8_quantize_blocks for a call that returns them."""
     if x.dim() != 2:
         raise ValueError("x must be 2-D")
     rows, cols = x.shape
@@ -184,14 +190,32 @@ def fp8_quantize(x: torch.Tensor, fmt: int, granularity: int = GRAN_TENSOR, scal
     if granularity != GRAN_TENSOR and scale_inv_blocks is None:
         br = 1 if granularity == GRAN_1x128 else 128
         scale_inv_blocks = torch.empty(rows // br, cols // 128, dtype=torch.float32, device=dev)
+    if granularity != GRAN_TENSOR and q_t is not None and scale_inv_blocks_t is None:
+        shape = (cols, rows // 128) if granularity == GRAN_1x128 else (cols // 128, rows // 128)
+        scale_inv_blocks_t = torch.empty(*shape, dtype=torch.float32, device=dev)
     if want_amax and amax_out is None:
         amax_out = torch.empty(1, dtype=torch.float32, device=dev)
     _check(lib().fp8_quantize(
         _ptr(x, "x", torch.bfloat16), rows, cols, int(fmt), int(granularity),
         _ptr(scale, "scale", torch.float32), int(bool(pow2)), _ptr(q, "q", _U8),
         _ptr(q_t, "q_t", _U8), _ptr(scale_inv_blocks, "scale_inv_blocks", torch.float32),
+        _ptr(scale_inv_blocks_t, "scale_inv_blocks_t", torch.float32),
         _ptr(amax_out, "amax_out", torch.float32), _stream(stream)))
     return q, q_t, scale_inv_blocks, amax_out
+
+
+def fp8_quantize_blocks(x: torch.Tensor, fmt: int, granularity: int, pow2: bool = False,
+                        transpose: bool = False, stream=None):
+    """Block cast; returns (q, scale_inv_blocks, q_t, scale_inv_blocks_t)."""
+    rows, cols = x.shape
+    q_t = torch.empty(cols, rows, dtype=torch.uint8, device=x.device) if transpose else None
+    st = None
+    if transpose:
+        shape = (cols, rows // 128) if granularity == GRAN_1x128 else (cols // 128, rows // 128)
+        st = torch.empty(*shape, dtype=torch.float32, device=x.device)
+    q, q_t, s, _ = fp8_quantize(x, fmt, granularity, pow2=pow2, q_t=q_t, scale_inv_blocks_t=st,
+                                stream=stream)
+    return q, s, q_t, st
 
 
 def fp8_gemm(A: torch.Tensor, fa: int, B: torch.Tensor, fb: int, scale_inv_a, scale_inv_b,
@@ -267,17 +291,22 @@ class Fp8Linear:
         self.x_q = torch.empty(M, K, **u8)
         self.w_q = torch.empty(N, K, **u8)
         block = self.recipe.scaling == SCALING_BLOCK
-        self.x_qt = None if block else torch.empty(K, M, **u8)
-        self.w_qt = None if block else torch.empty(K, N, **u8)
+        # block mode keeps the backward operands only when the token count
+        # allows 1x128 blocks along it
+        keep = not block or M % 128 == 0
+        self.x_qt = torch.empty(K, M, **u8) if keep else None
+        self.w_qt = torch.empty(K, N, **u8) if keep else None
         self.x_sinv = torch.empty(M, K // 128, **f32) if block else None
         self.w_sinv = torch.empty(N // 128, K // 128, **f32) if block else None
+        self.x_sinv_t = torch.empty(K, M // 128, **f32) if block and keep else None
+        self.w_sinv_t = torch.empty(K // 128, N // 128, **f32) if block and keep else None
         ws = fp8_workspace_size(M, N, K, self.recipe)
         self.workspace = torch.empty(max(ws, 16), **u8)
         p = lambda t: None if t is None else t.data_ptr()
         self.c_state = LinearStateC(p(self.scale), p(self.scale_inv), p(self.amax),
                                     p(self.history), p(self.pos), p(self.x_q), p(self.x_qt),
                                     p(self.w_q), p(self.w_qt), p(self.x_sinv), p(self.w_sinv),
-                                    p(self.qscale_inv))
+                                    p(self.qscale_inv), p(self.x_sinv_t), p(self.w_sinv_t))
 
     def forward(self, X: torch.Tensor, W: torch.Tensor, Y=None, stream=None) -> torch.Tensor:
         if Y is None:

@@ -98,8 +98,6 @@ int check_gemm_args(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t 
     if (N % 16 || K % 16) return set_error(FP8_ERR_SHAPE, "fp8_gemm: N and K must be multiples of 16");
     const bool block = ga != FP8_GRAN_TENSOR || gb != FP8_GRAN_TENSOR;
     if (block) {
-        if (gb == FP8_GRAN_1x128)
-            return set_error(FP8_ERR_UNSUPPORTED, "fp8_gemm: 1x128 scales on B are not supported");
         if (K % 128 || N % 128)
             return set_error(FP8_ERR_SHAPE, "fp8_gemm: block scales need N and K multiples of 128");
         if (ga == FP8_GRAN_128x128 && M % 128)
@@ -111,7 +109,8 @@ int check_gemm_args(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t 
 }
 
 int check_quantize_args(const void* x, int64_t rows, int64_t cols, int format, int gran,
-                        const float* scale, uint8_t* q, uint8_t* q_t, float* sinv, float* amax_out) {
+                        const float* scale, uint8_t* q, uint8_t* q_t, float* sinv, float* sinv_t,
+                        float* amax_out) {
     if ((!x || !q) && rows > 0 && cols > 0)
         return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: NULL pointer");
     if (!valid_format(format)) return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: unknown format");
@@ -123,11 +122,13 @@ int check_quantize_args(const void* x, int64_t rows, int64_t cols, int format, i
             return set_error(FP8_ERR_SHAPE, "fp8_quantize: the transpose needs rows and cols multiples of 16");
     } else {
         if (!sinv) return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: scale_inv_blocks is NULL");
-        if (q_t || amax_out || scale)
-            return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: block modes take no scale, q_t or amax_out");
+        if (amax_out || scale)
+            return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: block modes take no scale or amax_out");
+        if (q_t && !sinv_t)
+            return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: q_t needs scale_inv_blocks_t in block modes");
         if (cols % 128) return set_error(FP8_ERR_SHAPE, "fp8_quantize: block modes need cols multiple of 128");
-        if (gran == FP8_GRAN_128x128 && rows % 128)
-            return set_error(FP8_ERR_SHAPE, "fp8_quantize: 128x128 blocks need rows multiple of 128");
+        if ((gran == FP8_GRAN_128x128 || q_t) && rows % 128)
+            return set_error(FP8_ERR_SHAPE, "fp8_quantize: 128x128 blocks and block transposes need rows multiple of 128");
     }
     if (!aligned16(x) || !aligned16(q) || (q_t && !aligned16(q_t)))
         return set_error(FP8_ERR_ALIGN, "fp8_quantize: x, q and q_t must be 16-byte aligned");
@@ -151,6 +152,41 @@ int check_state_scales(const fp8_linear_state_t* s) {
 }
 
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+// Block-wise backward ("DeepSeek FP8 training recipe" > "Block-wise scaling
+// at 128 granularity"): one dual cast of dY gives the dgrad operand (1x128
+// blocks along N) and the wgrad operand (dY^T, 1x128 blocks along the
+// tokens); dgrad uses W_q^T with its 128x128 scales, wgrad X^T's 1x128
+// token-blocked cast kept by the forward pass.
+int linear_bwd_block(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe,
+                     const fp8_linear_state_t* s, void* dX, float* dW, int accumulate_dW,
+                     void* workspace, size_t workspace_bytes, cudaStream_t st) {
+    if (!s->x_qt || !s->w_qt || !s->x_sinv_t || !s->w_sinv_t)
+        return set_error(FP8_ERR_INVALID_ARG,
+                         "fp8_linear_bwd: block mode needs the forward's x_qt/x_sinv_t and w_qt/w_sinv_t");
+    if (M % 128) return set_error(FP8_ERR_SHAPE, "fp8_linear_bwd: block mode needs M multiple of 128");
+    const size_t mn = static_cast<size_t>(M) * static_cast<size_t>(N);
+    const size_t need = 2 * align256(mn) + 2 * align256(4 * (mn / 128));
+    if (workspace_bytes < need)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: workspace of %zu bytes, %zu needed",
+                         workspace_bytes, need);
+    if (!aligned16(dY) || !aligned16(dX) || !aligned16(dW) || !aligned16(workspace) ||
+        !aligned16(s->x_qt) || !aligned16(s->w_qt))
+        return set_error(FP8_ERR_ALIGN, "fp8_linear_bwd: tensors must be 16-byte aligned");
+    const int fb = recipe->bwd_format, ff = recipe->fwd_format;
+    uint8_t* dy_q = static_cast<uint8_t*>(workspace);
+    uint8_t* dy_qt = dy_q + align256(mn);
+    float* dy_s = reinterpret_cast<float*>(dy_qt + align256(mn));
+    float* dy_st = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dy_s) + align256(4 * (mn / 128)));
+    FP8_CHECK(cuda_status(launch_quantize_block(dY, M, N, fb, FP8_GRAN_1x128, recipe->pow2 != 0,
+                                                dy_q, dy_s, dy_qt, dy_st, st), "quantize dY"));
+    // dgrad: dX [M x K] = dY_q [M x N] . (W_q^T [K x N])^T
+    FP8_CHECK(launch_gemm(dy_q, fb, s->w_qt, ff, M, K, N, FP8_GRAN_1x128, dy_s, FP8_GRAN_128x128,
+                          s->w_sinv_t, dX, FP8_OUT_BF16, 0, st));
+    // wgrad: dW [N x K] (+)= dY_q^T [N x M] . (X_q^T [K x M])^T
+    return launch_gemm(dy_qt, fb, s->x_qt, ff, N, K, M, FP8_GRAN_1x128, dy_st, FP8_GRAN_1x128,
+                       s->x_sinv_t, dW, FP8_OUT_F32, accumulate_dW != 0, st);
+}
 
 }  // namespace
 }  // namespace fp8
@@ -187,15 +223,16 @@ int fp8_update_scale(const float* amax, float* history, int32_t* pos, int histor
 
 int fp8_quantize(const void* x, int64_t rows, int64_t cols, int format, int granularity,
                  const float* scale, int pow2, uint8_t* q, uint8_t* q_t, float* scale_inv_blocks,
-                 float* amax_out, void* stream) {
+                 float* scale_inv_blocks_t, float* amax_out, void* stream) {
     FP8_CHECK(check_quantize_args(x, rows, cols, format, granularity, scale, q, q_t,
-                                  scale_inv_blocks, amax_out));
+                                  scale_inv_blocks, scale_inv_blocks_t, amax_out));
     if (granularity == FP8_GRAN_TENSOR)
         return cuda_status(launch_quantize_tensor(x, rows, cols, format, scale, q, q_t, amax_out,
                                                   as_stream(stream)),
                            "fp8_quantize");
     return cuda_status(launch_quantize_block(x, rows, cols, format, granularity, pow2 != 0, q,
-                                             scale_inv_blocks, as_stream(stream)),
+                                             scale_inv_blocks, q_t, scale_inv_blocks_t,
+                                             as_stream(stream)),
                        "fp8_quantize");
 }
 
@@ -211,9 +248,11 @@ int fp8_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int6
 size_t fp8_workspace_size(int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe) {
     (void)K;
     if (check_recipe(recipe) != FP8_OK || M < 0 || N < 0) return 0;
-    if (recipe->scaling == FP8_SCALING_BLOCK) return 0;
-    // backward: dY quantised [M x N] and its transpose [N x M]
-    return 2 * align256(static_cast<size_t>(M) * static_cast<size_t>(N));
+    const size_t mn = static_cast<size_t>(M) * static_cast<size_t>(N);
+    // backward: dY quantised [M x N] and its transposed cast [N x M]
+    if (recipe->scaling != FP8_SCALING_BLOCK) return 2 * align256(mn);
+    // block mode adds their 1x128 scale arrays, [M][N/128] and [N][M/128]
+    return 2 * align256(mn) + 2 * align256(4 * (mn / 128));
 }
 
 int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K,
@@ -234,10 +273,18 @@ int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K
     if (recipe->scaling == FP8_SCALING_BLOCK) {
         if (!s->x_sinv || !s->w_sinv)
             return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_fwd: block mode needs x_sinv and w_sinv");
+        // training (x_qt and w_qt kept): the same casts also write the backward operands
+        const bool keep = s->x_qt && s->w_qt;
+        if (keep && (!s->x_sinv_t || !s->w_sinv_t))
+            return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_fwd: block mode with x_qt/w_qt needs x_sinv_t and w_sinv_t");
+        if (keep && M % 128)
+            return set_error(FP8_ERR_SHAPE, "fp8_linear_fwd: the block-wise backward operands need M multiple of 128");
         FP8_CHECK(cuda_status(launch_quantize_block(X, M, K, f, FP8_GRAN_1x128, recipe->pow2 != 0,
-                                                    s->x_q, s->x_sinv, st), "quantize X"));
+                                                    s->x_q, s->x_sinv, keep ? s->x_qt : nullptr,
+                                                    s->x_sinv_t, st), "quantize X"));
         FP8_CHECK(cuda_status(launch_quantize_block(W, N, K, f, FP8_GRAN_128x128, recipe->pow2 != 0,
-                                                    s->w_q, s->w_sinv, st), "quantize W"));
+                                                    s->w_q, s->w_sinv, keep ? s->w_qt : nullptr,
+                                                    s->w_sinv_t, st), "quantize W"));
         return launch_gemm(s->x_q, f, s->w_q, f, M, N, K, FP8_GRAN_1x128, s->x_sinv,
                            FP8_GRAN_128x128, s->w_sinv, Y, FP8_OUT_BF16, 0, st);
     }
@@ -276,11 +323,12 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
                    const fp8_linear_state_t* s, void* dX, float* dW, int accumulate_dW,
                    void* workspace, size_t workspace_bytes, void* stream) {
     FP8_CHECK(check_recipe(recipe));
-    if (recipe->scaling == FP8_SCALING_BLOCK)
-        return set_error(FP8_ERR_UNSUPPORTED, "fp8_linear_bwd: block-wise backward is not built");
     FP8_CHECK(check_linear_shape(M, N, K, recipe));
     if (!dY || !dX || !dW || !s || !workspace)
         return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: NULL pointer");
+    if (recipe->scaling == FP8_SCALING_BLOCK)
+        return linear_bwd_block(dY, M, N, K, recipe, s, dX, dW, accumulate_dW, workspace,
+                                workspace_bytes, as_stream(stream));
     FP8_CHECK(check_state_scales(s));
     if (!s->x_qt || !s->w_qt)
         return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: the forward pass must keep x_qt and w_qt");

@@ -50,6 +50,7 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 128;      // bytes = FP8 elements of K per stage
 constexpr int UMMA_K = 32;   // K of one kind::f8f6f4 instruction
+constexpr int kBlockGroup = 32;  // raster group of the block-scaled kernel (M-blocks)
 
 struct GemmParams {
     int64_t M, N, K;
@@ -64,10 +65,12 @@ struct GemmParams {
 };
 
 // Grouped rasterisation: walk GROUP consecutive M-blocks down each N-column
-// so that the CTAs resident at one time share A and B panels in L2.
+// so that the CTAs resident at one time share A and B panels in L2.  A
+// larger group re-reads each B panel from DRAM fewer times (once per group)
+// at the cost of more A panels resident at once.
+template <int GROUP = 8>
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk,
                                             int& n_blk) {
-    constexpr int GROUP = 8;
     const int per_group = GROUP * num_n;
     const int g = tile / per_group;
     const int first_m = g * GROUP;
@@ -89,7 +92,7 @@ struct Layout {
 
 // Producer role: stream the A / B tiles of every K block of every tile of
 // this CTA through the ring.  On exit, waits for its own copies in flight.
-template <int BN, int STAGES>
+template <int BN, int STAGES, int GROUP = 8>
 __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t* ring,
                          uint64_t* full, uint64_t* empty, const GemmParams& p,
                          volatile uint32_t* abort_flag) {
@@ -100,7 +103,7 @@ __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         int m_blk, n_blk;
-        tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+        tile_coords<GROUP>(tile, p.num_m, p.num_n, m_blk, n_blk);
         for (int kb = 0; kb < p.num_kb; ++kb) {
             if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
             uint8_t* sa = ring + stage * L::STAGE_BYTES;
@@ -261,7 +264,7 @@ __global__ void __launch_bounds__(256, 1)
         const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             int m_blk, n_blk;
-            tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+            tile_coords<>(tile, p.num_m, p.num_n, m_blk, n_blk);
             if (rmw)
                 prefetch_row(static_cast<int64_t>(m_blk) * BM + row, static_cast<int64_t>(n_blk) * BN,
                              BN, p);
@@ -367,7 +370,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             bool ok = true;
             for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
                 int m_blk, n_blk;
-                tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+                tile_coords<>(tile, p.num_m, p.num_n, m_blk, n_blk);
                 const int ya = m_blk * TILE + static_cast<int>(rank) * HALF;
                 const int yb = n_blk * TILE + static_cast<int>(rank) * HALF;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -436,7 +439,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = pair; tile < num_tiles; tile += npairs) {
             int m_blk, n_blk;
-            tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+            tile_coords<>(tile, p.num_m, p.num_n, m_blk, n_blk);
             const int64_t m = static_cast<int64_t>(m_blk) * TILE + rank * HALF + row;
             if (rmw) prefetch_row(m, static_cast<int64_t>(n_blk) * TILE, TILE, p);
             bool ok = (lane == 0) ? ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag) : false;
@@ -471,6 +474,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 
 // --------------------------------------------------------- block-scaled kernel
 
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+
+// Final store of one promoted accumulator row segment (32 columns, packed
+// pairs): bf16 round-to-nearest-even, or FP32 (added to the buffer if rmw).
+// Block mode has N % 128 == 0, so all 32 columns exist.
+__device__ __forceinline__ void store_block_row(const uint64_t (&acc)[16], int64_t m, int64_t n0,
+                                                const GemmParams& p, bool rmw) {
+    float a[32];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        a[2 * e] = __uint_as_float(static_cast<uint32_t>(acc[e]));
+        a[2 * e + 1] = __uint_as_float(static_cast<uint32_t>(acc[e] >> 32));
+    }
+    if (p.out == FP8_OUT_BF16) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.D) + m * p.N + n0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(a[8 * j + 2 * e], a[8 * j + 2 * e + 1]);
+                w[e] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    } else {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.D) + m * p.N + n0);
+        float4 o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j] = rmw ? dst[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float4 v = make_float4(a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
+            if (rmw) {
+                v.x += o[j].x; v.y += o[j].y; v.z += o[j].z; v.w += o[j].w;
+            }
+            dst[j] = v;
+        }
+    }
+}
+
 // Dequantisation factor of row r (of A or B) for K block kb.
 __device__ __forceinline__ float block_factor(const float* s, int gran, int64_t r, int kb,
                                               int KB) {
@@ -479,11 +525,18 @@ __device__ __forceinline__ float block_factor(const float* s, int gran, int64_t 
     return s[(r >> 7) * KB + kb];
 }
 
-template <int STAGES>
-__global__ void __launch_bounds__(384, 1)
+constexpr int kBlockEpiWarps = 16;   // 4 per TMEM lane quadrant, 32 columns each
+constexpr int kBlockThreads = (4 + kBlockEpiWarps) * 32;
+
+// COLSCALE: B carries 1x128 scales, i.e. one factor per output column and K
+// block; each epilogue warp then stages its 32 columns' factors in shared
+// memory per K block.
+template <int STAGES, bool COLSCALE>
+__global__ void __launch_bounds__(kBlockThreads, 1)
     gemm_block_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
     constexpr int BN = 128;
+    __shared__ __align__(16) float colf[COLSCALE ? kBlockEpiWarps : 1][32];
     constexpr int NBUF = 4;
     using L = Layout<BN, STAGES>;
     constexpr uint32_t TMEM_COLS = NBUF * BN;
@@ -506,7 +559,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         for (int a = 0; a < NBUF; ++a) {
             ptx::mbar_init(&tfull[a], 1);
-            ptx::mbar_init(&tempty[a], 8);
+            ptx::mbar_init(&tempty[a], kBlockEpiWarps);
         }
         ptx::mbar_init(done, 1);
         *abort_flag = 0;
@@ -527,7 +580,7 @@ __global__ void __launch_bounds__(384, 1)
     const int num_tiles = p.num_m * p.num_n;
 
     if (warp == 0) {
-        if (lane == 0) producer<BN, STAGES>(&tmA, &tmB, ring, full, empty, p, abort_flag);
+        if (lane == 0) producer<BN, STAGES, kBlockGroup>(&tmA, &tmB, ring, full, empty, p, abort_flag);
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = ptx::idesc_f8f6f4(p.fa, p.fb, BM, BN);
@@ -535,7 +588,7 @@ __global__ void __launch_bounds__(384, 1)
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!ptx::mbar_wait(&tempty[buf], buf_phase ^ 1u, abort_flag)) { ok = false; break; }
+                    if (!ptx::mbar_wait_spin(&tempty[buf], buf_phase ^ 1u, abort_flag)) { ok = false; break; }
                     if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
                     ptx::tc_fence_after();
                     uint8_t* sa = ring + stage * L::STAGE_BYTES;
@@ -557,92 +610,89 @@ __global__ void __launch_bounds__(384, 1)
             ptx::mbar_wait(done, 0, &never);
         }
     } else if (warp >= 4) {
-        const int qd = warp & 3;
-        const int half = (warp - 4) >> 2;  // which 64 of the 128 columns
+        const int qd = warp & 3;                 // TMEM lane quadrant of this warp
+        const int cg = (warp - 4) >> 2;          // which 32 of the 128 columns
         const int row = qd * 32 + lane;
         const int KB = p.num_kb;
+        const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
         uint32_t buf = 0, buf_phase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
             int m_blk, n_blk;
-            tile_coords(tile, p.num_m, p.num_n, m_blk, n_blk);
+            tile_coords<kBlockGroup>(tile, p.num_m, p.num_n, m_blk, n_blk);
             const int64_t m = static_cast<int64_t>(m_blk) * BM + row;
             const int64_t m_safe = m < p.M ? m : p.M - 1;
             const int64_t n_row = static_cast<int64_t>(n_blk) * BN;  // a row of B in this tile
-            const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
+            const int64_t n0 = n_row + cg * 32;
             if (rmw && m < p.M)
-                ptx::prefetch_l2(static_cast<const float*>(p.D) + m * p.N + n_row + half * 64, 64 * 4);
-            float acc[64];
+                ptx::prefetch_l2(static_cast<const float*>(p.D) + m * p.N + n0, 32 * 4);
+            // FP32 accumulator of 32 columns, as 16 packed pairs for fma.rn.f32x2
+            uint64_t acc[16];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
-            float f_next = __fmul_rn(block_factor(p.sa, p.ga, m_safe, 0, KB),
-                                     block_factor(p.sb, p.gb, n_row, 0, KB));
-            for (int kb = 0; kb < KB; ++kb) {
-                const float f = f_next;
-                if (kb + 1 < KB)
-                    f_next = __fmul_rn(block_factor(p.sa, p.ga, m_safe, kb + 1, KB),
-                                       block_factor(p.sb, p.gb, n_row, kb + 1, KB));
-                ok = (lane == 0) ? ptx::mbar_wait(&tfull[buf], buf_phase, abort_flag) : false;
-                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                if (!ok) break;
-                __syncwarp();
-                ptx::tc_fence_after();
-                const uint32_t tb = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + buf * BN +
-                                    half * 64;
+            for (int j = 0; j < 16; ++j) acc[j] = 0ull;
+            // dequantisation factors, loaded a group of 2 K blocks ahead so that
+            // their L2 latency hides behind the promotion of the current group
+            constexpr int G = 2;
+            float sa_next[G], sb_next[G];
+            // per-column B factors (COLSCALE): lane l holds column n0 + l's
+            const int64_t n_lane = COLSCALE ? n0 + lane : n_row;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t r[32];
-                    ptx::tmem_ld_32x32b_x32(tb + c * 32, r);
-                    ptx::tmem_wait_ld();
+            for (int j = 0; j < G; ++j) {
+                sa_next[j] = j < KB ? block_factor(p.sa, p.ga, m_safe, j, KB) : 0.0f;
+                sb_next[j] = j < KB ? block_factor(p.sb, p.gb, n_lane, j, KB) : 0.0f;
+            }
+            for (int kb0 = 0; ok && kb0 < KB; kb0 += G) {
+                float sa_cur[G], sb_cur[G];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        acc[c * 32 + j] = fmaf(__uint_as_float(r[j]), f, acc[c * 32 + j]);
+                for (int j = 0; j < G; ++j) {
+                    sa_cur[j] = sa_next[j];
+                    sb_cur[j] = sb_next[j];
+                    const int kn = kb0 + G + j;
+                    sa_next[j] = kn < KB ? block_factor(p.sa, p.ga, m_safe, kn, KB) : 0.0f;
+                    sb_next[j] = kn < KB ? block_factor(p.sb, p.gb, n_lane, kn, KB) : 0.0f;
                 }
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
-                if (++buf == NBUF) { buf = 0; buf_phase ^= 1u; }
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    if (kb0 + j >= KB) break;
+                    // COLSCALE: the factor of element (m, n0 + c) is sa(m) * sb(n0 + c);
+                    // the warp's 32 column factors go through shared memory
+                    const float* cf = colf[COLSCALE ? warp - 4 : 0];
+                    uint64_t ff = 0;
+                    if (COLSCALE) {
+                        __syncwarp();
+                        colf[COLSCALE ? warp - 4 : 0][lane] = sb_cur[j];
+                        __syncwarp();
+                    } else {
+                        const float f = __fmul_rn(sa_cur[j], sb_cur[j]);
+                        ff = pack2(f, f);
+                    }
+                    const float sa_j = sa_cur[j];
+                    ok = (lane == 0) ? ptx::mbar_wait_spin(&tfull[buf], buf_phase, abort_flag) : false;
+                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                    if (!ok) break;
+                    __syncwarp();
+                    ptx::tc_fence_after();
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(qd * 32) << 16) +
+                                                buf * BN + cg * 32, r);
+                    ptx::tmem_wait_ld();
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&tempty[buf]);   // buffer read: hand it back
+                    if (++buf == NBUF) { buf = 0; buf_phase ^= 1u; }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const uint64_t fe = COLSCALE ? pack2(__fmul_rn(sa_j, cf[2 * e]),
+                                                             __fmul_rn(sa_j, cf[2 * e + 1]))
+                                                     : ff;
+                        acc[e] = ptx::ffma2(static_cast<uint64_t>(r[2 * e]) |
+                                                (static_cast<uint64_t>(r[2 * e + 1]) << 32),
+                                            fe, acc[e]);
+                    }
+                }
             }
             if (!ok) break;
-            if (m < p.M) {
-                const int64_t n0 = n_row + half * 64;
-                if (p.out == FP8_OUT_BF16) {
-                    __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.D) + m * p.N;
-#pragma unroll
-                    for (int j = 0; j < 64; j += 8) {
-                        if (n0 + j < p.N) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const __nv_bfloat162 h =
-                                    __floats2bfloat162_rn(acc[j + 2 * e], acc[j + 2 * e + 1]);
-                                w[e] = *reinterpret_cast<const uint32_t*>(&h);
-                            }
-                            *reinterpret_cast<uint4*>(drow + n0 + j) =
-                                make_uint4(w[0], w[1], w[2], w[3]);
-                        }
-                    }
-                } else {
-                    // block mode has N % 128 == 0: all 64 columns of this half exist
-                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.D) + m * p.N + n0);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        float4 o[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            o[j] = rmw ? dst[h * 8 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int c = (h * 8 + j) * 4;
-                            float4 v = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
-                            if (rmw) {
-                                v.x += o[j].x; v.y += o[j].y; v.z += o[j].z; v.w += o[j].w;
-                            }
-                            dst[h * 8 + j] = v;
-                        }
-                    }
-                }
-            }
+            if (m < p.M) store_block_row(acc, m, n0, p, rmw);
         }
     }
 
@@ -722,25 +772,26 @@ int ensure_smem(Kernel k, int bytes, int kernel_id) {
 
 // How many 2-CTA clusters of the pair kernel fit on the device at once (the
 // persistent grid size); cached per device.
-int pair_clusters(const void* func) {
+int pair_clusters(const void* func, int kernel_id, int threads, int smem) {
     static std::mutex mu;
-    static int cache[64] = {};
+    static int cache[64][1] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
     std::lock_guard<std::mutex> lock(mu);
-    if (cache[dev] == 0) {
+    int& c = cache[dev][kernel_id];
+    if (c == 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * 1024, 1, 1);
-        cfg.blockDim = dim3(256, 1, 1);
-        cfg.dynamicSmemBytes = kPairSmemBytes;
+        cfg.blockDim = dim3(threads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess || n <= 0) {
             (void)cudaGetLastError();
             n = num_sms() / 2;
         }
-        cache[dev] = n;
+        c = n;
     }
-    return cache[dev];
+    return c;
 }
 
 }  // namespace
@@ -792,7 +843,8 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
     if (pair) {
         auto k = gemm_pair_kernel<kPairStages>;
         if ((st = ensure_smem(k, kPairSmemBytes, 2)) != FP8_OK) return st;
-        const int64_t clusters = pair_clusters(reinterpret_cast<const void*>(k));
+        const int64_t clusters =
+            pair_clusters(reinterpret_cast<const void*>(k), 0, 256, kPairSmemBytes);
         const int pgrid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
         k<<<pgrid, 256, kPairSmemBytes, stream>>>(tmA, tmB, p);
     } else if (!block) {
@@ -802,9 +854,15 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
         k<<<grid, 256, L::SMEM_BYTES, stream>>>(tmA, tmB, p);
     } else {
         using L = Layout<128, kBlockStages>;
-        auto k = gemm_block_kernel<kBlockStages>;
-        if ((st = ensure_smem(k, L::SMEM_BYTES, 1)) != FP8_OK) return st;
-        k<<<grid, 384, L::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        if (gb == FP8_GRAN_1x128) {
+            auto k = gemm_block_kernel<kBlockStages, true>;
+            if ((st = ensure_smem(k, L::SMEM_BYTES, 3)) != FP8_OK) return st;
+            k<<<grid, kBlockThreads, L::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        } else {
+            auto k = gemm_block_kernel<kBlockStages, false>;
+            if ((st = ensure_smem(k, L::SMEM_BYTES, 1)) != FP8_OK) return st;
+            k<<<grid, kBlockThreads, L::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        }
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(FP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));

@@ -30,8 +30,12 @@ cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, in
                                    cudaStream_t stream);
 
 // Block cast: gran 1 (1x128) or 2 (128x128); writes q and 1/scale per block.
+// q_t (nullable, rows % 128 == 0): gran 1 -> the 1x128 block cast of x^T with
+// scale_inv_t [cols][rows/128]; gran 2 -> the transposed codes with the
+// transposed scales scale_inv_t [cols/128][rows/128].
 cudaError_t launch_quantize_block(const void* x, int64_t rows, int64_t cols, int fmt, int gran,
-                                  int pow2, uint8_t* q, float* scale_inv, cudaStream_t stream);
+                                  int pow2, uint8_t* q, float* scale_inv, uint8_t* q_t,
+                                  float* scale_inv_t, cudaStream_t stream);
 
 // Scaled FP8 GEMM, TN layout.  Returns 0 or a negative fp8 status code
 // (tensor-map encoding can fail); launch errors come back as FP8_ERR_CUDA.

@@ -78,6 +78,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     }
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Same contract as mbar_wait, but polls with the non-blocking test_wait: the
+// thread never sleeps, so it sees the phase complete within a few cycles.
+// For short, latency-critical handshakes (one per 128-deep K block).
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity,
+                                               volatile uint32_t* abort_flag) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_test_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_test_wait(a, parity)) return true;
+        if ((it & 1023u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kWaitTimeoutNs) {
+                *abort_flag = 1u;
+                return false;
+            }
+        }
+    }
+}
+
 // ----------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -246,6 +278,14 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask
         " [%0], %1;" ::"r"(smem_u32(bar)),
         "h"(cta_mask)
         : "memory");
+}
+
+// Two IEEE fused multiply-adds on packed pairs: {a.lo*b.lo + c.lo, a.hi*b.hi + c.hi},
+// each rounded to nearest even.
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA

@@ -224,37 +224,15 @@ __global__ void __launch_bounds__(kThreads)
 // 8 banks.  rows and cols are multiples of 16.
 __device__ __forceinline__ int tr_swz(int row) { return ((row >> 2) & 7) << 2; }
 
-template <int FMT, bool AMAX>
-__global__ void __launch_bounds__(kThreads)
-    quantize_transpose_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
-                              int64_t tiles_c, const float* __restrict__ scale_p,
-                              uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
-                              unsigned* amax_bits) {
-    __shared__ __align__(16) uint32_t S[128 * 32];
-    const int64_t tile = blockIdx.x;
-    const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
-    const float s = *scale_p;
+// Phase 2 of the transposing casts: the 128 x 128 tile of codes at (r0, c0),
+// staged in S (rows of 32 words, swizzled by tr_swz), is written transposed
+// to qt [cols x ld] (ld = row length of qt): each thread gathers 4 x 4 byte
+// blocks, transposes them with byte permutes and writes 4 codes to each of 4
+// rows of qt (a warp covers 128 contiguous bytes per row).
+__device__ __forceinline__ void transpose_tile_out(const uint32_t* S, uint8_t* __restrict__ qt,
+                                                   int64_t ld, int64_t r0, int64_t c0,
+                                                   int64_t rows, int64_t cols) {
     const int t = threadIdx.x;
-    uint32_t m = 0;
-
-    const int cg = t & 7;
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int rl = it * 32 + (t >> 3);
-        const int64_t r = r0 + rl, c = c0 + cg * 16;
-        uint4 out = make_uint4(0u, 0u, 0u, 0u);
-        if (r < rows && c < cols) {
-            const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + c);
-            const uint4 a = ldg_stream(src), b = ldg_stream(src + 1);
-            if (AMAX) m = absmax_vec(absmax_vec(m, a), b);
-            out = make_uint4(cvt4<FMT>(a.x, a.y, s), cvt4<FMT>(a.z, a.w, s),
-                             cvt4<FMT>(b.x, b.y, s), cvt4<FMT>(b.z, b.w, s));
-            *reinterpret_cast<uint4*>(q + r * cols + c) = out;
-        }
-        *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = out;
-    }
-    __syncthreads();
-
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         const int b = it * kThreads + t;
@@ -272,9 +250,54 @@ __global__ void __launch_bounds__(kThreads)
         if (r < rows) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                if (c + k < cols) *reinterpret_cast<uint32_t*>(qt + (c + k) * rows + r) = o[k];
+                if (c + k < cols) *reinterpret_cast<uint32_t*>(qt + (c + k) * ld + r) = o[k];
         }
     }
+}
+
+template <int FMT, bool AMAX>
+__global__ void __launch_bounds__(kThreads)
+    quantize_transpose_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
+                              int64_t tiles_c, const float* __restrict__ scale_p,
+                              uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
+                              unsigned* amax_bits) {
+    __shared__ __align__(16) uint32_t S[128 * 32];
+    const int64_t tile = blockIdx.x;
+    const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
+    const float s = *scale_p;
+    const int t = threadIdx.x;
+    uint32_t m = 0;
+
+    const int cg = t & 7;
+    // all of this thread's loads first (8 x 16 B in flight), then cast and store
+    uint4 va[4], vb[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int64_t r = r0 + it * 32 + (t >> 3), c = c0 + cg * 16;
+        va[it] = vb[it] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows && c < cols) {
+            const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + c);
+            va[it] = ldg_stream(src);
+            vb[it] = ldg_stream(src + 1);
+        }
+    }
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int rl = it * 32 + (t >> 3);
+        const int64_t r = r0 + rl, c = c0 + cg * 16;
+        const uint4 a = va[it], b = vb[it];
+        uint4 out = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows && c < cols) {
+            if (AMAX) m = absmax_vec(absmax_vec(m, a), b);
+            out = make_uint4(cvt4<FMT>(a.x, a.y, s), cvt4<FMT>(a.z, a.w, s),
+                             cvt4<FMT>(b.x, b.y, s), cvt4<FMT>(b.z, b.w, s));
+            *reinterpret_cast<uint4*>(q + r * cols + c) = out;
+        }
+        *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = out;
+    }
+    __syncthreads();
+
+    transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
     if (AMAX) cta_amax_commit(m, amax_bits);
 }
 
@@ -314,11 +337,16 @@ __global__ void __launch_bounds__(kThreads)
 
 // 128x128: one CTA per tile; each thread holds 64 elements in registers
 // while the CTA reduces the tile's amax.
+// With qt (nullable): also the transposed codes q_t [C x R] -- the same
+// codes, since a 128 x 128 block keeps its scale under transposition -- and
+// the transposed scale array scale_inv_t [C/128][R/128].
 template <int FMT>
 __global__ void __launch_bounds__(kThreads)
     quantize_128x128_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int pow2,
-                            uint8_t* __restrict__ q, float* __restrict__ scale_inv) {
+                            uint8_t* __restrict__ q, float* __restrict__ scale_inv,
+                            uint8_t* __restrict__ qt, float* __restrict__ scale_inv_t) {
     __shared__ uint32_t warp_max[kThreads / 32];
+    __shared__ __align__(16) uint32_t S[128 * 32];
     const int64_t KB = cols / 128;
     const int64_t br = blockIdx.x / KB, bc = blockIdx.x % KB;
     const int t = threadIdx.x;
@@ -340,11 +368,88 @@ __global__ void __launch_bounds__(kThreads)
     const float s = block_scale<FMT>(__uint_as_float(m << 16), pow2);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int64_t r = br * 128 + i * 16 + (t >> 4), c = bc * 128 + (t & 15) * 8;
-        *reinterpret_cast<uint2*>(q + r * cols + c) =
-            make_uint2(cvt4<FMT>(v[i].x, v[i].y, s), cvt4<FMT>(v[i].z, v[i].w, s));
+        const int rl = i * 16 + (t >> 4);
+        const int64_t r = br * 128 + rl, c = bc * 128 + (t & 15) * 8;
+        const uint2 codes = make_uint2(cvt4<FMT>(v[i].x, v[i].y, s), cvt4<FMT>(v[i].z, v[i].w, s));
+        *reinterpret_cast<uint2*>(q + r * cols + c) = codes;
+        if (qt) *reinterpret_cast<uint2*>(&S[rl * 32 + (((t & 15) * 2) ^ tr_swz(rl))]) = codes;
     }
     if (t == 0) scale_inv[br * KB + bc] = __fdiv_rn(1.0f, s);
+    if (qt) {
+        __syncthreads();
+        transpose_tile_out(S, qt, rows, br * 128, bc * 128, rows, cols);
+        if (t == 0) scale_inv_t[bc * (rows / 128) + br] = __fdiv_rn(1.0f, s);
+    }
+}
+
+// Dual 1x128 cast for the block-wise backward: one read of a 128 x 128 bf16
+// tile gives
+//   q   [R x C]  with one scale per 1x128 row segment   (scale_inv [R][C/128])
+//   q_t [C x R]  with one scale per 1x128 segment of a column of x, i.e. the
+//                1x128 block cast of x^T                  (scale_inv_t [C][R/128]).
+// Phase 1 casts the rows (the 8 threads of a row reduce its amax with
+// shuffles) and stages the bf16 tile in shared memory; phase 2 gives each
+// column to two threads (64 rows each), which reduce the column amax through
+// shared memory and write 64 contiguous codes of q_t each.  R and C are
+// multiples of 128.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads)
+    quantize_1x128_dual_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
+                               int64_t tiles_c, int pow2, uint8_t* __restrict__ q,
+                               float* __restrict__ scale_inv, uint8_t* __restrict__ qt,
+                               float* __restrict__ scale_inv_t) {
+    __shared__ __align__(16) uint16_t T[128 * 128];
+    __shared__ uint32_t colmax[2][128];
+    const int64_t tile = blockIdx.x;
+    const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
+    const int t = threadIdx.x, cg = t & 7;
+    uint4 va[4], vb[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int64_t r = r0 + it * 32 + (t >> 3);
+        const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + c0 + cg * 16);
+        va[it] = ldg_stream(src);
+        vb[it] = ldg_stream(src + 1);
+    }
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int rl = it * 32 + (t >> 3);
+        const uint4 a = va[it], b = vb[it];
+        const uint32_t m2 = absmax_vec(absmax_vec(0u, a), b);
+        uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+        const float sc = block_scale<FMT>(__uint_as_float(m << 16), pow2);
+        const int64_t r = r0 + rl;
+        *reinterpret_cast<uint4*>(q + r * cols + c0 + cg * 16) =
+            make_uint4(cvt4<FMT>(a.x, a.y, sc), cvt4<FMT>(a.z, a.w, sc), cvt4<FMT>(b.x, b.y, sc),
+                       cvt4<FMT>(b.z, b.w, sc));
+        if (cg == 0) scale_inv[r * (cols / 128) + c0 / 128] = __fdiv_rn(1.0f, sc);
+        uint4* dst = reinterpret_cast<uint4*>(&T[rl * 128 + cg * 16]);
+        dst[0] = a;
+        dst[1] = b;
+    }
+    __syncthreads();
+    const int c = t & 127, h = t >> 7;
+    uint32_t m = 0;
+#pragma unroll 8
+    for (int i = 0; i < 64; ++i) m = max(m, static_cast<uint32_t>(T[(h * 64 + i) * 128 + c] & 0x7FFFu));
+    colmax[h][c] = m;
+    __syncthreads();
+    m = max(colmax[0][c], colmax[1][c]);
+    const float sc = block_scale<FMT>(__uint_as_float(m << 16), pow2);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t e0 = T[(h * 64 + 4 * i + 0) * 128 + c], e1 = T[(h * 64 + 4 * i + 1) * 128 + c];
+        const uint32_t e2 = T[(h * 64 + 4 * i + 2) * 128 + c], e3 = T[(h * 64 + 4 * i + 3) * 128 + c];
+        w[i] = cvt4<FMT>(e0 | (e1 << 16), e2 | (e3 << 16), sc);
+    }
+    uint4* out = reinterpret_cast<uint4*>(qt + (c0 + c) * rows + r0 + h * 64);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    if (h == 0) scale_inv_t[(c0 + c) * (rows / 128) + r0 / 128] = __fdiv_rn(1.0f, sc);
 }
 
 int grid_for(int64_t work_items, int per_cta) {
@@ -426,18 +531,26 @@ cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, in
 }
 
 cudaError_t launch_quantize_block(const void* x, int64_t rows, int64_t cols, int fmt, int gran,
-                                  int pow2, uint8_t* q, float* scale_inv, cudaStream_t stream) {
+                                  int pow2, uint8_t* q, float* scale_inv, uint8_t* q_t,
+                                  float* scale_inv_t, cudaStream_t stream) {
     if (rows == 0 || cols == 0) return cudaSuccess;
     const uint16_t* xs = static_cast<const uint16_t*>(x);
-    if (gran == 1) {
+    if (gran == 1 && q_t) {
+        const int64_t tiles_c = cols / 128;
+        const unsigned tiles = static_cast<unsigned>((rows / 128) * tiles_c);
+        if (fmt == 0)
+            quantize_1x128_dual_kernel<0><<<tiles, kThreads, 0, stream>>>(xs, rows, cols, tiles_c, pow2, q, scale_inv, q_t, scale_inv_t);
+        else
+            quantize_1x128_dual_kernel<1><<<tiles, kThreads, 0, stream>>>(xs, rows, cols, tiles_c, pow2, q, scale_inv, q_t, scale_inv_t);
+    } else if (gran == 1) {
         const int64_t pairs = (rows * (cols / 128) + 1) / 2;
         const int grid = grid_for(pairs, kThreads / 32);
         if (fmt == 0) quantize_1x128_kernel<0><<<grid, kThreads, 0, stream>>>(xs, rows, cols, pow2, q, scale_inv);
         else quantize_1x128_kernel<1><<<grid, kThreads, 0, stream>>>(xs, rows, cols, pow2, q, scale_inv);
     } else {
         const unsigned tiles = static_cast<unsigned>((rows / 128) * (cols / 128));
-        if (fmt == 0) quantize_128x128_kernel<0><<<tiles, kThreads, 0, stream>>>(xs, rows, cols, pow2, q, scale_inv);
-        else quantize_128x128_kernel<1><<<tiles, kThreads, 0, stream>>>(xs, rows, cols, pow2, q, scale_inv);
+        if (fmt == 0) quantize_128x128_kernel<0><<<tiles, kThreads, 0, stream>>>(xs, rows, cols, pow2, q, scale_inv, q_t, scale_inv_t);
+        else quantize_128x128_kernel<1><<<tiles, kThreads, 0, stream>>>(xs, rows, cols, pow2, q, scale_inv, q_t, scale_inv_t);
     }
     return cudaGetLastError();
 }

@@ -55,7 +55,6 @@ def test_gemm_argument_checks():
     assert call(N=120) == -2 and call(K=40) == -2  # not multiples of 16
     assert call(M=-1) == -2
     assert call(ga=1, K=144) == -2                 # block scales need K % 128 == 0
-    assert call(ga=1, gb=1) == -6                  # 1x128 on B: not built
     assert call(D=ctypes.c_void_p(FAKE + 4)) == -3
     assert "16-byte" in F.fp8_last_error()
 
@@ -63,14 +62,17 @@ def test_gemm_argument_checks():
 def test_quantize_update_amax_argument_checks():
     L = F.lib()
     p = ctypes.c_void_p(FAKE)
-    assert L.fp8_quantize(None, 4, 4, 0, 0, p, 0, p, None, None, None, None) == -1
-    assert L.fp8_quantize(p, 4, 4, 9, 0, p, 0, p, None, None, None, None) == -1
-    assert L.fp8_quantize(p, 4, 4, 0, 0, None, 0, p, None, None, None, None) == -1  # no scale
-    assert L.fp8_quantize(p, 24, 16, 0, 0, p, 0, p, p, None, None, None) == -2      # transpose rule
-    assert L.fp8_quantize(p, 4, 100, 0, 1, None, 0, p, None, p, None, None) == -2   # cols % 128
-    assert L.fp8_quantize(p, 100, 128, 0, 2, None, 0, p, None, p, None, None) == -2  # rows % 128
-    assert L.fp8_quantize(p, 128, 128, 0, 1, p, 0, p, None, p, None, None) == -1    # scale in block mode
-    assert L.fp8_quantize(ctypes.c_void_p(FAKE + 2), 4, 4, 0, 0, p, 0, p, None, None, None, None) == -3
+    # (x, rows, cols, fmt, gran, scale, pow2, q, q_t, sinv, sinv_t, amax, stream)
+    assert L.fp8_quantize(None, 4, 4, 0, 0, p, 0, p, None, None, None, None, None) == -1
+    assert L.fp8_quantize(p, 4, 4, 9, 0, p, 0, p, None, None, None, None, None) == -1
+    assert L.fp8_quantize(p, 4, 4, 0, 0, None, 0, p, None, None, None, None, None) == -1  # no scale
+    assert L.fp8_quantize(p, 24, 16, 0, 0, p, 0, p, p, None, None, None, None) == -2      # transpose rule
+    assert L.fp8_quantize(p, 4, 100, 0, 1, None, 0, p, None, p, None, None, None) == -2   # cols % 128
+    assert L.fp8_quantize(p, 100, 128, 0, 2, None, 0, p, None, p, None, None, None) == -2  # rows % 128
+    assert L.fp8_quantize(p, 128, 128, 0, 1, p, 0, p, None, p, None, None, None) == -1    # scale in block mode
+    assert L.fp8_quantize(p, 128, 128, 0, 1, None, 0, p, p, p, None, None, None) == -1    # q_t without sinv_t
+    assert L.fp8_quantize(p, 100, 128, 0, 1, None, 0, p, p, p, p, None, None) == -2       # block q_t: rows % 128
+    assert L.fp8_quantize(ctypes.c_void_p(FAKE + 2), 4, 4, 0, 0, p, 0, p, None, None, None, None, None) == -3
     assert L.fp8_update_scale(p, p, p, 0, 0, 0, 0, 0, p, p, None) == -1
     assert L.fp8_update_scale(p, p, p, 16, 0, 0, 65, 0, p, p, None) == -1
     assert L.fp8_update_scale(p, p, p, 16, 2, 0, 0, 0, p, p, None) == -1
@@ -82,7 +84,8 @@ def test_workspace_size_and_recipe_checks():
     r = F.Recipe()
     assert F.fp8_workspace_size(8192, 4096, 4096, r) == 2 * 8192 * 4096
     assert F.fp8_workspace_size(16, 16, 16, r) == 2 * 256
-    assert F.fp8_workspace_size(256, 256, 256, F.Recipe(scaling=F.SCALING_BLOCK)) == 0
+    # block: codes of dY and dY^T plus their 1x128 scale arrays
+    assert F.fp8_workspace_size(256, 256, 256, F.Recipe(scaling=F.SCALING_BLOCK)) == 2 * 65536 + 2 * 2048
     assert F.fp8_workspace_size(16, 16, 16, F.Recipe(history_len=0)) == 0
     assert F.fp8_workspace_size(16, 16, 16, F.Recipe(margin=-1)) == 0
     L = F.lib()
@@ -92,7 +95,9 @@ def test_workspace_size_and_recipe_checks():
     assert L.fp8_linear_fwd(p, p, 16, 16, 16, ctypes.byref(bad), ctypes.byref(st), p, None, 0, None) == -1
     blk = F.Recipe(scaling=F.SCALING_BLOCK)
     assert L.fp8_linear_fwd(p, p, 16, 16, 16, ctypes.byref(blk), ctypes.byref(st), p, None, 0, None) == -2
-    assert L.fp8_linear_bwd(p, 128, 128, 128, ctypes.byref(blk), ctypes.byref(st), p, p, 0, p, 0, None) == -6
+    # block-wise backward without the forward's transposed operands
+    assert L.fp8_linear_bwd(p, 128, 128, 128, ctypes.byref(blk), ctypes.byref(st), p, p, 0, p, 1 << 20, None) == -1
+    assert "x_qt" in F.fp8_last_error()
     r = F.Recipe()
     assert L.fp8_linear_fwd(p, p, 16, 16, 16, ctypes.byref(r), ctypes.byref(st), p, None, 0, None) == -1
 

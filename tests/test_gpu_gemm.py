@@ -116,7 +116,8 @@ def _block_operand(rng, shape, fmt, gran, std=1.0):
 @pytest.mark.parametrize("ga,gb", [(F.GRAN_1x128, F.GRAN_128x128),
                                    (F.GRAN_128x128, F.GRAN_128x128),
                                    (F.GRAN_TENSOR, F.GRAN_128x128),
-                                   (F.GRAN_1x128, F.GRAN_TENSOR)])
+                                   (F.GRAN_1x128, F.GRAN_TENSOR),
+                                   (F.GRAN_1x128, F.GRAN_1x128)])
 def test_block_scaled(M, N, K, ga, gb):
     if ga == F.GRAN_128x128 and M % 128:
         pytest.skip("128x128 scales on A need M % 128 == 0")
@@ -142,3 +143,21 @@ def test_block_scaled_exact():
                    out=F.OUT_F32)
     Do, _ = oracle.gemm(A, F.E4M3, B, F.E4M3, sa, sb, F.GRAN_1x128, F.GRAN_128x128)
     assert np.array_equal(D.cpu().numpy().astype(np.float64), Do)
+
+
+def test_block_scaled_exact_column_scales():
+    """1x128 scales on both operands (the wgrad case): every output column has
+    its own B factor per K block.  Power-of-two factors: exact in FP32."""
+    rng = np.random.default_rng(4)
+    M, N, K = 256, 256, 640
+    ai = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
+    bi = rng.integers(-3, 4, size=(N, K)).astype(np.float32)
+    sa = (2.0 ** rng.integers(-3, 4, size=(M, K // 128))).astype(np.float32)
+    sb = (2.0 ** rng.integers(-3, 4, size=(N, K // 128))).astype(np.float32)
+    A, B = oracle.encode(ai, F.E5M2), oracle.encode(bi, F.E4M3)
+    prev = rng.integers(-8, 8, size=(M, N)).astype(np.float32)
+    D = _t(prev, torch.float32)
+    F.fp8_gemm(_t(A), F.E5M2, _t(B), F.E4M3, _s(sa), _s(sb), F.GRAN_1x128, F.GRAN_1x128,
+               out=F.OUT_F32, D=D, accumulate=True)
+    Do, _ = oracle.gemm(A, F.E5M2, B, F.E4M3, sa, sb, F.GRAN_1x128, F.GRAN_1x128)
+    assert np.array_equal(D.cpu().numpy().astype(np.float64), Do + prev)

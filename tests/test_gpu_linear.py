@@ -94,6 +94,39 @@ def test_block_forward():
     assert_gemm_bound(Y, Yo, Yabs)
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (1024, 768, 1280)])
+def test_block_training_steps(M, N, K):
+    """Block-wise forward + backward over 3 steps, wgrad accumulated: every
+    quantised operand and block scale bit-exact, Y / dX / dW within the
+    bound."""
+    rec = F.Recipe(F.SCALING_BLOCK)
+    layer = F.Fp8Linear(M, N, K, rec, device=DEV)
+    orec = _orecipe(rec)
+    ost = oracle.LinearState(orec)
+    W = synthetic.student_t_rows((N, K), 0.02, 3, seed=77)
+    dW = torch.zeros(N, K, dtype=torch.float32, device=DEV)
+    dW_o = np.zeros((N, K))
+    for step in range(3):
+        X = synthetic.student_t_rows((M, K), 1.0, 3, seed=step)
+        dY = synthetic.normal((M, N), 1e-3 * (1 + step), seed=40 + step)
+        acc = step > 0
+        Y = layer.forward(X.to(DEV), W.to(DEV))
+        dX, _ = layer.backward(dY.to(DEV), dW=dW, accumulate_dW=acc)
+        Yo, Yabs = oracle.linear_fwd(bits(X), bits(W), orec, ost)
+        prev = dW_o.copy()
+        (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(bits(dY), orec, ost,
+                                                       dW_prev=prev if acc else None)
+        assert np.array_equal(u8(layer.x_q), ost.x_q)
+        assert np.array_equal(u8(layer.x_qt), ost.xt_q)
+        assert np.array_equal(f32bits(layer.x_sinv_t.cpu().numpy()), f32bits(ost.xt_sinv))
+        assert np.array_equal(u8(layer.w_qt), ost.wt_q)
+        assert np.array_equal(f32bits(layer.w_sinv_t.cpu().numpy()), f32bits(ost.wt_sinv))
+        assert_gemm_bound(Y, Yo, Yabs, what=f"Y step {step}")
+        assert_gemm_bound(dX, dXo, dXabs, what=f"dX step {step}")
+        assert_gemm_bound(dW, dWo, dWabs, prev=prev if acc else None, what=f"dW step {step}")
+        dW_o = dW.cpu().numpy().astype(np.float64)
+
+
 def test_checkpoint_restore_gives_identical_next_step():
     M, N, K = 128, 256, 256
     rec = F.Recipe(F.SCALING_DELAYED, history_len=16)

@@ -158,3 +158,31 @@ def test_quantizer_sweep_shapes(log2n, width, mag, fmt):
     assert sc.item() == st.scale[0]
     q2, _, _, _ = F.fp8_quantize(xd, fmt, scale=sc)
     assert np.array_equal(u8(q2), oracle.quantize(bx, fmt, st.scale[0])[0])
+
+
+@pytest.mark.parametrize("shape", [(128, 128), (384, 256), (1024, 640)])
+@pytest.mark.parametrize("fmt", [F.E4M3, F.E5M2])
+@pytest.mark.parametrize("pow2", [False, True])
+def test_block_1x128_dual_cast(shape, fmt, pow2):
+    """One pass gives the 1x128 cast of x and the 1x128 cast of x^T (blocks
+    along the columns of x): the wgrad operand layout."""
+    x = synthetic.student_t_rows(shape, 1.0, 3, seed=shape[0] * 3 + shape[1])
+    x[:128, 128:256] = 0                     # all-zero blocks in both directions
+    q, s, qt, st = F.fp8_quantize_blocks(x.to(DEV), fmt, F.GRAN_1x128, pow2=pow2, transpose=True)
+    qo, so = oracle.block_quantize(bits(x), fmt, 1, pow2)
+    qto, sto = oracle.block_quantize(np.ascontiguousarray(bits(x).T), fmt, 1, pow2)
+    assert np.array_equal(u8(q), qo)
+    assert np.array_equal(f32bits(s.cpu().numpy()), f32bits(so))
+    assert np.array_equal(u8(qt), qto)
+    assert np.array_equal(f32bits(st.cpu().numpy()), f32bits(sto))
+
+
+@pytest.mark.parametrize("shape", [(128, 128), (384, 640)])
+@pytest.mark.parametrize("fmt", [F.E4M3, F.E5M2])
+def test_block_128x128_cast_with_transpose(shape, fmt):
+    x = synthetic.student_t_rows(shape, 0.02, 3, seed=shape[0] + 7)
+    q, s, qt, st = F.fp8_quantize_blocks(x.to(DEV), fmt, F.GRAN_128x128, transpose=True)
+    qo, so = oracle.block_quantize(bits(x), fmt, 128)
+    assert np.array_equal(u8(q), qo)
+    assert np.array_equal(u8(qt), qo.T)
+    assert np.array_equal(f32bits(st.cpu().numpy()), f32bits(so.T))

@@ -214,3 +214,36 @@ def test_delayed_linear_uses_previous_step_scale():
     s1 = np.float32(448) / oracle.amax(X0)
     assert np.array_equal(st.x_q, oracle.quantize(X1, E4M3, s1)[0])
     assert st.roles[0].scale[0] == np.float32(448) / max(oracle.amax(X0), oracle.amax(X1))
+
+
+def _dequant_blocks(q, fmt, s, block_rows):
+    """Block-dequantised operand: codes times the scale of their block."""
+    d = oracle.decode(q, fmt)
+    f = np.repeat(np.repeat(np.asarray(s, np.float64), 128, axis=1), block_rows, axis=0)
+    return d * f
+
+
+def test_block_backward_against_dequantised_matmul():
+    # independent route: dequantise every operand block by block, then one
+    # fp64 matmul; sum_kb (sa sb) sum_k a b == sum_k (a sa)(b sb)
+    rng = np.random.default_rng(21)
+    M, N, K = 256, 384, 256
+    rec = oracle.Recipe(scaling=oracle.SCALING_BLOCK)
+    st = oracle.LinearState(rec)
+    X = _bits(rng.standard_normal((M, K)) * np.abs(rng.standard_t(3, (M, 1))))
+    W = _bits(rng.standard_normal((N, K)) * 0.02)
+    dY = _bits(rng.standard_normal((M, N)) * 1e-3)
+    oracle.linear_fwd(X, W, rec, st)
+    (dX, _), (dW, _) = oracle.linear_bwd(dY, rec, st)
+    dy = _dequant_blocks(*oracle.block_quantize(dY, E5M2, 1)[:1], E5M2,
+                         oracle.block_quantize(dY, E5M2, 1)[1], 1)
+    wq, ws = oracle.block_quantize(W, E4M3, 128)
+    w = _dequant_blocks(wq, E4M3, ws, 128)
+    np.testing.assert_allclose(dX, dy @ w, rtol=1e-10, atol=1e-14)
+    # wgrad operands: 1x128 blocks along the tokens, i.e. of dY^T and X^T
+    dytq, dyts = oracle.block_quantize(np.ascontiguousarray(dY.T), E5M2, 1)
+    xtq, xts = oracle.block_quantize(np.ascontiguousarray(X.T), E4M3, 1)
+    np.testing.assert_allclose(dW, _dequant_blocks(dytq, E5M2, dyts, 1)
+                               @ _dequant_blocks(xtq, E4M3, xts, 1).T, rtol=1e-10, atol=1e-14)
+    # the transposed weight operand is the transposed cast
+    assert np.array_equal(st.wt_q, wq.T) and np.array_equal(st.wt_sinv, ws.T)
