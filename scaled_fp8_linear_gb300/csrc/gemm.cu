@@ -757,7 +757,7 @@ constexpr int kBlockStages = 6;
 template <typename Kernel>
 int ensure_smem(Kernel k, int bytes, int kernel_id) {
     static std::mutex mu;
-    static bool done[64][4] = {};
+    static bool done[64][8] = {};   // [device][kernel id]: every GEMM kernel has this one type
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
     std::lock_guard<std::mutex> lock(mu);
@@ -821,6 +821,8 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
                                 : set_error(FP8_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
     }
     const bool block = ga != FP8_GRAN_TENSOR || gb != FP8_GRAN_TENSOR;
+    // CTA pairs for every problem of at least 256 rows, except the block GEMM
+    // with per-column B scales (the wgrad of the block recipe)
     const bool pair = !block && M >= kPairMinRows;
     const int BN = block ? 128 : kTensorBN;
     const int TM = pair ? 256 : BM;   // rows of C per tile
