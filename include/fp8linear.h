@@ -159,6 +159,18 @@ int fp8_quantize(const void* x, int64_t rows, int64_t cols, int format, int gran
                  float* scale_inv_blocks, float* scale_inv_blocks_t, float* amax_out,
                  void* stream);
 
+/* Per-tensor cast (FP8_GRAN_TENSOR semantics of fp8_quantize, same q, q_t
+ * and amax_out) with the dashboard counters of "Numerical-failure taxonomy"
+ * > "A diagnostic dashboard" fused into the same pass:
+ *   counts[0] += inputs x != +-0 whose FP8 code is +-0 (flushed to zero:
+ *                the numerator of the underflow ratio)
+ *   counts[1] += inputs whose scaled value |fp32(x) * scale| exceeds the
+ *                largest finite FP8 value (saturated; +-Inf included, NaN not)
+ * counts: 2 x uint64 in device memory, accumulated (zero it to start a count). */
+int fp8_quantize_counted(const void* x, int64_t rows, int64_t cols, int format,
+                         const float* scale, uint8_t* q, uint8_t* q_t, float* amax_out,
+                         unsigned long long* counts, void* stream);
+
 /* Scaled FP8 GEMM, layout FP8_LAYOUT_TN:
  *   D[m][n] = sum_k sa(m,k) * sb(n,k) * A[m][k] * B[n][k]
  * with FP32 accumulation on the tensor cores.  sa, sb are DEQUANTISATION

@@ -72,6 +72,8 @@ def lib():
                            _f64p, _f64p]
     L.orc_gemm_entries.argtypes = [_u8p, c_int, _u8p, c_int, i64, c_int, _f32p, c_int, _f32p,
                                    _i64p, _i64p, i64, _f64p, _f64p]
+    L.orc_cast_counts.argtypes = [_u16p, i64, c_int, c_float,
+                                  np.ctypeslib.ndpointer(dtype=np.uint64, flags="C_CONTIGUOUS")]
     L.orc_num_threads.restype = c_int
     _lib = L
     return L
@@ -149,6 +151,14 @@ def quantize(x_bits, fmt: int, scale, transpose: bool = False):
     lib().orc_quantize(x, rows, cols, fmt, float(np.float32(scale)), q.ctypes.data,
                        qt.ctypes.data if transpose else None)
     return q, qt
+
+
+def cast_counts(x_bits, fmt: int, scale):
+    """(underflow, saturated) counts of the per-tensor cast with `scale`."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16).reshape(-1)
+    out = np.zeros(2, np.uint64)
+    lib().orc_cast_counts(x, x.size, fmt, float(np.float32(scale)), out)
+    return int(out[0]), int(out[1])
 
 
 def block_quantize(x_bits, fmt: int, block_rows: int, pow2: bool = False):

@@ -236,6 +236,27 @@ void orc_quantize(const uint16_t* x, int64_t rows, int64_t cols, int fmt, float 
     }
 }
 
+/* Dashboard counters of a per-tensor cast ([MP] "Numerical-failure taxonomy"
+ * > "A diagnostic dashboard": underflow ratio, saturation), over the cast of
+ * orc_quantize with the same scale:
+ *   counts[0] = inputs x != +-0 whose FP8 code is +-0     (flushed to zero)
+ *   counts[1] = inputs whose scaled value |fp32(x) * s| is above the largest
+ *               finite FP8 value (so the cast saturates; +-Inf included,
+ *               NaN not) */
+void orc_cast_counts(const uint16_t* x, int64_t n, int fmt, float scale, uint64_t* counts)
+{
+    const float fmax = (float)orc_fp8_max(fmt);
+    uint64_t under = 0, sat = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        const float v = orc_bf16_to_f32(x[i]) * scale;
+        const uint8_t c = orc_encode(v, fmt);
+        if ((x[i] & 0x7FFF) != 0 && (c & 0x7F) == 0) ++under;
+        if (fabsf(v) > fmax) ++sat;
+    }
+    counts[0] = under;
+    counts[1] = sat;
+}
+
 /* [MP] "Block-wise scaling at 128 granularity": one scale per 1x128 segment
  * of a row (activations, gradients) or per 128x128 tile (weights).  Each
  * block's scale comes from its own amax with margin 0 and no history; an

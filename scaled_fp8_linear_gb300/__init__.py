@@ -24,7 +24,8 @@ __all__ = [
     "GRAN_TENSOR", "GRAN_1x128", "GRAN_128x128", "LAYOUT_TN",
     "SCALING_DELAYED", "SCALING_DYNAMIC", "SCALING_BLOCK",
     "Fp8Error", "Recipe", "LinearStateC", "Fp8Linear", "build", "lib", "library_path",
-    "fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_quantize_blocks", "fp8_gemm",
+    "fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_quantize_blocks",
+    "fp8_quantize_counted", "fp8_gemm",
     "fp8_workspace_size",
     "fp8_linear_fwd", "fp8_linear_bwd", "fp8_last_error", "fp8_device_status",
 ]
@@ -99,6 +100,7 @@ def lib() -> ctypes.CDLL:
     L.fp8_amax.argtypes = [_vp, i64, _vp, _vp]
     L.fp8_update_scale.argtypes = [_vp, _vp, _vp, i, i, i, i, i, _vp, _vp, _vp]
     L.fp8_quantize.argtypes = [_vp, i64, i64, i, i, _vp, i, _vp, _vp, _vp, _vp, _vp, _vp]
+    L.fp8_quantize_counted.argtypes = [_vp, i64, i64, i, _vp, _vp, _vp, _vp, _vp, _vp]
     L.fp8_gemm.argtypes = [_vp, i, _vp, i, i64, i64, i64, i, i, _vp, i, _vp, _vp, i, i, _vp]
     L.fp8_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(Recipe)]
     L.fp8_workspace_size.restype = sz
@@ -108,7 +110,8 @@ def lib() -> ctypes.CDLL:
                                  ctypes.POINTER(LinearStateC), _vp, _vp, i, _vp, sz, _vp]
     L.fp8_last_error.restype = ctypes.c_char_p
     L.fp8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i]
-    for name in ("fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_gemm", "fp8_linear_fwd",
+    for name in ("fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_quantize_counted",
+                 "fp8_gemm", "fp8_linear_fwd",
                  "fp8_linear_bwd", "fp8_device_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -202,6 +205,29 @@ def fp8_quantize(x: torch.Tensor, fmt: int, granularity: int = GRAN_TENSOR, scal
         _ptr(scale_inv_blocks_t, "scale_inv_blocks_t", torch.float32),
         _ptr(amax_out, "amax_out", torch.float32), _stream(stream)))
     return q, q_t, scale_inv_blocks, amax_out
+
+
+def fp8_quantize_counted(x: torch.Tensor, fmt: int, scale, counts=None, q=None, q_t=None,
+                         transpose: bool = False, amax_out=None, want_amax: bool = False,
+                         stream=None):
+    """Per-tensor cast with fused dashboard counters.  Returns
+    (q, q_t or None, amax or None, counts) where counts is a 2-element int64
+    device tensor [underflow, saturated] that the call adds to."""
+    rows, cols = x.shape
+    dev = x.device
+    if q is None:
+        q = torch.empty(rows, cols, dtype=torch.uint8, device=dev)
+    if transpose and q_t is None:
+        q_t = torch.empty(cols, rows, dtype=torch.uint8, device=dev)
+    if want_amax and amax_out is None:
+        amax_out = torch.empty(1, dtype=torch.float32, device=dev)
+    if counts is None:
+        counts = torch.zeros(2, dtype=torch.int64, device=dev)
+    _check(lib().fp8_quantize_counted(
+        _ptr(x, "x", torch.bfloat16), rows, cols, int(fmt), _ptr(scale, "scale", torch.float32),
+        _ptr(q, "q", _U8), _ptr(q_t, "q_t", _U8), _ptr(amax_out, "amax_out", torch.float32),
+        _ptr(counts, "counts", torch.int64), _stream(stream)))
+    return q, q_t, amax_out, counts
 
 
 def fp8_quantize_blocks(x: torch.Tensor, fmt: int, granularity: int, pow2: bool = False,

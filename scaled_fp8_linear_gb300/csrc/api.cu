@@ -236,6 +236,19 @@ int fp8_quantize(const void* x, int64_t rows, int64_t cols, int format, int gran
                        "fp8_quantize");
 }
 
+int fp8_quantize_counted(const void* x, int64_t rows, int64_t cols, int format,
+                         const float* scale, uint8_t* q, uint8_t* q_t, float* amax_out,
+                         unsigned long long* counts, void* stream) {
+    FP8_CHECK(check_quantize_args(x, rows, cols, format, FP8_GRAN_TENSOR, scale, q, q_t, nullptr,
+                                  nullptr, amax_out));
+    if (!counts) return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize_counted: counts is NULL");
+    if (reinterpret_cast<uintptr_t>(counts) & 7u)
+        return set_error(FP8_ERR_ALIGN, "fp8_quantize_counted: counts must be 8-byte aligned");
+    return cuda_status(launch_quantize_tensor(x, rows, cols, format, scale, q, q_t, amax_out,
+                                              as_stream(stream), counts),
+                       "fp8_quantize_counted");
+}
+
 int fp8_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N, int64_t K,
              int layout, int ga, const float* scale_inv_a, int gb, const float* scale_inv_b,
              void* D, int out, int accumulate, void* stream) {

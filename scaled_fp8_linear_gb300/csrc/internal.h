@@ -25,9 +25,11 @@ cudaError_t launch_update_scale(const float* amax, float* history, int32_t* pos,
 
 // Per-tensor cast of x [rows x cols]; q_t and amax may be null.  With q_t,
 // rows and cols are multiples of 16.
+// counts (nullable): the cast's dashboard counters [underflow, saturated] are
+// added to counts[0..1].
 cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, int fmt,
                                    const float* scale, uint8_t* q, uint8_t* q_t, float* amax,
-                                   cudaStream_t stream);
+                                   cudaStream_t stream, unsigned long long* counts = nullptr);
 
 // Block cast: gran 1 (1x128) or 2 (128x128); writes q and 1/scale per block.
 // q_t (nullable, rows % 128 == 0): gran 1 -> the 1x128 block cast of x^T with

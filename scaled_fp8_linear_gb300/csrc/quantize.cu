@@ -57,6 +57,57 @@ __device__ __forceinline__ uint32_t cvt4(uint32_t w0, uint32_t w1, float s) {
     return cvt2<FMT>(w0, s) | (cvt2<FMT>(w1, s) << 16);
 }
 
+// Dashboard counters of one cast ("Numerical-failure taxonomy" > "A
+// diagnostic dashboard"): `under` counts nonzero inputs whose code is +-0,
+// `sat` inputs whose scaled value exceeds the largest finite value.
+struct CastCounts {
+    uint32_t under = 0, sat = 0;
+};
+
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt2c(uint32_t w, float s, CastCounts& c) {
+    const float lo = __fmul_rn(__uint_as_float(w << 16), s);
+    const float hi = __fmul_rn(__uint_as_float(w & 0xFFFF0000u), s);
+    const uint32_t pair = static_cast<uint32_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, Fp8Traits<FMT>::kind));
+    c.sat += (fabsf(lo) > Fp8Traits<FMT>::max_finite) + (fabsf(hi) > Fp8Traits<FMT>::max_finite);
+    c.under += ((w & 0x7FFFu) != 0 && (pair & 0x7Fu) == 0) +
+               ((w & 0x7FFF0000u) != 0 && (pair & 0x7F00u) == 0);
+    return pair;
+}
+
+// cvt4 with or without counting.
+template <int FMT, bool COUNT>
+__device__ __forceinline__ uint32_t cvt4x(uint32_t w0, uint32_t w1, float s, CastCounts& c) {
+    if (COUNT) return cvt2c<FMT>(w0, s, c) | (cvt2c<FMT>(w1, s, c) << 16);
+    return cvt4<FMT>(w0, w1, s);
+}
+
+// CTA-wide sum of the counters, added to counts[0..1] with one atomic each.
+__device__ __forceinline__ void cta_counts_commit(const CastCounts& c, unsigned long long* counts) {
+    __shared__ uint32_t part[2][kThreads / 32];
+    const uint32_t u = __reduce_add_sync(0xFFFFFFFFu, c.under);
+    const uint32_t v = __reduce_add_sync(0xFFFFFFFFu, c.sat);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        part[0][warp] = u;
+        part[1][warp] = v;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = static_cast<int>(blockDim.x >> 5);
+        unsigned long long a = lane < nw ? part[0][lane] : 0u, b = lane < nw ? part[1][lane] : 0u;
+        for (int o = 16; o > 0; o >>= 1) {
+            a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+            b += __shfl_xor_sync(0xFFFFFFFFu, b, o);
+        }
+        if (lane == 0) {
+            if (a) atomicAdd(&counts[0], a);
+            if (b) atomicAdd(&counts[1], b);
+        }
+    }
+}
+
 // Running per-halfword max of |bf16| bit patterns.
 __device__ __forceinline__ uint32_t absmax2(uint32_t m, uint32_t w) {
     return __vmaxu2(m, w & 0x7FFF7FFFu);
@@ -181,36 +232,39 @@ __global__ void update_scale_kernel(const float* __restrict__ amax, float* __res
 // ------------------------------------------------------- per-tensor cast
 
 // Flat cast, 16 elements (32 B in, 16 B out) per thread per step.
-template <int FMT, bool AMAX>
+template <int FMT, bool AMAX, bool COUNT>
 __global__ void __launch_bounds__(kThreads)
     quantize_flat_kernel(const uint4* __restrict__ x, int64_t n16, const uint16_t* __restrict__ xt,
                          int tail_n, const float* __restrict__ scale_p, uint4* __restrict__ q,
-                         uint8_t* __restrict__ qtail, unsigned* amax_bits) {
+                         uint8_t* __restrict__ qtail, unsigned* amax_bits,
+                         unsigned long long* counts) {
     const float s = *scale_p;
     uint32_t m = 0;
+    CastCounts cc;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     for (; i + stride < n16; i += 2 * stride) {
         const uint4 a0 = ldg_stream(x + 2 * i), b0 = ldg_stream(x + 2 * i + 1);
         const uint4 a1 = ldg_stream(x + 2 * (i + stride)), b1 = ldg_stream(x + 2 * (i + stride) + 1);
         if (AMAX) m = absmax_vec(absmax_vec(absmax_vec(absmax_vec(m, a0), b0), a1), b1);
-        q[i] = make_uint4(cvt4<FMT>(a0.x, a0.y, s), cvt4<FMT>(a0.z, a0.w, s),
-                          cvt4<FMT>(b0.x, b0.y, s), cvt4<FMT>(b0.z, b0.w, s));
-        q[i + stride] = make_uint4(cvt4<FMT>(a1.x, a1.y, s), cvt4<FMT>(a1.z, a1.w, s),
-                                   cvt4<FMT>(b1.x, b1.y, s), cvt4<FMT>(b1.z, b1.w, s));
+        q[i] = make_uint4(cvt4x<FMT, COUNT>(a0.x, a0.y, s, cc), cvt4x<FMT, COUNT>(a0.z, a0.w, s, cc),
+                          cvt4x<FMT, COUNT>(b0.x, b0.y, s, cc), cvt4x<FMT, COUNT>(b0.z, b0.w, s, cc));
+        q[i + stride] = make_uint4(cvt4x<FMT, COUNT>(a1.x, a1.y, s, cc), cvt4x<FMT, COUNT>(a1.z, a1.w, s, cc),
+                                   cvt4x<FMT, COUNT>(b1.x, b1.y, s, cc), cvt4x<FMT, COUNT>(b1.z, b1.w, s, cc));
     }
     for (; i < n16; i += stride) {
         const uint4 a = ldg_stream(x + 2 * i), b = ldg_stream(x + 2 * i + 1);
         if (AMAX) m = absmax_vec(absmax_vec(m, a), b);
-        q[i] = make_uint4(cvt4<FMT>(a.x, a.y, s), cvt4<FMT>(a.z, a.w, s), cvt4<FMT>(b.x, b.y, s),
-                          cvt4<FMT>(b.z, b.w, s));
+        q[i] = make_uint4(cvt4x<FMT, COUNT>(a.x, a.y, s, cc), cvt4x<FMT, COUNT>(a.z, a.w, s, cc), cvt4x<FMT, COUNT>(b.x, b.y, s, cc),
+                          cvt4x<FMT, COUNT>(b.z, b.w, s, cc));
     }
     if (blockIdx.x == 0 && threadIdx.x < tail_n) {
         const uint32_t w = xt[threadIdx.x];
         if (AMAX) m = max(m, w & 0x7FFFu);
-        qtail[threadIdx.x] = static_cast<uint8_t>(cvt2<FMT>(w, s) & 0xFFu);
+        qtail[threadIdx.x] = static_cast<uint8_t>((COUNT ? cvt2c<FMT>(w & 0xFFFFu, s, cc) : cvt2<FMT>(w, s)) & 0xFFu);
     }
     if (AMAX) cta_amax_commit(m, amax_bits);
+    if (COUNT) cta_counts_commit(cc, counts);
 }
 
 // Cast with fused transpose.  One CTA per 128 x 128 tile:
@@ -255,12 +309,13 @@ __device__ __forceinline__ void transpose_tile_out(const uint32_t* S, uint8_t* _
     }
 }
 
-template <int FMT, bool AMAX>
+template <int FMT, bool AMAX, bool COUNT>
 __global__ void __launch_bounds__(kThreads)
     quantize_transpose_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
                               int64_t tiles_c, const float* __restrict__ scale_p,
                               uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
-                              unsigned* amax_bits) {
+                              unsigned* amax_bits, unsigned long long* counts) {
+    CastCounts cc;
     __shared__ __align__(16) uint32_t S[128 * 32];
     const int64_t tile = blockIdx.x;
     const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
@@ -289,8 +344,8 @@ __global__ void __launch_bounds__(kThreads)
         uint4 out = make_uint4(0u, 0u, 0u, 0u);
         if (r < rows && c < cols) {
             if (AMAX) m = absmax_vec(absmax_vec(m, a), b);
-            out = make_uint4(cvt4<FMT>(a.x, a.y, s), cvt4<FMT>(a.z, a.w, s),
-                             cvt4<FMT>(b.x, b.y, s), cvt4<FMT>(b.z, b.w, s));
+            out = make_uint4(cvt4x<FMT, COUNT>(a.x, a.y, s, cc), cvt4x<FMT, COUNT>(a.z, a.w, s, cc),
+                             cvt4x<FMT, COUNT>(b.x, b.y, s, cc), cvt4x<FMT, COUNT>(b.z, b.w, s, cc));
             *reinterpret_cast<uint4*>(q + r * cols + c) = out;
         }
         *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = out;
@@ -299,6 +354,7 @@ __global__ void __launch_bounds__(kThreads)
 
     transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
     if (AMAX) cta_amax_commit(m, amax_bits);
+    if (COUNT) cta_counts_commit(cc, counts);
 }
 
 // ----------------------------------------------------------- block casts
@@ -480,29 +536,42 @@ cudaError_t launch_update_scale(const float* amax, float* history, int32_t* pos,
     return cudaGetLastError();
 }
 
-template <int FMT, bool AMAX>
+template <int FMT, bool AMAX, bool COUNT>
 static void launch_flat(const void* x, int64_t n, const float* scale, uint8_t* q, float* amax,
-                        cudaStream_t stream) {
+                        unsigned long long* counts, cudaStream_t stream) {
     const int64_t n16 = n / 16;
     const int tail_n = static_cast<int>(n - n16 * 16);
-    quantize_flat_kernel<FMT, AMAX><<<grid_for(n16 + 1, kThreads * 2), kThreads, 0, stream>>>(
+    quantize_flat_kernel<FMT, AMAX, COUNT><<<grid_for(n16 + 1, kThreads * 2), kThreads, 0, stream>>>(
         static_cast<const uint4*>(x), n16, static_cast<const uint16_t*>(x) + n16 * 16, tail_n,
-        scale, reinterpret_cast<uint4*>(q), q + n16 * 16, reinterpret_cast<unsigned*>(amax));
+        scale, reinterpret_cast<uint4*>(q), q + n16 * 16, reinterpret_cast<unsigned*>(amax), counts);
+}
+
+template <int FMT, bool AMAX, bool COUNT>
+static void launch_transpose(const void* x, int64_t rows, int64_t cols, const float* scale,
+                             uint8_t* q, uint8_t* qt, float* amax, unsigned long long* counts,
+                             cudaStream_t stream) {
+    const int64_t tiles_c = (cols + 127) / 128, tiles_r = (rows + 127) / 128;
+    quantize_transpose_kernel<FMT, AMAX, COUNT><<<static_cast<unsigned>(tiles_r * tiles_c), kThreads,
+                                                  0, stream>>>(
+        static_cast<const uint16_t*>(x), rows, cols, tiles_c, scale, q, qt,
+        reinterpret_cast<unsigned*>(amax), counts);
 }
 
 template <int FMT, bool AMAX>
-static void launch_transpose(const void* x, int64_t rows, int64_t cols, const float* scale,
-                             uint8_t* q, uint8_t* qt, float* amax, cudaStream_t stream) {
-    const int64_t tiles_c = (cols + 127) / 128, tiles_r = (rows + 127) / 128;
-    quantize_transpose_kernel<FMT, AMAX><<<static_cast<unsigned>(tiles_r * tiles_c), kThreads, 0,
-                                           stream>>>(static_cast<const uint16_t*>(x), rows, cols,
-                                                     tiles_c, scale, q, qt,
-                                                     reinterpret_cast<unsigned*>(amax));
+static void launch_cast(const void* x, int64_t rows, int64_t cols, const float* scale, uint8_t* q,
+                        uint8_t* q_t, float* amax, unsigned long long* counts, cudaStream_t stream) {
+    if (q_t) {
+        if (counts) launch_transpose<FMT, AMAX, true>(x, rows, cols, scale, q, q_t, amax, counts, stream);
+        else launch_transpose<FMT, AMAX, false>(x, rows, cols, scale, q, q_t, amax, counts, stream);
+    } else {
+        if (counts) launch_flat<FMT, AMAX, true>(x, rows * cols, scale, q, amax, counts, stream);
+        else launch_flat<FMT, AMAX, false>(x, rows * cols, scale, q, amax, counts, stream);
+    }
 }
 
 cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, int fmt,
                                    const float* scale, uint8_t* q, uint8_t* q_t, float* amax,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, unsigned long long* counts) {
     const int64_t n = rows * cols;
     if (amax) {
         cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), stream);
@@ -510,22 +579,12 @@ cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, in
     }
     if (n == 0) return cudaSuccess;
     const bool A = amax != nullptr;
-    if (q_t) {
-        if (fmt == 0) {
-            if (A) launch_transpose<0, true>(x, rows, cols, scale, q, q_t, amax, stream);
-            else launch_transpose<0, false>(x, rows, cols, scale, q, q_t, amax, stream);
-        } else {
-            if (A) launch_transpose<1, true>(x, rows, cols, scale, q, q_t, amax, stream);
-            else launch_transpose<1, false>(x, rows, cols, scale, q, q_t, amax, stream);
-        }
+    if (fmt == 0) {
+        if (A) launch_cast<0, true>(x, rows, cols, scale, q, q_t, amax, counts, stream);
+        else launch_cast<0, false>(x, rows, cols, scale, q, q_t, amax, counts, stream);
     } else {
-        if (fmt == 0) {
-            if (A) launch_flat<0, true>(x, n, scale, q, amax, stream);
-            else launch_flat<0, false>(x, n, scale, q, amax, stream);
-        } else {
-            if (A) launch_flat<1, true>(x, n, scale, q, amax, stream);
-            else launch_flat<1, false>(x, n, scale, q, amax, stream);
-        }
+        if (A) launch_cast<1, true>(x, rows, cols, scale, q, q_t, amax, counts, stream);
+        else launch_cast<1, false>(x, rows, cols, scale, q, q_t, amax, counts, stream);
     }
     return cudaGetLastError();
 }

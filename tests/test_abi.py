@@ -107,3 +107,12 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(4, 4, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         F.fp8_amax(x)
+
+
+def test_quantize_counted_argument_checks():
+    L = F.lib()
+    p = ctypes.c_void_p(FAKE)
+    # (x, rows, cols, fmt, scale, q, q_t, amax, counts, stream)
+    assert L.fp8_quantize_counted(p, 4, 4, 0, p, p, None, None, None, None) == -1     # no counts
+    assert L.fp8_quantize_counted(p, 4, 4, 0, None, p, None, None, p, None) == -1     # no scale
+    assert L.fp8_quantize_counted(p, 4, 4, 0, p, p, None, None, ctypes.c_void_p(FAKE + 4), None) == -3

@@ -186,3 +186,29 @@ def test_block_128x128_cast_with_transpose(shape, fmt):
     assert np.array_equal(u8(q), qo)
     assert np.array_equal(u8(qt), qo.T)
     assert np.array_equal(f32bits(st.cpu().numpy()), f32bits(so.T))
+
+
+@pytest.mark.parametrize("fmt", [F.E4M3, F.E5M2])
+@pytest.mark.parametrize("scale", [1.0, 3.0, 1e-3, 2.0 ** 20])
+@pytest.mark.parametrize("transpose", [False, True])
+def test_cast_counters_every_bf16_pattern(fmt, scale, transpose):
+    x = _all_bf16_patterns()
+    s = torch.tensor([scale], dtype=torch.float32, device=DEV)
+    q, qt, am, counts = F.fp8_quantize_counted(x.to(DEV), fmt, s, transpose=transpose,
+                                               want_amax=True)
+    qo, _ = oracle.quantize(bits(x), fmt, np.float32(scale))
+    assert np.array_equal(u8(q), qo)
+    assert tuple(counts.cpu().tolist()) == oracle.cast_counts(bits(x), fmt, scale)
+    # the counters accumulate across calls
+    F.fp8_quantize_counted(x.to(DEV), fmt, s, counts=counts)
+    assert tuple(counts.cpu().tolist()) == tuple(2 * c for c in oracle.cast_counts(bits(x), fmt, scale))
+
+
+@pytest.mark.parametrize("shape,mag", [((4096, 4096), 1e2), ((4096, 4096), 1e-2), ((37, 61), 30.0)])
+def test_cast_counters_sweep_shapes(shape, mag):
+    """Stale scale 1 on heavy-tailed data: x1e2 saturates, x1e-2 underflows."""
+    x = synthetic.student_t(shape, 3, mag, seed=shape[0] + int(mag))
+    one = torch.ones(1, dtype=torch.float32, device=DEV)
+    tr = shape[0] % 16 == 0 and shape[1] % 16 == 0
+    _, _, _, counts = F.fp8_quantize_counted(x.to(DEV), F.E4M3, one, transpose=tr)
+    assert tuple(counts.cpu().tolist()) == oracle.cast_counts(bits(x), F.E4M3, 1.0)

@@ -143,3 +143,33 @@ def test_bf16_amax_matches_numpy():
     assert oracle.amax(np.array([0x8000, 0x0000], np.uint16)) == 0.0   # -0, +0
     assert oracle.amax(np.array([0xFF80, 0x3F80], np.uint16)) == np.inf   # -inf
     assert math.isnan(oracle.amax(np.array([0x3F80, 0x7FC1, 0xFF80], np.uint16)))
+
+
+def test_cast_counts_golden_cases():
+    # hand-picked values around the E4M3 edges with scale 1:
+    #   448 (max, not saturated), 464 and 1e30 and -inf (saturated), nan (neither),
+    #   2^-10 (tie -> 0: flushed), 3*2^-11 (above the tie: 2^-9, kept), 0 and -0 (not counted)
+    vals = np.array([448.0, 464.0, 1e30, -np.inf, np.nan, 2.0 ** -10, 3 * 2.0 ** -11, 0.0, -0.0,
+                     -2.0 ** -12], np.float32)
+    bits = (vals.view(np.uint32) >> 16).astype(np.uint16)
+    assert oracle.cast_counts(bits, E4M3, 1.0) == (2, 3)
+    # E5M2: 57344 max; 2^-17 is the tie to zero
+    vals = np.array([57344.0, 61440.0, 2.0 ** -17, 2.0 ** -16, 1.0], np.float32)
+    bits = (vals.view(np.uint32) >> 16).astype(np.uint16)
+    assert oracle.cast_counts(bits, E5M2, 1.0) == (1, 1)
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2])
+def test_cast_counts_match_direct_definition(fmt):
+    # every bf16 pattern, several scales: count straight from numpy and torch
+    bits = np.arange(65536, dtype=np.uint16)
+    for scale in (1.0, 3.0, 1e-3, 2.0 ** 20):
+        with np.errstate(invalid="ignore", over="ignore"):
+            v = oracle.bf16_to_f32(bits) * np.float32(scale)
+        sat = int(np.sum(np.abs(v) > oracle.fp8_max(fmt)))
+        # flushed: finite nonzero input whose product rounds to a zero code (torch's RNE cast)
+        t = torch.from_numpy(np.where(np.isfinite(v) & (np.abs(v) <= oracle.fp8_max(fmt)), v, 0)
+                             .astype(np.float32)).to(TORCH_FMT[fmt]).view(torch.uint8).numpy()
+        nz = (bits & 0x7FFF) != 0
+        under = int(np.sum(nz & np.isfinite(v) & (np.abs(v) <= oracle.fp8_max(fmt)) & ((t & 0x7F) == 0)))
+        assert oracle.cast_counts(bits, fmt, scale) == (under, sat)
