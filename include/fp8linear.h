@@ -58,7 +58,8 @@ typedef enum { FP8_AMAX_MAX = 0, FP8_AMAX_MOST_RECENT = 1 } fp8_amax_algo_t;
 typedef enum {
     FP8_GRAN_TENSOR = 0,     /* one scale for the tensor                    */
     FP8_GRAN_1x128 = 1,      /* one scale per 128 consecutive row elements  */
-    FP8_GRAN_128x128 = 2     /* one scale per 128 x 128 tile                */
+    FP8_GRAN_128x128 = 2,    /* one scale per 128 x 128 tile                */
+    FP8_GRAN_ROW = 3         /* one scale per row (per channel / token)     */
 } fp8_gran_t;
 typedef enum {
     FP8_LAYOUT_TN = 0        /* A [M x K] and B [N x K], both K-contiguous   */
@@ -66,7 +67,9 @@ typedef enum {
 typedef enum {
     FP8_SCALING_DELAYED = 0, /* per-tensor, scale from the amax history      */
     FP8_SCALING_DYNAMIC = 1, /* per-tensor, scale from the tensor's own amax */
-    FP8_SCALING_BLOCK = 2    /* 1x128 activations, 128x128 weights           */
+    FP8_SCALING_BLOCK = 2,   /* 1x128 activations, 128x128 weights           */
+    FP8_SCALING_ROW = 3      /* per-token X, per-output-channel W, per-token */
+                             /* dY (dynamic), re-cast per column for bwd     */
 } fp8_scaling_t;
 
 /* Recipe of one linear layer ("Calibration deep dive" > "Dynamic
@@ -153,6 +156,11 @@ int fp8_update_scale(const float* amax, float* history, int32_t* pos, int histor
  *              [cols][rows/128] (the operand layout of the wgrad GEMM);
  *     128x128: the transposed codes (a 128x128 block keeps its scale) with
  *              the transposed scales scale_inv_blocks_t [cols/128][rows/128].
+ * granularity FP8_GRAN_ROW ("Transformer Engine internals" > "Per-row vs
+ *   per-tensor scaling"): one scale per row, fp8_max / amax_row by the block
+ *   rule; scale_inv_blocks [rows].  q_t (with scale_inv_blocks_t, rows a
+ *   multiple of 16) gets the per-row cast of x^T -- one scale per column of x
+ *   -- with scale_inv_blocks_t [cols].  cols must be a multiple of 16.
  * x, q, q_t: 16-byte aligned.  format: FP8_E4M3 or FP8_E5M2. */
 int fp8_quantize(const void* x, int64_t rows, int64_t cols, int format, int granularity,
                  const float* scale, int pow2, uint8_t* q, uint8_t* q_t,
@@ -178,7 +186,11 @@ int fp8_quantize_counted(const void* x, int64_t rows, int64_t cols, int format,
  *   FP8_GRAN_TENSOR   scale_inv[0]
  *   FP8_GRAN_1x128    scale_inv[row][k/128]
  *   FP8_GRAN_128x128  scale_inv[row/128][k/128]
- * (a row of B is a column n of D: 1x128 scales on B scale D column-wise).
+ *   FP8_GRAN_ROW      scale_inv[row]
+ * (a row of B is a column n of D: 1x128 or per-row scales on B scale D
+ * column-wise).  Per-row factors are applied like per-tensor ones, in the
+ * epilogue: D[m][n] = fp32(sa[m] * sb[n]) * acc[m][n]; they cannot be mixed
+ * with block scales (FP8_ERR_UNSUPPORTED).
  * Per-tensor factors multiply the FP32 result once; block factors scale each
  * 128-deep partial sum before it is added ("applied during the matmul").
  * out FP8_OUT_BF16: D is bf16 [M x N], rounded to nearest even.
@@ -199,6 +211,11 @@ size_t fp8_workspace_size(int64_t M, int64_t N, int64_t K, const fp8_recipe_t* r
  *            transposes), GEMM, then update the X and W scales (the new
  *            scales take effect on the next call: one-step lag);
  *   dynamic: amax, scale update and quantisation of X and W, then GEMM;
+ *   row:     per-token scales for X and per-output-channel scales for W (the
+ *            state's x_sinv [M], w_sinv [N]), GEMM with vector factors; with
+ *            x_qt and w_qt set, also the per-row casts of X^T and W^T (one
+ *            scale per column of X and W: x_sinv_t [K], w_sinv_t [K]), which
+ *            the backward's reductions need;
  *   block:   1x128 quantisation of X, 128x128 of W, block-scaled GEMM; with
  *            state->x_qt and w_qt set (training) the same passes also write
  *            the 1x128 block cast of X^T (x_qt, x_sinv_t) and W_q^T (w_qt,
@@ -221,7 +238,10 @@ int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K
  *   dgrad = block GEMM with W_q^T's 128x128 scales; wgrad = block GEMM of
  *   dY^T and X^T, both with 1x128 scales along the tokens.  Needs the
  *   forward pass to have kept x_qt/x_sinv_t and w_qt/w_sinv_t, and
- *   M % 128 == 0.  Workspace: 2*M*N code bytes + 8*M*N/128 scale bytes. */
+ *   M % 128 == 0.  Workspace: 2*M*N code bytes + 8*M*N/128 scale bytes.
+ * Per-row scaling: dY is cast per token (dgrad, with W^T's per-input-channel
+ *   cast) and per output channel (dY^T, wgrad, with X^T's per-input-channel
+ *   cast); workspace 2*M*N code bytes + 4*(M+N) scale bytes. */
 int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K,
                    const fp8_recipe_t* recipe, const fp8_linear_state_t* state, void* dX,
                    float* dW, int accumulate_dW, void* workspace, size_t workspace_bytes,

@@ -34,7 +34,7 @@ from . import build as _build
 
 E4M3, E5M2 = 0, 1
 ALGO_MAX, ALGO_MOST_RECENT = 0, 1
-GRAN_TENSOR, GRAN_1x128, GRAN_128x128 = 0, 1, 2
+GRAN_TENSOR, GRAN_1x128, GRAN_128x128, GRAN_ROW = 0, 1, 2, 3
 ROLE_X, ROLE_W, ROLE_DY = 0, 1, 2
 
 _lib = None
@@ -68,6 +68,7 @@ def lib():
                                    _f32p, _f32p]
     L.orc_quantize.argtypes = [_u16p, i64, i64, c_int, c_float, ctypes.c_void_p, ctypes.c_void_p]
     L.orc_block_quantize.argtypes = [_u16p, i64, i64, c_int, c_int, c_int, _u8p, _f32p]
+    L.orc_row_quantize.argtypes = [_u16p, i64, i64, c_int, c_int, _u8p, _f32p]
     L.orc_gemm.argtypes = [_u8p, c_int, _u8p, c_int, i64, i64, i64, c_int, _f32p, c_int, _f32p,
                            _f64p, _f64p]
     L.orc_gemm_entries.argtypes = [_u8p, c_int, _u8p, c_int, i64, c_int, _f32p, c_int, _f32p,
@@ -153,6 +154,16 @@ def quantize(x_bits, fmt: int, scale, transpose: bool = False):
     return q, qt
 
 
+def row_quantize(x_bits, fmt: int, pow2: bool = False):
+    """Per-row cast; returns (q, scale_inv[rows])."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), np.uint8)
+    sinv = np.empty(rows, np.float32)
+    lib().orc_row_quantize(x, rows, cols, fmt, int(bool(pow2)), q, sinv)
+    return q, sinv
+
+
 def cast_counts(x_bits, fmt: int, scale):
     """(underflow, saturated) counts of the per-tensor cast with `scale`."""
     x = np.ascontiguousarray(x_bits, dtype=np.uint16).reshape(-1)
@@ -211,7 +222,7 @@ def gemm_entries(A, fa: int, B, fb: int, sa, sb, ii, jj, ga: int = GRAN_TENSOR,
 
 # ------------------------------------------------------------------ linear
 
-SCALING_DELAYED, SCALING_DYNAMIC, SCALING_BLOCK = 0, 1, 2
+SCALING_DELAYED, SCALING_DYNAMIC, SCALING_BLOCK, SCALING_ROW = 0, 1, 2, 3
 
 
 @dataclass
@@ -229,7 +240,7 @@ class LinearState:
     plus the quantised forward operands that the backward pass reuses."""
 
     def __init__(self, recipe: Recipe):
-        h = 1 if recipe.scaling == SCALING_DYNAMIC else recipe.history_len
+        h = recipe.history_len if recipe.scaling == SCALING_DELAYED else 1
         self.roles = [ScaleState(h) for _ in range(3)]
         self.last_amax = np.zeros(3, np.float32)
         self.x_q = self.x_qt = self.w_q = self.w_qt = None
@@ -254,6 +265,19 @@ def _per_tensor_operand(st: LinearState, role: int, x_bits, fmt: int, recipe: Re
 
 def linear_fwd(X_bits, W_bits, recipe: Recipe, st: LinearState, rows=None):
     """Y = X . W^T.  Returns (Y, Yabs) fp64 (all rows, or the listed rows)."""
+    if recipe.scaling == SCALING_ROW:
+        # per-token scales for X, per-output-channel scales for W; the
+        # backward operands are the per-row casts of X^T and W^T (per-column
+        # scales of X and W), since the row scales lie along the backward
+        # reductions
+        X = np.ascontiguousarray(X_bits, dtype=np.uint16)
+        W = np.ascontiguousarray(W_bits, dtype=np.uint16)
+        st.x_q, st.x_sinv = row_quantize(X, E4M3, recipe.pow2)
+        st.w_q, st.w_sinv = row_quantize(W, E4M3, recipe.pow2)
+        st.xt_q, st.xt_sinv = row_quantize(np.ascontiguousarray(X.T), E4M3, recipe.pow2)
+        st.wt_q, st.wt_sinv = row_quantize(np.ascontiguousarray(W.T), E4M3, recipe.pow2)
+        return _gemm_rows(st.x_q, E4M3, st.w_q, E4M3, st.x_sinv, st.w_sinv, rows, GRAN_ROW,
+                          GRAN_ROW)
     if recipe.scaling == SCALING_BLOCK:
         X = np.ascontiguousarray(X_bits, dtype=np.uint16)
         st.x_q, st.x_sinv = block_quantize(X, E4M3, 1, recipe.pow2)
@@ -278,6 +302,18 @@ def linear_bwd(dY_bits, recipe: Recipe, st: LinearState, dW_prev=None, rows_dx=N
     Returns ((dX, dXabs), (dW, dWabs)); dW includes dW_prev when given."""
     if recipe.scaling == SCALING_BLOCK:
         return _linear_bwd_block(dY_bits, recipe, st, dW_prev, rows_dx, rows_dw)
+    if recipe.scaling == SCALING_ROW:
+        dY = np.ascontiguousarray(dY_bits, dtype=np.uint16)
+        dy_q, dy_s = row_quantize(dY, E5M2, recipe.pow2)
+        dyt_q, dyt_s = row_quantize(np.ascontiguousarray(dY.T), E5M2, recipe.pow2)
+        st.dy_q, st.dy_s, st.dyt_q, st.dyt_s = dy_q, dy_s, dyt_q, dyt_s
+        dX = _gemm_rows(dy_q, E5M2, st.wt_q, E4M3, dy_s, st.wt_sinv, rows_dx, GRAN_ROW, GRAN_ROW)
+        dW, dWabs = _gemm_rows(dyt_q, E5M2, st.xt_q, E4M3, dyt_s, st.xt_sinv, rows_dw, GRAN_ROW,
+                               GRAN_ROW)
+        if dW_prev is not None:
+            prev = np.asarray(dW_prev, np.float64)
+            dW = dW + (prev if rows_dw is None else prev[np.asarray(rows_dw)])
+        return dX, (dW, dWabs)
     sx, sw = st.sinv_fwd
     dy_q, dy_qt, sdy = _per_tensor_operand(st, ROLE_DY, dY_bits, E5M2, recipe)
     dX = _gemm_rows(dy_q, E5M2, st.w_qt, E4M3, sdy, sw, rows_dx)

@@ -48,6 +48,7 @@
 #define ORC_GRAN_TENSOR 0
 #define ORC_GRAN_1x128 1
 #define ORC_GRAN_128x128 2
+#define ORC_GRAN_ROW 3
 
 static uint32_t f32_bits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
 static float bits_f32(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
@@ -287,6 +288,30 @@ void orc_block_quantize(const uint16_t* x, int64_t rows, int64_t cols, int fmt,
     }
 }
 
+/* Per-row (per-channel) scaling ([MP] "Transformer Engine internals" >
+ * "Per-row vs per-tensor scaling"; "Calibration deep dive" > "Per-channel vs
+ * per-tensor"): every row of x gets its own scale from its own amax, by the
+ * block rule with the whole row as the block (margin 0; 1 for an all-zero or
+ * non-finite row; optional power of two).  scale_inv [rows]. */
+void orc_row_quantize(const uint16_t* x, int64_t rows, int64_t cols, int fmt, int pow2,
+                      uint8_t* q, float* scale_inv)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < rows; ++i) {
+        uint16_t m = 0;
+        for (int64_t j = 0; j < cols; ++j) {
+            uint16_t a = x[i * cols + j] & 0x7FFF;
+            if (a > m) m = a;
+        }
+        const float amax = orc_bf16_to_f32(m);
+        float s = 1.0f;
+        if (amax > 0.0f && isfinite(amax)) s = scale_from_amax(amax, fmt, 0, pow2);
+        scale_inv[i] = 1.0f / s;
+        for (int64_t j = 0; j < cols; ++j)
+            q[i * cols + j] = orc_encode(orc_bf16_to_f32(x[i * cols + j]) * s, fmt);
+    }
+}
+
 /* ------------------------------------------------------------------- GEMM */
 
 /* Dequantisation factor of operand row r for K-block kb under a granularity:
@@ -294,6 +319,7 @@ void orc_block_quantize(const uint16_t* x, int64_t rows, int64_t cols, int fmt,
 static double factor(const float* s, int gran, int64_t r, int64_t kb, int64_t KB)
 {
     if (gran == ORC_GRAN_TENSOR) return (double)s[0];
+    if (gran == ORC_GRAN_ROW) return (double)s[r];
     if (gran == ORC_GRAN_1x128) return (double)s[r * KB + kb];
     return (double)s[(r / 128) * KB + kb];
 }
@@ -302,7 +328,8 @@ static double factor(const float* s, int gran, int64_t r, int64_t kb, int64_t KB
  * both row-major with K contiguous):
  *   per-tensor: D[i][j] = (sa * sb) * sum_k dec(A[i][k]) * dec(B[j][k])
  *   block:      D[i][j] = sum_kb sa(i,kb) * sb(j,kb) * sum_{k in kb} dec(A)dec(B)
- * where sa, sb are the dequantisation factors (1 / quantisation scale).  The
+ * where sa, sb are the dequantisation factors (1 / quantisation scale); a
+ * per-row factor (sa[i] or sb[j]) is used like a per-tensor one.  The
  * products of two FP8 values are exact in fp64 and are summed in fp64
  * ([MP] "Skipping the BAcc accumulator promotion": FP8 is the multiplicand
  * precision, the accumulator is wider).  Dabs is the same sum over |terms|,
@@ -313,14 +340,15 @@ static void gemm_entry(const double* ta, const double* tb, const uint8_t* A, con
 {
     const uint8_t* a = A + i * K;
     const uint8_t* b = B + j * K;
-    if (ga == ORC_GRAN_TENSOR && gb == ORC_GRAN_TENSOR) {
+    if ((ga == ORC_GRAN_TENSOR || ga == ORC_GRAN_ROW) && (gb == ORC_GRAN_TENSOR || gb == ORC_GRAN_ROW)) {
+        /* per-tensor or per-row factors do not vary along k: outside the sum */
         double acc = 0.0, aacc = 0.0;
         for (int64_t k = 0; k < K; ++k) {
             const double p = ta[a[k]] * tb[b[k]];
             acc += p;
             aacc += fabs(p);
         }
-        const double f = (double)sa[0] * (double)sb[0];
+        const double f = factor(sa, ga, i, 0, 1) * factor(sb, gb, j, 0, 1);
         *d = f * acc;
         *dabs = fabs(f) * aacc;
         return;

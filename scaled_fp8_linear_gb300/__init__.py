@@ -21,8 +21,8 @@ import torch
 
 __all__ = [
     "E4M3", "E5M2", "OUT_BF16", "OUT_F32", "AMAX_MAX", "AMAX_MOST_RECENT",
-    "GRAN_TENSOR", "GRAN_1x128", "GRAN_128x128", "LAYOUT_TN",
-    "SCALING_DELAYED", "SCALING_DYNAMIC", "SCALING_BLOCK",
+    "GRAN_TENSOR", "GRAN_1x128", "GRAN_128x128", "GRAN_ROW", "LAYOUT_TN",
+    "SCALING_DELAYED", "SCALING_DYNAMIC", "SCALING_BLOCK", "SCALING_ROW",
     "Fp8Error", "Recipe", "LinearStateC", "Fp8Linear", "build", "lib", "library_path",
     "fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_quantize_blocks",
     "fp8_quantize_counted", "fp8_gemm",
@@ -33,9 +33,9 @@ __all__ = [
 E4M3, E5M2 = 0, 1
 OUT_BF16, OUT_F32 = 0, 1
 AMAX_MAX, AMAX_MOST_RECENT = 0, 1
-GRAN_TENSOR, GRAN_1x128, GRAN_128x128 = 0, 1, 2
+GRAN_TENSOR, GRAN_1x128, GRAN_128x128, GRAN_ROW = 0, 1, 2, 3
 LAYOUT_TN = 0
-SCALING_DELAYED, SCALING_DYNAMIC, SCALING_BLOCK = 0, 1, 2
+SCALING_DELAYED, SCALING_DYNAMIC, SCALING_BLOCK, SCALING_ROW = 0, 1, 2, 3
 
 _STATUS = {0: "FP8_OK", -1: "FP8_ERR_INVALID_ARG", -2: "FP8_ERR_SHAPE", -3: "FP8_ERR_ALIGN",
            -4: "FP8_ERR_CUDA", -5: "FP8_ERR_TIMEOUT", -6: "FP8_ERR_UNSUPPORTED"}
@@ -173,6 +173,18 @@ def fp8_update_scale(amax, history, pos, history_len, algo, fmt, margin, pow2, s
         _ptr(scale_inv, "scale_inv", torch.float32), _stream(stream)))
 
 
+def _scale_shape(gran, rows, cols):
+    if gran == GRAN_ROW:
+        return (rows,)
+    return (rows // (1 if gran == GRAN_1x128 else 128), cols // 128)
+
+
+def _scale_shape_t(gran, rows, cols):
+    if gran == GRAN_ROW:
+        return (cols,)
+    return (cols, rows // 128) if gran == GRAN_1x128 else (cols // 128, rows // 128)
+
+
 def fp8_quantize(x: torch.Tensor, fmt: int, granularity: int = GRAN_TENSOR, scale=None,
                  pow2: bool = False, q=None, q_t=None, transpose: bool = False,
                  scale_inv_blocks=None, amax_out=None, want_amax: bool = False,
@@ -191,11 +203,11 @@ def fp8_quantize(x: torch.Tensor, fmt: int, granularity: int = GRAN_TENSOR, scal
     if transpose and q_t is None:
         q_t = torch.empty(cols, rows, dtype=torch.uint8, device=dev)
     if granularity != GRAN_TENSOR and scale_inv_blocks is None:
-        br = 1 if granularity == GRAN_1x128 else 128
-        scale_inv_blocks = torch.empty(rows // br, cols // 128, dtype=torch.float32, device=dev)
+        scale_inv_blocks = torch.empty(*_scale_shape(granularity, rows, cols), dtype=torch.float32,
+                                       device=dev)
     if granularity != GRAN_TENSOR and q_t is not None and scale_inv_blocks_t is None:
-        shape = (cols, rows // 128) if granularity == GRAN_1x128 else (cols // 128, rows // 128)
-        scale_inv_blocks_t = torch.empty(*shape, dtype=torch.float32, device=dev)
+        scale_inv_blocks_t = torch.empty(*_scale_shape_t(granularity, rows, cols),
+                                         dtype=torch.float32, device=dev)
     if want_amax and amax_out is None:
         amax_out = torch.empty(1, dtype=torch.float32, device=dev)
     _check(lib().fp8_quantize(
@@ -237,8 +249,8 @@ def fp8_quantize_blocks(x: torch.Tensor, fmt: int, granularity: int, pow2: bool 
     q_t = torch.empty(cols, rows, dtype=torch.uint8, device=x.device) if transpose else None
     st = None
     if transpose:
-        shape = (cols, rows // 128) if granularity == GRAN_1x128 else (cols // 128, rows // 128)
-        st = torch.empty(*shape, dtype=torch.float32, device=x.device)
+        st = torch.empty(*_scale_shape_t(granularity, rows, cols), dtype=torch.float32,
+                         device=x.device)
     q, q_t, s, _ = fp8_quantize(x, fmt, granularity, pow2=pow2, q_t=q_t, scale_inv_blocks_t=st,
                                 stream=stream)
     return q, s, q_t, st
@@ -317,15 +329,24 @@ class Fp8Linear:
         self.x_q = torch.empty(M, K, **u8)
         self.w_q = torch.empty(N, K, **u8)
         block = self.recipe.scaling == SCALING_BLOCK
+        rowwise = self.recipe.scaling == SCALING_ROW
         # block mode keeps the backward operands only when the token count
         # allows 1x128 blocks along it
         keep = not block or M % 128 == 0
         self.x_qt = torch.empty(K, M, **u8) if keep else None
         self.w_qt = torch.empty(K, N, **u8) if keep else None
-        self.x_sinv = torch.empty(M, K // 128, **f32) if block else None
-        self.w_sinv = torch.empty(N // 128, K // 128, **f32) if block else None
-        self.x_sinv_t = torch.empty(K, M // 128, **f32) if block and keep else None
-        self.w_sinv_t = torch.empty(K // 128, N // 128, **f32) if block and keep else None
+        self.x_sinv = self.w_sinv = self.x_sinv_t = self.w_sinv_t = None
+        if block:
+            self.x_sinv = torch.empty(M, K // 128, **f32)
+            self.w_sinv = torch.empty(N // 128, K // 128, **f32)
+            if keep:
+                self.x_sinv_t = torch.empty(K, M // 128, **f32)
+                self.w_sinv_t = torch.empty(K // 128, N // 128, **f32)
+        elif rowwise:
+            self.x_sinv = torch.empty(M, **f32)
+            self.w_sinv = torch.empty(N, **f32)
+            self.x_sinv_t = torch.empty(K, **f32)
+            self.w_sinv_t = torch.empty(K, **f32)
         ws = fp8_workspace_size(M, N, K, self.recipe)
         self.workspace = torch.empty(max(ws, 16), **u8)
         p = lambda t: None if t is None else t.data_ptr()

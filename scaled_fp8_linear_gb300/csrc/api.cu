@@ -44,7 +44,8 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool valid_format(int f) { return f == FP8_E4M3 || f == FP8_E5M2; }
-bool valid_gran(int g) { return g >= FP8_GRAN_TENSOR && g <= FP8_GRAN_128x128; }
+bool valid_gran(int g) { return g >= FP8_GRAN_TENSOR && g <= FP8_GRAN_ROW; }
+bool block_gran(int g) { return g == FP8_GRAN_1x128 || g == FP8_GRAN_128x128; }
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
@@ -61,7 +62,7 @@ int cuda_status(cudaError_t e, const char* what) {
 
 int check_recipe(const fp8_recipe_t* r) {
     if (!r) return set_error(FP8_ERR_INVALID_ARG, "recipe is NULL");
-    if (r->scaling < FP8_SCALING_DELAYED || r->scaling > FP8_SCALING_BLOCK)
+    if (r->scaling < FP8_SCALING_DELAYED || r->scaling > FP8_SCALING_ROW)
         return set_error(FP8_ERR_INVALID_ARG, "unknown scaling mode %d", r->scaling);
     if (r->margin < 0 || r->margin > 64)
         return set_error(FP8_ERR_INVALID_ARG, "margin %d outside 0..64", r->margin);
@@ -96,7 +97,9 @@ int check_gemm_args(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t 
     if (M < 0 || N < 0 || K < 0 || M > (1ll << 31) || N > (1ll << 31) || K > (1ll << 31))
         return set_error(FP8_ERR_SHAPE, "fp8_gemm: dimensions out of range");
     if (N % 16 || K % 16) return set_error(FP8_ERR_SHAPE, "fp8_gemm: N and K must be multiples of 16");
-    const bool block = ga != FP8_GRAN_TENSOR || gb != FP8_GRAN_TENSOR;
+    const bool block = block_gran(ga) || block_gran(gb);
+    if (block && (ga == FP8_GRAN_ROW || gb == FP8_GRAN_ROW))
+        return set_error(FP8_ERR_UNSUPPORTED, "fp8_gemm: per-row and block scales cannot be mixed");
     if (block) {
         if (K % 128 || N % 128)
             return set_error(FP8_ERR_SHAPE, "fp8_gemm: block scales need N and K multiples of 128");
@@ -120,6 +123,14 @@ int check_quantize_args(const void* x, int64_t rows, int64_t cols, int format, i
         if (!scale) return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: scale is NULL");
         if (q_t && (rows % 16 || cols % 16))
             return set_error(FP8_ERR_SHAPE, "fp8_quantize: the transpose needs rows and cols multiples of 16");
+    } else if (gran == FP8_GRAN_ROW) {
+        if (!sinv) return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: scale_inv_blocks is NULL");
+        if (amax_out || scale)
+            return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: per-row mode takes no scale or amax_out");
+        if (q_t && !sinv_t)
+            return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: q_t needs scale_inv_blocks_t in per-row mode");
+        if (cols % 16 || (q_t && rows % 16))
+            return set_error(FP8_ERR_SHAPE, "fp8_quantize: per-row mode needs cols (and, with q_t, rows) multiples of 16");
     } else {
         if (!sinv) return set_error(FP8_ERR_INVALID_ARG, "fp8_quantize: scale_inv_blocks is NULL");
         if (amax_out || scale)
@@ -188,6 +199,39 @@ int linear_bwd_block(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_
                        s->x_sinv_t, dW, FP8_OUT_F32, accumulate_dW != 0, st);
 }
 
+// Per-row backward: dY cast per token (dgrad operand) and per output
+// channel (dY^T, wgrad operand); dgrad takes W^T's per-input-channel cast
+// and wgrad X^T's, both kept by the forward pass.  Every factor is per row
+// or per column of the GEMM output, so all three GEMMs are per-tensor-kernel
+// GEMMs with vector epilogue factors.
+int linear_bwd_row(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe,
+                   const fp8_linear_state_t* s, void* dX, float* dW, int accumulate_dW,
+                   void* workspace, size_t workspace_bytes, cudaStream_t st) {
+    if (!s->x_qt || !s->w_qt || !s->x_sinv_t || !s->w_sinv_t)
+        return set_error(FP8_ERR_INVALID_ARG,
+                         "fp8_linear_bwd: per-row mode needs the forward's x_qt/x_sinv_t and w_qt/w_sinv_t");
+    const size_t mn = static_cast<size_t>(M) * static_cast<size_t>(N);
+    const size_t need = 2 * align256(mn) + align256(4 * static_cast<size_t>(M)) +
+                        align256(4 * static_cast<size_t>(N));
+    if (workspace_bytes < need)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: workspace of %zu bytes, %zu needed",
+                         workspace_bytes, need);
+    if (!aligned16(dY) || !aligned16(dX) || !aligned16(dW) || !aligned16(workspace) ||
+        !aligned16(s->x_qt) || !aligned16(s->w_qt))
+        return set_error(FP8_ERR_ALIGN, "fp8_linear_bwd: tensors must be 16-byte aligned");
+    const int fb = recipe->bwd_format, ff = recipe->fwd_format;
+    uint8_t* dy_q = static_cast<uint8_t*>(workspace);
+    uint8_t* dy_qt = dy_q + align256(mn);
+    float* dy_s = reinterpret_cast<float*>(dy_qt + align256(mn));
+    float* dy_st = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dy_s) + align256(4 * static_cast<size_t>(M)));
+    FP8_CHECK(cuda_status(launch_quantize_rows(dY, M, N, fb, recipe->pow2 != 0, dy_q, dy_s, dy_qt,
+                                               dy_st, st), "quantize dY"));
+    FP8_CHECK(launch_gemm(dy_q, fb, s->w_qt, ff, M, K, N, FP8_GRAN_ROW, dy_s, FP8_GRAN_ROW,
+                          s->w_sinv_t, dX, FP8_OUT_BF16, 0, st));
+    return launch_gemm(dy_qt, fb, s->x_qt, ff, N, K, M, FP8_GRAN_ROW, dy_st, FP8_GRAN_ROW,
+                       s->x_sinv_t, dW, FP8_OUT_F32, accumulate_dW != 0, st);
+}
+
 }  // namespace
 }  // namespace fp8
 
@@ -230,6 +274,11 @@ int fp8_quantize(const void* x, int64_t rows, int64_t cols, int format, int gran
         return cuda_status(launch_quantize_tensor(x, rows, cols, format, scale, q, q_t, amax_out,
                                                   as_stream(stream)),
                            "fp8_quantize");
+    if (granularity == FP8_GRAN_ROW)
+        return cuda_status(launch_quantize_rows(x, rows, cols, format, pow2 != 0, q,
+                                                scale_inv_blocks, q_t, scale_inv_blocks_t,
+                                                as_stream(stream)),
+                           "fp8_quantize");
     return cuda_status(launch_quantize_block(x, rows, cols, format, granularity, pow2 != 0, q,
                                              scale_inv_blocks, q_t, scale_inv_blocks_t,
                                              as_stream(stream)),
@@ -263,6 +312,8 @@ size_t fp8_workspace_size(int64_t M, int64_t N, int64_t K, const fp8_recipe_t* r
     if (check_recipe(recipe) != FP8_OK || M < 0 || N < 0) return 0;
     const size_t mn = static_cast<size_t>(M) * static_cast<size_t>(N);
     // backward: dY quantised [M x N] and its transposed cast [N x M]
+    if (recipe->scaling == FP8_SCALING_ROW)   // + per-row scales of both, [M] and [N]
+        return 2 * align256(mn) + align256(4 * static_cast<size_t>(M)) + align256(4 * static_cast<size_t>(N));
     if (recipe->scaling != FP8_SCALING_BLOCK) return 2 * align256(mn);
     // block mode adds their 1x128 scale arrays, [M][N/128] and [N][M/128]
     return 2 * align256(mn) + 2 * align256(4 * (mn / 128));
@@ -282,6 +333,24 @@ int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K
         return set_error(FP8_ERR_ALIGN, "fp8_linear_fwd: tensors must be 16-byte aligned");
     cudaStream_t st = as_stream(stream);
     const int f = recipe->fwd_format;
+
+    if (recipe->scaling == FP8_SCALING_ROW) {
+        // per-token X, per-output-channel W; with x_qt and w_qt kept (training)
+        // the same launches also cast X^T and W^T per row (per column of X, W)
+        if (!s->x_sinv || !s->w_sinv)
+            return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_fwd: per-row mode needs x_sinv and w_sinv");
+        const bool keep = s->x_qt && s->w_qt;
+        if (keep && (!s->x_sinv_t || !s->w_sinv_t))
+            return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_fwd: per-row mode with x_qt/w_qt needs x_sinv_t and w_sinv_t");
+        FP8_CHECK(cuda_status(launch_quantize_rows(X, M, K, f, recipe->pow2 != 0, s->x_q, s->x_sinv,
+                                                   keep ? s->x_qt : nullptr, s->x_sinv_t, st),
+                              "quantize X"));
+        FP8_CHECK(cuda_status(launch_quantize_rows(W, N, K, f, recipe->pow2 != 0, s->w_q, s->w_sinv,
+                                                   keep ? s->w_qt : nullptr, s->w_sinv_t, st),
+                              "quantize W"));
+        return launch_gemm(s->x_q, f, s->w_q, f, M, N, K, FP8_GRAN_ROW, s->x_sinv, FP8_GRAN_ROW,
+                           s->w_sinv, Y, FP8_OUT_BF16, 0, st);
+    }
 
     if (recipe->scaling == FP8_SCALING_BLOCK) {
         if (!s->x_sinv || !s->w_sinv)
@@ -342,6 +411,9 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
     if (recipe->scaling == FP8_SCALING_BLOCK)
         return linear_bwd_block(dY, M, N, K, recipe, s, dX, dW, accumulate_dW, workspace,
                                 workspace_bytes, as_stream(stream));
+    if (recipe->scaling == FP8_SCALING_ROW)
+        return linear_bwd_row(dY, M, N, K, recipe, s, dX, dW, accumulate_dW, workspace,
+                              workspace_bytes, as_stream(stream));
     FP8_CHECK(check_state_scales(s));
     if (!s->x_qt || !s->w_qt)
         return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: the forward pass must keep x_qt and w_qt");

@@ -123,10 +123,34 @@ __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t
     }
 }
 
-// Epilogue of one 32-column chunk of an accumulator row: scale by alpha, then
-// round to bf16 or (optionally) add into the FP32 buffer; 16-byte stores.
+// Dequantisation factors of one 32-column chunk, f[j] = fp32(fa * sb(n0 + j)):
+// fa is the thread's row factor (sa[m] for per-row A, else sa[0]); sb is per
+// column for per-row B (lane j loads column n0 + j, shuffled to all lanes)
+// or sb[0].  Warp-collective: every lane of the warp calls it.
+__device__ __forceinline__ void chunk_factors(float (&f)[32], float fa, int64_t n0,
+                                              const GemmParams& p) {
+    if (p.gb == FP8_GRAN_ROW) {
+        const int lane = threadIdx.x & 31;
+        const float sbv = n0 + lane < p.N ? p.sb[n0 + lane] : 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = __fmul_rn(fa, __shfl_sync(0xFFFFFFFFu, sbv, j));
+    } else {
+        const float a = __fmul_rn(fa, p.sb[0]);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = a;
+    }
+}
+
+// Row factor of the A operand for row m (clamped into the matrix).
+__device__ __forceinline__ float row_factor(const GemmParams& p, int64_t m) {
+    return p.ga == FP8_GRAN_ROW ? p.sa[m < p.M ? m : p.M - 1] : p.sa[0];
+}
+
+// Epilogue of one 32-column chunk of an accumulator row: multiply column j
+// by f[j], then round to bf16 or (optionally) add into the FP32 buffer;
+// 16-byte stores.
 __device__ __forceinline__ void store_chunk(const uint32_t (&r)[32], int64_t m, int64_t n0,
-                                            const GemmParams& p, float alpha, bool rmw) {
+                                            const GemmParams& p, const float (&f)[32], bool rmw) {
     if (p.out == FP8_OUT_BF16) {
         __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.D) + m * p.N;
 #pragma unroll
@@ -136,8 +160,8 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&r)[32], int64_t m, 
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const __nv_bfloat162 h =
-                        __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[j + 2 * e]), alpha),
-                                              __fmul_rn(__uint_as_float(r[j + 2 * e + 1]), alpha));
+                        __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[j + 2 * e]), f[j + 2 * e]),
+                                              __fmul_rn(__uint_as_float(r[j + 2 * e + 1]), f[j + 2 * e + 1]));
                     w[e] = *reinterpret_cast<const uint32_t*>(&h);
                 }
                 *reinterpret_cast<uint4*>(drow + n0 + j) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -153,10 +177,10 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&r)[32], int64_t m, 
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             if (n0 + 4 * j < p.N) {
-                float4 v = make_float4(__fmul_rn(__uint_as_float(r[4 * j]), alpha),
-                                       __fmul_rn(__uint_as_float(r[4 * j + 1]), alpha),
-                                       __fmul_rn(__uint_as_float(r[4 * j + 2]), alpha),
-                                       __fmul_rn(__uint_as_float(r[4 * j + 3]), alpha));
+                float4 v = make_float4(__fmul_rn(__uint_as_float(r[4 * j]), f[4 * j]),
+                                       __fmul_rn(__uint_as_float(r[4 * j + 1]), f[4 * j + 1]),
+                                       __fmul_rn(__uint_as_float(r[4 * j + 2]), f[4 * j + 2]),
+                                       __fmul_rn(__uint_as_float(r[4 * j + 3]), f[4 * j + 3]));
                 if (rmw) {
                     v.x += o[j].x; v.y += o[j].y; v.z += o[j].z; v.w += o[j].w;
                 }
@@ -259,7 +283,6 @@ __global__ void __launch_bounds__(256, 1)
     } else if (warp >= 4) {
         const int qd = warp & 3;  // TMEM lane quadrant this warp may access
         const int row = qd * 32 + lane;
-        const float alpha = __fmul_rn(p.sa[0], p.sb[0]);
         uint32_t acc = 0, acc_phase = 0;
         const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -274,6 +297,7 @@ __global__ void __launch_bounds__(256, 1)
             __syncwarp();
             ptx::tc_fence_after();
             const int64_t m = static_cast<int64_t>(m_blk) * BM + row;
+            const float fa = row_factor(p, m);
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + acc * BN;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
@@ -281,7 +305,9 @@ __global__ void __launch_bounds__(256, 1)
                 ptx::tmem_ld_32x32b_x32(tbase + c * 32, r);
                 ptx::tmem_wait_ld();
                 const int64_t n0 = static_cast<int64_t>(n_blk) * BN + c * 32;
-                if (m < p.M) store_chunk(r, m, n0, p, alpha, rmw);
+                float f[32];
+                chunk_factors(f, fa, n0, p);
+                if (m < p.M) store_chunk(r, m, n0, p, f, rmw);
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -434,7 +460,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     } else if (warp >= 4) {
         const int qd = warp & 3;
         const int row = qd * 32 + lane;
-        const float alpha = __fmul_rn(p.sa[0], p.sb[0]);
         const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
         uint32_t acc = 0, acc_phase = 0;
         for (int tile = pair; tile < num_tiles; tile += npairs) {
@@ -447,13 +472,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             if (!ok) break;
             __syncwarp();
             ptx::tc_fence_after();
+            const float fa = row_factor(p, m);
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + acc * TILE;
 #pragma unroll 1
             for (int c = 0; c < TILE / 32; ++c) {
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(tbase + c * 32, r);
                 ptx::tmem_wait_ld();
-                if (m < p.M) store_chunk(r, m, static_cast<int64_t>(n_blk) * TILE + c * 32, p, alpha, rmw);
+                const int64_t n0 = static_cast<int64_t>(n_blk) * TILE + c * 32;
+                float f[32];
+                chunk_factors(f, fa, n0, p);
+                if (m < p.M) store_chunk(r, m, n0, p, f, rmw);
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -820,9 +849,9 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
         return e == cudaSuccess ? FP8_OK
                                 : set_error(FP8_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
     }
-    const bool block = ga != FP8_GRAN_TENSOR || gb != FP8_GRAN_TENSOR;
-    // CTA pairs for every problem of at least 256 rows, except the block GEMM
-    // with per-column B scales (the wgrad of the block recipe)
+    const bool block = ga == FP8_GRAN_1x128 || ga == FP8_GRAN_128x128 || gb == FP8_GRAN_1x128 ||
+                       gb == FP8_GRAN_128x128;
+    // per-tensor and per-row scales: CTA pairs for every problem of at least 256 rows
     const bool pair = !block && M >= kPairMinRows;
     const int BN = block ? 128 : kTensorBN;
     const int TM = pair ? 256 : BM;   // rows of C per tile

@@ -39,6 +39,13 @@ cudaError_t launch_quantize_block(const void* x, int64_t rows, int64_t cols, int
                                   int pow2, uint8_t* q, float* scale_inv, uint8_t* q_t,
                                   float* scale_inv_t, cudaStream_t stream);
 
+// Per-row cast: q with one scale per row (scale_inv [rows]); q_t (nullable,
+// rows and cols multiples of 16) is the per-row cast of x^T, i.e. one scale
+// per column of x (scale_inv_t [cols]).  cols is a multiple of 8.
+cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int fmt, int pow2,
+                                 uint8_t* q, float* scale_inv, uint8_t* q_t, float* scale_inv_t,
+                                 cudaStream_t stream);
+
 // Scaled FP8 GEMM, TN layout.  Returns 0 or a negative fp8 status code
 // (tensor-map encoding can fail); launch errors come back as FP8_ERR_CUDA.
 int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,

@@ -508,6 +508,128 @@ __global__ void __launch_bounds__(kThreads)
     if (h == 0) scale_inv_t[(c0 + c) * (rows / 128) + r0 / 128] = __fdiv_rn(1.0f, sc);
 }
 
+// ------------------------------------------------------ per-row scaling
+
+// Per-row cast: one CTA per row, the row's amax (pass 1), then the cast with
+// the row's scale (pass 2, the re-read hits L2).  scale_inv[row] = 1/s.
+// cols is a multiple of 8.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads)
+    quantize_row_kernel(const uint16_t* __restrict__ x, int64_t cols, int pow2,
+                        uint8_t* __restrict__ q, float* __restrict__ scale_inv) {
+    __shared__ uint32_t warp_max[kThreads / 32];
+    const int64_t row = blockIdx.x;
+    const uint4* src = reinterpret_cast<const uint4*>(x + row * cols);
+    const int64_t nv = cols / 8;
+    uint32_t m2 = 0;
+    for (int64_t i = threadIdx.x; i < nv; i += kThreads) m2 = absmax_vec(m2, src[i]);
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) m = max(m, warp_max[w]);
+    const float s = block_scale<FMT>(__uint_as_float(m << 16), pow2);
+    uint2* dst = reinterpret_cast<uint2*>(q + row * cols);
+    for (int64_t i = threadIdx.x; i < nv; i += kThreads) {
+        const uint4 v = src[i];
+        dst[i] = make_uint2(cvt4<FMT>(v.x, v.y, s), cvt4<FMT>(v.z, v.w, s));
+    }
+    if (threadIdx.x == 0) scale_inv[row] = __fdiv_rn(1.0f, s);
+}
+
+// Column amax of x (the per-row scales of x^T): each CTA reduces a 128 x 128
+// tile through shared memory and raises colmax[c] (fp32 bit patterns of the
+// |bf16| maxima, zeroed beforehand) with one atomicMax per column.
+__global__ void __launch_bounds__(kThreads)
+    column_amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t tiles_c,
+                       unsigned* __restrict__ colmax) {
+    __shared__ uint16_t part[32][128];
+    const int64_t tile = blockIdx.x;
+    const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
+    const int t = threadIdx.x, cg = t & 7, rg = t >> 3;
+    uint32_t cm[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // 16 columns, 2 per word
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int64_t r = r0 + it * 32 + rg, c = c0 + cg * 16;
+        if (r < rows && c < cols) {
+            const uint4* p = reinterpret_cast<const uint4*>(x + r * cols + c);
+            const uint4 a = ldg_stream(p), b = ldg_stream(p + 1);
+            cm[0] = absmax2(cm[0], a.x); cm[1] = absmax2(cm[1], a.y);
+            cm[2] = absmax2(cm[2], a.z); cm[3] = absmax2(cm[3], a.w);
+            cm[4] = absmax2(cm[4], b.x); cm[5] = absmax2(cm[5], b.y);
+            cm[6] = absmax2(cm[6], b.z); cm[7] = absmax2(cm[7], b.w);
+        }
+    }
+    uint32_t* prow = reinterpret_cast<uint32_t*>(&part[rg][cg * 16]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) prow[j] = cm[j];
+    __syncthreads();
+    if (t < 128 && c0 + t < cols) {
+        uint32_t m = 0;
+#pragma unroll 8
+        for (int g = 0; g < 32; ++g) m = max(m, static_cast<uint32_t>(part[g][t]));
+        if (m) atomicMax(&colmax[c0 + t], m << 16);
+    }
+}
+
+// The per-row cast of x^T, written as q_t [cols x rows]: every column of x
+// is cast with its own scale (from colmax), staged in shared memory and
+// written transposed like quantize_transpose_kernel.  rows, cols: multiples
+// of 16.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads)
+    quantize_col_transpose_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
+                                  int64_t tiles_c, int pow2, const unsigned* __restrict__ colmax,
+                                  uint8_t* __restrict__ qt) {
+    __shared__ __align__(16) uint32_t S[128 * 32];
+    const int64_t tile = blockIdx.x;
+    const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
+    const int t = threadIdx.x, cg = t & 7;
+    float sc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int64_t c = c0 + cg * 16 + j;
+        sc[j] = c < cols ? block_scale<FMT>(__uint_as_float(colmax[c]), pow2) : 1.0f;
+    }
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int rl = it * 32 + (t >> 3);
+        const int64_t r = r0 + rl, c = c0 + cg * 16;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (r < rows && c < cols) {
+            const uint4* p = reinterpret_cast<const uint4*>(x + r * cols + c);
+            const uint4 a = ldg_stream(p), b = ldg_stream(p + 1);
+            const uint32_t in[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t w0 = in[2 * k], w1 = in[2 * k + 1];
+                const float f0 = __fmul_rn(__uint_as_float(w0 << 16), sc[4 * k]);
+                const float f1 = __fmul_rn(__uint_as_float(w0 & 0xFFFF0000u), sc[4 * k + 1]);
+                const float f2 = __fmul_rn(__uint_as_float(w1 << 16), sc[4 * k + 2]);
+                const float f3 = __fmul_rn(__uint_as_float(w1 & 0xFFFF0000u), sc[4 * k + 3]);
+                const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f0, f1), __NV_SATFINITE, Fp8Traits<FMT>::kind);
+                const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f2, f3), __NV_SATFINITE, Fp8Traits<FMT>::kind);
+                w[k] = lo | (hi << 16);
+            }
+        }
+        *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncthreads();
+    transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
+}
+
+// scale_inv_t[c] = 1 / s(amax_c), in place over the column amaxes.
+template <int FMT>
+__global__ void column_scale_finalize_kernel(float* __restrict__ sinv_t, int64_t cols, int pow2) {
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (c < cols) {
+        const float amax = sinv_t[c];
+        sinv_t[c] = __fdiv_rn(1.0f, block_scale<FMT>(amax, pow2));
+    }
+}
+
 int grid_for(int64_t work_items, int per_cta) {
     const int64_t need = (work_items + per_cta - 1) / per_cta;
     const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
@@ -587,6 +709,33 @@ cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, in
         else launch_cast<1, false>(x, rows, cols, scale, q, q_t, amax, counts, stream);
     }
     return cudaGetLastError();
+}
+
+template <int FMT>
+static cudaError_t launch_row(const uint16_t* xs, int64_t rows, int64_t cols, int pow2, uint8_t* q,
+                              float* scale_inv, uint8_t* q_t, float* scale_inv_t,
+                              cudaStream_t stream) {
+    quantize_row_kernel<FMT><<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(xs, cols, pow2, q, scale_inv);
+    if (!q_t) return cudaGetLastError();
+    cudaError_t e = cudaMemsetAsync(scale_inv_t, 0, cols * sizeof(float), stream);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles_c = (cols + 127) / 128, tiles = ((rows + 127) / 128) * tiles_c;
+    column_amax_kernel<<<static_cast<unsigned>(tiles), kThreads, 0, stream>>>(
+        xs, rows, cols, tiles_c, reinterpret_cast<unsigned*>(scale_inv_t));
+    quantize_col_transpose_kernel<FMT><<<static_cast<unsigned>(tiles), kThreads, 0, stream>>>(
+        xs, rows, cols, tiles_c, pow2, reinterpret_cast<const unsigned*>(scale_inv_t), q_t);
+    column_scale_finalize_kernel<FMT><<<static_cast<unsigned>((cols + 255) / 256), 256, 0, stream>>>(
+        scale_inv_t, cols, pow2);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int fmt, int pow2,
+                                 uint8_t* q, float* scale_inv, uint8_t* q_t, float* scale_inv_t,
+                                 cudaStream_t stream) {
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    const uint16_t* xs = static_cast<const uint16_t*>(x);
+    return fmt == 0 ? launch_row<0>(xs, rows, cols, pow2, q, scale_inv, q_t, scale_inv_t, stream)
+                    : launch_row<1>(xs, rows, cols, pow2, q, scale_inv, q_t, scale_inv_t, stream);
 }
 
 cudaError_t launch_quantize_block(const void* x, int64_t rows, int64_t cols, int fmt, int gran,

@@ -161,3 +161,26 @@ def test_block_scaled_exact_column_scales():
                out=F.OUT_F32, D=D, accumulate=True)
     Do, _ = oracle.gemm(A, F.E5M2, B, F.E4M3, sa, sb, F.GRAN_1x128, F.GRAN_1x128)
     assert np.array_equal(D.cpu().numpy().astype(np.float64), Do + prev)
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 336, 304), (512, 768, 1024), (1, 16, 16)])
+@pytest.mark.parametrize("ga,gb", [(F.GRAN_ROW, F.GRAN_ROW), (F.GRAN_ROW, F.GRAN_TENSOR),
+                                   (F.GRAN_TENSOR, F.GRAN_ROW)])
+@pytest.mark.parametrize("out", [F.OUT_BF16, F.OUT_F32])
+def test_row_scaled(M, N, K, ga, gb, out):
+    rng = np.random.default_rng(M + N + K + ga + 3 * gb + out)
+
+    def operand(rows, gran, std):
+        v = rng.standard_normal((rows, K)).astype(np.float32) * std
+        v *= np.abs(rng.standard_t(3, size=(rows, 1))).astype(np.float32)
+        b = (v.view(np.uint32) >> 16).astype(np.uint16)
+        if gran == F.GRAN_ROW:
+            return oracle.row_quantize(b, F.E4M3)
+        s = np.float32(448) / oracle.amax(b)
+        return oracle.quantize(b, F.E4M3, s)[0], np.array([1 / s], np.float32)
+
+    A, sa = operand(M, ga, 1.0)
+    B, sb = operand(N, gb, 0.02)
+    D = F.fp8_gemm(_t(A), F.E4M3, _t(B), F.E4M3, _s(sa), _s(sb), ga, gb, out=out)
+    Do, Dabs = oracle.gemm(A, F.E4M3, B, F.E4M3, sa, sb, ga, gb)
+    assert_gemm_bound(D, Do, Dabs, what=f"row {M}x{N}x{K}")

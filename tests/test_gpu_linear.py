@@ -127,6 +127,45 @@ def test_block_training_steps(M, N, K):
         dW_o = dW.cpu().numpy().astype(np.float64)
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (4096, 2048, 1024)])
+def test_row_training_steps(M, N, K):
+    """Per-row (per-token / per-channel) scaling, forward + backward, 2 steps
+    with wgrad accumulation: casts and scales bit-exact, GEMMs within the
+    bound."""
+    rec = F.Recipe(F.SCALING_ROW)
+    layer = F.Fp8Linear(M, N, K, rec, device=DEV)
+    orec = _orecipe(rec)
+    ost = oracle.LinearState(orec)
+    W = synthetic.student_t_rows((N, K), 0.02, 3, seed=91)
+    dW = torch.zeros(N, K, dtype=torch.float32, device=DEV)
+    dW_o = np.zeros((N, K))
+    rows = None if M * N <= 256 * 384 else np.arange(0, M, 97)
+    for step in range(2):
+        X = synthetic.with_outlier_channels((M, K), 1.0, 4, 50.0, seed=60 + step)
+        dY = synthetic.normal((M, N), 1e-3, seed=70 + step)
+        acc = step > 0
+        Y = layer.forward(X.to(DEV), W.to(DEV))
+        dX, _ = layer.backward(dY.to(DEV), dW=dW, accumulate_dW=acc)
+        Yo, Yabs = oracle.linear_fwd(bits(X), bits(W), orec, ost, rows=rows)
+        prev = dW_o.copy()
+        rows_dw = None if rows is None else np.arange(0, N, 53)
+        (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(
+            bits(dY), orec, ost, dW_prev=prev if acc else None, rows_dx=rows, rows_dw=rows_dw)
+        for got, want in ((layer.x_q, ost.x_q), (layer.w_q, ost.w_q), (layer.x_qt, ost.xt_q),
+                          (layer.w_qt, ost.wt_q)):
+            assert np.array_equal(u8(got), want)
+        for got, want in ((layer.x_sinv, ost.x_sinv), (layer.w_sinv, ost.w_sinv),
+                          (layer.x_sinv_t, ost.xt_sinv), (layer.w_sinv_t, ost.wt_sinv)):
+            assert np.array_equal(f32bits(got.cpu().numpy()), f32bits(want))
+        sel = (lambda t, r: t if r is None else t[torch.as_tensor(r, device=DEV)])
+        assert_gemm_bound(sel(Y, rows), Yo, Yabs, what=f"Y step {step}")
+        assert_gemm_bound(sel(dX, rows), dXo, dXabs, what=f"dX step {step}")
+        assert_gemm_bound(sel(dW, rows_dw), dWo, dWabs,
+                          prev=(prev if rows_dw is None else prev[rows_dw]) if acc else None,
+                          what=f"dW step {step}")
+        dW_o = dW.cpu().numpy().astype(np.float64)
+
+
 def test_checkpoint_restore_gives_identical_next_step():
     M, N, K = 128, 256, 256
     rec = F.Recipe(F.SCALING_DELAYED, history_len=16)

@@ -212,3 +212,21 @@ def test_cast_counters_sweep_shapes(shape, mag):
     tr = shape[0] % 16 == 0 and shape[1] % 16 == 0
     _, _, _, counts = F.fp8_quantize_counted(x.to(DEV), F.E4M3, one, transpose=tr)
     assert tuple(counts.cpu().tolist()) == oracle.cast_counts(bits(x), F.E4M3, 1.0)
+
+
+@pytest.mark.parametrize("shape", [(16, 16), (48, 400), (1024, 640), (129, 272)])
+@pytest.mark.parametrize("fmt", [F.E4M3, F.E5M2])
+@pytest.mark.parametrize("pow2", [False, True])
+def test_row_cast_and_transposed_column_cast(shape, fmt, pow2):
+    x = synthetic.student_t_rows(shape, 1.0, 3, seed=shape[0] * 5 + shape[1])
+    x[min(3, shape[0] - 1)] = 0                    # an all-zero row
+    x[:, 5] = 0                                    # an all-zero column
+    tr = shape[0] % 16 == 0
+    q, s, qt, st = F.fp8_quantize_blocks(x.to(DEV), fmt, F.GRAN_ROW, pow2=pow2, transpose=tr)
+    qo, so = oracle.row_quantize(bits(x), fmt, pow2)
+    assert np.array_equal(u8(q), qo)
+    assert np.array_equal(f32bits(s.cpu().numpy()), f32bits(so))
+    if tr:
+        qto, sto = oracle.row_quantize(np.ascontiguousarray(bits(x).T), fmt, pow2)
+        assert np.array_equal(u8(qt), qto)
+        assert np.array_equal(f32bits(st.cpu().numpy()), f32bits(sto))

@@ -247,3 +247,40 @@ def test_block_backward_against_dequantised_matmul():
                                @ _dequant_blocks(xtq, E4M3, xts, 1).T, rtol=1e-10, atol=1e-14)
     # the transposed weight operand is the transposed cast
     assert np.array_equal(st.wt_q, wq.T) and np.array_equal(st.wt_sinv, ws.T)
+
+
+def test_row_scales_are_an_outer_product():
+    rng = np.random.default_rng(41)
+    M, N, K = 33, 47, 160
+    A, ai = _int_codes(rng, (M, K), E4M3)
+    B, bi = _int_codes(rng, (N, K), E5M2)
+    sa = (2.0 ** rng.integers(-4, 4, M)).astype(np.float32)
+    sb = (2.0 ** rng.integers(-4, 4, N)).astype(np.float32)
+    D, _ = oracle.gemm(A, E4M3, B, E5M2, sa, sb, oracle.GRAN_ROW, oracle.GRAN_ROW)
+    want = (ai @ bi.T).astype(np.float64) * np.outer(sa, sb)
+    assert np.array_equal(D, want)
+    D2, _ = oracle.gemm(A, E4M3, B, E5M2, sa, np.float32(0.5), oracle.GRAN_ROW, GRAN_TENSOR)
+    assert np.array_equal(D2, (ai @ bi.T).astype(np.float64) * sa[:, None] * 0.5)
+
+
+def test_row_scaled_linear_against_dequantised_matmul():
+    rng = np.random.default_rng(42)
+    M, N, K = 64, 48, 96
+    rec = oracle.Recipe(scaling=oracle.SCALING_ROW)
+    st = oracle.LinearState(rec)
+    X = _bits(rng.standard_normal((M, K)) * np.abs(rng.standard_t(3, (M, 1))))
+    W = _bits(rng.standard_normal((N, K)) * 0.02)
+    dY = _bits(rng.standard_normal((M, N)) * 1e-3)
+    Y, _ = oracle.linear_fwd(X, W, rec, st)
+    (dX, _), (dW, _) = oracle.linear_bwd(dY, rec, st)
+
+    def deq(bits, fmt, axis):
+        # cast with one scale per row (axis 1) or per column (axis 0), dequantised
+        src = bits if axis == 1 else np.ascontiguousarray(bits.T)
+        q, s = oracle.row_quantize(src, fmt)
+        d = oracle.decode(q, fmt) * s[:, None].astype(np.float64)
+        return d if axis == 1 else d.T
+
+    np.testing.assert_allclose(Y, deq(X, E4M3, 1) @ deq(W, E4M3, 1).T, rtol=1e-12)
+    np.testing.assert_allclose(dX, deq(dY, E5M2, 1) @ deq(W, E4M3, 0), rtol=1e-12, atol=1e-18)
+    np.testing.assert_allclose(dW, deq(dY, E5M2, 0).T @ deq(X, E4M3, 0), rtol=1e-12, atol=1e-18)

@@ -163,3 +163,17 @@ def test_block_pow2_scales_are_powers_of_two():
     _, sinv = oracle.block_quantize(bits, E4M3, 1, pow2=True)
     m, e = np.frexp(sinv)
     assert (m == 0.5).all()
+
+
+def test_row_quantize_rows_are_per_tensor_casts():
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((7, 300)).astype(np.float32) * (10.0 ** rng.integers(-3, 3, (7, 1)))
+    x[4] = 0
+    bits = _bits(x)
+    for fmt, fmax in ((E4M3, 448.0), (E5M2, 57344.0)):
+        q, sinv = oracle.row_quantize(bits, fmt)
+        for i in range(7):
+            a = oracle.amax(bits[i])
+            s = np.float32(1) if a == 0 else np.float32(fmax) / a
+            assert sinv[i] == np.float32(1) / s
+            assert np.array_equal(q[i], oracle.quantize(bits[i:i + 1], fmt, s)[0][0])
