@@ -480,8 +480,9 @@ def run_reference(args):
 def run_kernel(args):
     """Time one kernel of the path on one shape (not the headline number):
     gemm (per-tensor, E4M3 or E5M2 x E4M3, bf16 out), block_gemm (1x128 x
-    128x128 scales, bf16 out) or quantize (fused amax + cast + transpose,
-    stale scale).  L2 is flushed before every timed launch."""
+    128x128 scales, bf16 out), quantize (fused amax + cast + transpose,
+    stale scale) or quantize_sr (the same with stochastic rounding, a new
+    seed per launch).  L2 is flushed before every timed launch."""
     import scaled_fp8_linear_gb300 as F
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
@@ -521,7 +522,11 @@ def run_kernel(args):
         qt = torch.empty(C, R, dtype=torch.uint8, device=dev)
         am = torch.empty(1, dtype=torch.float32, device=dev)
         one = torch.ones(1, dtype=torch.float32, device=dev)
-        call = lambda: F.fp8_quantize(x, fa, scale=one, q=q, q_t=qt, amax_out=am)
+        if args.kernel == "quantize_sr":
+            seed = iter(range(1, 1 << 30))
+            call = lambda: F.fp8_quantize_sr(x, fa, one, next(seed), 0, q=q, q_t=qt, amax_out=am)
+        else:
+            call = lambda: F.fp8_quantize(x, fa, scale=one, q=q, q_t=qt, amax_out=am)
         work, unit, peak = 4.0 * R * C, "GB/s", hbm_gbs
     for _ in range(args.warmup):
         call()
@@ -615,7 +620,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=32)
     ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["gemm", "block_gemm", "quantize", "gemm_step"],
+    ap.add_argument("--kernel", choices=["gemm", "block_gemm", "quantize", "quantize_sr",
+                                         "gemm_step"],
                     help="time one kernel on --shape instead of the layer step")
     ap.add_argument("--shape", default="8192,12288,4096")
     ap.add_argument("--fmt", choices=["e4m3", "e5m2"], default="e4m3")

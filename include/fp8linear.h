@@ -179,6 +179,28 @@ int fp8_quantize_counted(const void* x, int64_t rows, int64_t cols, int format,
                          const float* scale, uint8_t* q, uint8_t* q_t, float* amax_out,
                          unsigned long long* counts, void* stream);
 
+/* Per-tensor cast (FP8_GRAN_TENSOR semantics of fp8_quantize: same scale,
+ * q, q_t, amax_out and shape rules) with stochastic rounding instead of
+ * round-to-nearest-even ("Mixed Precision LLM Training: The Complete
+ * Guide", "Stochastic rounding": round up or down at random, with the
+ * probability given by the remainder, so the cast is unbiased).
+ *   v = fp32(x) * scale (one fp32 multiply), lo <= |v| <= hi its two FP8
+ *   neighbours, f = (|v| - lo) / (hi - lo); the magnitude becomes hi iff
+ *   r < floor(f * 2^32), r a uniform 32-bit word, so P(hi) = f exactly
+ *   in the normal FP8 range.  Saturating to the largest finite value; NaN ->
+ *   0x7F; zeros keep their sign.
+ *   r for element i (row-major index i = row * cols + col) is word (i mod 4)
+ *   of Philox-4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers:
+ *   as easy as 1, 2, 3", SC'11) at counter (lo32(i/4), hi32(i/4),
+ *   lo32(offset), hi32(offset)) and key (lo32(seed), hi32(seed)).  The codes
+ *   depend only on (x, scale, seed, offset), not on the launch; q_t holds the
+ *   same codes as q, transposed.  Advance offset (or change seed) between
+ *   casts that need independent draws.
+ * Errors as fp8_quantize. */
+int fp8_quantize_sr(const void* x, int64_t rows, int64_t cols, int format, const float* scale,
+                    uint64_t seed, uint64_t offset, uint8_t* q, uint8_t* q_t, float* amax_out,
+                    void* stream);
+
 /* Scaled FP8 GEMM, layout FP8_LAYOUT_TN:
  *   D[m][n] = sum_k sa(m,k) * sb(n,k) * A[m][k] * B[n][k]
  * with FP32 accumulation on the tensor cores.  sa, sb are DEQUANTISATION

@@ -75,6 +75,12 @@ def lib():
                                    _i64p, _i64p, i64, _f64p, _f64p]
     L.orc_cast_counts.argtypes = [_u16p, i64, c_int, c_float,
                                   np.ctypeslib.ndpointer(dtype=np.uint64, flags="C_CONTIGUOUS")]
+    _u32p = np.ctypeslib.ndpointer(dtype=np.uint32, flags="C_CONTIGUOUS")
+    L.orc_philox4x32_10.argtypes = [_u32p, _u32p, _u32p]
+    L.orc_encode_sr.restype = ctypes.c_uint8
+    L.orc_encode_sr.argtypes = [c_float, c_int, ctypes.c_uint32]
+    L.orc_quantize_sr.argtypes = [_u16p, i64, i64, c_int, c_float, ctypes.c_uint64,
+                                  ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p]
     L.orc_num_threads.restype = c_int
     _lib = L
     return L
@@ -151,6 +157,28 @@ def quantize(x_bits, fmt: int, scale, transpose: bool = False):
     qt = np.empty((cols, rows), np.uint8) if transpose else None
     lib().orc_quantize(x, rows, cols, fmt, float(np.float32(scale)), q.ctypes.data,
                        qt.ctypes.data if transpose else None)
+    return q, qt
+
+
+def philox4x32_10(ctr, key):
+    """Philox-4x32-10 of a 4-word counter and 2-word key -> 4 uint32 words."""
+    out = np.zeros(4, np.uint32)
+    lib().orc_philox4x32_10(np.asarray(ctr, np.uint32), np.asarray(key, np.uint32), out)
+    return out
+
+
+def encode_sr(value, fmt: int, r32: int) -> int:
+    return int(lib().orc_encode_sr(float(np.float32(value)), fmt, int(r32) & 0xFFFFFFFF))
+
+
+def quantize_sr(x_bits, fmt: int, scale, seed: int, offset: int = 0, transpose: bool = False):
+    """Per-tensor cast with stochastic rounding; returns (q, q_t or None)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), np.uint8)
+    qt = np.empty((cols, rows), np.uint8) if transpose else None
+    lib().orc_quantize_sr(x, rows, cols, fmt, float(np.float32(scale)), int(seed), int(offset),
+                          q.ctypes.data, qt.ctypes.data if transpose else None)
     return q, qt
 
 

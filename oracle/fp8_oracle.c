@@ -218,6 +218,105 @@ void orc_update_scale(float amax, float* history, int32_t* pos, int H, int algo,
     *scale_inv = 1.0f / s;
 }
 
+/* ------------------------------------------------------ stochastic rounding */
+
+/* Philox-4x32-10, the counter-based generator of Salmon, Moraes, Dror and
+ * Shaw, "Parallel random numbers: as easy as 1, 2, 3" (SC'11): ten rounds of
+ *   (c0,c1,c2,c3) -> (hi(B*c2)^c1^k0, lo(B*c2), hi(A*c0)^c3^k1, lo(A*c0))
+ * with A = 0xD2511F53, B = 0xCD9E8D57, the key bumped by the Weyl constants
+ * (0x9E3779B9, 0xBB67AE85) between rounds. */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        const uint32_t n1 = (uint32_t)p1;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        const uint32_t n3 = (uint32_t)p0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* Stochastic rounding of one fp32 value onto the FP8 grid ([MP] "Stochastic
+ * rounding": round up or down at random, in proportion to the remainder):
+ * |v| = sig * 2^e2 lies between the grid points n*2^qe and (n+1)*2^qe with
+ * remainder rem = sig mod 2^shift (shift = qe - e2); the magnitude is rounded
+ * up iff r32 < floor(rem * 2^32 / 2^shift), r32 a uniform 32-bit draw, so a
+ * value rounds up with probability rem/2^shift (exactly, for shift <= 32).
+ * NaN, infinities, saturation and signed zeros as in orc_encode. */
+uint8_t orc_encode_sr(float v, int fmt, uint32_t r32)
+{
+    const int mb = (fmt == ORC_E4M3) ? 3 : 2;
+    const int bias = (fmt == ORC_E4M3) ? 7 : 15;
+    const int emin = 1 - bias;
+    const uint32_t u = f32_bits(v);
+    const uint8_t sign = (u >> 31) ? 0x80 : 0x00;
+    const uint32_t ex = (u >> 23) & 0xFF, fr = u & 0x7FFFFF;
+    if (ex == 0xFF) return fr ? 0x7F : (uint8_t)(sign | max_code(fmt));
+    if (ex == 0 && fr == 0) return sign;
+    uint64_t sig;
+    int e2;
+    if (ex == 0) { sig = fr; e2 = -149; }
+    else { sig = fr | 0x800000u; e2 = (int)ex - 150; }
+    int top = 63;
+    while (!((sig >> top) & 1u)) --top;
+    const int E = e2 + top;
+    int qe = (E > emin ? E : emin) - mb;
+    const int shift = qe - e2;                     /* >= 1 */
+    uint64_t n, threshold;
+    if (shift >= 56) {
+        n = 0;                                     /* sig < 2^24: rem * 2^32 / 2^shift < 1 */
+        threshold = 0;
+    } else {
+        n = sig >> shift;
+        const uint64_t rem = sig & ((1ull << shift) - 1);
+        threshold = shift <= 32 ? rem << (32 - shift) : rem >> (shift - 32);
+    }
+    if ((uint64_t)r32 < threshold) n += 1;
+    if (n == 0) return sign;
+    if (n == (1ull << (mb + 1))) { n >>= 1; qe += 1; }
+    if (n < (1ull << mb)) return (uint8_t)(sign | n);
+    const int field = qe + mb + bias;
+    const uint64_t man = n - (1ull << mb);
+    if (fmt == ORC_E4M3) {
+        if (field > 15 || (field == 15 && man == 7)) return (uint8_t)(sign | max_code(fmt));
+        return (uint8_t)(sign | (field << 3) | man);
+    } else {
+        if (field > 30) return (uint8_t)(sign | max_code(fmt));
+        return (uint8_t)(sign | (field << 2) | man);
+    }
+}
+
+/* Per-tensor cast with stochastic rounding: element i (row-major index) uses
+ * word (i mod 4) of Philox(counter = (lo(i/4), hi(i/4), lo(offset),
+ * hi(offset)), key = (lo(seed), hi(seed))).  q_t (nullable) = transpose. */
+void orc_quantize_sr(const uint16_t* x, int64_t rows, int64_t cols, int fmt, float scale,
+                     uint64_t seed, uint64_t offset, uint8_t* q, uint8_t* qt)
+{
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < rows; ++i) {
+        for (int64_t j = 0; j < cols; ++j) {
+            const uint64_t idx = (uint64_t)(i * cols + j);
+            const uint64_t g = idx >> 2;
+            const uint32_t ctr[4] = {(uint32_t)g, (uint32_t)(g >> 32), (uint32_t)offset,
+                                     (uint32_t)(offset >> 32)};
+            uint32_t r[4];
+            orc_philox4x32_10(ctr, key, r);
+            const float v = orc_bf16_to_f32(x[idx]) * scale;
+            const uint8_t c = orc_encode_sr(v, fmt, r[idx & 3]);
+            if (q) q[idx] = c;
+            if (qt) qt[j * rows + i] = c;
+        }
+    }
+}
+
 /* --------------------------------------------------------------- quantize */
 
 /* [MP] "Per-tensor scaling": multiply by the scale, then cast to FP8.

@@ -25,7 +25,7 @@ __all__ = [
     "SCALING_DELAYED", "SCALING_DYNAMIC", "SCALING_BLOCK", "SCALING_ROW",
     "Fp8Error", "Recipe", "LinearStateC", "Fp8Linear", "build", "lib", "library_path",
     "fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_quantize_blocks",
-    "fp8_quantize_counted", "fp8_gemm",
+    "fp8_quantize_counted", "fp8_quantize_sr", "fp8_gemm",
     "fp8_workspace_size",
     "fp8_linear_fwd", "fp8_linear_bwd", "fp8_last_error", "fp8_device_status",
 ]
@@ -101,6 +101,8 @@ def lib() -> ctypes.CDLL:
     L.fp8_update_scale.argtypes = [_vp, _vp, _vp, i, i, i, i, i, _vp, _vp, _vp]
     L.fp8_quantize.argtypes = [_vp, i64, i64, i, i, _vp, i, _vp, _vp, _vp, _vp, _vp, _vp]
     L.fp8_quantize_counted.argtypes = [_vp, i64, i64, i, _vp, _vp, _vp, _vp, _vp, _vp]
+    L.fp8_quantize_sr.argtypes = [_vp, i64, i64, i, _vp, ctypes.c_uint64, ctypes.c_uint64,
+                                  _vp, _vp, _vp, _vp]
     L.fp8_gemm.argtypes = [_vp, i, _vp, i, i64, i64, i64, i, i, _vp, i, _vp, _vp, i, i, _vp]
     L.fp8_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(Recipe)]
     L.fp8_workspace_size.restype = sz
@@ -111,7 +113,7 @@ def lib() -> ctypes.CDLL:
     L.fp8_last_error.restype = ctypes.c_char_p
     L.fp8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i]
     for name in ("fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_quantize_counted",
-                 "fp8_gemm", "fp8_linear_fwd",
+                 "fp8_quantize_sr", "fp8_gemm", "fp8_linear_fwd",
                  "fp8_linear_bwd", "fp8_device_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -240,6 +242,27 @@ def fp8_quantize_counted(x: torch.Tensor, fmt: int, scale, counts=None, q=None, 
         _ptr(q, "q", _U8), _ptr(q_t, "q_t", _U8), _ptr(amax_out, "amax_out", torch.float32),
         _ptr(counts, "counts", torch.int64), _stream(stream)))
     return q, q_t, amax_out, counts
+
+
+def fp8_quantize_sr(x: torch.Tensor, fmt: int, scale, seed: int, offset: int = 0, q=None,
+                    q_t=None, transpose: bool = False, amax_out=None, want_amax: bool = False,
+                    stream=None):
+    """Per-tensor cast with stochastic rounding (Philox-4x32-10 keyed by seed,
+    counter offset).  Returns (q, q_t or None, amax or None)."""
+    rows, cols = x.shape
+    dev = x.device
+    if q is None:
+        q = torch.empty(rows, cols, dtype=torch.uint8, device=dev)
+    if transpose and q_t is None:
+        q_t = torch.empty(cols, rows, dtype=torch.uint8, device=dev)
+    if want_amax and amax_out is None:
+        amax_out = torch.empty(1, dtype=torch.float32, device=dev)
+    _check(lib().fp8_quantize_sr(
+        _ptr(x, "x", torch.bfloat16), rows, cols, int(fmt), _ptr(scale, "scale", torch.float32),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFFFFFFFFFF,
+        _ptr(q, "q", _U8), _ptr(q_t, "q_t", _U8), _ptr(amax_out, "amax_out", torch.float32),
+        _stream(stream)))
+    return q, q_t, amax_out
 
 
 def fp8_quantize_blocks(x: torch.Tensor, fmt: int, granularity: int, pow2: bool = False,

@@ -298,6 +298,16 @@ int fp8_quantize_counted(const void* x, int64_t rows, int64_t cols, int format,
                        "fp8_quantize_counted");
 }
 
+int fp8_quantize_sr(const void* x, int64_t rows, int64_t cols, int format, const float* scale,
+                    uint64_t seed, uint64_t offset, uint8_t* q, uint8_t* q_t, float* amax_out,
+                    void* stream) {
+    FP8_CHECK(check_quantize_args(x, rows, cols, format, FP8_GRAN_TENSOR, scale, q, q_t, nullptr,
+                                  nullptr, amax_out));
+    return cuda_status(launch_quantize_sr(x, rows, cols, format, scale, seed, offset, q, q_t,
+                                          amax_out, as_stream(stream)),
+                       "fp8_quantize_sr");
+}
+
 int fp8_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N, int64_t K,
              int layout, int ga, const float* scale_inv_a, int gb, const float* scale_inv_b,
              void* D, int out, int accumulate, void* stream) {

@@ -31,6 +31,13 @@ cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, in
                                    const float* scale, uint8_t* q, uint8_t* q_t, float* amax,
                                    cudaStream_t stream, unsigned long long* counts = nullptr);
 
+// Per-tensor cast of launch_quantize_tensor with stochastic rounding: element
+// i (row-major) draws word i % 4 of Philox-4x32-10(counter = (i / 4, offset),
+// key = seed).
+cudaError_t launch_quantize_sr(const void* x, int64_t rows, int64_t cols, int fmt,
+                               const float* scale, uint64_t seed, uint64_t offset, uint8_t* q,
+                               uint8_t* q_t, float* amax, cudaStream_t stream);
+
 // Block cast: gran 1 (1x128) or 2 (128x128); writes q and 1/scale per block.
 // q_t (nullable, rows % 128 == 0): gran 1 -> the 1x128 block cast of x^T with
 // scale_inv_t [cols][rows/128]; gran 2 -> the transposed codes with the

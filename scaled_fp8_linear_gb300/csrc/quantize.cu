@@ -108,6 +108,134 @@ __device__ __forceinline__ void cta_counts_commit(const CastCounts& c, unsigned 
     }
 }
 
+// ------------------------------------------------------ stochastic rounding
+//
+// "Mixed Precision LLM Training: The Complete Guide", "Stochastic rounding":
+// round up or down at random with the probability set by the remainder, so
+// the cast is unbiased.  The random bits come from Philox-4x32-10 (Salmon et
+// al., "Parallel random numbers: as easy as 1, 2, 3", SC'11), a counter-based
+// generator: element i of a row-major tensor takes word (i mod 4) of
+// Philox(counter = (i/4, offset), key = seed), so any thread can draw any
+// element's bits without state and the result does not depend on the launch.
+
+struct SrKey {
+    uint32_t k0, k1, o0, o1;  // key (seed) and the upper counter words (offset)
+};
+
+// The key schedule (the key of each of the ten rounds), computed once per
+// thread, and the offset words.
+struct SrSched {
+    uint32_t k0[10], k1[10], o0, o1;
+};
+
+__device__ __forceinline__ SrSched sr_sched(const SrKey& k) {
+    SrSched s;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        s.k0[r] = k.k0 + static_cast<uint32_t>(r) * 0x9E3779B9u;
+        s.k1[r] = k.k1 + static_cast<uint32_t>(r) * 0xBB67AE85u;
+    }
+    s.o0 = k.o0;
+    s.o1 = k.o1;
+    return s;
+}
+
+// Philox-4x32-10 of counter (lo32(group), hi32(group), o0, o1): ten rounds
+// of two 32 x 32 -> 64-bit products (multipliers 0xD2511F53, 0xCD9E8D57)
+// whose halves are crossed and XORed with the other counter words and the
+// round key.
+__device__ __forceinline__ uint4 sr_bits(const SrSched& k, uint64_t group) {
+    uint4 c = make_uint4(static_cast<uint32_t>(group), static_cast<uint32_t>(group >> 32), k.o0, k.o1);
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t lo0 = c.x * 0xD2511F53u, hi0 = __umulhi(c.x, 0xD2511F53u);
+        const uint32_t lo1 = c.z * 0xCD9E8D57u, hi1 = __umulhi(c.z, 0xCD9E8D57u);
+        c = make_uint4(hi1 ^ c.y ^ k.k0[r], lo1, hi0 ^ c.w ^ k.k1[r], lo0);
+    }
+    return c;
+}
+
+// Stochastic rounding of one fp32 value onto the FP8 grid, driven by the
+// uniform 32-bit word r.  With f the remainder below the FP8 grid spacing as
+// a fraction of that spacing, the magnitude rounds up iff r < floor(f * 2^32).
+// The decision is taken by adding ~r (= 2^32 - 1 - r), aligned below the
+// kept bits, and truncating: the sum carries into the kept bits exactly when
+// r < floor(f * 2^32).  The result is an fp32 value that lies on the FP8 grid
+// (or is beyond the largest finite value, +-Inf or NaN), so the saturating
+// round-to-nearest conversion that follows is exact.
+//  * normal FP8 range, finite: f has 20 (E4M3) or 21 (E5M2) bits, so the add
+//    acts on the fp32 bit pattern itself (a mantissa overflow carries into
+//    the exponent, never into the sign) and the low bits are then cleared;
+//  * below the smallest normal: the 24-bit significand, shifted to fixed
+//    point with 32 fraction bits on the subnormal grid, plus ~r, gives the
+//    number of grid steps;
+//  * +-Inf and NaN pass through (the conversion saturates / yields NaN).
+template <int FMT>
+__device__ __forceinline__ float sr_round(float v, uint32_t r) {
+    constexpr int kMant = FMT == 0 ? 3 : 2, kBias = FMT == 0 ? 7 : 15, kEmin = 1 - kBias;
+    constexpr int kShift = 23 - kMant;
+    constexpr uint32_t kNormMin = static_cast<uint32_t>(127 + kEmin) << 23;   // 2^emin
+    constexpr uint32_t kLow = (1u << kShift) - 1u;
+    const uint32_t u = __float_as_uint(v), a = u & 0x7FFFFFFFu;
+    if (a - kNormMin < 0x7F800000u - kNormMin)                 // normal range, finite
+        return __uint_as_float((u + (kLow - (r >> (32 - kShift)))) & ~kLow);
+    if (a >= 0x7F800000u) return v;
+    const uint32_t ex = a >> 23;
+    const uint32_t sig = ex ? ((a & 0x7FFFFFu) | 0x800000u) : a;
+    // grid exponent minus the significand's exponent: >= 24 - kMant
+    const int sh = min(kEmin - kMant + 150 - static_cast<int>(max(ex, 1u)), 63);
+    const uint64_t t = (static_cast<uint64_t>(sig) << 32) >> sh;
+    const uint32_t steps = static_cast<uint32_t>((t + static_cast<uint64_t>(~r)) >> 32);
+    const float m = __fmul_rn(__uint2float_rn(steps), __uint_as_float(static_cast<uint32_t>(127 + kEmin - kMant) << 23));
+    return __uint_as_float(__float_as_uint(m) | (u & 0x80000000u));
+}
+
+// One fp32 value to its stochastically rounded FP8 code.
+template <int FMT>
+__device__ __forceinline__ uint32_t sr_code(float v, uint32_t r) {
+    const float t = sr_round<FMT>(v, r);
+    return static_cast<uint32_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(t, 0.0f), __NV_SATFINITE, Fp8Traits<FMT>::kind)) & 0xFFu;
+}
+
+// Four consecutive bf16 (two words) times s to four codes, stochastically
+// rounded with the four words of r.
+template <int FMT>
+__device__ __forceinline__ uint32_t sr4(uint32_t w0, uint32_t w1, float s, uint4 r) {
+    const float t0 = sr_round<FMT>(__fmul_rn(__uint_as_float(w0 << 16), s), r.x);
+    const float t1 = sr_round<FMT>(__fmul_rn(__uint_as_float(w0 & 0xFFFF0000u), s), r.y);
+    const float t2 = sr_round<FMT>(__fmul_rn(__uint_as_float(w1 << 16), s), r.z);
+    const float t3 = sr_round<FMT>(__fmul_rn(__uint_as_float(w1 & 0xFFFF0000u), s), r.w);
+    const uint32_t lo = static_cast<uint32_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(t0, t1), __NV_SATFINITE, Fp8Traits<FMT>::kind));
+    const uint32_t hi = static_cast<uint32_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(t2, t3), __NV_SATFINITE, Fp8Traits<FMT>::kind));
+    return lo | (hi << 16);
+}
+
+// The four codes of elements 4*group .. 4*group+3: round to nearest even
+// (with or without counters) or, with SR, stochastically.
+template <int FMT, bool COUNT, bool SR>
+__device__ __forceinline__ uint32_t cast4(uint32_t w0, uint32_t w1, float s, CastCounts& c,
+                                          const SrSched& k, uint64_t group) {
+    if constexpr (SR) {
+        static_assert(!COUNT, "stochastic rounding has no counters");
+        return sr4<FMT>(w0, w1, s, sr_bits(k, group));
+    } else {
+        return cvt4x<FMT, COUNT>(w0, w1, s, c);
+    }
+}
+
+// 16 consecutive bf16 (two 16-byte vectors) starting at element 16*v.
+template <int FMT, bool COUNT, bool SR>
+__device__ __forceinline__ uint4 cast16(const uint4& a, const uint4& b, float s, CastCounts& c,
+                                        const SrSched& k, uint64_t v) {
+    return make_uint4(cast4<FMT, COUNT, SR>(a.x, a.y, s, c, k, 4 * v),
+                      cast4<FMT, COUNT, SR>(a.z, a.w, s, c, k, 4 * v + 1),
+                      cast4<FMT, COUNT, SR>(b.x, b.y, s, c, k, 4 * v + 2),
+                      cast4<FMT, COUNT, SR>(b.z, b.w, s, c, k, 4 * v + 3));
+}
+
 // Running per-halfword max of |bf16| bit patterns.
 __device__ __forceinline__ uint32_t absmax2(uint32_t m, uint32_t w) {
     return __vmaxu2(m, w & 0x7FFF7FFFu);
@@ -232,13 +360,14 @@ __global__ void update_scale_kernel(const float* __restrict__ amax, float* __res
 // ------------------------------------------------------- per-tensor cast
 
 // Flat cast, 16 elements (32 B in, 16 B out) per thread per step.
-template <int FMT, bool AMAX, bool COUNT>
+template <int FMT, bool AMAX, bool COUNT, bool SR>
 __global__ void __launch_bounds__(kThreads)
     quantize_flat_kernel(const uint4* __restrict__ x, int64_t n16, const uint16_t* __restrict__ xt,
                          int tail_n, const float* __restrict__ scale_p, uint4* __restrict__ q,
                          uint8_t* __restrict__ qtail, unsigned* amax_bits,
-                         unsigned long long* counts) {
+                         unsigned long long* counts, SrKey sr_key) {
     const float s = *scale_p;
+    const SrSched key = sr_sched(sr_key);
     uint32_t m = 0;
     CastCounts cc;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -247,21 +376,27 @@ __global__ void __launch_bounds__(kThreads)
         const uint4 a0 = ldg_stream(x + 2 * i), b0 = ldg_stream(x + 2 * i + 1);
         const uint4 a1 = ldg_stream(x + 2 * (i + stride)), b1 = ldg_stream(x + 2 * (i + stride) + 1);
         if (AMAX) m = absmax_vec(absmax_vec(absmax_vec(absmax_vec(m, a0), b0), a1), b1);
-        q[i] = make_uint4(cvt4x<FMT, COUNT>(a0.x, a0.y, s, cc), cvt4x<FMT, COUNT>(a0.z, a0.w, s, cc),
-                          cvt4x<FMT, COUNT>(b0.x, b0.y, s, cc), cvt4x<FMT, COUNT>(b0.z, b0.w, s, cc));
-        q[i + stride] = make_uint4(cvt4x<FMT, COUNT>(a1.x, a1.y, s, cc), cvt4x<FMT, COUNT>(a1.z, a1.w, s, cc),
-                                   cvt4x<FMT, COUNT>(b1.x, b1.y, s, cc), cvt4x<FMT, COUNT>(b1.z, b1.w, s, cc));
+        q[i] = cast16<FMT, COUNT, SR>(a0, b0, s, cc, key, i);
+        q[i + stride] = cast16<FMT, COUNT, SR>(a1, b1, s, cc, key, i + stride);
     }
     for (; i < n16; i += stride) {
         const uint4 a = ldg_stream(x + 2 * i), b = ldg_stream(x + 2 * i + 1);
         if (AMAX) m = absmax_vec(absmax_vec(m, a), b);
-        q[i] = make_uint4(cvt4x<FMT, COUNT>(a.x, a.y, s, cc), cvt4x<FMT, COUNT>(a.z, a.w, s, cc), cvt4x<FMT, COUNT>(b.x, b.y, s, cc),
-                          cvt4x<FMT, COUNT>(b.z, b.w, s, cc));
+        q[i] = cast16<FMT, COUNT, SR>(a, b, s, cc, key, i);
     }
     if (blockIdx.x == 0 && threadIdx.x < tail_n) {
         const uint32_t w = xt[threadIdx.x];
         if (AMAX) m = max(m, w & 0x7FFFu);
-        qtail[threadIdx.x] = static_cast<uint8_t>((COUNT ? cvt2c<FMT>(w & 0xFFFFu, s, cc) : cvt2<FMT>(w, s)) & 0xFFu);
+        uint32_t code;
+        if constexpr (SR) {
+            const uint64_t e = static_cast<uint64_t>(n16) * 16 + threadIdx.x;
+            const uint4 r = sr_bits(key, e >> 2);
+            const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+            code = sr_code<FMT>(__fmul_rn(__uint_as_float(w << 16), s), rw[e & 3]);
+        } else {
+            code = COUNT ? cvt2c<FMT>(w & 0xFFFFu, s, cc) : cvt2<FMT>(w, s);
+        }
+        qtail[threadIdx.x] = static_cast<uint8_t>(code & 0xFFu);
     }
     if (AMAX) cta_amax_commit(m, amax_bits);
     if (COUNT) cta_counts_commit(cc, counts);
@@ -309,13 +444,14 @@ __device__ __forceinline__ void transpose_tile_out(const uint32_t* S, uint8_t* _
     }
 }
 
-template <int FMT, bool AMAX, bool COUNT>
+template <int FMT, bool AMAX, bool COUNT, bool SR>
 __global__ void __launch_bounds__(kThreads)
     quantize_transpose_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
                               int64_t tiles_c, const float* __restrict__ scale_p,
                               uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
-                              unsigned* amax_bits, unsigned long long* counts) {
+                              unsigned* amax_bits, unsigned long long* counts, SrKey sr_key) {
     CastCounts cc;
+    const SrSched key = sr_sched(sr_key);
     __shared__ __align__(16) uint32_t S[128 * 32];
     const int64_t tile = blockIdx.x;
     const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
@@ -324,6 +460,29 @@ __global__ void __launch_bounds__(kThreads)
     uint32_t m = 0;
 
     const int cg = t & 7;
+    if constexpr (SR) {
+        // stochastic rounding is ALU-heavy (one Philox call per 4 elements):
+        // a rolled loop keeps the code small, and the arithmetic of one row
+        // segment hides the latency of the next one's loads
+#pragma unroll 1
+        for (int it = 0; it < 4; ++it) {
+            const int rl = it * 32 + (t >> 3);
+            const int64_t r = r0 + rl, c = c0 + cg * 16;
+            uint4 out = make_uint4(0u, 0u, 0u, 0u);
+            if (r < rows && c < cols) {
+                const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + c);
+                const uint4 a = ldg_stream(src), b = ldg_stream(src + 1);
+                if (AMAX) m = absmax_vec(absmax_vec(m, a), b);
+                out = cast16<FMT, COUNT, SR>(a, b, s, cc, key, static_cast<uint64_t>(r * cols + c) >> 4);
+                *reinterpret_cast<uint4*>(q + r * cols + c) = out;
+            }
+            *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = out;
+        }
+        __syncthreads();
+        transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
+        if (AMAX) cta_amax_commit(m, amax_bits);
+        return;
+    }
     // all of this thread's loads first (8 x 16 B in flight), then cast and store
     uint4 va[4], vb[4];
 #pragma unroll
@@ -344,8 +503,8 @@ __global__ void __launch_bounds__(kThreads)
         uint4 out = make_uint4(0u, 0u, 0u, 0u);
         if (r < rows && c < cols) {
             if (AMAX) m = absmax_vec(absmax_vec(m, a), b);
-            out = make_uint4(cvt4x<FMT, COUNT>(a.x, a.y, s, cc), cvt4x<FMT, COUNT>(a.z, a.w, s, cc),
-                             cvt4x<FMT, COUNT>(b.x, b.y, s, cc), cvt4x<FMT, COUNT>(b.z, b.w, s, cc));
+            // cols % 16 == 0: the 16 elements are vector (r * cols + c) / 16
+            out = cast16<FMT, COUNT, SR>(a, b, s, cc, key, static_cast<uint64_t>(r * cols + c) >> 4);
             *reinterpret_cast<uint4*>(q + r * cols + c) = out;
         }
         *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = out;
@@ -658,42 +817,49 @@ cudaError_t launch_update_scale(const float* amax, float* history, int32_t* pos,
     return cudaGetLastError();
 }
 
-template <int FMT, bool AMAX, bool COUNT>
+template <int FMT, bool AMAX, bool COUNT, bool SR>
 static void launch_flat(const void* x, int64_t n, const float* scale, uint8_t* q, float* amax,
-                        unsigned long long* counts, cudaStream_t stream) {
+                        unsigned long long* counts, const SrKey& key, cudaStream_t stream) {
     const int64_t n16 = n / 16;
     const int tail_n = static_cast<int>(n - n16 * 16);
-    quantize_flat_kernel<FMT, AMAX, COUNT><<<grid_for(n16 + 1, kThreads * 2), kThreads, 0, stream>>>(
+    quantize_flat_kernel<FMT, AMAX, COUNT, SR><<<grid_for(n16 + 1, kThreads * 2), kThreads, 0, stream>>>(
         static_cast<const uint4*>(x), n16, static_cast<const uint16_t*>(x) + n16 * 16, tail_n,
-        scale, reinterpret_cast<uint4*>(q), q + n16 * 16, reinterpret_cast<unsigned*>(amax), counts);
+        scale, reinterpret_cast<uint4*>(q), q + n16 * 16, reinterpret_cast<unsigned*>(amax), counts,
+        key);
 }
 
-template <int FMT, bool AMAX, bool COUNT>
+template <int FMT, bool AMAX, bool COUNT, bool SR>
 static void launch_transpose(const void* x, int64_t rows, int64_t cols, const float* scale,
                              uint8_t* q, uint8_t* qt, float* amax, unsigned long long* counts,
-                             cudaStream_t stream) {
+                             const SrKey& key, cudaStream_t stream) {
     const int64_t tiles_c = (cols + 127) / 128, tiles_r = (rows + 127) / 128;
-    quantize_transpose_kernel<FMT, AMAX, COUNT><<<static_cast<unsigned>(tiles_r * tiles_c), kThreads,
-                                                  0, stream>>>(
+    quantize_transpose_kernel<FMT, AMAX, COUNT, SR><<<static_cast<unsigned>(tiles_r * tiles_c),
+                                                      kThreads, 0, stream>>>(
         static_cast<const uint16_t*>(x), rows, cols, tiles_c, scale, q, qt,
-        reinterpret_cast<unsigned*>(amax), counts);
+        reinterpret_cast<unsigned*>(amax), counts, key);
 }
 
-template <int FMT, bool AMAX>
+template <int FMT, bool AMAX, bool SR>
 static void launch_cast(const void* x, int64_t rows, int64_t cols, const float* scale, uint8_t* q,
-                        uint8_t* q_t, float* amax, unsigned long long* counts, cudaStream_t stream) {
-    if (q_t) {
-        if (counts) launch_transpose<FMT, AMAX, true>(x, rows, cols, scale, q, q_t, amax, counts, stream);
-        else launch_transpose<FMT, AMAX, false>(x, rows, cols, scale, q, q_t, amax, counts, stream);
+                        uint8_t* q_t, float* amax, unsigned long long* counts, const SrKey& key,
+                        cudaStream_t stream) {
+    if constexpr (SR) {
+        if (q_t) launch_transpose<FMT, AMAX, false, true>(x, rows, cols, scale, q, q_t, amax, nullptr, key, stream);
+        else launch_flat<FMT, AMAX, false, true>(x, rows * cols, scale, q, amax, nullptr, key, stream);
+    } else if (q_t) {
+        if (counts) launch_transpose<FMT, AMAX, true, false>(x, rows, cols, scale, q, q_t, amax, counts, key, stream);
+        else launch_transpose<FMT, AMAX, false, false>(x, rows, cols, scale, q, q_t, amax, counts, key, stream);
     } else {
-        if (counts) launch_flat<FMT, AMAX, true>(x, rows * cols, scale, q, amax, counts, stream);
-        else launch_flat<FMT, AMAX, false>(x, rows * cols, scale, q, amax, counts, stream);
+        if (counts) launch_flat<FMT, AMAX, true, false>(x, rows * cols, scale, q, amax, counts, key, stream);
+        else launch_flat<FMT, AMAX, false, false>(x, rows * cols, scale, q, amax, counts, key, stream);
     }
 }
 
-cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, int fmt,
+template <bool SR>
+static cudaError_t quantize_tensor(const void* x, int64_t rows, int64_t cols, int fmt,
                                    const float* scale, uint8_t* q, uint8_t* q_t, float* amax,
-                                   cudaStream_t stream, unsigned long long* counts) {
+                                   unsigned long long* counts, const SrKey& key,
+                                   cudaStream_t stream) {
     const int64_t n = rows * cols;
     if (amax) {
         cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), stream);
@@ -702,13 +868,28 @@ cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, in
     if (n == 0) return cudaSuccess;
     const bool A = amax != nullptr;
     if (fmt == 0) {
-        if (A) launch_cast<0, true>(x, rows, cols, scale, q, q_t, amax, counts, stream);
-        else launch_cast<0, false>(x, rows, cols, scale, q, q_t, amax, counts, stream);
+        if (A) launch_cast<0, true, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream);
+        else launch_cast<0, false, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream);
     } else {
-        if (A) launch_cast<1, true>(x, rows, cols, scale, q, q_t, amax, counts, stream);
-        else launch_cast<1, false>(x, rows, cols, scale, q, q_t, amax, counts, stream);
+        if (A) launch_cast<1, true, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream);
+        else launch_cast<1, false, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream);
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, int fmt,
+                                   const float* scale, uint8_t* q, uint8_t* q_t, float* amax,
+                                   cudaStream_t stream, unsigned long long* counts) {
+    return quantize_tensor<false>(x, rows, cols, fmt, scale, q, q_t, amax, counts, SrKey{},
+                                  stream);
+}
+
+cudaError_t launch_quantize_sr(const void* x, int64_t rows, int64_t cols, int fmt,
+                               const float* scale, uint64_t seed, uint64_t offset, uint8_t* q,
+                               uint8_t* q_t, float* amax, cudaStream_t stream) {
+    const SrKey key{static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32),
+                    static_cast<uint32_t>(offset), static_cast<uint32_t>(offset >> 32)};
+    return quantize_tensor<true>(x, rows, cols, fmt, scale, q, q_t, amax, nullptr, key, stream);
 }
 
 template <int FMT>

@@ -116,3 +116,16 @@ def test_quantize_counted_argument_checks():
     assert L.fp8_quantize_counted(p, 4, 4, 0, p, p, None, None, None, None) == -1     # no counts
     assert L.fp8_quantize_counted(p, 4, 4, 0, None, p, None, None, p, None) == -1     # no scale
     assert L.fp8_quantize_counted(p, 4, 4, 0, p, p, None, None, ctypes.c_void_p(FAKE + 4), None) == -3
+
+
+def test_quantize_sr_argument_checks():
+    L = F.lib()
+    p = ctypes.c_void_p(FAKE)
+    # (x, rows, cols, fmt, scale, seed, offset, q, q_t, amax, stream)
+    assert L.fp8_quantize_sr(p, 4, 4, 0, None, 1, 0, p, None, None, None) == -1       # no scale
+    assert L.fp8_quantize_sr(p, 4, 4, 2, p, 1, 0, p, None, None, None) == -1          # format
+    assert L.fp8_quantize_sr(None, 4, 4, 0, p, 1, 0, p, None, None, None) == -1      # no x
+    assert L.fp8_quantize_sr(p, -1, 4, 0, p, 1, 0, p, None, None, None) == -2         # shape
+    assert L.fp8_quantize_sr(p, 4, 24, 0, p, 1, 0, p, p, None, None) == -2            # q_t needs %16
+    assert L.fp8_quantize_sr(ctypes.c_void_p(FAKE + 2), 4, 4, 0, p, 1, 0, p, None, None, None) == -3
+    assert "fp8_quantize" in F.fp8_last_error()
