@@ -215,6 +215,10 @@ int fp8_quantize_sr(const void* x, int64_t rows, int64_t cols, int format, const
  * with block scales (FP8_ERR_UNSUPPORTED).
  * Per-tensor factors multiply the FP32 result once; block factors scale each
  * 128-deep partial sum before it is added ("applied during the matmul").
+ * bias (nullable): bf16 [N], 16-byte aligned, added in FP32 to every row of
+ * the scaled result before the output rounding (te.Linear's bias, "Mixed
+ * Precision LLM Training: The Complete Guide", "Transformer Engine
+ * internals"): D[m][n] = fp32(factors * acc[m][n]) + bias[n].
  * out FP8_OUT_BF16: D is bf16 [M x N], rounded to nearest even.
  * out FP8_OUT_F32:  D is fp32 [M x N]; accumulate != 0 adds to D.
  * Shape rule: M >= 0; N, K multiples of 16 (multiples of 128 when either
@@ -222,13 +226,18 @@ int fp8_quantize_sr(const void* x, int64_t rows, int64_t cols, int format, const
  * fa, fb: FP8_E4M3 / FP8_E5M2 in any combination. */
 int fp8_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
              int64_t K, int layout, int ga, const float* scale_inv_a, int gb,
-             const float* scale_inv_b, void* D, int out, int accumulate, void* stream);
+             const float* scale_inv_b, const void* bias, void* D, int out, int accumulate,
+             void* stream);
 
-/* Bytes of workspace that fp8_linear_fwd / fp8_linear_bwd need for a layer
- * of this shape and recipe (0 if none).  Returns 0 for an invalid recipe. */
+/* Bytes of workspace that fp8_linear_bwd needs for a layer of this shape
+ * and recipe: the quantised dY operands (and their scale arrays), plus
+ * 4*ceil(M/128)*N bytes for the bias gradient's partial sums, which only a
+ * call with dbias uses.  fp8_linear_fwd needs none.  Returns 0 for an
+ * invalid recipe. */
 size_t fp8_workspace_size(int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe);
 
-/* Forward pass Y [M x N] (bf16) = X [M x K] . W [N x K]^T.
+/* Forward pass Y [M x N] (bf16) = X [M x K] . W [N x K]^T (+ bias [N], bf16,
+ * nullable, 16-byte aligned, added in the GEMM epilogue in FP32).
  *   delayed: quantise X and W with the current scales (fusing their amax and
  *            transposes), GEMM, then update the X and W scales (the new
  *            scales take effect on the next call: one-step lag);
@@ -245,9 +254,9 @@ size_t fp8_workspace_size(int64_t M, int64_t N, int64_t K, const fp8_recipe_t* r
  * Writes state->x_q/x_qt/w_q/w_qt (and the block scale arrays) for the
  * backward pass.  Shape rule: M, N, K multiples of 16 (N, K multiples of 128
  * for block). */
-int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K,
-                   const fp8_recipe_t* recipe, const fp8_linear_state_t* state, void* Y,
-                   void* workspace, size_t workspace_bytes, void* stream);
+int fp8_linear_fwd(const void* X, const void* W, const void* bias, int64_t M, int64_t N,
+                   int64_t K, const fp8_recipe_t* recipe, const fp8_linear_state_t* state,
+                   void* Y, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Backward pass after fp8_linear_fwd on the same state:
  *   dX [M x K] (bf16) = dY . W,   dW [N x K] (fp32) = dY^T . X  (+ dW if
@@ -263,11 +272,18 @@ int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K
  *   M % 128 == 0.  Workspace: 2*M*N code bytes + 8*M*N/128 scale bytes.
  * Per-row scaling: dY is cast per token (dgrad, with W^T's per-input-channel
  *   cast) and per output channel (dY^T, wgrad, with X^T's per-input-channel
- *   cast); workspace 2*M*N code bytes + 4*(M+N) scale bytes. */
+ *   cast); workspace 2*M*N code bytes + 4*(M+N) scale bytes.
+ * dbias (nullable, fp32 [N], 4-byte aligned): the bias gradient, the column
+ *   sums of dY, dbias[n] = sum_m dY[m][n] (+ dbias[n] if accumulate_dW),
+ *   summed in FP32 in a fixed order (per 128-token tile, then over the
+ *   tiles), so repeated calls give identical bits.  With per-tensor scaling
+ *   the tile sums come out of the dY cast's own pass; the block-wise and
+ *   per-row modes read dY once more.  Needs the partial-sum part of
+ *   fp8_workspace_size(). */
 int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K,
                    const fp8_recipe_t* recipe, const fp8_linear_state_t* state, void* dX,
-                   float* dW, int accumulate_dW, void* workspace, size_t workspace_bytes,
-                   void* stream);
+                   float* dW, int accumulate_dW, float* dbias, void* workspace,
+                   size_t workspace_bytes, void* stream);
 
 /* Size of the built-in device scratch of fp8_linear_bwd_noalloc: 32 MiB. */
 #define FP8_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
@@ -278,11 +294,12 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K,
  * that must avoid cudaMalloc's implicit synchronisation, or a process whose
  * caching allocator has reserved almost all device memory.  (The pages have
  * no counterpart: this is a property of the library, not of the method.)
- * Same arguments and results as fp8_linear_bwd, minus the workspace: the
+ * Same arguments and results as fp8_linear_bwd, minus the workspace and the
+ * bias gradient (dbias = NULL): the
  * quantised gradient and its transpose go to a fixed device array of
  * FP8_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
- * the library holds until the process exits.  Shapes whose
- * fp8_workspace_size() exceeds it (2*M*N > 32 MiB, e.g. more than 4096 x
+ * the library holds until the process exits.  Shapes whose dY operands
+ * exceed it (2*M*N > 32 MiB with per-tensor scaling, e.g. more than 4096 x
  * 4096) are rejected with FP8_ERR_SHAPE and a message naming the limit.
  * Calls no allocating routine.  The first call on each device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current;

@@ -218,9 +218,17 @@ def _f32(a):
     return np.ascontiguousarray(np.asarray(a, dtype=np.float32).reshape(-1))
 
 
-def gemm(A, fa: int, B, fb: int, sa, sb, ga: int = GRAN_TENSOR, gb: int = GRAN_TENSOR):
+def _bias64(bias_bits):
+    """A bf16 bias vector (bit patterns) as exact fp64 values."""
+    return bf16_to_f32(np.ascontiguousarray(bias_bits, dtype=np.uint16)).astype(np.float64)
+
+
+def gemm(A, fa: int, B, fb: int, sa, sb, ga: int = GRAN_TENSOR, gb: int = GRAN_TENSOR,
+         bias=None):
     """D = A . B^T with dequantisation factors; A [M,K], B [N,K] FP8 codes.
-    Returns (D, Dabs) in fp64, unrounded."""
+    bias (bf16 bits [N], optional) is added to every row ("Transformer Engine
+    internals": te.Linear's bias).  Returns (D, Dabs) in fp64, unrounded;
+    Dabs is the sum of |products| that bounds the GEMM's rounding."""
     A = np.ascontiguousarray(A, dtype=np.uint8)
     B = np.ascontiguousarray(B, dtype=np.uint8)
     M, K = A.shape
@@ -229,7 +237,17 @@ def gemm(A, fa: int, B, fb: int, sa, sb, ga: int = GRAN_TENSOR, gb: int = GRAN_T
     D = np.empty((M, N), np.float64)
     Dabs = np.empty((M, N), np.float64)
     lib().orc_gemm(A, fa, B, fb, M, N, K, ga, _f32(sa), gb, _f32(sb), D, Dabs)
+    if bias is not None:
+        D = D + _bias64(bias)[None, :]
     return D, Dabs
+
+
+def dbias(dY_bits):
+    """Bias gradient: the column sums of dY [M x N] (the bias is added to
+    every row, so its gradient sums the rows).  Returns (sum, sum of |.|) in
+    fp64 over the exact bf16 values."""
+    v = bf16_to_f32(np.ascontiguousarray(dY_bits, dtype=np.uint16)).astype(np.float64)
+    return v.sum(axis=0), np.abs(v).sum(axis=0)
 
 
 def gemm_entries(A, fa: int, B, fb: int, sa, sb, ii, jj, ga: int = GRAN_TENSOR,
@@ -291,8 +309,16 @@ def _per_tensor_operand(st: LinearState, role: int, x_bits, fmt: int, recipe: Re
     return q, qt, sinv
 
 
-def linear_fwd(X_bits, W_bits, recipe: Recipe, st: LinearState, rows=None):
-    """Y = X . W^T.  Returns (Y, Yabs) fp64 (all rows, or the listed rows)."""
+def linear_fwd(X_bits, W_bits, recipe: Recipe, st: LinearState, rows=None, bias=None):
+    """Y = X . W^T (+ bias, bf16 bits [N]).  Returns (Y, Yabs) fp64 (all
+    rows, or the listed rows)."""
+    Y, Yabs = _linear_fwd(X_bits, W_bits, recipe, st, rows)
+    if bias is not None:
+        Y = Y + _bias64(bias)[None, :]
+    return Y, Yabs
+
+
+def _linear_fwd(X_bits, W_bits, recipe: Recipe, st: LinearState, rows):
     if recipe.scaling == SCALING_ROW:
         # per-token scales for X, per-output-channel scales for W; the
         # backward operands are the per-row casts of X^T and W^T (per-column

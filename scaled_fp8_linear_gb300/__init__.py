@@ -103,13 +103,13 @@ def lib() -> ctypes.CDLL:
     L.fp8_quantize_counted.argtypes = [_vp, i64, i64, i, _vp, _vp, _vp, _vp, _vp, _vp]
     L.fp8_quantize_sr.argtypes = [_vp, i64, i64, i, _vp, ctypes.c_uint64, ctypes.c_uint64,
                                   _vp, _vp, _vp, _vp]
-    L.fp8_gemm.argtypes = [_vp, i, _vp, i, i64, i64, i64, i, i, _vp, i, _vp, _vp, i, i, _vp]
+    L.fp8_gemm.argtypes = [_vp, i, _vp, i, i64, i64, i64, i, i, _vp, i, _vp, _vp, _vp, i, i, _vp]
     L.fp8_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(Recipe)]
     L.fp8_workspace_size.restype = sz
-    L.fp8_linear_fwd.argtypes = [_vp, _vp, i64, i64, i64, ctypes.POINTER(Recipe),
+    L.fp8_linear_fwd.argtypes = [_vp, _vp, _vp, i64, i64, i64, ctypes.POINTER(Recipe),
                                  ctypes.POINTER(LinearStateC), _vp, _vp, sz, _vp]
     L.fp8_linear_bwd.argtypes = [_vp, i64, i64, i64, ctypes.POINTER(Recipe),
-                                 ctypes.POINTER(LinearStateC), _vp, _vp, i, _vp, sz, _vp]
+                                 ctypes.POINTER(LinearStateC), _vp, _vp, i, _vp, _vp, sz, _vp]
     L.fp8_last_error.restype = ctypes.c_char_p
     L.fp8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i]
     for name in ("fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_quantize_counted",
@@ -281,8 +281,10 @@ def fp8_quantize_blocks(x: torch.Tensor, fmt: int, granularity: int, pow2: bool 
 
 def fp8_gemm(A: torch.Tensor, fa: int, B: torch.Tensor, fb: int, scale_inv_a, scale_inv_b,
              ga: int = GRAN_TENSOR, gb: int = GRAN_TENSOR, out: int = OUT_BF16, D=None,
-             accumulate: bool = False, layout: int = LAYOUT_TN, stream=None) -> torch.Tensor:
-    """D = (A . B^T) with dequantisation factors; A [M,K], B [N,K] FP8 codes."""
+             accumulate: bool = False, layout: int = LAYOUT_TN, stream=None,
+             bias=None) -> torch.Tensor:
+    """D = (A . B^T) with dequantisation factors (+ bias [N], bf16); A [M,K],
+    B [N,K] FP8 codes."""
     M, K = A.shape
     N = B.shape[0]
     if B.shape[1] != K:
@@ -293,7 +295,7 @@ def fp8_gemm(A: torch.Tensor, fa: int, B: torch.Tensor, fb: int, scale_inv_a, sc
     _check(lib().fp8_gemm(
         _ptr(A, "A", _U8), int(fa), _ptr(B, "B", _U8), int(fb), M, N, K, int(layout), int(ga),
         _ptr(scale_inv_a, "scale_inv_a", torch.float32), int(gb),
-        _ptr(scale_inv_b, "scale_inv_b", torch.float32),
+        _ptr(scale_inv_b, "scale_inv_b", torch.float32), _ptr(bias, "bias", torch.bfloat16),
         _ptr(D, "D", torch.bfloat16 if out == OUT_BF16 else torch.float32), int(out),
         int(bool(accumulate)), _stream(stream)))
     return D
@@ -304,21 +306,23 @@ def fp8_workspace_size(M: int, N: int, K: int, recipe: Recipe) -> int:
 
 
 def fp8_linear_fwd(X, W, recipe: Recipe, state: "LinearStateC", Y, workspace=None,
-                   stream=None) -> None:
+                   stream=None, bias=None) -> None:
     M, K = X.shape
     N = W.shape[0]
     _check(lib().fp8_linear_fwd(
-        _ptr(X, "X", torch.bfloat16), _ptr(W, "W", torch.bfloat16), M, N, K,
+        _ptr(X, "X", torch.bfloat16), _ptr(W, "W", torch.bfloat16),
+        _ptr(bias, "bias", torch.bfloat16), M, N, K,
         ctypes.byref(recipe), ctypes.byref(state), _ptr(Y, "Y", torch.bfloat16),
         _ptr(workspace, "workspace"), 0 if workspace is None else workspace.numel(),
         _stream(stream)))
 
 
 def fp8_linear_bwd(dY, M, N, K, recipe: Recipe, state: "LinearStateC", dX, dW,
-                   accumulate_dW: bool, workspace, stream=None) -> None:
+                   accumulate_dW: bool, workspace, stream=None, dbias=None) -> None:
     _check(lib().fp8_linear_bwd(
         _ptr(dY, "dY", torch.bfloat16), M, N, K, ctypes.byref(recipe), ctypes.byref(state),
         _ptr(dX, "dX", torch.bfloat16), _ptr(dW, "dW", torch.float32), int(bool(accumulate_dW)),
+        _ptr(dbias, "dbias", torch.float32),
         _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream)))
 
 
@@ -378,20 +382,24 @@ class Fp8Linear:
                                     p(self.w_q), p(self.w_qt), p(self.x_sinv), p(self.w_sinv),
                                     p(self.qscale_inv), p(self.x_sinv_t), p(self.w_sinv_t))
 
-    def forward(self, X: torch.Tensor, W: torch.Tensor, Y=None, stream=None) -> torch.Tensor:
+    def forward(self, X: torch.Tensor, W: torch.Tensor, Y=None, stream=None,
+                bias=None) -> torch.Tensor:
+        """Y = X . W^T (+ bias [N], bf16)."""
         if Y is None:
             Y = torch.empty(self.M, self.N, dtype=torch.bfloat16, device=X.device)
-        fp8_linear_fwd(X, W, self.recipe, self.c_state, Y, None, stream)
+        fp8_linear_fwd(X, W, self.recipe, self.c_state, Y, None, stream, bias=bias)
         return Y
 
     def backward(self, dY: torch.Tensor, dX=None, dW=None, accumulate_dW: bool = False,
-                 stream=None):
+                 stream=None, dbias=None):
+        """dX, dW (+)= ...; with dbias (fp32 [N]) also the bias gradient,
+        accumulated like dW."""
         if dX is None:
             dX = torch.empty(self.M, self.K, dtype=torch.bfloat16, device=dY.device)
         if dW is None:
             dW = torch.zeros(self.N, self.K, dtype=torch.float32, device=dY.device)
         fp8_linear_bwd(dY, self.M, self.N, self.K, self.recipe, self.c_state, dX, dW,
-                       accumulate_dW, self.workspace, stream)
+                       accumulate_dW, self.workspace, stream, dbias=dbias)
         return dX, dW
 
     def state_dict(self) -> dict:

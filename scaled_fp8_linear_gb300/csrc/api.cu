@@ -164,6 +164,39 @@ int check_state_scales(const fp8_linear_state_t* s) {
 
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
+// Workspace of the backward pass, in order: the dY operands (dY_q, dY_q^T,
+// and their scale arrays in the block-wise and per-row modes), then the bias
+// gradient's partial column sums, one row of N floats per 128 tokens.
+size_t bwd_operand_bytes(int64_t M, int64_t N, const fp8_recipe_t* recipe) {
+    const size_t mn = static_cast<size_t>(M) * static_cast<size_t>(N);
+    if (recipe->scaling == FP8_SCALING_ROW)   // + per-row scales of both, [M] and [N]
+        return 2 * align256(mn) + align256(4 * static_cast<size_t>(M)) +
+               align256(4 * static_cast<size_t>(N));
+    if (recipe->scaling == FP8_SCALING_BLOCK)  // + 1x128 scales, [M][N/128] and [N][M/128]
+        return 2 * align256(mn) + 2 * align256(4 * (mn / 128));
+    return 2 * align256(mn);
+}
+
+size_t dbias_partial_bytes(int64_t M, int64_t N) {
+    return align256(4 * static_cast<size_t>((M + 127) / 128) * static_cast<size_t>(N));
+}
+
+// Checks shared by the three backward variants: workspace size (the partial
+// sums only when dbias is wanted) and alignment.
+int check_bwd_buffers(const void* dY, int64_t M, int64_t N, const fp8_recipe_t* recipe,
+                      const fp8_linear_state_t* s, const void* dX, const float* dW,
+                      const float* dbias, const void* workspace, size_t workspace_bytes) {
+    const size_t need = bwd_operand_bytes(M, N, recipe) + (dbias ? dbias_partial_bytes(M, N) : 0);
+    if (workspace_bytes < need)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: workspace of %zu bytes, %zu needed",
+                         workspace_bytes, need);
+    if (!aligned16(dY) || !aligned16(dX) || !aligned16(dW) || !aligned16(workspace) ||
+        !aligned16(s->x_qt) || !aligned16(s->w_qt) ||
+        (reinterpret_cast<uintptr_t>(dbias) & 3u))
+        return set_error(FP8_ERR_ALIGN, "fp8_linear_bwd: tensors must be 16-byte aligned (dbias 4-byte)");
+    return FP8_OK;
+}
+
 // Block-wise backward ("DeepSeek FP8 training recipe" > "Block-wise scaling
 // at 128 granularity"): one dual cast of dY gives the dgrad operand (1x128
 // blocks along N) and the wgrad operand (dY^T, 1x128 blocks along the
@@ -171,19 +204,13 @@ size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 // token-blocked cast kept by the forward pass.
 int linear_bwd_block(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe,
                      const fp8_linear_state_t* s, void* dX, float* dW, int accumulate_dW,
-                     void* workspace, size_t workspace_bytes, cudaStream_t st) {
+                     float* dbias, void* workspace, size_t workspace_bytes, cudaStream_t st) {
     if (!s->x_qt || !s->w_qt || !s->x_sinv_t || !s->w_sinv_t)
         return set_error(FP8_ERR_INVALID_ARG,
                          "fp8_linear_bwd: block mode needs the forward's x_qt/x_sinv_t and w_qt/w_sinv_t");
     if (M % 128) return set_error(FP8_ERR_SHAPE, "fp8_linear_bwd: block mode needs M multiple of 128");
+    FP8_CHECK(check_bwd_buffers(dY, M, N, recipe, s, dX, dW, dbias, workspace, workspace_bytes));
     const size_t mn = static_cast<size_t>(M) * static_cast<size_t>(N);
-    const size_t need = 2 * align256(mn) + 2 * align256(4 * (mn / 128));
-    if (workspace_bytes < need)
-        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: workspace of %zu bytes, %zu needed",
-                         workspace_bytes, need);
-    if (!aligned16(dY) || !aligned16(dX) || !aligned16(dW) || !aligned16(workspace) ||
-        !aligned16(s->x_qt) || !aligned16(s->w_qt))
-        return set_error(FP8_ERR_ALIGN, "fp8_linear_bwd: tensors must be 16-byte aligned");
     const int fb = recipe->bwd_format, ff = recipe->fwd_format;
     uint8_t* dy_q = static_cast<uint8_t*>(workspace);
     uint8_t* dy_qt = dy_q + align256(mn);
@@ -191,12 +218,18 @@ int linear_bwd_block(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_
     float* dy_st = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dy_s) + align256(4 * (mn / 128)));
     FP8_CHECK(cuda_status(launch_quantize_block(dY, M, N, fb, FP8_GRAN_1x128, recipe->pow2 != 0,
                                                 dy_q, dy_s, dy_qt, dy_st, st), "quantize dY"));
+    if (dbias) {
+        float* partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                  bwd_operand_bytes(M, N, recipe));
+        FP8_CHECK(cuda_status(launch_dbias(dY, M, N, partial, false, dbias, accumulate_dW, st),
+                              "dbias"));
+    }
     // dgrad: dX [M x K] = dY_q [M x N] . (W_q^T [K x N])^T
     FP8_CHECK(launch_gemm(dy_q, fb, s->w_qt, ff, M, K, N, FP8_GRAN_1x128, dy_s, FP8_GRAN_128x128,
-                          s->w_sinv_t, dX, FP8_OUT_BF16, 0, st));
+                          s->w_sinv_t, nullptr, dX, FP8_OUT_BF16, 0, st));
     // wgrad: dW [N x K] (+)= dY_q^T [N x M] . (X_q^T [K x M])^T
     return launch_gemm(dy_qt, fb, s->x_qt, ff, N, K, M, FP8_GRAN_1x128, dy_st, FP8_GRAN_1x128,
-                       s->x_sinv_t, dW, FP8_OUT_F32, accumulate_dW != 0, st);
+                       s->x_sinv_t, nullptr, dW, FP8_OUT_F32, accumulate_dW != 0, st);
 }
 
 // Per-row backward: dY cast per token (dgrad operand) and per output
@@ -206,19 +239,12 @@ int linear_bwd_block(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_
 // GEMMs with vector epilogue factors.
 int linear_bwd_row(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe,
                    const fp8_linear_state_t* s, void* dX, float* dW, int accumulate_dW,
-                   void* workspace, size_t workspace_bytes, cudaStream_t st) {
+                   float* dbias, void* workspace, size_t workspace_bytes, cudaStream_t st) {
     if (!s->x_qt || !s->w_qt || !s->x_sinv_t || !s->w_sinv_t)
         return set_error(FP8_ERR_INVALID_ARG,
                          "fp8_linear_bwd: per-row mode needs the forward's x_qt/x_sinv_t and w_qt/w_sinv_t");
+    FP8_CHECK(check_bwd_buffers(dY, M, N, recipe, s, dX, dW, dbias, workspace, workspace_bytes));
     const size_t mn = static_cast<size_t>(M) * static_cast<size_t>(N);
-    const size_t need = 2 * align256(mn) + align256(4 * static_cast<size_t>(M)) +
-                        align256(4 * static_cast<size_t>(N));
-    if (workspace_bytes < need)
-        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: workspace of %zu bytes, %zu needed",
-                         workspace_bytes, need);
-    if (!aligned16(dY) || !aligned16(dX) || !aligned16(dW) || !aligned16(workspace) ||
-        !aligned16(s->x_qt) || !aligned16(s->w_qt))
-        return set_error(FP8_ERR_ALIGN, "fp8_linear_bwd: tensors must be 16-byte aligned");
     const int fb = recipe->bwd_format, ff = recipe->fwd_format;
     uint8_t* dy_q = static_cast<uint8_t*>(workspace);
     uint8_t* dy_qt = dy_q + align256(mn);
@@ -226,13 +252,24 @@ int linear_bwd_row(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
     float* dy_st = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dy_s) + align256(4 * static_cast<size_t>(M)));
     FP8_CHECK(cuda_status(launch_quantize_rows(dY, M, N, fb, recipe->pow2 != 0, dy_q, dy_s, dy_qt,
                                                dy_st, st), "quantize dY"));
+    if (dbias) {
+        float* partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                  bwd_operand_bytes(M, N, recipe));
+        FP8_CHECK(cuda_status(launch_dbias(dY, M, N, partial, false, dbias, accumulate_dW, st),
+                              "dbias"));
+    }
     FP8_CHECK(launch_gemm(dy_q, fb, s->w_qt, ff, M, K, N, FP8_GRAN_ROW, dy_s, FP8_GRAN_ROW,
-                          s->w_sinv_t, dX, FP8_OUT_BF16, 0, st));
+                          s->w_sinv_t, nullptr, dX, FP8_OUT_BF16, 0, st));
     return launch_gemm(dy_qt, fb, s->x_qt, ff, N, K, M, FP8_GRAN_ROW, dy_st, FP8_GRAN_ROW,
-                       s->x_sinv_t, dW, FP8_OUT_F32, accumulate_dW != 0, st);
+                       s->x_sinv_t, nullptr, dW, FP8_OUT_F32, accumulate_dW != 0, st);
 }
 
 }  // namespace
+
+size_t bwd_operand_workspace(int64_t M, int64_t N, const fp8_recipe_t* recipe) {
+    return bwd_operand_bytes(M, N, recipe);
+}
+
 }  // namespace fp8
 
 using namespace fp8;
@@ -310,27 +347,23 @@ int fp8_quantize_sr(const void* x, int64_t rows, int64_t cols, int format, const
 
 int fp8_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N, int64_t K,
              int layout, int ga, const float* scale_inv_a, int gb, const float* scale_inv_b,
-             void* D, int out, int accumulate, void* stream) {
+             const void* bias, void* D, int out, int accumulate, void* stream) {
     FP8_CHECK(check_gemm_args(A, fa, B, fb, M, N, K, layout, ga, scale_inv_a, gb, scale_inv_b, D,
                               out, accumulate));
-    return launch_gemm(A, fa, B, fb, M, N, K, ga, scale_inv_a, gb, scale_inv_b, D, out,
+    if (bias && !aligned16(bias))
+        return set_error(FP8_ERR_ALIGN, "fp8_gemm: bias must be 16-byte aligned");
+    return launch_gemm(A, fa, B, fb, M, N, K, ga, scale_inv_a, gb, scale_inv_b, bias, D, out,
                        accumulate != 0, as_stream(stream));
 }
 
 size_t fp8_workspace_size(int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe) {
     (void)K;
     if (check_recipe(recipe) != FP8_OK || M < 0 || N < 0) return 0;
-    const size_t mn = static_cast<size_t>(M) * static_cast<size_t>(N);
-    // backward: dY quantised [M x N] and its transposed cast [N x M]
-    if (recipe->scaling == FP8_SCALING_ROW)   // + per-row scales of both, [M] and [N]
-        return 2 * align256(mn) + align256(4 * static_cast<size_t>(M)) + align256(4 * static_cast<size_t>(N));
-    if (recipe->scaling != FP8_SCALING_BLOCK) return 2 * align256(mn);
-    // block mode adds their 1x128 scale arrays, [M][N/128] and [N][M/128]
-    return 2 * align256(mn) + 2 * align256(4 * (mn / 128));
+    return bwd_operand_bytes(M, N, recipe) + dbias_partial_bytes(M, N);
 }
 
-int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K,
-                   const fp8_recipe_t* recipe, const fp8_linear_state_t* s, void* Y,
+int fp8_linear_fwd(const void* X, const void* W, const void* bias, int64_t M, int64_t N,
+                   int64_t K, const fp8_recipe_t* recipe, const fp8_linear_state_t* s, void* Y,
                    void* workspace, size_t workspace_bytes, void* stream) {
     (void)workspace;
     (void)workspace_bytes;
@@ -339,6 +372,7 @@ int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K
     if (!X || !W || !Y || !s) return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_fwd: NULL pointer");
     if (!s->x_q || !s->w_q) return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_fwd: state->x_q / w_q must be set");
     if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(s->x_q) || !aligned16(s->w_q) ||
+        (bias && !aligned16(bias)) ||
         (s->x_qt && !aligned16(s->x_qt)) || (s->w_qt && !aligned16(s->w_qt)))
         return set_error(FP8_ERR_ALIGN, "fp8_linear_fwd: tensors must be 16-byte aligned");
     cudaStream_t st = as_stream(stream);
@@ -359,7 +393,7 @@ int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K
                                                    keep ? s->w_qt : nullptr, s->w_sinv_t, st),
                               "quantize W"));
         return launch_gemm(s->x_q, f, s->w_q, f, M, N, K, FP8_GRAN_ROW, s->x_sinv, FP8_GRAN_ROW,
-                           s->w_sinv, Y, FP8_OUT_BF16, 0, st);
+                           s->w_sinv, bias, Y, FP8_OUT_BF16, 0, st);
     }
 
     if (recipe->scaling == FP8_SCALING_BLOCK) {
@@ -378,7 +412,7 @@ int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K
                                                     s->w_q, s->w_sinv, keep ? s->w_qt : nullptr,
                                                     s->w_sinv_t, st), "quantize W"));
         return launch_gemm(s->x_q, f, s->w_q, f, M, N, K, FP8_GRAN_1x128, s->x_sinv,
-                           FP8_GRAN_128x128, s->w_sinv, Y, FP8_OUT_BF16, 0, st);
+                           FP8_GRAN_128x128, s->w_sinv, bias, Y, FP8_OUT_BF16, 0, st);
     }
 
     FP8_CHECK(check_state_scales(s));
@@ -395,7 +429,7 @@ int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K
         FP8_CHECK(cuda_status(launch_quantize_tensor(W, N, K, f, s->scale + 1, s->w_q, s->w_qt,
                                                      nullptr, st), "quantize W"));
         return launch_gemm(s->x_q, f, s->w_q, f, M, N, K, FP8_GRAN_TENSOR, s->scale_inv + 0,
-                           FP8_GRAN_TENSOR, s->scale_inv + 1, Y, FP8_OUT_BF16, 0, st);
+                           FP8_GRAN_TENSOR, s->scale_inv + 1, bias, Y, FP8_OUT_BF16, 0, st);
     }
 
     // delayed: cast with the scales of earlier steps, fold this step's amax in afterwards
@@ -404,7 +438,7 @@ int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K
     FP8_CHECK(cuda_status(launch_quantize_tensor(W, N, K, f, s->scale + 1, s->w_q, s->w_qt,
                                                  s->amax + 1, st), "quantize W"));
     FP8_CHECK(launch_gemm(s->x_q, f, s->w_q, f, M, N, K, FP8_GRAN_TENSOR, s->scale_inv + 0,
-                          FP8_GRAN_TENSOR, s->scale_inv + 1, Y, FP8_OUT_BF16, 0, st));
+                          FP8_GRAN_TENSOR, s->scale_inv + 1, bias, Y, FP8_OUT_BF16, 0, st));
     return cuda_status(launch_update_scale(s->amax, s->history, s->pos, H, recipe->amax_algo, f,
                                            recipe->margin, recipe->pow2 != 0, s->scale,
                                            s->scale_inv, 2, st, s->qscale_inv, 0),
@@ -413,28 +447,26 @@ int fp8_linear_fwd(const void* X, const void* W, int64_t M, int64_t N, int64_t K
 
 int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe,
                    const fp8_linear_state_t* s, void* dX, float* dW, int accumulate_dW,
-                   void* workspace, size_t workspace_bytes, void* stream) {
+                   float* dbias, void* workspace, size_t workspace_bytes, void* stream) {
     FP8_CHECK(check_recipe(recipe));
     FP8_CHECK(check_linear_shape(M, N, K, recipe));
     if (!dY || !dX || !dW || !s || !workspace)
         return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: NULL pointer");
     if (recipe->scaling == FP8_SCALING_BLOCK)
-        return linear_bwd_block(dY, M, N, K, recipe, s, dX, dW, accumulate_dW, workspace,
+        return linear_bwd_block(dY, M, N, K, recipe, s, dX, dW, accumulate_dW, dbias, workspace,
                                 workspace_bytes, as_stream(stream));
     if (recipe->scaling == FP8_SCALING_ROW)
-        return linear_bwd_row(dY, M, N, K, recipe, s, dX, dW, accumulate_dW, workspace,
+        return linear_bwd_row(dY, M, N, K, recipe, s, dX, dW, accumulate_dW, dbias, workspace,
                               workspace_bytes, as_stream(stream));
     FP8_CHECK(check_state_scales(s));
     if (!s->x_qt || !s->w_qt)
         return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: the forward pass must keep x_qt and w_qt");
-    const size_t need = fp8_workspace_size(M, N, K, recipe);
-    if (workspace_bytes < need)
-        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: workspace of %zu bytes, %zu needed",
-                         workspace_bytes, need);
-    if (!aligned16(dY) || !aligned16(dX) || !aligned16(dW) || !aligned16(workspace) ||
-        !aligned16(s->x_qt) || !aligned16(s->w_qt))
-        return set_error(FP8_ERR_ALIGN, "fp8_linear_bwd: tensors must be 16-byte aligned");
+    FP8_CHECK(check_bwd_buffers(dY, M, N, recipe, s, dX, dW, dbias, workspace, workspace_bytes));
     cudaStream_t st = as_stream(stream);
+    // bias gradient: partial column sums fused into the dY cast, then summed in order
+    float* partial = dbias ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                      bwd_operand_bytes(M, N, recipe))
+                           : nullptr;
     const int fb = recipe->bwd_format, ff = recipe->fwd_format;
     const int H = history_len_of(recipe);
     uint8_t* dy_q = static_cast<uint8_t*>(workspace);
@@ -446,18 +478,21 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
         FP8_CHECK(cuda_status(launch_update_scale(s->amax + 2, h2, s->pos + 2, H, FP8_AMAX_MOST_RECENT,
                                                   fb, recipe->margin, recipe->pow2 != 0, s->scale + 2,
                                                   s->scale_inv + 2, 1, st), "update dY scale"));
-        FP8_CHECK(cuda_status(launch_quantize_tensor(dY, M, N, fb, s->scale + 2, dy_q, dy_qt, nullptr, st),
+        FP8_CHECK(cuda_status(launch_quantize_tensor(dY, M, N, fb, s->scale + 2, dy_q, dy_qt, nullptr, st,
+                                                     nullptr, partial),
                               "quantize dY"));
     } else {
         FP8_CHECK(cuda_status(launch_quantize_tensor(dY, M, N, fb, s->scale + 2, dy_q, dy_qt,
-                                                     s->amax + 2, st), "quantize dY"));
+                                                     s->amax + 2, st, nullptr, partial), "quantize dY"));
     }
+    if (dbias)
+        FP8_CHECK(cuda_status(launch_dbias(dY, M, N, partial, true, dbias, accumulate_dW, st), "dbias"));
     // dgrad: dX [M x K] = dY_q [M x N] . (W_q^T [K x N])^T
     FP8_CHECK(launch_gemm(dy_q, fb, s->w_qt, ff, M, K, N, FP8_GRAN_TENSOR, s->scale_inv + 2,
-                          FP8_GRAN_TENSOR, s->qscale_inv + 1, dX, FP8_OUT_BF16, 0, st));
+                          FP8_GRAN_TENSOR, s->qscale_inv + 1, nullptr, dX, FP8_OUT_BF16, 0, st));
     // wgrad: dW [N x K] (+)= dY_q^T [N x M] . (X_q^T [K x M])^T
     FP8_CHECK(launch_gemm(dy_qt, fb, s->x_qt, ff, N, K, M, FP8_GRAN_TENSOR, s->scale_inv + 2,
-                          FP8_GRAN_TENSOR, s->qscale_inv + 0, dW, FP8_OUT_F32, accumulate_dW != 0, st));
+                          FP8_GRAN_TENSOR, s->qscale_inv + 0, nullptr, dW, FP8_OUT_F32, accumulate_dW != 0, st));
     if (recipe->scaling == FP8_SCALING_DELAYED)
         return cuda_status(launch_update_scale(s->amax + 2, h2, s->pos + 2, H, recipe->amax_algo, fb,
                                                recipe->margin, recipe->pow2 != 0, s->scale + 2,

@@ -59,10 +59,23 @@ struct GemmParams {
     int ga, gb;
     const float* sa;
     const float* sb;
+    const __nv_bfloat16* bias;   // nullable: [N], added before the output rounding
     void* D;
     int out;          // FP8_OUT_BF16 / FP8_OUT_F32
     int accumulate;
 };
+
+// Eight bias values of columns n .. n+7 (n % 8 == 0) as fp32; every lane of
+// a warp reads the same 16 bytes, so the load is one broadcast.
+__device__ __forceinline__ void load_bias8(float (&b)[8], const __nv_bfloat16* bias, int64_t n) {
+    const uint4 v = *reinterpret_cast<const uint4*>(bias + n);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        b[2 * e] = __uint_as_float(w[e] << 16);
+        b[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+}
 
 // Grouped rasterisation: walk GROUP consecutive M-blocks down each N-column
 // so that the CTAs resident at one time share A and B panels in L2.  A
@@ -147,8 +160,8 @@ __device__ __forceinline__ float row_factor(const GemmParams& p, int64_t m) {
 }
 
 // Epilogue of one 32-column chunk of an accumulator row: multiply column j
-// by f[j], then round to bf16 or (optionally) add into the FP32 buffer;
-// 16-byte stores.
+// by f[j], add the bias (if any), then round to bf16 or (optionally) add
+// into the FP32 buffer; 16-byte stores.  N % 8 == 0.
 __device__ __forceinline__ void store_chunk(const uint32_t (&r)[32], int64_t m, int64_t n0,
                                             const GemmParams& p, const float (&f)[32], bool rmw) {
     if (p.out == FP8_OUT_BF16) {
@@ -156,12 +169,19 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&r)[32], int64_t m, 
 #pragma unroll
         for (int j = 0; j < 32; j += 8) {
             if (n0 + j < p.N) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(__uint_as_float(r[j + e]), f[j + e]);
+                if (p.bias) {
+                    float b[8];
+                    load_bias8(b, p.bias, n0 + j);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = __fadd_rn(v[e], b[e]);
+                }
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const __nv_bfloat162 h =
-                        __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[j + 2 * e]), f[j + 2 * e]),
-                                              __fmul_rn(__uint_as_float(r[j + 2 * e + 1]), f[j + 2 * e + 1]));
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
                     w[e] = *reinterpret_cast<const uint32_t*>(&h);
                 }
                 *reinterpret_cast<uint4*>(drow + n0 + j) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -181,6 +201,13 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&r)[32], int64_t m, 
                                        __fmul_rn(__uint_as_float(r[4 * j + 1]), f[4 * j + 1]),
                                        __fmul_rn(__uint_as_float(r[4 * j + 2]), f[4 * j + 2]),
                                        __fmul_rn(__uint_as_float(r[4 * j + 3]), f[4 * j + 3]));
+                if (p.bias) {
+                    const uint2 bw = *reinterpret_cast<const uint2*>(p.bias + n0 + 4 * j);
+                    v.x = __fadd_rn(v.x, __uint_as_float(bw.x << 16));
+                    v.y = __fadd_rn(v.y, __uint_as_float(bw.x & 0xFFFF0000u));
+                    v.z = __fadd_rn(v.z, __uint_as_float(bw.y << 16));
+                    v.w = __fadd_rn(v.w, __uint_as_float(bw.y & 0xFFFF0000u));
+                }
                 if (rmw) {
                     v.x += o[j].x; v.y += o[j].y; v.z += o[j].z; v.w += o[j].w;
                 }
@@ -508,7 +535,8 @@ __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
 }
 
 // Final store of one promoted accumulator row segment (32 columns, packed
-// pairs): bf16 round-to-nearest-even, or FP32 (added to the buffer if rmw).
+// pairs), plus the bias if any: bf16 round-to-nearest-even, or FP32 (added
+// to the buffer if rmw).
 // Block mode has N % 128 == 0, so all 32 columns exist.
 __device__ __forceinline__ void store_block_row(const uint64_t (&acc)[16], int64_t m, int64_t n0,
                                                 const GemmParams& p, bool rmw) {
@@ -517,6 +545,15 @@ __device__ __forceinline__ void store_block_row(const uint64_t (&acc)[16], int64
     for (int e = 0; e < 16; ++e) {
         a[2 * e] = __uint_as_float(static_cast<uint32_t>(acc[e]));
         a[2 * e + 1] = __uint_as_float(static_cast<uint32_t>(acc[e] >> 32));
+    }
+    if (p.bias) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float b[8];
+            load_bias8(b, p.bias, n0 + 8 * j);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a[8 * j + e] = __fadd_rn(a[8 * j + e], b[e]);
+        }
     }
     if (p.out == FP8_OUT_BF16) {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.D) + m * p.N + n0);
@@ -838,10 +875,32 @@ int num_sms() {
     return cache[dev];
 }
 
+// D[m][n] (+)= bias[n] for a GEMM with K = 0 (grid-stride over M x N).
+__global__ void bias_rows_kernel(const __nv_bfloat16* __restrict__ bias, int64_t M, int64_t N,
+                                 void* D, int out, int rmw) {
+    const int64_t n_all = M * N;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_all;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const float b = __bfloat162float(bias[i % N]);
+        if (out == FP8_OUT_BF16) static_cast<__nv_bfloat16*>(D)[i] = __float2bfloat16_rn(b);
+        else static_cast<float*>(D)[i] = rmw ? static_cast<float*>(D)[i] + b : b;
+    }
+}
+
 int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
-                int64_t K, int ga, const float* sa, int gb, const float* sb, void* D, int out,
-                int accumulate, cudaStream_t stream) {
+                int64_t K, int ga, const float* sa, int gb, const float* sb, const void* bias,
+                void* D, int out, int accumulate, cudaStream_t stream) {
     if (M == 0 || N == 0) return FP8_OK;
+    if (K == 0 && bias) {   // an empty sum: D (+)= bias
+        const int64_t n = M * N;
+        const int64_t blocks = (n + 255) / 256;
+        bias_rows_kernel<<<static_cast<unsigned>(blocks < 65535 * 16 ? blocks : 65535 * 16), 256,
+                           0, stream>>>(static_cast<const __nv_bfloat16*>(bias), M, N, D, out,
+                                        out == FP8_OUT_F32 && accumulate);
+        const cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? FP8_OK
+                                : set_error(FP8_ERR_CUDA, "bias launch: %s", cudaGetErrorString(e));
+    }
     if (K == 0) {
         if (out == FP8_OUT_F32 && accumulate) return FP8_OK;
         const size_t bytes = static_cast<size_t>(M) * N * (out == FP8_OUT_F32 ? 4 : 2);
@@ -861,6 +920,7 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
     p.num_n = static_cast<int>((N + BN - 1) / BN);
     p.num_kb = static_cast<int>((K + BK - 1) / BK);
     p.fa = fa; p.fb = fb; p.ga = ga; p.gb = gb; p.sa = sa; p.sb = sb;
+    p.bias = static_cast<const __nv_bfloat16*>(bias);
     p.D = D; p.out = out; p.accumulate = accumulate;
 
     CUtensorMap tmA, tmB;

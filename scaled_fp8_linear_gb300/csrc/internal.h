@@ -4,7 +4,10 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <cstddef>
 #include <cstdint>
+
+#include "../../include/fp8linear.h"
 
 namespace fp8 {
 
@@ -27,9 +30,19 @@ cudaError_t launch_update_scale(const float* amax, float* history, int32_t* pos,
 // rows and cols are multiples of 16.
 // counts (nullable): the cast's dashboard counters [underflow, saturated] are
 // added to counts[0..1].
+// dbias_partial (nullable; needs q_t): the same pass also writes the bias
+// gradient's partial column sums, one row of `cols` floats per 128-row tile.
 cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, int fmt,
                                    const float* scale, uint8_t* q, uint8_t* q_t, float* amax,
-                                   cudaStream_t stream, unsigned long long* counts = nullptr);
+                                   cudaStream_t stream, unsigned long long* counts = nullptr,
+                                   float* dbias_partial = nullptr);
+
+// Bias gradient dbias[n] (+)= sum_m x[m][n] of a bf16 x [rows x cols]
+// (cols % 16 == 0), in fp32 and a fixed order.  partial: ceil(rows/128) x
+// cols floats of workspace, already filled by a fused cast when
+// partial_ready, else filled here from x first.
+cudaError_t launch_dbias(const void* x, int64_t rows, int64_t cols, float* partial,
+                         bool partial_ready, float* dbias, int accumulate, cudaStream_t stream);
 
 // Per-tensor cast of launch_quantize_tensor with stochastic rounding: element
 // i (row-major) draws word i % 4 of Philox-4x32-10(counter = (i / 4, offset),
@@ -55,9 +68,14 @@ cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int 
 
 // Scaled FP8 GEMM, TN layout.  Returns 0 or a negative fp8 status code
 // (tensor-map encoding can fail); launch errors come back as FP8_ERR_CUDA.
+// bias (nullable): bf16 [N] added to every row before the output rounding.
 int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
-                int64_t K, int ga, const float* sa, int gb, const float* sb, void* D, int out,
-                int accumulate, cudaStream_t stream);
+                int64_t K, int ga, const float* sa, int gb, const float* sb, const void* bias,
+                void* D, int out, int accumulate, cudaStream_t stream);
+
+// Workspace bytes of fp8_linear_bwd's dY operands (without the bias
+// gradient's partial sums) for a valid recipe.
+size_t bwd_operand_workspace(int64_t M, int64_t N, const fp8_recipe_t* recipe);
 
 // Device status word (bit 0: a bounded wait timed out).
 int read_device_status(unsigned* status, bool clear);

@@ -67,7 +67,11 @@ extern "C" int fp8_linear_bwd_noalloc(const void* dY, int64_t M, int64_t N, int6
                                       const fp8_recipe_t* recipe,
                                       const fp8_linear_state_t* state, void* dX, float* dW,
                                       int accumulate_dW, void* stream) {
-    const size_t need = fp8_workspace_size(M, N, K, recipe);
+    // the dY operands only: this entry point computes no bias gradient (an
+    // invalid recipe sizes to 0 and is reported by fp8_linear_bwd)
+    const size_t need = fp8_workspace_size(M, N, K, recipe) == 0
+                            ? 0
+                            : fp8::bwd_operand_workspace(M, N, recipe);
     if (need > kScratchBytes)
         return fp8::set_error(FP8_ERR_SHAPE,
                               "fp8_linear_bwd_noalloc: M x N = %lld x %lld needs %zu bytes of "
@@ -78,6 +82,6 @@ extern "C" int fp8_linear_bwd_noalloc(const void* dY, int64_t M, int64_t N, int6
     void* scratch = nullptr;
     const int st = scratch_on_current_device(&scratch);
     if (st != FP8_OK) return st;
-    return fp8_linear_bwd(dY, M, N, K, recipe, state, dX, dW, accumulate_dW, scratch,
+    return fp8_linear_bwd(dY, M, N, K, recipe, state, dX, dW, accumulate_dW, nullptr, scratch,
                           kScratchBytes, stream);
 }

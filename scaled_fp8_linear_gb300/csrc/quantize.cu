@@ -444,12 +444,59 @@ __device__ __forceinline__ void transpose_tile_out(const uint32_t* S, uint8_t* _
     }
 }
 
-template <int FMT, bool AMAX, bool COUNT, bool SR>
+// Column sums of one 128 x 128 bf16 tile for the bias gradient.  The tile
+// is held as in the transposing cast: thread t has rows it*32 + t/8
+// (it = 0..3) and columns 16*(t%8) .. +15 in va[it] (first 8) and vb[it]
+// (last 8), zero outside the matrix.  Sums run over the thread's 4 rows,
+// then over the 4 lanes of a warp that share the columns (xor 8, xor 16),
+// then over the 8 warps in warp order, all in fp32 and in a fixed order, so
+// the result does not depend on scheduling.  Threads 0..127 write column
+// c0 + t of `prow` (one row of partial sums per 128-row tile).
+// CTA-collective.
+__device__ __forceinline__ void tile_column_sums(const uint4 (&va)[4], const uint4 (&vb)[4],
+                                                 float* __restrict__ prow, int64_t cols,
+                                                 int64_t c0) {
+    __shared__ float red[kThreads / 32][128];
+    float sum[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) sum[j] = 0.0f;
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const uint32_t w[8] = {va[it].x, va[it].y, va[it].z, va[it].w,
+                               vb[it].x, vb[it].y, vb[it].z, vb[it].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            sum[2 * e] = __fadd_rn(sum[2 * e], __uint_as_float(w[e] << 16));
+            sum[2 * e + 1] = __fadd_rn(sum[2 * e + 1], __uint_as_float(w[e] & 0xFFFF0000u));
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        sum[j] = __fadd_rn(sum[j], __shfl_xor_sync(0xFFFFFFFFu, sum[j], 8));
+        sum[j] = __fadd_rn(sum[j], __shfl_xor_sync(0xFFFFFFFFu, sum[j], 16));
+    }
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    if (lane < 8) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) red[warp][lane * 16 + j] = sum[j];
+    }
+    __syncthreads();
+    if (t < 128) {
+        float v = red[0][t];
+#pragma unroll
+        for (int w = 1; w < kThreads / 32; ++w) v = __fadd_rn(v, red[w][t]);
+        if (c0 + t < cols) prow[c0 + t] = v;
+    }
+}
+
+template <int FMT, bool AMAX, bool COUNT, bool SR, bool DBIAS>
 __global__ void __launch_bounds__(kThreads)
     quantize_transpose_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
                               int64_t tiles_c, const float* __restrict__ scale_p,
                               uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
-                              unsigned* amax_bits, unsigned long long* counts, SrKey sr_key) {
+                              unsigned* amax_bits, unsigned long long* counts, SrKey sr_key,
+                              float* __restrict__ dbias_partial) {
+    static_assert(!(SR && DBIAS), "the bias-gradient sums ride on the round-to-nearest cast");
     CastCounts cc;
     const SrSched key = sr_sched(sr_key);
     __shared__ __align__(16) uint32_t S[128 * 32];
@@ -495,6 +542,7 @@ __global__ void __launch_bounds__(kThreads)
             vb[it] = ldg_stream(src + 1);
         }
     }
+    if (DBIAS) tile_column_sums(va, vb, dbias_partial + (r0 >> 7) * cols, cols, c0);
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         const int rl = it * 32 + (t >> 3);
@@ -514,6 +562,41 @@ __global__ void __launch_bounds__(kThreads)
     transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
     if (AMAX) cta_amax_commit(m, amax_bits);
     if (COUNT) cta_counts_commit(cc, counts);
+}
+
+// Bias-gradient partial sums without a cast (for the block-wise and per-row
+// backward, whose dY casts have other layouts): one CTA per 128 x 128 tile
+// of x [rows x cols] (cols % 16 == 0), the same loads and the same sums as
+// the fused variant of the transposing cast.
+__global__ void __launch_bounds__(kThreads)
+    column_partial_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
+                          int64_t tiles_c, float* __restrict__ partial) {
+    const int64_t tile = blockIdx.x;
+    const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
+    const int t = threadIdx.x, cg = t & 7;
+    uint4 va[4], vb[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int64_t r = r0 + it * 32 + (t >> 3), c = c0 + cg * 16;
+        va[it] = vb[it] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows && c < cols) {
+            const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + c);
+            va[it] = ldg_stream(src);
+            vb[it] = ldg_stream(src + 1);
+        }
+    }
+    tile_column_sums(va, vb, partial + (r0 >> 7) * cols, cols, c0);
+}
+
+// dbias[n] = sum over the P partial rows of column n, in row order
+// (+ the old dbias[n] when accumulating).
+__global__ void dbias_finalize_kernel(const float* __restrict__ partial, int64_t P, int64_t cols,
+                                      float* __restrict__ dbias, int accumulate) {
+    const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (n >= cols) return;
+    float v = 0.0f;
+    for (int64_t p = 0; p < P; ++p) v = __fadd_rn(v, partial[p * cols + n]);
+    dbias[n] = accumulate ? __fadd_rn(dbias[n], v) : v;
 }
 
 // ----------------------------------------------------------- block casts
@@ -828,21 +911,28 @@ static void launch_flat(const void* x, int64_t n, const float* scale, uint8_t* q
         key);
 }
 
-template <int FMT, bool AMAX, bool COUNT, bool SR>
+template <int FMT, bool AMAX, bool COUNT, bool SR, bool DBIAS = false>
 static void launch_transpose(const void* x, int64_t rows, int64_t cols, const float* scale,
                              uint8_t* q, uint8_t* qt, float* amax, unsigned long long* counts,
-                             const SrKey& key, cudaStream_t stream) {
+                             const SrKey& key, cudaStream_t stream, float* dbias_partial = nullptr) {
     const int64_t tiles_c = (cols + 127) / 128, tiles_r = (rows + 127) / 128;
-    quantize_transpose_kernel<FMT, AMAX, COUNT, SR><<<static_cast<unsigned>(tiles_r * tiles_c),
-                                                      kThreads, 0, stream>>>(
+    quantize_transpose_kernel<FMT, AMAX, COUNT, SR, DBIAS><<<static_cast<unsigned>(tiles_r * tiles_c),
+                                                             kThreads, 0, stream>>>(
         static_cast<const uint16_t*>(x), rows, cols, tiles_c, scale, q, qt,
-        reinterpret_cast<unsigned*>(amax), counts, key);
+        reinterpret_cast<unsigned*>(amax), counts, key, dbias_partial);
 }
 
 template <int FMT, bool AMAX, bool SR>
 static void launch_cast(const void* x, int64_t rows, int64_t cols, const float* scale, uint8_t* q,
                         uint8_t* q_t, float* amax, unsigned long long* counts, const SrKey& key,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, float* dbias_partial) {
+    if constexpr (!SR) {
+        if (dbias_partial) {   // the bias-gradient sums ride on the transposing cast
+            launch_transpose<FMT, AMAX, false, false, true>(x, rows, cols, scale, q, q_t, amax,
+                                                            nullptr, key, stream, dbias_partial);
+            return;
+        }
+    }
     if constexpr (SR) {
         if (q_t) launch_transpose<FMT, AMAX, false, true>(x, rows, cols, scale, q, q_t, amax, nullptr, key, stream);
         else launch_flat<FMT, AMAX, false, true>(x, rows * cols, scale, q, amax, nullptr, key, stream);
@@ -859,7 +949,7 @@ template <bool SR>
 static cudaError_t quantize_tensor(const void* x, int64_t rows, int64_t cols, int fmt,
                                    const float* scale, uint8_t* q, uint8_t* q_t, float* amax,
                                    unsigned long long* counts, const SrKey& key,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, float* dbias_partial = nullptr) {
     const int64_t n = rows * cols;
     if (amax) {
         cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), stream);
@@ -868,20 +958,35 @@ static cudaError_t quantize_tensor(const void* x, int64_t rows, int64_t cols, in
     if (n == 0) return cudaSuccess;
     const bool A = amax != nullptr;
     if (fmt == 0) {
-        if (A) launch_cast<0, true, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream);
-        else launch_cast<0, false, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream);
+        if (A) launch_cast<0, true, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream, dbias_partial);
+        else launch_cast<0, false, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream, dbias_partial);
     } else {
-        if (A) launch_cast<1, true, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream);
-        else launch_cast<1, false, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream);
+        if (A) launch_cast<1, true, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream, dbias_partial);
+        else launch_cast<1, false, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream, dbias_partial);
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, int fmt,
                                    const float* scale, uint8_t* q, uint8_t* q_t, float* amax,
-                                   cudaStream_t stream, unsigned long long* counts) {
+                                   cudaStream_t stream, unsigned long long* counts,
+                                   float* dbias_partial) {
     return quantize_tensor<false>(x, rows, cols, fmt, scale, q, q_t, amax, counts, SrKey{},
-                                  stream);
+                                  stream, dbias_partial);
+}
+
+cudaError_t launch_dbias(const void* x, int64_t rows, int64_t cols, float* partial,
+                         bool partial_ready, float* dbias, int accumulate, cudaStream_t stream) {
+    if (cols == 0) return cudaSuccess;
+    const int64_t P = (rows + 127) / 128;
+    if (!partial_ready && rows > 0) {
+        const int64_t tiles_c = (cols + 127) / 128;
+        column_partial_kernel<<<static_cast<unsigned>(P * tiles_c), kThreads, 0, stream>>>(
+            static_cast<const uint16_t*>(x), rows, cols, tiles_c, partial);
+    }
+    dbias_finalize_kernel<<<static_cast<unsigned>((cols + 255) / 256), 256, 0, stream>>>(
+        partial, P, cols, dbias, accumulate);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_sr(const void* x, int64_t rows, int64_t cols, int fmt,

@@ -40,12 +40,13 @@ def test_gemm_argument_checks():
     L = F.lib()
     one = ctypes.c_void_p(FAKE)
     ok = dict(A=one, fa=0, B=one, fb=0, M=128, N=128, K=128, layout=0, ga=0, sa=one, gb=0,
-              sb=one, D=one, out=0, acc=0, s=None)
+              sb=one, bias=None, D=one, out=0, acc=0, s=None)
 
     def call(**kw):
         a = dict(ok, **kw)
         return L.fp8_gemm(a["A"], a["fa"], a["B"], a["fb"], a["M"], a["N"], a["K"], a["layout"],
-                          a["ga"], a["sa"], a["gb"], a["sb"], a["D"], a["out"], a["acc"], a["s"])
+                          a["ga"], a["sa"], a["gb"], a["sb"], a["bias"], a["D"], a["out"], a["acc"],
+                          a["s"])
 
     assert call(A=None) == -1
     assert call(fa=7) == -1
@@ -57,6 +58,8 @@ def test_gemm_argument_checks():
     assert call(ga=1, K=144) == -2                 # block scales need K % 128 == 0
     assert call(D=ctypes.c_void_p(FAKE + 4)) == -3
     assert "16-byte" in F.fp8_last_error()
+    assert call(bias=ctypes.c_void_p(FAKE + 2)) == -3
+    assert "bias" in F.fp8_last_error()
 
 
 def test_quantize_update_amax_argument_checks():
@@ -82,24 +85,27 @@ def test_quantize_update_amax_argument_checks():
 
 def test_workspace_size_and_recipe_checks():
     r = F.Recipe()
-    assert F.fp8_workspace_size(8192, 4096, 4096, r) == 2 * 8192 * 4096
-    assert F.fp8_workspace_size(16, 16, 16, r) == 2 * 256
-    # block: codes of dY and dY^T plus their 1x128 scale arrays
-    assert F.fp8_workspace_size(256, 256, 256, F.Recipe(scaling=F.SCALING_BLOCK)) == 2 * 65536 + 2 * 2048
+    # codes of dY and dY^T, then the bias gradient's partial sums (N floats per 128 tokens)
+    assert F.fp8_workspace_size(8192, 4096, 4096, r) == 2 * 8192 * 4096 + 64 * 4096 * 4
+    assert F.fp8_workspace_size(16, 16, 16, r) == 2 * 256 + 256
+    assert F.fp8_workspace_size(0, 16, 16, r) == 0
+    # block: plus the 1x128 scale arrays of dY and dY^T
+    assert F.fp8_workspace_size(256, 256, 256, F.Recipe(scaling=F.SCALING_BLOCK)) == \
+        2 * 65536 + 2 * 2048 + 2 * 256 * 4
     assert F.fp8_workspace_size(16, 16, 16, F.Recipe(history_len=0)) == 0
     assert F.fp8_workspace_size(16, 16, 16, F.Recipe(margin=-1)) == 0
     L = F.lib()
     p = ctypes.c_void_p(FAKE)
     st = F.LinearStateC()
     bad = F.Recipe(history_len=2000)
-    assert L.fp8_linear_fwd(p, p, 16, 16, 16, ctypes.byref(bad), ctypes.byref(st), p, None, 0, None) == -1
+    assert L.fp8_linear_fwd(p, p, None, 16, 16, 16, ctypes.byref(bad), ctypes.byref(st), p, None, 0, None) == -1
     blk = F.Recipe(scaling=F.SCALING_BLOCK)
-    assert L.fp8_linear_fwd(p, p, 16, 16, 16, ctypes.byref(blk), ctypes.byref(st), p, None, 0, None) == -2
+    assert L.fp8_linear_fwd(p, p, None, 16, 16, 16, ctypes.byref(blk), ctypes.byref(st), p, None, 0, None) == -2
     # block-wise backward without the forward's transposed operands
-    assert L.fp8_linear_bwd(p, 128, 128, 128, ctypes.byref(blk), ctypes.byref(st), p, p, 0, p, 1 << 20, None) == -1
+    assert L.fp8_linear_bwd(p, 128, 128, 128, ctypes.byref(blk), ctypes.byref(st), p, p, 0, None, p, 1 << 20, None) == -1
     assert "x_qt" in F.fp8_last_error()
     r = F.Recipe()
-    assert L.fp8_linear_fwd(p, p, 16, 16, 16, ctypes.byref(r), ctypes.byref(st), p, None, 0, None) == -1
+    assert L.fp8_linear_fwd(p, p, None, 16, 16, 16, ctypes.byref(r), ctypes.byref(st), p, None, 0, None) == -1
 
 
 def test_binding_refuses_cpu_tensors():
@@ -129,3 +135,21 @@ def test_quantize_sr_argument_checks():
     assert L.fp8_quantize_sr(p, 4, 24, 0, p, 1, 0, p, p, None, None) == -2            # q_t needs %16
     assert L.fp8_quantize_sr(ctypes.c_void_p(FAKE + 2), 4, 4, 0, p, 1, 0, p, None, None, None) == -3
     assert "fp8_quantize" in F.fp8_last_error()
+
+
+def test_bias_argument_checks():
+    L = F.lib()
+    p = ctypes.c_void_p(FAKE)
+    r = F.Recipe()
+    # a state whose every pointer is set (never dereferenced: the calls fail validation)
+    st = F.LinearStateC(*([FAKE] * len(F.LinearStateC._fields_)))
+    odd = ctypes.c_void_p(FAKE + 2)
+    assert L.fp8_linear_fwd(p, p, odd, 16, 16, 16, ctypes.byref(r), ctypes.byref(st), p, None, 0, None) == -3
+    ws = F.fp8_workspace_size(256, 256, 256, r)
+    ws_operands = 2 * 256 * 256
+    # dbias needs the partial-sum part of the workspace; without dbias the operands suffice
+    assert L.fp8_linear_bwd(p, 256, 256, 256, ctypes.byref(r), ctypes.byref(st), p, p, 0, p, p,
+                            ws_operands, None) == -1
+    assert "workspace" in F.fp8_last_error()
+    assert L.fp8_linear_bwd(p, 256, 256, 256, ctypes.byref(r), ctypes.byref(st), p, p, 0,
+                            ctypes.c_void_p(FAKE + 1), p, ws, None) == -3
