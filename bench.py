@@ -310,7 +310,8 @@ def e2e_pass(F, recipe, dev, args, stream):
     pinned memory, fp8_linear_fwd + fp8_linear_bwd, D2H of Y, dX, dW -- all
     inside the timed region.  Copies run on their own streams so that the
     next linear's inputs arrive and the previous one's results leave while
-    the current linear computes (two device buffer sets, event-ordered)."""
+    the current linear computes (two device buffer sets, event-ordered,
+    pipelined across step boundaries as a training loop would be)."""
     nl = len(LINEARS)
     h_in, h_out, layers = [], [], []
     for li, (name, K, N) in enumerate(LINEARS):
@@ -338,64 +339,81 @@ def e2e_pass(F, recipe, dev, args, stream):
     h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     h2d = sum(t.numel() * t.element_size() for tr in h_in for t in tr)
     d2h = sum(t.numel() * t.element_size() for tr in h_out for t in tr)
+    # Linears are numbered across steps (g = step * 5 + li) and alternate
+    # between the two device buffer sets, so the loads of the next linear
+    # (also across a step boundary) and the drains of the previous one run on
+    # the host link while the current one computes.  Each copy waits only for
+    # the last user of its own buffer set.
+    computed, drained = {}, {}
+    counter = [0]
 
-    def one():
-        loaded = [torch.cuda.Event() for _ in range(nl)]
-        computed = [torch.cuda.Event() for _ in range(nl)]
-        drained = [torch.cuda.Event() for _ in range(nl)]
-        h2d_s.wait_stream(stream)        # previous step's readers of both buffer sets are done
+    def run_linear():
+        g = counter[0]
+        counter[0] += 1
+        li = g % nl
+        _, K, N = LINEARS[li]
+        b = bufs[g % 2]
+        loaded = torch.cuda.Event()
+        with torch.cuda.stream(h2d_s):
+            if g - 2 in computed:
+                h2d_s.wait_event(computed.pop(g - 2))      # last reader of this set's inputs
+            hx, hw, hdy = h_in[li]
+            b["X"][:TOKENS * K].view(TOKENS, K).copy_(hx, non_blocking=True)
+            b["W"][:N * K].view(N, K).copy_(hw, non_blocking=True)
+            b["dY"][:TOKENS * N].view(TOKENS, N).copy_(hdy, non_blocking=True)
+            loaded.record(h2d_s)
+        return g, li, K, N, b, loaded
 
-        def load(li):
-            _, K, N = LINEARS[li]
-            b = bufs[li % 2]
-            with torch.cuda.stream(h2d_s):
-                if li >= 2:
-                    h2d_s.wait_event(computed[li - 2])   # the buffer set's last reader
-                hx, hw, hdy = h_in[li]
-                b["X"][:TOKENS * K].view(TOKENS, K).copy_(hx, non_blocking=True)
-                b["W"][:N * K].view(N, K).copy_(hw, non_blocking=True)
-                b["dY"][:TOKENS * N].view(TOKENS, N).copy_(hdy, non_blocking=True)
-                loaded[li].record(h2d_s)
+    def compute_and_drain(g, li, K, N, b, loaded):
+        stream.wait_event(loaded)
+        if g - 2 in drained:
+            stream.wait_event(drained.pop(g - 2))          # this set's outputs have left
+        Y = b["Y"][:TOKENS * N].view(TOKENS, N)
+        dX = b["dX"][:TOKENS * K].view(TOKENS, K)
+        dW = b["dW"][:N * K].view(N, K)
+        L = layers[li]
+        L.forward(b["X"][:TOKENS * K].view(TOKENS, K), b["W"][:N * K].view(N, K), Y=Y)
+        L.backward(b["dY"][:TOKENS * N].view(TOKENS, N), dX=dX, dW=dW, accumulate_dW=False)
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        computed[g] = ev
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(ev)
+            hy, hdx, hdw = h_out[li]
+            hy.copy_(Y, non_blocking=True)
+            hdx.copy_(dX, non_blocking=True)
+            hdw.copy_(dW, non_blocking=True)
+            dev_ev = torch.cuda.Event()
+            dev_ev.record(d2h_s)
+            drained[g] = dev_ev
 
-        load(0)
-        for li, (name, K, N) in enumerate(LINEARS):
-            if li + 1 < nl:
-                load(li + 1)
-            b = bufs[li % 2]
-            stream.wait_event(loaded[li])
-            if li >= 2:
-                stream.wait_event(drained[li - 2])       # outputs of this set have left
-            Y = b["Y"][:TOKENS * N].view(TOKENS, N)
-            dX = b["dX"][:TOKENS * K].view(TOKENS, K)
-            dW = b["dW"][:N * K].view(N, K)
-            L = layers[li]
-            L.forward(b["X"][:TOKENS * K].view(TOKENS, K), b["W"][:N * K].view(N, K), Y=Y)
-            L.backward(b["dY"][:TOKENS * N].view(TOKENS, N), dX=dX, dW=dW, accumulate_dW=False)
-            computed[li].record(stream)
-            with torch.cuda.stream(d2h_s):
-                d2h_s.wait_event(computed[li])
-                hy, hdx, hdw = h_out[li]
-                hy.copy_(Y, non_blocking=True)
-                hdx.copy_(dX, non_blocking=True)
-                hdw.copy_(dW, non_blocking=True)
-                drained[li].record(d2h_s)
-        stream.wait_stream(d2h_s)
+    def steps(k):
+        """k steps, issued one linear ahead on the load stream."""
+        h2d_s.wait_stream(stream)                          # copies start after the start event
+        d2h_s.wait_stream(stream)
+        pending = run_linear()
+        for i in range(k * nl):
+            nxt = run_linear() if i + 1 < k * nl else None
+            compute_and_drain(*pending)
+            pending = nxt
+        stream.wait_stream(d2h_s)                          # the last results are on the host
+        stream.wait_stream(h2d_s)
 
-    for _ in range(max(1, min(args.warmup, 3))):
-        one()
+    steps(max(1, min(args.warmup, 3)))
     torch.cuda.synchronize()
     n = max(1, min(args.steps, 10))
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(n):
-        one()
+    steps(n)
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / n
     return {"value": round(_flops_step() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "steps": n, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "copies": "pinned host <-> device on two copy streams, overlapped with compute"}
+            "copies": "pinned host <-> device on two copy streams, overlapped with compute and "
+                      "with each other across linears and steps; host link measured at "
+                      "~211 GB/s H2D, ~193 GB/s D2H, ~342 GB/s both ways"}
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -477,6 +495,70 @@ def run_reference(args):
                 "d2h_bytes_per_step": 0}}))
 
 
+def run_quantize_sweep(F, args, dev, flush):
+    """The quantizer sweep: n = 2^20 .. 2^30 bf16 elements as [n/4096 x 4096]
+    and [n/8192 x 8192], t_3-distributed, E4M3 and E5M2, with and without the
+    fused transpose, in two modes:
+      stale:   one cast with a fixed scale and the fused amax
+               (2 + 1 (+1) bytes per element);
+      dynamic: amax pass, scale update, then the cast with the new scale
+               (2 + 2 + 1 (+1) bytes per element).
+    One JSON line per case; L2 flushed before every timed iteration."""
+    hbm_gbs = _peaks()[0]
+    stream = torch.cuda.current_stream()
+    for log2n in range(20, 31, 2):
+        n = 1 << log2n
+        for width in (4096, 8192):
+            rows = n // width
+            x = synthetic.student_t((rows, width), 3, 1.0, seed=log2n, device=dev)
+            q = torch.empty(rows, width, dtype=torch.uint8, device=dev)
+            qt = torch.empty(width, rows, dtype=torch.uint8, device=dev)
+            am = torch.empty(1, dtype=torch.float32, device=dev)
+            scale = torch.ones(1, dtype=torch.float32, device=dev)
+            scale_inv = torch.ones(1, dtype=torch.float32, device=dev)
+            hist = torch.zeros(1, dtype=torch.float32, device=dev)
+            pos = torch.zeros(1, dtype=torch.int32, device=dev)
+            for fname, fmt in (("e4m3", F.E4M3), ("e5m2", F.E5M2)):
+                for transpose in (False, True):
+                    qt_arg = qt if transpose else None
+                    for mode in ("stale", "dynamic"):
+                        if mode == "stale":
+                            def call():
+                                F.fp8_quantize(x, fmt, scale=scale, q=q, q_t=qt_arg, amax_out=am)
+                            per_elem = 3 + (1 if transpose else 0)
+                        else:
+                            def call():
+                                F.fp8_amax(x, am)
+                                F.fp8_update_scale(am, hist, pos, 1, F.AMAX_MOST_RECENT, fmt, 0,
+                                                   False, scale, scale_inv)
+                                F.fp8_quantize(x, fmt, scale=scale, q=q, q_t=qt_arg)
+                            per_elem = 5 + (1 if transpose else 0)
+                        for _ in range(3):
+                            call()
+                        iters = args.iters
+                        ev = [(torch.cuda.Event(enable_timing=True),
+                               torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+                        for i in range(iters):
+                            flush.fill_(float(i))
+                            ev[i][0].record(stream)
+                            call()
+                            ev[i][1].record(stream)
+                        torch.cuda.synchronize()
+                        ms = sorted(a.elapsed_time(b) for a, b in ev)
+                        med = ms[len(ms) // 2]
+                        gbs = per_elem * n / (med * 1e-3) / 1e9
+                        print(json.dumps({
+                            "kernel": "quantize_sweep", "mode": mode, "log2_elements": log2n,
+                            "shape": [rows, width], "format": fname, "transpose": transpose,
+                            "bytes_per_element": per_elem, "median_ms": round(med, 5),
+                            "achieved": round(gbs, 1), "unit": "GB/s", "peak": round(hbm_gbs, 1),
+                            "frac": round(gbs / hbm_gbs, 4), "iters": iters,
+                            "l2": "flushed before every launch"}), flush=True)
+            del x, q, qt
+            torch.cuda.empty_cache()
+    assert F.fp8_device_status() == 0
+
+
 def run_kernel(args):
     """Time one kernel of the path on one shape (not the headline number):
     gemm (per-tensor, E4M3 or E5M2 x E4M3, bf16 out), block_gemm (1x128 x
@@ -502,6 +584,8 @@ def run_kernel(args):
 
     if args.kernel == "gemm_step":
         return run_gemm_step(F, args, dev, codes, flush)
+    if args.kernel == "quantize_sweep":
+        return run_quantize_sweep(F, args, dev, flush)
     if args.kernel in ("gemm", "block_gemm"):
         M, N, K = dims
         A, B = codes(M, K), codes(N, K)
@@ -621,7 +705,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", choices=["gemm", "block_gemm", "quantize", "quantize_sr",
-                                         "gemm_step"],
+                                         "quantize_sweep", "gemm_step"],
                     help="time one kernel on --shape instead of the layer step")
     ap.add_argument("--shape", default="8192,12288,4096")
     ap.add_argument("--fmt", choices=["e4m3", "e5m2"], default="e4m3")
