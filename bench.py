@@ -203,6 +203,7 @@ def run_gpu(args):
     comp = component_pass(F, layers, Xs, dYs, Ws, Ys, dXs, dWs, flush, args, stream)
 
     e2e = e2e_pass(F, recipe, dev, args, stream) if rank == 0 else None
+    small = small_case_pass(F, dev, stream) if rank == 0 else None
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -234,6 +235,7 @@ def run_gpu(args):
         "component_pass_ms_per_step": round(comp["total_ms"] / comp["steps"], 4),
         "gpu_launches": 8 * len(LINEARS) * args.steps,
         "e2e": e2e,
+        "small_case": small,
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
@@ -303,6 +305,61 @@ def component_pass(F, layers, Xs, dYs, Ws, Ys, dXs, dWs, flush, args, stream):
     return {"by_kind": by_kind, "gemm_ms": by_kind["gemm"], "quant_ms": by_kind["quantize"],
             "gemm_flops": gemm_flops, "quant_bytes": quant_bytes, "total_ms": total,
             "steps": n_steps}
+
+
+def small_case_pass(F, dev, stream, iters=200):
+    """The small forward case (X 256 x 512 with outliers, W 512 x 512, dynamic
+    scaling): latency of fp8_linear_fwd and of fwd + bwd, issued eagerly and
+    replayed from a CUDA graph of the same calls.  Launch-bound at this size
+    (~12 launches per fwd + bwd), so it reports microseconds, not a roofline."""
+    M, K, N = 256, 512, 512
+    layer = F.Fp8Linear(M, N, K, F.Recipe(F.SCALING_DYNAMIC), device=dev)
+    X = synthetic.with_outlier_entries((M, K), 1.0, 0.001, 50.0, seed=0, device=dev)
+    W = synthetic.normal((N, K), 0.02, seed=1, device=dev)
+    dY = synthetic.normal((M, N), 1e-3, seed=2, device=dev)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    dX = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    dW = torch.zeros(N, K, dtype=torch.float32, device=dev)
+
+    def fwd():
+        layer.forward(X, W, Y=Y)
+
+    def fwd_bwd():
+        layer.forward(X, W, Y=Y)
+        layer.backward(dY, dX=dX, dW=dW)
+
+    def timed(fn):
+        for _ in range(10):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / iters
+
+    out = {"workload": "small forward: X 256x512 (0.1% entries x50), W 512x512, dynamic scaling",
+           "fwd_us": round(timed(fwd), 2), "fwd_bwd_us": round(timed(fwd_bwd), 2)}
+    graphs = {}
+    for name, fn in (("fwd", fwd), ("fwd_bwd", fwd_bwd)):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn()                                   # warm: kernel attributes, tensor maps
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=side):
+                fn()
+        stream.wait_stream(side)
+        graphs[name] = g
+    out["graph_fwd_us"] = round(timed(graphs["fwd"].replay), 2)
+    out["graph_fwd_bwd_us"] = round(timed(graphs["fwd_bwd"].replay), 2)
+    out["graph_fwd_bwd_tflops"] = round(6.0 * M * N * K / (out["graph_fwd_bwd_us"] * 1e-6) / 1e12, 3)
+    out["l2"] = "resident (1.3 MB of operands)"
+    assert F.fp8_device_status() == 0
+    return out
 
 
 def e2e_pass(F, recipe, dev, args, stream):

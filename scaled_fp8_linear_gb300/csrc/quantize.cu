@@ -528,40 +528,40 @@ __global__ void __launch_bounds__(kThreads)
         __syncthreads();
         transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
         if (AMAX) cta_amax_commit(m, amax_bits);
-        return;
-    }
-    // all of this thread's loads first (8 x 16 B in flight), then cast and store
-    uint4 va[4], vb[4];
+    } else {
+        // all of this thread's loads first (8 x 16 B in flight), then cast and store
+        uint4 va[4], vb[4];
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int64_t r = r0 + it * 32 + (t >> 3), c = c0 + cg * 16;
-        va[it] = vb[it] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < rows && c < cols) {
-            const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + c);
-            va[it] = ldg_stream(src);
-            vb[it] = ldg_stream(src + 1);
+        for (int it = 0; it < 4; ++it) {
+            const int64_t r = r0 + it * 32 + (t >> 3), c = c0 + cg * 16;
+            va[it] = vb[it] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < rows && c < cols) {
+                const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + c);
+                va[it] = ldg_stream(src);
+                vb[it] = ldg_stream(src + 1);
+            }
         }
-    }
-    if (DBIAS) tile_column_sums(va, vb, dbias_partial + (r0 >> 7) * cols, cols, c0);
+        if (DBIAS) tile_column_sums(va, vb, dbias_partial + (r0 >> 7) * cols, cols, c0);
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int rl = it * 32 + (t >> 3);
-        const int64_t r = r0 + rl, c = c0 + cg * 16;
-        const uint4 a = va[it], b = vb[it];
-        uint4 out = make_uint4(0u, 0u, 0u, 0u);
-        if (r < rows && c < cols) {
-            if (AMAX) m = absmax_vec(absmax_vec(m, a), b);
-            // cols % 16 == 0: the 16 elements are vector (r * cols + c) / 16
-            out = cast16<FMT, COUNT, SR>(a, b, s, cc, key, static_cast<uint64_t>(r * cols + c) >> 4);
-            *reinterpret_cast<uint4*>(q + r * cols + c) = out;
+        for (int it = 0; it < 4; ++it) {
+            const int rl = it * 32 + (t >> 3);
+            const int64_t r = r0 + rl, c = c0 + cg * 16;
+            const uint4 a = va[it], b = vb[it];
+            uint4 out = make_uint4(0u, 0u, 0u, 0u);
+            if (r < rows && c < cols) {
+                if (AMAX) m = absmax_vec(absmax_vec(m, a), b);
+                // cols % 16 == 0: the 16 elements are vector (r * cols + c) / 16
+                out = cast16<FMT, COUNT, SR>(a, b, s, cc, key, static_cast<uint64_t>(r * cols + c) >> 4);
+                *reinterpret_cast<uint4*>(q + r * cols + c) = out;
+            }
+            *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = out;
         }
-        *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = out;
-    }
-    __syncthreads();
+        __syncthreads();
 
-    transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
-    if (AMAX) cta_amax_commit(m, amax_bits);
-    if (COUNT) cta_counts_commit(cc, counts);
+        transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
+        if (AMAX) cta_amax_commit(m, amax_bits);
+        if (COUNT) cta_counts_commit(cc, counts);
+    }
 }
 
 // Bias-gradient partial sums without a cast (for the block-wise and per-row

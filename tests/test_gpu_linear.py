@@ -243,3 +243,49 @@ def test_full_size_block_gemm_sampled(M, N, K):
                                   F.GRAN_128x128)
     assert_gemm_bound(Y[torch.as_tensor(rows, device=DEV)], D.reshape(len(rows), N),
                       Dabs.reshape(len(rows), N))
+
+
+def test_step_replays_from_a_cuda_graph():
+    """fp8_linear_fwd + fp8_linear_bwd captured once in a CUDA graph and
+    replayed: every output bit equal to the eager calls on the same state
+    (dynamic scaling, so the state does not drift between the runs)."""
+    M, N, K = 256, 512, 512
+    dev = torch.device(DEV)
+    rec = F.Recipe(F.SCALING_DYNAMIC)
+    eager = F.Fp8Linear(M, N, K, rec, device=DEV)
+    graphed = F.Fp8Linear(M, N, K, rec, device=DEV)
+    X = synthetic.with_outlier_entries((M, K), 1.0, 0.001, 50.0, seed=0).to(dev)
+    W = synthetic.normal((N, K), 0.02, seed=1).to(dev)
+    dY = synthetic.normal((M, N), 1e-3, seed=2).to(dev)
+    b = synthetic.normal((N,), 0.1, seed=3).to(dev)
+    outs = {}
+    for name, layer in (("eager", eager), ("graph", graphed)):
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        dX = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        dW = torch.zeros(N, K, dtype=torch.float32, device=dev)
+        db = torch.zeros(N, dtype=torch.float32, device=dev)
+
+        def run():
+            layer.forward(X, W, Y=Y, bias=b)
+            layer.backward(dY, dX=dX, dW=dW, dbias=db)
+        if name == "eager":
+            run()
+        else:
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                run()                                # warm-up outside the capture
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    run()
+            torch.cuda.current_stream().wait_stream(side)
+            for t in (Y, dX, dW, db):
+                t.zero_()
+            g.replay()
+            g.replay()
+        torch.cuda.synchronize()
+        outs[name] = [t.clone() for t in (Y, dX, dW, db)]
+    for a, c in zip(outs["eager"], outs["graph"]):
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
+                           c.view(torch.int16) if c.dtype == torch.bfloat16 else c.view(torch.int32))
