@@ -83,6 +83,9 @@ typedef struct {
     int32_t pow2;         /* nonzero: round scales down to powers of two     */
     int32_t fwd_format;   /* format of X and W (FP8_E4M3 for HYBRID)         */
     int32_t bwd_format;   /* format of dY (FP8_E5M2 for HYBRID)              */
+    int32_t sr_grad;      /* 0 or 1: cast dY with stochastic rounding (the   */
+                          /*   fp8_quantize_sr rule; per-tensor modes only,  */
+                          /*   needs state->sr_key)                          */
 } fp8_recipe_t;
 
 /* Caller-owned device state of one linear layer.  Role r indexes the
@@ -109,6 +112,10 @@ typedef struct {
     float*   x_sinv_t;   /* [K][M/128] block mode: scales of x_qt, the 1x128   */
                          /*   block cast of X^T (blocks run along the tokens)  */
     float*   w_sinv_t;   /* [K/128][N/128] block mode: scales of w_qt = W_q^T  */
+    uint64_t* sr_key;    /* [2] with recipe->sr_grad: (seed, counter) of the   */
+                         /*   stochastic dY cast, i.e. fp8_quantize_sr's seed  */
+                         /*   and offset; each backward call uses the counter  */
+                         /*   and then adds 1 to it on the device              */
 } fp8_linear_state_t;
 
 /* ---------------------------------------------------------------- calls */

@@ -279,13 +279,18 @@ class Recipe:
     history_len: int = 16
     algo: int = ALGO_MAX
     pow2: bool = False
+    sr_grad: bool = False      # cast dY with stochastic rounding ("Stochastic rounding")
 
 
 class LinearState:
     """The oracle's own scaling state for one linear layer (roles X, W, dY)
-    plus the quantised forward operands that the backward pass reuses."""
+    plus the quantised forward operands that the backward pass reuses.  With
+    recipe.sr_grad, backward call t casts dY with quantize_sr(seed=sr_seed,
+    offset=t)."""
 
-    def __init__(self, recipe: Recipe):
+    def __init__(self, recipe: Recipe, sr_seed: int = 0):
+        self.sr_seed = int(sr_seed)
+        self.sr_counter = 0
         h = recipe.history_len if recipe.scaling == SCALING_DELAYED else 1
         self.roles = [ScaleState(h) for _ in range(3)]
         self.last_amax = np.zeros(3, np.float32)
@@ -297,13 +302,21 @@ def _per_tensor_operand(st: LinearState, role: int, x_bits, fmt: int, recipe: Re
     rs = st.roles[role]
     a = amax(x_bits)
     st.last_amax[role] = a
+
+    def cast(scale):
+        if role == ROLE_DY and recipe.sr_grad:
+            q, qt = quantize_sr(x_bits, fmt, scale, st.sr_seed, st.sr_counter, transpose=True)
+            st.sr_counter += 1
+            return q, qt
+        return quantize(x_bits, fmt, scale, transpose=True)
+
     if recipe.scaling == SCALING_DYNAMIC:
         # current scaling: this tensor's own amax sets the scale it is cast with
         update_scale(rs, a, ALGO_MOST_RECENT, fmt, recipe.margin, recipe.pow2)
-        q, qt = quantize(x_bits, fmt, rs.scale[0], transpose=True)
+        q, qt = cast(rs.scale[0])
         return q, qt, rs.scale_inv.copy()
     # delayed: cast with the scale from earlier steps, then fold this amax in
-    q, qt = quantize(x_bits, fmt, rs.scale[0], transpose=True)
+    q, qt = cast(rs.scale[0])
     sinv = rs.scale_inv.copy()
     update_scale(rs, a, recipe.algo, fmt, recipe.margin, recipe.pow2)
     return q, qt, sinv
@@ -370,6 +383,7 @@ def linear_bwd(dY_bits, recipe: Recipe, st: LinearState, dW_prev=None, rows_dx=N
         return dX, (dW, dWabs)
     sx, sw = st.sinv_fwd
     dy_q, dy_qt, sdy = _per_tensor_operand(st, ROLE_DY, dY_bits, E5M2, recipe)
+    st.dy_q = dy_q
     dX = _gemm_rows(dy_q, E5M2, st.w_qt, E4M3, sdy, sw, rows_dx)
     dW, dWabs = _gemm_rows(dy_qt, E5M2, st.x_qt, E4M3, sdy, sx, rows_dw)
     if dW_prev is not None:

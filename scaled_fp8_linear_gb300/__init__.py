@@ -64,12 +64,12 @@ class Recipe(ctypes.Structure):
     _fields_ = [("scaling", ctypes.c_int32), ("margin", ctypes.c_int32),
                 ("history_len", ctypes.c_int32), ("amax_algo", ctypes.c_int32),
                 ("pow2", ctypes.c_int32), ("fwd_format", ctypes.c_int32),
-                ("bwd_format", ctypes.c_int32)]
+                ("bwd_format", ctypes.c_int32), ("sr_grad", ctypes.c_int32)]
 
     def __init__(self, scaling=SCALING_DELAYED, margin=0, history_len=16, amax_algo=AMAX_MAX,
-                 pow2=False, fwd_format=E4M3, bwd_format=E5M2):
+                 pow2=False, fwd_format=E4M3, bwd_format=E5M2, sr_grad=False):
         super().__init__(scaling, margin, history_len, amax_algo, int(bool(pow2)), fwd_format,
-                         bwd_format)
+                         bwd_format, int(bool(sr_grad)))
 
 
 _vp = ctypes.c_void_p
@@ -80,7 +80,7 @@ class LinearStateC(ctypes.Structure):
     _fields_ = [("scale", _vp), ("scale_inv", _vp), ("amax", _vp), ("history", _vp),
                 ("pos", _vp), ("x_q", _vp), ("x_qt", _vp), ("w_q", _vp), ("w_qt", _vp),
                 ("x_sinv", _vp), ("w_sinv", _vp), ("qscale_inv", _vp), ("x_sinv_t", _vp),
-                ("w_sinv_t", _vp)]
+                ("w_sinv_t", _vp), ("sr_key", _vp)]
 
 
 _lib = None
@@ -338,9 +338,11 @@ class Fp8Linear:
     """One FP8 linear layer's device state (scales, histories, quantised
     operands, workspace), allocated with torch on `device`, plus fwd/bwd
     calls into the library.  `state_dict()` / `load_state_dict()` copy the
-    scaling state for checkpoints."""
+    scaling state for checkpoints.  With recipe.sr_grad the gradient cast
+    rounds stochastically from the key (sr_seed, call counter)."""
 
-    def __init__(self, M: int, N: int, K: int, recipe: Recipe | None = None, device="cuda"):
+    def __init__(self, M: int, N: int, K: int, recipe: Recipe | None = None, device="cuda",
+                 sr_seed: int = 0):
         self.M, self.N, self.K = M, N, K
         self.recipe = recipe or Recipe()
         dev = torch.device(device)
@@ -374,13 +376,18 @@ class Fp8Linear:
             self.w_sinv = torch.empty(N, **f32)
             self.x_sinv_t = torch.empty(K, **f32)
             self.w_sinv_t = torch.empty(K, **f32)
+        # (seed, counter) of the stochastic gradient cast, as two 64-bit words
+        seed = int(sr_seed) & 0xFFFFFFFFFFFFFFFF
+        self.sr_key = torch.tensor([seed - (1 << 64) if seed >> 63 else seed, 0],
+                                   dtype=torch.int64, device=dev)
         ws = fp8_workspace_size(M, N, K, self.recipe)
         self.workspace = torch.empty(max(ws, 16), **u8)
         p = lambda t: None if t is None else t.data_ptr()
         self.c_state = LinearStateC(p(self.scale), p(self.scale_inv), p(self.amax),
                                     p(self.history), p(self.pos), p(self.x_q), p(self.x_qt),
                                     p(self.w_q), p(self.w_qt), p(self.x_sinv), p(self.w_sinv),
-                                    p(self.qscale_inv), p(self.x_sinv_t), p(self.w_sinv_t))
+                                    p(self.qscale_inv), p(self.x_sinv_t), p(self.w_sinv_t),
+                                    p(self.sr_key))
 
     def forward(self, X: torch.Tensor, W: torch.Tensor, Y=None, stream=None,
                 bias=None) -> torch.Tensor:
@@ -404,7 +411,7 @@ class Fp8Linear:
 
     def state_dict(self) -> dict:
         return {k: getattr(self, k).clone()
-                for k in ("scale", "scale_inv", "amax", "history", "pos", "qscale_inv")}
+                for k in ("scale", "scale_inv", "amax", "history", "pos", "qscale_inv", "sr_key")}
 
     def load_state_dict(self, sd: dict) -> None:
         for k, v in sd.items():

@@ -72,6 +72,11 @@ int check_recipe(const fp8_recipe_t* r) {
         return set_error(FP8_ERR_INVALID_ARG, "unknown amax_algo %d", r->amax_algo);
     if (!valid_format(r->fwd_format) || !valid_format(r->bwd_format))
         return set_error(FP8_ERR_INVALID_ARG, "unknown FP8 format");
+    if (r->sr_grad != 0 && r->sr_grad != 1)
+        return set_error(FP8_ERR_INVALID_ARG, "sr_grad %d is not 0 or 1", r->sr_grad);
+    if (r->sr_grad && (r->scaling == FP8_SCALING_BLOCK || r->scaling == FP8_SCALING_ROW))
+        return set_error(FP8_ERR_UNSUPPORTED,
+                         "sr_grad: stochastic rounding of dY is built for per-tensor scaling only");
     return FP8_OK;
 }
 
@@ -462,11 +467,16 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
     if (!s->x_qt || !s->w_qt)
         return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: the forward pass must keep x_qt and w_qt");
     FP8_CHECK(check_bwd_buffers(dY, M, N, recipe, s, dX, dW, dbias, workspace, workspace_bytes));
+    if (recipe->sr_grad && (!s->sr_key || (reinterpret_cast<uintptr_t>(s->sr_key) & 7u)))
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: sr_grad needs an 8-byte aligned state->sr_key");
     cudaStream_t st = as_stream(stream);
-    // bias gradient: partial column sums fused into the dY cast, then summed in order
+    // bias gradient: partial column sums fused into the (round-to-nearest) dY
+    // cast, then summed in order; the stochastic cast leaves them to a pass
+    // of their own
     float* partial = dbias ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                                       bwd_operand_bytes(M, N, recipe))
                            : nullptr;
+    float* fused_partial = recipe->sr_grad ? nullptr : partial;
     const int fb = recipe->bwd_format, ff = recipe->fwd_format;
     const int H = history_len_of(recipe);
     uint8_t* dy_q = static_cast<uint8_t*>(workspace);
@@ -478,15 +488,18 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
         FP8_CHECK(cuda_status(launch_update_scale(s->amax + 2, h2, s->pos + 2, H, FP8_AMAX_MOST_RECENT,
                                                   fb, recipe->margin, recipe->pow2 != 0, s->scale + 2,
                                                   s->scale_inv + 2, 1, st), "update dY scale"));
-        FP8_CHECK(cuda_status(launch_quantize_tensor(dY, M, N, fb, s->scale + 2, dy_q, dy_qt, nullptr, st,
-                                                     nullptr, partial),
-                              "quantize dY"));
-    } else {
-        FP8_CHECK(cuda_status(launch_quantize_tensor(dY, M, N, fb, s->scale + 2, dy_q, dy_qt,
-                                                     s->amax + 2, st, nullptr, partial), "quantize dY"));
     }
+    float* dy_amax = recipe->scaling == FP8_SCALING_DYNAMIC ? nullptr : s->amax + 2;
+    if (recipe->sr_grad)   // "Stochastic rounding": unbiased gradient codes
+        FP8_CHECK(cuda_status(launch_quantize_sr(dY, M, N, fb, s->scale + 2, 0, 0, dy_q, dy_qt,
+                                                 dy_amax, st, s->sr_key), "quantize dY"));
+    else
+        FP8_CHECK(cuda_status(launch_quantize_tensor(dY, M, N, fb, s->scale + 2, dy_q, dy_qt,
+                                                     dy_amax, st, nullptr, fused_partial),
+                              "quantize dY"));
     if (dbias)
-        FP8_CHECK(cuda_status(launch_dbias(dY, M, N, partial, true, dbias, accumulate_dW, st), "dbias"));
+        FP8_CHECK(cuda_status(launch_dbias(dY, M, N, partial, fused_partial != nullptr, dbias,
+                                           accumulate_dW, st), "dbias"));
     // dgrad: dX [M x K] = dY_q [M x N] . (W_q^T [K x N])^T
     FP8_CHECK(launch_gemm(dy_q, fb, s->w_qt, ff, M, K, N, FP8_GRAN_TENSOR, s->scale_inv + 2,
                           FP8_GRAN_TENSOR, s->qscale_inv + 1, nullptr, dX, FP8_OUT_BF16, 0, st));

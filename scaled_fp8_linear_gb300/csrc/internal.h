@@ -46,10 +46,12 @@ cudaError_t launch_dbias(const void* x, int64_t rows, int64_t cols, float* parti
 
 // Per-tensor cast of launch_quantize_tensor with stochastic rounding: element
 // i (row-major) draws word i % 4 of Philox-4x32-10(counter = (i / 4, offset),
-// key = seed).
+// key = seed).  key_dev (nullable): take (seed, offset) from key_dev[0..1]
+// in device memory instead, and add 1 to key_dev[1] after the cast.
 cudaError_t launch_quantize_sr(const void* x, int64_t rows, int64_t cols, int fmt,
                                const float* scale, uint64_t seed, uint64_t offset, uint8_t* q,
-                               uint8_t* q_t, float* amax, cudaStream_t stream);
+                               uint8_t* q_t, float* amax, cudaStream_t stream,
+                               uint64_t* key_dev = nullptr);
 
 // Block cast: gran 1 (1x128) or 2 (128x128); writes q and 1/scale per block.
 // q_t (nullable, rows % 128 == 0): gran 1 -> the 1x128 block cast of x^T with

@@ -128,6 +128,15 @@ struct SrSched {
     uint32_t k0[10], k1[10], o0, o1;
 };
 
+// The key of a launch: the one passed by value, or (seed, counter) read
+// from device memory when key_dev is set.
+__device__ __forceinline__ SrKey sr_key_of(const SrKey& k, const unsigned long long* key_dev) {
+    if (!key_dev) return k;
+    const unsigned long long seed = key_dev[0], ctr = key_dev[1];
+    return SrKey{static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32),
+                 static_cast<uint32_t>(ctr), static_cast<uint32_t>(ctr >> 32)};
+}
+
 __device__ __forceinline__ SrSched sr_sched(const SrKey& k) {
     SrSched s;
 #pragma unroll
@@ -365,9 +374,10 @@ __global__ void __launch_bounds__(kThreads)
     quantize_flat_kernel(const uint4* __restrict__ x, int64_t n16, const uint16_t* __restrict__ xt,
                          int tail_n, const float* __restrict__ scale_p, uint4* __restrict__ q,
                          uint8_t* __restrict__ qtail, unsigned* amax_bits,
-                         unsigned long long* counts, SrKey sr_key) {
+                         unsigned long long* counts, SrKey sr_key,
+                         const unsigned long long* key_dev) {
     const float s = *scale_p;
-    const SrSched key = sr_sched(sr_key);
+    const SrSched key = sr_sched(sr_key_of(sr_key, SR ? key_dev : nullptr));
     uint32_t m = 0;
     CastCounts cc;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -495,10 +505,11 @@ __global__ void __launch_bounds__(kThreads)
                               int64_t tiles_c, const float* __restrict__ scale_p,
                               uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
                               unsigned* amax_bits, unsigned long long* counts, SrKey sr_key,
-                              float* __restrict__ dbias_partial) {
+                              float* __restrict__ dbias_partial,
+                              const unsigned long long* key_dev) {
     static_assert(!(SR && DBIAS), "the bias-gradient sums ride on the round-to-nearest cast");
     CastCounts cc;
-    const SrSched key = sr_sched(sr_key);
+    const SrSched key = sr_sched(sr_key_of(sr_key, SR ? key_dev : nullptr));
     __shared__ __align__(16) uint32_t S[128 * 32];
     const int64_t tile = blockIdx.x;
     const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
@@ -598,6 +609,10 @@ __global__ void dbias_finalize_kernel(const float* __restrict__ partial, int64_t
     for (int64_t p = 0; p < P; ++p) v = __fadd_rn(v, partial[p * cols + n]);
     dbias[n] = accumulate ? __fadd_rn(dbias[n], v) : v;
 }
+
+// The counter word of a device-held stochastic-rounding key moves on by
+// one after a cast has used it.
+__global__ void sr_advance_kernel(unsigned long long* key_dev) { key_dev[1] += 1ull; }
 
 // ----------------------------------------------------------- block casts
 
@@ -902,30 +917,33 @@ cudaError_t launch_update_scale(const float* amax, float* history, int32_t* pos,
 
 template <int FMT, bool AMAX, bool COUNT, bool SR>
 static void launch_flat(const void* x, int64_t n, const float* scale, uint8_t* q, float* amax,
-                        unsigned long long* counts, const SrKey& key, cudaStream_t stream) {
+                        unsigned long long* counts, const SrKey& key, cudaStream_t stream,
+                        const unsigned long long* key_dev = nullptr) {
     const int64_t n16 = n / 16;
     const int tail_n = static_cast<int>(n - n16 * 16);
     quantize_flat_kernel<FMT, AMAX, COUNT, SR><<<grid_for(n16 + 1, kThreads * 2), kThreads, 0, stream>>>(
         static_cast<const uint4*>(x), n16, static_cast<const uint16_t*>(x) + n16 * 16, tail_n,
         scale, reinterpret_cast<uint4*>(q), q + n16 * 16, reinterpret_cast<unsigned*>(amax), counts,
-        key);
+        key, key_dev);
 }
 
 template <int FMT, bool AMAX, bool COUNT, bool SR, bool DBIAS = false>
 static void launch_transpose(const void* x, int64_t rows, int64_t cols, const float* scale,
                              uint8_t* q, uint8_t* qt, float* amax, unsigned long long* counts,
-                             const SrKey& key, cudaStream_t stream, float* dbias_partial = nullptr) {
+                             const SrKey& key, cudaStream_t stream, float* dbias_partial = nullptr,
+                             const unsigned long long* key_dev = nullptr) {
     const int64_t tiles_c = (cols + 127) / 128, tiles_r = (rows + 127) / 128;
     quantize_transpose_kernel<FMT, AMAX, COUNT, SR, DBIAS><<<static_cast<unsigned>(tiles_r * tiles_c),
                                                              kThreads, 0, stream>>>(
         static_cast<const uint16_t*>(x), rows, cols, tiles_c, scale, q, qt,
-        reinterpret_cast<unsigned*>(amax), counts, key, dbias_partial);
+        reinterpret_cast<unsigned*>(amax), counts, key, dbias_partial, key_dev);
 }
 
 template <int FMT, bool AMAX, bool SR>
 static void launch_cast(const void* x, int64_t rows, int64_t cols, const float* scale, uint8_t* q,
                         uint8_t* q_t, float* amax, unsigned long long* counts, const SrKey& key,
-                        cudaStream_t stream, float* dbias_partial) {
+                        cudaStream_t stream, float* dbias_partial,
+                        const unsigned long long* key_dev) {
     if constexpr (!SR) {
         if (dbias_partial) {   // the bias-gradient sums ride on the transposing cast
             launch_transpose<FMT, AMAX, false, false, true>(x, rows, cols, scale, q, q_t, amax,
@@ -934,8 +952,8 @@ static void launch_cast(const void* x, int64_t rows, int64_t cols, const float* 
         }
     }
     if constexpr (SR) {
-        if (q_t) launch_transpose<FMT, AMAX, false, true>(x, rows, cols, scale, q, q_t, amax, nullptr, key, stream);
-        else launch_flat<FMT, AMAX, false, true>(x, rows * cols, scale, q, amax, nullptr, key, stream);
+        if (q_t) launch_transpose<FMT, AMAX, false, true>(x, rows, cols, scale, q, q_t, amax, nullptr, key, stream, nullptr, key_dev);
+        else launch_flat<FMT, AMAX, false, true>(x, rows * cols, scale, q, amax, nullptr, key, stream, key_dev);
     } else if (q_t) {
         if (counts) launch_transpose<FMT, AMAX, true, false>(x, rows, cols, scale, q, q_t, amax, counts, key, stream);
         else launch_transpose<FMT, AMAX, false, false>(x, rows, cols, scale, q, q_t, amax, counts, key, stream);
@@ -949,7 +967,8 @@ template <bool SR>
 static cudaError_t quantize_tensor(const void* x, int64_t rows, int64_t cols, int fmt,
                                    const float* scale, uint8_t* q, uint8_t* q_t, float* amax,
                                    unsigned long long* counts, const SrKey& key,
-                                   cudaStream_t stream, float* dbias_partial = nullptr) {
+                                   cudaStream_t stream, float* dbias_partial = nullptr,
+                                   const unsigned long long* key_dev = nullptr) {
     const int64_t n = rows * cols;
     if (amax) {
         cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), stream);
@@ -958,11 +977,11 @@ static cudaError_t quantize_tensor(const void* x, int64_t rows, int64_t cols, in
     if (n == 0) return cudaSuccess;
     const bool A = amax != nullptr;
     if (fmt == 0) {
-        if (A) launch_cast<0, true, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream, dbias_partial);
-        else launch_cast<0, false, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream, dbias_partial);
+        if (A) launch_cast<0, true, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream, dbias_partial, key_dev);
+        else launch_cast<0, false, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream, dbias_partial, key_dev);
     } else {
-        if (A) launch_cast<1, true, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream, dbias_partial);
-        else launch_cast<1, false, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream, dbias_partial);
+        if (A) launch_cast<1, true, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream, dbias_partial, key_dev);
+        else launch_cast<1, false, SR>(x, rows, cols, scale, q, q_t, amax, counts, key, stream, dbias_partial, key_dev);
     }
     return cudaGetLastError();
 }
@@ -991,10 +1010,16 @@ cudaError_t launch_dbias(const void* x, int64_t rows, int64_t cols, float* parti
 
 cudaError_t launch_quantize_sr(const void* x, int64_t rows, int64_t cols, int fmt,
                                const float* scale, uint64_t seed, uint64_t offset, uint8_t* q,
-                               uint8_t* q_t, float* amax, cudaStream_t stream) {
+                               uint8_t* q_t, float* amax, cudaStream_t stream,
+                               uint64_t* key_dev) {
     const SrKey key{static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32),
                     static_cast<uint32_t>(offset), static_cast<uint32_t>(offset >> 32)};
-    return quantize_tensor<true>(x, rows, cols, fmt, scale, q, q_t, amax, nullptr, key, stream);
+    auto* kd = reinterpret_cast<unsigned long long*>(key_dev);
+    cudaError_t e = quantize_tensor<true>(x, rows, cols, fmt, scale, q, q_t, amax, nullptr, key,
+                                          stream, nullptr, kd);
+    if (e != cudaSuccess || !key_dev) return e;
+    sr_advance_kernel<<<1, 1, 0, stream>>>(kd);
+    return cudaGetLastError();
 }
 
 template <int FMT>

@@ -153,3 +153,26 @@ def test_bias_argument_checks():
     assert "workspace" in F.fp8_last_error()
     assert L.fp8_linear_bwd(p, 256, 256, 256, ctypes.byref(r), ctypes.byref(st), p, p, 0,
                             ctypes.c_void_p(FAKE + 1), p, ws, None) == -3
+
+
+def test_sr_grad_recipe_checks():
+    L = F.lib()
+    p = ctypes.c_void_p(FAKE)
+    st = F.LinearStateC(*([FAKE] * (len(F.LinearStateC._fields_) - 1) + [None]))
+    assert F.fp8_workspace_size(256, 256, 256, F.Recipe(sr_grad=True)) > 0
+    # stochastic dY rounding is built for per-tensor scaling only
+    for mode in (F.SCALING_BLOCK, F.SCALING_ROW):
+        r = F.Recipe(scaling=mode, sr_grad=True)
+        assert F.fp8_workspace_size(256, 256, 256, r) == 0
+        assert L.fp8_linear_fwd(p, p, None, 256, 256, 256, ctypes.byref(r), ctypes.byref(st),
+                                p, None, 0, None) == -6
+    bad = F.Recipe(sr_grad=True)
+    bad.sr_grad = 2
+    assert L.fp8_linear_fwd(p, p, None, 256, 256, 256, ctypes.byref(bad), ctypes.byref(st),
+                            p, None, 0, None) == -1
+    # the backward needs the state's key
+    r = F.Recipe(sr_grad=True)
+    ws = F.fp8_workspace_size(256, 256, 256, r)
+    assert L.fp8_linear_bwd(p, 256, 256, 256, ctypes.byref(r), ctypes.byref(st), p, p, 0, None,
+                            p, ws, None) == -1
+    assert "sr_key" in F.fp8_last_error()

@@ -86,3 +86,36 @@ def test_gpu_draws_are_unbiased():
     f = (v - lo) / (hi - lo)
     sigma = (hi - lo) * (f * (1 - f) / d.numel()) ** 0.5
     assert abs(d.mean().item() - v) < 5 * sigma
+
+
+@pytest.mark.parametrize("scaling", [F.SCALING_DELAYED, F.SCALING_DYNAMIC], ids=["delayed", "dynamic"])
+def test_linear_with_stochastic_gradient_cast(scaling):
+    """recipe.sr_grad through fp8_linear_bwd: the dY codes bit-exact with the
+    oracle's quantize_sr(seed, call number) at every step, the scaling state
+    bit-exact, dX / dW within the GEMM bound, dbias unaffected, and the
+    device counter advanced once per call."""
+    from tests.helpers import assert_gemm_bound
+    M, N, K = 256, 384, 512
+    seed = 0xC0FFEE12345
+    rec = F.Recipe(scaling, history_len=16, sr_grad=True)
+    layer = F.Fp8Linear(M, N, K, rec, device=DEV, sr_seed=seed)
+    orec = oracle.Recipe(scaling=scaling, history_len=16, sr_grad=True)
+    ost = oracle.LinearState(orec, sr_seed=seed)
+    W = synthetic.normal((N, K), 0.02, seed=3)
+    db = torch.zeros(N, dtype=torch.float32, device=DEV)
+    for step in range(5):
+        X = synthetic.with_outlier_channels((M, K), 1.0, 4, 50.0, seed=10 + step)
+        dY = synthetic.student_t((M, N), 3, 1e-3, seed=20 + step)
+        layer.forward(X.to(DEV), W.to(DEV))
+        dX, dW = layer.backward(dY.to(DEV), dbias=db)
+        oracle.linear_fwd(bits(X), bits(W), orec, ost)
+        (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(bits(dY), orec, ost)
+        assert np.array_equal(u8(layer.workspace[:M * N].view(M, N)), ost.dy_q), step
+        for r in range(3):
+            assert f32bits(layer.scale[r].cpu().numpy()) == f32bits(ost.roles[r].scale[0])
+        assert_gemm_bound(dX, dXo, dXabs, what=f"dX step {step}")
+        assert_gemm_bound(dW, dWo, dWabs, what=f"dW step {step}")
+        s, sabs = oracle.dbias(bits(dY))
+        assert np.all(np.abs(db.cpu().numpy() - s) <= (18 * 2.0 ** -24) * sabs)
+    key = layer.sr_key.cpu().numpy().view(np.uint64)
+    assert int(key[0]) == seed and int(key[1]) == 5

@@ -172,3 +172,34 @@ def test_seed_and_offset_select_independent_draws():
         agree = np.mean(a == o)
         # independent draws with P(up) = 0.6: agreement 0.6^2 + 0.4^2 = 0.52
         assert 0.47 < agree < 0.57
+
+
+def test_linear_backward_with_stochastic_gradient_cast():
+    """recipe.sr_grad: backward call t casts dY with quantize_sr(seed, t); the
+    dequantised codes average to the scaled gradient over many calls."""
+    import torch
+    M, N, K = 32, 64, 32
+    X = torch.randn(M, K).to(torch.bfloat16)
+    W = (torch.randn(N, K) * 0.02).to(torch.bfloat16)
+    dY = torch.full((M, N), 0.3e-3, dtype=torch.float32)
+    dY[0, 0] = 1e-3                       # sets the amax: the rest falls between grid points
+    dY = dY.to(torch.bfloat16)
+    b = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    rec = oracle.Recipe(scaling=oracle.SCALING_DYNAMIC, sr_grad=True)
+    st = oracle.LinearState(rec, sr_seed=42)
+    codes = []
+    for t in range(40):
+        oracle.linear_fwd(b(X), b(W), rec, st)
+        oracle.linear_bwd(b(dY), rec, st)
+        want, _ = oracle.quantize_sr(b(dY), E5M2, st.roles[2].scale[0], 42, t)
+        assert np.array_equal(st.dy_q, want)
+        codes.append(oracle.decode(st.dy_q.ravel()[1:], E5M2))
+    assert st.sr_counter == 40
+    v = float(np.float32(float(dY[0, 1].float())) * np.float32(st.roles[2].scale[0]))
+    mean = np.mean(codes)
+    vals, _ = _table(E5M2)
+    k = int(np.searchsorted(vals, v, side="right")) - 1
+    lo, hi = vals[k], vals[k + 1]
+    f = (v - lo) / (hi - lo)
+    sigma = (hi - lo) * np.sqrt(f * (1 - f) / (40 * (M * N - 1)))
+    assert 0.05 < f < 0.95 and abs(mean - v) < 5 * sigma
