@@ -233,7 +233,7 @@ def run_gpu(args):
                      "frac": round(quant_gbs / hbm_gbs, 4), "peak_source": f"{peak_kind} hbm_gbs"},
         "kernels_ms_per_step": {k: round(v / comp["steps"], 4) for k, v in comp["by_kind"].items()},
         "component_pass_ms_per_step": round(comp["total_ms"] / comp["steps"], 4),
-        "gpu_launches": 8 * len(LINEARS) * args.steps,
+        "gpu_launches": 7 * len(LINEARS) * args.steps,
         "e2e": e2e,
         "small_case": small,
         "clocks": clk,

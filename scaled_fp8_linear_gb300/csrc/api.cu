@@ -188,6 +188,22 @@ size_t dbias_partial_bytes(int64_t M, int64_t N) {
 
 // Checks shared by the three backward variants: workspace size (the partial
 // sums only when dbias is wanted) and alignment.
+// The forward's per-tensor casts of X and W (with their amax if `amax`):
+// one launch over both tensors' tiles when both transposes are kept
+// (training), else one cast each.
+cudaError_t quantize_x_w(const void* X, const void* W, int64_t M, int64_t N, int64_t K, int f,
+                         const fp8_linear_state_t* s, bool amax, cudaStream_t st) {
+    if (s->x_qt && s->w_qt)
+        return launch_quantize_pair(X, M, K, s->scale + 0, s->x_q, s->x_qt, amax ? s->amax + 0 : nullptr,
+                                    W, N, K, s->scale + 1, s->w_q, s->w_qt, amax ? s->amax + 1 : nullptr,
+                                    f, st);
+    cudaError_t e = launch_quantize_tensor(X, M, K, f, s->scale + 0, s->x_q, s->x_qt,
+                                           amax ? s->amax + 0 : nullptr, st);
+    if (e != cudaSuccess) return e;
+    return launch_quantize_tensor(W, N, K, f, s->scale + 1, s->w_q, s->w_qt,
+                                  amax ? s->amax + 1 : nullptr, st);
+}
+
 int check_bwd_buffers(const void* dY, int64_t M, int64_t N, const fp8_recipe_t* recipe,
                       const fp8_linear_state_t* s, const void* dX, const float* dW,
                       const float* dbias, const void* workspace, size_t workspace_bytes) {
@@ -429,19 +445,13 @@ int fp8_linear_fwd(const void* X, const void* W, const void* bias, int64_t M, in
                                                   f, recipe->margin, recipe->pow2 != 0, s->scale,
                                                   s->scale_inv, 2, st, s->qscale_inv, 1),
                               "update scales"));
-        FP8_CHECK(cuda_status(launch_quantize_tensor(X, M, K, f, s->scale + 0, s->x_q, s->x_qt,
-                                                     nullptr, st), "quantize X"));
-        FP8_CHECK(cuda_status(launch_quantize_tensor(W, N, K, f, s->scale + 1, s->w_q, s->w_qt,
-                                                     nullptr, st), "quantize W"));
+        FP8_CHECK(cuda_status(quantize_x_w(X, W, M, N, K, f, s, false, st), "quantize X, W"));
         return launch_gemm(s->x_q, f, s->w_q, f, M, N, K, FP8_GRAN_TENSOR, s->scale_inv + 0,
                            FP8_GRAN_TENSOR, s->scale_inv + 1, bias, Y, FP8_OUT_BF16, 0, st);
     }
 
     // delayed: cast with the scales of earlier steps, fold this step's amax in afterwards
-    FP8_CHECK(cuda_status(launch_quantize_tensor(X, M, K, f, s->scale + 0, s->x_q, s->x_qt,
-                                                 s->amax + 0, st), "quantize X"));
-    FP8_CHECK(cuda_status(launch_quantize_tensor(W, N, K, f, s->scale + 1, s->w_q, s->w_qt,
-                                                 s->amax + 1, st), "quantize W"));
+    FP8_CHECK(cuda_status(quantize_x_w(X, W, M, N, K, f, s, true, st), "quantize X, W"));
     FP8_CHECK(launch_gemm(s->x_q, f, s->w_q, f, M, N, K, FP8_GRAN_TENSOR, s->scale_inv + 0,
                           FP8_GRAN_TENSOR, s->scale_inv + 1, bias, Y, FP8_OUT_BF16, 0, st));
     return cuda_status(launch_update_scale(s->amax, s->history, s->pos, H, recipe->amax_algo, f,

@@ -499,6 +499,50 @@ __device__ __forceinline__ void tile_column_sums(const uint4 (&va)[4], const uin
     }
 }
 
+// Round-to-nearest cast of the 128 x 128 tile at (r0, c0) of x [rows x
+// cols] with its transposed copy, staged in S (128 rows of 32 words);
+// optional fused amax, counters and bias-gradient sums.  CTA-collective.
+template <int FMT, bool AMAX, bool COUNT, bool DBIAS>
+__device__ __forceinline__ void rne_cast_transpose_tile(
+    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t r0, int64_t c0, float s,
+    uint8_t* __restrict__ q, uint8_t* __restrict__ qt, unsigned* amax_bits,
+    unsigned long long* counts, float* __restrict__ dbias_partial, uint32_t* S) {
+    CastCounts cc;
+    const SrSched key{};
+    const int t = threadIdx.x, cg = t & 7;
+    uint32_t m = 0;
+    // all of this thread's loads first (8 x 16 B in flight), then cast and store
+    uint4 va[4], vb[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int64_t r = r0 + it * 32 + (t >> 3), c = c0 + cg * 16;
+        va[it] = vb[it] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows && c < cols) {
+            const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + c);
+            va[it] = ldg_stream(src);
+            vb[it] = ldg_stream(src + 1);
+        }
+    }
+    if (DBIAS) tile_column_sums(va, vb, dbias_partial + (r0 >> 7) * cols, cols, c0);
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int rl = it * 32 + (t >> 3);
+        const int64_t r = r0 + rl, c = c0 + cg * 16;
+        const uint4 a = va[it], b = vb[it];
+        uint4 out = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows && c < cols) {
+            if (AMAX) m = absmax_vec(absmax_vec(m, a), b);
+            out = cast16<FMT, COUNT, false>(a, b, s, cc, key, 0);
+            *reinterpret_cast<uint4*>(q + r * cols + c) = out;
+        }
+        *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = out;
+    }
+    __syncthreads();
+    transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
+    if (AMAX) cta_amax_commit(m, amax_bits);
+    if (COUNT) cta_counts_commit(cc, counts);
+}
+
 template <int FMT, bool AMAX, bool COUNT, bool SR, bool DBIAS>
 __global__ void __launch_bounds__(kThreads)
     quantize_transpose_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
@@ -540,39 +584,34 @@ __global__ void __launch_bounds__(kThreads)
         transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
         if (AMAX) cta_amax_commit(m, amax_bits);
     } else {
-        // all of this thread's loads first (8 x 16 B in flight), then cast and store
-        uint4 va[4], vb[4];
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int64_t r = r0 + it * 32 + (t >> 3), c = c0 + cg * 16;
-            va[it] = vb[it] = make_uint4(0u, 0u, 0u, 0u);
-            if (r < rows && c < cols) {
-                const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + c);
-                va[it] = ldg_stream(src);
-                vb[it] = ldg_stream(src + 1);
-            }
-        }
-        if (DBIAS) tile_column_sums(va, vb, dbias_partial + (r0 >> 7) * cols, cols, c0);
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int rl = it * 32 + (t >> 3);
-            const int64_t r = r0 + rl, c = c0 + cg * 16;
-            const uint4 a = va[it], b = vb[it];
-            uint4 out = make_uint4(0u, 0u, 0u, 0u);
-            if (r < rows && c < cols) {
-                if (AMAX) m = absmax_vec(absmax_vec(m, a), b);
-                // cols % 16 == 0: the 16 elements are vector (r * cols + c) / 16
-                out = cast16<FMT, COUNT, SR>(a, b, s, cc, key, static_cast<uint64_t>(r * cols + c) >> 4);
-                *reinterpret_cast<uint4*>(q + r * cols + c) = out;
-            }
-            *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = out;
-        }
-        __syncthreads();
-
-        transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
-        if (AMAX) cta_amax_commit(m, amax_bits);
-        if (COUNT) cta_counts_commit(cc, counts);
+        rne_cast_transpose_tile<FMT, AMAX, COUNT, DBIAS>(x, rows, cols, r0, c0, s, q, qt, amax_bits,
+                                                         counts, dbias_partial, S);
     }
+}
+
+// One pass over the 128 x 128 tiles of two tensors (the X and W of a
+// forward pass): tiles [0, tiles0) belong to job 0, the rest to job 1.  One
+// launch instead of two, and the smaller tensor's tiles fill the other's
+// last wave.
+struct CastJob {
+    const uint16_t* x;
+    int64_t rows, cols, tiles_c;
+    const float* scale;
+    uint8_t* q;
+    uint8_t* qt;
+    unsigned* amax_bits;
+};
+
+template <int FMT, bool AMAX>
+__global__ void __launch_bounds__(kThreads)
+    quantize_transpose_pair_kernel(CastJob j0, CastJob j1, int64_t tiles0) {
+    __shared__ __align__(16) uint32_t S[128 * 32];
+    const bool second = blockIdx.x >= tiles0;
+    const CastJob& j = second ? j1 : j0;
+    const int64_t tile = second ? blockIdx.x - tiles0 : blockIdx.x;
+    const int64_t r0 = (tile / j.tiles_c) * 128, c0 = (tile % j.tiles_c) * 128;
+    rne_cast_transpose_tile<FMT, AMAX, false, false>(j.x, j.rows, j.cols, r0, c0, *j.scale, j.q,
+                                                     j.qt, j.amax_bits, nullptr, nullptr, S);
 }
 
 // Bias-gradient partial sums without a cast (for the block-wise and per-row
@@ -992,6 +1031,42 @@ cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, in
                                    float* dbias_partial) {
     return quantize_tensor<false>(x, rows, cols, fmt, scale, q, q_t, amax, counts, SrKey{},
                                   stream, dbias_partial);
+}
+
+cudaError_t launch_quantize_pair(const void* x0, int64_t rows0, int64_t cols0, const float* scale0,
+                                 uint8_t* q0, uint8_t* qt0, float* amax0, const void* x1,
+                                 int64_t rows1, int64_t cols1, const float* scale1, uint8_t* q1,
+                                 uint8_t* qt1, float* amax1, int fmt, cudaStream_t stream) {
+    const bool A = amax0 != nullptr;
+    if (A) {
+        cudaError_t e;
+        if (amax1 == amax0 + 1) {
+            e = cudaMemsetAsync(amax0, 0, 2 * sizeof(float), stream);
+        } else {
+            e = cudaMemsetAsync(amax0, 0, sizeof(float), stream);
+            if (e == cudaSuccess) e = cudaMemsetAsync(amax1, 0, sizeof(float), stream);
+        }
+        if (e != cudaSuccess) return e;
+    }
+    auto job = [](const void* x, int64_t rows, int64_t cols, const float* scale, uint8_t* q,
+                  uint8_t* qt, float* amax) {
+        return CastJob{static_cast<const uint16_t*>(x), rows, cols, (cols + 127) / 128, scale, q,
+                       qt, reinterpret_cast<unsigned*>(amax)};
+    };
+    const CastJob j0 = job(x0, rows0, cols0, scale0, q0, qt0, amax0);
+    const CastJob j1 = job(x1, rows1, cols1, scale1, q1, qt1, amax1);
+    const int64_t t0 = rows0 * cols0 ? ((rows0 + 127) / 128) * j0.tiles_c : 0;
+    const int64_t t1 = rows1 * cols1 ? ((rows1 + 127) / 128) * j1.tiles_c : 0;
+    if (t0 + t1 == 0) return cudaSuccess;
+    const unsigned grid = static_cast<unsigned>(t0 + t1);
+    if (fmt == 0) {
+        if (A) quantize_transpose_pair_kernel<0, true><<<grid, kThreads, 0, stream>>>(j0, j1, t0);
+        else quantize_transpose_pair_kernel<0, false><<<grid, kThreads, 0, stream>>>(j0, j1, t0);
+    } else {
+        if (A) quantize_transpose_pair_kernel<1, true><<<grid, kThreads, 0, stream>>>(j0, j1, t0);
+        else quantize_transpose_pair_kernel<1, false><<<grid, kThreads, 0, stream>>>(j0, j1, t0);
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_dbias(const void* x, int64_t rows, int64_t cols, float* partial,
