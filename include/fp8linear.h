@@ -320,9 +320,14 @@ int fp8_linear_bwd_noalloc(const void* dY, int64_t M, int64_t N, int64_t K,
 /* Message of the last failing call on this host thread ("" if none). */
 const char* fp8_last_error(void);
 
-/* Read (and, if clear != 0, reset) the device status word that kernels set
- * when a bounded wait gives up (bit 0: timeout).  Synchronises the device.
- * Returns FP8_OK and *status = 0 when every kernel finished normally. */
+/* Read (and, if clear != 0, reset) the device status word that kernels set:
+ *   bit 0 (1): a bounded wait gave up (timeout);
+ *   bit 1 (2): a scale update met a non-finite amax -- a NaN or Inf in a
+ *              cast tensor, or still in its amax history -- and kept the
+ *              previous scale ("Numerical-failure taxonomy": NaN / Inf are
+ *              caught at the first step that sees them).
+ * Synchronises the device.  Returns FP8_OK and *status = 0 when every
+ * kernel finished normally. */
 int fp8_device_status(int* status, int clear);
 
 #ifdef __cplusplus

@@ -960,6 +960,20 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
     return FP8_OK;
 }
 
+unsigned* device_status_word() {
+    static std::mutex mu;
+    static unsigned* ptr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        ptr[dev] = static_cast<unsigned*>(p);
+    }
+    return ptr[dev];
+}
+
 int read_device_status(unsigned* status, bool clear) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess)

@@ -87,8 +87,13 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
 // gradient's partial sums) for a valid recipe.
 size_t bwd_operand_workspace(int64_t M, int64_t N, const fp8_recipe_t* recipe);
 
-// Device status word (bit 0: a bounded wait timed out).
+// Device status word (bit 0: a bounded wait timed out; bit 1: a scale
+// update saw a non-finite amax).
 int read_device_status(unsigned* status, bool clear);
+
+// Device address of the status word on the current device (null if it
+// cannot be looked up), for kernels outside gemm.cu to set bits in.
+unsigned* device_status_word();
 
 // Record a message for fp8_last_error() and return `code`.
 int set_error(int code, const char* fmt, ...);

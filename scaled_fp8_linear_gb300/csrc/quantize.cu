@@ -329,7 +329,7 @@ __global__ void update_scale_kernel(const float* __restrict__ amax, float* __res
                                     int32_t* __restrict__ pos, int H, int algo, float fmax,
                                     int margin, int pow2, float* __restrict__ scale,
                                     float* __restrict__ scale_inv, float* __restrict__ saved,
-                                    int save_after) {
+                                    int save_after, unsigned* status) {
     const int r = blockIdx.x, lane = threadIdx.x;
     float* hist = history + static_cast<int64_t>(r) * H;
     const float a = amax[r];
@@ -353,6 +353,10 @@ __global__ void update_scale_kernel(const float* __restrict__ amax, float* __res
         if (saved && !save_after) saved[r] = scale_inv[r];
         hist[p] = a;
         pos[r] = (p + 1 == H) ? 0 : p + 1;
+        // a NaN or Inf in the tensor (or still in the history): the scale
+        // stays, and the device status word records it ("Numerical-failure
+        // taxonomy": catch NaN / Inf at the first step that sees them)
+        if (!isfinite(eff) && status) atomicOr(status, 2u);
         if (eff > 0.0f && isfinite(eff)) {
             float s = __fdiv_rn(fmax, eff);
             s = __fmul_rn(s, __uint_as_float(static_cast<uint32_t>(127 - margin) << 23));
@@ -950,7 +954,8 @@ cudaError_t launch_update_scale(const float* amax, float* history, int32_t* pos,
                                 int nroles, cudaStream_t stream, float* saved, int save_after) {
     const float fmax = fmt == 0 ? 448.0f : 57344.0f;
     update_scale_kernel<<<nroles, 32, 0, stream>>>(amax, history, pos, H, algo, fmax, margin,
-                                                   pow2, scale, scale_inv, saved, save_after);
+                                                   pow2, scale, scale_inv, saved, save_after,
+                                                   device_status_word());
     return cudaGetLastError();
 }
 

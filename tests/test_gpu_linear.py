@@ -289,3 +289,24 @@ def test_step_replays_from_a_cuda_graph():
     for a, c in zip(outs["eager"], outs["graph"]):
         assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
                            c.view(torch.int16) if c.dtype == torch.bfloat16 else c.view(torch.int32))
+
+
+def test_non_finite_input_is_flagged_and_the_scale_held():
+    """A NaN in X: the delayed update keeps the X scale and sets bit 1 of the
+    device status word, at this step and for as long as the NaN stays in the
+    amax history (4 steps here); the other roles are unaffected."""
+    M, N, K = 256, 256, 256
+    rec = F.Recipe(F.SCALING_DELAYED, history_len=4)
+    layer = F.Fp8Linear(M, N, K, rec, device=DEV)
+    W = synthetic.normal((N, K), 0.02, seed=1).to(DEV)
+    flags = []
+    for step in range(7):
+        X = synthetic.normal((M, K), 1.0, seed=10 + step)
+        if step == 1:
+            X[5, 7] = float("nan")
+        before = layer.scale.clone()
+        layer.forward(X.to(DEV), W)
+        flags.append(F.fp8_device_status(clear=True))
+        if step >= 1 and step <= 4:
+            assert layer.scale[0].item() == before[0].item(), step
+    assert flags == [0, 2, 2, 2, 2, 0, 0]

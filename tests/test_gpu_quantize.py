@@ -95,6 +95,10 @@ def test_update_scale_state_machine(algo, margin, pow2, fmt, H):
         amax.fill_(float(a))
         F.fp8_update_scale(amax, hist, pos, H, algo, fmt, margin, pow2, scale, sinv)
         oracle.update_scale(st, a, algo, fmt, margin, pow2)
+        # status bit 1: the effective amax (the new one, or the history max) is not finite
+        nonfinite = (not np.isfinite(a)) if algo == F.AMAX_MOST_RECENT else \
+            (not np.all(np.isfinite(st.history)))
+        assert F.fp8_device_status(clear=True) == (2 if nonfinite else 0), t
         assert f32bits(scale.cpu().numpy())[0] == f32bits(st.scale)[0], t
         assert f32bits(sinv.cpu().numpy())[0] == f32bits(st.scale_inv)[0], t
         assert pos.item() == st.pos[0]
