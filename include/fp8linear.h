@@ -236,6 +236,35 @@ int fp8_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int6
              const float* scale_inv_b, const void* bias, void* D, int out, int accumulate,
              void* stream);
 
+/* The arguments of one fp8_gemm call, for fp8_gemm_group. */
+typedef struct {
+    const uint8_t* A;
+    int32_t fa;
+    const uint8_t* B;
+    int32_t fb;
+    int64_t M, N, K;
+    int32_t layout;
+    int32_t ga;
+    const float* scale_inv_a;
+    int32_t gb;
+    const float* scale_inv_b;
+    const void* bias;
+    void* D;
+    int32_t out;
+    int32_t accumulate;
+} fp8_gemm_args_t;
+
+/* Two independent GEMMs in one launch: the same results, bit for bit, as
+ * fp8_gemm(g1) followed by fp8_gemm(g2).  When both are per-tensor / per-row
+ * problems of at least 256 rows without bias, one persistent CTA-pair grid
+ * deals both problems' 256 x 256 tiles from one list, the deeper problem's
+ * first, so that neither leaves a partly filled last wave of its own (the
+ * dgrad and wgrad of a backward pass are such a pair); otherwise the two run
+ * as two launches.  The problems run concurrently: neither may read or
+ * write the other's output.  Each is validated as by fp8_gemm; NULL g1 or
+ * g2 is FP8_ERR_INVALID_ARG. */
+int fp8_gemm_group(const fp8_gemm_args_t* g1, const fp8_gemm_args_t* g2, void* stream);
+
 /* Bytes of workspace that fp8_linear_bwd needs for a layer of this shape
  * and recipe: the quantised dY operands (and their scale arrays), plus
  * 4*ceil(M/128)*N bytes for the bias gradient's partial sums, which only a

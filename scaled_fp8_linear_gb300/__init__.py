@@ -25,7 +25,7 @@ __all__ = [
     "SCALING_DELAYED", "SCALING_DYNAMIC", "SCALING_BLOCK", "SCALING_ROW",
     "Fp8Error", "Recipe", "LinearStateC", "Fp8Linear", "build", "lib", "library_path",
     "fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_quantize_blocks",
-    "fp8_quantize_counted", "fp8_quantize_sr", "fp8_gemm",
+    "fp8_quantize_counted", "fp8_quantize_sr", "fp8_gemm", "fp8_gemm_group", "GemmArgsC",
     "fp8_workspace_size",
     "fp8_linear_fwd", "fp8_linear_bwd", "fp8_last_error", "fp8_device_status",
 ]
@@ -75,6 +75,15 @@ class Recipe(ctypes.Structure):
 _vp = ctypes.c_void_p
 
 
+class GemmArgsC(ctypes.Structure):
+    """fp8_gemm_args_t: the arguments of one fp8_gemm call."""
+    _fields_ = [("A", _vp), ("fa", ctypes.c_int32), ("B", _vp), ("fb", ctypes.c_int32),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("layout", ctypes.c_int32), ("ga", ctypes.c_int32), ("scale_inv_a", _vp),
+                ("gb", ctypes.c_int32), ("scale_inv_b", _vp), ("bias", _vp), ("D", _vp),
+                ("out", ctypes.c_int32), ("accumulate", ctypes.c_int32)]
+
+
 class LinearStateC(ctypes.Structure):
     """fp8_linear_state_t: device pointers of one layer's scaling state."""
     _fields_ = [("scale", _vp), ("scale_inv", _vp), ("amax", _vp), ("history", _vp),
@@ -104,6 +113,7 @@ def lib() -> ctypes.CDLL:
     L.fp8_quantize_sr.argtypes = [_vp, i64, i64, i, _vp, ctypes.c_uint64, ctypes.c_uint64,
                                   _vp, _vp, _vp, _vp]
     L.fp8_gemm.argtypes = [_vp, i, _vp, i, i64, i64, i64, i, i, _vp, i, _vp, _vp, _vp, i, i, _vp]
+    L.fp8_gemm_group.argtypes = [ctypes.POINTER(GemmArgsC), ctypes.POINTER(GemmArgsC), _vp]
     L.fp8_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(Recipe)]
     L.fp8_workspace_size.restype = sz
     L.fp8_linear_fwd.argtypes = [_vp, _vp, _vp, i64, i64, i64, ctypes.POINTER(Recipe),
@@ -113,7 +123,7 @@ def lib() -> ctypes.CDLL:
     L.fp8_last_error.restype = ctypes.c_char_p
     L.fp8_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), i]
     for name in ("fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_quantize_counted",
-                 "fp8_quantize_sr", "fp8_gemm", "fp8_linear_fwd",
+                 "fp8_quantize_sr", "fp8_gemm", "fp8_gemm_group", "fp8_linear_fwd",
                  "fp8_linear_bwd", "fp8_device_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -299,6 +309,33 @@ def fp8_gemm(A: torch.Tensor, fa: int, B: torch.Tensor, fb: int, scale_inv_a, sc
         _ptr(D, "D", torch.bfloat16 if out == OUT_BF16 else torch.float32), int(out),
         int(bool(accumulate)), _stream(stream)))
     return D
+
+
+def _gemm_args(A, fa, B, fb, scale_inv_a, scale_inv_b, ga=GRAN_TENSOR, gb=GRAN_TENSOR,
+               out=OUT_BF16, D=None, accumulate=False, layout=LAYOUT_TN, bias=None):
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("A and B disagree on K")
+    if D is None:
+        D = torch.empty(M, N, dtype=torch.bfloat16 if out == OUT_BF16 else torch.float32,
+                        device=A.device)
+    g = GemmArgsC(_ptr(A, "A", _U8), int(fa), _ptr(B, "B", _U8), int(fb), M, N, K, int(layout),
+                  int(ga), _ptr(scale_inv_a, "scale_inv_a", torch.float32), int(gb),
+                  _ptr(scale_inv_b, "scale_inv_b", torch.float32), _ptr(bias, "bias", torch.bfloat16),
+                  _ptr(D, "D", torch.bfloat16 if out == OUT_BF16 else torch.float32), int(out),
+                  int(bool(accumulate)))
+    return g, D
+
+
+def fp8_gemm_group(g1: dict, g2: dict, stream=None):
+    """Two independent GEMMs in one launch; g1, g2 hold fp8_gemm's arguments
+    by name (A, fa, B, fb, scale_inv_a, scale_inv_b and optionally ga, gb,
+    out, D, accumulate, bias).  Returns (D1, D2)."""
+    a1, D1 = _gemm_args(**g1)
+    a2, D2 = _gemm_args(**g2)
+    _check(lib().fp8_gemm_group(ctypes.byref(a1), ctypes.byref(a2), _stream(stream)))
+    return D1, D2
 
 
 def fp8_workspace_size(M: int, N: int, K: int, recipe: Recipe) -> int:

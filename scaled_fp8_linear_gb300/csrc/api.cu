@@ -279,10 +279,12 @@ int linear_bwd_row(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
         FP8_CHECK(cuda_status(launch_dbias(dY, M, N, partial, false, dbias, accumulate_dW, st),
                               "dbias"));
     }
-    FP8_CHECK(launch_gemm(dy_q, fb, s->w_qt, ff, M, K, N, FP8_GRAN_ROW, dy_s, FP8_GRAN_ROW,
-                          s->w_sinv_t, nullptr, dX, FP8_OUT_BF16, 0, st));
-    return launch_gemm(dy_qt, fb, s->x_qt, ff, N, K, M, FP8_GRAN_ROW, dy_st, FP8_GRAN_ROW,
-                       s->x_sinv_t, nullptr, dW, FP8_OUT_F32, accumulate_dW != 0, st);
+    return launch_gemm_group(
+        GemmArgs{dy_q, fb, s->w_qt, ff, M, K, N, FP8_GRAN_ROW, dy_s, FP8_GRAN_ROW, s->w_sinv_t,
+                 nullptr, dX, FP8_OUT_BF16, 0},
+        GemmArgs{dy_qt, fb, s->x_qt, ff, N, K, M, FP8_GRAN_ROW, dy_st, FP8_GRAN_ROW, s->x_sinv_t,
+                 nullptr, dW, FP8_OUT_F32, accumulate_dW != 0},
+        st);
 }
 
 }  // namespace
@@ -375,6 +377,22 @@ int fp8_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int6
         return set_error(FP8_ERR_ALIGN, "fp8_gemm: bias must be 16-byte aligned");
     return launch_gemm(A, fa, B, fb, M, N, K, ga, scale_inv_a, gb, scale_inv_b, bias, D, out,
                        accumulate != 0, as_stream(stream));
+}
+
+int fp8_gemm_group(const fp8_gemm_args_t* g1, const fp8_gemm_args_t* g2, void* stream) {
+    if (!g1 || !g2) return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm_group: NULL problem");
+    for (const fp8_gemm_args_t* g : {g1, g2}) {
+        FP8_CHECK(check_gemm_args(g->A, g->fa, g->B, g->fb, g->M, g->N, g->K, g->layout, g->ga,
+                                  g->scale_inv_a, g->gb, g->scale_inv_b, g->D, g->out,
+                                  g->accumulate));
+        if (g->bias && !aligned16(g->bias))
+            return set_error(FP8_ERR_ALIGN, "fp8_gemm_group: bias must be 16-byte aligned");
+    }
+    auto args = [](const fp8_gemm_args_t* g) {
+        return GemmArgs{g->A, g->fa, g->B, g->fb, g->M, g->N, g->K, g->ga, g->scale_inv_a,
+                        g->gb, g->scale_inv_b, g->bias, g->D, g->out, g->accumulate != 0};
+    };
+    return launch_gemm_group(args(g1), args(g2), as_stream(stream));
 }
 
 size_t fp8_workspace_size(int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe) {
@@ -510,12 +528,14 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
     if (dbias)
         FP8_CHECK(cuda_status(launch_dbias(dY, M, N, partial, fused_partial != nullptr, dbias,
                                            accumulate_dW, st), "dbias"));
-    // dgrad: dX [M x K] = dY_q [M x N] . (W_q^T [K x N])^T
-    FP8_CHECK(launch_gemm(dy_q, fb, s->w_qt, ff, M, K, N, FP8_GRAN_TENSOR, s->scale_inv + 2,
-                          FP8_GRAN_TENSOR, s->qscale_inv + 1, nullptr, dX, FP8_OUT_BF16, 0, st));
-    // wgrad: dW [N x K] (+)= dY_q^T [N x M] . (X_q^T [K x M])^T
-    FP8_CHECK(launch_gemm(dy_qt, fb, s->x_qt, ff, N, K, M, FP8_GRAN_TENSOR, s->scale_inv + 2,
-                          FP8_GRAN_TENSOR, s->qscale_inv + 0, nullptr, dW, FP8_OUT_F32, accumulate_dW != 0, st));
+    // dgrad: dX [M x K] = dY_q [M x N] . (W_q^T [K x N])^T, and
+    // wgrad: dW [N x K] (+)= dY_q^T [N x M] . (X_q^T [K x M])^T, in one launch
+    FP8_CHECK(launch_gemm_group(
+        GemmArgs{dy_q, fb, s->w_qt, ff, M, K, N, FP8_GRAN_TENSOR, s->scale_inv + 2,
+                 FP8_GRAN_TENSOR, s->qscale_inv + 1, nullptr, dX, FP8_OUT_BF16, 0},
+        GemmArgs{dy_qt, fb, s->x_qt, ff, N, K, M, FP8_GRAN_TENSOR, s->scale_inv + 2,
+                 FP8_GRAN_TENSOR, s->qscale_inv + 0, nullptr, dW, FP8_OUT_F32, accumulate_dW != 0},
+        st));
     if (recipe->scaling == FP8_SCALING_DELAYED)
         return cuda_status(launch_update_scale(s->amax + 2, h2, s->pos + 2, H, recipe->amax_algo, fb,
                                                recipe->margin, recipe->pow2 != 0, s->scale + 2,

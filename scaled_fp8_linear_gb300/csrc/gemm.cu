@@ -368,7 +368,10 @@ __global__ void __launch_bounds__(256, 1)
 template <int STAGES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ GemmParams p,
+                     const __grid_constant__ CUtensorMap tmA2,
+                     const __grid_constant__ CUtensorMap tmB2,
+                     const __grid_constant__ GemmParams p2) {
     constexpr int HALF = 128;              // rows of A and of B held by each CTA
     constexpr int TILE = 2 * HALF;         // pair tile: 256 x 256
     constexpr int A_BYTES = HALF * BK, B_BYTES = HALF * BK;
@@ -401,9 +404,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
+    // work units: the tiles of problem 1, then those of problem 2 (a second
+    // GEMM of the same pass, e.g. the dgrad next to the wgrad; none if
+    // p2.num_m == 0), dealt round-robin to the clusters
+    const int t1 = p.num_m * p.num_n;
+    const int num_units = t1 + p2.num_m * p2.num_n;
     if (warp == 0 && lane == 0) {
         ptx::tma_prefetch_desc(&tmA);
         ptx::tma_prefetch_desc(&tmB);
+        if (num_units > t1) {
+            ptx::tma_prefetch_desc(&tmA2);
+            ptx::tma_prefetch_desc(&tmB2);
+        }
     }
     if (warp == 2) {
         ptx::tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -413,7 +425,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     ptx::cluster_sync();   // the peer's barriers exist before any remote arrival
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int num_tiles = p.num_m * p.num_n;
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
     if (warp == 0) {
@@ -421,18 +432,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             uint32_t stage = 0, phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
+            for (int u = pair; ok && u < num_units; u += npairs) {
+                const bool second = u >= t1;
+                const GemmParams& q = second ? p2 : p;
+                const CUtensorMap* ma = second ? &tmA2 : &tmA;
+                const CUtensorMap* mb = second ? &tmB2 : &tmB;
                 int m_blk, n_blk;
-                tile_coords<>(tile, p.num_m, p.num_n, m_blk, n_blk);
+                tile_coords<>(second ? u - t1 : u, q.num_m, q.num_n, m_blk, n_blk);
                 const int ya = m_blk * TILE + static_cast<int>(rank) * HALF;
                 const int yb = n_blk * TILE + static_cast<int>(rank) * HALF;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = 0; kb < q.num_kb; ++kb) {
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
                     uint8_t* sa = ring + stage * STAGE_BYTES;
                     const uint32_t bar = ptx::cluster_addr(&full[stage], 0);
                     if (leader) ptx::mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
-                    ptx::tma_load_2d_pair(sa, &tmA, bar, kb * BK, ya);
-                    ptx::tma_load_2d_pair(sa + A_BYTES, &tmB, bar, kb * BK, yb);
+                    ptx::tma_load_2d_pair(sa, ma, bar, kb * BK, ya);
+                    ptx::tma_load_2d_pair(sa + A_BYTES, mb, bar, kb * BK, yb);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -455,14 +470,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
-            const uint32_t idesc = ptx::idesc_f8f6f4(p.fa, p.fb, TILE, TILE);
+            const uint32_t idesc1 = ptx::idesc_f8f6f4(p.fa, p.fb, TILE, TILE);
+            const uint32_t idesc2 = ptx::idesc_f8f6f4(p2.fa, p2.fb, TILE, TILE);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int tile = pair; ok && tile < num_tiles; tile += npairs) {
+            for (int u = pair; ok && u < num_units; u += npairs) {
+                const int num_kb = u >= t1 ? p2.num_kb : p.num_kb;
+                const uint32_t idesc = u >= t1 ? idesc2 : idesc1;
                 if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) break;
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + acc * TILE;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = 0; kb < num_kb; ++kb) {
                     if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
                     ptx::tc_fence_after();
                     uint8_t* sa = ring + stage * STAGE_BYTES;
@@ -487,11 +505,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     } else if (warp >= 4) {
         const int qd = warp & 3;
         const int row = qd * 32 + lane;
-        const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
+        const GemmParams& p1 = p;
         uint32_t acc = 0, acc_phase = 0;
-        for (int tile = pair; tile < num_tiles; tile += npairs) {
+        for (int u = pair; u < num_units; u += npairs) {
+            const bool second = u >= t1;
+            const GemmParams& p = second ? p2 : p1;   // this unit's problem
+            const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
             int m_blk, n_blk;
-            tile_coords<>(tile, p.num_m, p.num_n, m_blk, n_blk);
+            tile_coords<>(second ? u - t1 : u, p.num_m, p.num_n, m_blk, n_blk);
             const int64_t m = static_cast<int64_t>(m_blk) * TILE + rank * HALF + row;
             if (rmw) prefetch_row(m, static_cast<int64_t>(n_blk) * TILE, TILE, p);
             bool ok = (lane == 0) ? ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag) : false;
@@ -937,7 +958,8 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
         const int64_t clusters =
             pair_clusters(reinterpret_cast<const void*>(k), 0, 256, kPairSmemBytes);
         const int pgrid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
-        k<<<pgrid, 256, kPairSmemBytes, stream>>>(tmA, tmB, p);
+        GemmParams none{};
+        k<<<pgrid, 256, kPairSmemBytes, stream>>>(tmA, tmB, p, tmA, tmB, none);
     } else if (!block) {
         using L = Layout<kTensorBN, kTensorStages>;
         auto k = gemm_tensor_kernel<kTensorBN, kTensorStages>;
@@ -955,6 +977,60 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
             k<<<grid, kBlockThreads, L::SMEM_BYTES, stream>>>(tmA, tmB, p);
         }
     }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(FP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+    return FP8_OK;
+}
+
+namespace {
+
+// A problem the CTA-pair kernel takes: per-tensor or per-row scales, at least
+// 256 rows, a nonempty K.
+bool pair_eligible(const GemmArgs& g) {
+    const bool block = g.ga == FP8_GRAN_1x128 || g.ga == FP8_GRAN_128x128 ||
+                       g.gb == FP8_GRAN_1x128 || g.gb == FP8_GRAN_128x128;
+    return !block && g.M >= kPairMinRows && g.N > 0 && g.K > 0 && !g.bias;
+}
+
+int pair_params(const GemmArgs& g, GemmParams& p, CUtensorMap& tmA, CUtensorMap& tmB) {
+    p = GemmParams{};
+    p.M = g.M; p.N = g.N; p.K = g.K;
+    p.num_m = static_cast<int>((g.M + 255) / 256);
+    p.num_n = static_cast<int>((g.N + kTensorBN - 1) / kTensorBN);
+    p.num_kb = static_cast<int>((g.K + BK - 1) / BK);
+    p.fa = g.fa; p.fb = g.fb; p.ga = g.ga; p.gb = g.gb; p.sa = g.sa; p.sb = g.sb;
+    p.bias = static_cast<const __nv_bfloat16*>(g.bias);
+    p.D = g.D; p.out = g.out; p.accumulate = g.accumulate;
+    int st = make_kmajor_map(&tmA, g.A, g.M, g.K, BM);
+    if (st != FP8_OK) return st;
+    return make_kmajor_map(&tmB, g.B, g.N, g.K, 128);
+}
+
+}  // namespace
+
+int launch_gemm_group(const GemmArgs& g1, const GemmArgs& g2, cudaStream_t stream) {
+    if (!pair_eligible(g1) || !pair_eligible(g2)) {
+        int st = launch_gemm(g1.A, g1.fa, g1.B, g1.fb, g1.M, g1.N, g1.K, g1.ga, g1.sa, g1.gb,
+                             g1.sb, g1.bias, g1.D, g1.out, g1.accumulate, stream);
+        if (st != FP8_OK) return st;
+        return launch_gemm(g2.A, g2.fa, g2.B, g2.fb, g2.M, g2.N, g2.K, g2.ga, g2.sa, g2.gb,
+                           g2.sb, g2.bias, g2.D, g2.out, g2.accumulate, stream);
+    }
+    GemmParams p1, p2;
+    CUtensorMap a1, b1, a2, b2;
+    int st = pair_params(g1, p1, a1, b1);
+    if (st == FP8_OK) st = pair_params(g2, p2, a2, b2);
+    if (st != FP8_OK) return st;
+    // the deeper problem's tiles first, so the last round holds the cheaper tiles
+    const bool swap = p2.num_kb > p1.num_kb;
+    auto k = gemm_pair_kernel<kPairStages>;
+    if ((st = ensure_smem(k, kPairSmemBytes, 2)) != FP8_OK) return st;
+    const int64_t units = static_cast<int64_t>(p1.num_m) * p1.num_n +
+                          static_cast<int64_t>(p2.num_m) * p2.num_n;
+    const int64_t clusters = pair_clusters(reinterpret_cast<const void*>(k), 0, 256, kPairSmemBytes);
+    const int grid = static_cast<int>(2 * (units < clusters ? units : clusters));
+    if (swap) k<<<grid, 256, kPairSmemBytes, stream>>>(a2, b2, p2, a1, b1, p1);
+    else k<<<grid, 256, kPairSmemBytes, stream>>>(a1, b1, p1, a2, b2, p2);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(FP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
     return FP8_OK;

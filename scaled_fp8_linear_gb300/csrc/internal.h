@@ -87,6 +87,30 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
 // gradient's partial sums) for a valid recipe.
 size_t bwd_operand_workspace(int64_t M, int64_t N, const fp8_recipe_t* recipe);
 
+// The arguments of one launch_gemm call.
+struct GemmArgs {
+    const uint8_t* A;
+    int fa;
+    const uint8_t* B;
+    int fb;
+    int64_t M, N, K;
+    int ga;
+    const float* sa;
+    int gb;
+    const float* sb;
+    const void* bias;
+    void* D;
+    int out;
+    int accumulate;
+};
+
+// Two independent GEMMs of one pass (the dgrad and the wgrad of a backward)
+// in one persistent launch of the CTA-pair kernel: both problems' tiles are
+// dealt to the clusters from one list, the deeper problem's first, so that
+// neither leaves a partly filled last wave of its own.  Falls back to two
+// launch_gemm calls when either problem is not a CTA-pair problem.
+int launch_gemm_group(const GemmArgs& g1, const GemmArgs& g2, cudaStream_t stream);
+
 // Device status word (bit 0: a bounded wait timed out; bit 1: a scale
 // update saw a non-finite amax).
 int read_device_status(unsigned* status, bool clear);

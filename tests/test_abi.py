@@ -176,3 +176,16 @@ def test_sr_grad_recipe_checks():
     assert L.fp8_linear_bwd(p, 256, 256, 256, ctypes.byref(r), ctypes.byref(st), p, p, 0, None,
                             p, ws, None) == -1
     assert "sr_key" in F.fp8_last_error()
+
+
+def test_gemm_group_argument_checks():
+    L = F.lib()
+    one = ctypes.c_void_p(FAKE)
+    good = F.GemmArgsC(one, 0, one, 0, 256, 256, 256, 0, 0, one, 0, one, None, one, 0, 0)
+    bad = F.GemmArgsC(one, 0, one, 0, 256, 120, 256, 0, 0, one, 0, one, None, one, 0, 0)
+    assert L.fp8_gemm_group(None, ctypes.byref(good), None) == -1
+    assert L.fp8_gemm_group(ctypes.byref(good), None, None) == -1
+    assert L.fp8_gemm_group(ctypes.byref(good), ctypes.byref(bad), None) == -2   # N % 16
+    odd_bias = F.GemmArgsC(one, 0, one, 0, 256, 256, 256, 0, 0, one, 0, one,
+                           ctypes.c_void_p(FAKE + 2), one, 0, 0)
+    assert L.fp8_gemm_group(ctypes.byref(odd_bias), ctypes.byref(good), None) == -3

@@ -184,3 +184,64 @@ def test_row_scaled(M, N, K, ga, gb, out):
     D = F.fp8_gemm(_t(A), F.E4M3, _t(B), F.E4M3, _s(sa), _s(sb), ga, gb, out=out)
     Do, Dabs = oracle.gemm(A, F.E4M3, B, F.E4M3, sa, sb, ga, gb)
     assert_gemm_bound(D, Do, Dabs, what=f"row {M}x{N}x{K}")
+
+
+def _rand_codes(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    v = torch.randint(0, 0x7C, shape, generator=g, dtype=torch.int32)
+    v |= torch.randint(0, 2, shape, generator=g, dtype=torch.int32) << 7
+    return v.to(torch.uint8).to(DEV)
+
+
+@pytest.mark.parametrize("case", ["bwd_like", "ragged", "rowscaled", "fallback_block", "small_m"])
+def test_gemm_group_equals_two_gemms(case):
+    """fp8_gemm_group gives, bit for bit, the results of two fp8_gemm calls:
+    the grouped CTA-pair launch computes every tile exactly as the single
+    launch does; problems it does not take fall back to two launches."""
+    one = torch.ones(1, dtype=torch.float32, device=DEV)
+    if case == "bwd_like":        # dgrad (bf16) and wgrad (FP32, accumulated) of a linear
+        M, N, K = 1024, 768, 640
+        g1 = dict(A=_rand_codes((M, N), 1), fa=F.E5M2, B=_rand_codes((K, N), 2), fb=F.E4M3,
+                  scale_inv_a=one * 2 ** -7, scale_inv_b=one * 2 ** -5)
+        g2 = dict(A=_rand_codes((N, M), 3), fa=F.E5M2, B=_rand_codes((K, M), 4), fb=F.E4M3,
+                  scale_inv_a=one * 2 ** -7, scale_inv_b=one * 2 ** -6, out=F.OUT_F32,
+                  accumulate=True)
+    elif case == "ragged":
+        g1 = dict(A=_rand_codes((400, 272), 5), fa=F.E4M3, B=_rand_codes((528, 272), 6),
+                  fb=F.E4M3, scale_inv_a=one, scale_inv_b=one)
+        g2 = dict(A=_rand_codes((300, 1056), 7), fa=F.E4M3, B=_rand_codes((144, 1056), 8),
+                  fb=F.E5M2, scale_inv_a=one, scale_inv_b=one * 0.5)
+    elif case == "rowscaled":
+        s = lambda n, sd: (torch.rand(n, generator=torch.Generator().manual_seed(sd)) + 0.5).to(DEV)
+        g1 = dict(A=_rand_codes((512, 256), 9), fa=F.E4M3, B=_rand_codes((384, 256), 10),
+                  fb=F.E4M3, scale_inv_a=s(512, 1), scale_inv_b=s(384, 2), ga=F.GRAN_ROW,
+                  gb=F.GRAN_ROW)
+        g2 = dict(A=_rand_codes((384, 512), 11), fa=F.E5M2, B=_rand_codes((256, 512), 12),
+                  fb=F.E4M3, scale_inv_a=s(384, 3), scale_inv_b=s(256, 4), ga=F.GRAN_ROW,
+                  gb=F.GRAN_ROW)
+    elif case == "fallback_block":
+        sa = torch.rand(256, 2, generator=torch.Generator().manual_seed(5)).to(DEV) + 0.5
+        sb = torch.rand(2, 2, generator=torch.Generator().manual_seed(6)).to(DEV) + 0.5
+        g1 = dict(A=_rand_codes((256, 256), 13), fa=F.E4M3, B=_rand_codes((256, 256), 14),
+                  fb=F.E4M3, scale_inv_a=sa, scale_inv_b=sb, ga=F.GRAN_1x128, gb=F.GRAN_128x128)
+        g2 = dict(A=_rand_codes((512, 256), 15), fa=F.E4M3, B=_rand_codes((256, 256), 16),
+                  fb=F.E4M3, scale_inv_a=one, scale_inv_b=one)
+    else:                          # M < 256: the 1-CTA kernel, two launches
+        g1 = dict(A=_rand_codes((128, 256), 17), fa=F.E4M3, B=_rand_codes((256, 256), 18),
+                  fb=F.E4M3, scale_inv_a=one, scale_inv_b=one)
+        g2 = dict(A=_rand_codes((512, 256), 19), fa=F.E4M3, B=_rand_codes((256, 256), 20),
+                  fb=F.E4M3, scale_inv_a=one, scale_inv_b=one)
+    prev = None
+    if g2.get("out") == F.OUT_F32:
+        prev = torch.randn(g2["A"].shape[0], g2["B"].shape[0], device=DEV)
+        g2["D"] = prev.clone()
+    D1, D2 = F.fp8_gemm_group(g1, g2)
+    r1 = F.fp8_gemm(**g1)
+    g2b = dict(g2)
+    if prev is not None:
+        g2b["D"] = prev.clone()
+    r2 = F.fp8_gemm(**g2b)
+    torch.cuda.synchronize()
+    for a, b in ((D1, r1), (D2, r2)):
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32))
