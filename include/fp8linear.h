@@ -262,7 +262,9 @@ typedef struct {
  * dgrad and wgrad of a backward pass are such a pair); otherwise the two run
  * as two launches.  The problems run concurrently: neither may read or
  * write the other's output.  Each is validated as by fp8_gemm; NULL g1 or
- * g2 is FP8_ERR_INVALID_ARG. */
+ * g2 is FP8_ERR_INVALID_ARG.  (The pages have no counterpart: this is a
+ * scheduling property of the library -- the dgrad and wgrad GEMMs of
+ * "Transformer Engine internals" computed together -- not of the method.) */
 int fp8_gemm_group(const fp8_gemm_args_t* g1, const fp8_gemm_args_t* g2, void* stream);
 
 /* Bytes of workspace that fp8_linear_bwd needs for a layer of this shape
