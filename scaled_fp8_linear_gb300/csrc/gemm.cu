@@ -28,6 +28,7 @@
 // Block-scaled kernel: BM x BN = 128 x 128, four TMEM partial-sum buffers
 // rotated per 128-deep K block; 8 epilogue warps promote them into FP32
 // registers.
+#include <atomic>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -846,14 +847,15 @@ int ensure_smem(Kernel k, int bytes, int kernel_id) {
     static std::mutex mu;
     static bool done[64][8] = {};   // [device][kernel id]: every GEMM kernel has this one type
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    const bool cached = dev >= 0 && dev < 64;   // other devices: set it on every call
     std::lock_guard<std::mutex> lock(mu);
-    if (done[dev][kernel_id]) return FP8_OK;
+    if (cached && done[dev][kernel_id]) return FP8_OK;
     const cudaError_t e =
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess)
         return set_error(FP8_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    done[dev][kernel_id] = true;
+    if (cached) done[dev][kernel_id] = true;
     return FP8_OK;
 }
 
@@ -863,9 +865,10 @@ int pair_clusters(const void* func, int kernel_id, int threads, int smem) {
     static std::mutex mu;
     static int cache[64][1] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    int uncached = 0;                            // devices past the table: computed per call
     std::lock_guard<std::mutex> lock(mu);
-    int& c = cache[dev][kernel_id];
+    int& c = (dev >= 0 && dev < 64) ? cache[dev][kernel_id] : uncached;
     if (c == 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * 1024, 1, 1);
@@ -884,16 +887,16 @@ int pair_clusters(const void* func, int kernel_id, int threads, int smem) {
 }  // namespace
 
 int num_sms() {
-    static int cache[64] = {};
+    static std::atomic<int> cache[64] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (cache[dev] == 0) {
-        int n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+    int n = dev < 64 ? cache[dev].load(std::memory_order_relaxed) : 0;
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
             n = 148;
-        cache[dev] = n;
+        if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
 // D[m][n] (+)= bias[n] for a GEMM with K = 0 (grid-stride over M x N).
@@ -1040,14 +1043,16 @@ unsigned* device_status_word() {
     static std::mutex mu;
     static unsigned* ptr[64] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (!ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-        ptr[dev] = static_cast<unsigned*>(p);
+    if (dev < 64 && ptr[dev]) return ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
     }
-    return ptr[dev];
+    if (dev < 64) ptr[dev] = static_cast<unsigned*>(p);
+    return static_cast<unsigned*>(p);
 }
 
 int read_device_status(unsigned* status, bool clear) {
