@@ -665,12 +665,27 @@ def run_kernel(args):
         qt = torch.empty(C, R, dtype=torch.uint8, device=dev)
         am = torch.empty(1, dtype=torch.float32, device=dev)
         one = torch.ones(1, dtype=torch.float32, device=dev)
+        gran = {"tensor": F.GRAN_TENSOR, "1x128": F.GRAN_1x128, "128x128": F.GRAN_128x128,
+                "row": F.GRAN_ROW}[args.gran]
+        transpose = not args.no_transpose
+        qt_arg = qt if transpose else None
+        # algorithmic bytes: bf16 read, codes (and transposed codes), scale arrays
+        work = (2.0 + (2.0 if transpose else 1.0)) * R * C
         if args.kernel == "quantize_sr":
             seed = iter(range(1, 1 << 30))
-            call = lambda: F.fp8_quantize_sr(x, fa, one, next(seed), 0, q=q, q_t=qt, amax_out=am)
+            call = lambda: F.fp8_quantize_sr(x, fa, one, next(seed), 0, q=q, q_t=qt_arg, amax_out=am)
+        elif gran == F.GRAN_TENSOR:
+            call = lambda: F.fp8_quantize(x, fa, scale=one, q=q, q_t=qt_arg, amax_out=am)
         else:
-            call = lambda: F.fp8_quantize(x, fa, scale=one, q=q, q_t=qt, amax_out=am)
-        work, unit, peak = 4.0 * R * C, "GB/s", hbm_gbs
+            s1 = torch.empty(F._scale_shape(gran, R, C), dtype=torch.float32, device=dev)
+            st_ = None
+            if transpose:
+                st_ = torch.empty(F._scale_shape_t(gran, R, C), dtype=torch.float32, device=dev)
+                work += 4.0 * st_.numel()
+            work += 4.0 * s1.numel()
+            call = lambda: F.fp8_quantize(x, fa, gran, q=q, q_t=qt_arg, scale_inv_blocks=s1,
+                                          scale_inv_blocks_t=st_)
+        unit, peak = "GB/s", hbm_gbs
     for _ in range(args.warmup):
         call()
     stream = torch.cuda.current_stream()
@@ -687,7 +702,10 @@ def run_kernel(args):
     med = ms[len(ms) // 2]
     scale = 1e12 if unit == "TFLOP/s" else 1e9
     ach = work / (med * 1e-3) / scale
-    print(json.dumps({"kernel": args.kernel, "shape": dims, "format": args.fmt,
+    extra = {}
+    if args.kernel in ("quantize", "quantize_sr"):
+        extra = {"granularity": args.gran, "transpose": not args.no_transpose}
+    print(json.dumps({"kernel": args.kernel, "shape": dims, "format": args.fmt, **extra,
                       "median_ms": round(med, 4), "min_ms": round(ms[0], 4),
                       "achieved": round(ach, 1), "unit": unit, "peak": round(peak, 1),
                       "frac": round(ach / peak, 4),
@@ -769,6 +787,10 @@ def main():
     ap.add_argument("--shape", default="8192,12288,4096")
     ap.add_argument("--fmt", choices=["e4m3", "e5m2"], default="e4m3")
     ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--gran", choices=["tensor", "1x128", "128x128", "row"], default="tensor",
+                    help="--kernel quantize: scale granularity")
+    ap.add_argument("--no-transpose", action="store_true",
+                    help="--kernel quantize / quantize_sr: no transposed copy")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

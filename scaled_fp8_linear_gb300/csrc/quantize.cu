@@ -665,28 +665,41 @@ template <int FMT>
 __global__ void __launch_bounds__(kThreads)
     quantize_1x128_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int pow2,
                           uint8_t* __restrict__ q, float* __restrict__ scale_inv) {
-    const int64_t KB = cols / 128;
-    const int64_t nseg = rows * KB;
+    // a half-warp per 128-element segment, a warp per pair of segments; each
+    // warp takes kU pairs per step with all their loads issued first, so that
+    // enough bytes are in flight to cover the memory latency
+    constexpr int kU = 4;
+    const int64_t nseg = rows * (cols / 128);
     const int64_t npairs = (nseg + 1) / 2;
     const int lane = threadIdx.x & 31, sub = lane & 15;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    for (int64_t p = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-         p < npairs; p += warps) {
-        const int64_t seg = 2 * p + (lane >> 4);
-        const bool valid = seg < nseg;
-        const int64_t row = seg / KB, kb = seg - row * KB;
-        const int64_t off = row * cols + kb * 128 + sub * 8;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) v = ldg_stream(reinterpret_cast<const uint4*>(x + off));
-        uint32_t m2 = absmax_vec(0u, v);
-        uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    for (int64_t p0 = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         p0 < npairs; p0 += kU * warps) {
+        uint4 v[kU];
+        int64_t off[kU], seg[kU];
+        bool valid[kU];
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        const float s = block_scale<FMT>(__uint_as_float(m << 16), pow2);
-        if (valid) {
-            *reinterpret_cast<uint2*>(q + off) =
-                make_uint2(cvt4<FMT>(v.x, v.y, s), cvt4<FMT>(v.z, v.w, s));
-            if (sub == 0) scale_inv[seg] = __fdiv_rn(1.0f, s);
+        for (int u = 0; u < kU; ++u) {
+            const int64_t p = p0 + u * warps;
+            seg[u] = 2 * p + (lane >> 4);
+            valid[u] = p < npairs && seg[u] < nseg;
+            // cols = 128 * KB: segment seg starts at element 128 * seg
+            off[u] = seg[u] * 128 + sub * 8;
+            v[u] = valid[u] ? ldg_stream(reinterpret_cast<const uint4*>(x + off[u]))
+                            : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const uint32_t m2 = absmax_vec(0u, v[u]);
+            uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            const float s = block_scale<FMT>(__uint_as_float(m << 16), pow2);
+            if (valid[u]) {
+                *reinterpret_cast<uint2*>(q + off[u]) =
+                    make_uint2(cvt4<FMT>(v[u].x, v[u].y, s), cvt4<FMT>(v[u].z, v[u].w, s));
+                if (sub == 0) scale_inv[seg[u]] = __fdiv_rn(1.0f, s);
+            }
         }
     }
 }
@@ -755,7 +768,7 @@ __global__ void __launch_bounds__(kThreads)
                                float* __restrict__ scale_inv, uint8_t* __restrict__ qt,
                                float* __restrict__ scale_inv_t) {
     __shared__ __align__(16) uint16_t T[128 * 128];
-    __shared__ uint32_t colmax[2][128];
+    __shared__ uint32_t colpart[kThreads / 32][64];   // per warp: 128 column maxima, 2 per word
     const int64_t tile = blockIdx.x;
     const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
     const int t = threadIdx.x, cg = t & 7;
@@ -766,6 +779,24 @@ __global__ void __launch_bounds__(kThreads)
         const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + c0 + cg * 16);
         va[it] = ldg_stream(src);
         vb[it] = ldg_stream(src + 1);
+    }
+    // column maxima from registers: this thread's 4 rows of its 16 columns
+    uint32_t cm[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        cm[0] = absmax2(cm[0], va[it].x); cm[1] = absmax2(cm[1], va[it].y);
+        cm[2] = absmax2(cm[2], va[it].z); cm[3] = absmax2(cm[3], va[it].w);
+        cm[4] = absmax2(cm[4], vb[it].x); cm[5] = absmax2(cm[5], vb[it].y);
+        cm[6] = absmax2(cm[6], vb[it].z); cm[7] = absmax2(cm[7], vb[it].w);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {   // the 4 lanes of a warp with the same columns
+        cm[j] = __vmaxu2(cm[j], __shfl_xor_sync(0xFFFFFFFFu, cm[j], 8));
+        cm[j] = __vmaxu2(cm[j], __shfl_xor_sync(0xFFFFFFFFu, cm[j], 16));
+    }
+    if ((t & 31) < 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) colpart[t >> 5][cg * 8 + j] = cm[j];
     }
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
@@ -787,25 +818,36 @@ __global__ void __launch_bounds__(kThreads)
         dst[1] = b;
     }
     __syncthreads();
-    const int c = t & 127, h = t >> 7;
-    uint32_t m = 0;
-#pragma unroll 8
-    for (int i = 0; i < 64; ++i) m = max(m, static_cast<uint32_t>(T[(h * 64 + i) * 128 + c] & 0x7FFFu));
-    colmax[h][c] = m;
-    __syncthreads();
-    m = max(colmax[0][c], colmax[1][c]);
-    const float sc = block_scale<FMT>(__uint_as_float(m << 16), pow2);
-    uint32_t w[16];
+    // column pass: thread t takes the column pair (2w, 2w + 1), w = t % 64, over
+    // the row quarter q = t / 64; 32-bit shared loads hold both columns
+    const uint32_t* T32 = reinterpret_cast<const uint32_t*>(T);   // [128 rows][64 words]
+    const int w = t & 63, rq = t >> 6;
+    uint32_t m2 = 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const uint32_t e0 = T[(h * 64 + 4 * i + 0) * 128 + c], e1 = T[(h * 64 + 4 * i + 1) * 128 + c];
-        const uint32_t e2 = T[(h * 64 + 4 * i + 2) * 128 + c], e3 = T[(h * 64 + 4 * i + 3) * 128 + c];
-        w[i] = cvt4<FMT>(e0 | (e1 << 16), e2 | (e3 << 16), sc);
+    for (int g = 0; g < kThreads / 32; ++g) m2 = __vmaxu2(m2, colpart[g][w]);
+    const uint32_t ma = m2 & 0xFFFFu, mb = m2 >> 16;
+    const float sa = block_scale<FMT>(__uint_as_float(ma << 16), pow2);
+    const float sb = block_scale<FMT>(__uint_as_float(mb << 16), pow2);
+    uint32_t wa[8], wb[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = rq * 32 + 4 * i;
+        const uint32_t e0 = T32[(r + 0) * 64 + w], e1 = T32[(r + 1) * 64 + w];
+        const uint32_t e2 = T32[(r + 2) * 64 + w], e3 = T32[(r + 3) * 64 + w];
+        // low halves: column 2w of rows r..r+3; high halves: column 2w + 1
+        wa[i] = cvt4<FMT>(__byte_perm(e0, e1, 0x5410), __byte_perm(e2, e3, 0x5410), sa);
+        wb[i] = cvt4<FMT>(__byte_perm(e0, e1, 0x7632), __byte_perm(e2, e3, 0x7632), sb);
     }
-    uint4* out = reinterpret_cast<uint4*>(qt + (c0 + c) * rows + r0 + h * 64);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) out[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-    if (h == 0) scale_inv_t[(c0 + c) * (rows / 128) + r0 / 128] = __fdiv_rn(1.0f, sc);
+    uint4* oa = reinterpret_cast<uint4*>(qt + (c0 + 2 * w) * rows + r0 + rq * 32);
+    uint4* ob = reinterpret_cast<uint4*>(qt + (c0 + 2 * w + 1) * rows + r0 + rq * 32);
+    oa[0] = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+    oa[1] = make_uint4(wa[4], wa[5], wa[6], wa[7]);
+    ob[0] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+    ob[1] = make_uint4(wb[4], wb[5], wb[6], wb[7]);
+    if (rq == 0) {
+        scale_inv_t[(c0 + 2 * w) * (rows / 128) + r0 / 128] = __fdiv_rn(1.0f, sa);
+        scale_inv_t[(c0 + 2 * w + 1) * (rows / 128) + r0 / 128] = __fdiv_rn(1.0f, sb);
+    }
 }
 
 // ------------------------------------------------------ per-row scaling
