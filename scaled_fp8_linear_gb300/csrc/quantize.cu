@@ -767,8 +767,9 @@ __global__ void __launch_bounds__(kThreads)
                                int64_t tiles_c, int pow2, uint8_t* __restrict__ q,
                                float* __restrict__ scale_inv, uint8_t* __restrict__ qt,
                                float* __restrict__ scale_inv_t) {
-    __shared__ __align__(16) uint16_t T[128 * 128];
-    __shared__ uint32_t colpart[kThreads / 32][64];   // per warp: 128 column maxima, 2 per word
+    __shared__ __align__(16) uint32_t S[128 * 32];          // column-scaled codes, swizzled rows
+    __shared__ uint32_t colpart[kThreads / 32][64];         // per warp: 128 column maxima, 2 per word
+    __shared__ __align__(16) float colscale[128];
     const int64_t tile = blockIdx.x;
     const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
     const int t = threadIdx.x, cg = t & 7;
@@ -780,7 +781,8 @@ __global__ void __launch_bounds__(kThreads)
         va[it] = ldg_stream(src);
         vb[it] = ldg_stream(src + 1);
     }
-    // column maxima from registers: this thread's 4 rows of its 16 columns
+    // column maxima from registers: this thread's 4 rows of its 16 columns,
+    // then the 4 lanes of the warp with the same columns, then the 8 warps
     uint32_t cm[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
@@ -790,7 +792,7 @@ __global__ void __launch_bounds__(kThreads)
         cm[6] = absmax2(cm[6], vb[it].z); cm[7] = absmax2(cm[7], vb[it].w);
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {   // the 4 lanes of a warp with the same columns
+    for (int j = 0; j < 8; ++j) {
         cm[j] = __vmaxu2(cm[j], __shfl_xor_sync(0xFFFFFFFFu, cm[j], 8));
         cm[j] = __vmaxu2(cm[j], __shfl_xor_sync(0xFFFFFFFFu, cm[j], 16));
     }
@@ -798,9 +800,9 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int j = 0; j < 8; ++j) colpart[t >> 5][cg * 8 + j] = cm[j];
     }
+    // row blocks: each 128-element row segment of the tile has its own scale
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
-        const int rl = it * 32 + (t >> 3);
         const uint4 a = va[it], b = vb[it];
         const uint32_t m2 = absmax_vec(absmax_vec(0u, a), b);
         uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
@@ -808,46 +810,49 @@ __global__ void __launch_bounds__(kThreads)
         m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
         m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
         const float sc = block_scale<FMT>(__uint_as_float(m << 16), pow2);
-        const int64_t r = r0 + rl;
+        const int64_t r = r0 + it * 32 + (t >> 3);
         *reinterpret_cast<uint4*>(q + r * cols + c0 + cg * 16) =
             make_uint4(cvt4<FMT>(a.x, a.y, sc), cvt4<FMT>(a.z, a.w, sc), cvt4<FMT>(b.x, b.y, sc),
                        cvt4<FMT>(b.z, b.w, sc));
         if (cg == 0) scale_inv[r * (cols / 128) + c0 / 128] = __fdiv_rn(1.0f, sc);
-        uint4* dst = reinterpret_cast<uint4*>(&T[rl * 128 + cg * 16]);
-        dst[0] = a;
-        dst[1] = b;
     }
     __syncthreads();
-    // column pass: thread t takes the column pair (2w, 2w + 1), w = t % 64, over
-    // the row quarter q = t / 64; 32-bit shared loads hold both columns
-    const uint32_t* T32 = reinterpret_cast<const uint32_t*>(T);   // [128 rows][64 words]
-    const int w = t & 63, rq = t >> 6;
-    uint32_t m2 = 0;
+    // column blocks: one scale per column of the tile (thread c < 128), kept in
+    // shared memory; then each thread casts its 4 x 16 elements with them into
+    // S, rows swizzled as in the per-tensor transpose, which then writes q_t
+    // in whole 128-byte row segments
+    if (t < 128) {
+        uint32_t w2 = 0;
 #pragma unroll
-    for (int g = 0; g < kThreads / 32; ++g) m2 = __vmaxu2(m2, colpart[g][w]);
-    const uint32_t ma = m2 & 0xFFFFu, mb = m2 >> 16;
-    const float sa = block_scale<FMT>(__uint_as_float(ma << 16), pow2);
-    const float sb = block_scale<FMT>(__uint_as_float(mb << 16), pow2);
-    uint32_t wa[8], wb[8];
+        for (int g = 0; g < kThreads / 32; ++g) w2 = __vmaxu2(w2, colpart[g][t >> 1]);
+        const uint32_t m = (t & 1) ? (w2 >> 16) : (w2 & 0xFFFFu);
+        const float sc = block_scale<FMT>(__uint_as_float(m << 16), pow2);
+        colscale[t] = sc;
+        scale_inv_t[(c0 + t) * (rows / 128) + r0 / 128] = __fdiv_rn(1.0f, sc);
+    }
+    __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int r = rq * 32 + 4 * i;
-        const uint32_t e0 = T32[(r + 0) * 64 + w], e1 = T32[(r + 1) * 64 + w];
-        const uint32_t e2 = T32[(r + 2) * 64 + w], e3 = T32[(r + 3) * 64 + w];
-        // low halves: column 2w of rows r..r+3; high halves: column 2w + 1
-        wa[i] = cvt4<FMT>(__byte_perm(e0, e1, 0x5410), __byte_perm(e2, e3, 0x5410), sa);
-        wb[i] = cvt4<FMT>(__byte_perm(e0, e1, 0x7632), __byte_perm(e2, e3, 0x7632), sb);
+    for (int it = 0; it < 4; ++it) {
+        const int rl = it * 32 + (t >> 3);
+        const uint32_t in[8] = {va[it].x, va[it].y, va[it].z, va[it].w,
+                                vb[it].x, vb[it].y, vb[it].z, vb[it].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 cs = *reinterpret_cast<const float4*>(&colscale[cg * 16 + 4 * k]);
+            const uint32_t w0 = in[2 * k], w1 = in[2 * k + 1];
+            const float f0 = __fmul_rn(__uint_as_float(w0 << 16), cs.x);
+            const float f1 = __fmul_rn(__uint_as_float(w0 & 0xFFFF0000u), cs.y);
+            const float f2 = __fmul_rn(__uint_as_float(w1 << 16), cs.z);
+            const float f3 = __fmul_rn(__uint_as_float(w1 & 0xFFFF0000u), cs.w);
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f0, f1), __NV_SATFINITE, Fp8Traits<FMT>::kind);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f2, f3), __NV_SATFINITE, Fp8Traits<FMT>::kind);
+            o[k] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    uint4* oa = reinterpret_cast<uint4*>(qt + (c0 + 2 * w) * rows + r0 + rq * 32);
-    uint4* ob = reinterpret_cast<uint4*>(qt + (c0 + 2 * w + 1) * rows + r0 + rq * 32);
-    oa[0] = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-    oa[1] = make_uint4(wa[4], wa[5], wa[6], wa[7]);
-    ob[0] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
-    ob[1] = make_uint4(wb[4], wb[5], wb[6], wb[7]);
-    if (rq == 0) {
-        scale_inv_t[(c0 + 2 * w) * (rows / 128) + r0 / 128] = __fdiv_rn(1.0f, sa);
-        scale_inv_t[(c0 + 2 * w + 1) * (rows / 128) + r0 / 128] = __fdiv_rn(1.0f, sb);
-    }
+    __syncthreads();
+    transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
 }
 
 // ------------------------------------------------------ per-row scaling
