@@ -886,82 +886,120 @@ __global__ void __launch_bounds__(kThreads)
     if (threadIdx.x == 0) scale_inv[row] = __fdiv_rn(1.0f, s);
 }
 
-// Column amax of x (the per-row scales of x^T): each CTA reduces a 128 x 128
-// tile through shared memory and raises colmax[c] (fp32 bit patterns of the
-// |bf16| maxima, zeroed beforehand) with one atomicMax per column.
+// The per-row cast together with the per-row cast of x^T (one scale per row
+// and one per column) in two reads of x.  Pass 1: each 128 x 128 tile raises
+// the row maxima rowmax[r] and column maxima colmax[c] of its elements (fp32
+// bit patterns of |bf16| maxima, in arrays zeroed beforehand) with one
+// atomicMax per row and per column.  rows, cols: multiples of 16.
 __global__ void __launch_bounds__(kThreads)
-    column_amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t tiles_c,
-                       unsigned* __restrict__ colmax) {
-    __shared__ uint16_t part[32][128];
+    row_col_amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
+                        int64_t tiles_c, unsigned* __restrict__ rowmax,
+                        unsigned* __restrict__ colmax) {
+    __shared__ uint32_t colpart[kThreads / 32][64];
     const int64_t tile = blockIdx.x;
     const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
-    const int t = threadIdx.x, cg = t & 7, rg = t >> 3;
-    uint32_t cm[8] = {0, 0, 0, 0, 0, 0, 0, 0};   // 16 columns, 2 per word
+    const int t = threadIdx.x, cg = t & 7;
+    uint4 va[4], vb[4];
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
-        const int64_t r = r0 + it * 32 + rg, c = c0 + cg * 16;
+        const int64_t r = r0 + it * 32 + (t >> 3), c = c0 + cg * 16;
+        va[it] = vb[it] = make_uint4(0u, 0u, 0u, 0u);
         if (r < rows && c < cols) {
-            const uint4* p = reinterpret_cast<const uint4*>(x + r * cols + c);
-            const uint4 a = ldg_stream(p), b = ldg_stream(p + 1);
-            cm[0] = absmax2(cm[0], a.x); cm[1] = absmax2(cm[1], a.y);
-            cm[2] = absmax2(cm[2], a.z); cm[3] = absmax2(cm[3], a.w);
-            cm[4] = absmax2(cm[4], b.x); cm[5] = absmax2(cm[5], b.y);
-            cm[6] = absmax2(cm[6], b.z); cm[7] = absmax2(cm[7], b.w);
+            const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + c);
+            va[it] = ldg_stream(src);
+            vb[it] = ldg_stream(src + 1);
         }
     }
-    uint32_t* prow = reinterpret_cast<uint32_t*>(&part[rg][cg * 16]);
+    uint32_t cm[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) prow[j] = cm[j];
+    for (int it = 0; it < 4; ++it) {
+        const uint4 a = va[it], b = vb[it];
+        cm[0] = absmax2(cm[0], a.x); cm[1] = absmax2(cm[1], a.y);
+        cm[2] = absmax2(cm[2], a.z); cm[3] = absmax2(cm[3], a.w);
+        cm[4] = absmax2(cm[4], b.x); cm[5] = absmax2(cm[5], b.y);
+        cm[6] = absmax2(cm[6], b.z); cm[7] = absmax2(cm[7], b.w);
+        // the row's maximum over the tile: the 8 lanes that hold the row
+        const uint32_t m2 = absmax_vec(absmax_vec(0u, a), b);
+        uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+        const int64_t r = r0 + it * 32 + (t >> 3);
+        if (cg == 0 && m && r < rows) atomicMax(&rowmax[r], m << 16);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        cm[j] = __vmaxu2(cm[j], __shfl_xor_sync(0xFFFFFFFFu, cm[j], 8));
+        cm[j] = __vmaxu2(cm[j], __shfl_xor_sync(0xFFFFFFFFu, cm[j], 16));
+    }
+    if ((t & 31) < 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) colpart[t >> 5][cg * 8 + j] = cm[j];
+    }
     __syncthreads();
     if (t < 128 && c0 + t < cols) {
-        uint32_t m = 0;
-#pragma unroll 8
-        for (int g = 0; g < 32; ++g) m = max(m, static_cast<uint32_t>(part[g][t]));
+        uint32_t w2 = 0;
+#pragma unroll
+        for (int g = 0; g < kThreads / 32; ++g) w2 = __vmaxu2(w2, colpart[g][t >> 1]);
+        const uint32_t m = (t & 1) ? (w2 >> 16) : (w2 & 0xFFFFu);
         if (m) atomicMax(&colmax[c0 + t], m << 16);
     }
 }
 
-// The per-row cast of x^T, written as q_t [cols x rows]: every column of x
-// is cast with its own scale (from colmax), staged in shared memory and
-// written transposed like quantize_transpose_kernel.  rows, cols: multiples
-// of 16.
+// Pass 2: each tile cast twice from registers -- with its rows' scales into
+// q, with its columns' scales into the byte staging that the per-tensor
+// transpose writes out as q_t.
 template <int FMT>
 __global__ void __launch_bounds__(kThreads)
-    quantize_col_transpose_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
-                                  int64_t tiles_c, int pow2, const unsigned* __restrict__ colmax,
-                                  uint8_t* __restrict__ qt) {
+    quantize_row_col_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
+                            int64_t tiles_c, int pow2, const unsigned* __restrict__ rowmax,
+                            const unsigned* __restrict__ colmax, uint8_t* __restrict__ q,
+                            uint8_t* __restrict__ qt) {
     __shared__ __align__(16) uint32_t S[128 * 32];
+    __shared__ __align__(16) float colscale[128];
     const int64_t tile = blockIdx.x;
     const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
     const int t = threadIdx.x, cg = t & 7;
-    float sc[16];
+    if (t < 128)
+        colscale[t] = c0 + t < cols ? block_scale<FMT>(__uint_as_float(colmax[c0 + t]), pow2) : 1.0f;
+    uint4 va[4], vb[4];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const int64_t c = c0 + cg * 16 + j;
-        sc[j] = c < cols ? block_scale<FMT>(__uint_as_float(colmax[c]), pow2) : 1.0f;
+    for (int it = 0; it < 4; ++it) {
+        const int64_t r = r0 + it * 32 + (t >> 3), c = c0 + cg * 16;
+        va[it] = vb[it] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < rows && c < cols) {
+            const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + c);
+            va[it] = ldg_stream(src);
+            vb[it] = ldg_stream(src + 1);
+        }
     }
+    __syncthreads();
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         const int rl = it * 32 + (t >> 3);
         const int64_t r = r0 + rl, c = c0 + cg * 16;
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        const uint4 a = va[it], b = vb[it];
         if (r < rows && c < cols) {
-            const uint4* p = reinterpret_cast<const uint4*>(x + r * cols + c);
-            const uint4 a = ldg_stream(p), b = ldg_stream(p + 1);
-            const uint32_t in[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t w0 = in[2 * k], w1 = in[2 * k + 1];
-                const float f0 = __fmul_rn(__uint_as_float(w0 << 16), sc[4 * k]);
-                const float f1 = __fmul_rn(__uint_as_float(w0 & 0xFFFF0000u), sc[4 * k + 1]);
-                const float f2 = __fmul_rn(__uint_as_float(w1 << 16), sc[4 * k + 2]);
-                const float f3 = __fmul_rn(__uint_as_float(w1 & 0xFFFF0000u), sc[4 * k + 3]);
-                const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f0, f1), __NV_SATFINITE, Fp8Traits<FMT>::kind);
-                const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f2, f3), __NV_SATFINITE, Fp8Traits<FMT>::kind);
-                w[k] = lo | (hi << 16);
-            }
+            const float rs = block_scale<FMT>(__uint_as_float(rowmax[r]), pow2);
+            *reinterpret_cast<uint4*>(q + r * cols + c) =
+                make_uint4(cvt4<FMT>(a.x, a.y, rs), cvt4<FMT>(a.z, a.w, rs),
+                           cvt4<FMT>(b.x, b.y, rs), cvt4<FMT>(b.z, b.w, rs));
         }
-        *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = make_uint4(w[0], w[1], w[2], w[3]);
+        const uint32_t in[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 cs = *reinterpret_cast<const float4*>(&colscale[cg * 16 + 4 * k]);
+            const uint32_t w0 = in[2 * k], w1 = in[2 * k + 1];
+            const float f0 = __fmul_rn(__uint_as_float(w0 << 16), cs.x);
+            const float f1 = __fmul_rn(__uint_as_float(w0 & 0xFFFF0000u), cs.y);
+            const float f2 = __fmul_rn(__uint_as_float(w1 << 16), cs.z);
+            const float f3 = __fmul_rn(__uint_as_float(w1 & 0xFFFF0000u), cs.w);
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f0, f1), __NV_SATFINITE, Fp8Traits<FMT>::kind);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f2, f3), __NV_SATFINITE, Fp8Traits<FMT>::kind);
+            o[k] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = make_uint4(o[0], o[1], o[2], o[3]);
     }
     __syncthreads();
     transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
@@ -1153,15 +1191,24 @@ template <int FMT>
 static cudaError_t launch_row(const uint16_t* xs, int64_t rows, int64_t cols, int pow2, uint8_t* q,
                               float* scale_inv, uint8_t* q_t, float* scale_inv_t,
                               cudaStream_t stream) {
-    quantize_row_kernel<FMT><<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(xs, cols, pow2, q, scale_inv);
-    if (!q_t) return cudaGetLastError();
-    cudaError_t e = cudaMemsetAsync(scale_inv_t, 0, cols * sizeof(float), stream);
+    if (!q_t) {
+        quantize_row_kernel<FMT><<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(xs, cols, pow2, q, scale_inv);
+        return cudaGetLastError();
+    }
+    // with the transposed copy: two tiled reads of x; the scale arrays hold the
+    // row / column maxima until the last step turns them into 1/scale
+    cudaError_t e = cudaMemsetAsync(scale_inv, 0, rows * sizeof(float), stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(scale_inv_t, 0, cols * sizeof(float), stream);
     if (e != cudaSuccess) return e;
     const int64_t tiles_c = (cols + 127) / 128, tiles = ((rows + 127) / 128) * tiles_c;
-    column_amax_kernel<<<static_cast<unsigned>(tiles), kThreads, 0, stream>>>(
-        xs, rows, cols, tiles_c, reinterpret_cast<unsigned*>(scale_inv_t));
-    quantize_col_transpose_kernel<FMT><<<static_cast<unsigned>(tiles), kThreads, 0, stream>>>(
-        xs, rows, cols, tiles_c, pow2, reinterpret_cast<const unsigned*>(scale_inv_t), q_t);
+    auto* rmax = reinterpret_cast<unsigned*>(scale_inv);
+    auto* cmax = reinterpret_cast<unsigned*>(scale_inv_t);
+    row_col_amax_kernel<<<static_cast<unsigned>(tiles), kThreads, 0, stream>>>(xs, rows, cols, tiles_c,
+                                                                               rmax, cmax);
+    quantize_row_col_kernel<FMT><<<static_cast<unsigned>(tiles), kThreads, 0, stream>>>(
+        xs, rows, cols, tiles_c, pow2, rmax, cmax, q, q_t);
+    column_scale_finalize_kernel<FMT><<<static_cast<unsigned>((rows + 255) / 256), 256, 0, stream>>>(
+        scale_inv, rows, pow2);
     column_scale_finalize_kernel<FMT><<<static_cast<unsigned>((cols + 255) / 256), 256, 0, stream>>>(
         scale_inv_t, cols, pow2);
     return cudaGetLastError();
