@@ -366,7 +366,9 @@ __global__ void __launch_bounds__(256, 1)
 //     of the 256 x 256 FP32 accumulator (two accumulators, 512 columns);
 //   - MMA completion is multicast to both CTAs' `empty` and `tfull` barriers;
 //     both CTAs' epilogue warps arrive on the even CTA's `tempty` barrier.
-template <int STAGES>
+// GROUPED: a second problem (tmA2, tmB2, p2) shares the launch; without
+// it those parameters are ignored and the kernel is the single-problem one.
+template <int STAGES, bool GROUPED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ GemmParams p,
@@ -409,11 +411,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     // GEMM of the same pass, e.g. the dgrad next to the wgrad; none if
     // p2.num_m == 0), dealt round-robin to the clusters
     const int t1 = p.num_m * p.num_n;
-    const int num_units = t1 + p2.num_m * p2.num_n;
+    const int num_units = GROUPED ? t1 + p2.num_m * p2.num_n : t1;
     if (warp == 0 && lane == 0) {
         ptx::tma_prefetch_desc(&tmA);
         ptx::tma_prefetch_desc(&tmB);
-        if (num_units > t1) {
+        if (GROUPED && num_units > t1) {
             ptx::tma_prefetch_desc(&tmA2);
             ptx::tma_prefetch_desc(&tmB2);
         }
@@ -434,7 +436,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             int64_t issued = 0;
             bool ok = true;
             for (int u = pair; ok && u < num_units; u += npairs) {
-                const bool second = u >= t1;
+                const bool second = GROUPED && u >= t1;
                 const GemmParams& q = second ? p2 : p;
                 const CUtensorMap* ma = second ? &tmA2 : &tmA;
                 const CUtensorMap* mb = second ? &tmB2 : &tmB;
@@ -476,8 +478,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (int u = pair; ok && u < num_units; u += npairs) {
-                const int num_kb = u >= t1 ? p2.num_kb : p.num_kb;
-                const uint32_t idesc = u >= t1 ? idesc2 : idesc1;
+                const bool second = GROUPED && u >= t1;
+                const int num_kb = second ? p2.num_kb : p.num_kb;
+                const uint32_t idesc = second ? idesc2 : idesc1;
                 if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) break;
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + acc * TILE;
@@ -509,7 +512,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         const GemmParams& p1 = p;
         uint32_t acc = 0, acc_phase = 0;
         for (int u = pair; u < num_units; u += npairs) {
-            const bool second = u >= t1;
+            const bool second = GROUPED && u >= t1;
             const GemmParams& p = second ? p2 : p1;   // this unit's problem
             const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
             int m_blk, n_blk;
@@ -863,7 +866,7 @@ int ensure_smem(Kernel k, int bytes, int kernel_id) {
 // persistent grid size); cached per device.
 int pair_clusters(const void* func, int kernel_id, int threads, int smem) {
     static std::mutex mu;
-    static int cache[64][1] = {};
+    static int cache[64][2] = {};   // [device][kernel id]: 0 single, 1 grouped pair kernel
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
     int uncached = 0;                            // devices past the table: computed per call
@@ -956,7 +959,7 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
     const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
     const int grid = static_cast<int>(tiles < num_sms() ? tiles : num_sms());
     if (pair) {
-        auto k = gemm_pair_kernel<kPairStages>;
+        auto k = gemm_pair_kernel<kPairStages, false>;
         if ((st = ensure_smem(k, kPairSmemBytes, 2)) != FP8_OK) return st;
         const int64_t clusters =
             pair_clusters(reinterpret_cast<const void*>(k), 0, 256, kPairSmemBytes);
@@ -1026,11 +1029,11 @@ int launch_gemm_group(const GemmArgs& g1, const GemmArgs& g2, cudaStream_t strea
     if (st != FP8_OK) return st;
     // the deeper problem's tiles first, so the last round holds the cheaper tiles
     const bool swap = p2.num_kb > p1.num_kb;
-    auto k = gemm_pair_kernel<kPairStages>;
-    if ((st = ensure_smem(k, kPairSmemBytes, 2)) != FP8_OK) return st;
+    auto k = gemm_pair_kernel<kPairStages, true>;
+    if ((st = ensure_smem(k, kPairSmemBytes, 4)) != FP8_OK) return st;
     const int64_t units = static_cast<int64_t>(p1.num_m) * p1.num_n +
                           static_cast<int64_t>(p2.num_m) * p2.num_n;
-    const int64_t clusters = pair_clusters(reinterpret_cast<const void*>(k), 0, 256, kPairSmemBytes);
+    const int64_t clusters = pair_clusters(reinterpret_cast<const void*>(k), 1, 256, kPairSmemBytes);
     const int grid = static_cast<int>(2 * (units < clusters ? units : clusters));
     if (swap) k<<<grid, 256, kPairSmemBytes, stream>>>(a2, b2, p2, a1, b1, p1);
     else k<<<grid, 256, kPairSmemBytes, stream>>>(a1, b1, p1, a2, b2, p2);
