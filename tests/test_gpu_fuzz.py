@@ -1,0 +1,128 @@
+"""Seeded randomized parity sweep over the composed paths: random shapes (ragged
+where the call allows it), formats, scale granularities, recipes, bias and
+stochastic rounding, each checked against the oracle with the same bars as
+the targeted tests -- codes and scales bit-exact, GEMM results within
+2e-3 * sum|a b| * s_a * s_b (+ bf16 rounding)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scaled_fp8_linear_gb300 as F
+import synthetic
+from tests.helpers import assert_gemm_bound, bits, f32bits, u8
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    F.build()
+    F.lib()
+    yield
+    torch.cuda.synchronize()
+    assert F.fp8_device_status() == 0
+
+
+def _pick(rng, choices):
+    return choices[int(rng.integers(len(choices)))]
+
+
+@pytest.mark.parametrize("case", range(24))
+def test_random_casts(case):
+    rng = np.random.default_rng(1000 + case)
+    gran = _pick(rng, [F.GRAN_TENSOR, F.GRAN_1x128, F.GRAN_128x128, F.GRAN_ROW])
+    fmt = _pick(rng, [F.E4M3, F.E5M2])
+    transpose = bool(rng.integers(2))
+    pow2 = bool(rng.integers(2))
+    if gran == F.GRAN_TENSOR:
+        rows, cols = 16 * int(rng.integers(1, 40)), 16 * int(rng.integers(1, 40))
+    elif gran == F.GRAN_1x128:
+        rows = 128 * int(rng.integers(1, 5)) if transpose else int(rng.integers(1, 300))
+        cols = 128 * int(rng.integers(1, 5))
+    elif gran == F.GRAN_128x128:
+        rows, cols = 128 * int(rng.integers(1, 5)), 128 * int(rng.integers(1, 5))
+    else:
+        rows, cols = 16 * int(rng.integers(1, 40)), 16 * int(rng.integers(1, 40))
+    x = synthetic.student_t_rows((rows, cols), 1.0, 3, seed=case) * float(10.0 ** rng.integers(-3, 3))
+    x = x.to(torch.bfloat16)
+    if gran == F.GRAN_TENSOR:
+        sc = np.float32(10.0 ** rng.uniform(-2, 3))
+        q, qt, _, am = F.fp8_quantize(x.to(DEV), fmt, scale=torch.tensor([sc], device=DEV),
+                                      transpose=transpose, want_amax=True)
+        qo, qto = oracle.quantize(bits(x), fmt, sc, transpose=True)
+        assert np.array_equal(u8(q), qo)
+        if transpose:
+            assert np.array_equal(u8(qt), qto)
+        assert f32bits(am.cpu().numpy())[0] == f32bits(oracle.amax(bits(x)))
+        return
+    q, s, qt, st = F.fp8_quantize_blocks(x.to(DEV), fmt, gran, pow2=pow2, transpose=transpose)
+    if gran == F.GRAN_ROW:
+        qo, so = oracle.row_quantize(bits(x), fmt, pow2)
+    else:
+        qo, so = oracle.block_quantize(bits(x), fmt, 1 if gran == F.GRAN_1x128 else 128, pow2)
+    assert np.array_equal(u8(q), qo)
+    assert np.array_equal(f32bits(s.cpu().numpy()), f32bits(so))
+    if transpose:
+        xt = np.ascontiguousarray(bits(x).T)
+        if gran == F.GRAN_ROW:
+            qto, sto = oracle.row_quantize(xt, fmt, pow2)
+        elif gran == F.GRAN_1x128:
+            qto, sto = oracle.block_quantize(xt, fmt, 1, pow2)
+        else:
+            qto, sto = np.ascontiguousarray(qo.T), np.ascontiguousarray(so.T)
+        assert np.array_equal(u8(qt), qto)
+        assert np.array_equal(f32bits(st.cpu().numpy()), f32bits(sto))
+
+
+def _orecipe(r):
+    return oracle.Recipe(scaling=r.scaling, margin=r.margin, history_len=r.history_len,
+                         algo=r.amax_algo, pow2=bool(r.pow2), sr_grad=bool(r.sr_grad))
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_random_linear_steps(case):
+    rng = np.random.default_rng(2000 + case)
+    scaling = _pick(rng, [F.SCALING_DELAYED, F.SCALING_DYNAMIC, F.SCALING_BLOCK, F.SCALING_ROW])
+    mult = 128 if scaling == F.SCALING_BLOCK else 16
+    M = 128 * int(rng.integers(1, 5)) if scaling == F.SCALING_BLOCK else 16 * int(rng.integers(1, 40))
+    N, K = mult * int(rng.integers(1, 6 if mult == 128 else 40)), mult * int(rng.integers(1, 6 if mult == 128 else 40))
+    sr = scaling in (F.SCALING_DELAYED, F.SCALING_DYNAMIC) and bool(rng.integers(2))
+    rec = F.Recipe(scaling, margin=int(rng.integers(0, 2)), history_len=int(rng.integers(1, 20)),
+                   amax_algo=_pick(rng, [F.AMAX_MAX, F.AMAX_MOST_RECENT]), pow2=bool(rng.integers(2)),
+                   sr_grad=sr)
+    with_bias = bool(rng.integers(2))
+    seed = int(rng.integers(1 << 62))
+    layer = F.Fp8Linear(M, N, K, rec, device=DEV, sr_seed=seed)
+    orec = _orecipe(rec)
+    ost = oracle.LinearState(orec, sr_seed=seed)
+    W = synthetic.normal((N, K), 0.02, seed=case)
+    b = synthetic.normal((N,), 0.1, seed=case + 1) if with_bias else None
+    dW = torch.zeros(N, K, dtype=torch.float32, device=DEV)
+    db = torch.zeros(N, dtype=torch.float32, device=DEV) if with_bias else None
+    dW_o = np.zeros((N, K))
+    db_o = np.zeros(N)
+    for step in range(3):
+        X = synthetic.with_outlier_channels((M, K), 1.0, min(4, K), 50.0, seed=100 * case + step)
+        dY = synthetic.student_t((M, N), 3, 1e-3, seed=200 * case + step)
+        acc = step > 0
+        Y = layer.forward(X.to(DEV), W.to(DEV), bias=None if b is None else b.to(DEV))
+        dX, _ = layer.backward(dY.to(DEV), dW=dW, accumulate_dW=acc, dbias=db)
+        Yo, Yabs = oracle.linear_fwd(bits(X), bits(W), orec, ost, bias=None if b is None else bits(b))
+        prev = dW_o.copy()
+        (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(bits(dY), orec, ost,
+                                                       dW_prev=prev if acc else None)
+        assert_gemm_bound(Y, Yo, Yabs + 2.0 ** -13 * np.abs(Yo), what=f"Y step {step}")
+        assert_gemm_bound(dX, dXo, dXabs, what=f"dX step {step}")
+        assert_gemm_bound(dW, dWo, dWabs, prev=prev if acc else None, what=f"dW step {step}")
+        dW_o = dW.cpu().numpy().astype(np.float64)
+        if with_bias:
+            # fixed-order FP32 column sums: at most 16 + ceil(M/128) chained additions
+            s_, sabs = oracle.dbias(bits(dY))
+            want = s_ + (db_o if acc else 0.0)
+            tol = (18 + (M + 127) // 128) * 2.0 ** -24 * (sabs + np.abs(db_o))
+            got = db.cpu().numpy().astype(np.float64)
+            assert np.all(np.abs(got - want) <= tol), f"dbias step {step}"
+            db_o = got
+    torch.cuda.synchronize()
