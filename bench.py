@@ -431,15 +431,19 @@ def e2e_pass(F, recipe, dev, args, stream):
         dX = b["dX"][:TOKENS * K].view(TOKENS, K)
         dW = b["dW"][:N * K].view(N, K)
         L = layers[li]
+        hy, hdx, hdw = h_out[li]
         L.forward(b["X"][:TOKENS * K].view(TOKENS, K), b["W"][:N * K].view(N, K), Y=Y)
+        fwd_done = torch.cuda.Event()
+        fwd_done.record(stream)
+        with torch.cuda.stream(d2h_s):                     # Y leaves while the backward runs
+            d2h_s.wait_event(fwd_done)
+            hy.copy_(Y, non_blocking=True)
         L.backward(b["dY"][:TOKENS * N].view(TOKENS, N), dX=dX, dW=dW, accumulate_dW=False)
         ev = torch.cuda.Event()
         ev.record(stream)
         computed[g] = ev
         with torch.cuda.stream(d2h_s):
             d2h_s.wait_event(ev)
-            hy, hdx, hdw = h_out[li]
-            hy.copy_(Y, non_blocking=True)
             hdx.copy_(dX, non_blocking=True)
             hdw.copy_(dW, non_blocking=True)
             dev_ev = torch.cuda.Event()
