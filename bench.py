@@ -656,6 +656,12 @@ def run_kernel(args):
         if args.kernel == "gemm":
             one = torch.ones(1, dtype=torch.float32, device=dev)
             call = lambda: F.fp8_gemm(A, fa, B, F.E4M3, one, one, D=D)
+        elif args.pow2:
+            # power-of-two block factors: the block-scaled MMA path
+            sa = 2.0 ** torch.randint(-3, 4, (M, K // 128), generator=g, device=dev).float()
+            sb = 2.0 ** torch.randint(-3, 4, (N // 128, K // 128), generator=g, device=dev).float()
+            call = lambda: F.fp8_gemm(A, F.E4M3, B, F.E4M3, sa, sb, F.GRAN_1x128 | F.SCALE_POW2,
+                                      F.GRAN_128x128 | F.SCALE_POW2, D=D)
         else:
             sa = torch.rand(M, K // 128, generator=g, device=dev) + 0.5
             sb = torch.rand(N // 128, K // 128, generator=g, device=dev) + 0.5
@@ -709,6 +715,9 @@ def run_kernel(args):
     extra = {}
     if args.kernel in ("quantize", "quantize_sr"):
         extra = {"granularity": args.gran, "transpose": not args.no_transpose}
+    if args.kernel == "block_gemm":
+        extra = {"factors": "power of two (block-scaled MMA)" if args.pow2
+                 else "fp32 (per-128-K promotion)"}
     print(json.dumps({"kernel": args.kernel, "shape": dims, "format": args.fmt, **extra,
                       "median_ms": round(med, 4), "min_ms": round(ms[0], 4),
                       "achieved": round(ach, 1), "unit": unit, "peak": round(peak, 1),
@@ -793,6 +802,8 @@ def main():
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--gran", choices=["tensor", "1x128", "128x128", "row"], default="tensor",
                     help="--kernel quantize: scale granularity")
+    ap.add_argument("--pow2", action="store_true",
+                    help="block_gemm: power-of-two block factors (the block-scaled MMA path)")
     ap.add_argument("--no-transpose", action="store_true",
                     help="--kernel quantize / quantize_sr: no transposed copy")
     args = ap.parse_args()

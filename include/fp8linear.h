@@ -61,6 +61,19 @@ typedef enum {
     FP8_GRAN_128x128 = 2,    /* one scale per 128 x 128 tile                */
     FP8_GRAN_ROW = 3         /* one scale per row (per channel / token)     */
 } fp8_gran_t;
+/* Flag for fp8_gemm's ga / gb (and fp8_gemm_args_t), OR'd into
+ * FP8_GRAN_1x128 or FP8_GRAN_128x128: every factor of that operand is a
+ * power of two, as a cast with pow2 writes them (the per-tensor "scaling
+ * bias" of "Training and inference of large language models using 8-bit
+ * floating point", applied per block).  When both operands
+ * carry it, the GEMM applies the factors inside the tensor core as UE8M0
+ * block scales, each 128-deep block's factor on its four 32-deep steps: the
+ * same terms, with one FP32 accumulation over all of K instead of a
+ * promotion per 128-deep block.  Only the exponent of such a factor is read
+ * (2^-127 and below read as 2^-127).  With one operand flagged, or with
+ * other granularities, the flag changes nothing (it is rejected on
+ * FP8_GRAN_TENSOR and FP8_GRAN_ROW). */
+#define FP8_SCALE_POW2 16
 typedef enum {
     FP8_LAYOUT_TN = 0        /* A [M x K] and B [N x K], both K-contiguous   */
 } fp8_layout_t;

@@ -21,7 +21,7 @@ import torch
 
 __all__ = [
     "E4M3", "E5M2", "OUT_BF16", "OUT_F32", "AMAX_MAX", "AMAX_MOST_RECENT",
-    "GRAN_TENSOR", "GRAN_1x128", "GRAN_128x128", "GRAN_ROW", "LAYOUT_TN",
+    "GRAN_TENSOR", "GRAN_1x128", "GRAN_128x128", "GRAN_ROW", "SCALE_POW2", "LAYOUT_TN",
     "SCALING_DELAYED", "SCALING_DYNAMIC", "SCALING_BLOCK", "SCALING_ROW",
     "Fp8Error", "Recipe", "LinearStateC", "Fp8Linear", "build", "lib", "library_path",
     "fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_quantize_blocks",
@@ -34,6 +34,7 @@ E4M3, E5M2 = 0, 1
 OUT_BF16, OUT_F32 = 0, 1
 AMAX_MAX, AMAX_MOST_RECENT = 0, 1
 GRAN_TENSOR, GRAN_1x128, GRAN_128x128, GRAN_ROW = 0, 1, 2, 3
+SCALE_POW2 = 16   # OR'd into a block granularity: every factor is a power of two
 LAYOUT_TN = 0
 SCALING_DELAYED, SCALING_DYNAMIC, SCALING_BLOCK, SCALING_ROW = 0, 1, 2, 3
 

@@ -46,6 +46,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool valid_format(int f) { return f == FP8_E4M3 || f == FP8_E5M2; }
 bool valid_gran(int g) { return g >= FP8_GRAN_TENSOR && g <= FP8_GRAN_ROW; }
 bool block_gran(int g) { return g == FP8_GRAN_1x128 || g == FP8_GRAN_128x128; }
+// A GEMM operand's granularity: a valid one, with FP8_SCALE_POW2 only on
+// block granularities.
+bool valid_gemm_gran(int g) {
+    const int base = g & ~FP8_SCALE_POW2;
+    return valid_gran(base) && (!(g & FP8_SCALE_POW2) || block_gran(base));
+}
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
@@ -93,8 +99,10 @@ int check_gemm_args(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t 
     if (!valid_format(fa) || !valid_format(fb))
         return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: unknown FP8 format");
     if (layout != FP8_LAYOUT_TN) return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: unknown layout %d", layout);
-    if (!valid_gran(ga) || !valid_gran(gb))
+    if (!valid_gemm_gran(ga) || !valid_gemm_gran(gb))
         return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: unknown scale granularity");
+    ga &= ~FP8_SCALE_POW2;
+    gb &= ~FP8_SCALE_POW2;
     if (out != FP8_OUT_BF16 && out != FP8_OUT_F32)
         return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: unknown output type %d", out);
     if (accumulate && out != FP8_OUT_F32)
@@ -245,12 +253,15 @@ int linear_bwd_block(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_
         FP8_CHECK(cuda_status(launch_dbias(dY, M, N, partial, false, dbias, accumulate_dW, st),
                               "dbias"));
     }
+    // power-of-two factors (pow2 casts) go to the block-scaled MMA
+    const int p2 = recipe->pow2 ? FP8_SCALE_POW2 : 0;
     // dgrad: dX [M x K] = dY_q [M x N] . (W_q^T [K x N])^T
-    FP8_CHECK(launch_gemm(dy_q, fb, s->w_qt, ff, M, K, N, FP8_GRAN_1x128, dy_s, FP8_GRAN_128x128,
-                          s->w_sinv_t, nullptr, dX, FP8_OUT_BF16, 0, st));
+    FP8_CHECK(launch_gemm(dy_q, fb, s->w_qt, ff, M, K, N, FP8_GRAN_1x128 | p2, dy_s,
+                          FP8_GRAN_128x128 | p2, s->w_sinv_t, nullptr, dX, FP8_OUT_BF16, 0, st));
     // wgrad: dW [N x K] (+)= dY_q^T [N x M] . (X_q^T [K x M])^T
-    return launch_gemm(dy_qt, fb, s->x_qt, ff, N, K, M, FP8_GRAN_1x128, dy_st, FP8_GRAN_1x128,
-                       s->x_sinv_t, nullptr, dW, FP8_OUT_F32, accumulate_dW != 0, st);
+    return launch_gemm(dy_qt, fb, s->x_qt, ff, N, K, M, FP8_GRAN_1x128 | p2, dy_st,
+                       FP8_GRAN_1x128 | p2, s->x_sinv_t, nullptr, dW, FP8_OUT_F32,
+                       accumulate_dW != 0, st);
 }
 
 // Per-row backward: dY cast per token (dgrad operand) and per output
@@ -450,8 +461,9 @@ int fp8_linear_fwd(const void* X, const void* W, const void* bias, int64_t M, in
         FP8_CHECK(cuda_status(launch_quantize_block(W, N, K, f, FP8_GRAN_128x128, recipe->pow2 != 0,
                                                     s->w_q, s->w_sinv, keep ? s->w_qt : nullptr,
                                                     s->w_sinv_t, st), "quantize W"));
-        return launch_gemm(s->x_q, f, s->w_q, f, M, N, K, FP8_GRAN_1x128, s->x_sinv,
-                           FP8_GRAN_128x128, s->w_sinv, bias, Y, FP8_OUT_BF16, 0, st);
+        const int p2 = recipe->pow2 ? FP8_SCALE_POW2 : 0;
+        return launch_gemm(s->x_q, f, s->w_q, f, M, N, K, FP8_GRAN_1x128 | p2, s->x_sinv,
+                           FP8_GRAN_128x128 | p2, s->w_sinv, bias, Y, FP8_OUT_BF16, 0, st);
     }
 
     FP8_CHECK(check_state_scales(s));

@@ -796,6 +796,302 @@ __global__ void __launch_bounds__(kBlockThreads, 1)
     if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_device_status, 1u);
 }
 
+// ------------------------------------------ block-scaled kernel, power-of-two factors
+
+// With power-of-two factors the block scales go into the tensor core itself
+// (tcgen05.mma kind::mxf8f6f4.block_scale, one UE8M0 factor per 32 elements
+// of K): each 1x128 or 128x128 factor is given to the four 32-deep K steps of
+// its 128-deep block, so the products are the same terms as "Block-wise
+// scaling at 128 granularity" computes, and the accumulator stays in TMEM for
+// the whole K loop as with per-tensor scales -- nothing is promoted per K
+// block.
+//
+// Factor words: a 32-bit TMEM word holds four UE8M0 bytes, and each MMA
+// picks one byte of it (the instruction descriptor's factor byte).  Byte j of
+// a word here is the factor of K block 4g + j, so one word serves a group of
+// four K blocks: the writers store and hand over factors once per 512 of K.
+//
+// CTA pair (cluster of 2), 256 x 256 tiles, one TMEM accumulator (256
+// columns) plus a ring of factor slots (one group of four K blocks each) in
+// the other 256 columns.
+//   warp 0      TMA producer (as the per-tensor pair kernel);
+//   warp 1      MMA issuer (even CTA): per K block, waits for the operand
+//               stage (and, at a group's first block, for its factor slot),
+//               4 block-scaled MMAs with byte kb % 4, then releases the
+//               stage (and, after a group's last block, the slot) with
+//               tcgen05.commit;
+//   warp 2      TMEM allocation;
+//   warps 4-7   factor writers, one per TMEM lane quarter: convert the fp32
+//               factors of a group to UE8M0 words and tcgen05.st them into
+//               the slot (A: lane r, column r/32; B: every quarter's copy,
+//               column n/32); the next group's factors are loaded meanwhile;
+//   warps 8-15  epilogue, 2 per lane quarter (128 columns each): read the
+//               accumulator, hand it back to the MMA as soon as it is in
+//               registers, then round / store.
+constexpr int kMxStages = 6;
+constexpr int kMxSfStages = 8;
+constexpr int kMxEpiWarps = 8;
+constexpr int kMxThreads = (8 + kMxEpiWarps) * 32;
+constexpr int kMxSmemBytes = kMxStages * 2 * 128 * BK + 512 + 1024;
+
+// Factors of row r of an operand with `rows` rows for the K blocks
+// 4g .. 4g+3 (1.0 outside the matrix and past the last K block).
+__device__ __forceinline__ void mx_load4(float (&f)[4], const float* s, int gran, int64_t r,
+                                         int64_t rows, int g, int KB) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int kb = 4 * g + j;
+        f[j] = (r < rows && kb < KB) ? block_factor(s, gran, r, kb, KB) : 1.0f;
+    }
+}
+
+// TMEM factor word of four power-of-two factors: byte j is the UE8M0 code
+// of f[j] -- its biased fp32 exponent; mantissa bits are ignored, and 2^-127
+// or less gives 0.
+__device__ __forceinline__ uint32_t ue8m0_word(const float (&f)[4]) {
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w |= ((__float_as_uint(f[j]) >> 23) & 0xFFu) << (8 * j);
+    return w;
+}
+
+template <int STAGES, int SFS>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
+    gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ GemmParams p) {
+    constexpr int HALF = 128;              // rows of A and of B held by each CTA
+    constexpr int TILE = 2 * HALF;         // pair tile: 256 x 256
+    constexpr int A_BYTES = HALF * BK, B_BYTES = HALF * BK;
+    constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    constexpr uint32_t TMEM_COLS = 512;
+    constexpr uint32_t SF_COL0 = TILE;     // factor ring after the accumulator
+    constexpr uint32_t SF_SLOT = 16;       // columns per slot: A at +0..3, B at +4..11
+    const int num_groups = (p.num_kb + 3) >> 2;   // groups of four K blocks per tile
+    static_assert(SF_COL0 + SFS * SF_SLOT <= TMEM_COLS, "factor ring exceeds TMEM");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + STAGES * STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* sf_full = empty + STAGES;
+    uint64_t* sf_empty = sf_full + SFS;
+    uint64_t* tfull = sf_empty + SFS;
+    uint64_t* tempty = tfull + 1;
+    uint64_t* done = tempty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const bool leader = rank == 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < SFS; ++s) {
+            ptx::mbar_init(&sf_full[s], 8);   // 4 writer warps x 2 CTAs
+            ptx::mbar_init(&sf_empty[s], 1);
+        }
+        ptx::mbar_init(tfull, 1);
+        ptx::mbar_init(tempty, 2 * kMxEpiWarps);
+        ptx::mbar_init(done, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::tma_prefetch_desc(&tmA);
+        ptx::tma_prefetch_desc(&tmB);
+    }
+    if (warp == 2) {
+        ptx::tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    ptx::cluster_sync();   // the peer's barriers exist before any remote arrival
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int num_units = p.num_m * p.num_n;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int u = pair; ok && u < num_units; u += npairs) {
+                int m_blk, n_blk;
+                tile_coords<>(u, p.num_m, p.num_n, m_blk, n_blk);
+                const int ya = m_blk * TILE + static_cast<int>(rank) * HALF;
+                const int yb = n_blk * TILE + static_cast<int>(rank) * HALF;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+                    uint8_t* sa = ring + stage * STAGE_BYTES;
+                    const uint32_t bar = ptx::cluster_addr(&full[stage], 0);
+                    if (leader) ptx::mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
+                    ptx::tma_load_2d_pair(sa, &tmA, bar, kb * BK, ya);
+                    ptx::tma_load_2d_pair(sa + A_BYTES, &tmB, bar, kb * BK, yb);
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            uint32_t never = 0;
+            if (leader) {
+                // drain: the last copies into each slot (both CTAs' bytes) have landed
+                for (int s = 0; s < STAGES; ++s) {
+                    if (issued <= s && issued < STAGES) break;
+                    const uint32_t par = (static_cast<uint32_t>(s) < stage) ? phase : (phase ^ 1u);
+                    ptx::mbar_wait(&full[s], par, &never);
+                }
+            } else if (!ok) {
+                // copies signal the peer's barriers: after an abort, give those in
+                // flight a bounded grace period to land before this CTA moves on
+                const uint64_t t0 = ptx::globaltimer();
+                while (ptx::globaltimer() - t0 < 1000000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // byte j of the factor words: K block 4g + j of the slot's group
+            uint32_t idesc[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) idesc[j] = ptx::idesc_mxf8f6f4(p.fa, p.fb, TILE, TILE, j, j);
+            uint32_t stage = 0, phase = 0, sfs = 0, sf_phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int u = pair; ok && u < num_units; u += npairs) {
+                if (!ptx::mbar_wait(tempty, acc_phase ^ 1u, abort_flag)) break;
+                ptx::tc_fence_after();
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+                    if ((kb & 3) == 0 &&
+                        !ptx::mbar_wait(&sf_full[sfs], sf_phase, abort_flag)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    uint8_t* sa = ring + stage * STAGE_BYTES;
+                    const uint64_t ad = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa));
+                    const uint64_t bd = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa + A_BYTES));
+                    const uint32_t sfa = tmem_base + SF_COL0 + sfs * SF_SLOT;
+                    const uint32_t id = idesc[kb & 3];
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k)
+                        ptx::mma_mxf8f6f4_pair(tmem_base, ad + (k * UMMA_K >> 4),
+                                               bd + (k * UMMA_K >> 4), id, sfa, sfa + 4,
+                                               (kb | k) != 0);
+                    ptx::mma_commit_pair(&empty[stage], 0x3);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    if ((kb & 3) == 3 || kb == p.num_kb - 1) {   // the group's last K block
+                        ptx::mma_commit_pair(&sf_empty[sfs], 0x3);
+                        if (++sfs == SFS) { sfs = 0; sf_phase ^= 1u; }
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit_pair(tfull, 0x3);
+                acc_phase ^= 1u;
+            }
+            uint32_t never = 0;
+            ptx::mma_commit_pair(done, 0x1);
+            ptx::mbar_wait(done, 0, &never);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // factor writers: warp 4 + q owns TMEM lanes 32q .. 32q+31
+        const int q = warp & 3;
+        const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
+        // the factors of group g of unit u: this lane's A row, and B rows
+        // 32c + lane of the tile for c = 0..7
+        auto load = [&](int u, int g, float (&fa)[4], float (&fb)[8][4]) {
+            int m_blk, n_blk;
+            tile_coords<>(u, p.num_m, p.num_n, m_blk, n_blk);
+            const int64_t ra = static_cast<int64_t>(m_blk) * TILE + rank * HALF + q * 32 + lane;
+            mx_load4(fa, p.sa, p.ga, ra, p.M, g, p.num_kb);
+            const int64_t rb = static_cast<int64_t>(n_blk) * TILE + lane;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) mx_load4(fb[c], p.sb, p.gb, rb + 32 * c, p.N, g, p.num_kb);
+        };
+        uint32_t sfs = 0, sf_phase = 0;
+        int u = pair, g = 0;
+        float fa[4], fb[8][4];
+        if (u < num_units) load(u, g, fa, fb);
+        while (u < num_units) {
+            // the next group's factors are loaded while this one is stored
+            int nu = u, ng = g + 1;
+            if (ng == num_groups) { ng = 0; nu += npairs; }
+            float na[4], nb[8][4];
+            if (nu < num_units) load(nu, ng, na, nb);
+            uint32_t wb[8];
+            const uint32_t wa = ue8m0_word(fa);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) wb[c] = ue8m0_word(fb[c]);
+            bool ok = (lane == 0) ? ptx::mbar_wait(&sf_empty[sfs], sf_phase ^ 1u, abort_flag) : false;
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint32_t col = tmem_base + lanes + SF_COL0 + sfs * SF_SLOT;
+            ptx::tmem_st_32x32b_x1(col + q, wa);
+            ptx::tmem_st_32x32b_x8(col + 4, wb);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(ptx::cluster_addr(&sf_full[sfs], 0));
+            if (++sfs == SFS) { sfs = 0; sf_phase ^= 1u; }
+            if (nu >= num_units) break;
+            u = nu; g = ng;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                fa[j] = na[j];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) fb[c][j] = nb[c][j];
+            }
+        }
+    } else if (warp >= 8) {
+        const int q = warp & 3, h = (warp - 8) >> 2;
+        const int row = q * 32 + lane;
+        const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
+        float ones[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ones[j] = 1.0f;
+        uint32_t acc_phase = 0;
+        for (int u = pair; u < num_units; u += npairs) {
+            int m_blk, n_blk;
+            tile_coords<>(u, p.num_m, p.num_n, m_blk, n_blk);
+            const int64_t m = static_cast<int64_t>(m_blk) * TILE + rank * HALF + row;
+            const int64_t n0 = static_cast<int64_t>(n_blk) * TILE + h * 128;
+            if (rmw && n0 < p.N) prefetch_row(m, n0, 128, p);
+            bool ok = (lane == 0) ? ptx::mbar_wait(tfull, acc_phase, abort_flag) : false;
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            __syncwarp();
+            ptx::tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
+#pragma unroll 1
+            for (int c = 0; c < 4; c += 2) {
+                uint32_t r0[32], r1[32];
+                ptx::tmem_ld_32x32b_x32(tbase + c * 32, r0);
+                ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * 32, r1);
+                ptx::tmem_wait_ld();
+                if (c == 2) {
+                    // the whole accumulator has been read: the next tile may start
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive_cluster(ptx::cluster_addr(tempty, 0));
+                }
+                if (m < p.M) {
+                    store_chunk(r0, m, n0 + c * 32, p, ones, rmw);
+                    store_chunk(r1, m, n0 + (c + 1) * 32, p, ones, rmw);
+                }
+            }
+            acc_phase ^= 1u;
+        }
+    }
+
+    ptx::tc_fence_before();
+    ptx::cluster_sync();   // the pair's MMAs, copies, factor stores and remote arrivals are done
+    if (warp == 2) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_device_status, 1u);
+}
+
 // ---------------------------------------------------------------- host side
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -866,7 +1162,8 @@ int ensure_smem(Kernel k, int bytes, int kernel_id) {
 // persistent grid size); cached per device.
 int pair_clusters(const void* func, int kernel_id, int threads, int smem) {
     static std::mutex mu;
-    static int cache[64][2] = {};   // [device][kernel id]: 0 single, 1 grouped pair kernel
+    static int cache[64][3] = {};   // [device][kernel id]: 0 single, 1 grouped pair kernel,
+                                    // 2 power-of-two block kernel
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
     int uncached = 0;                            // devices past the table: computed per call
@@ -914,10 +1211,47 @@ __global__ void bias_rows_kernel(const __nv_bfloat16* __restrict__ bias, int64_t
     }
 }
 
+namespace {
+
+// Block-scaled GEMM with power-of-two factors on the CTA-pair block-scaled
+// MMA kernel (ga, gb: FP8_GRAN_1x128 / FP8_GRAN_128x128, flag removed; K > 0).
+int launch_gemm_mx(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
+                   int64_t K, int ga, const float* sa, int gb, const float* sb, const void* bias,
+                   void* D, int out, int accumulate, cudaStream_t stream) {
+    GemmParams p;
+    p.M = M; p.N = N; p.K = K;
+    p.num_m = static_cast<int>((M + 255) / 256);
+    p.num_n = static_cast<int>((N + 255) / 256);
+    p.num_kb = static_cast<int>((K + BK - 1) / BK);
+    p.fa = fa; p.fb = fb; p.ga = ga; p.gb = gb; p.sa = sa; p.sb = sb;
+    p.bias = static_cast<const __nv_bfloat16*>(bias);
+    p.D = D; p.out = out; p.accumulate = accumulate;
+    CUtensorMap tmA, tmB;
+    int st = make_kmajor_map(&tmA, A, M, K, BM);
+    if (st != FP8_OK) return st;
+    if ((st = make_kmajor_map(&tmB, B, N, K, 128)) != FP8_OK) return st;
+    auto k = gemm_mx_kernel<kMxStages, kMxSfStages>;
+    if ((st = ensure_smem(k, kMxSmemBytes, 5)) != FP8_OK) return st;
+    const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
+    const int64_t clusters =
+        pair_clusters(reinterpret_cast<const void*>(k), 2, kMxThreads, kMxSmemBytes);
+    const int grid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
+    k<<<grid, kMxThreads, kMxSmemBytes, stream>>>(tmA, tmB, p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(FP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+    return FP8_OK;
+}
+
+}  // namespace
+
 int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
                 int64_t K, int ga, const float* sa, int gb, const float* sb, const void* bias,
                 void* D, int out, int accumulate, cudaStream_t stream) {
     if (M == 0 || N == 0) return FP8_OK;
+    // power-of-two block factors on both operands: the block-scaled MMA
+    const bool pow2 = (ga & FP8_SCALE_POW2) && (gb & FP8_SCALE_POW2);
+    ga &= ~FP8_SCALE_POW2;
+    gb &= ~FP8_SCALE_POW2;
     if (K == 0 && bias) {   // an empty sum: D (+)= bias
         const int64_t n = M * N;
         const int64_t blocks = (n + 255) / 256;
@@ -937,6 +1271,10 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
     }
     const bool block = ga == FP8_GRAN_1x128 || ga == FP8_GRAN_128x128 || gb == FP8_GRAN_1x128 ||
                        gb == FP8_GRAN_128x128;
+    const bool mx = pow2 && (ga == FP8_GRAN_1x128 || ga == FP8_GRAN_128x128) &&
+                    (gb == FP8_GRAN_1x128 || gb == FP8_GRAN_128x128);
+    if (mx) return launch_gemm_mx(A, fa, B, fb, M, N, K, ga, sa, gb, sb, bias, D, out, accumulate,
+                                  stream);
     // per-tensor and per-row scales: CTA pairs for every problem of at least 256 rows
     const bool pair = !block && M >= kPairMinRows;
     const int BN = block ? 128 : kTensorBN;
@@ -993,8 +1331,9 @@ namespace {
 // A problem the CTA-pair kernel takes: per-tensor or per-row scales, at least
 // 256 rows, a nonempty K.
 bool pair_eligible(const GemmArgs& g) {
-    const bool block = g.ga == FP8_GRAN_1x128 || g.ga == FP8_GRAN_128x128 ||
-                       g.gb == FP8_GRAN_1x128 || g.gb == FP8_GRAN_128x128;
+    const int ga = g.ga & ~FP8_SCALE_POW2, gb = g.gb & ~FP8_SCALE_POW2;
+    const bool block = ga == FP8_GRAN_1x128 || ga == FP8_GRAN_128x128 ||
+                       gb == FP8_GRAN_1x128 || gb == FP8_GRAN_128x128;
     return !block && g.M >= kPairMinRows && g.N > 0 && g.K > 0 && !g.bias;
 }
 

@@ -280,6 +280,45 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask
         : "memory");
 }
 
+// Pair MMA with block scales (kind::mxf8f6f4.block_scale, one UE8M0 factor
+// per 32 elements of K for every row of A and of B, applied inside the
+// tensor core).  sfa / sfb are the TMEM addresses of the factor columns; the
+// instruction descriptor selects the byte of each 32-bit TMEM word that
+// holds this K=32 step's factors.  Layout (per CTA of the pair): the factor
+// of A row r (r < 128 of this CTA's rows) is at lane r, column sfa + r/32;
+// the factor of B row n is at column sfb + n/32 of lane 32*q + n%32, for
+// every lane quarter q (each quarter reads its own copy).
+__device__ __forceinline__ void mma_mxf8f6f4_pair(uint32_t d_tmem, uint64_t a_desc,
+                                                  uint64_t b_desc, uint32_t idesc, uint32_t sfa,
+                                                  uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+        "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+// 32 lanes x 32 bits stores into TMEM: thread t of the warp writes `n`
+// consecutive columns from `col` of lane (lane_base + t).
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Two IEEE fused multiply-adds on packed pairs: {a.lo*b.lo + c.lo, a.hi*b.hi + c.hi},
 // each rounded to nearest even.
 __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
@@ -323,6 +362,28 @@ __host__ __device__ __forceinline__ uint32_t idesc_f8f6f4(int a_fmt, int b_fmt, 
     d |= static_cast<uint32_t>(b_fmt & 7) << 10;
     d |= static_cast<uint32_t>(n >> 3) << 17;
     d |= static_cast<uint32_t>(m >> 4) << 24;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::mxf8f6f4 (block-scaled,
+// dense, FP32 accumulator, K-major operands, UE8M0 factors).
+//   bits  4-5   byte of the B factor word used by this instruction
+//   bits  7-9   A format (0 = E4M3, 1 = E5M2)
+//   bits 10-12  B format
+//   bits 17-22  N >> 3
+//   bit  23     factor type (1 = UE8M0)
+//   bits 24-28  M >> 4
+//   bits 29-30  byte of the A factor word used by this instruction
+__host__ __device__ __forceinline__ uint32_t idesc_mxf8f6f4(int a_fmt, int b_fmt, int m, int n,
+                                                            int a_byte, int b_byte) {
+    uint32_t d = 0;
+    d |= static_cast<uint32_t>(b_byte & 3) << 4;
+    d |= static_cast<uint32_t>(a_fmt & 7) << 7;
+    d |= static_cast<uint32_t>(b_fmt & 7) << 10;
+    d |= static_cast<uint32_t>(n >> 3) << 17;
+    d |= 1u << 23;
+    d |= static_cast<uint32_t>(m >> 4) << 24;
+    d |= static_cast<uint32_t>(a_byte & 3) << 29;
     return d;
 }
 

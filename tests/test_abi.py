@@ -56,6 +56,14 @@ def test_gemm_argument_checks():
     assert call(N=120) == -2 and call(K=40) == -2  # not multiples of 16
     assert call(M=-1) == -2
     assert call(ga=1, K=144) == -2                 # block scales need K % 128 == 0
+    # the power-of-two flag: only on block granularities; with it the block
+    # shape rules still apply
+    assert call(ga=F.GRAN_TENSOR | F.SCALE_POW2) == -1
+    assert call(gb=F.GRAN_ROW | F.SCALE_POW2) == -1
+    assert call(ga=F.GRAN_1x128 | F.SCALE_POW2, gb=F.GRAN_128x128 | F.SCALE_POW2, K=144) == -2
+    assert call(ga=F.GRAN_128x128 | F.SCALE_POW2, gb=F.GRAN_128x128 | F.SCALE_POW2, M=200) == -2
+    assert call(ga=F.GRAN_1x128 | F.SCALE_POW2, gb=F.GRAN_ROW) == -6   # block and per-row mixed
+    assert call(ga=F.GRAN_1x128 | 32) == -1                             # unknown flag bits
     assert call(D=ctypes.c_void_p(FAKE + 4)) == -3
     assert "16-byte" in F.fp8_last_error()
     assert call(bias=ctypes.c_void_p(FAKE + 2)) == -3

@@ -163,6 +163,88 @@ def test_block_scaled_exact_column_scales():
     assert np.array_equal(D.cpu().numpy().astype(np.float64), Do + prev)
 
 
+# Power-of-two block factors on both operands (pow2 block casts) run on the
+# block-scaled MMA (UE8M0 factors inside the tensor core).  Shapes: one tile,
+# ragged M (not a multiple of 256, and below 256), N a multiple of 128 but not
+# of 256 (a half-empty last tile column), several tiles and K blocks, and
+# more tiles than the grid has CTA pairs.
+POW2_SHAPES = [(256, 256, 128), (200, 384, 1024), (128, 128, 256), (384, 640, 2048),
+               (1, 128, 128), (1536, 1152, 512), (4096, 4352, 256)]
+
+
+@pytest.mark.parametrize("M,N,K", POW2_SHAPES)
+@pytest.mark.parametrize("ga,gb", [(F.GRAN_1x128, F.GRAN_128x128), (F.GRAN_1x128, F.GRAN_1x128),
+                                   (F.GRAN_128x128, F.GRAN_128x128)])
+def test_block_scaled_pow2(M, N, K, ga, gb):
+    if ga == F.GRAN_128x128 and M % 128:
+        pytest.skip("128x128 scales on A need M % 128 == 0")
+    rng = np.random.default_rng(M + 3 * N + K + ga * 10 + gb)
+
+    def operand(shape, fmt, gran, std):
+        v = rng.standard_normal(shape).astype(np.float32) * std
+        v *= np.abs(rng.standard_t(3, size=(shape[0], 1))).astype(np.float32)
+        b = (v.view(np.uint32) >> 16).astype(np.uint16)
+        return oracle.block_quantize(b, fmt, 1 if gran == F.GRAN_1x128 else 128, pow2=True)
+
+    A, sa = operand((M, K), F.E4M3, ga, 1.0)
+    B, sb = operand((N, K), F.E5M2 if gb == F.GRAN_1x128 else F.E4M3, gb, 0.02)
+    fb = F.E5M2 if gb == F.GRAN_1x128 else F.E4M3
+    Do, Dabs = oracle.gemm(A, F.E4M3, B, fb, sa, sb, ga, gb)
+    for out in (F.OUT_BF16, F.OUT_F32):
+        D = F.fp8_gemm(_t(A), F.E4M3, _t(B), fb, _s(sa), _s(sb), ga | F.SCALE_POW2,
+                       gb | F.SCALE_POW2, out=out)
+        assert_gemm_bound(D, Do, Dabs, what=f"pow2 block {M}x{N}x{K} out={out}")
+
+
+def test_block_scaled_pow2_exact():
+    """Integer codes and power-of-two factors spanning 2^-2..2^2 per 128-deep
+    block: every partial sum is representable, so the block-scaled MMA must
+    reproduce the oracle exactly -- including the FP32 accumulation into D,
+    the bias, and the per-column (1x128 on B) factors of the wgrad case."""
+    rng = np.random.default_rng(11)
+    for M, N, K, ga, gb in [(384, 512, 1024, F.GRAN_1x128, F.GRAN_128x128),
+                            (256, 384, 640, F.GRAN_1x128, F.GRAN_1x128),
+                            (200, 256, 384, F.GRAN_1x128, F.GRAN_1x128)]:
+        ai = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
+        bi = rng.integers(-3, 4, size=(N, K)).astype(np.float32)
+        sa = (2.0 ** rng.integers(-2, 3, size=(M, K // 128))).astype(np.float32)
+        rows_b = N if gb == F.GRAN_1x128 else N // 128
+        sb = (2.0 ** rng.integers(-2, 3, size=(rows_b, K // 128))).astype(np.float32)
+        A, B = oracle.encode(ai, F.E4M3), oracle.encode(bi, F.E5M2)
+        Do, _ = oracle.gemm(A, F.E4M3, B, F.E5M2, sa, sb, ga, gb)
+        prev = rng.integers(-8, 8, size=(M, N)).astype(np.float32)
+        D = _t(prev, torch.float32)
+        F.fp8_gemm(_t(A), F.E4M3, _t(B), F.E5M2, _s(sa), _s(sb), ga | F.SCALE_POW2,
+                   gb | F.SCALE_POW2, out=F.OUT_F32, D=D, accumulate=True)
+        assert np.array_equal(D.cpu().numpy().astype(np.float64), Do + prev), (M, N, K)
+        bias = rng.integers(-4, 5, size=N).astype(np.float32)
+        Db = F.fp8_gemm(_t(A), F.E4M3, _t(B), F.E5M2, _s(sa), _s(sb), ga | F.SCALE_POW2,
+                        gb | F.SCALE_POW2, out=F.OUT_F32,
+                        bias=torch.tensor(bias, device=DEV).to(torch.bfloat16))
+        assert np.array_equal(Db.cpu().numpy().astype(np.float64), Do + bias[None, :]), (M, N, K)
+
+
+def test_block_scaled_pow2_equals_promotion():
+    """The same power-of-two operands through both block paths (one operand
+    flagged runs the per-128-K promotion kernel): equal to within the FP32
+    rounding of the two accumulation orders, and both within the bound."""
+    rng = np.random.default_rng(12)
+    M, N, K = 512, 768, 2048
+    v = rng.standard_normal((M, K)).astype(np.float32)
+    A, sa = oracle.block_quantize((v.view(np.uint32) >> 16).astype(np.uint16), F.E4M3, 1, pow2=True)
+    w = rng.standard_normal((N, K)).astype(np.float32) * 0.02
+    B, sb = oracle.block_quantize((w.view(np.uint32) >> 16).astype(np.uint16), F.E4M3, 128, pow2=True)
+    args = (_t(A), F.E4M3, _t(B), F.E4M3, _s(sa), _s(sb))
+    D_mx = F.fp8_gemm(*args, F.GRAN_1x128 | F.SCALE_POW2, F.GRAN_128x128 | F.SCALE_POW2,
+                      out=F.OUT_F32)
+    D_pr = F.fp8_gemm(*args, F.GRAN_1x128 | F.SCALE_POW2, F.GRAN_128x128, out=F.OUT_F32)
+    Do, Dabs = oracle.gemm(A, F.E4M3, B, F.E4M3, sa, sb, F.GRAN_1x128, F.GRAN_128x128)
+    assert_gemm_bound(D_mx, Do, Dabs, what="pow2 MMA")
+    assert_gemm_bound(D_pr, Do, Dabs, what="promotion")
+    diff = (D_mx - D_pr).abs().cpu().numpy().astype(np.float64)
+    assert (diff <= 1e-4 * Dabs + 1e-30).all()
+
+
 @pytest.mark.parametrize("M,N,K", [(200, 336, 304), (512, 768, 1024), (1, 16, 16)])
 @pytest.mark.parametrize("ga,gb", [(F.GRAN_ROW, F.GRAN_ROW), (F.GRAN_ROW, F.GRAN_TENSOR),
                                    (F.GRAN_TENSOR, F.GRAN_ROW)])

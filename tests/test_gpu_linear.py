@@ -94,12 +94,13 @@ def test_block_forward():
     assert_gemm_bound(Y, Yo, Yabs)
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (1024, 768, 1280)])
-def test_block_training_steps(M, N, K):
+@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (1024, 768, 1280), (640, 896, 384)])
+@pytest.mark.parametrize("pow2", [False, True], ids=["fp32_scales", "pow2_scales"])
+def test_block_training_steps(M, N, K, pow2):
     """Block-wise forward + backward over 3 steps, wgrad accumulated: every
     quantised operand and block scale bit-exact, Y / dX / dW within the
-    bound."""
-    rec = F.Recipe(F.SCALING_BLOCK)
+    bound.  With pow2 the three GEMMs run on the block-scaled MMA."""
+    rec = F.Recipe(F.SCALING_BLOCK, pow2=pow2)
     layer = F.Fp8Linear(M, N, K, rec, device=DEV)
     orec = _orecipe(rec)
     ost = oracle.LinearState(orec)
@@ -221,9 +222,10 @@ def test_full_size_linear_sampled(name, M, N, K, recipe):
 
 
 @pytest.mark.parametrize("M,N,K", [(16384, 18432, 7168), (16384, 7168, 18432)])
-def test_full_size_block_gemm_sampled(M, N, K):
+@pytest.mark.parametrize("pow2", [False, True], ids=["fp32_scales", "pow2_scales"])
+def test_full_size_block_gemm_sampled(M, N, K, pow2):
     """Block-wise scaled forward at the DeepSeek-style shapes."""
-    layer = F.Fp8Linear(M, N, K, F.Recipe(F.SCALING_BLOCK), device=DEV)
+    layer = F.Fp8Linear(M, N, K, F.Recipe(F.SCALING_BLOCK, pow2=pow2), device=DEV)
     X = synthetic.student_t_rows((M, K), 1.0, 3, seed=11, device=DEV)
     W = synthetic.student_t_rows((N, K), 0.02, 3, seed=12, device=DEV)
     Y = layer.forward(X, W)
@@ -231,10 +233,10 @@ def test_full_size_block_gemm_sampled(M, N, K):
     rows = _sample_rows(M, 8, 3)
     x_q, x_s = layer.x_q.cpu().numpy(), layer.x_sinv.cpu().numpy()
     # the quantised rows and their scales against the oracle's block cast of those rows
-    qo, so = oracle.block_quantize(bits(X[torch.as_tensor(rows, device=DEV)]), F.E4M3, 1)
+    qo, so = oracle.block_quantize(bits(X[torch.as_tensor(rows, device=DEV)]), F.E4M3, 1, pow2)
     assert np.array_equal(x_q[rows], qo)
     assert np.array_equal(f32bits(x_s[rows]), f32bits(so))
-    wq, ws = oracle.block_quantize(bits(W), F.E4M3, 128)
+    wq, ws = oracle.block_quantize(bits(W), F.E4M3, 128, pow2)
     assert np.array_equal(u8(layer.w_q), wq)
     assert np.array_equal(f32bits(layer.w_sinv.cpu().numpy()), f32bits(ws))
     ii = np.repeat(rows, N)
