@@ -806,42 +806,57 @@ __global__ void __launch_bounds__(kBlockThreads, 1)
 // the whole K loop as with per-tensor scales -- nothing is promoted per K
 // block.
 //
-// Factor words: a 32-bit TMEM word holds four UE8M0 bytes, and each MMA
-// picks one byte of it (the instruction descriptor's factor byte).  Byte j of
-// a word here is the factor of K block 4g + j, so one word serves a group of
-// four K blocks: the writers store and hand over factors once per 512 of K.
+// Factor words: a 32-bit TMEM word holds four UE8M0 bytes and each MMA picks
+// one of them (the instruction descriptor's factor byte), so one word serves
+// four K blocks (byte j: K block 4w + j of the slot).  A ring slot holds four
+// words per row, i.e. the factors of 16 K blocks; the MMA selects the word by
+// the TMEM address it passes (A: slot + 4w, B: slot + 16 + 8w).
+//   A, row r of the CTA's 128:      lane r, column slot + 4w + r/32
+//   B, row n of the tile's 256:     column slot + 16 + 8w + n/32 of lane
+//                                   32q + n%32, for every lane quarter q
+//                                   (each quarter reads its own copy)
 //
 // CTA pair (cluster of 2), 256 x 256 tiles, one TMEM accumulator (256
-// columns) plus a ring of factor slots (one group of four K blocks each) in
-// the other 256 columns.
+// columns) plus the factor ring in the other 256 columns.
 //   warp 0      TMA producer (as the per-tensor pair kernel);
 //   warp 1      MMA issuer (even CTA): per K block, waits for the operand
-//               stage (and, at a group's first block, for its factor slot),
-//               4 block-scaled MMAs with byte kb % 4, then releases the
-//               stage (and, after a group's last block, the slot) with
-//               tcgen05.commit;
+//               stage (and, every 16 K blocks, for a factor slot), issues 4
+//               block-scaled MMAs, then releases the stage (and the slot
+//               after its 16th K block) with tcgen05.commit;
 //   warp 2      TMEM allocation;
-//   warps 4-7   factor writers, one per TMEM lane quarter: convert the fp32
-//               factors of a group to UE8M0 words and tcgen05.st them into
-//               the slot (A: lane r, column r/32; B: every quarter's copy,
-//               column n/32); the next group's factors are loaded meanwhile;
+//   warps 4-7   factor writers: per slot, load the fp32 factors coalesced
+//               (4 lanes per row, 16 K blocks of a row in one 64-byte
+//               segment), convert them to UE8M0 words, exchange them
+//               through shared memory, and tcgen05.st each lane quarter's
+//               A words and copy of the B words into the slot;
 //   warps 8-15  epilogue, 2 per lane quarter (128 columns each): read the
 //               accumulator, hand it back to the MMA as soon as it is in
 //               registers, then round / store.
 constexpr int kMxStages = 6;
-constexpr int kMxSfStages = 8;
+constexpr int kMxSfSlots = 4;
 constexpr int kMxEpiWarps = 8;
 constexpr int kMxThreads = (8 + kMxEpiWarps) * 32;
-constexpr int kMxSmemBytes = kMxStages * 2 * 128 * BK + 512 + 1024;
+constexpr int kMxStageA = 4 * 136;   // words per buffer: [word][128 rows + pad]
+constexpr int kMxStageB = 4 * 264;   //                   [word][256 rows + pad]
+constexpr int kMxSmemBytes =
+    kMxStages * 2 * 128 * BK + 2 * (kMxStageA + kMxStageB) * 4 + 512 + 1024;
 
-// Factors of row r of an operand with `rows` rows for the K blocks
-// 4g .. 4g+3 (1.0 outside the matrix and past the last K block).
+// Factors of row r (of an operand with `rows` rows) for the K blocks
+// kb0 .. kb0+3; 1.0 outside the matrix and past the last K block.  vec: the
+// four are one aligned float4 (KB % 4 == 0 and a 16-byte aligned array).
 __device__ __forceinline__ void mx_load4(float (&f)[4], const float* s, int gran, int64_t r,
-                                         int64_t rows, int g, int KB) {
+                                         int64_t rows, int kb0, int KB, bool vec) {
+    if (r >= rows || kb0 >= KB) {
+        f[0] = f[1] = f[2] = f[3] = 1.0f;
+        return;
+    }
+    const float* src = s + (gran == FP8_GRAN_1x128 ? r : (r >> 7)) * KB + kb0;
+    if (vec) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+    } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int kb = 4 * g + j;
-        f[j] = (r < rows && kb < KB) ? block_factor(s, gran, r, kb, KB) : 1.0f;
+        for (int j = 0; j < 4; ++j) f[j] = kb0 + j < KB ? src[j] : 1.0f;
     }
 }
 
@@ -858,20 +873,23 @@ __device__ __forceinline__ uint32_t ue8m0_word(const float (&f)[4]) {
 template <int STAGES, int SFS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ GemmParams p,
+                   int vec_a, int vec_b) {
     constexpr int HALF = 128;              // rows of A and of B held by each CTA
     constexpr int TILE = 2 * HALF;         // pair tile: 256 x 256
     constexpr int A_BYTES = HALF * BK, B_BYTES = HALF * BK;
     constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     constexpr uint32_t TMEM_COLS = 512;
     constexpr uint32_t SF_COL0 = TILE;     // factor ring after the accumulator
-    constexpr uint32_t SF_SLOT = 16;       // columns per slot: A at +0..3, B at +4..11
-    const int num_groups = (p.num_kb + 3) >> 2;   // groups of four K blocks per tile
+    constexpr uint32_t SF_SLOT = 48;       // columns per slot: A at +0..15, B at +16..47
+    constexpr int KPS = 16;                // K blocks per slot
     static_assert(SF_COL0 + SFS * SF_SLOT <= TMEM_COLS, "factor ring exceeds TMEM");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(ring + STAGES * STAGE_BYTES);
+    uint32_t* stage_a = reinterpret_cast<uint32_t*>(ring + STAGES * STAGE_BYTES);  // [2][4][136]
+    uint32_t* stage_b = stage_a + 2 * kMxStageA;                                  // [2][4][264]
+    uint64_t* full = reinterpret_cast<uint64_t*>(stage_b + 2 * kMxStageB);
     uint64_t* empty = full + STAGES;
     uint64_t* sf_full = empty + STAGES;
     uint64_t* sf_empty = sf_full + SFS;
@@ -913,6 +931,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     const int num_units = p.num_m * p.num_n;
+    const int num_slots = (p.num_kb + KPS - 1) / KPS;   // factor slots per tile
 
     if (warp == 0) {
         if (lane == 0) {
@@ -953,10 +972,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
-            // byte j of the factor words: K block 4g + j of the slot's group
-            uint32_t idesc[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) idesc[j] = ptx::idesc_mxf8f6f4(p.fa, p.fb, TILE, TILE, j, j);
+            // factor byte j (K block 4w + j of the slot's word w) in both bytes fields
+            const uint32_t idesc0 = ptx::idesc_mxf8f6f4(p.fa, p.fb, TILE, TILE, 0, 0);
             uint32_t stage = 0, phase = 0, sfs = 0, sf_phase = 0, acc_phase = 0;
             bool ok = true;
             for (int u = pair; ok && u < num_units; u += npairs) {
@@ -964,22 +981,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
                 ptx::tc_fence_after();
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
-                    if ((kb & 3) == 0 &&
+                    if ((kb % KPS) == 0 &&
                         !ptx::mbar_wait(&sf_full[sfs], sf_phase, abort_flag)) { ok = false; break; }
                     ptx::tc_fence_after();
                     uint8_t* sa = ring + stage * STAGE_BYTES;
                     const uint64_t ad = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa));
                     const uint64_t bd = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa + A_BYTES));
-                    const uint32_t sfa = tmem_base + SF_COL0 + sfs * SF_SLOT;
-                    const uint32_t id = idesc[kb & 3];
+                    const uint32_t w = static_cast<uint32_t>(kb % KPS) >> 2;
+                    const uint32_t byte = static_cast<uint32_t>(kb) & 3u;
+                    const uint32_t sfa = tmem_base + SF_COL0 + sfs * SF_SLOT + 4 * w;
+                    const uint32_t sfb = tmem_base + SF_COL0 + sfs * SF_SLOT + 16 + 8 * w;
+                    const uint32_t id = idesc0 | (byte << 4) | (byte << 29);
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k)
                         ptx::mma_mxf8f6f4_pair(tmem_base, ad + (k * UMMA_K >> 4),
-                                               bd + (k * UMMA_K >> 4), id, sfa, sfa + 4,
-                                               (kb | k) != 0);
+                                               bd + (k * UMMA_K >> 4), id, sfa, sfb, (kb | k) != 0);
                     ptx::mma_commit_pair(&empty[stage], 0x3);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                    if ((kb & 3) == 3 || kb == p.num_kb - 1) {   // the group's last K block
+                    if ((kb % KPS) == KPS - 1 || kb == p.num_kb - 1) {   // the slot's last K block
                         ptx::mma_commit_pair(&sf_empty[sfs], 0x3);
                         if (++sfs == SFS) { sfs = 0; sf_phase ^= 1u; }
                     }
@@ -993,53 +1012,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
             ptx::mbar_wait(done, 0, &never);
         }
     } else if (warp >= 4 && warp < 8) {
-        // factor writers: warp 4 + q owns TMEM lanes 32q .. 32q+31
+        // factor writers: warp 4 + q owns TMEM lanes 32q .. 32q+31.  Loads use
+        // 4 lanes per row (lane = 4 * row + K quarter), 8 rows per instruction:
+        // warp q loads A rows 32q + 8i + lane/4 (i < 4) and B rows
+        // 64q + 8i + lane/4 (i < 8), K blocks 16s + 4 (lane % 4) .. + 3.
         const int q = warp & 3;
         const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
-        // the factors of group g of unit u: this lane's A row, and B rows
-        // 32c + lane of the tile for c = 0..7
-        auto load = [&](int u, int g, float (&fa)[4], float (&fb)[8][4]) {
+        const int rsub = lane >> 2, kq = lane & 3;
+        uint32_t sfs = 0, sf_phase = 0, buf = 0;
+        // after a failed wait this warp keeps meeting the writers' named barrier
+        // (so that the other three cannot wait on it forever) but does nothing else
+        bool live = true;
+        for (int u = pair; u < num_units; u += npairs) {
             int m_blk, n_blk;
             tile_coords<>(u, p.num_m, p.num_n, m_blk, n_blk);
-            const int64_t ra = static_cast<int64_t>(m_blk) * TILE + rank * HALF + q * 32 + lane;
-            mx_load4(fa, p.sa, p.ga, ra, p.M, g, p.num_kb);
-            const int64_t rb = static_cast<int64_t>(n_blk) * TILE + lane;
+            const int64_t a0 = static_cast<int64_t>(m_blk) * TILE + rank * HALF;
+            const int64_t b0 = static_cast<int64_t>(n_blk) * TILE;
+            for (int s2 = 0; s2 < num_slots; ++s2) {
+                uint32_t* sta = stage_a + buf * kMxStageA;
+                uint32_t* stb = stage_b + buf * kMxStageB;
+                if (live) {
+                    const int kb0 = KPS * s2 + 4 * kq;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) mx_load4(fb[c], p.sb, p.gb, rb + 32 * c, p.N, g, p.num_kb);
-        };
-        uint32_t sfs = 0, sf_phase = 0;
-        int u = pair, g = 0;
-        float fa[4], fb[8][4];
-        if (u < num_units) load(u, g, fa, fb);
-        while (u < num_units) {
-            // the next group's factors are loaded while this one is stored
-            int nu = u, ng = g + 1;
-            if (ng == num_groups) { ng = 0; nu += npairs; }
-            float na[4], nb[8][4];
-            if (nu < num_units) load(nu, ng, na, nb);
-            uint32_t wb[8];
-            const uint32_t wa = ue8m0_word(fa);
+                    for (int i = 0; i < 4; ++i) {
+                        const int row = q * 32 + 8 * i + rsub;
+                        float f[4];
+                        mx_load4(f, p.sa, p.ga, a0 + row, p.M, kb0, p.num_kb, vec_a != 0);
+                        sta[kq * 136 + row] = ue8m0_word(f);
+                    }
 #pragma unroll
-            for (int c = 0; c < 8; ++c) wb[c] = ue8m0_word(fb[c]);
-            bool ok = (lane == 0) ? ptx::mbar_wait(&sf_empty[sfs], sf_phase ^ 1u, abort_flag) : false;
-            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            const uint32_t col = tmem_base + lanes + SF_COL0 + sfs * SF_SLOT;
-            ptx::tmem_st_32x32b_x1(col + q, wa);
-            ptx::tmem_st_32x32b_x8(col + 4, wb);
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive_cluster(ptx::cluster_addr(&sf_full[sfs], 0));
-            if (++sfs == SFS) { sfs = 0; sf_phase ^= 1u; }
-            if (nu >= num_units) break;
-            u = nu; g = ng;
+                    for (int i = 0; i < 8; ++i) {
+                        const int row = q * 64 + 8 * i + rsub;
+                        float f[4];
+                        mx_load4(f, p.sb, p.gb, b0 + row, p.N, kb0, p.num_kb, vec_b != 0);
+                        stb[kq * 264 + row] = ue8m0_word(f);
+                    }
+                }
+                ptx::named_bar_sync(1, 128);   // the slot's words of all four warps are staged
+                if (live) {
+                    // A: word w at column 4w + q of this quarter's lanes (the other
+                    // columns of these lanes are not read)
+                    uint32_t wa[16], wb[32];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                fa[j] = na[j];
+                    for (int w = 0; w < 4; ++w) {
+                        const uint32_t v = sta[w * 136 + q * 32 + lane];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) fb[c][j] = nb[c][j];
+                        for (int j = 0; j < 4; ++j) wa[4 * w + j] = j == q ? v : 0u;
+                    }
+#pragma unroll
+                    for (int w = 0; w < 4; ++w)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) wb[8 * w + c] = stb[w * 264 + 32 * c + lane];
+                    bool ok = (lane == 0) ? ptx::mbar_wait(&sf_empty[sfs], sf_phase ^ 1u, abort_flag)
+                                          : false;
+                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                    if (ok) {
+                        ptx::tc_fence_after();
+                        const uint32_t col = tmem_base + lanes + SF_COL0 + sfs * SF_SLOT;
+                        ptx::tmem_st_32x32b_x16(col, wa);
+                        ptx::tmem_st_32x32b_x32(col + 16, wb);
+                        ptx::tmem_wait_st();
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive_cluster(ptx::cluster_addr(&sf_full[sfs], 0));
+                    } else {
+                        live = false;
+                    }
+                }
+                if (++sfs == SFS) { sfs = 0; sf_phase ^= 1u; }
+                buf ^= 1u;
             }
         }
     } else if (warp >= 8) {
@@ -1230,13 +1271,16 @@ int launch_gemm_mx(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M
     int st = make_kmajor_map(&tmA, A, M, K, BM);
     if (st != FP8_OK) return st;
     if ((st = make_kmajor_map(&tmB, B, N, K, 128)) != FP8_OK) return st;
-    auto k = gemm_mx_kernel<kMxStages, kMxSfStages>;
+    auto k = gemm_mx_kernel<kMxStages, kMxSfSlots>;
     if ((st = ensure_smem(k, kMxSmemBytes, 5)) != FP8_OK) return st;
     const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
     const int64_t clusters =
         pair_clusters(reinterpret_cast<const void*>(k), 2, kMxThreads, kMxSmemBytes);
     const int grid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
-    k<<<grid, kMxThreads, kMxSmemBytes, stream>>>(tmA, tmB, p);
+    // factors of four K blocks as one float4: rows of a multiple of 4 floats, aligned arrays
+    const int vec_a = p.num_kb % 4 == 0 && (reinterpret_cast<uintptr_t>(sa) & 15u) == 0;
+    const int vec_b = p.num_kb % 4 == 0 && (reinterpret_cast<uintptr_t>(sb) & 15u) == 0;
+    k<<<grid, kMxThreads, kMxSmemBytes, stream>>>(tmA, tmB, p, vec_a, vec_b);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(FP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
     return FP8_OK;
