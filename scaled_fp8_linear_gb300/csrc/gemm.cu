@@ -870,6 +870,30 @@ __device__ __forceinline__ uint32_t ue8m0_word(const float (&f)[4]) {
     return w;
 }
 
+// One 32-column accumulator chunk (FP32 bits) plus the bias (if any) as 16
+// bf16 pairs, rounded to nearest even -- the same values store_chunk writes
+// with unit factors.  Columns past N are packed but never stored.
+__device__ __forceinline__ void pack_bf16_chunk(uint32_t (&pk)[16], const uint32_t (&r)[32],
+                                                int64_t n0, const GemmParams& p) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[j + e]);
+        if (p.bias && n0 + j < p.N) {
+            float b[8];
+            load_bias8(b, p.bias, n0 + j);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = __fadd_rn(v[e], b[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+            pk[j / 2 + e] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+    }
+}
+
 template <int STAGES, int SFS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -1103,21 +1127,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
             __syncwarp();
             ptx::tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
-#pragma unroll 1
-            for (int c = 0; c < 4; c += 2) {
-                uint32_t r0[32], r1[32];
-                ptx::tmem_ld_32x32b_x32(tbase + c * 32, r0);
-                ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * 32, r1);
-                ptx::tmem_wait_ld();
-                if (c == 2) {
-                    // the whole accumulator has been read: the next tile may start
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive_cluster(ptx::cluster_addr(tempty, 0));
+            if (p.out == FP8_OUT_BF16) {
+                // bf16: the 128 columns are read and packed (with the bias)
+                // first, the accumulator handed back, and only then stored, so
+                // that the row-per-thread stores overlap the next tile's MMAs
+                uint32_t pk[4][16];
+#pragma unroll
+                for (int c = 0; c < 4; c += 2) {
+                    uint32_t r0[32], r1[32];
+                    ptx::tmem_ld_32x32b_x32(tbase + c * 32, r0);
+                    ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * 32, r1);
+                    ptx::tmem_wait_ld();
+                    pack_bf16_chunk(pk[c], r0, n0 + c * 32, p);
+                    pack_bf16_chunk(pk[c + 1], r1, n0 + (c + 1) * 32, p);
                 }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive_cluster(ptx::cluster_addr(tempty, 0));
                 if (m < p.M) {
-                    store_chunk(r0, m, n0 + c * 32, p, ones, rmw);
-                    store_chunk(r1, m, n0 + (c + 1) * 32, p, ones, rmw);
+                    __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.D) + m * p.N;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (n0 + c * 32 + 8 * j < p.N)
+                                *reinterpret_cast<uint4*>(drow + n0 + c * 32 + 8 * j) =
+                                    make_uint4(pk[c][4 * j], pk[c][4 * j + 1], pk[c][4 * j + 2],
+                                               pk[c][4 * j + 3]);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < 4; c += 2) {
+                    uint32_t r0[32], r1[32];
+                    ptx::tmem_ld_32x32b_x32(tbase + c * 32, r0);
+                    ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * 32, r1);
+                    ptx::tmem_wait_ld();
+                    if (c == 2) {
+                        // the whole accumulator has been read: the next tile may start
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive_cluster(ptx::cluster_addr(tempty, 0));
+                    }
+                    if (m < p.M) {
+                        store_chunk(r0, m, n0 + c * 32, p, ones, rmw);
+                        store_chunk(r1, m, n0 + (c + 1) * 32, p, ones, rmw);
+                    }
                 }
             }
             acc_phase ^= 1u;
