@@ -649,6 +649,8 @@ def run_kernel(args):
         return run_gemm_step(F, args, dev, codes, flush)
     if args.kernel == "quantize_sweep":
         return run_quantize_sweep(F, args, dev, flush)
+    if args.kernel == "block_step":
+        return run_block_step(F, args, dev, flush)
     if args.kernel in ("gemm", "block_gemm"):
         M, N, K = dims
         A, B = codes(M, K), codes(N, K)
@@ -770,6 +772,53 @@ def run_gemm_step(F, args, dev, codes, flush):
                       "unit": "TFLOP/s"}))
 
 
+def run_block_step(F, args, dev, flush):
+    """One block-scaled linear layer step -- forward, dgrad and wgrad with
+    their 1x128 / 128x128 casts, dW accumulated -- on the DeepSeek-style
+    shapes, with fp32 or (--pow2) power-of-two block factors.  Inputs are
+    seeded synthetic tensors resident on the device; L2 is flushed before
+    every timed step."""
+    shapes = [(16384, 18432, 7168), (16384, 7168, 18432)]
+    if args.shape != "8192,12288,4096":
+        shapes = [tuple(int(v) for v in args.shape.split(","))]
+    stream = torch.cuda.current_stream()
+    for M, N, K in shapes:
+        layer = F.Fp8Linear(M, N, K, F.Recipe(F.SCALING_BLOCK, pow2=args.pow2), device=dev)
+        X = synthetic.student_t_rows((M, K), 1.0, 3, seed=1, device=dev)
+        W = synthetic.student_t_rows((N, K), 0.02, 3, seed=2, device=dev)
+        dY = synthetic.normal((M, N), 1e-3, seed=3, device=dev)
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        dX = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        dW = torch.zeros(N, K, dtype=torch.float32, device=dev)
+
+        def step():
+            layer.forward(X, W, Y=Y)
+            layer.backward(dY, dX=dX, dW=dW, accumulate_dW=True)
+
+        for _ in range(args.warmup):
+            step()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.iters)]
+        for i in range(args.iters):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        assert F.fp8_device_status() == 0
+        ms = sorted(a.elapsed_time(b) for a, b in ev)
+        med = ms[len(ms) // 2]
+        print(json.dumps({
+            "kernel": "block_step", "shape": [M, N, K],
+            "factors": "power of two (block-scaled MMA)" if args.pow2 else "fp32 (per-128-K promotion)",
+            "median_ms": round(med, 4), "min_ms": round(ms[0], 4),
+            "achieved": round(6.0 * M * N * K / (med * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+            "work": "6 M N K (fwd + dgrad + wgrad); casts included",
+            "iters": args.iters, "l2": "flushed before every step"}), flush=True)
+        del layer, X, W, dY, Y, dX, dW
+        torch.cuda.empty_cache()
+
+
 def _gemm_traffic():
     """DRAM bytes per GEMM launch of the step (mean over its 15 GEMMs), as
     measured by ncu and recorded in profiles/ together with a hash of the
@@ -795,7 +844,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", choices=["gemm", "block_gemm", "quantize", "quantize_sr",
-                                         "quantize_sweep", "gemm_step"],
+                                         "quantize_sweep", "gemm_step", "block_step"],
                     help="time one kernel on --shape instead of the layer step")
     ap.add_argument("--shape", default="8192,12288,4096")
     ap.add_argument("--fmt", choices=["e4m3", "e5m2"], default="e4m3")
@@ -803,7 +852,7 @@ def main():
     ap.add_argument("--gran", choices=["tensor", "1x128", "128x128", "row"], default="tensor",
                     help="--kernel quantize: scale granularity")
     ap.add_argument("--pow2", action="store_true",
-                    help="block_gemm: power-of-two block factors (the block-scaled MMA path)")
+                    help="block_gemm / block_step: power-of-two block factors (the block-scaled MMA path)")
     ap.add_argument("--no-transpose", action="store_true",
                     help="--kernel quantize / quantize_sr: no transposed copy")
     args = ap.parse_args()
