@@ -25,9 +25,12 @@
 //               scale, convert, store to global memory.
 // Per-tensor kernel: BM x BN = 128 x 256, two TMEM accumulators (512
 // columns) so the epilogue of one tile overlaps the mainloop of the next.
-// Block-scaled kernel: BM x BN = 128 x 128, four TMEM partial-sum buffers
-// rotated per 128-deep K block; 8 epilogue warps promote them into FP32
-// registers.
+// Block-scaled kernel (fp32 factors): BM x BN = 128 x 128, four TMEM
+// partial-sum buffers rotated per 128-deep K block; 16 epilogue warps
+// promote them into FP32 registers.
+// Block-scaled kernel (power-of-two factors): CTA pairs, 256 x 256 tiles,
+// tcgen05.mma kind::mxf8f6f4.block_scale with the factors as UE8M0 words in
+// a TMEM ring written by four factor-writer warps.
 #include <atomic>
 #include <cstdarg>
 #include <cstdint>
