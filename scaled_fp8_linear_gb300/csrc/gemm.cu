@@ -834,15 +834,22 @@ __global__ void __launch_bounds__(kBlockThreads, 1)
 //               A words and copy of the B words into the slot;
 //   warps 8-15  epilogue, 2 per lane quarter (128 columns each): read the
 //               accumulator, hand it back to the MMA as soon as it is in
-//               registers, then round / store.
+//               registers, then round and write each 32-row x 64-byte box to
+//               a shared-memory staging slot in the TMA's 64-byte swizzled
+//               layout and store it with a TMA bulk store -- or, for an
+//               accumulating FP32 output, a TMA reduce-add (D += box, one
+//               FP32 add per element, as a read-modify-write would do).
+//               Row-per-thread global stores (32 rows per instruction) held
+//               up the next tile's MMA issue.
 constexpr int kMxStages = 6;
 constexpr int kMxSfSlots = 4;
 constexpr int kMxEpiWarps = 8;
 constexpr int kMxThreads = (8 + kMxEpiWarps) * 32;
 constexpr int kMxStageA = 4 * 136;   // words per buffer: [word][128 rows + pad]
 constexpr int kMxStageB = 4 * 264;   //                   [word][256 rows + pad]
-constexpr int kMxSmemBytes =
-    kMxStages * 2 * 128 * BK + 2 * (kMxStageA + kMxStageB) * 4 + 512 + 1024;
+constexpr int kMxEpiStage = 2048;     // bytes of output staging per epilogue warp: one box
+constexpr int kMxSmemBytes = kMxStages * 2 * 128 * BK + kMxEpiWarps * kMxEpiStage +
+                             2 * (kMxStageA + kMxStageB) * 4 + 512 + 1024;
 
 // Factors of row r (of an operand with `rows` rows) for the K blocks
 // kb0 .. kb0+3; 1.0 outside the matrix and past the last K block.  vec: the
@@ -900,8 +907,8 @@ __device__ __forceinline__ void pack_bf16_chunk(uint32_t (&pk)[16], const uint32
 template <int STAGES, int SFS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ GemmParams p,
-                   int vec_a, int vec_b) {
+                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmD,
+                   const __grid_constant__ GemmParams p, int vec_a, int vec_b) {
     constexpr int HALF = 128;              // rows of A and of B held by each CTA
     constexpr int TILE = 2 * HALF;         // pair tile: 256 x 256
     constexpr int A_BYTES = HALF * BK, B_BYTES = HALF * BK;
@@ -914,7 +921,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint32_t* stage_a = reinterpret_cast<uint32_t*>(ring + STAGES * STAGE_BYTES);  // [2][4][136]
+    uint8_t* epi_stage = ring + STAGES * STAGE_BYTES;   // [8 warps][2048 B], 1024-aligned
+    uint32_t* stage_a = reinterpret_cast<uint32_t*>(epi_stage + kMxEpiWarps * kMxEpiStage);  // [2][4][136]
     uint32_t* stage_b = stage_a + 2 * kMxStageA;                                  // [2][4][264]
     uint64_t* full = reinterpret_cast<uint64_t*>(stage_b + 2 * kMxStageB);
     uint64_t* empty = full + STAGES;
@@ -947,6 +955,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
     if (warp == 0 && lane == 0) {
         ptx::tma_prefetch_desc(&tmA);
         ptx::tma_prefetch_desc(&tmB);
+        ptx::tma_prefetch_desc(&tmD);
     }
     if (warp == 2) {
         ptx::tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -1111,29 +1120,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
             }
         }
     } else if (warp >= 8) {
+        // epilogue warp: 32 rows (lane quarter q) x 128 columns (half h) of the
+        // CTA's 128 x 256 accumulator.  Output boxes are 32 rows x 64 bytes
+        // (32 bf16 or 16 FP32 columns), staged with the TMA's 64-byte swizzle:
+        // 16-byte piece j of row r at piece j ^ ((r >> 1) & 3).
         const int q = warp & 3, h = (warp - 8) >> 2;
-        const int row = q * 32 + lane;
-        const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
-        float ones[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) ones[j] = 1.0f;
+        uint8_t* stg = epi_stage + (warp - 8) * kMxEpiStage;
+        const uint32_t stg_s = ptx::smem_u32(stg);
+        uint8_t* my_row = stg + lane * 64;
+        const int swz = (lane >> 1) & 3;
+        const bool f32 = p.out == FP8_OUT_F32;
         uint32_t acc_phase = 0;
         for (int u = pair; u < num_units; u += npairs) {
             int m_blk, n_blk;
             tile_coords<>(u, p.num_m, p.num_n, m_blk, n_blk);
-            const int64_t m = static_cast<int64_t>(m_blk) * TILE + rank * HALF + row;
+            const int64_t m0 = static_cast<int64_t>(m_blk) * TILE + rank * HALF + q * 32;
             const int64_t n0 = static_cast<int64_t>(n_blk) * TILE + h * 128;
-            if (rmw && n0 < p.N) prefetch_row(m, n0, 128, p);
             bool ok = (lane == 0) ? ptx::mbar_wait(tfull, acc_phase, abort_flag) : false;
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
             __syncwarp();
             ptx::tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
-            if (p.out == FP8_OUT_BF16) {
-                // bf16: the 128 columns are read and packed (with the bias)
-                // first, the accumulator handed back, and only then stored, so
-                // that the row-per-thread stores overlap the next tile's MMAs
+            // stage one box (this thread's row: four 16-byte pieces) and store it
+            // at column x (whole-warp call)
+            auto emit = [&](const uint4 (&piece)[4], int64_t x) {
+                if (lane == 0) ptx::bulk_wait_group_read<0>();   // the slot's last store has read it
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4*>(my_row + 16 * (j ^ swz)) = piece[j];
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (m0 < p.M && x < p.N) {
+                        if (f32 && p.accumulate)
+                            ptx::tma_reduce_add_2d(&tmD, stg_s, static_cast<int32_t>(x),
+                                                   static_cast<int32_t>(m0));
+                        else
+                            ptx::tma_store_2d(&tmD, stg_s, static_cast<int32_t>(x),
+                                              static_cast<int32_t>(m0));
+                    }
+                    ptx::bulk_commit_group();
+                }
+            };
+            if (!f32) {
+                // read and pack the 128 columns first, hand the accumulator back,
+                // then stage and store
                 uint32_t pk[4][16];
 #pragma unroll
                 for (int c = 0; c < 4; c += 2) {
@@ -1141,44 +1174,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
                     ptx::tmem_ld_32x32b_x32(tbase + c * 32, r0);
                     ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * 32, r1);
                     ptx::tmem_wait_ld();
-                    pack_bf16_chunk(pk[c], r0, n0 + c * 32, p);
-                    pack_bf16_chunk(pk[c + 1], r1, n0 + (c + 1) * 32, p);
-                }
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive_cluster(ptx::cluster_addr(tempty, 0));
-                if (m < p.M) {
-                    __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.D) + m * p.N;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (n0 + c * 32 + 8 * j < p.N)
-                                *reinterpret_cast<uint4*>(drow + n0 + c * 32 + 8 * j) =
-                                    make_uint4(pk[c][4 * j], pk[c][4 * j + 1], pk[c][4 * j + 2],
-                                               pk[c][4 * j + 3]);
-                }
-            } else {
-#pragma unroll 1
-                for (int c = 0; c < 4; c += 2) {
-                    uint32_t r0[32], r1[32];
-                    ptx::tmem_ld_32x32b_x32(tbase + c * 32, r0);
-                    ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * 32, r1);
-                    ptx::tmem_wait_ld();
                     if (c == 2) {
-                        // the whole accumulator has been read: the next tile may start
                         ptx::tc_fence_before();
                         __syncwarp();
                         if (lane == 0) ptx::mbar_arrive_cluster(ptx::cluster_addr(tempty, 0));
                     }
-                    if (m < p.M) {
-                        store_chunk(r0, m, n0 + c * 32, p, ones, rmw);
-                        store_chunk(r1, m, n0 + (c + 1) * 32, p, ones, rmw);
+                    pack_bf16_chunk(pk[c], r0, n0 + c * 32, p);
+                    pack_bf16_chunk(pk[c + 1], r1, n0 + (c + 1) * 32, p);
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 piece[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        piece[j] = make_uint4(pk[c][4 * j], pk[c][4 * j + 1], pk[c][4 * j + 2],
+                                              pk[c][4 * j + 3]);
+                    emit(piece, n0 + c * 32);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < 4; c += 2) {
+                    uint32_t r[2][32];
+                    ptx::tmem_ld_32x32b_x32(tbase + c * 32, r[0]);
+                    ptx::tmem_ld_32x32b_x32(tbase + (c + 1) * 32, r[1]);
+                    ptx::tmem_wait_ld();
+                    if (c == 2) {
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive_cluster(ptx::cluster_addr(tempty, 0));
+                    }
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int64_t nc = n0 + (c + i) * 32;
+                        float v[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i][e]);
+                        if (p.bias) {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 8) {
+                                if (nc + j < p.N) {
+                                    float b[8];
+                                    load_bias8(b, p.bias, nc + j);
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) v[j + e] = __fadd_rn(v[j + e], b[e]);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int hb = 0; hb < 2; ++hb) {   // two 16-column boxes
+                            uint4 piece[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                piece[j] = make_uint4(__float_as_uint(v[16 * hb + 4 * j]),
+                                                      __float_as_uint(v[16 * hb + 4 * j + 1]),
+                                                      __float_as_uint(v[16 * hb + 4 * j + 2]),
+                                                      __float_as_uint(v[16 * hb + 4 * j + 3]));
+                            emit(piece, nc + 16 * hb);
+                        }
                     }
                 }
             }
             acc_phase ^= 1u;
         }
+        if (lane == 0) ptx::bulk_wait_group_all();   // every store has completed
+        __syncwarp();
     }
 
     ptx::tc_fence_before();
@@ -1229,6 +1288,28 @@ int make_kmajor_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K,
         return set_error(FP8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%lld x %lld]",
                          static_cast<int>(r), static_cast<long long>(rows),
                          static_cast<long long>(K));
+    return FP8_OK;
+}
+
+// Tensor map of the output D [M x N] (bf16 or FP32, row-major) for TMA stores
+// of boxes of 32 rows x 64 bytes (32 bf16 or 16 FP32 columns) with the
+// 64-byte swizzle.
+int make_store_map(CUtensorMap* map, void* ptr, int64_t M, int64_t N, int out) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return set_error(FP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const bool f32 = out == FP8_OUT_F32;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * (f32 ? 4 : 2)};
+    const cuuint32_t box[2] = {f32 ? 16u : 32u, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(FP8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for output [%lld x %lld]",
+                         static_cast<int>(r), static_cast<long long>(M),
+                         static_cast<long long>(N));
     return FP8_OK;
 }
 
@@ -1324,10 +1405,11 @@ int launch_gemm_mx(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M
     p.fa = fa; p.fb = fb; p.ga = ga; p.gb = gb; p.sa = sa; p.sb = sb;
     p.bias = static_cast<const __nv_bfloat16*>(bias);
     p.D = D; p.out = out; p.accumulate = accumulate;
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmD;
     int st = make_kmajor_map(&tmA, A, M, K, BM);
     if (st != FP8_OK) return st;
     if ((st = make_kmajor_map(&tmB, B, N, K, 128)) != FP8_OK) return st;
+    if ((st = make_store_map(&tmD, D, M, N, out)) != FP8_OK) return st;
     auto k = gemm_mx_kernel<kMxStages, kMxSfSlots>;
     if ((st = ensure_smem(k, kMxSmemBytes, 5)) != FP8_OK) return st;
     const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
@@ -1337,7 +1419,7 @@ int launch_gemm_mx(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M
     // factors of four K blocks as one float4: rows of a multiple of 4 floats, aligned arrays
     const int vec_a = p.num_kb % 4 == 0 && (reinterpret_cast<uintptr_t>(sa) & 15u) == 0;
     const int vec_b = p.num_kb % 4 == 0 && (reinterpret_cast<uintptr_t>(sb) & 15u) == 0;
-    k<<<grid, kMxThreads, kMxSmemBytes, stream>>>(tmA, tmB, p, vec_a, vec_b);
+    k<<<grid, kMxThreads, kMxSmemBytes, stream>>>(tmA, tmB, tmD, p, vec_a, vec_b);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(FP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
     return FP8_OK;
