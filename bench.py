@@ -651,6 +651,8 @@ def run_kernel(args):
         return run_quantize_sweep(F, args, dev, flush)
     if args.kernel == "block_step":
         return run_block_step(F, args, dev, flush)
+    if args.kernel == "llama70b_step":
+        return run_llama70b_step(F, args, dev, flush)
     if args.kernel in ("gemm", "block_gemm"):
         M, N, K = dims
         A, B = codes(M, K), codes(N, K)
@@ -819,6 +821,59 @@ def run_block_step(F, args, dev, flush):
         torch.cuda.empty_cache()
 
 
+LINEARS_70B = [("qkv", 8192, 10240), ("o", 8192, 8192), ("gate", 8192, 28672),
+               ("up", 8192, 28672), ("down", 28672, 8192)]
+
+
+def run_llama70b_step(F, args, dev, flush):
+    """The Llama-2-70B-shaped block linears (4096 tokens, d = 8192, GQA QKV
+    8192 -> 10240, O, gate/up 8192 -> 28672, down 28672 -> 8192) through
+    fp8_linear_fwd + fp8_linear_bwd with per-tensor dynamic scaling, dW
+    accumulated in FP32.  Seeded synthetic inputs resident on the device
+    (X with outlier channels, W ~ N(0, 0.02), dY ~ N(0, 1e-3)); L2 flushed
+    before every timed step."""
+    tokens = 4096
+    recipe = F.Recipe(F.SCALING_DYNAMIC)
+    layers, Xs, Ws, dYs, Ys, dXs, dWs = [], [], [], [], [], [], []
+    for li, (name, K, N) in enumerate(LINEARS_70B):
+        layers.append(F.Fp8Linear(tokens, N, K, recipe, device=dev))
+        Xs.append(synthetic.with_outlier_channels((tokens, K), 1.0, max(1, K // 256), 50.0,
+                                                  seed=10 * li, device=dev))
+        Ws.append(synthetic.normal((N, K), 0.02, seed=1000 + li, device=dev))
+        dYs.append(synthetic.normal((tokens, N), 1e-3, seed=500 + li, device=dev))
+        Ys.append(torch.empty(tokens, N, dtype=torch.bfloat16, device=dev))
+        dXs.append(torch.empty(tokens, K, dtype=torch.bfloat16, device=dev))
+        dWs.append(torch.zeros(N, K, dtype=torch.float32, device=dev))
+
+    def step():
+        for li in range(len(LINEARS_70B)):
+            layers[li].forward(Xs[li], Ws[li], Y=Ys[li])
+            layers[li].backward(dYs[li], dX=dXs[li], dW=dWs[li], accumulate_dW=True)
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.iters)]
+    for i in range(args.iters):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert F.fp8_device_status() == 0
+    ms = sorted(a.elapsed_time(b) for a, b in ev)
+    med = ms[len(ms) // 2]
+    flops = sum(6.0 * tokens * N * K for _, K, N in LINEARS_70B)
+    print(json.dumps({
+        "kernel": "llama70b_step", "tokens": tokens,
+        "linears": {n: [k, v] for n, k, v in LINEARS_70B}, "recipe": "dynamic per-tensor, HYBRID",
+        "median_ms": round(med, 4), "min_ms": round(ms[0], 4),
+        "achieved": round(flops / (med * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+        "work": "6 M N K per linear (fwd + dgrad + wgrad); casts, amax and scale updates included",
+        "iters": args.iters, "l2": "flushed before every step"}), flush=True)
+
+
 def _gemm_traffic():
     """DRAM bytes per GEMM launch of the step (mean over its 15 GEMMs), as
     measured by ncu and recorded in profiles/ together with a hash of the
@@ -844,7 +899,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", choices=["gemm", "block_gemm", "quantize", "quantize_sr",
-                                         "quantize_sweep", "gemm_step", "block_step"],
+                                         "quantize_sweep", "gemm_step", "block_step",
+                                         "llama70b_step"],
                     help="time one kernel on --shape instead of the layer step")
     ap.add_argument("--shape", default="8192,12288,4096")
     ap.add_argument("--fmt", choices=["e4m3", "e5m2"], default="e4m3")
