@@ -230,6 +230,73 @@ __device__ __forceinline__ void prefetch_row(int64_t m, int64_t n0, int width,
     ptx::prefetch_l2(static_cast<const float*>(p.D) + m * p.N + n0, static_cast<uint32_t>(cols * 4));
 }
 
+// Stage one output box of 32 rows x 64 bytes (this thread's row: four 16-byte
+// pieces) in `slot` (2 KB of shared memory) with the TMA's 64-byte swizzle --
+// piece j of row r at piece j ^ ((r >> 1) & 3), so the 32 rows' writes hit
+// distinct banks -- and write it to global memory at (x, y) with a TMA bulk
+// store, or, with `add`, a TMA reduce-add (D += box, one FP32 add per element
+// performed by the memory system).  Whole-warp call.  The slot is reused, so
+// the previous box's store must first have read it.  in_range = false skips
+// the store (the box starts past the matrix) but keeps the group count.
+__device__ __forceinline__ void emit_box(uint8_t* slot, const uint4 (&piece)[4],
+                                         const CUtensorMap* map, int64_t x, int64_t y,
+                                         bool in_range, bool add) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) ptx::bulk_wait_group_read<0>();
+    __syncwarp();
+    uint8_t* row = slot + lane * 64;
+    const int swz = (lane >> 1) & 3;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(row + 16 * (j ^ swz)) = piece[j];
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (in_range) {
+            if (add)
+                ptx::tma_reduce_add_2d(map, ptx::smem_u32(slot), static_cast<int32_t>(x),
+                                       static_cast<int32_t>(y));
+            else
+                ptx::tma_store_2d(map, ptx::smem_u32(slot), static_cast<int32_t>(x),
+                                  static_cast<int32_t>(y));
+        }
+        ptx::bulk_commit_group();
+    }
+}
+
+// FP32 output of one 32-column accumulator chunk of a warp's 32 rows (first
+// row m0, first column n0): v = fp32(acc * f) (+ bias), as two 16-column TMA
+// boxes through `slot`, stored or (accumulate) added.  Whole-warp call.
+__device__ __forceinline__ void emit_f32_chunk(uint8_t* slot, const uint32_t (&r)[32],
+                                               const float (&f)[32], int64_t m0, int64_t n0,
+                                               const GemmParams& p, const CUtensorMap* map) {
+    float v[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = __fmul_rn(__uint_as_float(r[e]), f[e]);
+    if (p.bias) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+            if (n0 + j < p.N) {
+                float b[8];
+                load_bias8(b, p.bias, n0 + j);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[j + e] = __fadd_rn(v[j + e], b[e]);
+            }
+        }
+    }
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+        uint4 piece[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            piece[j] = make_uint4(__float_as_uint(v[16 * hb + 4 * j]),
+                                  __float_as_uint(v[16 * hb + 4 * j + 1]),
+                                  __float_as_uint(v[16 * hb + 4 * j + 2]),
+                                  __float_as_uint(v[16 * hb + 4 * j + 3]));
+        const int64_t x = n0 + 16 * hb;
+        emit_box(slot, piece, map, x, m0, m0 < p.M && x < p.N, p.accumulate != 0);
+    }
+}
+
 // --------------------------------------------------------- per-tensor kernel
 
 template <int BN, int STAGES>
@@ -374,9 +441,11 @@ __global__ void __launch_bounds__(256, 1)
 template <int STAGES, bool GROUPED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ GemmParams p,
+                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmD,
+                     const __grid_constant__ GemmParams p,
                      const __grid_constant__ CUtensorMap tmA2,
                      const __grid_constant__ CUtensorMap tmB2,
+                     const __grid_constant__ CUtensorMap tmD2,
                      const __grid_constant__ GemmParams p2) {
     constexpr int HALF = 128;              // rows of A and of B held by each CTA
     constexpr int TILE = 2 * HALF;         // pair tile: 256 x 256
@@ -386,7 +455,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(ring + STAGES * STAGE_BYTES);
+    uint8_t* epi_stage = ring + STAGES * STAGE_BYTES;   // FP32 output boxes: 2 KB per epilogue warp
+    uint64_t* full = reinterpret_cast<uint64_t*>(epi_stage + 4 * 2048);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
@@ -510,18 +580,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             ptx::mbar_wait(done, 0, &never);
         }
     } else if (warp >= 4) {
+        // bf16 output: row-per-thread 16-byte stores; FP32 output: 32-row x
+        // 16-column TMA boxes from this warp's 2 KB staging slot, stored or
+        // (accumulate) added by the TMA -- no read of D by the SM
         const int qd = warp & 3;
-        const int row = qd * 32 + lane;
+        uint8_t* slot = epi_stage + qd * 2048;
         const GemmParams& p1 = p;
         uint32_t acc = 0, acc_phase = 0;
         for (int u = pair; u < num_units; u += npairs) {
             const bool second = GROUPED && u >= t1;
             const GemmParams& p = second ? p2 : p1;   // this unit's problem
-            const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
+            const CUtensorMap* map = second ? &tmD2 : &tmD;
+            const bool f32 = p.out == FP8_OUT_F32;
             int m_blk, n_blk;
             tile_coords<>(second ? u - t1 : u, p.num_m, p.num_n, m_blk, n_blk);
-            const int64_t m = static_cast<int64_t>(m_blk) * TILE + rank * HALF + row;
-            if (rmw) prefetch_row(m, static_cast<int64_t>(n_blk) * TILE, TILE, p);
+            const int64_t m0 = static_cast<int64_t>(m_blk) * TILE + rank * HALF + qd * 32;
+            const int64_t m = m0 + lane;
             bool ok = (lane == 0) ? ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag) : false;
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
@@ -537,7 +611,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 const int64_t n0 = static_cast<int64_t>(n_blk) * TILE + c * 32;
                 float f[32];
                 chunk_factors(f, fa, n0, p);
-                if (m < p.M) store_chunk(r, m, n0, p, f, rmw);
+                if (f32) emit_f32_chunk(slot, r, f, m0, n0, p, map);
+                else if (m < p.M) store_chunk(r, m, n0, p, f, false);
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -545,6 +620,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
+        if (lane == 0) ptx::bulk_wait_group_all();   // every TMA store has completed
+        __syncwarp();
     }
 
     ptx::tc_fence_before();
@@ -1126,10 +1203,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
         // 16-byte piece j of row r at piece j ^ ((r >> 1) & 3).
         const int q = warp & 3, h = (warp - 8) >> 2;
         uint8_t* stg = epi_stage + (warp - 8) * kMxEpiStage;
-        const uint32_t stg_s = ptx::smem_u32(stg);
-        uint8_t* my_row = stg + lane * 64;
-        const int swz = (lane >> 1) & 3;
         const bool f32 = p.out == FP8_OUT_F32;
+        const bool add = f32 && p.accumulate;
+        float ones[32];   // unit factors: the block scales are applied in the MMA
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ones[j] = 1.0f;
         uint32_t acc_phase = 0;
         for (int u = pair; u < num_units; u += npairs) {
             int m_blk, n_blk;
@@ -1142,27 +1220,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
             __syncwarp();
             ptx::tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
-            // stage one box (this thread's row: four 16-byte pieces) and store it
-            // at column x (whole-warp call)
+            // one staged 32-row x 64-byte box to global memory at column x
             auto emit = [&](const uint4 (&piece)[4], int64_t x) {
-                if (lane == 0) ptx::bulk_wait_group_read<0>();   // the slot's last store has read it
-                __syncwarp();
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4*>(my_row + 16 * (j ^ swz)) = piece[j];
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (m0 < p.M && x < p.N) {
-                        if (f32 && p.accumulate)
-                            ptx::tma_reduce_add_2d(&tmD, stg_s, static_cast<int32_t>(x),
-                                                   static_cast<int32_t>(m0));
-                        else
-                            ptx::tma_store_2d(&tmD, stg_s, static_cast<int32_t>(x),
-                                              static_cast<int32_t>(m0));
-                    }
-                    ptx::bulk_commit_group();
-                }
+                emit_box(stg, piece, &tmD, x, m0, m0 < p.M && x < p.N, add);
             };
             if (!f32) {
                 // read and pack the 128 columns first, hand the accumulator back,
@@ -1204,34 +1264,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
                         if (lane == 0) ptx::mbar_arrive_cluster(ptx::cluster_addr(tempty, 0));
                     }
 #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const int64_t nc = n0 + (c + i) * 32;
-                        float v[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[i][e]);
-                        if (p.bias) {
-#pragma unroll
-                            for (int j = 0; j < 32; j += 8) {
-                                if (nc + j < p.N) {
-                                    float b[8];
-                                    load_bias8(b, p.bias, nc + j);
-#pragma unroll
-                                    for (int e = 0; e < 8; ++e) v[j + e] = __fadd_rn(v[j + e], b[e]);
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int hb = 0; hb < 2; ++hb) {   // two 16-column boxes
-                            uint4 piece[4];
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                piece[j] = make_uint4(__float_as_uint(v[16 * hb + 4 * j]),
-                                                      __float_as_uint(v[16 * hb + 4 * j + 1]),
-                                                      __float_as_uint(v[16 * hb + 4 * j + 2]),
-                                                      __float_as_uint(v[16 * hb + 4 * j + 3]));
-                            emit(piece, nc + 16 * hb);
-                        }
-                    }
+                    for (int i = 0; i < 2; ++i)
+                        emit_f32_chunk(stg, r[i], ones, m0, n0 + (c + i) * 32, p, &tmD);
                 }
             }
             acc_phase ^= 1u;
@@ -1315,7 +1349,7 @@ int make_store_map(CUtensorMap* map, void* ptr, int64_t M, int64_t N, int out) {
 
 constexpr int kTensorBN = 256, kTensorStages = 4;
 constexpr int kPairStages = 6;
-constexpr int kPairSmemBytes = kPairStages * 2 * 128 * BK + 256 + 1024;
+constexpr int kPairSmemBytes = kPairStages * 2 * 128 * BK + 4 * 2048 + 256 + 1024;
 // Problems with at least this many rows use the CTA-pair kernel.
 constexpr int64_t kPairMinRows = 256;
 constexpr int kBlockStages = 6;
@@ -1480,13 +1514,15 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
     const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
     const int grid = static_cast<int>(tiles < num_sms() ? tiles : num_sms());
     if (pair) {
+        CUtensorMap tmD;
+        if ((st = make_store_map(&tmD, D, M, N, out)) != FP8_OK) return st;
         auto k = gemm_pair_kernel<kPairStages, false>;
         if ((st = ensure_smem(k, kPairSmemBytes, 2)) != FP8_OK) return st;
         const int64_t clusters =
             pair_clusters(reinterpret_cast<const void*>(k), 0, 256, kPairSmemBytes);
         const int pgrid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
         GemmParams none{};
-        k<<<pgrid, 256, kPairSmemBytes, stream>>>(tmA, tmB, p, tmA, tmB, none);
+        k<<<pgrid, 256, kPairSmemBytes, stream>>>(tmA, tmB, tmD, p, tmA, tmB, tmD, none);
     } else if (!block) {
         using L = Layout<kTensorBN, kTensorStages>;
         auto k = gemm_tensor_kernel<kTensorBN, kTensorStages>;
@@ -1520,7 +1556,8 @@ bool pair_eligible(const GemmArgs& g) {
     return !block && g.M >= kPairMinRows && g.N > 0 && g.K > 0 && !g.bias;
 }
 
-int pair_params(const GemmArgs& g, GemmParams& p, CUtensorMap& tmA, CUtensorMap& tmB) {
+int pair_params(const GemmArgs& g, GemmParams& p, CUtensorMap& tmA, CUtensorMap& tmB,
+                CUtensorMap& tmD) {
     p = GemmParams{};
     p.M = g.M; p.N = g.N; p.K = g.K;
     p.num_m = static_cast<int>((g.M + 255) / 256);
@@ -1531,7 +1568,8 @@ int pair_params(const GemmArgs& g, GemmParams& p, CUtensorMap& tmA, CUtensorMap&
     p.D = g.D; p.out = g.out; p.accumulate = g.accumulate;
     int st = make_kmajor_map(&tmA, g.A, g.M, g.K, BM);
     if (st != FP8_OK) return st;
-    return make_kmajor_map(&tmB, g.B, g.N, g.K, 128);
+    if ((st = make_kmajor_map(&tmB, g.B, g.N, g.K, 128)) != FP8_OK) return st;
+    return make_store_map(&tmD, g.D, g.M, g.N, g.out);
 }
 
 }  // namespace
@@ -1545,9 +1583,9 @@ int launch_gemm_group(const GemmArgs& g1, const GemmArgs& g2, cudaStream_t strea
                            g2.sb, g2.bias, g2.D, g2.out, g2.accumulate, stream);
     }
     GemmParams p1, p2;
-    CUtensorMap a1, b1, a2, b2;
-    int st = pair_params(g1, p1, a1, b1);
-    if (st == FP8_OK) st = pair_params(g2, p2, a2, b2);
+    CUtensorMap a1, b1, d1, a2, b2, d2;
+    int st = pair_params(g1, p1, a1, b1, d1);
+    if (st == FP8_OK) st = pair_params(g2, p2, a2, b2, d2);
     if (st != FP8_OK) return st;
     // the deeper problem's tiles first, so the last round holds the cheaper tiles
     const bool swap = p2.num_kb > p1.num_kb;
@@ -1557,8 +1595,8 @@ int launch_gemm_group(const GemmArgs& g1, const GemmArgs& g2, cudaStream_t strea
                           static_cast<int64_t>(p2.num_m) * p2.num_n;
     const int64_t clusters = pair_clusters(reinterpret_cast<const void*>(k), 1, 256, kPairSmemBytes);
     const int grid = static_cast<int>(2 * (units < clusters ? units : clusters));
-    if (swap) k<<<grid, 256, kPairSmemBytes, stream>>>(a2, b2, p2, a1, b1, p1);
-    else k<<<grid, 256, kPairSmemBytes, stream>>>(a1, b1, p1, a2, b2, p2);
+    if (swap) k<<<grid, 256, kPairSmemBytes, stream>>>(a2, b2, d2, p2, a1, b1, d1, p1);
+    else k<<<grid, 256, kPairSmemBytes, stream>>>(a1, b1, d1, p1, a2, b2, d2, p2);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(FP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
     return FP8_OK;
