@@ -471,12 +471,54 @@ def e2e_pass(F, recipe, dev, args, stream):
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / n
+    link = _host_link(dev)
+    floor_ms = (h2d + d2h) / (link["both_gbs"] * 1e9) * 1e3
     return {"value": round(_flops_step() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "steps": n, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "copies": "pinned host <-> device on two copy streams, overlapped with compute and "
-                      "with each other across linears and steps; host link measured at "
-                      "~211 GB/s H2D, ~193 GB/s D2H, ~342 GB/s both ways"}
+                      "with each other across linears and steps",
+            "host_link": link,
+            "link_floor_ms": round(floor_ms, 3),
+            "link_floor_note": "(h2d + d2h bytes) / measured both-ways link bandwidth: no "
+                               "schedule of these copies can take less"}
+
+
+def _host_link(dev, mib=1024, reps=3):
+    """Pinned host <-> device copy bandwidth of this machine, measured now: H2D
+    alone, D2H alone, and both at once on two streams (GB/s, best of reps)."""
+    n = mib << 20
+    hs = [torch.empty(n, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    ds = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(2)]
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            best = min(best, time.perf_counter() - t0)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            ds[0].copy_(hs[0], non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            hs[1].copy_(ds[1], non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    t_h, t_d, t_b = timed(h2d), timed(d2h), timed(both)
+    out = {"h2d_gbs": round(n / t_h / 1e9, 1), "d2h_gbs": round(n / t_d / 1e9, 1),
+           "both_gbs": round(2 * n / t_b / 1e9, 1), "bytes_per_test": n}
+    del hs, ds
+    return out
 
 
 # ------------------------------------------------------------- CPU oracle
