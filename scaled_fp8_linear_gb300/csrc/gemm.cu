@@ -303,6 +303,7 @@ template <int BN, int STAGES>
 __global__ void __launch_bounds__(256, 1)
     gemm_tensor_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    ptx::griddep_launch_dependents();   // the next kernel may launch now
     using L = Layout<BN, STAGES>;
     constexpr uint32_t TMEM_COLS = 2 * BN;
     extern __shared__ uint8_t smem_raw[];
@@ -342,6 +343,7 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    ptx::griddep_wait();   // the previous kernel's results (operands, factors) are visible
     const int num_tiles = p.num_m * p.num_n;
 
     if (warp == 0) {
@@ -447,6 +449,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                      const __grid_constant__ CUtensorMap tmB2,
                      const __grid_constant__ CUtensorMap tmD2,
                      const __grid_constant__ GemmParams p2) {
+    ptx::griddep_launch_dependents();   // the next kernel may launch now
     constexpr int HALF = 128;              // rows of A and of B held by each CTA
     constexpr int TILE = 2 * HALF;         // pair tile: 256 x 256
     constexpr int A_BYTES = HALF * BK, B_BYTES = HALF * BK;
@@ -501,6 +504,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     ptx::cluster_sync();   // the peer's barriers exist before any remote arrival
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    ptx::griddep_wait();   // the previous kernel's results (operands, factors) are visible
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
     if (warp == 0) {
@@ -706,6 +710,7 @@ template <int STAGES, bool COLSCALE>
 __global__ void __launch_bounds__(kBlockThreads, 1)
     gemm_block_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+    ptx::griddep_launch_dependents();   // the next kernel may launch now
     constexpr int BN = 128;
     __shared__ __align__(16) float colf[COLSCALE ? kBlockEpiWarps : 1][32];
     constexpr int NBUF = 4;
@@ -748,6 +753,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    ptx::griddep_wait();   // the previous kernel's results (operands, factors) are visible
     const int num_tiles = p.num_m * p.num_n;
 
     if (warp == 0) {
@@ -986,6 +992,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmD,
                    const __grid_constant__ GemmParams p, int vec_a, int vec_b) {
+    ptx::griddep_launch_dependents();   // the next kernel may launch now
     constexpr int HALF = 128;              // rows of A and of B held by each CTA
     constexpr int TILE = 2 * HALF;         // pair tile: 256 x 256
     constexpr int A_BYTES = HALF * BK, B_BYTES = HALF * BK;
@@ -1042,6 +1049,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
     ptx::cluster_sync();   // the peer's barriers exist before any remote arrival
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    ptx::griddep_wait();   // the previous kernel's results (operands, factors) are visible
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     const int num_units = p.num_m * p.num_n;
     const int num_slots = (p.num_kb + KPS - 1) / KPS;   // factor slots per tile
@@ -1415,6 +1423,8 @@ int num_sms() {
 // D[m][n] (+)= bias[n] for a GEMM with K = 0 (grid-stride over M x N).
 __global__ void bias_rows_kernel(const __nv_bfloat16* __restrict__ bias, int64_t M, int64_t N,
                                  void* D, int out, int rmw) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
     const int64_t n_all = M * N;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_all;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -1453,7 +1463,7 @@ int launch_gemm_mx(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M
     // factors of four K blocks as one float4: rows of a multiple of 4 floats, aligned arrays
     const int vec_a = p.num_kb % 4 == 0 && (reinterpret_cast<uintptr_t>(sa) & 15u) == 0;
     const int vec_b = p.num_kb % 4 == 0 && (reinterpret_cast<uintptr_t>(sb) & 15u) == 0;
-    k<<<grid, kMxThreads, kMxSmemBytes, stream>>>(tmA, tmB, tmD, p, vec_a, vec_b);
+    launch_pdl(k, dim3(grid), dim3(kMxThreads), kMxSmemBytes, stream, tmA, tmB, tmD, p, vec_a, vec_b);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(FP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
     return FP8_OK;
@@ -1472,8 +1482,7 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
     if (K == 0 && bias) {   // an empty sum: D (+)= bias
         const int64_t n = M * N;
         const int64_t blocks = (n + 255) / 256;
-        bias_rows_kernel<<<static_cast<unsigned>(blocks < 65535 * 16 ? blocks : 65535 * 16), 256,
-                           0, stream>>>(static_cast<const __nv_bfloat16*>(bias), M, N, D, out,
+        launch_pdl(bias_rows_kernel, dim3(static_cast<unsigned>(blocks < 65535 * 16 ? blocks : 65535 * 16)), dim3(256), 0, stream, static_cast<const __nv_bfloat16*>(bias), M, N, D, out,
                                         out == FP8_OUT_F32 && accumulate);
         const cudaError_t e = cudaGetLastError();
         return e == cudaSuccess ? FP8_OK
@@ -1522,22 +1531,22 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
             pair_clusters(reinterpret_cast<const void*>(k), 0, 256, kPairSmemBytes);
         const int pgrid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
         GemmParams none{};
-        k<<<pgrid, 256, kPairSmemBytes, stream>>>(tmA, tmB, tmD, p, tmA, tmB, tmD, none);
+        launch_pdl(k, dim3(pgrid), dim3(256), kPairSmemBytes, stream, tmA, tmB, tmD, p, tmA, tmB, tmD, none);
     } else if (!block) {
         using L = Layout<kTensorBN, kTensorStages>;
         auto k = gemm_tensor_kernel<kTensorBN, kTensorStages>;
         if ((st = ensure_smem(k, L::SMEM_BYTES, 0)) != FP8_OK) return st;
-        k<<<grid, 256, L::SMEM_BYTES, stream>>>(tmA, tmB, p);
+        launch_pdl(k, dim3(grid), dim3(256), L::SMEM_BYTES, stream, tmA, tmB, p);
     } else {
         using L = Layout<128, kBlockStages>;
         if (gb == FP8_GRAN_1x128) {
             auto k = gemm_block_kernel<kBlockStages, true>;
             if ((st = ensure_smem(k, L::SMEM_BYTES, 3)) != FP8_OK) return st;
-            k<<<grid, kBlockThreads, L::SMEM_BYTES, stream>>>(tmA, tmB, p);
+            launch_pdl(k, dim3(grid), dim3(kBlockThreads), L::SMEM_BYTES, stream, tmA, tmB, p);
         } else {
             auto k = gemm_block_kernel<kBlockStages, false>;
             if ((st = ensure_smem(k, L::SMEM_BYTES, 1)) != FP8_OK) return st;
-            k<<<grid, kBlockThreads, L::SMEM_BYTES, stream>>>(tmA, tmB, p);
+            launch_pdl(k, dim3(grid), dim3(kBlockThreads), L::SMEM_BYTES, stream, tmA, tmB, p);
         }
     }
     const cudaError_t e = cudaGetLastError();
@@ -1595,8 +1604,8 @@ int launch_gemm_group(const GemmArgs& g1, const GemmArgs& g2, cudaStream_t strea
                           static_cast<int64_t>(p2.num_m) * p2.num_n;
     const int64_t clusters = pair_clusters(reinterpret_cast<const void*>(k), 1, 256, kPairSmemBytes);
     const int grid = static_cast<int>(2 * (units < clusters ? units : clusters));
-    if (swap) k<<<grid, 256, kPairSmemBytes, stream>>>(a2, b2, d2, p2, a1, b1, d1, p1);
-    else k<<<grid, 256, kPairSmemBytes, stream>>>(a1, b1, d1, p1, a2, b2, d2, p2);
+    if (swap) launch_pdl(k, dim3(grid), dim3(256), kPairSmemBytes, stream, a2, b2, d2, p2, a1, b1, d1, p1);
+    else launch_pdl(k, dim3(grid), dim3(256), kPairSmemBytes, stream, a1, b1, d1, p1, a2, b2, d2, p2);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(FP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
     return FP8_OK;

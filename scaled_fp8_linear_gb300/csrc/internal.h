@@ -6,10 +6,31 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "../../include/fp8linear.h"
 
 namespace fp8 {
+
+// Launch `kernel` on `stream` with programmatic stream serialisation: it may
+// start while the previous kernel of the stream finishes, and it waits for
+// that kernel (griddepcontrol.wait) before touching global memory -- every
+// kernel of this library does.  Errors are also left for cudaGetLastError().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Number of SMs of the current device (cached per device).
 int num_sms();

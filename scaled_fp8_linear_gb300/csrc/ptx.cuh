@@ -110,6 +110,26 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity,
     }
 }
 
+// ------------------------------------------------- programmatic dependent launch
+//
+// Kernels of this library may be launched with programmatic stream
+// serialisation: the next kernel in the stream can start (run its prologue)
+// while this one finishes.  Every kernel therefore calls griddep_wait() before
+// its first access to global memory (it returns at once when the kernel was
+// not launched that way), and griddep_launch_dependents() early, which lets
+// the next kernel launch once every CTA of this one has started.
+
+// Wait until the preceding kernel in the stream has completed and its memory
+// operations are visible.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next (programmatically serialised) kernel in the stream to launch.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

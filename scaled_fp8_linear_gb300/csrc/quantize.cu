@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace fp8 {
 namespace {
@@ -300,6 +301,8 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint4* __restrict_
                                                         int64_t nvec,
                                                         const uint16_t* __restrict__ tail,
                                                         int tail_n, unsigned* amax_bits) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
     uint32_t m = 0;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -330,6 +333,8 @@ __global__ void update_scale_kernel(const float* __restrict__ amax, float* __res
                                     int margin, int pow2, float* __restrict__ scale,
                                     float* __restrict__ scale_inv, float* __restrict__ saved,
                                     int save_after, unsigned* status) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
     const int r = blockIdx.x, lane = threadIdx.x;
     float* hist = history + static_cast<int64_t>(r) * H;
     const float a = amax[r];
@@ -380,6 +385,8 @@ __global__ void __launch_bounds__(kThreads)
                          uint8_t* __restrict__ qtail, unsigned* amax_bits,
                          unsigned long long* counts, SrKey sr_key,
                          const unsigned long long* key_dev) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
     const float s = *scale_p;
     const SrSched key = sr_sched(sr_key_of(sr_key, SR ? key_dev : nullptr));
     uint32_t m = 0;
@@ -555,6 +562,8 @@ __global__ void __launch_bounds__(kThreads)
                               unsigned* amax_bits, unsigned long long* counts, SrKey sr_key,
                               float* __restrict__ dbias_partial,
                               const unsigned long long* key_dev) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
     static_assert(!(SR && DBIAS), "the bias-gradient sums ride on the round-to-nearest cast");
     CastCounts cc;
     const SrSched key = sr_sched(sr_key_of(sr_key, SR ? key_dev : nullptr));
@@ -609,6 +618,8 @@ struct CastJob {
 template <int FMT, bool AMAX>
 __global__ void __launch_bounds__(kThreads)
     quantize_transpose_pair_kernel(CastJob j0, CastJob j1, int64_t tiles0) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
     __shared__ __align__(16) uint32_t S[128 * 32];
     const bool second = blockIdx.x >= tiles0;
     const CastJob& j = second ? j1 : j0;
@@ -625,6 +636,8 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     column_partial_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
                           int64_t tiles_c, float* __restrict__ partial) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
     const int64_t tile = blockIdx.x;
     const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
     const int t = threadIdx.x, cg = t & 7;
@@ -646,6 +659,8 @@ __global__ void __launch_bounds__(kThreads)
 // (+ the old dbias[n] when accumulating).
 __global__ void dbias_finalize_kernel(const float* __restrict__ partial, int64_t P, int64_t cols,
                                       float* __restrict__ dbias, int accumulate) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
     const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (n >= cols) return;
     float v = 0.0f;
@@ -655,7 +670,11 @@ __global__ void dbias_finalize_kernel(const float* __restrict__ partial, int64_t
 
 // The counter word of a device-held stochastic-rounding key moves on by
 // one after a cast has used it.
-__global__ void sr_advance_kernel(unsigned long long* key_dev) { key_dev[1] += 1ull; }
+__global__ void sr_advance_kernel(unsigned long long* key_dev) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
+    key_dev[1] += 1ull;
+}
 
 // ----------------------------------------------------------- block casts
 
@@ -665,6 +684,8 @@ template <int FMT>
 __global__ void __launch_bounds__(kThreads)
     quantize_1x128_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int pow2,
                           uint8_t* __restrict__ q, float* __restrict__ scale_inv) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
     // a half-warp per 128-element segment, a warp per pair of segments; each
     // warp takes kU pairs per step with all their loads issued first, so that
     // enough bytes are in flight to cover the memory latency
@@ -714,6 +735,8 @@ __global__ void __launch_bounds__(kThreads)
     quantize_128x128_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int pow2,
                             uint8_t* __restrict__ q, float* __restrict__ scale_inv,
                             uint8_t* __restrict__ qt, float* __restrict__ scale_inv_t) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
     __shared__ uint32_t warp_max[kThreads / 32];
     __shared__ __align__(16) uint32_t S[128 * 32];
     const int64_t KB = cols / 128;
@@ -767,6 +790,8 @@ __global__ void __launch_bounds__(kThreads)
                                int64_t tiles_c, int pow2, uint8_t* __restrict__ q,
                                float* __restrict__ scale_inv, uint8_t* __restrict__ qt,
                                float* __restrict__ scale_inv_t) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
     __shared__ __align__(16) uint32_t S[128 * 32];          // column-scaled codes, swizzled rows
     __shared__ uint32_t colpart[kThreads / 32][64];         // per warp: 128 column maxima, 2 per word
     __shared__ __align__(16) float colscale[128];
@@ -864,6 +889,8 @@ template <int FMT>
 __global__ void __launch_bounds__(kThreads)
     quantize_row_kernel(const uint16_t* __restrict__ x, int64_t cols, int pow2,
                         uint8_t* __restrict__ q, float* __restrict__ scale_inv) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
     __shared__ uint32_t warp_max[kThreads / 32];
     const int64_t row = blockIdx.x;
     const uint4* src = reinterpret_cast<const uint4*>(x + row * cols);
@@ -895,6 +922,8 @@ __global__ void __launch_bounds__(kThreads)
     row_col_amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
                         int64_t tiles_c, unsigned* __restrict__ rowmax,
                         unsigned* __restrict__ colmax) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
     __shared__ uint32_t colpart[kThreads / 32][64];
     const int64_t tile = blockIdx.x;
     const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
@@ -955,6 +984,8 @@ __global__ void __launch_bounds__(kThreads)
                             int64_t tiles_c, int pow2, const unsigned* __restrict__ rowmax,
                             const unsigned* __restrict__ colmax, uint8_t* __restrict__ q,
                             uint8_t* __restrict__ qt) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
     __shared__ __align__(16) uint32_t S[128 * 32];
     __shared__ __align__(16) float colscale[128];
     const int64_t tile = blockIdx.x;
@@ -1008,6 +1039,8 @@ __global__ void __launch_bounds__(kThreads)
 // scale_inv_t[c] = 1 / s(amax_c), in place over the column amaxes.
 template <int FMT>
 __global__ void column_scale_finalize_kernel(float* __restrict__ sinv_t, int64_t cols, int pow2) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
     const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (c < cols) {
         const float amax = sinv_t[c];
@@ -1029,7 +1062,7 @@ cudaError_t launch_amax(const void* x, int64_t n, float* amax, cudaStream_t stre
     const int64_t nvec = n / 8;
     const int tail_n = static_cast<int>(n - nvec * 8);
     const uint16_t* tail = static_cast<const uint16_t*>(x) + nvec * 8;
-    amax_kernel<<<grid_for(nvec + 1, kThreads * 4), kThreads, 0, stream>>>(
+    launch_pdl(amax_kernel, dim3(grid_for(nvec + 1, kThreads * 4)), dim3(kThreads), 0, stream, 
         static_cast<const uint4*>(x), nvec, tail, tail_n, reinterpret_cast<unsigned*>(amax));
     return cudaGetLastError();
 }
@@ -1038,7 +1071,7 @@ cudaError_t launch_update_scale(const float* amax, float* history, int32_t* pos,
                                 int fmt, int margin, int pow2, float* scale, float* scale_inv,
                                 int nroles, cudaStream_t stream, float* saved, int save_after) {
     const float fmax = fmt == 0 ? 448.0f : 57344.0f;
-    update_scale_kernel<<<nroles, 32, 0, stream>>>(amax, history, pos, H, algo, fmax, margin,
+    launch_pdl(update_scale_kernel, dim3(nroles), dim3(32), 0, stream, amax, history, pos, H, algo, fmax, margin,
                                                    pow2, scale, scale_inv, saved, save_after,
                                                    device_status_word());
     return cudaGetLastError();
@@ -1050,7 +1083,7 @@ static void launch_flat(const void* x, int64_t n, const float* scale, uint8_t* q
                         const unsigned long long* key_dev = nullptr) {
     const int64_t n16 = n / 16;
     const int tail_n = static_cast<int>(n - n16 * 16);
-    quantize_flat_kernel<FMT, AMAX, COUNT, SR><<<grid_for(n16 + 1, kThreads * 2), kThreads, 0, stream>>>(
+    launch_pdl(quantize_flat_kernel<FMT, AMAX, COUNT, SR>, dim3(grid_for(n16 + 1, kThreads * 2)), dim3(kThreads), 0, stream, 
         static_cast<const uint4*>(x), n16, static_cast<const uint16_t*>(x) + n16 * 16, tail_n,
         scale, reinterpret_cast<uint4*>(q), q + n16 * 16, reinterpret_cast<unsigned*>(amax), counts,
         key, key_dev);
@@ -1062,8 +1095,7 @@ static void launch_transpose(const void* x, int64_t rows, int64_t cols, const fl
                              const SrKey& key, cudaStream_t stream, float* dbias_partial = nullptr,
                              const unsigned long long* key_dev = nullptr) {
     const int64_t tiles_c = (cols + 127) / 128, tiles_r = (rows + 127) / 128;
-    quantize_transpose_kernel<FMT, AMAX, COUNT, SR, DBIAS><<<static_cast<unsigned>(tiles_r * tiles_c),
-                                                             kThreads, 0, stream>>>(
+    launch_pdl(quantize_transpose_kernel<FMT, AMAX, COUNT, SR, DBIAS>, dim3(static_cast<unsigned>(tiles_r * tiles_c)), dim3(kThreads), 0, stream, 
         static_cast<const uint16_t*>(x), rows, cols, tiles_c, scale, q, qt,
         reinterpret_cast<unsigned*>(amax), counts, key, dbias_partial, key_dev);
 }
@@ -1150,11 +1182,11 @@ cudaError_t launch_quantize_pair(const void* x0, int64_t rows0, int64_t cols0, c
     if (t0 + t1 == 0) return cudaSuccess;
     const unsigned grid = static_cast<unsigned>(t0 + t1);
     if (fmt == 0) {
-        if (A) quantize_transpose_pair_kernel<0, true><<<grid, kThreads, 0, stream>>>(j0, j1, t0);
-        else quantize_transpose_pair_kernel<0, false><<<grid, kThreads, 0, stream>>>(j0, j1, t0);
+        if (A) launch_pdl(quantize_transpose_pair_kernel<0, true>, dim3(grid), dim3(kThreads), 0, stream, j0, j1, t0);
+        else launch_pdl(quantize_transpose_pair_kernel<0, false>, dim3(grid), dim3(kThreads), 0, stream, j0, j1, t0);
     } else {
-        if (A) quantize_transpose_pair_kernel<1, true><<<grid, kThreads, 0, stream>>>(j0, j1, t0);
-        else quantize_transpose_pair_kernel<1, false><<<grid, kThreads, 0, stream>>>(j0, j1, t0);
+        if (A) launch_pdl(quantize_transpose_pair_kernel<1, true>, dim3(grid), dim3(kThreads), 0, stream, j0, j1, t0);
+        else launch_pdl(quantize_transpose_pair_kernel<1, false>, dim3(grid), dim3(kThreads), 0, stream, j0, j1, t0);
     }
     return cudaGetLastError();
 }
@@ -1165,10 +1197,10 @@ cudaError_t launch_dbias(const void* x, int64_t rows, int64_t cols, float* parti
     const int64_t P = (rows + 127) / 128;
     if (!partial_ready && rows > 0) {
         const int64_t tiles_c = (cols + 127) / 128;
-        column_partial_kernel<<<static_cast<unsigned>(P * tiles_c), kThreads, 0, stream>>>(
+        launch_pdl(column_partial_kernel, dim3(static_cast<unsigned>(P * tiles_c)), dim3(kThreads), 0, stream, 
             static_cast<const uint16_t*>(x), rows, cols, tiles_c, partial);
     }
-    dbias_finalize_kernel<<<static_cast<unsigned>((cols + 255) / 256), 256, 0, stream>>>(
+    launch_pdl(dbias_finalize_kernel, dim3(static_cast<unsigned>((cols + 255) / 256)), dim3(256), 0, stream, 
         partial, P, cols, dbias, accumulate);
     return cudaGetLastError();
 }
@@ -1183,7 +1215,7 @@ cudaError_t launch_quantize_sr(const void* x, int64_t rows, int64_t cols, int fm
     cudaError_t e = quantize_tensor<true>(x, rows, cols, fmt, scale, q, q_t, amax, nullptr, key,
                                           stream, nullptr, kd);
     if (e != cudaSuccess || !key_dev) return e;
-    sr_advance_kernel<<<1, 1, 0, stream>>>(kd);
+    launch_pdl(sr_advance_kernel, dim3(1), dim3(1), 0, stream, kd);
     return cudaGetLastError();
 }
 
@@ -1192,7 +1224,7 @@ static cudaError_t launch_row(const uint16_t* xs, int64_t rows, int64_t cols, in
                               float* scale_inv, uint8_t* q_t, float* scale_inv_t,
                               cudaStream_t stream) {
     if (!q_t) {
-        quantize_row_kernel<FMT><<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(xs, cols, pow2, q, scale_inv);
+        launch_pdl(quantize_row_kernel<FMT>, dim3(static_cast<unsigned>(rows)), dim3(kThreads), 0, stream, xs, cols, pow2, q, scale_inv);
         return cudaGetLastError();
     }
     // with the transposed copy: two tiled reads of x; the scale arrays hold the
@@ -1203,13 +1235,13 @@ static cudaError_t launch_row(const uint16_t* xs, int64_t rows, int64_t cols, in
     const int64_t tiles_c = (cols + 127) / 128, tiles = ((rows + 127) / 128) * tiles_c;
     auto* rmax = reinterpret_cast<unsigned*>(scale_inv);
     auto* cmax = reinterpret_cast<unsigned*>(scale_inv_t);
-    row_col_amax_kernel<<<static_cast<unsigned>(tiles), kThreads, 0, stream>>>(xs, rows, cols, tiles_c,
+    launch_pdl(row_col_amax_kernel, dim3(static_cast<unsigned>(tiles)), dim3(kThreads), 0, stream, xs, rows, cols, tiles_c,
                                                                                rmax, cmax);
-    quantize_row_col_kernel<FMT><<<static_cast<unsigned>(tiles), kThreads, 0, stream>>>(
+    launch_pdl(quantize_row_col_kernel<FMT>, dim3(static_cast<unsigned>(tiles)), dim3(kThreads), 0, stream, 
         xs, rows, cols, tiles_c, pow2, rmax, cmax, q, q_t);
-    column_scale_finalize_kernel<FMT><<<static_cast<unsigned>((rows + 255) / 256), 256, 0, stream>>>(
+    launch_pdl(column_scale_finalize_kernel<FMT>, dim3(static_cast<unsigned>((rows + 255) / 256)), dim3(256), 0, stream, 
         scale_inv, rows, pow2);
-    column_scale_finalize_kernel<FMT><<<static_cast<unsigned>((cols + 255) / 256), 256, 0, stream>>>(
+    launch_pdl(column_scale_finalize_kernel<FMT>, dim3(static_cast<unsigned>((cols + 255) / 256)), dim3(256), 0, stream, 
         scale_inv_t, cols, pow2);
     return cudaGetLastError();
 }
@@ -1232,18 +1264,18 @@ cudaError_t launch_quantize_block(const void* x, int64_t rows, int64_t cols, int
         const int64_t tiles_c = cols / 128;
         const unsigned tiles = static_cast<unsigned>((rows / 128) * tiles_c);
         if (fmt == 0)
-            quantize_1x128_dual_kernel<0><<<tiles, kThreads, 0, stream>>>(xs, rows, cols, tiles_c, pow2, q, scale_inv, q_t, scale_inv_t);
+            launch_pdl(quantize_1x128_dual_kernel<0>, dim3(tiles), dim3(kThreads), 0, stream, xs, rows, cols, tiles_c, pow2, q, scale_inv, q_t, scale_inv_t);
         else
-            quantize_1x128_dual_kernel<1><<<tiles, kThreads, 0, stream>>>(xs, rows, cols, tiles_c, pow2, q, scale_inv, q_t, scale_inv_t);
+            launch_pdl(quantize_1x128_dual_kernel<1>, dim3(tiles), dim3(kThreads), 0, stream, xs, rows, cols, tiles_c, pow2, q, scale_inv, q_t, scale_inv_t);
     } else if (gran == 1) {
         const int64_t pairs = (rows * (cols / 128) + 1) / 2;
         const int grid = grid_for(pairs, kThreads / 32);
-        if (fmt == 0) quantize_1x128_kernel<0><<<grid, kThreads, 0, stream>>>(xs, rows, cols, pow2, q, scale_inv);
-        else quantize_1x128_kernel<1><<<grid, kThreads, 0, stream>>>(xs, rows, cols, pow2, q, scale_inv);
+        if (fmt == 0) launch_pdl(quantize_1x128_kernel<0>, dim3(grid), dim3(kThreads), 0, stream, xs, rows, cols, pow2, q, scale_inv);
+        else launch_pdl(quantize_1x128_kernel<1>, dim3(grid), dim3(kThreads), 0, stream, xs, rows, cols, pow2, q, scale_inv);
     } else {
         const unsigned tiles = static_cast<unsigned>((rows / 128) * (cols / 128));
-        if (fmt == 0) quantize_128x128_kernel<0><<<tiles, kThreads, 0, stream>>>(xs, rows, cols, pow2, q, scale_inv, q_t, scale_inv_t);
-        else quantize_128x128_kernel<1><<<tiles, kThreads, 0, stream>>>(xs, rows, cols, pow2, q, scale_inv, q_t, scale_inv_t);
+        if (fmt == 0) launch_pdl(quantize_128x128_kernel<0>, dim3(tiles), dim3(kThreads), 0, stream, xs, rows, cols, pow2, q, scale_inv, q_t, scale_inv_t);
+        else launch_pdl(quantize_128x128_kernel<1>, dim3(tiles), dim3(kThreads), 0, stream, xs, rows, cols, pow2, q, scale_inv, q_t, scale_inv_t);
     }
     return cudaGetLastError();
 }

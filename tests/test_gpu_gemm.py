@@ -275,7 +275,8 @@ def _rand_codes(shape, seed):
     return v.to(torch.uint8).to(DEV)
 
 
-@pytest.mark.parametrize("case", ["bwd_like", "ragged", "rowscaled", "fallback_block", "small_m"])
+@pytest.mark.parametrize("case", ["bwd_like", "ragged", "rowscaled", "fallback_block", "small_m",
+                                  "pow2_block_bwd"])
 def test_gemm_group_equals_two_gemms(case):
     """fp8_gemm_group gives, bit for bit, the results of two fp8_gemm calls:
     the grouped CTA-pair launch computes every tile exactly as the single
@@ -308,6 +309,17 @@ def test_gemm_group_equals_two_gemms(case):
                   fb=F.E4M3, scale_inv_a=sa, scale_inv_b=sb, ga=F.GRAN_1x128, gb=F.GRAN_128x128)
         g2 = dict(A=_rand_codes((512, 256), 15), fa=F.E4M3, B=_rand_codes((256, 256), 16),
                   fb=F.E4M3, scale_inv_a=one, scale_inv_b=one)
+    elif case == "pow2_block_bwd":   # the block backward with power-of-two factors
+        M, N, K = 512, 384, 640      # dgrad (bf16) and wgrad (FP32, accumulated)
+        p2 = lambda shape, sd: (2.0 ** torch.randint(
+            -3, 4, shape, generator=torch.Generator().manual_seed(sd))).float().to(DEV)
+        g1 = dict(A=_rand_codes((M, N), 21), fa=F.E5M2, B=_rand_codes((K, N), 22), fb=F.E4M3,
+                  scale_inv_a=p2((M, N // 128), 1), scale_inv_b=p2((K // 128, N // 128), 2),
+                  ga=F.GRAN_1x128 | F.SCALE_POW2, gb=F.GRAN_128x128 | F.SCALE_POW2)
+        g2 = dict(A=_rand_codes((N, M), 23), fa=F.E5M2, B=_rand_codes((K, M), 24), fb=F.E4M3,
+                  scale_inv_a=p2((N, M // 128), 3), scale_inv_b=p2((K, M // 128), 4),
+                  ga=F.GRAN_1x128 | F.SCALE_POW2, gb=F.GRAN_1x128 | F.SCALE_POW2,
+                  out=F.OUT_F32, accumulate=True)
     else:                          # M < 256: the 1-CTA kernel, two launches
         g1 = dict(A=_rand_codes((128, 256), 17), fa=F.E4M3, B=_rand_codes((256, 256), 18),
                   fb=F.E4M3, scale_inv_a=one, scale_inv_b=one)
