@@ -333,7 +333,8 @@ __global__ void update_scale_kernel(const float* __restrict__ amax, float* __res
                                     int margin, int pow2, float* __restrict__ scale,
                                     float* __restrict__ scale_inv, float* __restrict__ saved,
                                     int save_after, unsigned* status) {
-    ptx::griddep_launch_dependents();
+    // (tiny kernel: the next one may launch when this one exits, not earlier,
+    // so a chain of launches cannot run ahead of the large kernel before it)
     ptx::griddep_wait();   // the previous kernel's results are visible
     const int r = blockIdx.x, lane = threadIdx.x;
     float* hist = history + static_cast<int64_t>(r) * H;
@@ -659,7 +660,8 @@ __global__ void __launch_bounds__(kThreads)
 // (+ the old dbias[n] when accumulating).
 __global__ void dbias_finalize_kernel(const float* __restrict__ partial, int64_t P, int64_t cols,
                                       float* __restrict__ dbias, int accumulate) {
-    ptx::griddep_launch_dependents();
+    // (tiny kernel: the next one may launch when this one exits, not earlier,
+    // so a chain of launches cannot run ahead of the large kernel before it)
     ptx::griddep_wait();   // the previous kernel's results are visible
     const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (n >= cols) return;
@@ -671,7 +673,8 @@ __global__ void dbias_finalize_kernel(const float* __restrict__ partial, int64_t
 // The counter word of a device-held stochastic-rounding key moves on by
 // one after a cast has used it.
 __global__ void sr_advance_kernel(unsigned long long* key_dev) {
-    ptx::griddep_launch_dependents();
+    // (tiny kernel: the next one may launch when this one exits, not earlier,
+    // so a chain of launches cannot run ahead of the large kernel before it)
     ptx::griddep_wait();   // the previous kernel's results are visible
     key_dev[1] += 1ull;
 }
@@ -1039,7 +1042,8 @@ __global__ void __launch_bounds__(kThreads)
 // scale_inv_t[c] = 1 / s(amax_c), in place over the column amaxes.
 template <int FMT>
 __global__ void column_scale_finalize_kernel(float* __restrict__ sinv_t, int64_t cols, int pow2) {
-    ptx::griddep_launch_dependents();
+    // (tiny kernel: the next one may launch when this one exits, not earlier,
+    // so a chain of launches cannot run ahead of the large kernel before it)
     ptx::griddep_wait();   // the previous kernel's results are visible
     const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (c < cols) {
@@ -1054,10 +1058,35 @@ int grid_for(int64_t work_items, int per_cta) {
     return static_cast<int>(need < 1 ? 1 : (need < cap ? need : cap));
 }
 
+// a[0..na) = 0 and b[0..nb) = 0 (b nullable): the maxima that the casts
+// raise atomically start from zero.  A kernel rather than a memset, so that it
+// takes part in programmatic dependent launch like the kernels around it.
+__global__ void zero_words_kernel(float* __restrict__ a, int64_t na, float* __restrict__ b,
+                                  int64_t nb) {
+    // (tiny kernel: the next one may launch when this one exits, not earlier,
+    // so a chain of launches cannot run ahead of the large kernel before it)
+    ptx::griddep_wait();   // the previous kernel's results are visible
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < na + nb;
+         i += stride) {
+        if (i < na) a[i] = 0.0f;
+        else b[i - na] = 0.0f;
+    }
+}
+
+cudaError_t launch_zero(float* a, int64_t na, float* b, int64_t nb, cudaStream_t stream) {
+    const int64_t n = na + (b ? nb : 0);
+    if (n == 0) return cudaSuccess;
+    const int64_t blocks = (n + 255) / 256;
+    launch_pdl(zero_words_kernel, dim3(static_cast<unsigned>(blocks < 1024 ? blocks : 1024)),
+               dim3(256), 0, stream, a, na, b, b ? nb : int64_t{0});
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_amax(const void* x, int64_t n, float* amax, cudaStream_t stream) {
-    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), stream);
+    cudaError_t e = launch_zero(amax, 1, nullptr, 0, stream);
     if (e != cudaSuccess || n == 0) return e;
     const int64_t nvec = n / 8;
     const int tail_n = static_cast<int>(n - nvec * 8);
@@ -1132,7 +1161,7 @@ static cudaError_t quantize_tensor(const void* x, int64_t rows, int64_t cols, in
                                    const unsigned long long* key_dev = nullptr) {
     const int64_t n = rows * cols;
     if (amax) {
-        cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), stream);
+        cudaError_t e = launch_zero(amax, 1, nullptr, 0, stream);
         if (e != cudaSuccess) return e;
     }
     if (n == 0) return cudaSuccess;
@@ -1161,13 +1190,7 @@ cudaError_t launch_quantize_pair(const void* x0, int64_t rows0, int64_t cols0, c
                                  uint8_t* qt1, float* amax1, int fmt, cudaStream_t stream) {
     const bool A = amax0 != nullptr;
     if (A) {
-        cudaError_t e;
-        if (amax1 == amax0 + 1) {
-            e = cudaMemsetAsync(amax0, 0, 2 * sizeof(float), stream);
-        } else {
-            e = cudaMemsetAsync(amax0, 0, sizeof(float), stream);
-            if (e == cudaSuccess) e = cudaMemsetAsync(amax1, 0, sizeof(float), stream);
-        }
+        const cudaError_t e = launch_zero(amax0, 1, amax1, 1, stream);
         if (e != cudaSuccess) return e;
     }
     auto job = [](const void* x, int64_t rows, int64_t cols, const float* scale, uint8_t* q,
@@ -1229,8 +1252,7 @@ static cudaError_t launch_row(const uint16_t* xs, int64_t rows, int64_t cols, in
     }
     // with the transposed copy: two tiled reads of x; the scale arrays hold the
     // row / column maxima until the last step turns them into 1/scale
-    cudaError_t e = cudaMemsetAsync(scale_inv, 0, rows * sizeof(float), stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(scale_inv_t, 0, cols * sizeof(float), stream);
+    const cudaError_t e = launch_zero(scale_inv, rows, scale_inv_t, cols, stream);
     if (e != cudaSuccess) return e;
     const int64_t tiles_c = (cols + 127) / 128, tiles = ((rows + 127) / 128) * tiles_c;
     auto* rmax = reinterpret_cast<unsigned*>(scale_inv);
