@@ -85,7 +85,8 @@ class Clocks:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        out_dir = os.environ.get("FP8_BENCH_OUT", os.path.join(ROOT, "bench_out"))
+        self.path = os.path.join(out_dir, f"clocks_rank{index}.csv")
 
     def start(self):
         try:
@@ -501,7 +502,7 @@ def _link_floor_ms(h2d, d2h, link):
 
 
 def _host_link(dev, mib=1024, reps=3):
-    """Pinned host <-> device copy bandwidth of this box, measured now: H2D
+    """Pinned host <-> device copy bandwidth of this machine, measured now: H2D
     alone, D2H alone, and both at once on two streams (GB/s, best of reps;
     for the concurrent test each direction is timed on its own stream)."""
     n = mib << 20

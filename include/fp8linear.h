@@ -49,7 +49,7 @@ extern "C" {
 #define FP8_ERR_ALIGN       (-3)  /* a pointer is not 16-byte aligned */
 #define FP8_ERR_CUDA        (-4)  /* a CUDA call failed; see fp8_last_error() */
 #define FP8_ERR_TIMEOUT     (-5)  /* a kernel's bounded wait gave up (device status) */
-#define FP8_ERR_UNSUPPORTED (-6)  /* valid combination that this build does not run */
+#define FP8_ERR_UNSUPPORTED (-6)  /* valid combination this library does not implement */
 
 /* ------------------------------------------------------------------ enums */
 typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_format_t;
