@@ -733,7 +733,13 @@ def run_kernel(args):
         M, N, K = dims
         A, B = codes(M, K), codes(N, K)
         D = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-        if args.kernel == "gemm":
+        if args.kernel == "gemm" and args.f32acc:
+            # the wgrad form: FP32 output accumulated into D
+            one = torch.ones(1, dtype=torch.float32, device=dev)
+            D = torch.zeros(M, N, dtype=torch.float32, device=dev)
+            call = lambda: F.fp8_gemm(A, fa, B, F.E4M3, one, one, D=D, out=F.OUT_F32,
+                                      accumulate=True)
+        elif args.kernel == "gemm":
             one = torch.ones(1, dtype=torch.float32, device=dev)
             call = lambda: F.fp8_gemm(A, fa, B, F.E4M3, one, one, D=D)
         elif args.pow2:
@@ -798,6 +804,8 @@ def run_kernel(args):
     if args.kernel == "block_gemm":
         extra = {"factors": "power of two (block-scaled MMA)" if args.pow2
                  else "fp32 (per-128-K promotion)"}
+    if args.kernel == "gemm":
+        extra = {"output": "fp32, accumulated" if args.f32acc else "bf16"}
     print(json.dumps({"kernel": args.kernel, "shape": dims, "format": args.fmt, **extra,
                       "median_ms": round(med, 4), "min_ms": round(ms[0], 4),
                       "achieved": round(ach, 1), "unit": unit, "peak": round(peak, 1),
@@ -983,6 +991,8 @@ def main():
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--gran", choices=["tensor", "1x128", "128x128", "row"], default="tensor",
                     help="--kernel quantize: scale granularity")
+    ap.add_argument("--f32acc", action="store_true",
+                    help="gemm: FP32 output accumulated into D (the wgrad form)")
     ap.add_argument("--pow2", action="store_true",
                     help="block_gemm / block_step: power-of-two block factors (the block-scaled MMA path)")
     ap.add_argument("--no-transpose", action="store_true",
