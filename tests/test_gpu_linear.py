@@ -78,6 +78,44 @@ def test_training_steps(recipe):
         dW_o = dW.cpu().numpy().astype(np.float64)   # next step accumulates onto the GPU buffer
 
 
+@pytest.mark.parametrize("M,N,K,with_bias", [(656, 272, 400, False), (656, 272, 400, True),
+                                             (272, 656, 400, False)],
+                         ids=["x_larger", "x_larger_dbias", "w_larger"])
+def test_dynamic_cast_order(M, N, K, with_bias):
+    """Dynamic scaling where X or W is the larger operand (the casts then
+    take the smaller one first and the larger one from its last tile), with
+    ragged tiles in every dimension: codes, transposes, amaxes and scales
+    bit-exact, Y / dX / dW (and dbias) within the bound, over 2 steps."""
+    rec = F.Recipe(F.SCALING_DYNAMIC)
+    layer = F.Fp8Linear(M, N, K, rec, device=DEV)
+    orec = _orecipe(rec)
+    ost = oracle.LinearState(orec)
+    W = synthetic.normal((N, K), 0.02, seed=21)
+    b = synthetic.normal((N,), 0.1, seed=22) if with_bias else None
+    dW = torch.zeros(N, K, dtype=torch.float32, device=DEV)
+    for step in range(2):
+        X = synthetic.with_outlier_channels((M, K), 1.0, 3, 40.0, seed=30 + step)
+        dY = synthetic.normal((M, N), 1e-3, seed=40 + step)
+        db = torch.zeros(N, dtype=torch.float32, device=DEV) if with_bias else None
+        Y = layer.forward(X.to(DEV), W.to(DEV), bias=b.to(DEV) if with_bias else None)
+        dX, _ = layer.backward(dY.to(DEV), dW=dW, dbias=db)
+        Yo, Yabs = oracle.linear_fwd(bits(X), bits(W), orec, ost,
+                                     bias=bits(b) if with_bias else None)
+        (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(bits(dY), orec, ost)
+        for got, want in ((layer.x_q, ost.x_q), (layer.w_q, ost.w_q), (layer.x_qt, ost.x_qt),
+                          (layer.w_qt, ost.w_qt)):
+            assert np.array_equal(u8(got), want), step
+        assert np.array_equal(f32bits(layer.amax.cpu().numpy()), f32bits(ost.last_amax)), step
+        _check_state(layer, ost)
+        assert_gemm_bound(Y, Yo, Yabs, what=f"Y step {step}")
+        assert_gemm_bound(dX, dXo, dXabs, what=f"dX step {step}")
+        assert_gemm_bound(dW, dWo, dWabs, what=f"dW step {step}")
+        if with_bias:   # fp32 column sums of 128-row partials, in order
+            want, wabs = oracle.dbias(bits(dY))
+            err = np.abs(db.cpu().numpy().astype(np.float64) - want)
+            assert np.all(err <= (16 + (M + 127) // 128) * 2.0 ** -24 * wabs), step
+
+
 def test_block_forward():
     M, N, K = 300, 512, 768
     rec = F.Recipe(F.SCALING_BLOCK)
