@@ -67,7 +67,7 @@ def _gemm_alg_bytes():
     operands read once, the output written once (FP32 accumulation: read
     and written)."""
     tot = 0.0
-    for _, M, N, K, _, out in step_gemms():
+    for _, M, N, K, _, out, _ in step_gemms():
         tot += M * K + N * K + (2 * M * N if out == "bf16" else 8 * M * N)
     return tot / len(step_gemms())
 
@@ -221,6 +221,7 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD, "tokens": TOKENS,
                    "linears": {n: [k, n_] for n, k, n_ in LINEARS},
                    "recipe": "HYBRID delayed, history 16, margin 0, amax max",
+                   "backward_operands": "forward codes read MN-major (no transposed copies)",
                    "l2": "flushed (256 MiB write) before every timed step",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
         "roofline": {"bound": "tensor", "kernel": "gemm_pair_kernel (tcgen05.mma.cta_group::2 kind::f8f6f4)",
@@ -270,6 +271,7 @@ def component_pass(F, layers, Xs, dYs, Ws, Ys, dXs, dWs, flush, args, stream):
             M = TOKENS
             X, W, dY = Xs[li][s % 2], Ws[li], dYs[li][s % 2]
             am = L.amax
+            tr = L.x_qt is not None   # transposed copies kept: K-major backward operands
             timed("quantize", lambda: F.fp8_quantize(X, F.E4M3, scale=L.scale[0:1], q=L.x_q,
                                                      q_t=L.x_qt, amax_out=am[0:1]))
             timed("quantize", lambda: F.fp8_quantize(W, F.E4M3, scale=L.scale[1:2], q=L.w_q,
@@ -281,21 +283,25 @@ def component_pass(F, layers, Xs, dYs, Ws, Ys, dXs, dWs, flush, args, stream):
                 L.scale[r:r + 1], L.scale_inv[r:r + 1]) for r in (0, 1)])
             dyq = L.workspace[:M * N].view(M, N)
             off = (M * N + 255) // 256 * 256          # dY_q^T follows dY_q, 256-byte aligned
-            dyqt = L.workspace[off:off + M * N].view(N, M)
+            dyqt = L.workspace[off:off + M * N].view(N, M) if tr else None
             timed("quantize", lambda: F.fp8_quantize(dY, F.E5M2, scale=L.scale[2:3], q=dyq,
                                                      q_t=dyqt, amax_out=am[2:3]))
-            # dgrad and wgrad in one grouped launch, as fp8_linear_bwd issues them
+            # dgrad and wgrad in one grouped launch, as fp8_linear_bwd issues them:
+            # without transposed copies they read W_q, dY_q and X_q as stored
             timed("gemm", lambda: F.fp8_gemm_group(
-                dict(A=dyq, fa=F.E5M2, B=L.w_qt, fb=F.E4M3, scale_inv_a=L.scale_inv[2:3],
-                     scale_inv_b=L.scale_inv[1:2], D=dXs[li]),
-                dict(A=dyqt, fa=F.E5M2, B=L.x_qt, fb=F.E4M3, scale_inv_a=L.scale_inv[2:3],
-                     scale_inv_b=L.scale_inv[0:1], out=F.OUT_F32, D=dWs[li], accumulate=True)))
+                dict(A=dyq, fa=F.E5M2, B=L.w_qt if tr else L.w_q, fb=F.E4M3,
+                     scale_inv_a=L.scale_inv[2:3], scale_inv_b=L.scale_inv[1:2], D=dXs[li],
+                     layout=F.LAYOUT_TN if tr else F.LAYOUT_B_KN),
+                dict(A=dyqt if tr else dyq, fa=F.E5M2, B=L.x_qt if tr else L.x_q, fb=F.E4M3,
+                     scale_inv_a=L.scale_inv[2:3], scale_inv_b=L.scale_inv[0:1], out=F.OUT_F32,
+                     D=dWs[li], accumulate=True,
+                     layout=F.LAYOUT_TN if tr else F.LAYOUT_KM_KN)))
             timed("update_scale", lambda: F.fp8_update_scale(
                 am[2:3], L.history[2], L.pos[2:3], 16, F.AMAX_MAX, F.E5M2, 0, False,
                 L.scale[2:3], L.scale_inv[2:3]))
             gemm_flops += 6.0 * M * N * K
-            # quantiser bytes: bf16 read (2 B) + q and q_t writes (1 B + 1 B) per element
-            quant_bytes += 4.0 * (M * K + N * K + M * N)
+            # quantiser bytes: bf16 read (2 B) + q write (1 B) (+ q_t write (1 B)) per element
+            quant_bytes += (4.0 if tr else 3.0) * (M * K + N * K + M * N)
         t1.record(stream)
         pending.append(("__step", t0, t1))
     torch.cuda.synchronize()
@@ -815,12 +821,15 @@ def run_kernel(args):
 
 
 def step_gemms():
-    """The 15 GEMMs of one layer step: (name, M, N, K, A format, output)."""
+    """The 15 GEMMs of one layer step: (name, M, N, K, A format, output,
+    layout).  The backward GEMMs read the forward's codes as stored (the
+    layer's default): dgrad's B is W_q [N x K], wgrad's A and B are dY_q and
+    X_q, both [tokens x ...]."""
     out = []
     for name, K, N in LINEARS:
-        out.append((name + ".fwd", TOKENS, N, K, "e4m3", "bf16"))
-        out.append((name + ".dgrad", TOKENS, K, N, "e5m2", "bf16"))
-        out.append((name + ".wgrad", N, K, TOKENS, "e5m2", "f32acc"))
+        out.append((name + ".fwd", TOKENS, N, K, "e4m3", "bf16", 0))
+        out.append((name + ".dgrad", TOKENS, K, N, "e5m2", "bf16", 1))
+        out.append((name + ".wgrad", N, K, TOKENS, "e5m2", "f32acc", 3))
     return out
 
 
@@ -833,8 +842,9 @@ def run_gemm_step(F, args, dev, codes, flush):
     stream = torch.cuda.current_stream()
     times = []
     for rep in range(2):
-        for name, M, N, K, fa, out in gemms:
-            A, B = codes(M, K), codes(N, K)
+        for name, M, N, K, fa, out, layout in gemms:
+            A = codes(K, M) if layout & F.LAYOUT_A_KM else codes(M, K)
+            B = codes(K, N) if layout & F.LAYOUT_B_KN else codes(N, K)
             if out == "bf16":
                 D = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
             else:
@@ -844,14 +854,14 @@ def run_gemm_step(F, args, dev, codes, flush):
             a.record(stream)
             F.fp8_gemm(A, F.E5M2 if fa == "e5m2" else F.E4M3, B, F.E4M3, one, one,
                        out=F.OUT_BF16 if out == "bf16" else F.OUT_F32, D=D,
-                       accumulate=out == "f32acc")
+                       accumulate=out == "f32acc", layout=layout)
             b.record(stream)
             torch.cuda.synchronize()
             if rep == 1:
                 times.append(a.elapsed_time(b))
             del A, B, D
     assert F.fp8_device_status() == 0
-    flops = sum(2.0 * M * N * K for _, M, N, K, _, _ in gemms)
+    flops = sum(2.0 * M * N * K for _, M, N, K, _, _, _ in gemms)
     print(json.dumps({"kernel": "gemm_step", "gemms": [g[0] for g in gemms],
                       "ms": [round(t, 4) for t in times], "total_ms": round(sum(times), 4),
                       "achieved": round(flops / (sum(times) * 1e-3) / 1e12, 1),

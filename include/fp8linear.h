@@ -74,8 +74,16 @@ typedef enum {
  * other granularities, the flag changes nothing (it is rejected on
  * FP8_GRAN_TENSOR and FP8_GRAN_ROW). */
 #define FP8_SCALE_POW2 16
+/* Operand layouts of fp8_gemm.  The product is the same, D = A . B^T in the
+ * [M x K] / [N x K] view; a layout only says how an operand is stored.  The
+ * tensor core reads either form ("K-major" or "MN-major" tiles), so the
+ * backward GEMMs can read the forward's codes as they are instead of
+ * transposed copies. */
 typedef enum {
-    FP8_LAYOUT_TN = 0        /* A [M x K] and B [N x K], both K-contiguous   */
+    FP8_LAYOUT_TN = 0,       /* A [M x K] and B [N x K], both K-contiguous   */
+    FP8_LAYOUT_B_KN = 1,     /* A [M x K]; B stored [K x N], N-contiguous    */
+    FP8_LAYOUT_A_KM = 2,     /* A stored [K x M], M-contiguous; B [N x K]    */
+    FP8_LAYOUT_KM_KN = 3     /* A stored [K x M] and B stored [K x N]        */
 } fp8_layout_t;
 typedef enum {
     FP8_SCALING_DELAYED = 0, /* per-tensor, scale from the amax history      */
@@ -114,9 +122,10 @@ typedef struct {
                          /*   dynamic), initialise to 0                        */
     int32_t* pos;        /* [3] next history slot, initialise to 0             */
     uint8_t* x_q;        /* [M][K] written by fwd                              */
-    uint8_t* x_qt;       /* [K][M] written by fwd (per-tensor modes)           */
+    uint8_t* x_qt;       /* [K][M] written by fwd; nullable in per-tensor      */
+                         /*   modes (see fp8_linear_bwd)                       */
     uint8_t* w_q;        /* [N][K] written by fwd                              */
-    uint8_t* w_qt;       /* [K][N] written by fwd (per-tensor modes)           */
+    uint8_t* w_qt;       /* [K][N] written by fwd; nullable in per-tensor modes*/
     float*   x_sinv;     /* [M][K/128] written by fwd (block mode)             */
     float*   w_sinv;     /* [N/128][K/128] written by fwd (block mode)         */
     float*   qscale_inv; /* [2] out: dequantisation factors that x_q/x_qt (0)  */
@@ -221,8 +230,13 @@ int fp8_quantize_sr(const void* x, int64_t rows, int64_t cols, int format, const
                     uint64_t seed, uint64_t offset, uint8_t* q, uint8_t* q_t, float* amax_out,
                     void* stream);
 
-/* Scaled FP8 GEMM, layout FP8_LAYOUT_TN:
+/* Scaled FP8 GEMM:
  *   D[m][n] = sum_k sa(m,k) * sb(n,k) * A[m][k] * B[n][k]
+ * where A[m][k] is the byte at A + m*K + k (FP8_LAYOUT_TN, FP8_LAYOUT_B_KN)
+ * or at A + k*M + m (FP8_LAYOUT_A_KM, FP8_LAYOUT_KM_KN), and B[n][k] the
+ * byte at B + n*K + k or, with FP8_LAYOUT_B_KN / FP8_LAYOUT_KM_KN, at
+ * B + k*N + n.  The layouts other than FP8_LAYOUT_TN take per-tensor and
+ * per-row factors (FP8_ERR_UNSUPPORTED with block factors).
  * with FP32 accumulation on the tensor cores.  sa, sb are DEQUANTISATION
  * factors (scale_inv = 1/scale, device memory):
  *   FP8_GRAN_TENSOR   scale_inv[0]
@@ -242,7 +256,8 @@ int fp8_quantize_sr(const void* x, int64_t rows, int64_t cols, int format, const
  * out FP8_OUT_BF16: D is bf16 [M x N], rounded to nearest even.
  * out FP8_OUT_F32:  D is fp32 [M x N]; accumulate != 0 adds to D.
  * Shape rule: M >= 0; N, K multiples of 16 (multiples of 128 when either
- * operand uses block scales).  A, B, D: 16-byte aligned.
+ * operand uses block scales); M a multiple of 16 when A is stored [K x M].
+ * A, B, D: 16-byte aligned.  An unknown layout is FP8_ERR_INVALID_ARG.
  * fa, fb: FP8_E4M3 / FP8_E5M2 in any combination. */
 int fp8_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
              int64_t K, int layout, int ga, const float* scale_inv_a, int gb,
@@ -289,9 +304,10 @@ size_t fp8_workspace_size(int64_t M, int64_t N, int64_t K, const fp8_recipe_t* r
 
 /* Forward pass Y [M x N] (bf16) = X [M x K] . W [N x K]^T (+ bias [N], bf16,
  * nullable, 16-byte aligned, added in the GEMM epilogue in FP32).
- *   delayed: quantise X and W with the current scales (fusing their amax and
- *            transposes), GEMM, then update the X and W scales (the new
- *            scales take effect on the next call: one-step lag);
+ *   delayed: quantise X and W with the current scales (fusing their amax,
+ *            and their transposes when x_qt / w_qt are set), GEMM, then
+ *            update the X and W scales (the new scales take effect on the
+ *            next call: one-step lag);
  *   dynamic: amax, scale update and quantisation of X and W, then GEMM;
  *   row:     per-token scales for X and per-output-channel scales for W (the
  *            state's x_sinv [M], w_sinv [N]), GEMM with vector factors; with
@@ -313,7 +329,13 @@ int fp8_linear_fwd(const void* X, const void* W, const void* bias, int64_t M, in
  *   dX [M x K] (bf16) = dY . W,   dW [N x K] (fp32) = dY^T . X  (+ dW if
  *   accumulate_dW).  dY is cast to the recipe's bwd_format with the dY
  *   role's scale (delayed: current scale, then update; dynamic: its own
- *   amax).  The quantised dY and its transpose live in the workspace.
+ *   amax).  The quantised dY (and its transpose) live in the workspace.
+ * Per-tensor scaling: with both x_qt and w_qt set the backward GEMMs read
+ *   the transposed copies (K-major operands, dY_q^T included, as in
+ *   "Transformer Engine internals"); with either one NULL they read x_q,
+ *   w_q and dY_q as stored (FP8_LAYOUT_B_KN for dgrad, FP8_LAYOUT_KM_KN for
+ *   wgrad) and no transposed copy is made.  Both give the same codes and
+ *   the same GEMM results.
  * Block scaling ("DeepSeek FP8 training recipe" > "Block-wise scaling at
  *   128 granularity"): dY is cast once into 1x128 blocks along N (dgrad
  *   operand) and 1x128 blocks along the tokens of dY^T (wgrad operand);

@@ -21,7 +21,7 @@ import torch
 
 __all__ = [
     "E4M3", "E5M2", "OUT_BF16", "OUT_F32", "AMAX_MAX", "AMAX_MOST_RECENT",
-    "GRAN_TENSOR", "GRAN_1x128", "GRAN_128x128", "GRAN_ROW", "SCALE_POW2", "LAYOUT_TN",
+    "GRAN_TENSOR", "GRAN_1x128", "GRAN_128x128", "GRAN_ROW", "SCALE_POW2", "LAYOUT_TN", "LAYOUT_B_KN", "LAYOUT_A_KM", "LAYOUT_KM_KN",
     "SCALING_DELAYED", "SCALING_DYNAMIC", "SCALING_BLOCK", "SCALING_ROW",
     "Fp8Error", "Recipe", "LinearStateC", "Fp8Linear", "build", "lib", "library_path",
     "fp8_amax", "fp8_update_scale", "fp8_quantize", "fp8_quantize_blocks",
@@ -36,6 +36,9 @@ AMAX_MAX, AMAX_MOST_RECENT = 0, 1
 GRAN_TENSOR, GRAN_1x128, GRAN_128x128, GRAN_ROW = 0, 1, 2, 3
 SCALE_POW2 = 16   # OR'd into a block granularity: every factor is a power of two
 LAYOUT_TN = 0
+LAYOUT_B_KN = 1       # B stored [K, N]
+LAYOUT_A_KM = 2       # A stored [K, M]
+LAYOUT_KM_KN = 3      # both
 SCALING_DELAYED, SCALING_DYNAMIC, SCALING_BLOCK, SCALING_ROW = 0, 1, 2, 3
 
 _STATUS = {0: "FP8_OK", -1: "FP8_ERR_INVALID_ARG", -2: "FP8_ERR_SHAPE", -3: "FP8_ERR_ALIGN",
@@ -290,16 +293,25 @@ def fp8_quantize_blocks(x: torch.Tensor, fmt: int, granularity: int, pow2: bool 
     return q, s, q_t, st
 
 
+def _gemm_dims(A, B, layout):
+    """(M, K, N) of A . B^T from the stored shapes: A [M,K] or, with
+    LAYOUT_A_KM, [K,M]; B [N,K] or, with LAYOUT_B_KN, [K,N]."""
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A and B must be 2-D")
+    M, K = (A.shape[1], A.shape[0]) if int(layout) & LAYOUT_A_KM else A.shape
+    N, Kb = (B.shape[1], B.shape[0]) if int(layout) & LAYOUT_B_KN else B.shape
+    if Kb != K:
+        raise ValueError("A and B disagree on K")
+    return M, K, N
+
+
 def fp8_gemm(A: torch.Tensor, fa: int, B: torch.Tensor, fb: int, scale_inv_a, scale_inv_b,
              ga: int = GRAN_TENSOR, gb: int = GRAN_TENSOR, out: int = OUT_BF16, D=None,
              accumulate: bool = False, layout: int = LAYOUT_TN, stream=None,
              bias=None) -> torch.Tensor:
     """D = (A . B^T) with dequantisation factors (+ bias [N], bf16); A [M,K],
-    B [N,K] FP8 codes."""
-    M, K = A.shape
-    N = B.shape[0]
-    if B.shape[1] != K:
-        raise ValueError("A and B disagree on K")
+    B [N,K] FP8 codes, or stored [K,M] / [K,N] per `layout`."""
+    M, K, N = _gemm_dims(A, B, layout)
     if D is None:
         D = torch.empty(M, N, dtype=torch.bfloat16 if out == OUT_BF16 else torch.float32,
                         device=A.device)
@@ -314,10 +326,7 @@ def fp8_gemm(A: torch.Tensor, fa: int, B: torch.Tensor, fb: int, scale_inv_a, sc
 
 def _gemm_args(A, fa, B, fb, scale_inv_a, scale_inv_b, ga=GRAN_TENSOR, gb=GRAN_TENSOR,
                out=OUT_BF16, D=None, accumulate=False, layout=LAYOUT_TN, bias=None):
-    M, K = A.shape
-    N = B.shape[0]
-    if B.shape[1] != K:
-        raise ValueError("A and B disagree on K")
+    M, K, N = _gemm_dims(A, B, layout)
     if D is None:
         D = torch.empty(M, N, dtype=torch.bfloat16 if out == OUT_BF16 else torch.float32,
                         device=A.device)
@@ -377,10 +386,14 @@ class Fp8Linear:
     operands, workspace), allocated with torch on `device`, plus fwd/bwd
     calls into the library.  `state_dict()` / `load_state_dict()` copy the
     scaling state for checkpoints.  With recipe.sr_grad the gradient cast
-    rounds stochastically from the key (sr_seed, call counter)."""
+    rounds stochastically from the key (sr_seed, call counter).
+    transposes (per-tensor recipes): keep transposed copies of the forward's
+    codes for K-major backward GEMMs; by default (False) the backward reads
+    the codes as stored (MN-major) and no copy is made.  The block-wise and
+    per-row recipes always keep them (their transposed codes differ)."""
 
     def __init__(self, M: int, N: int, K: int, recipe: Recipe | None = None, device="cuda",
-                 sr_seed: int = 0):
+                 sr_seed: int = 0, transposes: bool = False):
         self.M, self.N, self.K = M, N, K
         self.recipe = recipe or Recipe()
         dev = torch.device(device)
@@ -399,7 +412,7 @@ class Fp8Linear:
         rowwise = self.recipe.scaling == SCALING_ROW
         # block mode keeps the backward operands only when the token count
         # allows 1x128 blocks along it
-        keep = not block or M % 128 == 0
+        keep = (M % 128 == 0) if block else (rowwise or bool(transposes))
         self.x_qt = torch.empty(K, M, **u8) if keep else None
         self.w_qt = torch.empty(K, N, **u8) if keep else None
         self.x_sinv = self.w_sinv = self.x_sinv_t = self.w_sinv_t = None

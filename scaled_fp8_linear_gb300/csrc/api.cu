@@ -98,7 +98,8 @@ int check_gemm_args(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t 
         return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: NULL pointer");
     if (!valid_format(fa) || !valid_format(fb))
         return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: unknown FP8 format");
-    if (layout != FP8_LAYOUT_TN) return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: unknown layout %d", layout);
+    if (layout < FP8_LAYOUT_TN || layout > FP8_LAYOUT_KM_KN)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: unknown layout %d", layout);
     if (!valid_gemm_gran(ga) || !valid_gemm_gran(gb))
         return set_error(FP8_ERR_INVALID_ARG, "fp8_gemm: unknown scale granularity");
     ga &= ~FP8_SCALE_POW2;
@@ -113,6 +114,10 @@ int check_gemm_args(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t 
     const bool block = block_gran(ga) || block_gran(gb);
     if (block && (ga == FP8_GRAN_ROW || gb == FP8_GRAN_ROW))
         return set_error(FP8_ERR_UNSUPPORTED, "fp8_gemm: per-row and block scales cannot be mixed");
+    if (block && layout != FP8_LAYOUT_TN)
+        return set_error(FP8_ERR_UNSUPPORTED, "fp8_gemm: block scales need layout FP8_LAYOUT_TN");
+    if ((layout & FP8_LAYOUT_A_KM) && M % 16)
+        return set_error(FP8_ERR_SHAPE, "fp8_gemm: A stored [K x M] needs M multiple of 16");
     if (block) {
         if (K % 128 || N % 128)
             return set_error(FP8_ERR_SHAPE, "fp8_gemm: block scales need N and K multiples of 128");
@@ -220,7 +225,7 @@ int check_bwd_buffers(const void* dY, int64_t M, int64_t N, const fp8_recipe_t* 
         return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: workspace of %zu bytes, %zu needed",
                          workspace_bytes, need);
     if (!aligned16(dY) || !aligned16(dX) || !aligned16(dW) || !aligned16(workspace) ||
-        !aligned16(s->x_qt) || !aligned16(s->w_qt) ||
+        !aligned16(s->x_q) || !aligned16(s->w_q) || !aligned16(s->x_qt) || !aligned16(s->w_qt) ||
         (reinterpret_cast<uintptr_t>(dbias) & 3u))
         return set_error(FP8_ERR_ALIGN, "fp8_linear_bwd: tensors must be 16-byte aligned (dbias 4-byte)");
     return FP8_OK;
@@ -387,7 +392,7 @@ int fp8_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int6
     if (bias && !aligned16(bias))
         return set_error(FP8_ERR_ALIGN, "fp8_gemm: bias must be 16-byte aligned");
     return launch_gemm(A, fa, B, fb, M, N, K, ga, scale_inv_a, gb, scale_inv_b, bias, D, out,
-                       accumulate != 0, as_stream(stream));
+                       accumulate != 0, as_stream(stream), layout);
 }
 
 int fp8_gemm_group(const fp8_gemm_args_t* g1, const fp8_gemm_args_t* g2, void* stream) {
@@ -401,7 +406,8 @@ int fp8_gemm_group(const fp8_gemm_args_t* g1, const fp8_gemm_args_t* g2, void* s
     }
     auto args = [](const fp8_gemm_args_t* g) {
         return GemmArgs{g->A, g->fa, g->B, g->fb, g->M, g->N, g->K, g->ga, g->scale_inv_a,
-                        g->gb, g->scale_inv_b, g->bias, g->D, g->out, g->accumulate != 0};
+                        g->gb, g->scale_inv_b, g->bias, g->D, g->out, g->accumulate != 0,
+                        g->layout};
     };
     return launch_gemm_group(args(g1), args(g2), as_stream(stream));
 }
@@ -504,8 +510,8 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
         return linear_bwd_row(dY, M, N, K, recipe, s, dX, dW, accumulate_dW, dbias, workspace,
                               workspace_bytes, as_stream(stream));
     FP8_CHECK(check_state_scales(s));
-    if (!s->x_qt || !s->w_qt)
-        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: the forward pass must keep x_qt and w_qt");
+    if (!s->x_q || !s->w_q)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: state->x_q / w_q must be set");
     FP8_CHECK(check_bwd_buffers(dY, M, N, recipe, s, dX, dW, dbias, workspace, workspace_bytes));
     if (recipe->sr_grad && (!s->sr_key || (reinterpret_cast<uintptr_t>(s->sr_key) & 7u)))
         return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: sr_grad needs an 8-byte aligned state->sr_key");
@@ -519,8 +525,14 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
     float* fused_partial = recipe->sr_grad ? nullptr : partial;
     const int fb = recipe->bwd_format, ff = recipe->fwd_format;
     const int H = history_len_of(recipe);
+    // With the forward's transposed copies (x_qt and w_qt both kept) the
+    // backward GEMMs read K-major operands, dY_q^T included.  Without them
+    // they read the codes as stored, MN-major: W_q [N x K] as dgrad's B,
+    // dY_q [M x N] and X_q [M x K] as wgrad's A and B.
+    const bool kmajor = s->x_qt && s->w_qt;
     uint8_t* dy_q = static_cast<uint8_t*>(workspace);
-    uint8_t* dy_qt = dy_q + align256(static_cast<size_t>(M) * static_cast<size_t>(N));
+    uint8_t* dy_qt =
+        kmajor ? dy_q + align256(static_cast<size_t>(M) * static_cast<size_t>(N)) : nullptr;
     float* h2 = s->history + 2 * static_cast<int64_t>(H);
 
     if (recipe->scaling == FP8_SCALING_DYNAMIC) {
@@ -543,10 +555,12 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
     // dgrad: dX [M x K] = dY_q [M x N] . (W_q^T [K x N])^T, and
     // wgrad: dW [N x K] (+)= dY_q^T [N x M] . (X_q^T [K x M])^T, in one launch
     FP8_CHECK(launch_gemm_group(
-        GemmArgs{dy_q, fb, s->w_qt, ff, M, K, N, FP8_GRAN_TENSOR, s->scale_inv + 2,
-                 FP8_GRAN_TENSOR, s->qscale_inv + 1, nullptr, dX, FP8_OUT_BF16, 0},
-        GemmArgs{dy_qt, fb, s->x_qt, ff, N, K, M, FP8_GRAN_TENSOR, s->scale_inv + 2,
-                 FP8_GRAN_TENSOR, s->qscale_inv + 0, nullptr, dW, FP8_OUT_F32, accumulate_dW != 0},
+        GemmArgs{dy_q, fb, kmajor ? s->w_qt : s->w_q, ff, M, K, N, FP8_GRAN_TENSOR,
+                 s->scale_inv + 2, FP8_GRAN_TENSOR, s->qscale_inv + 1, nullptr, dX, FP8_OUT_BF16,
+                 0, kmajor ? FP8_LAYOUT_TN : FP8_LAYOUT_B_KN},
+        GemmArgs{kmajor ? dy_qt : dy_q, fb, kmajor ? s->x_qt : s->x_q, ff, N, K, M,
+                 FP8_GRAN_TENSOR, s->scale_inv + 2, FP8_GRAN_TENSOR, s->qscale_inv + 0, nullptr,
+                 dW, FP8_OUT_F32, accumulate_dW != 0, kmajor ? FP8_LAYOUT_TN : FP8_LAYOUT_KM_KN},
         st));
     if (recipe->scaling == FP8_SCALING_DELAYED)
         return cuda_status(launch_update_scale(s->amax + 2, h2, s->pos + 2, H, recipe->amax_algo, fb,

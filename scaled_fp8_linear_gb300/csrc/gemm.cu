@@ -67,6 +67,7 @@ struct GemmParams {
     void* D;
     int out;          // FP8_OUT_BF16 / FP8_OUT_F32
     int accumulate;
+    int a_mn, b_mn;   // operand stored MN-major ([K x M] / [K x N]); CTA-pair kernel only
 };
 
 // Eight bias values of columns n .. n+7 (n % 8 == 0) as fp32; every lane of
@@ -526,8 +527,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                     uint8_t* sa = ring + stage * STAGE_BYTES;
                     const uint32_t bar = ptx::cluster_addr(&full[stage], 0);
                     if (leader) ptx::mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
-                    ptx::tma_load_2d_pair(sa, ma, bar, kb * BK, ya);
-                    ptx::tma_load_2d_pair(sa + A_BYTES, mb, bar, kb * BK, yb);
+                    // K-major: box (128 K bytes, 128 rows); MN-major: box
+                    // (128 M/N elements, 128 k) -- 16 KB either way
+                    if (q.a_mn) ptx::tma_load_2d_pair(sa, ma, bar, ya, kb * BK);
+                    else ptx::tma_load_2d_pair(sa, ma, bar, kb * BK, ya);
+                    if (q.b_mn) ptx::tma_load_2d_pair(sa + A_BYTES, mb, bar, yb, kb * BK);
+                    else ptx::tma_load_2d_pair(sa + A_BYTES, mb, bar, kb * BK, yb);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -550,14 +555,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
-            const uint32_t idesc1 = ptx::idesc_f8f6f4(p.fa, p.fb, TILE, TILE);
-            const uint32_t idesc2 = ptx::idesc_f8f6f4(p2.fa, p2.fb, TILE, TILE);
+            const uint32_t idesc1 = ptx::idesc_f8f6f4(p.fa, p.fb, TILE, TILE, p.a_mn, p.b_mn);
+            const uint32_t idesc2 = ptx::idesc_f8f6f4(p2.fa, p2.fb, TILE, TILE, p2.a_mn, p2.b_mn);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (int u = pair; ok && u < num_units; u += npairs) {
                 const bool second = GROUPED && u >= t1;
                 const int num_kb = second ? p2.num_kb : p.num_kb;
                 const uint32_t idesc = second ? idesc2 : idesc1;
+                const bool a_mn = (second ? p2.a_mn : p.a_mn) != 0;
+                const bool b_mn = (second ? p2.b_mn : p.b_mn) != 0;
+                // descriptor advance per MMA of K = 32, in 16-byte units: 32
+                // bytes along a K-major row, or 32 rows of 128 bytes MN-major
+                const uint32_t a_step = a_mn ? (UMMA_K * 128) >> 4 : UMMA_K >> 4;
+                const uint32_t b_step = b_mn ? (UMMA_K * 128) >> 4 : UMMA_K >> 4;
                 if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) break;
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + acc * TILE;
@@ -565,12 +576,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                     if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
                     ptx::tc_fence_after();
                     uint8_t* sa = ring + stage * STAGE_BYTES;
-                    const uint64_t ad = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa));
-                    const uint64_t bd = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa + A_BYTES));
+                    const uint32_t a_addr = ptx::smem_u32(sa), b_addr = ptx::smem_u32(sa + A_BYTES);
+                    const uint64_t ad = a_mn ? ptx::sdesc_mnmajor_sw128(a_addr)
+                                             : ptx::sdesc_kmajor_sw128(a_addr);
+                    const uint64_t bd = b_mn ? ptx::sdesc_mnmajor_sw128(b_addr)
+                                             : ptx::sdesc_kmajor_sw128(b_addr);
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k)
-                        ptx::mma_f8f6f4_pair(d, ad + (k * UMMA_K >> 4), bd + (k * UMMA_K >> 4),
-                                             idesc, (kb | k) != 0);
+                        ptx::mma_f8f6f4_pair(d, ad + k * a_step, bd + k * b_step, idesc,
+                                             (kb | k) != 0);
                     ptx::mma_commit_pair(&empty[stage], 0x3);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -1333,6 +1347,27 @@ int make_kmajor_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K,
     return FP8_OK;
 }
 
+// Tensor map of an MN-contiguous FP8 matrix stored [K x MN] (the transpose of
+// a K-major operand): boxes of 128 elements of MN by BK rows of K, 128-byte
+// swizzle, zero fill outside the matrix.
+int make_mnmajor_map(CUtensorMap* map, const void* ptr, int64_t MN, int64_t K) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return set_error(FP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(MN), static_cast<cuuint64_t>(K)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(MN)};
+    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(BK)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(FP8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%lld x %lld]",
+                         static_cast<int>(r), static_cast<long long>(K),
+                         static_cast<long long>(MN));
+    return FP8_OK;
+}
+
 // Tensor map of the output D [M x N] (bf16 or FP32, row-major) for TMA stores
 // of boxes of 32 rows x 64 bytes (32 bf16 or 16 FP32 columns) with the
 // 64-byte swizzle.
@@ -1473,8 +1508,9 @@ int launch_gemm_mx(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M
 
 int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
                 int64_t K, int ga, const float* sa, int gb, const float* sb, const void* bias,
-                void* D, int out, int accumulate, cudaStream_t stream) {
+                void* D, int out, int accumulate, cudaStream_t stream, int layout) {
     if (M == 0 || N == 0) return FP8_OK;
+    const bool a_mn = (layout & FP8_LAYOUT_A_KM) != 0, b_mn = (layout & FP8_LAYOUT_B_KN) != 0;
     // power-of-two block factors on both operands: the block-scaled MMA
     const bool pow2 = (ga & FP8_SCALE_POW2) && (gb & FP8_SCALE_POW2);
     ga &= ~FP8_SCALE_POW2;
@@ -1501,8 +1537,10 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
                     (gb == FP8_GRAN_1x128 || gb == FP8_GRAN_128x128);
     if (mx) return launch_gemm_mx(A, fa, B, fb, M, N, K, ga, sa, gb, sb, bias, D, out, accumulate,
                                   stream);
-    // per-tensor and per-row scales: CTA pairs for every problem of at least 256 rows
-    const bool pair = !block && M >= kPairMinRows;
+    // per-tensor and per-row scales: CTA pairs for every problem of at least
+    // 256 rows, and for every MN-major operand (the single-CTA kernel reads
+    // K-major tiles only; rows past M are zero-filled and not stored)
+    const bool pair = !block && (M >= kPairMinRows || a_mn || b_mn);
     const int BN = block ? 128 : kTensorBN;
     const int TM = pair ? 256 : BM;   // rows of C per tile
     GemmParams p;
@@ -1513,11 +1551,12 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
     p.fa = fa; p.fb = fb; p.ga = ga; p.gb = gb; p.sa = sa; p.sb = sb;
     p.bias = static_cast<const __nv_bfloat16*>(bias);
     p.D = D; p.out = out; p.accumulate = accumulate;
+    p.a_mn = a_mn; p.b_mn = b_mn;
 
     CUtensorMap tmA, tmB;
-    int st = make_kmajor_map(&tmA, A, M, K, BM);
+    int st = a_mn ? make_mnmajor_map(&tmA, A, M, K) : make_kmajor_map(&tmA, A, M, K, BM);
     if (st != FP8_OK) return st;
-    st = make_kmajor_map(&tmB, B, N, K, pair ? 128 : BN);
+    st = b_mn ? make_mnmajor_map(&tmB, B, N, K) : make_kmajor_map(&tmB, B, N, K, pair ? 128 : BN);
     if (st != FP8_OK) return st;
 
     const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
@@ -1557,12 +1596,13 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
 namespace {
 
 // A problem the CTA-pair kernel takes: per-tensor or per-row scales, at least
-// 256 rows, a nonempty K.
+// 256 rows or an MN-major operand, a nonempty K.
 bool pair_eligible(const GemmArgs& g) {
     const int ga = g.ga & ~FP8_SCALE_POW2, gb = g.gb & ~FP8_SCALE_POW2;
     const bool block = ga == FP8_GRAN_1x128 || ga == FP8_GRAN_128x128 ||
                        gb == FP8_GRAN_1x128 || gb == FP8_GRAN_128x128;
-    return !block && g.M >= kPairMinRows && g.N > 0 && g.K > 0 && !g.bias;
+    return !block && (g.M >= kPairMinRows || g.layout != FP8_LAYOUT_TN) && g.N > 0 && g.K > 0 &&
+           !g.bias;
 }
 
 int pair_params(const GemmArgs& g, GemmParams& p, CUtensorMap& tmA, CUtensorMap& tmB,
@@ -1575,9 +1615,12 @@ int pair_params(const GemmArgs& g, GemmParams& p, CUtensorMap& tmA, CUtensorMap&
     p.fa = g.fa; p.fb = g.fb; p.ga = g.ga; p.gb = g.gb; p.sa = g.sa; p.sb = g.sb;
     p.bias = static_cast<const __nv_bfloat16*>(g.bias);
     p.D = g.D; p.out = g.out; p.accumulate = g.accumulate;
-    int st = make_kmajor_map(&tmA, g.A, g.M, g.K, BM);
+    p.a_mn = (g.layout & FP8_LAYOUT_A_KM) != 0;
+    p.b_mn = (g.layout & FP8_LAYOUT_B_KN) != 0;
+    int st = p.a_mn ? make_mnmajor_map(&tmA, g.A, g.M, g.K) : make_kmajor_map(&tmA, g.A, g.M, g.K, BM);
     if (st != FP8_OK) return st;
-    if ((st = make_kmajor_map(&tmB, g.B, g.N, g.K, 128)) != FP8_OK) return st;
+    st = p.b_mn ? make_mnmajor_map(&tmB, g.B, g.N, g.K) : make_kmajor_map(&tmB, g.B, g.N, g.K, 128);
+    if (st != FP8_OK) return st;
     return make_store_map(&tmD, g.D, g.M, g.N, g.out);
 }
 
@@ -1586,10 +1629,10 @@ int pair_params(const GemmArgs& g, GemmParams& p, CUtensorMap& tmA, CUtensorMap&
 int launch_gemm_group(const GemmArgs& g1, const GemmArgs& g2, cudaStream_t stream) {
     if (!pair_eligible(g1) || !pair_eligible(g2)) {
         int st = launch_gemm(g1.A, g1.fa, g1.B, g1.fb, g1.M, g1.N, g1.K, g1.ga, g1.sa, g1.gb,
-                             g1.sb, g1.bias, g1.D, g1.out, g1.accumulate, stream);
+                             g1.sb, g1.bias, g1.D, g1.out, g1.accumulate, stream, g1.layout);
         if (st != FP8_OK) return st;
         return launch_gemm(g2.A, g2.fa, g2.B, g2.fb, g2.M, g2.N, g2.K, g2.ga, g2.sa, g2.gb,
-                           g2.sb, g2.bias, g2.D, g2.out, g2.accumulate, stream);
+                           g2.sb, g2.bias, g2.D, g2.out, g2.accumulate, stream, g2.layout);
     }
     GemmParams p1, p2;
     CUtensorMap a1, b1, d1, a2, b2, d2;

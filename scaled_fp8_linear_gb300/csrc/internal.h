@@ -97,12 +97,16 @@ cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int 
                                  uint8_t* q, float* scale_inv, uint8_t* q_t, float* scale_inv_t,
                                  cudaStream_t stream);
 
-// Scaled FP8 GEMM, TN layout.  Returns 0 or a negative fp8 status code
-// (tensor-map encoding can fail); launch errors come back as FP8_ERR_CUDA.
-// bias (nullable): bf16 [N] added to every row before the output rounding.
+// Scaled FP8 GEMM.  layout: FP8_LAYOUT_TN (A [M x K], B [N x K]), or with
+// FP8_LAYOUT_A_KM / FP8_LAYOUT_B_KN an operand stored [K x M] / [K x N]
+// (per-tensor and per-row scales only).  Returns 0 or a negative fp8 status
+// code (tensor-map encoding can fail); launch errors come back as
+// FP8_ERR_CUDA.  bias (nullable): bf16 [N] added to every row before the
+// output rounding.
 int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
                 int64_t K, int ga, const float* sa, int gb, const float* sb, const void* bias,
-                void* D, int out, int accumulate, cudaStream_t stream);
+                void* D, int out, int accumulate, cudaStream_t stream,
+                int layout = FP8_LAYOUT_TN);
 
 // Workspace bytes of fp8_linear_bwd's dY operands (without the bias
 // gradient's partial sums) for a valid recipe.
@@ -123,6 +127,7 @@ struct GemmArgs {
     void* D;
     int out;
     int accumulate;
+    int layout = FP8_LAYOUT_TN;
 };
 
 // Two independent GEMMs of one pass (the dgrad and the wgrad of a backward)

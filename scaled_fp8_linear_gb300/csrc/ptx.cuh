@@ -445,19 +445,41 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f8f6f4, dense, FP32 accumulator,
-// both operands K-major.
+// Shared-memory matrix descriptor for an MN-major operand tile written by
+// TMA with 128-byte swizzling: each 128-byte row holds 128 consecutive M (or
+// N) elements of one k, and 8 rows (1024 bytes) form a swizzle atom; the
+// atoms are stacked along K.
+//   bits 16-29  leading-dimension byte offset >> 4: the distance between
+//               128-element blocks along M/N.  A CTA's operand tile here is
+//               one such block, so it is never used; set to the atom size.
+//   bits 32-45  stride-dimension byte offset >> 4: 1024 B between 8-k groups
+// (other fields as for the K-major descriptor).  One MMA of K = 32 reads four
+// atoms, so the next instruction's operand starts 4096 bytes further on.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1024 >> 4) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f8f6f4, dense, FP32 accumulator.
 //   bits  4-5   D format (1 = F32)
 //   bits  7-9   A format (0 = E4M3, 1 = E5M2)
 //   bits 10-12  B format
-//   bit  15/16  A / B major (0 = K)
+//   bit  15/16  A / B major (0 = K-major, 1 = MN-major)
 //   bits 17-22  N >> 3
 //   bits 24-28  M >> 4
-__host__ __device__ __forceinline__ uint32_t idesc_f8f6f4(int a_fmt, int b_fmt, int m, int n) {
+__host__ __device__ __forceinline__ uint32_t idesc_f8f6f4(int a_fmt, int b_fmt, int m, int n,
+                                                          int a_mn = 0, int b_mn = 0) {
     uint32_t d = 0;
     d |= 1u << 4;
     d |= static_cast<uint32_t>(a_fmt & 7) << 7;
     d |= static_cast<uint32_t>(b_fmt & 7) << 10;
+    d |= static_cast<uint32_t>(a_mn ? 1 : 0) << 15;
+    d |= static_cast<uint32_t>(b_mn ? 1 : 0) << 16;
     d |= static_cast<uint32_t>(n >> 3) << 17;
     d |= static_cast<uint32_t>(m >> 4) << 24;
     return d;

@@ -547,10 +547,12 @@ __device__ __forceinline__ void rne_cast_transpose_tile(
             out = cast16<FMT, COUNT, false>(a, b, s, cc, key, 0);
             *reinterpret_cast<uint4*>(q + r * cols + c) = out;
         }
-        *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = out;
+        if (qt) *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = out;
     }
-    __syncthreads();
-    transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
+    if (qt) {   // (null: the bias-gradient sums without a transposed copy)
+        __syncthreads();
+        transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
+    }
     if (AMAX) cta_amax_commit(m, amax_bits);
     if (COUNT) cta_counts_commit(cc, counts);
 }
@@ -1135,7 +1137,7 @@ static void launch_cast(const void* x, int64_t rows, int64_t cols, const float* 
                         cudaStream_t stream, float* dbias_partial,
                         const unsigned long long* key_dev) {
     if constexpr (!SR) {
-        if (dbias_partial) {   // the bias-gradient sums ride on the transposing cast
+        if (dbias_partial) {   // the bias-gradient sums ride on the tiled cast (q_t nullable)
             launch_transpose<FMT, AMAX, false, false, true>(x, rows, cols, scale, q, q_t, amax,
                                                             nullptr, key, stream, dbias_partial);
             return;

@@ -50,7 +50,9 @@ def test_gemm_argument_checks():
 
     assert call(A=None) == -1
     assert call(fa=7) == -1
-    assert call(layout=3) == -1
+    assert call(layout=4) == -1 and call(layout=-1) == -1
+    assert call(layout=F.LAYOUT_A_KM, M=200) == -2             # A stored [K x M]: M % 16 == 0
+    assert call(layout=F.LAYOUT_B_KN, ga=F.GRAN_1x128, gb=F.GRAN_128x128) == -6   # block: TN only
     assert call(out=5) == -1
     assert call(acc=1) == -1                      # accumulate needs fp32 output
     assert call(N=120) == -2 and call(K=40) == -2  # not multiples of 16

@@ -101,6 +101,73 @@ def test_degenerate_shapes():
     assert (D == 7).all()
 
 
+MN_LAYOUTS = [F.LAYOUT_B_KN, F.LAYOUT_A_KM, F.LAYOUT_KM_KN]
+
+
+def _stored(A, B, layout):
+    """A [M x K] and B [N x K] as fp8_gemm reads them under `layout`."""
+    return (_t(A.T if layout & F.LAYOUT_A_KM else A), _t(B.T if layout & F.LAYOUT_B_KN else B))
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (304, 272, 400), (48, 80, 1040),
+                                   (640, 768, 1152), (1024, 512, 4096)])
+@pytest.mark.parametrize("layout", MN_LAYOUTS)
+def test_mn_major_layouts(M, N, K, layout):
+    """Operands stored [K x M] / [K x N] (read MN-major by the tensor core):
+    within the oracle bound, and from 256 rows on bit-identical to the same
+    codes in the TN layout (the same CTA-pair kernel, the same K order)."""
+    rng = np.random.default_rng(M + 3 * N + 5 * K + layout)
+    A, sa = _codes(rng, (M, K), F.E5M2)
+    B, sb = _codes(rng, (N, K), F.E4M3, 0.02)
+    a, b = _stored(A, B, layout)
+    D = F.fp8_gemm(a, F.E5M2, b, F.E4M3, _s(sa), _s(sb), layout=layout)
+    Do, Dabs = oracle.gemm(A, F.E5M2, B, F.E4M3, sa, sb)
+    assert_gemm_bound(D, Do, Dabs, what=f"layout {layout} {M}x{N}x{K}")
+    if M >= 256:
+        ref = F.fp8_gemm(_t(A), F.E5M2, _t(B), F.E4M3, _s(sa), _s(sb))
+        assert torch.equal(D.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (304, 400, 1040), (32, 16, 272)])
+@pytest.mark.parametrize("layout", MN_LAYOUTS)
+def test_mn_major_exact_integer_products(M, N, K, layout):
+    """Small-integer codes in every layout: every partial sum is an exact
+    integer, so a misplaced element anywhere (a wrong stride, a swizzle or
+    K-step error) changes the FP32 result."""
+    rng = np.random.default_rng(K + layout)
+    ai = rng.integers(-4, 5, size=(M, K)).astype(np.float32)
+    bi = rng.integers(-4, 5, size=(N, K)).astype(np.float32)
+    a, b = _stored(oracle.encode(ai, F.E4M3), oracle.encode(bi, F.E5M2), layout)
+    D = F.fp8_gemm(a, F.E4M3, b, F.E5M2, _s(0.5), _s(4.0), out=F.OUT_F32, layout=layout)
+    want = (ai.astype(np.int64) @ bi.astype(np.int64).T).astype(np.float64) * 2.0
+    assert np.array_equal(D.cpu().numpy().astype(np.float64), want)
+
+
+@pytest.mark.parametrize("layout", MN_LAYOUTS)
+@pytest.mark.parametrize("ga,gb,out,acc", [(F.GRAN_ROW, F.GRAN_ROW, F.OUT_BF16, False),
+                                           (F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_F32, True),
+                                           (F.GRAN_ROW, F.GRAN_TENSOR, F.OUT_F32, False)])
+def test_mn_major_row_scales_and_f32(layout, ga, gb, out, acc):
+    """Per-row factors and the FP32 (accumulating) epilogue with MN-major
+    operands: the factors index output rows and columns, not storage."""
+    M, N, K = 512, 384, 640
+    rng = np.random.default_rng(layout + 10 * ga + 100 * out)
+    A, _ = _codes(rng, (M, K), F.E4M3)
+    B, _ = _codes(rng, (N, K), F.E4M3, 0.02)
+    sa = (rng.random(M if ga == F.GRAN_ROW else 1) + 0.5).astype(np.float32)
+    sb = (rng.random(N if gb == F.GRAN_ROW else 1) + 0.5).astype(np.float32)
+    a, b = _stored(A, B, layout)
+    prev = rng.standard_normal((M, N)).astype(np.float32)
+    D = _t(prev, torch.float32) if out == F.OUT_F32 else None
+    D = F.fp8_gemm(a, F.E4M3, b, F.E4M3, _s(sa), _s(sb), ga=ga, gb=gb, out=out, D=D,
+                   accumulate=acc, layout=layout)
+    Do, Dabs = oracle.gemm(A, F.E4M3, B, F.E4M3, sa, sb, ga, gb)
+    if acc:
+        assert_gemm_bound(D, Do + prev, Dabs, prev=prev)
+    else:
+        assert_gemm_bound(D, Do, Dabs)
+
+
 def _block_operand(rng, shape, fmt, gran, std=1.0):
     v = rng.standard_normal(shape).astype(np.float32) * std
     v *= np.abs(rng.standard_t(3, size=(shape[0], 1))).astype(np.float32)
@@ -276,7 +343,7 @@ def _rand_codes(shape, seed):
 
 
 @pytest.mark.parametrize("case", ["bwd_like", "ragged", "rowscaled", "fallback_block", "small_m",
-                                  "pow2_block_bwd"])
+                                  "pow2_block_bwd", "bwd_mn_major", "small_m_mn_major"])
 def test_gemm_group_equals_two_gemms(case):
     """fp8_gemm_group gives, bit for bit, the results of two fp8_gemm calls:
     the grouped CTA-pair launch computes every tile exactly as the single
@@ -320,6 +387,20 @@ def test_gemm_group_equals_two_gemms(case):
                   scale_inv_a=p2((N, M // 128), 3), scale_inv_b=p2((K, M // 128), 4),
                   ga=F.GRAN_1x128 | F.SCALE_POW2, gb=F.GRAN_1x128 | F.SCALE_POW2,
                   out=F.OUT_F32, accumulate=True)
+    elif case == "bwd_mn_major":   # dgrad and wgrad reading the forward's codes as stored
+        M, N, K = 1024, 768, 640
+        dy, w, x = _rand_codes((M, N), 25), _rand_codes((N, K), 26), _rand_codes((M, K), 27)
+        g1 = dict(A=dy, fa=F.E5M2, B=w, fb=F.E4M3, scale_inv_a=one * 2 ** -7,
+                  scale_inv_b=one * 2 ** -5, layout=F.LAYOUT_B_KN)
+        g2 = dict(A=dy, fa=F.E5M2, B=x, fb=F.E4M3, scale_inv_a=one * 2 ** -7,
+                  scale_inv_b=one * 2 ** -6, out=F.OUT_F32, accumulate=True,
+                  layout=F.LAYOUT_KM_KN)
+    elif case == "small_m_mn_major":   # fewer than 256 rows: still one CTA-pair launch
+        g1 = dict(A=_rand_codes((640, 96), 28), fa=F.E5M2, B=_rand_codes((640, 512), 29),
+                  fb=F.E4M3, scale_inv_a=one, scale_inv_b=one, out=F.OUT_F32,
+                  layout=F.LAYOUT_KM_KN)
+        g2 = dict(A=_rand_codes((128, 640), 30), fa=F.E5M2, B=_rand_codes((640, 256), 31),
+                  fb=F.E4M3, scale_inv_a=one, scale_inv_b=one, layout=F.LAYOUT_B_KN)
     else:                          # M < 256: the 1-CTA kernel, two launches
         g1 = dict(A=_rand_codes((128, 256), 17), fa=F.E4M3, B=_rand_codes((256, 256), 18),
                   fb=F.E4M3, scale_inv_a=one, scale_inv_b=one)
@@ -327,7 +408,8 @@ def test_gemm_group_equals_two_gemms(case):
                   fb=F.E4M3, scale_inv_a=one, scale_inv_b=one)
     prev = None
     if g2.get("out") == F.OUT_F32:
-        prev = torch.randn(g2["A"].shape[0], g2["B"].shape[0], device=DEV)
+        M2, _, N2 = F._gemm_dims(g2["A"], g2["B"], g2.get("layout", F.LAYOUT_TN))
+        prev = torch.randn(M2, N2, device=DEV)
         g2["D"] = prev.clone()
     D1, D2 = F.fp8_gemm_group(g1, g2)
     r1 = F.fp8_gemm(**g1)

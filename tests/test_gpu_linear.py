@@ -43,11 +43,13 @@ def _check_state(layer, ost, roles=(0, 1, 2)):
     F.Recipe(F.SCALING_DELAYED, history_len=4, amax_algo=F.AMAX_MOST_RECENT, margin=1),
     F.Recipe(F.SCALING_DELAYED, history_len=16, pow2=True),
     F.Recipe(F.SCALING_DYNAMIC)], ids=["delayed16", "delayed4_recent_m1", "delayed16_pow2", "dynamic"])
-def test_training_steps(recipe):
+@pytest.mark.parametrize("transposes", [False, True], ids=["mn_major", "transposed_copies"])
+def test_training_steps(recipe, transposes):
     """20 steps (wrapping a 16-long history), fresh seeded X, dY each step,
-    fixed W; wgrad accumulated over pairs of steps (two micro-batches)."""
+    fixed W; wgrad accumulated over pairs of steps (two micro-batches).  The
+    backward reads the forward's codes as stored, or transposed copies."""
     M, N, K = 256, 384, 512
-    layer = F.Fp8Linear(M, N, K, recipe, device=DEV)
+    layer = F.Fp8Linear(M, N, K, recipe, device=DEV, transposes=transposes)
     orec = _orecipe(recipe)
     ost = oracle.LinearState(orec)
     W = synthetic.normal((N, K), 0.02, seed=1000)
@@ -66,8 +68,12 @@ def test_training_steps(recipe):
         (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(bits(dY), orec, ost,
                                                        dW_prev=prev if acc else None)
         assert np.array_equal(u8(layer.x_q), ost.x_q), step
-        assert np.array_equal(u8(layer.w_qt), ost.w_qt), step
-        assert np.array_equal(u8(layer.x_qt), ost.x_qt), step
+        assert np.array_equal(u8(layer.w_q), ost.w_q), step
+        if transposes:
+            assert np.array_equal(u8(layer.w_qt), ost.w_qt), step
+            assert np.array_equal(u8(layer.x_qt), ost.x_qt), step
+        else:
+            assert layer.x_qt is None and layer.w_qt is None
         assert np.array_equal(f32bits(layer.amax.cpu().numpy()), f32bits(ost.last_amax)), step
         assert np.array_equal(f32bits(layer.qscale_inv.cpu().numpy()),
                               f32bits(np.concatenate(ost.sinv_fwd))), step
@@ -78,16 +84,18 @@ def test_training_steps(recipe):
         dW_o = dW.cpu().numpy().astype(np.float64)   # next step accumulates onto the GPU buffer
 
 
-@pytest.mark.parametrize("M,N,K,with_bias", [(656, 272, 400, False), (656, 272, 400, True),
-                                             (272, 656, 400, False)],
-                         ids=["x_larger", "x_larger_dbias", "w_larger"])
-def test_dynamic_cast_order(M, N, K, with_bias):
-    """Dynamic scaling where X or W is the larger operand (the casts then
-    take the smaller one first and the larger one from its last tile), with
-    ragged tiles in every dimension: codes, transposes, amaxes and scales
-    bit-exact, Y / dX / dW (and dbias) within the bound, over 2 steps."""
+@pytest.mark.parametrize("M,N,K,with_bias,transposes", [
+    (656, 272, 400, False, False), (656, 272, 400, True, False), (272, 656, 400, False, False),
+    (656, 272, 400, True, True), (48, 272, 400, True, False), (656, 48, 400, False, False)],
+    ids=["x_larger", "x_larger_dbias", "w_larger", "x_larger_dbias_transposes", "few_tokens_dbias",
+         "few_features"])
+def test_dynamic_ragged(M, N, K, with_bias, transposes):
+    """Dynamic scaling with X or W the larger operand and ragged tiles in
+    every dimension (fewer than 256 tokens or output features included):
+    codes (and transposed copies), amaxes and scales bit-exact, Y / dX / dW
+    (and dbias) within the bound, over 2 steps."""
     rec = F.Recipe(F.SCALING_DYNAMIC)
-    layer = F.Fp8Linear(M, N, K, rec, device=DEV)
+    layer = F.Fp8Linear(M, N, K, rec, device=DEV, transposes=transposes)
     orec = _orecipe(rec)
     ost = oracle.LinearState(orec)
     W = synthetic.normal((N, K), 0.02, seed=21)
@@ -102,8 +110,10 @@ def test_dynamic_cast_order(M, N, K, with_bias):
         Yo, Yabs = oracle.linear_fwd(bits(X), bits(W), orec, ost,
                                      bias=bits(b) if with_bias else None)
         (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(bits(dY), orec, ost)
-        for got, want in ((layer.x_q, ost.x_q), (layer.w_q, ost.w_q), (layer.x_qt, ost.x_qt),
-                          (layer.w_qt, ost.w_qt)):
+        pairs = [(layer.x_q, ost.x_q), (layer.w_q, ost.w_q)]
+        if transposes:
+            pairs += [(layer.x_qt, ost.x_qt), (layer.w_qt, ost.w_qt)]
+        for got, want in pairs:
             assert np.array_equal(u8(got), want), step
         assert np.array_equal(f32bits(layer.amax.cpu().numpy()), f32bits(ost.last_amax)), step
         _check_state(layer, ost)
@@ -229,13 +239,15 @@ def _sample_rows(n, k, seed):
     return np.sort(np.concatenate([[0, n - 1], rng.choice(n, k, replace=False)]))
 
 
-@pytest.mark.parametrize("name,M,N,K,recipe", [
-    ("llama2-7b qkv, delayed", 8192, 12288, 4096, F.Recipe(F.SCALING_DELAYED, history_len=16)),
-    ("llama2-7b down, delayed", 8192, 4096, 11008, F.Recipe(F.SCALING_DELAYED, history_len=16)),
-    ("llama2-70b gate, dynamic", 4096, 28672, 8192, F.Recipe(F.SCALING_DYNAMIC)),
-    ("llama2-70b down, dynamic", 4096, 8192, 28672, F.Recipe(F.SCALING_DYNAMIC))])
-def test_full_size_linear_sampled(name, M, N, K, recipe):
-    layer = F.Fp8Linear(M, N, K, recipe, device=DEV)
+@pytest.mark.parametrize("name,M,N,K,recipe,transposes", [
+    ("llama2-7b qkv, delayed", 8192, 12288, 4096, F.Recipe(F.SCALING_DELAYED, history_len=16), False),
+    ("llama2-7b qkv, delayed, transposed copies", 8192, 12288, 4096,
+     F.Recipe(F.SCALING_DELAYED, history_len=16), True),
+    ("llama2-7b down, delayed", 8192, 4096, 11008, F.Recipe(F.SCALING_DELAYED, history_len=16), False),
+    ("llama2-70b gate, dynamic", 4096, 28672, 8192, F.Recipe(F.SCALING_DYNAMIC), False),
+    ("llama2-70b down, dynamic", 4096, 8192, 28672, F.Recipe(F.SCALING_DYNAMIC), False)])
+def test_full_size_linear_sampled(name, M, N, K, recipe, transposes):
+    layer = F.Fp8Linear(M, N, K, recipe, device=DEV, transposes=transposes)
     X = synthetic.with_outlier_channels((M, K), 1.0, max(1, K // 256), 50.0, seed=1, device=DEV)
     W = synthetic.normal((N, K), 0.02, seed=2, device=DEV)
     dY = synthetic.normal((M, N), 1e-3, seed=3, device=DEV)
@@ -251,7 +263,9 @@ def test_full_size_linear_sampled(name, M, N, K, recipe):
     Yo, Yabs = oracle.linear_fwd(bx, bw, orec, ost, rows=rows_y)
     (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(bdy, orec, ost, rows_dx=rows_y, rows_dw=rows_dw)
     assert np.array_equal(u8(layer.x_q), ost.x_q)
-    assert np.array_equal(u8(layer.w_qt), ost.w_qt)
+    assert np.array_equal(u8(layer.w_q), ost.w_q)
+    if transposes:
+        assert np.array_equal(u8(layer.w_qt), ost.w_qt)
     _check_state(layer, ost)
     ry, rw = torch.as_tensor(rows_y, device=DEV), torch.as_tensor(rows_dw, device=DEV)
     assert_gemm_bound(Y[ry], Yo, Yabs, what=name + " Y")
