@@ -202,11 +202,11 @@ size_t dbias_partial_bytes(int64_t M, int64_t N) {
 // Checks shared by the three backward variants: workspace size (the partial
 // sums only when dbias is wanted) and alignment.
 // The forward's per-tensor casts of X and W (with their amax if `amax`):
-// one launch over both tensors' tiles when both transposes are kept
-// (training), else one cast each.
+// one launch over both tensors when both transposes or neither are kept,
+// else one cast each.
 cudaError_t quantize_x_w(const void* X, const void* W, int64_t M, int64_t N, int64_t K, int f,
                          const fp8_linear_state_t* s, bool amax, cudaStream_t st) {
-    if (s->x_qt && s->w_qt)
+    if ((s->x_qt && s->w_qt) || (!s->x_qt && !s->w_qt))
         return launch_quantize_pair(X, M, K, s->scale + 0, s->x_q, s->x_qt, amax ? s->amax + 0 : nullptr,
                                     W, N, K, s->scale + 1, s->w_q, s->w_qt, amax ? s->amax + 1 : nullptr,
                                     f, st);

@@ -522,6 +522,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 tile_coords<>(second ? u - t1 : u, q.num_m, q.num_n, m_blk, n_blk);
                 const int ya = m_blk * TILE + static_cast<int>(rank) * HALF;
                 const int yb = n_blk * TILE + static_cast<int>(rank) * HALF;
+                const bool a_mn = q.a_mn != 0, b_mn = q.b_mn != 0;
                 for (int kb = 0; kb < q.num_kb; ++kb) {
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
                     uint8_t* sa = ring + stage * STAGE_BYTES;
@@ -529,10 +530,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                     if (leader) ptx::mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
                     // K-major: box (128 K bytes, 128 rows); MN-major: box
                     // (128 M/N elements, 128 k) -- 16 KB either way
-                    if (q.a_mn) ptx::tma_load_2d_pair(sa, ma, bar, ya, kb * BK);
-                    else ptx::tma_load_2d_pair(sa, ma, bar, kb * BK, ya);
-                    if (q.b_mn) ptx::tma_load_2d_pair(sa + A_BYTES, mb, bar, yb, kb * BK);
-                    else ptx::tma_load_2d_pair(sa + A_BYTES, mb, bar, kb * BK, yb);
+                    const int kx = kb * BK;
+                    ptx::tma_load_2d_pair(sa, ma, bar, a_mn ? ya : kx, a_mn ? kx : ya);
+                    ptx::tma_load_2d_pair(sa + A_BYTES, mb, bar, b_mn ? yb : kx, b_mn ? kx : yb);
                     ++issued;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -569,6 +569,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 // bytes along a K-major row, or 32 rows of 128 bytes MN-major
                 const uint32_t a_step = a_mn ? (UMMA_K * 128) >> 4 : UMMA_K >> 4;
                 const uint32_t b_step = b_mn ? (UMMA_K * 128) >> 4 : UMMA_K >> 4;
+                // the descriptors' fixed fields; the start address is or-ed in per stage
+                const uint64_t a_tmpl = a_mn ? ptx::sdesc_mnmajor_sw128(0) : ptx::sdesc_kmajor_sw128(0);
+                const uint64_t b_tmpl = b_mn ? ptx::sdesc_mnmajor_sw128(0) : ptx::sdesc_kmajor_sw128(0);
                 if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) break;
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + acc * TILE;
@@ -576,11 +579,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                     if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
                     ptx::tc_fence_after();
                     uint8_t* sa = ring + stage * STAGE_BYTES;
-                    const uint32_t a_addr = ptx::smem_u32(sa), b_addr = ptx::smem_u32(sa + A_BYTES);
-                    const uint64_t ad = a_mn ? ptx::sdesc_mnmajor_sw128(a_addr)
-                                             : ptx::sdesc_kmajor_sw128(a_addr);
-                    const uint64_t bd = b_mn ? ptx::sdesc_mnmajor_sw128(b_addr)
-                                             : ptx::sdesc_kmajor_sw128(b_addr);
+                    const uint64_t ad = a_tmpl | ((ptx::smem_u32(sa) & 0x3FFFFu) >> 4);
+                    const uint64_t bd = b_tmpl | ((ptx::smem_u32(sa + A_BYTES) & 0x3FFFFu) >> 4);
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k)
                         ptx::mma_f8f6f4_pair(d, ad + k * a_step, bd + k * b_step, idesc,

@@ -58,9 +58,10 @@ cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, in
                                    cudaStream_t stream, unsigned long long* counts = nullptr,
                                    float* dbias_partial = nullptr);
 
-// Per-tensor casts with transposes of two tensors in one launch (x0 and x1
-// each [rows x cols], rows and cols multiples of 16), both to `fmt`; amax0
-// and amax1 both null or both set (zeroed first, one memset when adjacent).
+// Per-tensor casts of two tensors in one launch (x0 and x1 each [rows x
+// cols]), both to `fmt`: with transposes (qt0 and qt1 set; rows and cols
+// multiples of 16), or without (both null: the chunked cast, any size).
+// amax0 and amax1 both null or both set (zeroed first).
 cudaError_t launch_quantize_pair(const void* x0, int64_t rows0, int64_t cols0, const float* scale0,
                                  uint8_t* q0, uint8_t* qt0, float* amax0, const void* x1,
                                  int64_t rows1, int64_t cols1, const float* scale1, uint8_t* q1,

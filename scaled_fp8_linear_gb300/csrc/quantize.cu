@@ -424,6 +424,68 @@ __global__ void __launch_bounds__(kThreads)
     if (COUNT) cta_counts_commit(cc, counts);
 }
 
+// Round-to-nearest cast without a transpose, one chunk per CTA: each thread
+// loads 4 groups of 16 elements (8 x 16 B in flight) before it casts, and a
+// warp's loads and stores of one group cover contiguous 1 KB / 512 B.  The
+// grid is the work (one CTA per 16384 elements), so CTAs come and go as
+// the SMs free up instead of sweeping the tensor in lockstep.  Two tensors
+// may share a launch (the X and W of a forward pass): CTAs [0, ctas0) take
+// job 0, the rest job 1; the first CTA of a job also casts its last n % 16
+// elements.
+struct FlatJob {
+    const uint4* x;
+    int64_t n16;
+    const uint16_t* xt;   // the last tail_n elements
+    int tail_n;
+    const float* scale;
+    uint4* q;
+    uint8_t* qtail;
+    unsigned* amax_bits;
+};
+
+constexpr int kChunkGroups = 4 * kThreads;   // 16-element groups per CTA
+
+template <int FMT, bool AMAX, bool COUNT>
+__global__ void __launch_bounds__(kThreads)
+    quantize_chunk_kernel(FlatJob j0, FlatJob j1, int64_t ctas0, unsigned long long* counts) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
+    const bool second = blockIdx.x >= ctas0;
+    const FlatJob& j = second ? j1 : j0;
+    const int64_t cta = second ? blockIdx.x - ctas0 : blockIdx.x;
+    const float s = *j.scale;
+    const SrSched key{};
+    uint32_t m = 0;
+    CastCounts cc;
+    const int64_t g0 = cta * kChunkGroups + threadIdx.x;
+    uint4 a[4], b[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int64_t g = g0 + u * kThreads;
+        a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (g < j.n16) {
+            a[u] = ldg_stream(j.x + 2 * g);
+            b[u] = ldg_stream(j.x + 2 * g + 1);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int64_t g = g0 + u * kThreads;
+        if (g < j.n16) {
+            if (AMAX) m = absmax_vec(absmax_vec(m, a[u]), b[u]);
+            j.q[g] = cast16<FMT, COUNT, false>(a[u], b[u], s, cc, key, 0);
+        }
+    }
+    if (cta == 0 && threadIdx.x < j.tail_n) {
+        const uint32_t w = j.xt[threadIdx.x];
+        if (AMAX) m = max(m, w & 0x7FFFu);
+        const uint32_t code = COUNT ? cvt2c<FMT>(w & 0xFFFFu, s, cc) : cvt2<FMT>(w, s);
+        j.qtail[threadIdx.x] = static_cast<uint8_t>(code & 0xFFu);
+    }
+    if (AMAX) cta_amax_commit(m, j.amax_bits);
+    if (COUNT) cta_counts_commit(cc, counts);
+}
+
 // Cast with fused transpose.  One CTA per 128 x 128 tile:
 //  phase 1: each thread reads 16 consecutive bf16 of a row (2 x 16 B), writes
 //           16 FP8 codes of q (16 B) and keeps them in shared memory;
@@ -1108,10 +1170,36 @@ cudaError_t launch_update_scale(const float* amax, float* history, int32_t* pos,
     return cudaGetLastError();
 }
 
+FlatJob flat_job(const void* x, int64_t n, const float* scale, uint8_t* q, float* amax) {
+    const int64_t n16 = n / 16;
+    return FlatJob{static_cast<const uint4*>(x), n16, static_cast<const uint16_t*>(x) + n16 * 16,
+                   static_cast<int>(n - n16 * 16), scale, reinterpret_cast<uint4*>(q), q + n16 * 16,
+                   reinterpret_cast<unsigned*>(amax)};
+}
+
+int64_t chunk_ctas(const FlatJob& j) {
+    if (j.n16 == 0 && j.tail_n == 0) return 0;
+    const int64_t c = (j.n16 + kChunkGroups - 1) / kChunkGroups;
+    return c < 1 ? 1 : c;
+}
+
+template <int FMT, bool AMAX, bool COUNT>
+static void launch_chunk(const FlatJob& j0, const FlatJob& j1, unsigned long long* counts,
+                         cudaStream_t stream) {
+    const int64_t c0 = chunk_ctas(j0), c1 = chunk_ctas(j1);
+    if (c0 + c1 == 0) return;
+    launch_pdl(quantize_chunk_kernel<FMT, AMAX, COUNT>, dim3(static_cast<unsigned>(c0 + c1)),
+               dim3(kThreads), 0, stream, j0, j1, c0, counts);
+}
+
 template <int FMT, bool AMAX, bool COUNT, bool SR>
 static void launch_flat(const void* x, int64_t n, const float* scale, uint8_t* q, float* amax,
                         unsigned long long* counts, const SrKey& key, cudaStream_t stream,
                         const unsigned long long* key_dev = nullptr) {
+    if constexpr (!SR) {   // round to nearest: one chunk per CTA
+        launch_chunk<FMT, AMAX, COUNT>(flat_job(x, n, scale, q, amax), FlatJob{}, counts, stream);
+        return;
+    }
     const int64_t n16 = n / 16;
     const int tail_n = static_cast<int>(n - n16 * 16);
     launch_pdl(quantize_flat_kernel<FMT, AMAX, COUNT, SR>, dim3(grid_for(n16 + 1, kThreads * 2)), dim3(kThreads), 0, stream, 
@@ -1200,6 +1288,18 @@ cudaError_t launch_quantize_pair(const void* x0, int64_t rows0, int64_t cols0, c
         return CastJob{static_cast<const uint16_t*>(x), rows, cols, (cols + 127) / 128, scale, q,
                        qt, reinterpret_cast<unsigned*>(amax)};
     };
+    if (!qt0 && !qt1) {   // no transposed copies: one chunked cast over both tensors
+        const FlatJob f0 = flat_job(x0, rows0 * cols0, scale0, q0, amax0);
+        const FlatJob f1 = flat_job(x1, rows1 * cols1, scale1, q1, amax1);
+        if (fmt == 0) {
+            if (A) launch_chunk<0, true, false>(f0, f1, nullptr, stream);
+            else launch_chunk<0, false, false>(f0, f1, nullptr, stream);
+        } else {
+            if (A) launch_chunk<1, true, false>(f0, f1, nullptr, stream);
+            else launch_chunk<1, false, false>(f0, f1, nullptr, stream);
+        }
+        return cudaGetLastError();
+    }
     const CastJob j0 = job(x0, rows0, cols0, scale0, q0, qt0, amax0);
     const CastJob j1 = job(x1, rows1, cols1, scale1, q1, qt1, amax1);
     const int64_t t0 = rows0 * cols0 ? ((rows0 + 127) / 128) * j0.tiles_c : 0;
