@@ -737,17 +737,20 @@ def run_kernel(args):
         return run_llama70b_step(F, args, dev, flush)
     if args.kernel in ("gemm", "block_gemm"):
         M, N, K = dims
-        A, B = codes(M, K), codes(N, K)
+        lay = {"tn": F.LAYOUT_TN, "b_kn": F.LAYOUT_B_KN, "a_km": F.LAYOUT_A_KM,
+               "km_kn": F.LAYOUT_KM_KN}[args.layout] if args.kernel == "gemm" else F.LAYOUT_TN
+        A = codes(K, M) if lay & F.LAYOUT_A_KM else codes(M, K)
+        B = codes(K, N) if lay & F.LAYOUT_B_KN else codes(N, K)
         D = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         if args.kernel == "gemm" and args.f32acc:
             # the wgrad form: FP32 output accumulated into D
             one = torch.ones(1, dtype=torch.float32, device=dev)
             D = torch.zeros(M, N, dtype=torch.float32, device=dev)
             call = lambda: F.fp8_gemm(A, fa, B, F.E4M3, one, one, D=D, out=F.OUT_F32,
-                                      accumulate=True)
+                                      accumulate=True, layout=lay)
         elif args.kernel == "gemm":
             one = torch.ones(1, dtype=torch.float32, device=dev)
-            call = lambda: F.fp8_gemm(A, fa, B, F.E4M3, one, one, D=D)
+            call = lambda: F.fp8_gemm(A, fa, B, F.E4M3, one, one, D=D, layout=lay)
         elif args.pow2:
             # power-of-two block factors: the block-scaled MMA path
             sa = 2.0 ** torch.randint(-3, 4, (M, K // 128), generator=g, device=dev).float()
@@ -811,7 +814,7 @@ def run_kernel(args):
         extra = {"factors": "power of two (block-scaled MMA)" if args.pow2
                  else "fp32 (per-128-K promotion)"}
     if args.kernel == "gemm":
-        extra = {"output": "fp32, accumulated" if args.f32acc else "bf16"}
+        extra = {"output": "fp32, accumulated" if args.f32acc else "bf16", "layout": args.layout}
     print(json.dumps({"kernel": args.kernel, "shape": dims, "format": args.fmt, **extra,
                       "median_ms": round(med, 4), "min_ms": round(ms[0], 4),
                       "achieved": round(ach, 1), "unit": unit, "peak": round(peak, 1),
@@ -1003,6 +1006,8 @@ def main():
                     help="--kernel quantize: scale granularity")
     ap.add_argument("--f32acc", action="store_true",
                     help="gemm: FP32 output accumulated into D (the wgrad form)")
+    ap.add_argument("--layout", choices=["tn", "b_kn", "a_km", "km_kn"], default="tn",
+                    help="gemm: operand storage (b_kn: B as [K x N]; a_km: A as [K x M]; km_kn: both)")
     ap.add_argument("--pow2", action="store_true",
                     help="block_gemm / block_step: power-of-two block factors (the block-scaled MMA path)")
     ap.add_argument("--no-transpose", action="store_true",
