@@ -118,10 +118,11 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity,
 // its first access to global memory (it returns at once when the kernel was
 // not launched that way).  The casts and GEMMs call griddep_launch_dependents()
 // early, which lets the next kernel launch once every CTA of this one has
-// started.  The tiny kernels (scale update, zeroing, finalisers) do not: their
-// dependents launch when they exit.  Otherwise a chain of early launches runs
-// ahead of a long GEMM and parks the next cast's CTAs beside it on its SMs,
-// which measured 5% slower on the Llama-2-7B step.
+// started.  The tiny kernels (scale update, zeroing, finalisers) call it only
+// after their own griddep_wait(), when the kernel before them has completed:
+// triggered at entry, a chain of early launches runs ahead of a long GEMM and
+// parks the next cast's CTAs beside it on its SMs, which measured 5% slower
+// on the Llama-2-7B step.
 
 // Wait until the preceding kernel in the stream has completed and its memory
 // operations are visible.

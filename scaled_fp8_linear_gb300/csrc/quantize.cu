@@ -333,9 +333,11 @@ __global__ void update_scale_kernel(const float* __restrict__ amax, float* __res
                                     int margin, int pow2, float* __restrict__ scale,
                                     float* __restrict__ scale_inv, float* __restrict__ saved,
                                     int save_after, unsigned* status) {
-    // (tiny kernel: the next one may launch when this one exits, not earlier,
-    // so a chain of launches cannot run ahead of the large kernel before it)
+    // (tiny kernel: the next one may launch once the kernel before this one
+    // has completed, not earlier, so a chain of launches cannot run ahead of
+    // a large kernel)
     ptx::griddep_wait();   // the previous kernel's results are visible
+    ptx::griddep_launch_dependents();
     const int r = blockIdx.x, lane = threadIdx.x;
     float* hist = history + static_cast<int64_t>(r) * H;
     const float a = amax[r];
@@ -724,9 +726,11 @@ __global__ void __launch_bounds__(kThreads)
 // (+ the old dbias[n] when accumulating).
 __global__ void dbias_finalize_kernel(const float* __restrict__ partial, int64_t P, int64_t cols,
                                       float* __restrict__ dbias, int accumulate) {
-    // (tiny kernel: the next one may launch when this one exits, not earlier,
-    // so a chain of launches cannot run ahead of the large kernel before it)
+    // (tiny kernel: the next one may launch once the kernel before this one
+    // has completed, not earlier, so a chain of launches cannot run ahead of
+    // a large kernel)
     ptx::griddep_wait();   // the previous kernel's results are visible
+    ptx::griddep_launch_dependents();
     const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (n >= cols) return;
     float v = 0.0f;
@@ -737,9 +741,11 @@ __global__ void dbias_finalize_kernel(const float* __restrict__ partial, int64_t
 // The counter word of a device-held stochastic-rounding key moves on by
 // one after a cast has used it.
 __global__ void sr_advance_kernel(unsigned long long* key_dev) {
-    // (tiny kernel: the next one may launch when this one exits, not earlier,
-    // so a chain of launches cannot run ahead of the large kernel before it)
+    // (tiny kernel: the next one may launch once the kernel before this one
+    // has completed, not earlier, so a chain of launches cannot run ahead of
+    // a large kernel)
     ptx::griddep_wait();   // the previous kernel's results are visible
+    ptx::griddep_launch_dependents();
     key_dev[1] += 1ull;
 }
 
@@ -1106,9 +1112,11 @@ __global__ void __launch_bounds__(kThreads)
 // scale_inv_t[c] = 1 / s(amax_c), in place over the column amaxes.
 template <int FMT>
 __global__ void column_scale_finalize_kernel(float* __restrict__ sinv_t, int64_t cols, int pow2) {
-    // (tiny kernel: the next one may launch when this one exits, not earlier,
-    // so a chain of launches cannot run ahead of the large kernel before it)
+    // (tiny kernel: the next one may launch once the kernel before this one
+    // has completed, not earlier, so a chain of launches cannot run ahead of
+    // a large kernel)
     ptx::griddep_wait();   // the previous kernel's results are visible
+    ptx::griddep_launch_dependents();
     const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (c < cols) {
         const float amax = sinv_t[c];
@@ -1127,9 +1135,11 @@ int grid_for(int64_t work_items, int per_cta) {
 // takes part in programmatic dependent launch like the kernels around it.
 __global__ void zero_words_kernel(float* __restrict__ a, int64_t na, float* __restrict__ b,
                                   int64_t nb) {
-    // (tiny kernel: the next one may launch when this one exits, not earlier,
-    // so a chain of launches cannot run ahead of the large kernel before it)
+    // (tiny kernel: the next one may launch once the kernel before this one
+    // has completed, not earlier, so a chain of launches cannot run ahead of
+    // a large kernel)
     ptx::griddep_wait();   // the previous kernel's results are visible
+    ptx::griddep_launch_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < na + nb;
          i += stride) {
