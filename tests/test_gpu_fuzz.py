@@ -1,6 +1,6 @@
 """Seeded randomized parity sweep over the composed paths: random shapes (ragged
-where the call allows it), formats, scale granularities, recipes, bias and
-stochastic rounding, each checked against the oracle with the same bars as
+where the call allows it), formats, scale granularities, GEMM operand layouts,
+recipes, bias and stochastic rounding, each checked against the oracle with the same bars as
 the targeted tests -- codes and scales bit-exact, GEMM results within
 2e-3 * sum|a b| * s_a * s_b (+ bf16 rounding)."""
 import numpy as np
@@ -76,6 +76,39 @@ def test_random_casts(case):
         assert np.array_equal(f32bits(st.cpu().numpy()), f32bits(sto))
 
 
+@pytest.mark.parametrize("case", range(16))
+def test_random_gemms(case):
+    """Random shapes (ragged against the 256 x 256 tiles), operand layouts,
+    per-tensor / per-row factors and outputs of fp8_gemm."""
+    rng = np.random.default_rng(3000 + case)
+    layout = _pick(rng, [F.LAYOUT_TN, F.LAYOUT_B_KN, F.LAYOUT_A_KM, F.LAYOUT_KM_KN])
+    M, N, K = (16 * int(rng.integers(1, 48)) for _ in range(3))
+    fa, fb = _pick(rng, [F.E4M3, F.E5M2]), _pick(rng, [F.E4M3, F.E5M2])
+    ga, gb = _pick(rng, [F.GRAN_TENSOR, F.GRAN_ROW]), _pick(rng, [F.GRAN_TENSOR, F.GRAN_ROW])
+    out = _pick(rng, [F.OUT_BF16, F.OUT_F32])
+    acc = out == F.OUT_F32 and bool(rng.integers(2))
+    g = torch.Generator().manual_seed(case)
+    A = torch.randint(0, 0x7C, (M, K), generator=g, dtype=torch.int32)
+    B = torch.randint(0, 0x7C, (N, K), generator=g, dtype=torch.int32)
+    A = (A | (torch.randint(0, 2, (M, K), generator=g, dtype=torch.int32) << 7)).to(torch.uint8).numpy()
+    B = (B | (torch.randint(0, 2, (N, K), generator=g, dtype=torch.int32) << 7)).to(torch.uint8).numpy()
+    sa = (rng.random(M if ga == F.GRAN_ROW else 1) * 2 ** -4 + 2 ** -6).astype(np.float32)
+    sb = (rng.random(N if gb == F.GRAN_ROW else 1) * 2 ** -4 + 2 ** -6).astype(np.float32)
+    a = A.T if layout & F.LAYOUT_A_KM else A
+    b = B.T if layout & F.LAYOUT_B_KN else B
+    prev = rng.standard_normal((M, N)).astype(np.float32)
+    D = torch.from_numpy(prev).to(DEV) if out == F.OUT_F32 else None
+    D = F.fp8_gemm(torch.from_numpy(np.ascontiguousarray(a)).to(DEV), fa,
+                   torch.from_numpy(np.ascontiguousarray(b)).to(DEV), fb,
+                   torch.from_numpy(sa).to(DEV), torch.from_numpy(sb).to(DEV), ga=ga, gb=gb,
+                   out=out, D=D, accumulate=acc, layout=layout)
+    Do, Dabs = oracle.gemm(A, fa, B, fb, sa, sb, ga, gb)
+    if acc:
+        assert_gemm_bound(D, Do + prev, Dabs, prev=prev, what=f"case {case}")
+    else:
+        assert_gemm_bound(D, Do, Dabs, what=f"case {case}")
+
+
 def _orecipe(r):
     return oracle.Recipe(scaling=r.scaling, margin=r.margin, history_len=r.history_len,
                          algo=r.amax_algo, pow2=bool(r.pow2), sr_grad=bool(r.sr_grad))
@@ -94,7 +127,8 @@ def test_random_linear_steps(case):
                    sr_grad=sr)
     with_bias = bool(rng.integers(2))
     seed = int(rng.integers(1 << 62))
-    layer = F.Fp8Linear(M, N, K, rec, device=DEV, sr_seed=seed)
+    transposes = bool(rng.integers(2))   # per-tensor recipes: K-major copies or MN-major reads
+    layer = F.Fp8Linear(M, N, K, rec, device=DEV, sr_seed=seed, transposes=transposes)
     orec = _orecipe(rec)
     ost = oracle.LinearState(orec, sr_seed=seed)
     W = synthetic.normal((N, K), 0.02, seed=case)
