@@ -47,6 +47,7 @@ WORKLOAD = ("llama2-7b block linears fwd+dgrad+wgrad, per-tensor delayed scaling
             "(history 16, margin 0, max), tokens 8192")
 METRIC = "FP8 linear fwd+bwd TFLOP/s and quantize GB/s, as fraction of GB300 peak"
 FLUSH_BYTES = 256 << 20
+LAUNCHES_PER_LINEAR = 8   # this library's kernels per linear in one fwd + bwd step
 
 
 def _peaks():
@@ -235,7 +236,10 @@ def run_gpu(args):
                      "frac": round(quant_gbs / hbm_gbs, 4), "peak_source": f"{peak_kind} hbm_gbs"},
         "kernels_ms_per_step": {k: round(v / comp["steps"], 4) for k, v in comp["by_kind"].items()},
         "component_pass_ms_per_step": round(comp["total_ms"] / comp["steps"], 4),
-        "gpu_launches": 6 * len(LINEARS) * args.steps,
+        # per linear and step: forward = amax zeroing, X and W cast (one launch),
+        # GEMM, X/W scale update; backward = amax zeroing, dY cast, grouped
+        # dgrad + wgrad GEMM, dY scale update (the ncu launch list agrees)
+        "gpu_launches": LAUNCHES_PER_LINEAR * len(LINEARS) * args.steps,
         "e2e": e2e,
         "small_case": small,
         "clocks": clk,
