@@ -50,18 +50,22 @@ def _scales(gran, rows, K, seed):
     return (torch.rand(shape, generator=g) + 0.5) * 2.0 ** -6
 
 
-@pytest.mark.parametrize("name,M,N,K,ga,gb,out,acc", [
-    ("tensor", 128, 384, 256, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_BF16, False),
-    ("tensor_ragged", 200, 144, 256, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_BF16, False),
-    ("pair", 512, 384, 256, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_BF16, False),
-    ("pair_f32_acc", 512, 400, 256, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_F32, True),
-    ("row", 512, 384, 256, F.GRAN_ROW, F.GRAN_ROW, F.OUT_BF16, False),
-    ("block", 256, 256, 384, F.GRAN_1x128, F.GRAN_128x128, F.OUT_BF16, False),
-    ("block_colscale_f32", 256, 384, 256, F.GRAN_1x128, F.GRAN_1x128, F.OUT_F32, True),
-    ("k0", 64, 96, 0, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_BF16, False),
-    ("k0_f32_acc", 64, 96, 0, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_F32, True),
+@pytest.mark.parametrize("name,M,N,K,ga,gb,out,acc,layout", [
+    ("tensor", 128, 384, 256, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_BF16, False, F.LAYOUT_TN),
+    ("tensor_ragged", 200, 144, 256, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_BF16, False, F.LAYOUT_TN),
+    ("pair", 512, 384, 256, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_BF16, False, F.LAYOUT_TN),
+    ("pair_f32_acc", 512, 400, 256, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_F32, True, F.LAYOUT_TN),
+    ("row", 512, 384, 256, F.GRAN_ROW, F.GRAN_ROW, F.OUT_BF16, False, F.LAYOUT_TN),
+    ("block", 256, 256, 384, F.GRAN_1x128, F.GRAN_128x128, F.OUT_BF16, False, F.LAYOUT_TN),
+    ("block_colscale_f32", 256, 384, 256, F.GRAN_1x128, F.GRAN_1x128, F.OUT_F32, True, F.LAYOUT_TN),
+    ("k0", 64, 96, 0, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_BF16, False, F.LAYOUT_TN),
+    ("k0_f32_acc", 64, 96, 0, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_F32, True, F.LAYOUT_TN),
+    ("mn_b", 512, 384, 256, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_BF16, False, F.LAYOUT_B_KN),
+    ("mn_both_f32_acc", 400, 272, 320, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_F32, True,
+     F.LAYOUT_KM_KN),
+    ("mn_a_row_small_m", 96, 384, 256, F.GRAN_ROW, F.GRAN_ROW, F.OUT_BF16, False, F.LAYOUT_A_KM),
 ])
-def test_gemm_bias_epilogue(name, M, N, K, ga, gb, out, acc):
+def test_gemm_bias_epilogue(name, M, N, K, ga, gb, out, acc, layout):
     A, B = _codes((M, K), 1), _codes((N, K), 2)
     sa, sb = _scales(ga, M, K, 3), _scales(gb, N, K, 4)
     b = synthetic.normal((N,), 0.5, seed=5)
@@ -70,8 +74,10 @@ def test_gemm_bias_epilogue(name, M, N, K, ga, gb, out, acc):
     if out == F.OUT_F32:
         prev = synthetic.normal((M, N), 1.0, seed=6).float()
         D = prev.to(DEV).clone()
-    got = F.fp8_gemm(A.to(DEV), F.E4M3, B.to(DEV), F.E5M2, sa.to(DEV), sb.to(DEV), ga, gb,
-                     out=out, D=D, accumulate=acc, bias=b.to(DEV))
+    a = A.t().contiguous() if layout & F.LAYOUT_A_KM else A
+    b_ = B.t().contiguous() if layout & F.LAYOUT_B_KN else B
+    got = F.fp8_gemm(a.to(DEV), F.E4M3, b_.to(DEV), F.E5M2, sa.to(DEV), sb.to(DEV), ga, gb,
+                     out=out, D=D, accumulate=acc, bias=b.to(DEV), layout=layout)
     Do, Dabs = oracle.gemm(A.numpy(), F.E4M3, B.numpy(), F.E5M2, sa.numpy(), sb.numpy(), ga, gb,
                            bias=bits(b))
     if prev is not None:
