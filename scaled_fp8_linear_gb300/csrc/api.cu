@@ -475,8 +475,8 @@ int fp8_linear_fwd(const void* X, const void* W, const void* bias, int64_t M, in
     FP8_CHECK(check_state_scales(s));
     const int H = history_len_of(recipe);
     if (recipe->scaling == FP8_SCALING_DYNAMIC) {
-        FP8_CHECK(cuda_status(launch_amax(X, M * K, s->amax + 0, st), "amax X"));
-        FP8_CHECK(cuda_status(launch_amax(W, N * K, s->amax + 1, st), "amax W"));
+        FP8_CHECK(cuda_status(launch_amax_pair(X, M * K, s->amax + 0, W, N * K, s->amax + 1, st),
+                              "amax X, W"));
         FP8_CHECK(cuda_status(launch_update_scale(s->amax, s->history, s->pos, H, FP8_AMAX_MOST_RECENT,
                                                   f, recipe->margin, recipe->pow2 != 0, s->scale,
                                                   s->scale_inv, 2, st, s->qscale_inv, 1),

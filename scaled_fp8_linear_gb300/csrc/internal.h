@@ -38,6 +38,11 @@ int num_sms();
 // max|x| over n bf16 values into *amax (zeroed first, then atomically raised).
 cudaError_t launch_amax(const void* x, int64_t n, float* amax, cudaStream_t stream);
 
+// The amaxes of two tensors (x1 may be empty, amax1 then nullable) in one
+// zeroing launch and one amax launch.
+cudaError_t launch_amax_pair(const void* x0, int64_t n0, float* amax0, const void* x1, int64_t n1,
+                             float* amax1, cudaStream_t stream);
+
 // Scale update for `nroles` consecutive roles of a state laid out as
 // amax[r], history[r * H + i], pos[r], scale[r], scale_inv[r].  `saved`
 // (nullable) receives scale_inv[r] from before (save_after = 0) or after

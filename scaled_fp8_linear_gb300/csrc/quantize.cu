@@ -297,15 +297,28 @@ __device__ __forceinline__ float block_scale(float amax, int pow2) {
 
 // ------------------------------------------------------------------ amax
 
-__global__ void __launch_bounds__(kThreads) amax_kernel(const uint4* __restrict__ x,
-                                                        int64_t nvec,
-                                                        const uint16_t* __restrict__ tail,
-                                                        int tail_n, unsigned* amax_bits) {
+// The amax of up to two tensors in one launch (the X and W of a forward
+// pass): CTAs [0, ctas0) walk job 0 grid-stride, the rest job 1.
+struct AmaxJob {
+    const uint4* x;        // the 8-element vectors
+    int64_t nvec;
+    const uint16_t* tail;  // the last tail_n (< 8) elements
+    int tail_n;
+    unsigned* amax_bits;
+};
+
+__global__ void __launch_bounds__(kThreads) amax_kernel(AmaxJob j0, AmaxJob j1, int ctas0) {
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();   // the previous kernel's results are visible
+    const bool second = static_cast<int>(blockIdx.x) >= ctas0;
+    const AmaxJob& j = second ? j1 : j0;
+    const uint4* __restrict__ x = j.x;
+    const int64_t nvec = j.nvec;
+    const int64_t cta = second ? blockIdx.x - ctas0 : blockIdx.x;
+    const int64_t nctas = second ? gridDim.x - ctas0 : ctas0;
     uint32_t m = 0;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t stride = nctas * blockDim.x;
+    int64_t i = cta * blockDim.x + threadIdx.x;
     for (; i + 3 * stride < nvec; i += 4 * stride) {
         const uint4 a = ldg_stream(x + i), b = ldg_stream(x + i + stride);
         const uint4 c = ldg_stream(x + i + 2 * stride), d = ldg_stream(x + i + 3 * stride);
@@ -315,8 +328,8 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint4* __restrict_
         m = absmax_vec(m, d);
     }
     for (; i < nvec; i += stride) m = absmax_vec(m, ldg_stream(x + i));
-    if (blockIdx.x == 0 && threadIdx.x < tail_n) m = max(m, (uint32_t)(tail[threadIdx.x] & 0x7FFFu));
-    cta_amax_commit(m, amax_bits);
+    if (cta == 0 && threadIdx.x < j.tail_n) m = max(m, (uint32_t)(j.tail[threadIdx.x] & 0x7FFFu));
+    cta_amax_commit(m, j.amax_bits);
 }
 
 // ---------------------------------------------------------- scale update
@@ -1159,15 +1172,25 @@ cudaError_t launch_zero(float* a, int64_t na, float* b, int64_t nb, cudaStream_t
 
 }  // namespace
 
-cudaError_t launch_amax(const void* x, int64_t n, float* amax, cudaStream_t stream) {
-    cudaError_t e = launch_zero(amax, 1, nullptr, 0, stream);
-    if (e != cudaSuccess || n == 0) return e;
-    const int64_t nvec = n / 8;
-    const int tail_n = static_cast<int>(n - nvec * 8);
-    const uint16_t* tail = static_cast<const uint16_t*>(x) + nvec * 8;
-    launch_pdl(amax_kernel, dim3(grid_for(nvec + 1, kThreads * 4)), dim3(kThreads), 0, stream, 
-        static_cast<const uint4*>(x), nvec, tail, tail_n, reinterpret_cast<unsigned*>(amax));
+cudaError_t launch_amax_pair(const void* x0, int64_t n0, float* amax0, const void* x1, int64_t n1,
+                             float* amax1, cudaStream_t stream) {
+    cudaError_t e = launch_zero(amax0, 1, amax1, 1, stream);
+    if (e != cudaSuccess || n0 + n1 == 0) return e;
+    auto job = [](const void* x, int64_t n, float* amax) {
+        const int64_t nvec = n / 8;
+        return AmaxJob{static_cast<const uint4*>(x), nvec,
+                       static_cast<const uint16_t*>(x) + nvec * 8, static_cast<int>(n - nvec * 8),
+                       reinterpret_cast<unsigned*>(amax)};
+    };
+    const AmaxJob j0 = job(x0, n0, amax0), j1 = job(x1, n1, amax1);
+    const int c0 = n0 ? grid_for(j0.nvec + 1, kThreads * 4) : 0;
+    const int c1 = n1 ? grid_for(j1.nvec + 1, kThreads * 4) : 0;
+    launch_pdl(amax_kernel, dim3(static_cast<unsigned>(c0 + c1)), dim3(kThreads), 0, stream, j0, j1, c0);
     return cudaGetLastError();
+}
+
+cudaError_t launch_amax(const void* x, int64_t n, float* amax, cudaStream_t stream) {
+    return launch_amax_pair(x, n, amax, nullptr, 0, nullptr, stream);
 }
 
 cudaError_t launch_update_scale(const float* amax, float* history, int32_t* pos, int H, int algo,
