@@ -199,8 +199,14 @@ size_t dbias_partial_bytes(int64_t M, int64_t N) {
     return align256(4 * static_cast<size_t>((M + 127) / 128) * static_cast<size_t>(N));
 }
 
-// Checks shared by the three backward variants: workspace size (the partial
-// sums only when dbias is wanted) and alignment.
+// The dynamic update of role r (its history has length 1), for a cast that
+// fuses it.
+ScaleUpd dynamic_update(const fp8_linear_state_t* s, int r, const fp8_recipe_t* recipe,
+                        float* saved) {
+    return ScaleUpd{s->amax + r, s->history + r, s->pos + r, recipe->margin, recipe->pow2 != 0,
+                    s->scale + r, s->scale_inv + r, saved, device_status_word()};
+}
+
 // The forward's per-tensor casts of X and W (with their amax if `amax`):
 // one launch over both tensors when both transposes or neither are kept,
 // else one cast each.
@@ -217,6 +223,8 @@ cudaError_t quantize_x_w(const void* X, const void* W, int64_t M, int64_t N, int
                                   amax ? s->amax + 1 : nullptr, st);
 }
 
+// Checks shared by the three backward variants: workspace size (the partial
+// sums only when dbias is wanted) and alignment.
 int check_bwd_buffers(const void* dY, int64_t M, int64_t N, const fp8_recipe_t* recipe,
                       const fp8_linear_state_t* s, const void* dX, const float* dW,
                       const float* dbias, const void* workspace, size_t workspace_bytes) {
@@ -477,6 +485,18 @@ int fp8_linear_fwd(const void* X, const void* W, const void* bias, int64_t M, in
     if (recipe->scaling == FP8_SCALING_DYNAMIC) {
         FP8_CHECK(cuda_status(launch_amax_pair(X, M * K, s->amax + 0, W, N * K, s->amax + 1, st),
                               "amax X, W"));
+        if (!s->x_qt && !s->w_qt) {
+            // one chunked cast of X and W that derives each scale from its amax
+            // and writes the roles' updates itself ("scale computation" fused)
+            const ScaleUpd ux = dynamic_update(s, 0, recipe, s->qscale_inv + 0);
+            const ScaleUpd uw = dynamic_update(s, 1, recipe, s->qscale_inv + 1);
+            FP8_CHECK(cuda_status(launch_quantize_pair(X, M, K, s->scale + 0, s->x_q, nullptr, nullptr,
+                                                       W, N, K, s->scale + 1, s->w_q, nullptr, nullptr,
+                                                       f, st, &ux, &uw),
+                                  "quantize X, W"));
+            return launch_gemm(s->x_q, f, s->w_q, f, M, N, K, FP8_GRAN_TENSOR, s->scale_inv + 0,
+                               FP8_GRAN_TENSOR, s->scale_inv + 1, bias, Y, FP8_OUT_BF16, 0, st);
+        }
         FP8_CHECK(cuda_status(launch_update_scale(s->amax, s->history, s->pos, H, FP8_AMAX_MOST_RECENT,
                                                   f, recipe->margin, recipe->pow2 != 0, s->scale,
                                                   s->scale_inv, 2, st, s->qscale_inv, 1),
@@ -535,17 +555,30 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
         kmajor ? dy_q + align256(static_cast<size_t>(M) * static_cast<size_t>(N)) : nullptr;
     float* h2 = s->history + 2 * static_cast<int64_t>(H);
 
+    // dynamic scaling with the chunked cast (no transposed copy, no bias
+    // sums, round to nearest): the cast derives the dY scale from its amax
+    // and writes the role's update itself
+    const bool fused_upd = recipe->scaling == FP8_SCALING_DYNAMIC && !recipe->sr_grad && !kmajor &&
+                           !fused_partial;
     if (recipe->scaling == FP8_SCALING_DYNAMIC) {
         FP8_CHECK(cuda_status(launch_amax(dY, M * N, s->amax + 2, st), "amax dY"));
-        FP8_CHECK(cuda_status(launch_update_scale(s->amax + 2, h2, s->pos + 2, H, FP8_AMAX_MOST_RECENT,
-                                                  fb, recipe->margin, recipe->pow2 != 0, s->scale + 2,
-                                                  s->scale_inv + 2, 1, st), "update dY scale"));
+        if (!fused_upd)
+            FP8_CHECK(cuda_status(launch_update_scale(s->amax + 2, h2, s->pos + 2, H,
+                                                      FP8_AMAX_MOST_RECENT, fb, recipe->margin,
+                                                      recipe->pow2 != 0, s->scale + 2,
+                                                      s->scale_inv + 2, 1, st), "update dY scale"));
     }
     float* dy_amax = recipe->scaling == FP8_SCALING_DYNAMIC ? nullptr : s->amax + 2;
     if (recipe->sr_grad)   // "Stochastic rounding": unbiased gradient codes
         FP8_CHECK(cuda_status(launch_quantize_sr(dY, M, N, fb, s->scale + 2, 0, 0, dy_q, dy_qt,
                                                  dy_amax, st, s->sr_key), "quantize dY"));
-    else
+    else if (fused_upd) {
+        const ScaleUpd u = dynamic_update(s, 2, recipe, nullptr);
+        FP8_CHECK(cuda_status(launch_quantize_pair(dY, M, N, s->scale + 2, dy_q, nullptr, nullptr,
+                                                   nullptr, 0, 0, nullptr, nullptr, nullptr,
+                                                   nullptr, fb, st, &u, nullptr),
+                              "quantize dY"));
+    } else
         FP8_CHECK(cuda_status(launch_quantize_tensor(dY, M, N, fb, s->scale + 2, dy_q, dy_qt,
                                                      dy_amax, st, nullptr, fused_partial),
                               "quantize dY"));

@@ -63,14 +63,36 @@ cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, in
                                    cudaStream_t stream, unsigned long long* counts = nullptr,
                                    float* dbias_partial = nullptr);
 
+// Dynamic scaling's update of one role, taken inside a cast kernel instead
+// of a launch of its own: every CTA derives the scale from the role's amax
+// (written by the amax pass before the cast) as the update kernel does
+// (history length 1, most recent), and the first CTA writes the role's
+// history, pos, scale and scale_inv (and `saved`, when set, after the
+// update).  An amax that is 0 or not finite leaves the scale as it was (a
+// non-finite one sets bit 1 of `status`).
+struct ScaleUpd {
+    const float* amax;   // null: no update, the cast reads *scale
+    float* history;
+    int32_t* pos;
+    int margin;
+    int pow2;
+    float* scale;
+    float* scale_inv;
+    float* saved;
+    unsigned* status;
+};
+
 // Per-tensor casts of two tensors in one launch (x0 and x1 each [rows x
 // cols]), both to `fmt`: with transposes (qt0 and qt1 set; rows and cols
 // multiples of 16), or without (both null: the chunked cast, any size).
-// amax0 and amax1 both null or both set (zeroed first).
+// amax0 and amax1 both null or both set (zeroed first).  upd0 / upd1
+// (chunked cast only, nullable): the dynamic update of each tensor's role,
+// fused into the cast; scale0 / scale1 are then that role's scale.
 cudaError_t launch_quantize_pair(const void* x0, int64_t rows0, int64_t cols0, const float* scale0,
                                  uint8_t* q0, uint8_t* qt0, float* amax0, const void* x1,
                                  int64_t rows1, int64_t cols1, const float* scale1, uint8_t* q1,
-                                 uint8_t* qt1, float* amax1, int fmt, cudaStream_t stream);
+                                 uint8_t* qt1, float* amax1, int fmt, cudaStream_t stream,
+                                 const ScaleUpd* upd0 = nullptr, const ScaleUpd* upd1 = nullptr);
 
 // Bias gradient dbias[n] (+)= sum_m x[m][n] of a bf16 x [rows x cols]
 // (cols % 16 == 0), in fp32 and a fixed order.  partial: ceil(rows/128) x

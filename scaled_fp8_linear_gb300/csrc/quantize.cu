@@ -334,6 +334,36 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(AmaxJob j0, AmaxJob j1, 
 
 // ---------------------------------------------------------- scale update
 
+// The scale of an effective amax 0 < a < inf: fp8_max / a * 2^-margin,
+// clamped to [FLT_MIN, FLT_MAX], optionally rounded down to a power of two.
+__device__ __forceinline__ float scale_from_amax(float fmax, float a, int margin, int pow2) {
+    float s = __fdiv_rn(fmax, a);
+    s = __fmul_rn(s, __uint_as_float(static_cast<uint32_t>(127 - margin) << 23));
+    if (!(s <= FLT_MAX)) s = FLT_MAX;
+    if (s < FLT_MIN) s = FLT_MIN;
+    if (pow2) s = __uint_as_float(__float_as_uint(s) & 0xFF800000u);
+    return s;
+}
+
+// The scale a cast with a fused dynamic update uses (every thread), and the
+// role's state update (the thread with `writer` set).
+__device__ __forceinline__ float fused_dynamic_scale(const ScaleUpd& u, float fmax, bool writer) {
+    const float a = *u.amax;
+    const bool ok = a > 0.0f && isfinite(a);
+    const float s = ok ? scale_from_amax(fmax, a, u.margin, u.pow2) : *u.scale;
+    if (writer) {
+        u.history[*u.pos] = a;
+        *u.pos = 0;   // history length 1
+        if (!isfinite(a) && u.status) atomicOr(u.status, 2u);
+        if (ok) {
+            *u.scale = s;
+            *u.scale_inv = __fdiv_rn(1.0f, s);
+        }
+        if (u.saved) *u.saved = *u.scale_inv;
+    }
+    return s;
+}
+
 // One warp per role.  history[pos] = amax; pos = (pos + 1) % H;
 // a = max(history) or amax; if 0 < a < inf: s = fp8_max / a * 2^-margin,
 // clamped to [FLT_MIN, FLT_MAX], optionally rounded down to 2^k; scale = s,
@@ -379,11 +409,7 @@ __global__ void update_scale_kernel(const float* __restrict__ amax, float* __res
         // taxonomy": catch NaN / Inf at the first step that sees them)
         if (!isfinite(eff) && status) atomicOr(status, 2u);
         if (eff > 0.0f && isfinite(eff)) {
-            float s = __fdiv_rn(fmax, eff);
-            s = __fmul_rn(s, __uint_as_float(static_cast<uint32_t>(127 - margin) << 23));
-            if (!(s <= FLT_MAX)) s = FLT_MAX;
-            if (s < FLT_MIN) s = FLT_MIN;
-            if (pow2) s = __uint_as_float(__float_as_uint(s) & 0xFF800000u);
+            const float s = scale_from_amax(fmax, eff, margin, pow2);
             scale[r] = s;
             scale_inv[r] = __fdiv_rn(1.0f, s);
         }
@@ -456,11 +482,12 @@ struct FlatJob {
     uint4* q;
     uint8_t* qtail;
     unsigned* amax_bits;
+    ScaleUpd upd;   // upd.amax null: the scale is *scale
 };
 
 constexpr int kChunkGroups = 4 * kThreads;   // 16-element groups per CTA
 
-template <int FMT, bool AMAX, bool COUNT>
+template <int FMT, bool AMAX, bool COUNT, bool UPD>
 __global__ void __launch_bounds__(kThreads)
     quantize_chunk_kernel(FlatJob j0, FlatJob j1, int64_t ctas0, unsigned long long* counts) {
     ptx::griddep_launch_dependents();
@@ -468,7 +495,10 @@ __global__ void __launch_bounds__(kThreads)
     const bool second = blockIdx.x >= ctas0;
     const FlatJob& j = second ? j1 : j0;
     const int64_t cta = second ? blockIdx.x - ctas0 : blockIdx.x;
-    const float s = *j.scale;
+    const float s = (UPD && j.upd.amax)
+                        ? fused_dynamic_scale(j.upd, Fp8Traits<FMT>::max_finite,
+                                              cta == 0 && threadIdx.x == 0)
+                        : *j.scale;
     const SrSched key{};
     uint32_t m = 0;
     CastCounts cc;
@@ -1207,21 +1237,23 @@ FlatJob flat_job(const void* x, int64_t n, const float* scale, uint8_t* q, float
     const int64_t n16 = n / 16;
     return FlatJob{static_cast<const uint4*>(x), n16, static_cast<const uint16_t*>(x) + n16 * 16,
                    static_cast<int>(n - n16 * 16), scale, reinterpret_cast<uint4*>(q), q + n16 * 16,
-                   reinterpret_cast<unsigned*>(amax)};
+                   reinterpret_cast<unsigned*>(amax), ScaleUpd{}};
 }
 
 int64_t chunk_ctas(const FlatJob& j) {
-    if (j.n16 == 0 && j.tail_n == 0) return 0;
+    // a job without elements still takes one CTA when it carries a fused
+    // update, so that its state is written
+    if (j.n16 == 0 && j.tail_n == 0) return j.upd.amax ? 1 : 0;
     const int64_t c = (j.n16 + kChunkGroups - 1) / kChunkGroups;
     return c < 1 ? 1 : c;
 }
 
-template <int FMT, bool AMAX, bool COUNT>
+template <int FMT, bool AMAX, bool COUNT, bool UPD = false>
 static void launch_chunk(const FlatJob& j0, const FlatJob& j1, unsigned long long* counts,
                          cudaStream_t stream) {
     const int64_t c0 = chunk_ctas(j0), c1 = chunk_ctas(j1);
     if (c0 + c1 == 0) return;
-    launch_pdl(quantize_chunk_kernel<FMT, AMAX, COUNT>, dim3(static_cast<unsigned>(c0 + c1)),
+    launch_pdl(quantize_chunk_kernel<FMT, AMAX, COUNT, UPD>, dim3(static_cast<unsigned>(c0 + c1)),
                dim3(kThreads), 0, stream, j0, j1, c0, counts);
 }
 
@@ -1310,7 +1342,8 @@ cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, in
 cudaError_t launch_quantize_pair(const void* x0, int64_t rows0, int64_t cols0, const float* scale0,
                                  uint8_t* q0, uint8_t* qt0, float* amax0, const void* x1,
                                  int64_t rows1, int64_t cols1, const float* scale1, uint8_t* q1,
-                                 uint8_t* qt1, float* amax1, int fmt, cudaStream_t stream) {
+                                 uint8_t* qt1, float* amax1, int fmt, cudaStream_t stream,
+                                 const ScaleUpd* upd0, const ScaleUpd* upd1) {
     const bool A = amax0 != nullptr;
     if (A) {
         const cudaError_t e = launch_zero(amax0, 1, amax1, 1, stream);
@@ -1322,13 +1355,18 @@ cudaError_t launch_quantize_pair(const void* x0, int64_t rows0, int64_t cols0, c
                        qt, reinterpret_cast<unsigned*>(amax)};
     };
     if (!qt0 && !qt1) {   // no transposed copies: one chunked cast over both tensors
-        const FlatJob f0 = flat_job(x0, rows0 * cols0, scale0, q0, amax0);
-        const FlatJob f1 = flat_job(x1, rows1 * cols1, scale1, q1, amax1);
+        FlatJob f0 = flat_job(x0, rows0 * cols0, scale0, q0, amax0);
+        FlatJob f1 = flat_job(x1, rows1 * cols1, scale1, q1, amax1);
+        if (upd0) f0.upd = *upd0;
+        if (upd1) f1.upd = *upd1;
+        const bool U = upd0 || upd1;
         if (fmt == 0) {
             if (A) launch_chunk<0, true, false>(f0, f1, nullptr, stream);
+            else if (U) launch_chunk<0, false, false, true>(f0, f1, nullptr, stream);
             else launch_chunk<0, false, false>(f0, f1, nullptr, stream);
         } else {
             if (A) launch_chunk<1, true, false>(f0, f1, nullptr, stream);
+            else if (U) launch_chunk<1, false, false, true>(f0, f1, nullptr, stream);
             else launch_chunk<1, false, false>(f0, f1, nullptr, stream);
         }
         return cudaGetLastError();
