@@ -345,6 +345,40 @@ def test_step_replays_from_a_cuda_graph():
                            c.view(torch.int16) if c.dtype == torch.bfloat16 else c.view(torch.int32))
 
 
+@pytest.mark.parametrize("transposes", [False, True], ids=["fused_update", "update_kernel"])
+def test_dynamic_non_finite_and_zero_inputs(transposes):
+    """Dynamic scaling (the scale computed inside the cast when no transposed
+    copies are kept, by the update kernel otherwise): a NaN in X keeps the X
+    scale and sets bit 1 of the device status word for that step only; an
+    all-zero dY keeps the dY scale; every other role and step matches the
+    oracle's state machine bit for bit."""
+    M, N, K = 256, 256, 256
+    rec = F.Recipe(F.SCALING_DYNAMIC)
+    layer = F.Fp8Linear(M, N, K, rec, device=DEV, transposes=transposes)
+    ost = oracle.LinearState(_orecipe(rec))
+    W = synthetic.normal((N, K), 0.02, seed=1)
+    flags = []
+    for step in range(4):
+        X = synthetic.normal((M, K), 1.0, seed=10 + step)
+        dY = synthetic.normal((M, N), 1e-3, seed=20 + step)
+        if step == 1:
+            X[5, 7] = float("nan")
+        if step == 2:
+            dY.zero_()
+        before = layer.scale.clone()
+        layer.forward(X.to(DEV), W.to(DEV))
+        layer.backward(dY.to(DEV))
+        flags.append(F.fp8_device_status(clear=True))
+        oracle.linear_fwd(bits(X), bits(W), _orecipe(rec), ost)
+        oracle.linear_bwd(bits(dY), _orecipe(rec), ost)
+        if step == 1:
+            assert layer.scale[0].item() == before[0].item()
+        if step == 2:
+            assert layer.scale[2].item() == before[2].item()
+        _check_state(layer, ost)
+    assert flags == [0, 2, 0, 0]
+
+
 def test_non_finite_input_is_flagged_and_the_scale_held():
     """A NaN in X: the delayed update keeps the X scale and sets bit 1 of the
     device status word, at this step and for as long as the NaN stays in the
