@@ -299,7 +299,9 @@ int fp8_gemm_group(const fp8_gemm_args_t* g1, const fp8_gemm_args_t* g2, void* s
  * and recipe: the quantised dY operands (and their scale arrays), plus
  * 4*ceil(M/128)*N bytes for the bias gradient's partial sums, which only a
  * call with dbias uses.  fp8_linear_fwd needs none.  Returns 0 for an
- * invalid recipe. */
+ * invalid recipe.  This is the size for either per-tensor backward; one
+ * whose state keeps no transposed copies needs M*N code bytes fewer (a
+ * smaller workspace is accepted then). */
 size_t fp8_workspace_size(int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe);
 
 /* Forward pass Y [M x N] (bf16) = X [M x K] . W [N x K]^T (+ bias [N], bf16,
@@ -369,11 +371,12 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K,
  * no counterpart: this is a property of the library, not of the method.)
  * Same arguments and results as fp8_linear_bwd, minus the workspace and the
  * bias gradient (dbias = NULL): the
- * quantised gradient and its transpose go to a fixed device array of
- * FP8_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
- * the library holds until the process exits.  Shapes whose dY operands
- * exceed it (2*M*N > 32 MiB with per-tensor scaling, e.g. more than 4096 x
- * 4096) are rejected with FP8_ERR_SHAPE and a message naming the limit.
+ * quantised gradient (and its transpose, where the backward makes one) goes
+ * to a fixed device array of FP8_NOALLOC_SCRATCH_BYTES inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ * Shapes whose dY operands exceed it are rejected with FP8_ERR_SHAPE and a
+ * message naming the limit: with per-tensor scaling M*N > 32 MiB (e.g. more
+ * than 4096 x 8192) without transposed copies, 2*M*N > 32 MiB with them.
  * Calls no allocating routine.  The first call on each device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current;
  * make that first call before any stream capture.  Every call on a device

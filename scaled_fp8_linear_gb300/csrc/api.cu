@@ -185,13 +185,18 @@ size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 // Workspace of the backward pass, in order: the dY operands (dY_q, dY_q^T,
 // and their scale arrays in the block-wise and per-row modes), then the bias
 // gradient's partial column sums, one row of N floats per 128 tokens.
-size_t bwd_operand_bytes(int64_t M, int64_t N, const fp8_recipe_t* recipe) {
+// With a state (s non-null) the per-tensor modes count what that state's
+// backward writes: dY_q alone when the forward kept no transposed copies
+// (the GEMMs then read the codes MN-major), dY_q and dY_q^T otherwise.
+size_t bwd_operand_bytes(int64_t M, int64_t N, const fp8_recipe_t* recipe,
+                         const fp8_linear_state_t* s = nullptr) {
     const size_t mn = static_cast<size_t>(M) * static_cast<size_t>(N);
     if (recipe->scaling == FP8_SCALING_ROW)   // + per-row scales of both, [M] and [N]
         return 2 * align256(mn) + align256(4 * static_cast<size_t>(M)) +
                align256(4 * static_cast<size_t>(N));
     if (recipe->scaling == FP8_SCALING_BLOCK)  // + 1x128 scales, [M][N/128] and [N][M/128]
         return 2 * align256(mn) + 2 * align256(4 * (mn / 128));
+    if (s && !(s->x_qt && s->w_qt)) return align256(mn);
     return 2 * align256(mn);
 }
 
@@ -228,7 +233,7 @@ cudaError_t quantize_x_w(const void* X, const void* W, int64_t M, int64_t N, int
 int check_bwd_buffers(const void* dY, int64_t M, int64_t N, const fp8_recipe_t* recipe,
                       const fp8_linear_state_t* s, const void* dX, const float* dW,
                       const float* dbias, const void* workspace, size_t workspace_bytes) {
-    const size_t need = bwd_operand_bytes(M, N, recipe) + (dbias ? dbias_partial_bytes(M, N) : 0);
+    const size_t need = bwd_operand_bytes(M, N, recipe, s) + (dbias ? dbias_partial_bytes(M, N) : 0);
     if (workspace_bytes < need)
         return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: workspace of %zu bytes, %zu needed",
                          workspace_bytes, need);
@@ -313,8 +318,9 @@ int linear_bwd_row(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
 
 }  // namespace
 
-size_t bwd_operand_workspace(int64_t M, int64_t N, const fp8_recipe_t* recipe) {
-    return bwd_operand_bytes(M, N, recipe);
+size_t bwd_operand_workspace(int64_t M, int64_t N, const fp8_recipe_t* recipe,
+                             const fp8_linear_state_t* s) {
+    return bwd_operand_bytes(M, N, recipe, s);
 }
 
 }  // namespace fp8
@@ -540,7 +546,7 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
     // cast, then summed in order; the stochastic cast leaves them to a pass
     // of their own
     float* partial = dbias ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                                      bwd_operand_bytes(M, N, recipe))
+                                                      bwd_operand_bytes(M, N, recipe, s))
                            : nullptr;
     float* fused_partial = recipe->sr_grad ? nullptr : partial;
     const int fb = recipe->bwd_format, ff = recipe->fwd_format;

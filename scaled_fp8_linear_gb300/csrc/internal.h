@@ -137,8 +137,11 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
                 int layout = FP8_LAYOUT_TN);
 
 // Workspace bytes of fp8_linear_bwd's dY operands (without the bias
-// gradient's partial sums) for a valid recipe.
-size_t bwd_operand_workspace(int64_t M, int64_t N, const fp8_recipe_t* recipe);
+// gradient's partial sums) for a valid recipe; with a state (nullable), what
+// that state's per-tensor backward needs (dY_q alone when it keeps no
+// transposed copies).
+size_t bwd_operand_workspace(int64_t M, int64_t N, const fp8_recipe_t* recipe,
+                             const fp8_linear_state_t* s = nullptr);
 
 // The arguments of one launch_gemm call.
 struct GemmArgs {

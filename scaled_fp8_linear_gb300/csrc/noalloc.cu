@@ -1,8 +1,10 @@
 // noalloc.cu -- fp8_linear_bwd_noalloc: the backward pass for callers that
 // cannot allocate device memory.
 //
-// fp8_linear_bwd needs 2 x M x N bytes of scratch for the quantised gradient
-// and its transpose, and asks the caller for it as a workspace.  Some callers
+// fp8_linear_bwd needs scratch for the quantised gradient (M x N bytes, and
+// as much again for its transpose when the state keeps transposed copies or
+// the recipe is block-wise or per-row), and asks the caller for it as a
+// workspace.  Some callers
 // have no way to provide one: a custom operator inside a host framework whose
 // memory planner owns every device buffer and hands the operator only its
 // inputs and outputs; a latency-critical caller that must not pay for
@@ -71,14 +73,13 @@ extern "C" int fp8_linear_bwd_noalloc(const void* dY, int64_t M, int64_t N, int6
     // invalid recipe sizes to 0 and is reported by fp8_linear_bwd)
     const size_t need = fp8_workspace_size(M, N, K, recipe) == 0
                             ? 0
-                            : fp8::bwd_operand_workspace(M, N, recipe);
+                            : fp8::bwd_operand_workspace(M, N, recipe, state);
     if (need > kScratchBytes)
         return fp8::set_error(FP8_ERR_SHAPE,
                               "fp8_linear_bwd_noalloc: M x N = %lld x %lld needs %zu bytes of "
-                              "scratch; the built-in scratch holds %zu bytes "
-                              "(2 x M x N <= %zu)",
+                              "scratch; the built-in scratch holds %zu bytes",
                               static_cast<long long>(M), static_cast<long long>(N), need,
-                              kScratchBytes, kScratchBytes);
+                              kScratchBytes);
     void* scratch = nullptr;
     const int st = scratch_on_current_device(&scratch);
     if (st != FP8_OK) return st;

@@ -71,6 +71,38 @@ def test_noalloc_rejects_shapes_beyond_the_scratch():
     rec = F.Recipe(F.SCALING_DELAYED, history_len=16)
     st = F.LinearStateC()
     p = ctypes.c_void_p(0x10000)
-    # 2 * 8192 * 4096 bytes > 32 MiB: rejected before any device work
-    assert fn(p, 8192, 4096, 4096, ctypes.byref(rec), ctypes.byref(st), p, p, 0, None) == -2
+    # without transposed copies the scratch holds dY_q alone: 8192 * 8192
+    # bytes > 32 MiB is rejected before any device work
+    assert fn(p, 8192, 8192, 4096, ctypes.byref(rec), ctypes.byref(st), p, p, 0, None) == -2
     assert "scratch" in F.fp8_last_error()
+    # with them it also holds dY_q^T: 2 * 8192 * 4096 bytes > 32 MiB
+    st_t = F.LinearStateC()
+    st_t.x_qt = st_t.w_qt = 0x10000
+    assert fn(p, 8192, 4096, 4096, ctypes.byref(rec), ctypes.byref(st_t), p, p, 0, None) == -2
+    assert "scratch" in F.fp8_last_error()
+
+
+def test_noalloc_takes_twice_the_tokens_without_transposed_copies():
+    """8192 x 4096 (32 MiB of dY codes): beyond the scratch with transposed
+    copies, within it when the backward reads the codes MN-major; the result
+    equals the workspace backward's."""
+    fn = _noalloc()
+    M, N, K = 8192, 4096, 512
+    rec = F.Recipe(F.SCALING_DYNAMIC)
+    ref_layer = F.Fp8Linear(M, N, K, rec, device=DEV)
+    na_layer = F.Fp8Linear(M, N, K, rec, device=DEV)
+    X = synthetic.normal((M, K), 1.0, seed=3, device=DEV)
+    W = synthetic.normal((N, K), 0.02, seed=4, device=DEV)
+    dY = synthetic.normal((M, N), 1e-3, seed=5, device=DEV)
+    ref_layer.forward(X, W)
+    na_layer.forward(X, W)
+    dX_ref, dW_ref = ref_layer.backward(dY)
+    dX_na = torch.empty(M, K, dtype=torch.bfloat16, device=DEV)
+    dW_na = torch.zeros(N, K, dtype=torch.float32, device=DEV)
+    st = fn(dY.data_ptr(), M, N, K, ctypes.byref(rec), ctypes.byref(na_layer.c_state),
+            dX_na.data_ptr(), dW_na.data_ptr(), 0, torch.cuda.current_stream().cuda_stream)
+    assert st == 0, F.fp8_last_error()
+    torch.cuda.synchronize()
+    assert torch.equal(dX_na.view(torch.int16), dX_ref.view(torch.int16))
+    assert torch.equal(dW_na.view(torch.int32), dW_ref.view(torch.int32))
+    assert torch.equal(na_layer.scale, ref_layer.scale)
