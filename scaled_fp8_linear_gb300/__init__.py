@@ -432,6 +432,8 @@ class Fp8Linear:
         self.sr_key = torch.tensor([seed - (1 << 64) if seed >> 63 else seed, 0],
                                    dtype=torch.int64, device=dev)
         ws = fp8_workspace_size(M, N, K, self.recipe)
+        if self.recipe.scaling in (SCALING_DELAYED, SCALING_DYNAMIC) and not keep:
+            ws -= (M * N + 255) // 256 * 256   # no dY_q^T: the backward reads dY_q MN-major
         self.workspace = torch.empty(max(ws, 16), **u8)
         p = lambda t: None if t is None else t.data_ptr()
         self.c_state = LinearStateC(p(self.scale), p(self.scale_inv), p(self.amax),

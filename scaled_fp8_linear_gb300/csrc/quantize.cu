@@ -419,7 +419,9 @@ __global__ void update_scale_kernel(const float* __restrict__ amax, float* __res
 
 // ------------------------------------------------------- per-tensor cast
 
-// Flat cast, 16 elements (32 B in, 16 B out) per thread per step.
+// Flat cast, 16 elements (32 B in, 16 B out) per thread per step: the
+// stochastic-rounding form (the round-to-nearest casts use the chunked
+// kernel below).
 template <int FMT, bool AMAX, bool COUNT, bool SR>
 __global__ void __launch_bounds__(kThreads)
     quantize_flat_kernel(const uint4* __restrict__ x, int64_t n16, const uint16_t* __restrict__ xt,
@@ -1263,14 +1265,15 @@ static void launch_flat(const void* x, int64_t n, const float* scale, uint8_t* q
                         const unsigned long long* key_dev = nullptr) {
     if constexpr (!SR) {   // round to nearest: one chunk per CTA
         launch_chunk<FMT, AMAX, COUNT>(flat_job(x, n, scale, q, amax), FlatJob{}, counts, stream);
-        return;
+    } else {               // stochastic rounding: grid-stride, bound by integer issue
+        const int64_t n16 = n / 16;
+        const int tail_n = static_cast<int>(n - n16 * 16);
+        launch_pdl(quantize_flat_kernel<FMT, AMAX, COUNT, SR>, dim3(grid_for(n16 + 1, kThreads * 2)),
+                   dim3(kThreads), 0, stream, static_cast<const uint4*>(x), n16,
+                   static_cast<const uint16_t*>(x) + n16 * 16, tail_n, scale,
+                   reinterpret_cast<uint4*>(q), q + n16 * 16, reinterpret_cast<unsigned*>(amax),
+                   counts, key, key_dev);
     }
-    const int64_t n16 = n / 16;
-    const int tail_n = static_cast<int>(n - n16 * 16);
-    launch_pdl(quantize_flat_kernel<FMT, AMAX, COUNT, SR>, dim3(grid_for(n16 + 1, kThreads * 2)), dim3(kThreads), 0, stream, 
-        static_cast<const uint4*>(x), n16, static_cast<const uint16_t*>(x) + n16 * 16, tail_n,
-        scale, reinterpret_cast<uint4*>(q), q + n16 * 16, reinterpret_cast<unsigned*>(amax), counts,
-        key, key_dev);
 }
 
 template <int FMT, bool AMAX, bool COUNT, bool SR, bool DBIAS = false>
