@@ -33,6 +33,30 @@ def test_library_exports_every_declared_call():
         assert hasattr(lib, n), n
 
 
+def _header_constants():
+    """Enumerators (NAME = value) and #defines of the public header."""
+    src = open(os.path.join(ROOT, "include", "fp8linear.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    vals = {k: int(v) for k, v in re.findall(r"\b(FP8_[A-Z0-9_x]+)\s*=\s*(-?\d+)", src)}
+    vals.update({k: int(v) for k, v in re.findall(r"#define\s+(FP8_[A-Z0-9_x]+)\s+(\d+)\b", src)})
+    return vals
+
+
+def test_binding_constants_match_the_header():
+    """Every constant the binding exports under an FP8_ name of the header
+    has the header's value (layouts, granularities, formats, recipes)."""
+    hdr = _header_constants()
+    checked = 0
+    for name in F.__all__:
+        if name.isupper() and "FP8_" + name in hdr:
+            assert getattr(F, name) == hdr["FP8_" + name], name
+            checked += 1
+    for name in ("LAYOUT_TN", "LAYOUT_B_KN", "LAYOUT_A_KM", "LAYOUT_KM_KN", "GRAN_ROW",
+                 "SCALE_POW2", "E4M3", "E5M2", "SCALING_DYNAMIC", "OUT_F32"):
+        assert "FP8_" + name in hdr and getattr(F, name) == hdr["FP8_" + name], name
+    assert checked >= 10
+
+
 FAKE = 0x10000  # a 16-byte-aligned address that is never dereferenced: every call below fails validation
 
 
