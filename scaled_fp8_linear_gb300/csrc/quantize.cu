@@ -1347,6 +1347,8 @@ cudaError_t launch_quantize_pair(const void* x0, int64_t rows0, int64_t cols0, c
                                  int64_t rows1, int64_t cols1, const float* scale1, uint8_t* q1,
                                  uint8_t* qt1, float* amax1, int fmt, cudaStream_t stream,
                                  const ScaleUpd* upd0, const ScaleUpd* upd1) {
+    // a fused update rides on the chunked cast without a fused amax only
+    if ((upd0 || upd1) && (qt0 || qt1 || amax0)) return cudaErrorInvalidValue;
     const bool A = amax0 != nullptr;
     if (A) {
         const cudaError_t e = launch_zero(amax0, 1, amax1, 1, stream);
