@@ -298,6 +298,39 @@ __device__ __forceinline__ void emit_f32_chunk(uint8_t* slot, const uint32_t (&r
     }
 }
 
+// bf16 output of one 32-column accumulator chunk of a warp's 32 rows (first
+// row m0, first column n0): v = fp32(acc * f) (+ bias), rounded to bf16, as
+// one 32-row x 64-byte TMA box through `slot` (rows past M and columns past N
+// are clipped by the copy).  Whole-warp call.
+__device__ __forceinline__ void emit_bf16_chunk(uint8_t* slot, const uint32_t (&r)[32],
+                                                const float (&f)[32], int64_t m0, int64_t n0,
+                                                const GemmParams& p, const CUtensorMap* map) {
+    float v[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = __fmul_rn(__uint_as_float(r[e]), f[e]);
+    if (p.bias) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+            if (n0 + j < p.N) {
+                float b[8];
+                load_bias8(b, p.bias, n0 + j);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[j + e] = __fadd_rn(v[j + e], b[e]);
+            }
+        }
+    }
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+        w[e] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    const uint4 piece[4] = {make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7]),
+                            make_uint4(w[8], w[9], w[10], w[11]),
+                            make_uint4(w[12], w[13], w[14], w[15])};
+    emit_box(slot, piece, map, n0, m0, m0 < p.M && n0 < p.N, false);
+}
+
 // --------------------------------------------------------- per-tensor kernel
 
 template <int BN, int STAGES>
@@ -598,9 +631,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             ptx::mbar_wait(done, 0, &never);
         }
     } else if (warp >= 4) {
-        // bf16 output: row-per-thread 16-byte stores; FP32 output: 32-row x
-        // 16-column TMA boxes from this warp's 2 KB staging slot, stored or
-        // (accumulate) added by the TMA -- no read of D by the SM
+        // 32-row x 64-byte TMA boxes from this warp's 2 KB staging slot: 32
+        // bf16 columns stored, or 16 FP32 columns stored or (accumulate) added
+        // by the TMA -- no read of D by the SM
         const int qd = warp & 3;
         uint8_t* slot = epi_stage + qd * 2048;
         const GemmParams& p1 = p;
@@ -630,7 +663,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 float f[32];
                 chunk_factors(f, fa, n0, p);
                 if (f32) emit_f32_chunk(slot, r, f, m0, n0, p, map);
-                else if (m < p.M) store_chunk(r, m, n0, p, f, false);
+                else emit_bf16_chunk(slot, r, f, m0, n0, p, map);
             }
             ptx::tc_fence_before();
             __syncwarp();
