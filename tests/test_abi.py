@@ -142,6 +142,24 @@ def test_workspace_size_and_recipe_checks():
     assert L.fp8_linear_fwd(p, p, None, 16, 16, 16, ctypes.byref(r), ctypes.byref(st), p, None, 0, None) == -1
 
 
+def test_gemm_shapes_follow_the_layout():
+    """The binding reads (M, K, N) from the stored shapes of each layout and
+    refuses operands that disagree on K."""
+    import torch
+    a_mk = torch.zeros(48, 32, dtype=torch.uint8)      # [M x K]
+    a_km = torch.zeros(32, 48, dtype=torch.uint8)      # [K x M]
+    b_nk = torch.zeros(80, 32, dtype=torch.uint8)      # [N x K]
+    b_kn = torch.zeros(32, 80, dtype=torch.uint8)      # [K x N]
+    assert F._gemm_dims(a_mk, b_nk, F.LAYOUT_TN) == (48, 32, 80)
+    assert F._gemm_dims(a_mk, b_kn, F.LAYOUT_B_KN) == (48, 32, 80)
+    assert F._gemm_dims(a_km, b_nk, F.LAYOUT_A_KM) == (48, 32, 80)
+    assert F._gemm_dims(a_km, b_kn, F.LAYOUT_KM_KN) == (48, 32, 80)
+    for layout, a, b in ((F.LAYOUT_TN, a_mk, b_kn), (F.LAYOUT_B_KN, a_mk, b_nk),
+                         (F.LAYOUT_A_KM, a_km, b_kn), (F.LAYOUT_KM_KN, a_mk, b_kn)):
+        with pytest.raises(ValueError):
+            F._gemm_dims(a, b, layout)
+
+
 def test_binding_refuses_cpu_tensors():
     import torch
     x = torch.zeros(4, 4, dtype=torch.bfloat16)
