@@ -377,11 +377,16 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K,
  * Shapes whose dY operands exceed it are rejected with FP8_ERR_SHAPE and a
  * message naming the limit: with per-tensor scaling M*N > 32 MiB (e.g. more
  * than 4096 x 8192) without transposed copies, 2*M*N > 32 MiB with them.
- * Calls no allocating routine.  The first call on each device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  Every call on a device
- * shares the array and leaves its contents behind; calls whose work overlaps
- * on the GPU race on it, so order them on one stream. */
+ * Calls no allocating routine.  Arguments are checked first: a call that
+ * fails them returns its status without touching the device.  The first
+ * call in each CUDA context (normally the device's primary context: once
+ * per device) looks up the array's device address (cudaGetSymbolAddress)
+ * with that context current and keeps it under the context's unique ID, so
+ * a context made after cudaDeviceReset, or one the caller makes current,
+ * gets its own lookup; make that first call before any stream capture.
+ * Every call on a device shares the array and leaves its contents behind;
+ * calls whose work overlaps on the GPU race on it, so order them on one
+ * stream. */
 int fp8_linear_bwd_noalloc(const void* dY, int64_t M, int64_t N, int64_t K,
                            const fp8_recipe_t* recipe, const fp8_linear_state_t* state,
                            void* dX, float* dW, int accumulate_dW, void* stream);

@@ -228,18 +228,17 @@ cudaError_t quantize_x_w(const void* X, const void* W, int64_t M, int64_t N, int
                                   amax ? s->amax + 1 : nullptr, st);
 }
 
-// Checks shared by the three backward variants: workspace size (the partial
-// sums only when dbias is wanted) and alignment.
-int check_bwd_buffers(const void* dY, int64_t M, int64_t N, const fp8_recipe_t* recipe,
-                      const fp8_linear_state_t* s, const void* dX, const float* dW,
-                      const float* dbias, const void* workspace, size_t workspace_bytes) {
+// The workspace of a backward call: its size (the partial sums only when
+// dbias is wanted) and alignment.
+int check_bwd_workspace(int64_t M, int64_t N, const fp8_recipe_t* recipe,
+                        const fp8_linear_state_t* s, const float* dbias, const void* workspace,
+                        size_t workspace_bytes) {
+    if (!workspace) return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: NULL pointer");
     const size_t need = bwd_operand_bytes(M, N, recipe, s) + (dbias ? dbias_partial_bytes(M, N) : 0);
     if (workspace_bytes < need)
         return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: workspace of %zu bytes, %zu needed",
                          workspace_bytes, need);
-    if (!aligned16(dY) || !aligned16(dX) || !aligned16(dW) || !aligned16(workspace) ||
-        !aligned16(s->x_q) || !aligned16(s->w_q) || !aligned16(s->x_qt) || !aligned16(s->w_qt) ||
-        (reinterpret_cast<uintptr_t>(dbias) & 3u))
+    if (!aligned16(workspace))
         return set_error(FP8_ERR_ALIGN, "fp8_linear_bwd: tensors must be 16-byte aligned (dbias 4-byte)");
     return FP8_OK;
 }
@@ -251,12 +250,7 @@ int check_bwd_buffers(const void* dY, int64_t M, int64_t N, const fp8_recipe_t* 
 // token-blocked cast kept by the forward pass.
 int linear_bwd_block(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe,
                      const fp8_linear_state_t* s, void* dX, float* dW, int accumulate_dW,
-                     float* dbias, void* workspace, size_t workspace_bytes, cudaStream_t st) {
-    if (!s->x_qt || !s->w_qt || !s->x_sinv_t || !s->w_sinv_t)
-        return set_error(FP8_ERR_INVALID_ARG,
-                         "fp8_linear_bwd: block mode needs the forward's x_qt/x_sinv_t and w_qt/w_sinv_t");
-    if (M % 128) return set_error(FP8_ERR_SHAPE, "fp8_linear_bwd: block mode needs M multiple of 128");
-    FP8_CHECK(check_bwd_buffers(dY, M, N, recipe, s, dX, dW, dbias, workspace, workspace_bytes));
+                     float* dbias, void* workspace, cudaStream_t st) {
     const size_t mn = static_cast<size_t>(M) * static_cast<size_t>(N);
     const int fb = recipe->bwd_format, ff = recipe->fwd_format;
     uint8_t* dy_q = static_cast<uint8_t*>(workspace);
@@ -289,11 +283,7 @@ int linear_bwd_block(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_
 // GEMMs with vector epilogue factors.
 int linear_bwd_row(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe,
                    const fp8_linear_state_t* s, void* dX, float* dW, int accumulate_dW,
-                   float* dbias, void* workspace, size_t workspace_bytes, cudaStream_t st) {
-    if (!s->x_qt || !s->w_qt || !s->x_sinv_t || !s->w_sinv_t)
-        return set_error(FP8_ERR_INVALID_ARG,
-                         "fp8_linear_bwd: per-row mode needs the forward's x_qt/x_sinv_t and w_qt/w_sinv_t");
-    FP8_CHECK(check_bwd_buffers(dY, M, N, recipe, s, dX, dW, dbias, workspace, workspace_bytes));
+                   float* dbias, void* workspace, cudaStream_t st) {
     const size_t mn = static_cast<size_t>(M) * static_cast<size_t>(N);
     const int fb = recipe->bwd_format, ff = recipe->fwd_format;
     uint8_t* dy_q = static_cast<uint8_t*>(workspace);
@@ -317,6 +307,36 @@ int linear_bwd_row(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
 }
 
 }  // namespace
+
+int check_linear_bwd_args(const void* dY, int64_t M, int64_t N, int64_t K,
+                          const fp8_recipe_t* recipe, const fp8_linear_state_t* s, const void* dX,
+                          const float* dW, const float* dbias) {
+    FP8_CHECK(check_recipe(recipe));
+    FP8_CHECK(check_linear_shape(M, N, K, recipe));
+    if (!dY || !dX || !dW || !s)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: NULL pointer");
+    const bool block = recipe->scaling == FP8_SCALING_BLOCK;
+    if (block || recipe->scaling == FP8_SCALING_ROW) {
+        if (!s->x_qt || !s->w_qt || !s->x_sinv_t || !s->w_sinv_t)
+            return set_error(FP8_ERR_INVALID_ARG,
+                             "fp8_linear_bwd: %s mode needs the forward's x_qt/x_sinv_t and w_qt/w_sinv_t",
+                             block ? "block" : "per-row");
+        if (block && M % 128)
+            return set_error(FP8_ERR_SHAPE, "fp8_linear_bwd: block mode needs M multiple of 128");
+    } else {
+        FP8_CHECK(check_state_scales(s));
+        if (!s->x_q || !s->w_q)
+            return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: state->x_q / w_q must be set");
+        if (recipe->sr_grad && (!s->sr_key || (reinterpret_cast<uintptr_t>(s->sr_key) & 7u)))
+            return set_error(FP8_ERR_INVALID_ARG,
+                             "fp8_linear_bwd: sr_grad needs an 8-byte aligned state->sr_key");
+    }
+    if (!aligned16(dY) || !aligned16(dX) || !aligned16(dW) || !aligned16(s->x_q) ||
+        !aligned16(s->w_q) || !aligned16(s->x_qt) || !aligned16(s->w_qt) ||
+        (reinterpret_cast<uintptr_t>(dbias) & 3u))
+        return set_error(FP8_ERR_ALIGN, "fp8_linear_bwd: tensors must be 16-byte aligned (dbias 4-byte)");
+    return FP8_OK;
+}
 
 size_t bwd_operand_workspace(int64_t M, int64_t N, const fp8_recipe_t* recipe,
                              const fp8_linear_state_t* s) {
@@ -525,22 +545,14 @@ int fp8_linear_fwd(const void* X, const void* W, const void* bias, int64_t M, in
 int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_recipe_t* recipe,
                    const fp8_linear_state_t* s, void* dX, float* dW, int accumulate_dW,
                    float* dbias, void* workspace, size_t workspace_bytes, void* stream) {
-    FP8_CHECK(check_recipe(recipe));
-    FP8_CHECK(check_linear_shape(M, N, K, recipe));
-    if (!dY || !dX || !dW || !s || !workspace)
-        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: NULL pointer");
+    FP8_CHECK(check_linear_bwd_args(dY, M, N, K, recipe, s, dX, dW, dbias));
+    FP8_CHECK(check_bwd_workspace(M, N, recipe, s, dbias, workspace, workspace_bytes));
     if (recipe->scaling == FP8_SCALING_BLOCK)
         return linear_bwd_block(dY, M, N, K, recipe, s, dX, dW, accumulate_dW, dbias, workspace,
-                                workspace_bytes, as_stream(stream));
+                                as_stream(stream));
     if (recipe->scaling == FP8_SCALING_ROW)
         return linear_bwd_row(dY, M, N, K, recipe, s, dX, dW, accumulate_dW, dbias, workspace,
-                              workspace_bytes, as_stream(stream));
-    FP8_CHECK(check_state_scales(s));
-    if (!s->x_q || !s->w_q)
-        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: state->x_q / w_q must be set");
-    FP8_CHECK(check_bwd_buffers(dY, M, N, recipe, s, dX, dW, dbias, workspace, workspace_bytes));
-    if (recipe->sr_grad && (!s->sr_key || (reinterpret_cast<uintptr_t>(s->sr_key) & 7u)))
-        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: sr_grad needs an 8-byte aligned state->sr_key");
+                              as_stream(stream));
     cudaStream_t st = as_stream(stream);
     // bias gradient: partial column sums fused into the (round-to-nearest) dY
     // cast, then summed in order; the stochastic cast leaves them to a pass

@@ -143,6 +143,13 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
 size_t bwd_operand_workspace(int64_t M, int64_t N, const fp8_recipe_t* recipe,
                              const fp8_linear_state_t* s = nullptr);
 
+// Every check that fp8_linear_bwd makes before it looks at its workspace:
+// recipe, shape, the state pointers the recipe's mode needs, alignment.
+// FP8_OK or the status (with its message) that fp8_linear_bwd would return.
+int check_linear_bwd_args(const void* dY, int64_t M, int64_t N, int64_t K,
+                          const fp8_recipe_t* recipe, const fp8_linear_state_t* s, const void* dX,
+                          const float* dW, const float* dbias);
+
 // The arguments of one launch_gemm call.
 struct GemmArgs {
     const uint8_t* A;

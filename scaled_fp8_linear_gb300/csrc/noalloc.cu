@@ -21,7 +21,10 @@
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
+#include <utility>
+#include <vector>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/fp8linear.h"
@@ -34,32 +37,72 @@ constexpr size_t kScratchBytes = FP8_NOALLOC_SCRATCH_BYTES;
 // Held by every GPU that loads the library, until the process exits.
 static __device__ __align__(256) uint8_t g_bwd_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of g_bwd_scratch on the current device.  The host-side
-// symbol is only a stand-in, so the address is looked up once per device
-// (with that device current) and cached.
-int scratch_on_current_device(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return fp8::set_error(FP8_ERR_CUDA, "fp8_linear_bwd_noalloc: cudaGetDevice: %s",
-                              cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices)
-        return fp8::set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd_noalloc: device %d out of range", dev);
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
+// The driver's cuCtxGetCurrent and cuCtxGetId, through the runtime's entry
+// point query (null when the driver lacks them).
+std::pair<CtxGetCurrentFn, CtxGetIdFn> ctx_fns() {
+    static CtxGetCurrentFn cur = nullptr;
+    static CtxGetIdFn id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_bwd_scratch);
-        if (e != cudaSuccess || !p)
-            return fp8::set_error(FP8_ERR_CUDA,
-                                  "fp8_linear_bwd_noalloc: cudaGetSymbolAddress: %s",
-                                  cudaGetErrorString(e));
-        g_scratch_ptr[dev] = p;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            cur = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    return {cur, id};
+}
+
+// Unique ID of the calling thread's current CUDA context, 0 if there is none
+// (or it cannot be read).  The driver never reuses an ID within a process,
+// so a context made after cudaDeviceReset, or another context made current
+// by the caller, has an ID of its own.
+unsigned long long current_ctx_id() {
+    const auto fns = ctx_fns();
+    if (!fns.first || !fns.second) return 0;
+    CUcontext ctx = nullptr;
+    if (fns.first(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    if (fns.second(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+std::mutex g_mu;
+std::vector<std::pair<unsigned long long, void*>> g_scratch_by_ctx;   // (context ID, address)
+
+// Device address of g_bwd_scratch in the current context.  The host-side
+// symbol is only a stand-in, and the module -- with the array -- is loaded
+// once per context, so the address is looked up (cudaGetSymbolAddress, with
+// the context current) on the first call in each context and kept under that
+// context's ID.
+int scratch_in_current_context(void** out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    const unsigned long long id = current_ctx_id();
+    if (id != 0) {
+        for (const auto& e : g_scratch_by_ctx)
+            if (e.first == id) {
+                *out = e.second;
+                return FP8_OK;
+            }
     }
-    *out = g_scratch_ptr[dev];
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_bwd_scratch);
+    if (e != cudaSuccess || !p)
+        return fp8::set_error(FP8_ERR_CUDA, "fp8_linear_bwd_noalloc: cudaGetSymbolAddress: %s",
+                              cudaGetErrorString(e));
+    // the lookup made the device's primary context current if none was
+    const unsigned long long id_now = id != 0 ? id : current_ctx_id();
+    if (id_now != 0) g_scratch_by_ctx.emplace_back(id_now, p);
+    *out = p;
     return FP8_OK;
 }
 
@@ -69,11 +112,12 @@ extern "C" int fp8_linear_bwd_noalloc(const void* dY, int64_t M, int64_t N, int6
                                       const fp8_recipe_t* recipe,
                                       const fp8_linear_state_t* state, void* dX, float* dW,
                                       int accumulate_dW, void* stream) {
-    // the dY operands only: this entry point computes no bias gradient (an
-    // invalid recipe sizes to 0 and is reported by fp8_linear_bwd)
-    const size_t need = fp8_workspace_size(M, N, K, recipe) == 0
-                            ? 0
-                            : fp8::bwd_operand_workspace(M, N, recipe, state);
+    // every argument check first: a call that fails them touches no device
+    // state (no context is made current, no module is loaded)
+    const int bad = fp8::check_linear_bwd_args(dY, M, N, K, recipe, state, dX, dW, nullptr);
+    if (bad != FP8_OK) return bad;
+    // the dY operands only: this entry point computes no bias gradient
+    const size_t need = fp8::bwd_operand_workspace(M, N, recipe, state);
     if (need > kScratchBytes)
         return fp8::set_error(FP8_ERR_SHAPE,
                               "fp8_linear_bwd_noalloc: M x N = %lld x %lld needs %zu bytes of "
@@ -81,7 +125,7 @@ extern "C" int fp8_linear_bwd_noalloc(const void* dY, int64_t M, int64_t N, int6
                               static_cast<long long>(M), static_cast<long long>(N), need,
                               kScratchBytes);
     void* scratch = nullptr;
-    const int st = scratch_on_current_device(&scratch);
+    const int st = scratch_in_current_context(&scratch);
     if (st != FP8_OK) return st;
     return fp8_linear_bwd(dY, M, N, K, recipe, state, dX, dW, accumulate_dW, nullptr, scratch,
                           kScratchBytes, stream);

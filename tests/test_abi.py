@@ -241,3 +241,29 @@ def test_gemm_group_argument_checks():
     odd_bias = F.GemmArgsC(one, 0, one, 0, 256, 256, 256, 0, 0, one, 0, one,
                            ctypes.c_void_p(FAKE + 2), one, 0, 0)
     assert L.fp8_gemm_group(ctypes.byref(odd_bias), ctypes.byref(good), None) == -3
+
+
+def test_noalloc_checks_arguments_before_touching_the_device():
+    """fp8_linear_bwd_noalloc validates everything before it looks up its
+    scratch array: on a machine without a GPU an invalid call still returns
+    its own status, not a CUDA error from the lookup."""
+    L = F.lib()
+    fn = L.fp8_linear_bwd_noalloc
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                   ctypes.POINTER(F.Recipe), ctypes.POINTER(F.LinearStateC), ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    p = ctypes.c_void_p(FAKE)
+    st = F.LinearStateC(*([FAKE] * len(F.LinearStateC._fields_)))
+    bad = F.Recipe(history_len=0)
+    assert fn(p, 256, 256, 256, ctypes.byref(bad), ctypes.byref(st), p, p, 0, None) == -1
+    assert fn(p, 256, 120, 256, ctypes.byref(F.Recipe()), ctypes.byref(st), p, p, 0, None) == -2
+    assert fn(p, 256, 256, 256, ctypes.byref(F.Recipe()), ctypes.byref(st),
+              ctypes.c_void_p(FAKE + 2), p, 0, None) == -3
+    blk = F.Recipe(scaling=F.SCALING_BLOCK)
+    assert fn(p, 256, 256, 256, ctypes.byref(blk), ctypes.byref(F.LinearStateC()), p, p, 0,
+              None) == -1
+    # a shape whose dY operands exceed the scratch: -2 with the limit named
+    assert fn(p, 8192, 8192, 4096, ctypes.byref(F.Recipe()), ctypes.byref(st), p, p, 0,
+              None) == -2
+    assert "scratch" in F.fp8_last_error()

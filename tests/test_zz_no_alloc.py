@@ -30,7 +30,17 @@ def _noalloc():
     return fn
 
 
+def _same_bits(got, want, what):
+    """dX (bf16) and dW (fp32) of the two entry points: the same kernels on
+    the same codes, so the same bits."""
+    ib = torch.int16 if got.dtype == torch.bfloat16 else torch.int32
+    assert torch.equal(got.view(ib), want.view(ib)), what
+
+
 def test_noalloc_backward_matches_workspace_backward():
+    """Delayed scaling over two calls with dW accumulated: the same bits as
+    fp8_linear_bwd with a workspace, and both within the GEMM bound of the
+    oracle."""
     fn = _noalloc()
     M, N, K = 512, 768, 1024
     rec = F.Recipe(F.SCALING_DELAYED, history_len=16)
@@ -54,15 +64,50 @@ def test_noalloc_backward_matches_workspace_backward():
                 dX_na.data_ptr(), dW_na.data_ptr(), int(step > 0), stream)
         assert st == 0, F.fp8_last_error()
         torch.cuda.synchronize()
+        _same_bits(dX_na, dX_ref, f"dX call {step}")
+        _same_bits(dW_na, dW_ref, f"dW call {step}")
         # tolerance of the GEMM tests: 2e-3 * sum|a b| * s_a * s_b (+ bf16 rounding)
         oracle.linear_fwd(bits(X), bits(W), orec, ost)
-        (_, dXabs), (_, dWabs) = oracle.linear_bwd(bits(dY), orec, ost)
-        assert_gemm_bound(dX_na, dX_ref.float().cpu().numpy().astype(np.float64), dXabs,
-                          what=f"dX call {step}")
-        assert_gemm_bound(dW_na, dW_ref.cpu().numpy().astype(np.float64), dWabs,
-                          what=f"dW call {step}")
+        (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(bits(dY), orec, ost)
+        assert_gemm_bound(dX_na, dXo, dXabs, what=f"dX call {step}")
+        if step == 0:
+            assert_gemm_bound(dW_na, dWo, dWabs, what="dW call 0")
         assert torch.equal(na_layer.scale, ref_layer.scale)
         assert torch.equal(na_layer.history, ref_layer.history)
+    assert F.fp8_device_status() == 0
+
+
+@pytest.mark.parametrize("mode,transposes", [
+    (F.SCALING_DELAYED, True),     # dY_q and dY_q^T: 2*M*N bytes of scratch
+    (F.SCALING_BLOCK, False),      # 1x128 dY and dY^T codes plus their scale arrays
+    (F.SCALING_ROW, False),        # per-token dY and per-channel dY^T plus their scales
+], ids=["delayed_transposed_copies", "block", "per_row"])
+def test_noalloc_matches_workspace_in_every_scratch_layout(mode, transposes):
+    """The recipes whose backward puts two dY operands (and scale arrays) in
+    the scratch: two calls in a row with dW accumulated, bit for bit the
+    workspace backward's results."""
+    fn = _noalloc()
+    M, N, K = 512, 768, 1024
+    rec = F.Recipe(mode, history_len=16)
+    ref_layer = F.Fp8Linear(M, N, K, rec, device=DEV, transposes=transposes)
+    na_layer = F.Fp8Linear(M, N, K, rec, device=DEV, transposes=transposes)
+    W = synthetic.student_t_rows((N, K), 0.02, 3, seed=8, device=DEV)
+    dW_ref = torch.zeros(N, K, dtype=torch.float32, device=DEV)
+    dW_na = torch.zeros(N, K, dtype=torch.float32, device=DEV)
+    stream = torch.cuda.current_stream().cuda_stream
+    for step in range(2):
+        X = synthetic.student_t_rows((M, K), 1.0, 3, seed=30 + step, device=DEV)
+        dY = synthetic.normal((M, N), 1e-3, seed=40 + step, device=DEV)
+        ref_layer.forward(X, W)
+        na_layer.forward(X, W)
+        dX_ref, _ = ref_layer.backward(dY, dW=dW_ref, accumulate_dW=step > 0)
+        dX_na = torch.empty(M, K, dtype=torch.bfloat16, device=DEV)
+        st = fn(dY.data_ptr(), M, N, K, ctypes.byref(rec), ctypes.byref(na_layer.c_state),
+                dX_na.data_ptr(), dW_na.data_ptr(), int(step > 0), stream)
+        assert st == 0, F.fp8_last_error()
+        torch.cuda.synchronize()
+        _same_bits(dX_na, dX_ref, f"dX call {step}")
+        _same_bits(dW_na, dW_ref, f"dW call {step}")
     assert F.fp8_device_status() == 0
 
 
@@ -103,6 +148,6 @@ def test_noalloc_takes_twice_the_tokens_without_transposed_copies():
             dX_na.data_ptr(), dW_na.data_ptr(), 0, torch.cuda.current_stream().cuda_stream)
     assert st == 0, F.fp8_last_error()
     torch.cuda.synchronize()
-    assert torch.equal(dX_na.view(torch.int16), dX_ref.view(torch.int16))
-    assert torch.equal(dW_na.view(torch.int32), dW_ref.view(torch.int32))
+    _same_bits(dX_na, dX_ref, "dX")
+    _same_bits(dW_na, dW_ref, "dW")
     assert torch.equal(na_layer.scale, ref_layer.scale)
