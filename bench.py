@@ -1,23 +1,33 @@
 """Throughput of the scaled FP8 linear layer on one GB300 (and N replicas).
 
-Workload: the Llama-2-7B-shaped linears of one transformer block, forward +
-dgrad + wgrad, per-tensor delayed scaling (amax history 16, margin 0,
-"max"): tokens M = 8192, d = 4096 -> QKV 4096x12288, O 4096x4096,
-gate/up 4096x11008, down 11008x4096; X ~ N(0,1) with outlier channels,
-W ~ N(0, 0.02^2), dY ~ N(0, (1e-3)^2); E4M3 forward operands, E5M2
-gradients, FP32 wgrad buffer.  One step = fp8_linear_fwd + fp8_linear_bwd of
-all five linears (every quantiser, GEMM and scale update of the path).
+Headline workload: the Llama-2-70B-shaped linears of one transformer block,
+forward + dgrad + wgrad, per-tensor dynamic scaling: tokens 4096 per
+micro-batch, d = 8192 -> GQA QKV 8192x10240, O 8192x8192, gate/up
+8192x28672, down 28672x8192; X ~ N(0,1) with outlier channels (1 in 256
+input columns x50), W ~ N(0, 0.02^2) bf16 master weights, dY ~ N(0, 1e-3^2);
+E4M3 weights and activations, E5M2 gradients.  One step = two micro-batches
+through fp8_linear_fwd + fp8_linear_bwd of all five linears, the FP32 dW
+buffers written by the first micro-batch and accumulated by the second (every
+amax, scale update, cast and GEMM of the path).
 
-value       = sum over linears of 6*M*N*K / step time (TFLOP/s), inputs
+value       = 2 x sum over linears of 6*M*N*K / step time (TFLOP/s), inputs
               resident in HBM, L2 flushed (256 MiB write) before each step.
-e2e         = the same through the public API with pinned host buffers:
-              H2D of X, W, dY and D2H of Y, dX, dW inside the timed region.
+e2e         = the same steps through the public API from pinned host
+              buffers: H2D of W (once per step), X and dY (per micro-batch),
+              D2H of Y and dX (per micro-batch) and dW (once per step), all
+              inside the timed region.
 roofline    = the dominant kernel (the FP8 GEMM): GEMM FLOPs / GEMM time,
               from CUDA events around each GEMM of a component-wise pass of
-              the same steps, against 2x the measured bf16 dense peak.
+              the same steps, against 2x the measured bf16 dense burst peak
+              (the FP8/BF16 nominal ratio).
 quantize    = the quantiser kernels' algorithmic bytes / their time against
               the measured HBM copy bandwidth.
 cpu_baseline= the CPU oracle on a bounded sample of the same step.
+extra keys  = the other configurations, each timed in this run: the
+              Llama-2-7B delayed-scaling step, the block-scaled GEMMs and
+              layer steps on the DeepSeek-style shapes (fp32 and power-of-two
+              block factors), points of the quantizer sweep, and the small
+              forward case.
 
 `--impl reference` times the CPU oracle (the only reference this method has)
 on the same workload; see the module docstring of oracle/.
@@ -40,14 +50,51 @@ if ROOT not in sys.path:
 
 import synthetic  # noqa: E402
 
-TOKENS = 8192
-LINEARS = [("qkv", 4096, 12288), ("o", 4096, 4096), ("gate", 4096, 11008),
-           ("up", 4096, 11008), ("down", 11008, 4096)]
-WORKLOAD = ("llama2-7b block linears fwd+dgrad+wgrad, per-tensor delayed scaling "
-            "(history 16, margin 0, max), tokens 8192")
 METRIC = "FP8 linear fwd+bwd TFLOP/s and quantize GB/s, as fraction of GB300 peak"
 FLUSH_BYTES = 256 << 20
-LAUNCHES_PER_LINEAR = 8   # this library's kernels per linear in one fwd + bwd step
+LAUNCHES_PER_LINEAR = 8   # this library's kernels per linear and micro-batch in fwd + bwd
+
+# (name, K = in-features, N = out-features)
+LINEARS_7B = [("qkv", 4096, 12288), ("o", 4096, 4096), ("gate", 4096, 11008),
+              ("up", 4096, 11008), ("down", 11008, 4096)]
+LINEARS_70B = [("qkv", 8192, 10240), ("o", 8192, 8192), ("gate", 8192, 28672),
+               ("up", 8192, 28672), ("down", 28672, 8192)]
+
+
+class Workload:
+    """One layer-step configuration: the linears of a transformer block, the
+    tokens per micro-batch, the scaling mode and the micro-batches per step
+    (with more than one, the first writes dW and the rest accumulate; with
+    one, two input sets alternate between steps and dW accumulates)."""
+
+    def __init__(self, key, tokens, linears, scaling, micro_batches, label, recipe_label):
+        self.key, self.tokens, self.linears = key, tokens, linears
+        self.scaling, self.micro_batches = scaling, micro_batches
+        self.label, self.recipe_label = label, recipe_label
+
+    def outlier_channels(self, K):
+        # 16 of 4096 input columns (43 of 11008): one in 256
+        return 43 if K == 11008 else max(1, K // 256)
+
+    def flops_step(self):
+        return self.micro_batches * sum(6.0 * self.tokens * n * k for _, k, n in self.linears)
+
+    def recipe(self, F):
+        if self.scaling == "dynamic":
+            return F.Recipe(F.SCALING_DYNAMIC)
+        return F.Recipe(F.SCALING_DELAYED, history_len=16, margin=0, amax_algo=F.AMAX_MAX)
+
+
+LLAMA70B = Workload(
+    "llama2-70b", 4096, LINEARS_70B, "dynamic", 2,
+    "llama2-70b block linears fwd+dgrad+wgrad, per-tensor dynamic scaling, tokens 4096 per "
+    "micro-batch, dW accumulated in FP32 over 2 micro-batches",
+    "HYBRID (E4M3 fwd, E5M2 grads), per-tensor dynamic (current) scaling, margin 0")
+LLAMA7B = Workload(
+    "llama2-7b", 8192, LINEARS_7B, "delayed", 1,
+    "llama2-7b block linears fwd+dgrad+wgrad, per-tensor delayed scaling (history 16, "
+    "margin 0, max), tokens 8192",
+    "HYBRID delayed, history 16, margin 0, amax max")
 
 
 def _peaks():
@@ -57,20 +104,6 @@ def _peaks():
         return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
     except Exception:
         return 6800.0, 1900.0, 1700.0, "fallback"
-
-
-def _flops_step():
-    return sum(6.0 * TOKENS * n * k for _, k, n in LINEARS)
-
-
-def _gemm_alg_bytes():
-    """Mean algorithmic DRAM bytes per GEMM launch of the step: both FP8
-    operands read once, the output written once (FP32 accumulation: read
-    and written)."""
-    tot = 0.0
-    for _, M, N, K, _, out, _ in step_gemms():
-        tot += M * K + N * K + (2 * M * N if out == "bf16" else 8 * M * N)
-    return tot / len(step_gemms())
 
 
 def _dist():
@@ -83,8 +116,9 @@ def _dist():
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, period_ms: int = 50):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
         out_dir = os.environ.get("FP8_BENCH_OUT", os.path.join(ROOT, "bench_out"))
         self.path = os.path.join(out_dir, f"clocks_rank{index}.csv")
@@ -98,7 +132,7 @@ class Clocks:
                  "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -112,7 +146,7 @@ class Clocks:
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
@@ -121,6 +155,7 @@ class Clocks:
             try:
                 sm.append(float(parts[1]))
                 mx.append(float(parts[2]))
+                pw.append(float(parts[3]))
             except ValueError:
                 continue
             for nm, v in zip(names, parts[5:9]):
@@ -129,7 +164,170 @@ class Clocks:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "period_ms": self.period_ms, "power_w_max": max(pw) if pw else None,
                 "reasons": sorted(reasons)}
+
+
+def _events(n):
+    return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(n)]
+
+
+def _median_ms(ev):
+    ms = sorted(a.elapsed_time(b) for a, b in ev)
+    return ms[len(ms) // 2], ms[0]
+
+
+# ------------------------------------------------------------ layer steps
+
+class LayerStep:
+    """The device state of one workload: a Fp8Linear per linear, bf16 master
+    weights, two sets of X and dY per linear (the two micro-batches of a
+    step, or the two input sets that alternate between single-micro-batch
+    steps), outputs and FP32 dW buffers."""
+
+    def __init__(self, F, wl: Workload, dev):
+        self.F, self.wl, self.dev = F, wl, dev
+        self.recipe = wl.recipe(F)
+        T = wl.tokens
+        self.layers, self.W, self.X, self.dY, self.Y, self.dX, self.dW = [], [], [], [], [], [], []
+        for li, (name, K, N) in enumerate(wl.linears):
+            self.layers.append(F.Fp8Linear(T, N, K, self.recipe, device=dev))
+            self.W.append(synthetic.normal((N, K), 0.02, seed=1000 + li, device=dev))
+            self.X.append([synthetic.with_outlier_channels(
+                (T, K), 1.0, wl.outlier_channels(K), 50.0, seed=10 * li + s, device=dev)
+                for s in range(2)])
+            self.dY.append([synthetic.normal((T, N), 1e-3, seed=500 + 10 * li + s, device=dev)
+                            for s in range(2)])
+            self.Y.append(torch.empty(T, N, dtype=torch.bfloat16, device=dev))
+            self.dX.append(torch.empty(T, K, dtype=torch.bfloat16, device=dev))
+            self.dW.append(torch.zeros(N, K, dtype=torch.float32, device=dev))
+
+    def passes(self, s):
+        """(input set, accumulate dW) of each micro-batch of step s."""
+        if self.wl.micro_batches == 1:
+            return [(s % 2, True)]
+        return [(mb, mb > 0) for mb in range(self.wl.micro_batches)]
+
+    def step(self, s):
+        for mb, acc in self.passes(s):
+            for li in range(len(self.wl.linears)):
+                L = self.layers[li]
+                L.forward(self.X[li][mb], self.W[li], Y=self.Y[li])
+                L.backward(self.dY[li][mb], dX=self.dX[li], dW=self.dW[li], accumulate_dW=acc)
+
+    def timed_steps(self, first, steps, flush, stream):
+        ev = _events(steps)
+        for i in range(steps):
+            flush.fill_(float(i))                   # evict L2 between steps (untimed)
+            ev[i][0].record(stream)
+            self.step(first + i)
+            ev[i][1].record(stream)
+        return ev
+
+    def component_pass(self, flush, stream, n_steps):
+        """The steps of fp8_linear_fwd/bwd issued as the individual C-ABI
+        calls (the same GEMM calls, the casts and scale updates as separate
+        public calls) with CUDA events around each call, to split the step
+        time between GEMMs, quantisers and scale updates."""
+        F, wl = self.F, self.wl
+        by_kind = {"gemm": 0.0, "quantize": 0.0, "update_scale": 0.0}
+        gemm_flops = quant_bytes = total = 0.0
+        pending = []
+        dyn = wl.scaling == "dynamic"
+        H = 1 if dyn else 16
+        algo = F.AMAX_MOST_RECENT if dyn else F.AMAX_MAX
+
+        def timed(kind, fn):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            pending.append((kind, a, b))
+
+        def cast(L, x, fmt, r, q):
+            """One role's cast as the layer's recipe does it: dynamic = amax
+            pass, scale update, cast with the new scale (5 B per element);
+            delayed = cast with the current scale and the fused amax, then the
+            update (3 B per element)."""
+            am = L.amax[r:r + 1]
+            upd = lambda: F.fp8_update_scale(am, L.history[r], L.pos[r:r + 1], H, algo, fmt, 0,
+                                             False, L.scale[r:r + 1], L.scale_inv[r:r + 1])
+            if dyn:
+                timed("quantize", lambda: F.fp8_amax(x, am))
+                timed("update_scale", upd)
+                timed("quantize", lambda: F.fp8_quantize(x, fmt, scale=L.scale[r:r + 1], q=q))
+                return 5.0 * x.numel(), None
+            timed("quantize", lambda: F.fp8_quantize(x, fmt, scale=L.scale[r:r + 1], q=q,
+                                                     amax_out=am))
+            return 3.0 * x.numel(), upd
+
+        for s in range(n_steps):
+            flush.fill_(float(s))
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for mb, acc in self.passes(s):
+                for li, (name, K, N) in enumerate(wl.linears):
+                    L = self.layers[li]
+                    M = wl.tokens
+                    X, W, dY = self.X[li][mb], self.W[li], self.dY[li][mb]
+                    bx, ux = cast(L, X, F.E4M3, 0, L.x_q)
+                    bw, uw = cast(L, W, F.E4M3, 1, L.w_q)
+                    timed("gemm", lambda: F.fp8_gemm(L.x_q, F.E4M3, L.w_q, F.E4M3,
+                                                     L.scale_inv[0:1], L.scale_inv[1:2],
+                                                     D=self.Y[li]))
+                    for u in (ux, uw):
+                        if u is not None:
+                            timed("update_scale", u)
+                    dyq = L.workspace[:M * N].view(M, N)
+                    bdy, udy = cast(L, dY, F.E5M2, 2, dyq)
+                    # dgrad and wgrad in one grouped launch, as fp8_linear_bwd
+                    # issues them: W_q, dY_q and X_q read as stored (MN-major)
+                    timed("gemm", lambda: F.fp8_gemm_group(
+                        dict(A=dyq, fa=F.E5M2, B=L.w_q, fb=F.E4M3, scale_inv_a=L.scale_inv[2:3],
+                             scale_inv_b=L.scale_inv[1:2], D=self.dX[li], layout=F.LAYOUT_B_KN),
+                        dict(A=dyq, fa=F.E5M2, B=L.x_q, fb=F.E4M3, scale_inv_a=L.scale_inv[2:3],
+                             scale_inv_b=L.scale_inv[0:1], out=F.OUT_F32, D=self.dW[li],
+                             accumulate=acc, layout=F.LAYOUT_KM_KN)))
+                    if udy is not None:
+                        timed("update_scale", udy)
+                    gemm_flops += 6.0 * M * N * K
+                    quant_bytes += bx + bw + bdy
+            t1.record(stream)
+            pending.append(("__step", t0, t1))
+        torch.cuda.synchronize()
+        for kind, a, b in pending:
+            ms = a.elapsed_time(b)
+            if kind == "__step":
+                total += ms
+            else:
+                by_kind[kind] += ms
+        return {"by_kind": by_kind, "gemm_ms": by_kind["gemm"], "quant_ms": by_kind["quantize"],
+                "gemm_flops": gemm_flops, "quant_bytes": quant_bytes, "total_ms": total,
+                "steps": n_steps}
+
+
+def gemm_alg_bytes(wl: Workload):
+    """Mean algorithmic DRAM bytes per GEMM launch of a step: both FP8
+    operands read once, the output written once (FP32 accumulation: read and
+    written)."""
+    g = step_gemms(wl)
+    return sum(M * K + N * K + (2 * M * N if out == "bf16" else 8 * M * N)
+               for _, M, N, K, _, out, _ in g) / len(g)
+
+
+def _roofline(comp, wl, bf16_burst, bf16_sust, peak_kind):
+    ach = comp["gemm_flops"] / (comp["gemm_ms"] * 1e-3) / 1e12
+    peak = 2.0 * bf16_burst
+    return {"bound": "tensor",
+            "kernel": "gemm_pair_kernel (tcgen05.mma.cta_group::2 kind::f8f6f4)",
+            "achieved": round(ach, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+            "frac": round(ach / peak, 4),
+            "peak_source": f"{peak_kind}: 2 x bf16_tflops (burst; FP8/BF16 nominal ratio 2)",
+            "frac_of_sustained": round(ach / (2.0 * bf16_sust), 4),
+            "traffic": _gemm_traffic(wl.key),
+            "traffic_unit": "DRAM bytes per GEMM launch (ncu, mean of the step's GEMM launches)",
+            "algorithmic_bytes_per_launch": round(gemm_alg_bytes(wl))}
 
 
 # ----------------------------------------------------------------- GPU arm
@@ -145,29 +343,10 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=dev)
     F.lib()
     hbm_gbs, bf16_burst, bf16_sust, peak_kind = _peaks()
-    fp8_peak = 2.0 * bf16_sust   # FP8 dense = 2x bf16 dense (nominal ratio), sustained figure
-
-    recipe = F.Recipe(F.SCALING_DELAYED, history_len=16, margin=0, amax_algo=F.AMAX_MAX)
-    layers, Ws, Xs, dYs, Ys, dXs, dWs = [], [], [], [], [], [], []
-    for li, (name, K, N) in enumerate(LINEARS):
-        layers.append(F.Fp8Linear(TOKENS, N, K, recipe, device=dev))
-        Ws.append(synthetic.normal((N, K), 0.02, seed=1000 + li, device=dev))
-        n_out = 43 if K == 11008 else 16
-        Xs.append([synthetic.with_outlier_channels((TOKENS, K), 1.0, n_out, 50.0,
-                                                    seed=10 * li + s, device=dev) for s in range(2)])
-        dYs.append([synthetic.normal((TOKENS, N), 1e-3, seed=500 + 10 * li + s, device=dev)
-                    for s in range(2)])
-        Ys.append(torch.empty(TOKENS, N, dtype=torch.bfloat16, device=dev))
-        dXs.append(torch.empty(TOKENS, K, dtype=torch.bfloat16, device=dev))
-        dWs.append(torch.zeros(N, K, dtype=torch.float32, device=dev))
+    wl = LLAMA70B
+    run = LayerStep(F, wl, dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-
-    def step(s):
-        for li in range(len(LINEARS)):
-            L = layers[li]
-            L.forward(Xs[li][s % 2], Ws[li], Y=Ys[li])
-            L.backward(dYs[li][s % 2], dX=dXs[li], dW=dWs[li], accumulate_dW=True)
 
     def barrier():
         if world > 1:
@@ -176,155 +355,208 @@ def run_gpu(args):
         torch.cuda.synchronize()
 
     for s in range(args.warmup):
-        step(s)
+        run.step(s)
     barrier()
 
     clocks = Clocks(local)
     clocks.start()
     time.sleep(0.5)                                 # let the sampler start before the region
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     barrier()
-    for s in range(args.steps):
-        flush.fill_(float(s))                       # evict L2 between steps (untimed)
-        ev[s][0].record(stream)
-        step(args.warmup + s)
-        ev[s][1].record(stream)
+    ev = run.timed_steps(args.warmup, args.steps, flush, stream)
     barrier()
-    ms = [a.elapsed_time(b) for a, b in ev]
     clk = clocks.stop()
+    ms = [a.elapsed_time(b) for a, b in ev]
     assert F.fp8_device_status() == 0, "a kernel reported a timeout"
     t_ms = sum(ms)
     if world > 1:
         from scaled_fp8_linear_gb300.distributed import max_over_ranks
         t_ms = max_over_ranks(t_ms, device=dev)
-    flops = _flops_step() * args.steps * world
+    flops = wl.flops_step() * args.steps * world
     value = flops / (t_ms * 1e-3) / 1e12
 
     # component-wise pass of the same steps: events around each kernel group
-    comp = component_pass(F, layers, Xs, dYs, Ws, Ys, dXs, dWs, flush, args, stream)
+    comp = run.component_pass(flush, stream, min(args.steps, 10))
+    del run
+    torch.cuda.empty_cache()
 
-    e2e = e2e_pass(F, recipe, dev, args, stream) if rank == 0 else None
-    small = small_case_pass(F, dev, stream) if rank == 0 else None
+    e2e = e2e_pass(F, wl, dev, args, stream) if rank == 0 else None
+    extras = {}
+    if rank == 0 and not args.no_extras:
+        extras["llama2_7b_delayed_step"] = extra_layer_step(F, LLAMA7B, dev, flush, stream,
+                                                            bf16_burst, bf16_sust, hbm_gbs,
+                                                            peak_kind)
+        extras["block_scaled"] = extra_block_scaled(F, dev, flush, stream, bf16_burst)
+        extras["quantize_sweep"] = extra_quantize_points(F, dev, flush, stream, hbm_gbs)
+        extras["small_case"] = small_case_pass(F, dev, stream)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
 
     if rank != 0:
         return
-    gemm_tflops = comp["gemm_flops"] / (comp["gemm_ms"] * 1e-3) / 1e12
     quant_gbs = comp["quant_bytes"] / (comp["quant_ms"] * 1e-3) / 1e9
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_ms / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8(e4m3/e5m2)xfp8->fp32acc", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens": TOKENS,
-                   "linears": {n: [k, n_] for n, k, n_ in LINEARS},
-                   "recipe": "HYBRID delayed, history 16, margin 0, amax max",
+        "config": {"workload": wl.label, "tokens_per_micro_batch": wl.tokens,
+                   "micro_batches_per_step": wl.micro_batches,
+                   "linears": {n: [k, n_] for n, k, n_ in wl.linears},
+                   "recipe": wl.recipe_label,
                    "backward_operands": "forward codes read MN-major (no transposed copies)",
-                   "l2": "flushed (256 MiB write) before every timed step",
+                   "l2": "flushed (256 MiB write) before every timed step; inputs larger than L2",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
-        "roofline": {"bound": "tensor", "kernel": "gemm_pair_kernel (tcgen05.mma.cta_group::2 kind::f8f6f4)",
-                     "achieved": round(gemm_tflops, 1), "peak": round(fp8_peak, 1),
-                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
-                     "peak_source": f"{peak_kind}: 2 x bf16_tflops_sustained (FP8/BF16 nominal 2x)",
-                     "traffic": _gemm_traffic(),
-                     "traffic_unit": "DRAM bytes per GEMM launch (ncu, mean of the step's 15)",
-                     "algorithmic_bytes_per_launch": round(_gemm_alg_bytes())},
+        "roofline": _roofline(comp, wl, bf16_burst, bf16_sust, peak_kind),
         "quantize": {"achieved_gbs": round(quant_gbs, 1), "peak_gbs": hbm_gbs,
-                     "frac": round(quant_gbs / hbm_gbs, 4), "peak_source": f"{peak_kind} hbm_gbs"},
+                     "frac": round(quant_gbs / hbm_gbs, 4), "peak_source": f"{peak_kind} hbm_gbs",
+                     "bytes_per_element": "5 (dynamic: amax read 2, cast read 2 + write 1)"},
         "kernels_ms_per_step": {k: round(v / comp["steps"], 4) for k, v in comp["by_kind"].items()},
         "component_pass_ms_per_step": round(comp["total_ms"] / comp["steps"], 4),
-        # per linear and step: forward = amax zeroing, X and W cast (one launch),
-        # GEMM, X/W scale update; backward = amax zeroing, dY cast, grouped
-        # dgrad + wgrad GEMM, dY scale update (the ncu launch list agrees)
-        "gpu_launches": LAUNCHES_PER_LINEAR * len(LINEARS) * args.steps,
+        # per linear and micro-batch: forward = amax zeroing, X and W amax (one
+        # launch), X and W cast with the fused scale update (one launch), GEMM;
+        # backward = amax zeroing, dY amax, dY cast with the fused update,
+        # grouped dgrad + wgrad GEMM
+        "gpu_launches": LAUNCHES_PER_LINEAR * len(wl.linears) * wl.micro_batches * args.steps,
         "e2e": e2e,
-        "small_case": small,
         "clocks": clk,
+        **extras,
     }
     if not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args)
+        out["cpu_baseline"] = cpu_baseline(args, run_dev=dev)
     print(json.dumps(out))
 
 
-def component_pass(F, layers, Xs, dYs, Ws, Ys, dXs, dWs, flush, args, stream):
-    """The steps of fp8_linear_fwd/bwd issued as the individual C-ABI calls
-    (same kernels, same order) with CUDA events around each call, to split
-    the step time between GEMMs, quantisers and scale updates."""
-    by_kind = {"gemm": 0.0, "quantize": 0.0, "update_scale": 0.0}
-    gemm_flops = quant_bytes = 0.0
-    total = 0.0
-    pending = []
-
-    def timed(kind, fn):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        fn()
-        b.record(stream)
-        pending.append((kind, a, b))
-
-    n_steps = min(args.steps, 20)
-    for s in range(n_steps):
-        flush.fill_(float(s))
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for li, (name, K, N) in enumerate(LINEARS):
-            L = layers[li]
-            M = TOKENS
-            X, W, dY = Xs[li][s % 2], Ws[li], dYs[li][s % 2]
-            am = L.amax
-            tr = L.x_qt is not None   # transposed copies kept: K-major backward operands
-            timed("quantize", lambda: F.fp8_quantize(X, F.E4M3, scale=L.scale[0:1], q=L.x_q,
-                                                     q_t=L.x_qt, amax_out=am[0:1]))
-            timed("quantize", lambda: F.fp8_quantize(W, F.E4M3, scale=L.scale[1:2], q=L.w_q,
-                                                     q_t=L.w_qt, amax_out=am[1:2]))
-            timed("gemm", lambda: F.fp8_gemm(L.x_q, F.E4M3, L.w_q, F.E4M3, L.scale_inv[0:1],
-                                             L.scale_inv[1:2], D=Ys[li]))
-            timed("update_scale", lambda: [F.fp8_update_scale(
-                am[r:r + 1], L.history[r], L.pos[r:r + 1], 16, F.AMAX_MAX, F.E4M3, 0, False,
-                L.scale[r:r + 1], L.scale_inv[r:r + 1]) for r in (0, 1)])
-            dyq = L.workspace[:M * N].view(M, N)
-            off = (M * N + 255) // 256 * 256          # dY_q^T follows dY_q, 256-byte aligned
-            dyqt = L.workspace[off:off + M * N].view(N, M) if tr else None
-            timed("quantize", lambda: F.fp8_quantize(dY, F.E5M2, scale=L.scale[2:3], q=dyq,
-                                                     q_t=dyqt, amax_out=am[2:3]))
-            # dgrad and wgrad in one grouped launch, as fp8_linear_bwd issues them:
-            # without transposed copies they read W_q, dY_q and X_q as stored
-            timed("gemm", lambda: F.fp8_gemm_group(
-                dict(A=dyq, fa=F.E5M2, B=L.w_qt if tr else L.w_q, fb=F.E4M3,
-                     scale_inv_a=L.scale_inv[2:3], scale_inv_b=L.scale_inv[1:2], D=dXs[li],
-                     layout=F.LAYOUT_TN if tr else F.LAYOUT_B_KN),
-                dict(A=dyqt if tr else dyq, fa=F.E5M2, B=L.x_qt if tr else L.x_q, fb=F.E4M3,
-                     scale_inv_a=L.scale_inv[2:3], scale_inv_b=L.scale_inv[0:1], out=F.OUT_F32,
-                     D=dWs[li], accumulate=True,
-                     layout=F.LAYOUT_TN if tr else F.LAYOUT_KM_KN)))
-            timed("update_scale", lambda: F.fp8_update_scale(
-                am[2:3], L.history[2], L.pos[2:3], 16, F.AMAX_MAX, F.E5M2, 0, False,
-                L.scale[2:3], L.scale_inv[2:3]))
-            gemm_flops += 6.0 * M * N * K
-            # quantiser bytes: bf16 read (2 B) + q write (1 B) (+ q_t write (1 B)) per element
-            quant_bytes += (4.0 if tr else 3.0) * (M * K + N * K + M * N)
-        t1.record(stream)
-        pending.append(("__step", t0, t1))
+def extra_layer_step(F, wl, dev, flush, stream, bf16_burst, bf16_sust, hbm_gbs, peak_kind,
+                     steps=30, warmup=3):
+    """A second layer-step configuration timed like the headline (its own
+    component pass for the GEMM and quantiser rates)."""
+    run = LayerStep(F, wl, dev)
+    for s in range(warmup):
+        run.step(s)
     torch.cuda.synchronize()
-    for kind, a, b in pending:
-        ms = a.elapsed_time(b)
-        if kind == "__step":
-            total += ms
-        else:
-            by_kind[kind] += ms
-    return {"by_kind": by_kind, "gemm_ms": by_kind["gemm"], "quant_ms": by_kind["quantize"],
-            "gemm_flops": gemm_flops, "quant_bytes": quant_bytes, "total_ms": total,
-            "steps": n_steps}
+    ev = run.timed_steps(warmup, steps, flush, stream)
+    torch.cuda.synchronize()
+    t_ms = sum(a.elapsed_time(b) for a, b in ev)
+    comp = run.component_pass(flush, stream, 10)
+    assert F.fp8_device_status() == 0
+    del run
+    torch.cuda.empty_cache()
+    quant_gbs = comp["quant_bytes"] / (comp["quant_ms"] * 1e-3) / 1e9
+    return {"workload": wl.label, "steps": steps, "ms_per_step": round(t_ms / steps, 4),
+            "value": round(wl.flops_step() * steps / (t_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+            "roofline": _roofline(comp, wl, bf16_burst, bf16_sust, peak_kind),
+            "quantize": {"achieved_gbs": round(quant_gbs, 1),
+                         "frac": round(quant_gbs / hbm_gbs, 4),
+                         "bytes_per_element": "3 (cast with fused amax: read 2 + write 1)"},
+            "kernels_ms_per_step": {k: round(v / comp["steps"], 4)
+                                    for k, v in comp["by_kind"].items()}}
+
+
+BLOCK_SHAPES = [(16384, 18432, 7168), (16384, 7168, 18432)]
+
+
+def extra_block_scaled(F, dev, flush, stream, bf16_burst, iters=10, warmup=3):
+    """The block-scaled configuration (1x128 activation and 128x128 weight
+    tiles) on both DeepSeek-style shapes, fp32 and power-of-two block
+    factors: the forward GEMM alone on the layer's own codes and scales, and
+    the whole layer step (casts, forward, dgrad, wgrad with dW accumulated).
+    Inputs: rows scaled by |t_3|."""
+    peak = 2.0 * bf16_burst
+    out = []
+    for M, N, K in BLOCK_SHAPES:
+        X = synthetic.student_t_rows((M, K), 1.0, 3, seed=1, device=dev)
+        W = synthetic.student_t_rows((N, K), 0.02, 3, seed=2, device=dev)
+        dY = synthetic.normal((M, N), 1e-3, seed=3, device=dev)
+        Y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        dX = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        dW = torch.zeros(N, K, dtype=torch.float32, device=dev)
+        for pow2 in (False, True):
+            layer = F.Fp8Linear(M, N, K, F.Recipe(F.SCALING_BLOCK, pow2=pow2), device=dev)
+            p2 = F.SCALE_POW2 if pow2 else 0
+            gemm = lambda: F.fp8_gemm(layer.x_q, F.E4M3, layer.w_q, F.E4M3, layer.x_sinv,
+                                      layer.w_sinv, F.GRAN_1x128 | p2, F.GRAN_128x128 | p2, D=Y)
+
+            def step():
+                layer.forward(X, W, Y=Y)
+                layer.backward(dY, dX=dX, dW=dW, accumulate_dW=True)
+
+            res = {"shape": [M, N, K],
+                   "factors": "power of two (block-scaled MMA)" if pow2 else
+                              "fp32 (per-128-K promotion)"}
+            for name, fn, work in (("step", step, 6.0 * M * N * K), ("gemm", gemm, 2.0 * M * N * K)):
+                for _ in range(warmup):
+                    fn()
+                ev = _events(iters)
+                for i in range(iters):
+                    flush.fill_(float(i))
+                    ev[i][0].record(stream)
+                    fn()
+                    ev[i][1].record(stream)
+                torch.cuda.synchronize()
+                med, _ = _median_ms(ev)
+                ach = work / (med * 1e-3) / 1e12
+                res[name] = {"median_ms": round(med, 4), "achieved": round(ach, 1),
+                             "unit": "TFLOP/s"}
+                if name == "gemm":
+                    res[name].update({"kernel": "gemm_mx_kernel" if pow2 else "gemm_block_kernel",
+                                      "peak": round(peak, 1), "frac": round(ach / peak, 4)})
+                else:
+                    res[name]["work"] = "6 M N K; casts included"
+            out.append(res)
+            del layer
+        del X, W, dY, Y, dX, dW
+        torch.cuda.empty_cache()
+    assert F.fp8_device_status() == 0
+    return {"iters": iters, "l2": "flushed before every launch / step",
+            "peak_source": "2 x bf16_tflops (burst)", "cases": out}
+
+
+def extra_quantize_points(F, dev, flush, stream, hbm_gbs, iters=10, warmup=3):
+    """Points of the quantizer sweep: n = 2^26, 2^28, 2^30 bf16 elements as
+    [n/8192 x 8192], t_3-distributed values, E4M3 and E5M2, with and without
+    the fused transpose; a fixed (stale) scale with the fused amax, i.e. one
+    pass of 3 (4 with the transpose) algorithmic bytes per element."""
+    out = []
+    for log2n in (26, 28, 30):
+        n = 1 << log2n
+        rows, width = n // 8192, 8192
+        x = synthetic.student_t((rows, width), 3, 1.0, seed=log2n, device=dev)
+        q = torch.empty(rows, width, dtype=torch.uint8, device=dev)
+        qt = torch.empty(width, rows, dtype=torch.uint8, device=dev)
+        am = torch.empty(1, dtype=torch.float32, device=dev)
+        scale = torch.ones(1, dtype=torch.float32, device=dev)
+        for fname, fmt in (("e4m3", F.E4M3), ("e5m2", F.E5M2)):
+            for transpose in (False, True):
+                qt_arg = qt if transpose else None
+                call = lambda: F.fp8_quantize(x, fmt, scale=scale, q=q, q_t=qt_arg, amax_out=am)
+                for _ in range(warmup):
+                    call()
+                ev = _events(iters)
+                for i in range(iters):
+                    flush.fill_(float(i))
+                    ev[i][0].record(stream)
+                    call()
+                    ev[i][1].record(stream)
+                torch.cuda.synchronize()
+                med, _ = _median_ms(ev)
+                per_elem = 4 if transpose else 3
+                gbs = per_elem * n / (med * 1e-3) / 1e9
+                out.append({"log2_elements": log2n, "shape": [rows, width], "format": fname,
+                            "transpose": transpose, "median_ms": round(med, 4),
+                            "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm_gbs, 4)})
+        del x, q, qt
+        torch.cuda.empty_cache()
+    assert F.fp8_device_status() == 0
+    return {"mode": "stale scale, fused amax", "iters": iters,
+            "l2": "flushed before every launch", "peak_gbs": hbm_gbs, "points": out}
 
 
 def small_case_pass(F, dev, stream, iters=200):
     """The small forward case (X 256 x 512 with outliers, W 512 x 512, dynamic
     scaling): latency of fp8_linear_fwd and of fwd + bwd, issued eagerly and
     replayed from a CUDA graph of the same calls.  Launch-bound at this size
-    (~12 launches per fwd + bwd), so it reports microseconds, not a roofline."""
+    (8 launches per fwd + bwd), so it reports microseconds, not a roofline."""
     M, K, N = 256, 512, 512
     layer = F.Fp8Linear(M, N, K, F.Recipe(F.SCALING_DYNAMIC), device=dev)
     X = synthetic.with_outlier_entries((M, K), 1.0, 0.001, 50.0, seed=0, device=dev)
@@ -375,120 +607,135 @@ def small_case_pass(F, dev, stream, iters=200):
     return out
 
 
-def e2e_pass(F, recipe, dev, args, stream):
-    """Public API with host buffers.  Per step and linear: H2D of X, W, dY from
-    pinned memory, fp8_linear_fwd + fp8_linear_bwd, D2H of Y, dX, dW -- all
-    inside the timed region.  Copies run on their own streams so that the
-    next linear's inputs arrive and the previous one's results leave while
-    the current linear computes (two device buffer sets, event-ordered,
-    pipelined across step boundaries as a training loop would be)."""
-    nl = len(LINEARS)
-    h_in, h_out, layers = [], [], []
-    for li, (name, K, N) in enumerate(LINEARS):
-        n_out = 43 if K == 11008 else 16
-        h_in.append((synthetic.with_outlier_channels((TOKENS, K), 1.0, n_out, 50.0, seed=li).pin_memory(),
-                     synthetic.normal((N, K), 0.02, seed=1000 + li).pin_memory(),
-                     synthetic.normal((TOKENS, N), 1e-3, seed=500 + li).pin_memory()))
-        h_out.append((torch.empty(TOKENS, N, dtype=torch.bfloat16).pin_memory(),
-                      torch.empty(TOKENS, K, dtype=torch.bfloat16).pin_memory(),
-                      torch.empty(N, K, dtype=torch.float32).pin_memory()))
-        layers.append(F.Fp8Linear(TOKENS, N, K, recipe, device=dev))
-    kmax = max(k for _, k, _ in LINEARS)
-    nmax = max(n for _, _, n in LINEARS)
-    nk = max(n * k for _, k, n in LINEARS)
+def e2e_pass(F, wl: Workload, dev, args, stream):
+    """Public API with host buffers.  Per step: H2D of each linear's W once,
+    and per micro-batch of its X and dY, from pinned memory;
+    fp8_linear_fwd + fp8_linear_bwd; D2H of Y and dX per micro-batch and of
+    dW once the last micro-batch has accumulated into it -- all inside the
+    timed region.  Copies run on their own streams so that the next unit's
+    inputs arrive and the previous one's results leave while the current
+    unit computes (two device buffer sets for X, dY, Y, dX; per-linear W and
+    dW buffers; event-ordered and pipelined across steps as a training loop
+    would be)."""
+    nl, MB, T = len(wl.linears), wl.micro_batches, wl.tokens
+    recipe = wl.recipe(F)
+    h_w, h_x, h_dy, h_y, h_dx, h_dw, layers = [], [], [], [], [], [], []
+    for li, (name, K, N) in enumerate(wl.linears):
+        h_w.append(synthetic.normal((N, K), 0.02, seed=1000 + li, device=dev).cpu().pin_memory())
+        h_x.append([synthetic.with_outlier_channels((T, K), 1.0, wl.outlier_channels(K), 50.0,
+                                                    seed=10 * li + mb, device=dev).cpu().pin_memory()
+                    for mb in range(MB)])
+        h_dy.append([synthetic.normal((T, N), 1e-3, seed=500 + 10 * li + mb,
+                                      device=dev).cpu().pin_memory() for mb in range(MB)])
+        h_y.append([torch.empty(T, N, dtype=torch.bfloat16).pin_memory() for _ in range(MB)])
+        h_dx.append([torch.empty(T, K, dtype=torch.bfloat16).pin_memory() for _ in range(MB)])
+        h_dw.append(torch.empty(N, K, dtype=torch.float32).pin_memory())
+        layers.append(F.Fp8Linear(T, N, K, recipe, device=dev))
+    kmax = max(k for _, k, _ in wl.linears)
+    nmax = max(n for _, _, n in wl.linears)
+    d_w = [torch.empty(n, k, dtype=torch.bfloat16, device=dev) for _, k, n in wl.linears]
+    d_dw = [torch.empty(n, k, dtype=torch.float32, device=dev) for _, k, n in wl.linears]
 
     def dbuf():
-        return {"X": torch.empty(TOKENS * kmax, dtype=torch.bfloat16, device=dev),
-                "W": torch.empty(nk, dtype=torch.bfloat16, device=dev),
-                "dY": torch.empty(TOKENS * nmax, dtype=torch.bfloat16, device=dev),
-                "Y": torch.empty(TOKENS * nmax, dtype=torch.bfloat16, device=dev),
-                "dX": torch.empty(TOKENS * kmax, dtype=torch.bfloat16, device=dev),
-                "dW": torch.empty(nk, dtype=torch.float32, device=dev)}
+        return {"X": torch.empty(T * kmax, dtype=torch.bfloat16, device=dev),
+                "dY": torch.empty(T * nmax, dtype=torch.bfloat16, device=dev),
+                "Y": torch.empty(T * nmax, dtype=torch.bfloat16, device=dev),
+                "dX": torch.empty(T * kmax, dtype=torch.bfloat16, device=dev)}
 
     bufs = [dbuf(), dbuf()]
     h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    h2d = sum(t.numel() * t.element_size() for tr in h_in for t in tr)
-    d2h = sum(t.numel() * t.element_size() for tr in h_out for t in tr)
-    # Linears are numbered across steps (g = step * 5 + li) and alternate
-    # between the two device buffer sets, so the loads of the next linear
-    # (also across a step boundary) and the drains of the previous one run on
-    # the host link while the current one computes.  Each copy waits only for
-    # the last user of its own buffer set.
-    computed, drained = {}, {}
+    nbytes = lambda t: t.numel() * t.element_size()
+    h2d = sum(nbytes(w) for w in h_w) + sum(nbytes(t) for ts in h_x + h_dy for t in ts)
+    d2h = sum(nbytes(t) for ts in h_y + h_dx for t in ts) + sum(nbytes(t) for t in h_dw)
+    # Units g = (step * MB + mb) * nl + li alternate between the two device
+    # buffer sets, so the loads of the next unit (also across a step
+    # boundary) and the drains of the previous one run on the host link while
+    # the current one computes.  Each copy waits only for the last user of
+    # its own buffer.
+    computed, drained, w_used, dw_drained = {}, {}, {}, {}
     counter = [0]
 
-    def run_linear():
+    def load_unit():
         g = counter[0]
         counter[0] += 1
-        li = g % nl
-        _, K, N = LINEARS[li]
+        li, mb = g % nl, (g // nl) % MB
+        _, K, N = wl.linears[li]
         b = bufs[g % 2]
         loaded = torch.cuda.Event()
         with torch.cuda.stream(h2d_s):
             if g - 2 in computed:
                 h2d_s.wait_event(computed.pop(g - 2))      # last reader of this set's inputs
-            hx, hw, hdy = h_in[li]
-            b["X"][:TOKENS * K].view(TOKENS, K).copy_(hx, non_blocking=True)
-            b["W"][:N * K].view(N, K).copy_(hw, non_blocking=True)
-            b["dY"][:TOKENS * N].view(TOKENS, N).copy_(hdy, non_blocking=True)
+            if mb == 0:
+                if li in w_used:
+                    h2d_s.wait_event(w_used.pop(li))       # last forward that read W[li]
+                d_w[li].copy_(h_w[li], non_blocking=True)
+            b["X"][:T * K].view(T, K).copy_(h_x[li][mb], non_blocking=True)
+            b["dY"][:T * N].view(T, N).copy_(h_dy[li][mb], non_blocking=True)
             loaded.record(h2d_s)
-        return g, li, K, N, b, loaded
+        return g, li, mb, K, N, b, loaded
 
-    def compute_and_drain(g, li, K, N, b, loaded):
+    def compute_and_drain(g, li, mb, K, N, b, loaded):
         stream.wait_event(loaded)
         if g - 2 in drained:
             stream.wait_event(drained.pop(g - 2))          # this set's outputs have left
-        Y = b["Y"][:TOKENS * N].view(TOKENS, N)
-        dX = b["dX"][:TOKENS * K].view(TOKENS, K)
-        dW = b["dW"][:N * K].view(N, K)
+        if mb == 0 and li in dw_drained:
+            stream.wait_event(dw_drained.pop(li))          # last step's dW[li] has left
+        Y = b["Y"][:T * N].view(T, N)
+        dX = b["dX"][:T * K].view(T, K)
         L = layers[li]
-        hy, hdx, hdw = h_out[li]
-        L.forward(b["X"][:TOKENS * K].view(TOKENS, K), b["W"][:N * K].view(N, K), Y=Y)
+        L.forward(b["X"][:T * K].view(T, K), d_w[li], Y=Y)
         fwd_done = torch.cuda.Event()
         fwd_done.record(stream)
+        if mb == MB - 1:
+            w_used[li] = fwd_done
         with torch.cuda.stream(d2h_s):                     # Y leaves while the backward runs
             d2h_s.wait_event(fwd_done)
-            hy.copy_(Y, non_blocking=True)
-        L.backward(b["dY"][:TOKENS * N].view(TOKENS, N), dX=dX, dW=dW, accumulate_dW=False)
+            h_y[li][mb].copy_(Y, non_blocking=True)
+        L.backward(b["dY"][:T * N].view(T, N), dX=dX, dW=d_dw[li], accumulate_dW=mb > 0)
         ev = torch.cuda.Event()
         ev.record(stream)
         computed[g] = ev
         with torch.cuda.stream(d2h_s):
             d2h_s.wait_event(ev)
-            hdx.copy_(dX, non_blocking=True)
-            hdw.copy_(dW, non_blocking=True)
-            dev_ev = torch.cuda.Event()
-            dev_ev.record(d2h_s)
-            drained[g] = dev_ev
+            h_dx[li][mb].copy_(dX, non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(d2h_s)
+            drained[g] = done
+            if mb == MB - 1:
+                h_dw[li].copy_(d_dw[li], non_blocking=True)
+                dwd = torch.cuda.Event()
+                dwd.record(d2h_s)
+                dw_drained[li] = dwd
 
     def steps(k):
-        """k steps, issued one linear ahead on the load stream."""
+        """k steps, issued one unit ahead on the load stream."""
         h2d_s.wait_stream(stream)                          # copies start after the start event
         d2h_s.wait_stream(stream)
-        pending = run_linear()
-        for i in range(k * nl):
-            nxt = run_linear() if i + 1 < k * nl else None
+        pending = load_unit()
+        for i in range(k * MB * nl):
+            nxt = load_unit() if i + 1 < k * MB * nl else None
             compute_and_drain(*pending)
             pending = nxt
         stream.wait_stream(d2h_s)                          # the last results are on the host
         stream.wait_stream(h2d_s)
 
-    steps(max(1, min(args.warmup, 3)))
+    steps(max(1, min(args.warmup, 2)))
     torch.cuda.synchronize()
-    n = max(1, min(args.steps, 30))
+    n = max(1, min(args.steps, 10))
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     steps(n)
     b.record(stream)
     torch.cuda.synchronize()
+    assert F.fp8_device_status() == 0
     ms = a.elapsed_time(b) / n
     link = _host_link(dev)
     floor_ms = _link_floor_ms(h2d, d2h, link)
-    return {"value": round(_flops_step() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    return {"value": round(wl.flops_step() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "steps": n, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "copies": "pinned host <-> device on two copy streams, overlapped with compute and "
-                      "with each other across linears and steps",
+                      "with each other across linears, micro-batches and steps",
             "host_link": link,
             "link_floor_ms": round(floor_ms, 3),
             "link_floor_note": "the time to move h2d and d2h bytes at the link rates measured "
@@ -567,53 +814,66 @@ def _host_link(dev, mib=1024, reps=3):
 
 # ------------------------------------------------------------- CPU oracle
 
-def _oracle_sample_step(rows_per_gemm, inputs, states, linears=None):
-    """One step of the oracle on a bounded sample: whole-tensor amax, scale
-    update and quantisation of X, W, dY for every linear in `linears` (all
-    five by default; the oracle's linear_fwd / linear_bwd), and
-    `rows_per_gemm` full output rows of each of their GEMMs.  Returns the
-    FLOPs of the sampled GEMM rows."""
-    import numpy as np
+def _oracle_inputs(wl: Workload, linears, device="cpu"):
+    """Bit patterns of micro-batch 0's X, W and dY for the listed linears,
+    drawn as the GPU arm draws them (same generators and seeds; on `device`,
+    then copied to the host)."""
     import oracle
-    flops = 0.0
-    for li, (name, K, N) in enumerate(LINEARS):
-        if linears is not None and li not in linears:
-            continue
-        bx, bw, bdy = inputs[li]
-        st, rec = states[li]
-        rows = np.arange(rows_per_gemm)
-        oracle.linear_fwd(bx, bw, rec, st, rows=rows)
-        oracle.linear_bwd(bdy, rec, st, rows_dx=rows, rows_dw=rows)
-        flops += 2.0 * rows_per_gemm * (N * K + K * N + K * TOKENS)
-    return flops
-
-
-def _oracle_inputs():
-    import oracle
-    inputs, states = [], []
-    rec = oracle.Recipe(scaling=oracle.SCALING_DELAYED, history_len=16)
-    for li, (name, K, N) in enumerate(LINEARS):
-        n_out = 43 if K == 11008 else 16
-        X = synthetic.with_outlier_channels((TOKENS, K), 1.0, n_out, 50.0, seed=10 * li)
-        W = synthetic.normal((N, K), 0.02, seed=1000 + li)
-        dY = synthetic.normal((TOKENS, N), 1e-3, seed=500 + 10 * li)
-        inputs.append((synthetic.bf16_bits(X), synthetic.bf16_bits(W), synthetic.bf16_bits(dY)))
-        states.append((oracle.LinearState(rec), rec))
+    inputs, states = {}, {}
+    rec = (oracle.Recipe(scaling=oracle.SCALING_DYNAMIC) if wl.scaling == "dynamic"
+           else oracle.Recipe(scaling=oracle.SCALING_DELAYED, history_len=16))
+    for li in linears:
+        _, K, N = wl.linears[li]
+        X = synthetic.with_outlier_channels((wl.tokens, K), 1.0, wl.outlier_channels(K), 50.0,
+                                            seed=10 * li, device=device)
+        W = synthetic.normal((N, K), 0.02, seed=1000 + li, device=device)
+        dY = synthetic.normal((wl.tokens, N), 1e-3, seed=500 + 10 * li, device=device)
+        inputs[li] = (synthetic.bf16_bits(X), synthetic.bf16_bits(W), synthetic.bf16_bits(dY))
+        states[li] = (oracle.LinearState(rec), rec)
     return inputs, states
 
 
-def cpu_baseline(args):
+def _oracle_unit(wl, li, rows, inputs, states, half=None):
+    """The oracle's fwd + bwd of one linear (its linear_fwd / linear_bwd):
+    whole-tensor amax, scale update and quantisation (with the transposed
+    copies) of X, W and dY, and `rows` full output rows of each of the three
+    GEMMs (fp64 accumulation).  half = "fwd" or "bwd" runs one of the two
+    passes (the backward uses the state the last forward of this linear
+    left).  Returns the FLOPs of the sampled rows."""
+    import numpy as np
     import oracle
-    inputs, states = _oracle_inputs()
+    _, K, N = wl.linears[li]
+    bx, bw, bdy = inputs[li]
+    st, rec = states[li]
+    r = np.arange(rows)
+    flops = 0.0
+    if half in (None, "fwd"):
+        oracle.linear_fwd(bx, bw, rec, st, rows=r)
+        flops += 2.0 * rows * N * K
+    if half in (None, "bwd"):
+        oracle.linear_bwd(bdy, rec, st, rows_dx=r, rows_dw=r)
+        flops += 2.0 * rows * (K * N + K * wl.tokens)
+    return flops
+
+
+def cpu_baseline(args, run_dev=None):
+    """The oracle as it stands, on the host cores, on one bounded sample of
+    the headline step: micro-batch 0 of all five linears with `--cpu-rows`
+    output rows per GEMM (inputs drawn on the GPU with the GPU arm's seeds)."""
+    import oracle
+    wl = LLAMA70B
+    lis = list(range(len(wl.linears)))
+    inputs, states = _oracle_inputs(wl, lis, device=run_dev or "cpu")
     rows = args.cpu_rows
     t0 = time.perf_counter()
-    flops = _oracle_sample_step(rows, inputs, states)
+    flops = sum(_oracle_unit(wl, li, rows, inputs, states) for li in lis)
     dt = time.perf_counter() - t0
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle", "seconds": round(dt, 2),
-            "sample": (f"one step: whole-tensor amax/scale/quantise(+transpose) of X, W, dY of the "
-                       f"5 linears, and {rows} full output rows of each of the 15 GEMMs "
-                       f"(fp64 accumulation); value = sampled GEMM FLOPs / wall time")}
+            "sample": (f"micro-batch 0 of the step (half of it): whole-tensor amax/scale/"
+                       f"quantise(+transpose) of X, W, dY of the 5 linears, and {rows} full "
+                       f"output rows of each of their 15 GEMMs (fp64 accumulation); value = "
+                       f"sampled GEMM FLOPs / wall time")}
 
 
 def run_reference(args):
@@ -621,32 +881,42 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    inputs, states = _oracle_inputs()
+    wl = LLAMA70B
+    nl = len(wl.linears)
     rows = args.ref_rows
-    # a step over all five linears takes seconds on the host cores; beyond 20
-    # steps each step samples one linear, in turn, so that the whole run
-    # stays within a few minutes
-    per_step = len(LINEARS) if args.steps + args.warmup <= 20 else 1
-    pick = lambda i: None if per_step == len(LINEARS) else {i % len(LINEARS)}
+    # one linear's fwd + bwd takes seconds on the host cores: short runs take
+    # all five linears per step; longer ones one half (the forward or the
+    # backward) of one linear per step, in turn, so that the whole run stays
+    # within a few minutes
+    short = args.steps + args.warmup <= 10
+    seq = [(li, h) for li in range(nl) for h in ("fwd", "bwd")]
+    units = (lambda i: [(li, None) for li in range(nl)]) if short else (lambda i: [seq[i % len(seq)]])
+    inputs, states = _oracle_inputs(wl, list(range(nl)))
+    for li in range(nl):        # every linear's state exists before a backward half runs
+        _oracle_unit(wl, li, 1, inputs, states, "fwd")
     for i in range(args.warmup):
-        _oracle_sample_step(rows, inputs, states, pick(i))
+        for li, h in units(i):
+            _oracle_unit(wl, li, rows, inputs, states, h)
     t0 = time.perf_counter()
     flops = 0.0
     for i in range(args.steps):
-        flops += _oracle_sample_step(rows, inputs, states, pick(i))
+        for li, h in units(args.warmup + i):
+            flops += _oracle_unit(wl, li, rows, inputs, states, h)
     dt = time.perf_counter() - t0
     v = flops / dt / 1e12
-    which = "the 5 linears" if per_step == len(LINEARS) else "one linear (in turn)"
-    sample = (f"per step: whole-tensor amax/scale/quantise(+transpose) of X, W, dY of {which} "
-              f"and {rows} full output rows of each of its GEMMs; value = sampled GEMM FLOPs / "
-              f"wall time")
+    which = ("one micro-batch of the 5 linears" if short else
+             "the forward or the backward of one linear (in turn over the 5 linears)")
+    sample = (f"per step: {which}: whole-tensor amax/scale/quantise(+transpose) of its "
+              f"operands and {rows} full output rows of each of its GEMMs; value = sampled "
+              f"GEMM FLOPs / wall time")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens": TOKENS,
-                   "linears": {n: [k, n_] for n, k, n_ in LINEARS}},
+        "config": {"workload": wl.label, "tokens_per_micro_batch": wl.tokens,
+                   "micro_batches_per_step": wl.micro_batches,
+                   "linears": {n: [k, n_] for n, k, n_ in wl.linears}},
         "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -746,8 +1016,6 @@ def run_kernel(args):
         return run_quantize_sweep(F, args, dev, flush)
     if args.kernel == "block_step":
         return run_block_step(F, args, dev, flush)
-    if args.kernel == "llama70b_step":
-        return run_llama70b_step(F, args, dev, flush)
     if args.kernel in ("gemm", "block_gemm"):
         M, N, K = dims
         lay = {"tn": F.LAYOUT_TN, "b_kn": F.LAYOUT_B_KN, "a_km": F.LAYOUT_A_KM,
@@ -836,24 +1104,28 @@ def run_kernel(args):
                       "iters": args.iters, "l2": "flushed before every launch"}))
 
 
-def step_gemms():
-    """The 15 GEMMs of one layer step: (name, M, N, K, A format, output,
-    layout).  The backward GEMMs read the forward's codes as stored (the
+def step_gemms(wl: Workload | None = None):
+    """The GEMMs of one micro-batch of a layer step: (name, M, N, K, A
+    format, output, layout) -- per linear the forward, the dgrad and the
+    wgrad.  The backward GEMMs read the forward's codes as stored (the
     layer's default): dgrad's B is W_q [N x K], wgrad's A and B are dY_q and
     X_q, both [tokens x ...]."""
+    wl = wl or LLAMA7B
+    T = wl.tokens
     out = []
-    for name, K, N in LINEARS:
-        out.append((name + ".fwd", TOKENS, N, K, "e4m3", "bf16", 0))
-        out.append((name + ".dgrad", TOKENS, K, N, "e5m2", "bf16", 1))
-        out.append((name + ".wgrad", N, K, TOKENS, "e5m2", "f32acc", 3))
+    for name, K, N in wl.linears:
+        out.append((name + ".fwd", T, N, K, "e4m3", "bf16", 0))
+        out.append((name + ".dgrad", T, K, N, "e5m2", "bf16", 1))
+        out.append((name + ".wgrad", N, K, T, "e5m2", "f32acc", 3))
     return out
 
 
 def run_gemm_step(F, args, dev, codes, flush):
-    """The step's 15 GEMMs with their shapes, formats and output types, each on
-    random codes, run once as warm-up and once timed (in that order), with
-    the operands of one GEMM on the device at a time."""
-    gemms = step_gemms()
+    """The 15 GEMMs of one micro-batch of a layer step (--workload) with their
+    shapes, formats and output types, each on random codes, run once as
+    warm-up and once timed (in that order), with the operands of one GEMM on
+    the device at a time."""
+    gemms = step_gemms(WORKLOADS[args.workload])
     one = torch.ones(1, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     times = []
@@ -878,7 +1150,8 @@ def run_gemm_step(F, args, dev, codes, flush):
             del A, B, D
     assert F.fp8_device_status() == 0
     flops = sum(2.0 * M * N * K for _, M, N, K, _, _, _ in gemms)
-    print(json.dumps({"kernel": "gemm_step", "gemms": [g[0] for g in gemms],
+    print(json.dumps({"kernel": "gemm_step", "workload": args.workload,
+                      "gemms": [g[0] for g in gemms],
                       "ms": [round(t, 4) for t in times], "total_ms": round(sum(times), 4),
                       "achieved": round(flops / (sum(times) * 1e-3) / 1e12, 1),
                       "unit": "TFLOP/s"}))
@@ -931,67 +1204,15 @@ def run_block_step(F, args, dev, flush):
         torch.cuda.empty_cache()
 
 
-LINEARS_70B = [("qkv", 8192, 10240), ("o", 8192, 8192), ("gate", 8192, 28672),
-               ("up", 8192, 28672), ("down", 28672, 8192)]
-
-
-def run_llama70b_step(F, args, dev, flush):
-    """The Llama-2-70B-shaped block linears (4096 tokens, d = 8192, GQA QKV
-    8192 -> 10240, O, gate/up 8192 -> 28672, down 28672 -> 8192) through
-    fp8_linear_fwd + fp8_linear_bwd with per-tensor dynamic scaling, dW
-    accumulated in FP32.  Seeded synthetic inputs resident on the device
-    (X with outlier channels, W ~ N(0, 0.02), dY ~ N(0, 1e-3)); L2 flushed
-    before every timed step."""
-    tokens = 4096
-    recipe = F.Recipe(F.SCALING_DYNAMIC)
-    layers, Xs, Ws, dYs, Ys, dXs, dWs = [], [], [], [], [], [], []
-    for li, (name, K, N) in enumerate(LINEARS_70B):
-        layers.append(F.Fp8Linear(tokens, N, K, recipe, device=dev))
-        Xs.append(synthetic.with_outlier_channels((tokens, K), 1.0, max(1, K // 256), 50.0,
-                                                  seed=10 * li, device=dev))
-        Ws.append(synthetic.normal((N, K), 0.02, seed=1000 + li, device=dev))
-        dYs.append(synthetic.normal((tokens, N), 1e-3, seed=500 + li, device=dev))
-        Ys.append(torch.empty(tokens, N, dtype=torch.bfloat16, device=dev))
-        dXs.append(torch.empty(tokens, K, dtype=torch.bfloat16, device=dev))
-        dWs.append(torch.zeros(N, K, dtype=torch.float32, device=dev))
-
-    def step():
-        for li in range(len(LINEARS_70B)):
-            layers[li].forward(Xs[li], Ws[li], Y=Ys[li])
-            layers[li].backward(dYs[li], dX=dXs[li], dW=dWs[li], accumulate_dW=True)
-
-    stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
-        step()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.iters)]
-    for i in range(args.iters):
-        flush.fill_(float(i))
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    assert F.fp8_device_status() == 0
-    ms = sorted(a.elapsed_time(b) for a, b in ev)
-    med = ms[len(ms) // 2]
-    flops = sum(6.0 * tokens * N * K for _, K, N in LINEARS_70B)
-    print(json.dumps({
-        "kernel": "llama70b_step", "tokens": tokens,
-        "linears": {n: [k, v] for n, k, v in LINEARS_70B}, "recipe": "dynamic per-tensor, HYBRID",
-        "median_ms": round(med, 4), "min_ms": round(ms[0], 4),
-        "achieved": round(flops / (med * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
-        "work": "6 M N K per linear (fwd + dgrad + wgrad); casts, amax and scale updates included",
-        "iters": args.iters, "l2": "flushed before every step"}), flush=True)
-
-
-def _gemm_traffic():
-    """DRAM bytes per GEMM launch of the step (mean over its 15 GEMMs), as
-    measured by ncu and recorded in profiles/ together with a hash of the
-    GEMM source it was measured on; None if the source has changed since."""
+def _gemm_traffic(key):
+    """DRAM bytes per GEMM launch of a workload's step (mean over its GEMM
+    launches), as measured by ncu and recorded in profiles/ together with a
+    hash of the GEMM source it was measured on; None if the source has
+    changed since or the workload has no record."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "gemm_step_traffic.json")) as f:
-            rec = json.load(f)
+            rec = json.load(f)["workloads"][key]
         with open(os.path.join(ROOT, "scaled_fp8_linear_gb300", "csrc", "gemm.cu"), "rb") as f:
             h = hashlib.sha256(f.read()).hexdigest()
         return rec["bytes_per_launch"] if rec.get("gemm_cu_sha256") == h else None
@@ -999,18 +1220,24 @@ def _gemm_traffic():
         return None
 
 
+WORKLOADS = {"llama2-70b": LLAMA70B, "llama2-7b": LLAMA7B}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=80)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=32)
-    ap.add_argument("--ref-rows", type=int, default=4)
+    ap.add_argument("--cpu-rows", type=int, default=8)
+    ap.add_argument("--ref-rows", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="headline step only (skip the other configurations' keys)")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama2-70b",
+                    help="--kernel gemm_step: whose step GEMMs")
     ap.add_argument("--kernel", choices=["gemm", "block_gemm", "quantize", "quantize_sr",
-                                         "quantize_sweep", "gemm_step", "block_step",
-                                         "llama70b_step"],
+                                         "quantize_sweep", "gemm_step", "block_step"],
                     help="time one kernel on --shape instead of the layer step")
     ap.add_argument("--shape", default="8192,12288,4096")
     ap.add_argument("--fmt", choices=["e4m3", "e5m2"], default="e4m3")

@@ -25,8 +25,8 @@
 //               scale, convert, store to global memory.
 // Per-tensor kernel: BM x BN = 128 x 256, two TMEM accumulators (512
 // columns) so the epilogue of one tile overlaps the mainloop of the next.
-// Block-scaled kernel (fp32 factors): BM x BN = 128 x 128, four TMEM
-// partial-sum buffers rotated per 128-deep K block; 16 epilogue warps
+// Block-scaled kernel (fp32 factors): CTA pairs, 256 x 128 tiles, four TMEM
+// partial-sum buffers rotated per 128-deep K block; 8 epilogue warps per CTA
 // promote them into FP32 registers.
 // Block-scaled kernel (power-of-two factors): CTA pairs, 256 x 256 tiles,
 // tcgen05.mma kind::mxf8f6f4.block_scale with the factors as UE8M0 words in
@@ -54,7 +54,6 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 128;      // bytes = FP8 elements of K per stage
 constexpr int UMMA_K = 32;   // K of one kind::f8f6f4 instruction
-constexpr int kBlockGroup = 32;  // raster group of the block-scaled kernel (M-blocks)
 
 struct GemmParams {
     int64_t M, N, K;
@@ -690,83 +689,180 @@ __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
     return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
 }
 
-// Final store of one promoted accumulator row segment (32 columns, packed
-// pairs), plus the bias if any: bf16 round-to-nearest-even, or FP32 (added
-// to the buffer if rmw).
-// Block mode has N % 128 == 0, so all 32 columns exist.
-__device__ __forceinline__ void store_block_row(const uint64_t (&acc)[16], int64_t m, int64_t n0,
-                                                const GemmParams& p, bool rmw) {
-    float a[32];
+// Block-scaled GEMM with fp32 factors ("Block-wise scaling at 128
+// granularity": every 128-deep partial sum is multiplied by its blocks'
+// factors before it is added to the FP32 accumulator).
+//
+// A cluster of two CTAs (the two SMs of a TPC) computes a 256 x 128 tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = 128, K = 32): CTA r loads rows
+// [r*128, r*128+128) of the tile's A panel and rows [r*64, r*64+64) of its B
+// panel (16 + 8 KiB per stage); both CTAs' copies count on the even CTA's
+// `full` barrier, whose MMA thread issues the MMAs.  Each 128-deep K block
+// goes to its own TMEM buffer -- four buffers of 128 columns, rotated -- so
+// the MMAs of the next three blocks run while the epilogue promotes one.
+// The pair tile halves the operand bytes each SM moves through shared memory
+// per FLOP against a 128 x 128 single-CTA tile, whose shared-memory traffic
+// (TMA writes plus MMA reads) capped the MMA at about half its rate.
+//   warp 0      TMA producer (one thread);
+//   warp 1      MMA issuer (one thread of the even CTA): per K block, waits
+//               for a free buffer and a full stage, issues 4 MMAs, commits
+//               the stage (`empty`) and the buffer (`tfull`) to both CTAs;
+//   warp 2      TMEM allocation (512 columns per CTA);
+//   warps 4-11  epilogue, 2 per TMEM lane quarter, 64 columns each: per K
+//               block, read the buffer (tcgen05.ld), hand it back to the MMA
+//               thread (both CTAs' warps arrive on the even CTA's `tempty`),
+//               then add partial * s_a(m, kb) * s_b(n, kb) into FP32
+//               registers with packed fma.rn.f32x2.  The factors of the next
+//               four K blocks are loaded while the current four are promoted.
+//               At the tile's end the accumulator is rounded (plus the bias)
+//               and leaves through 32-row x 64-byte TMA boxes: bf16 stores,
+//               or FP32 stores / reduce-adds (accumulate).
+// Every wait is a blocking try_wait, so that waiting epilogue warps do not
+// take issue slots from the producer and MMA warps on their sub-partitions.
+// COLSCALE: B carries 1x128 scales (one factor per output column and K
+// block, the block-wise wgrad); each epilogue warp stages its 64 columns'
+// factors of four K blocks in shared memory, read back as broadcasts.
+// Shape of one instance: pair tiles of 256 x TN, EPI promotion warps per CTA
+// (at most 4 per TMEM lane quarter), a ring of STAGES operand stages, and
+// TMEM split into 512 / TN partial-sum buffers.
+template <int TN_, int EPI_, int STAGES_>
+struct BpCfg {
+    static constexpr int TN = TN_;
+    static constexpr int EPI = EPI_;
+    static constexpr int STAGES = STAGES_;
+    static constexpr int NBUF = 512 / TN;
+    static constexpr int THREADS = (4 + EPI) * 32;
+    static constexpr int CW = 4 * TN / EPI;          // columns of one promotion warp
+    static constexpr int A_BYTES = 128 * BK;         // this CTA's 128 rows of A
+    static constexpr int B_BYTES = (TN / 2) * BK;    // this CTA's half of the TN rows of B
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + EPI * (2048 + 4 * CW * 4) + 256 + 1024;
+};
+constexpr int kBpGroup = 16;           // raster group (M-blocks of 256 rows)
+// 256 x 128 tiles, four TMEM buffers (three K blocks of slack for the
+// promotion), 8 promotion warps of 64 columns.  Measured on the 16384 x 18432
+// x 7168 shapes: 256 x 256 tiles with two buffers of 256 columns were slower
+// (each promotion warp then holds 128 accumulator columns and the promotion
+// must finish within one K block), and so were 16 promotion warps.
+using BpNarrow = BpCfg<128, 8, 8>;
+
+// Factors of row r of an operand (gran: FP8_GRAN_TENSOR, 1x128 or 128x128;
+// KB blocks per row) for the K blocks kb0 .. kb0+3, 0 past the last block.
+// vec: the four are one aligned float4 (KB % 4 == 0, 16-byte aligned array).
+__device__ __forceinline__ void block_factors4(float (&f)[4], const float* s, int gran, int64_t r,
+                                               int kb0, int KB, bool vec) {
+    if (gran == FP8_GRAN_TENSOR) {
+        const float v = s[0];
+        f[0] = f[1] = f[2] = f[3] = v;
+        return;
+    }
+    if (kb0 >= KB) {
+        f[0] = f[1] = f[2] = f[3] = 0.0f;
+        return;
+    }
+    const float* src = s + (gran == FP8_GRAN_1x128 ? r : (r >> 7)) * KB + kb0;
+    if (vec) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f[j] = kb0 + j < KB ? src[j] : 0.0f;
+    }
+}
+
+// acc[e] += r[2e..2e+1] * f for the 16 packed pairs of a 32-column chunk.
+__device__ __forceinline__ void promote_uniform(uint64_t* acc, const uint32_t (&r)[32], uint64_t ff) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        acc[e] = ptx::ffma2(static_cast<uint64_t>(r[2 * e]) | (static_cast<uint64_t>(r[2 * e + 1]) << 32),
+                            ff, acc[e]);
+}
+
+// acc[e] += r[2e..2e+1] * fp32(fa * cf[2e..2e+1]): per-column factors cf (32
+// floats in shared memory, read as broadcasts).
+__device__ __forceinline__ void promote_columns(uint64_t* acc, const uint32_t (&r)[32], float fa,
+                                                const float* cf) {
+#pragma unroll
+    for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 c = *reinterpret_cast<const float4*>(cf + 4 * e4);
+        const uint64_t f0 = pack2(__fmul_rn(fa, c.x), __fmul_rn(fa, c.y));
+        const uint64_t f1 = pack2(__fmul_rn(fa, c.z), __fmul_rn(fa, c.w));
+        acc[2 * e4] = ptx::ffma2(static_cast<uint64_t>(r[4 * e4]) |
+                                     (static_cast<uint64_t>(r[4 * e4 + 1]) << 32),
+                                 f0, acc[2 * e4]);
+        acc[2 * e4 + 1] = ptx::ffma2(static_cast<uint64_t>(r[4 * e4 + 2]) |
+                                         (static_cast<uint64_t>(r[4 * e4 + 3]) << 32),
+                                     f1, acc[2 * e4 + 1]);
+    }
+}
+
+// Round one promoted 32-column chunk (16 packed pairs) plus the bias (if
+// any) and write it through the warp's staging slot: one bf16 box of 32
+// columns, or two FP32 boxes of 16 columns (added to D when accumulating).
+// Whole-warp call; m0 is the warp's first row, n0 the chunk's first column.
+__device__ __forceinline__ void emit_block_chunk(uint8_t* slot, const uint64_t* acc, int64_t m0,
+                                                 int64_t n0, const GemmParams& p,
+                                                 const CUtensorMap* map) {
+    float v[32];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-        a[2 * e] = __uint_as_float(static_cast<uint32_t>(acc[e]));
-        a[2 * e + 1] = __uint_as_float(static_cast<uint32_t>(acc[e] >> 32));
+        v[2 * e] = __uint_as_float(static_cast<uint32_t>(acc[e]));
+        v[2 * e + 1] = __uint_as_float(static_cast<uint32_t>(acc[e] >> 32));
     }
     if (p.bias) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 32; j += 8) {
             float b[8];
-            load_bias8(b, p.bias, n0 + 8 * j);
+            load_bias8(b, p.bias, n0 + j);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) a[8 * j + e] = __fadd_rn(a[8 * j + e], b[e]);
+            for (int e = 0; e < 8; ++e) v[j + e] = __fadd_rn(v[j + e], b[e]);
         }
     }
     if (p.out == FP8_OUT_BF16) {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.D) + m * p.N + n0);
+        uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(a[8 * j + 2 * e], a[8 * j + 2 * e + 1]);
-                w[e] = *reinterpret_cast<const uint32_t*>(&h);
-            }
-            dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int e = 0; e < 16; ++e) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+            w[e] = *reinterpret_cast<const uint32_t*>(&h);
         }
+        const uint4 piece[4] = {make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7]),
+                                make_uint4(w[8], w[9], w[10], w[11]),
+                                make_uint4(w[12], w[13], w[14], w[15])};
+        emit_box(slot, piece, map, n0, m0, m0 < p.M, false);
     } else {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.D) + m * p.N + n0);
-        float4 o[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) o[j] = rmw ? dst[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int hb = 0; hb < 2; ++hb) {
+            uint4 piece[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float4 v = make_float4(a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
-            if (rmw) {
-                v.x += o[j].x; v.y += o[j].y; v.z += o[j].z; v.w += o[j].w;
-            }
-            dst[j] = v;
+            for (int j = 0; j < 4; ++j)
+                piece[j] = make_uint4(__float_as_uint(v[16 * hb + 4 * j]),
+                                      __float_as_uint(v[16 * hb + 4 * j + 1]),
+                                      __float_as_uint(v[16 * hb + 4 * j + 2]),
+                                      __float_as_uint(v[16 * hb + 4 * j + 3]));
+            emit_box(slot, piece, map, n0 + 16 * hb, m0, m0 < p.M, p.accumulate != 0);
         }
     }
 }
 
-// Dequantisation factor of row r (of A or B) for K block kb.
-__device__ __forceinline__ float block_factor(const float* s, int gran, int64_t r, int kb,
-                                              int KB) {
-    if (gran == FP8_GRAN_TENSOR) return s[0];
-    if (gran == FP8_GRAN_1x128) return s[r * KB + kb];
-    return s[(r >> 7) * KB + kb];
-}
-
-constexpr int kBlockEpiWarps = 16;   // 4 per TMEM lane quadrant, 32 columns each
-constexpr int kBlockThreads = (4 + kBlockEpiWarps) * 32;
-
-// COLSCALE: B carries 1x128 scales, i.e. one factor per output column and K
-// block; each epilogue warp then stages its 32 columns' factors in shared
-// memory per K block.
-template <int STAGES, bool COLSCALE>
-__global__ void __launch_bounds__(kBlockThreads, 1)
-    gemm_block_kernel(const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+template <typename Cfg, bool COLSCALE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
+    gemm_block_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmD,
+                           const __grid_constant__ GemmParams p, int vec_a, int vec_b) {
     ptx::griddep_launch_dependents();   // the next kernel may launch now
-    constexpr int BN = 128;
-    __shared__ __align__(16) float colf[COLSCALE ? kBlockEpiWarps : 1][32];
-    constexpr int NBUF = 4;
-    using L = Layout<BN, STAGES>;
-    constexpr uint32_t TMEM_COLS = NBUF * BN;
+    constexpr int STAGES = Cfg::STAGES, NBUF = Cfg::NBUF, EPI = Cfg::EPI;
+    constexpr int A_BYTES = Cfg::A_BYTES;
+    constexpr int STAGE_BYTES = Cfg::STAGE_BYTES;
+    constexpr int TN = Cfg::TN;
+    constexpr uint32_t TMEM_COLS = NBUF * TN;
+    static_assert(TMEM_COLS == 512, "the partial-sum buffers fill TMEM");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(ring + L::RING_BYTES);
+    uint8_t* epi_stage = ring + STAGES * STAGE_BYTES;   // output boxes: 2 KB per epilogue warp
+    float* colf = reinterpret_cast<float*>(epi_stage + EPI * 2048);   // [warp][4][cols]
+    uint64_t* full = reinterpret_cast<uint64_t*>(colf + EPI * 4 * Cfg::CW);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + NBUF;
@@ -775,14 +871,16 @@ __global__ void __launch_bounds__(kBlockThreads, 1)
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const bool leader = rank == 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
-        for (int a = 0; a < NBUF; ++a) {
-            ptx::mbar_init(&tfull[a], 1);
-            ptx::mbar_init(&tempty[a], kBlockEpiWarps);
+        for (int b = 0; b < NBUF; ++b) {
+            ptx::mbar_init(&tfull[b], 1);
+            ptx::mbar_init(&tempty[b], 2 * EPI);   // promotion warps of both CTAs
         }
         ptx::mbar_init(done, 1);
         *abort_flag = 0;
@@ -791,140 +889,211 @@ __global__ void __launch_bounds__(kBlockThreads, 1)
     if (warp == 0 && lane == 0) {
         ptx::tma_prefetch_desc(&tmA);
         ptx::tma_prefetch_desc(&tmB);
+        ptx::tma_prefetch_desc(&tmD);
     }
     if (warp == 2) {
-        ptx::tmem_alloc(tmem_slot, TMEM_COLS);
-        ptx::tmem_relinquish();
+        ptx::tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        ptx::tmem_relinquish_pair();
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::cluster_sync();   // the peer's barriers exist before any remote arrival
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     ptx::griddep_wait();   // the previous kernel's results (operands, factors) are visible
-    const int num_tiles = p.num_m * p.num_n;
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int num_units = p.num_m * p.num_n;
+    const int KB = p.num_kb;
 
     if (warp == 0) {
-        if (lane == 0) producer<BN, STAGES, kBlockGroup>(&tmA, &tmB, ring, full, empty, p, abort_flag);
-    } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc = ptx::idesc_f8f6f4(p.fa, p.fb, BM, BN);
+            uint32_t stage = 0, phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int u = pair; ok && u < num_units; u += npairs) {
+                int m_blk, n_blk;
+                tile_coords<kBpGroup>(u, p.num_m, p.num_n, m_blk, n_blk);
+                const int ya = m_blk * 256 + static_cast<int>(rank) * 128;
+                const int yb = n_blk * TN + static_cast<int>(rank) * (TN / 2);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+                    uint8_t* sa = ring + stage * STAGE_BYTES;
+                    const uint32_t bar = ptx::cluster_addr(&full[stage], 0);
+                    if (leader) ptx::mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
+                    ptx::tma_load_2d_pair(sa, &tmA, bar, kb * BK, ya);
+                    ptx::tma_load_2d_pair(sa + A_BYTES, &tmB, bar, kb * BK, yb);
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            uint32_t never = 0;
+            if (leader) {
+                // drain: the last copies into each slot (both CTAs' bytes) have landed
+                for (int s = 0; s < STAGES; ++s) {
+                    if (issued <= s && issued < STAGES) break;
+                    const uint32_t par = (static_cast<uint32_t>(s) < stage) ? phase : (phase ^ 1u);
+                    ptx::mbar_wait(&full[s], par, &never);
+                }
+            } else if (!ok) {
+                // copies signal the peer's barriers: after an abort, give those in
+                // flight a bounded grace period to land before this CTA moves on
+                const uint64_t t0 = ptx::globaltimer();
+                while (ptx::globaltimer() - t0 < 1000000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            const uint32_t idesc = ptx::idesc_f8f6f4(p.fa, p.fb, 256, TN);
             uint32_t stage = 0, phase = 0, buf = 0, buf_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!ptx::mbar_wait_spin(&tempty[buf], buf_phase ^ 1u, abort_flag)) { ok = false; break; }
+            for (int u = pair; ok && u < num_units; u += npairs) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!ptx::mbar_wait(&tempty[buf], buf_phase ^ 1u, abort_flag)) { ok = false; break; }
                     if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    uint8_t* sa = ring + stage * L::STAGE_BYTES;
+                    uint8_t* sa = ring + stage * STAGE_BYTES;
                     const uint64_t ad = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa));
-                    const uint64_t bd = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa + L::A_BYTES));
-                    const uint32_t d = tmem_base + buf * BN;
+                    const uint64_t bd = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa + A_BYTES));
+                    const uint32_t d = tmem_base + buf * TN;
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k)
-                        ptx::mma_f8f6f4(d, ad + (k * UMMA_K >> 4), bd + (k * UMMA_K >> 4), idesc,
-                                        k != 0);
-                    ptx::mma_commit(&empty[stage]);
-                    ptx::mma_commit(&tfull[buf]);
+                        ptx::mma_f8f6f4_pair(d, ad + (k * UMMA_K >> 4), bd + (k * UMMA_K >> 4),
+                                             idesc, k != 0);
+                    ptx::mma_commit_pair(&empty[stage], 0x3);
+                    ptx::mma_commit_pair(&tfull[buf], 0x3);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                     if (++buf == NBUF) { buf = 0; buf_phase ^= 1u; }
                 }
             }
             uint32_t never = 0;
-            ptx::mma_commit(done);
+            ptx::mma_commit_pair(done, 0x1);
             ptx::mbar_wait(done, 0, &never);
         }
     } else if (warp >= 4) {
-        const int qd = warp & 3;                 // TMEM lane quadrant of this warp
-        const int cg = (warp - 4) >> 2;          // which 32 of the 128 columns
-        const int row = qd * 32 + lane;
-        const int KB = p.num_kb;
-        const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
+        constexpr int CW = Cfg::CW;              // columns of this warp
+        constexpr int NCH = CW / 32;             // 32-column chunks
+        const int qd = warp & 3;                 // TMEM lane quarter of this warp
+        const int h = (warp - 4) >> 2;           // which CW of the tile's 128 columns
+        uint8_t* slot = epi_stage + (warp - 4) * 2048;
+        float* cf = colf + (warp - 4) * 4 * CW;  // COLSCALE: [4 K blocks][CW columns]
+        const uint32_t lanes = static_cast<uint32_t>(qd * 32) << 16;
         uint32_t buf = 0, buf_phase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        for (int u = pair; ok && u < num_units; u += npairs) {
             int m_blk, n_blk;
-            tile_coords<kBlockGroup>(tile, p.num_m, p.num_n, m_blk, n_blk);
-            const int64_t m = static_cast<int64_t>(m_blk) * BM + row;
+            tile_coords<kBpGroup>(u, p.num_m, p.num_n, m_blk, n_blk);
+            const int64_t m0 = static_cast<int64_t>(m_blk) * 256 + rank * 128 + qd * 32;
+            const int64_t m = m0 + lane;
             const int64_t m_safe = m < p.M ? m : p.M - 1;
-            const int64_t n_row = static_cast<int64_t>(n_blk) * BN;  // a row of B in this tile
-            const int64_t n0 = n_row + cg * 32;
-            if (rmw && m < p.M)
-                ptx::prefetch_l2(static_cast<const float*>(p.D) + m * p.N + n0, 32 * 4);
-            // FP32 accumulator of 32 columns, as 16 packed pairs for fma.rn.f32x2
-            uint64_t acc[16];
+            const int64_t n0 = static_cast<int64_t>(n_blk) * TN + h * CW;
+            // FP32 accumulator of CW columns, as packed pairs
+            uint64_t acc[CW / 2];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = 0ull;
-            // dequantisation factors, loaded a group of 2 K blocks ahead so that
-            // their L2 latency hides behind the promotion of the current group
-            constexpr int G = 2;
-            float sa_next[G], sb_next[G];
-            // per-column B factors (COLSCALE): lane l holds column n0 + l's
-            const int64_t n_lane = COLSCALE ? n0 + lane : n_row;
+            for (int e = 0; e < CW / 2; ++e) acc[e] = 0ull;
+            // factors of the next group of four K blocks: A per row, B per
+            // 128-column block (or, COLSCALE, per column: lane l holds columns
+            // n0 + 32c + l)
+            float fa_n[4], fb_n[4], fc_n[NCH][4];
+            block_factors4(fa_n, p.sa, p.ga, m_safe, 0, KB, vec_a != 0);
+            if (COLSCALE) {
 #pragma unroll
-            for (int j = 0; j < G; ++j) {
-                sa_next[j] = j < KB ? block_factor(p.sa, p.ga, m_safe, j, KB) : 0.0f;
-                sb_next[j] = j < KB ? block_factor(p.sb, p.gb, n_lane, j, KB) : 0.0f;
+                for (int c = 0; c < NCH; ++c)
+                    block_factors4(fc_n[c], p.sb, p.gb, n0 + 32 * c + lane, 0, KB, vec_b != 0);
+            } else {
+                block_factors4(fb_n, p.sb, p.gb, n0, 0, KB, vec_b != 0);
             }
-            for (int kb0 = 0; ok && kb0 < KB; kb0 += G) {
-                float sa_cur[G], sb_cur[G];
+            for (int kb0 = 0; ok && kb0 < KB; kb0 += 4) {
+                float fa[4], fb[4];
 #pragma unroll
-                for (int j = 0; j < G; ++j) {
-                    sa_cur[j] = sa_next[j];
-                    sb_cur[j] = sb_next[j];
-                    const int kn = kb0 + G + j;
-                    sa_next[j] = kn < KB ? block_factor(p.sa, p.ga, m_safe, kn, KB) : 0.0f;
-                    sb_next[j] = kn < KB ? block_factor(p.sb, p.gb, n_lane, kn, KB) : 0.0f;
+                for (int j = 0; j < 4; ++j) {
+                    fa[j] = fa_n[j];
+                    fb[j] = fb_n[j];
+                }
+                if (COLSCALE) {
+                    __syncwarp();   // the previous group's factors have been read
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) cf[j * CW + 32 * c + lane] = fc_n[c][j];
+                    __syncwarp();
+                }
+                // the next group's factors load while this group is promoted
+                block_factors4(fa_n, p.sa, p.ga, m_safe, kb0 + 4, KB, vec_a != 0);
+                if (COLSCALE) {
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c)
+                        block_factors4(fc_n[c], p.sb, p.gb, n0 + 32 * c + lane, kb0 + 4, KB,
+                                       vec_b != 0);
+                } else {
+                    block_factors4(fb_n, p.sb, p.gb, n0, kb0 + 4, KB, vec_b != 0);
                 }
 #pragma unroll
-                for (int j = 0; j < G; ++j) {
+                for (int j = 0; j < 4; ++j) {
                     if (kb0 + j >= KB) break;
-                    // COLSCALE: the factor of element (m, n0 + c) is sa(m) * sb(n0 + c);
-                    // the warp's 32 column factors go through shared memory
-                    const float* cf = colf[COLSCALE ? warp - 4 : 0];
-                    uint64_t ff = 0;
-                    if (COLSCALE) {
-                        __syncwarp();
-                        colf[COLSCALE ? warp - 4 : 0][lane] = sb_cur[j];
-                        __syncwarp();
-                    } else {
-                        const float f = __fmul_rn(sa_cur[j], sb_cur[j]);
-                        ff = pack2(f, f);
-                    }
-                    const float sa_j = sa_cur[j];
-                    ok = (lane == 0) ? ptx::mbar_wait_spin(&tfull[buf], buf_phase, abort_flag) : false;
+                    ok = (lane == 0) ? ptx::mbar_wait(&tfull[buf], buf_phase, abort_flag) : false;
                     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
                     if (!ok) break;
                     __syncwarp();
                     ptx::tc_fence_after();
-                    uint32_t r[32];
-                    ptx::tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(qd * 32) << 16) +
-                                                buf * BN + cg * 32, r);
-                    ptx::tmem_wait_ld();
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&tempty[buf]);   // buffer read: hand it back
-                    if (++buf == NBUF) { buf = 0; buf_phase ^= 1u; }
+                    const uint32_t ta = tmem_base + lanes + buf * TN + h * CW;
+                    if (COLSCALE || NCH == 1) {
+                        // one 32-column chunk at a time (the per-column factors
+                        // need the registers): the buffer goes back after the
+                        // last chunk's load
+                        uint32_t r[32];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const uint64_t fe = COLSCALE ? pack2(__fmul_rn(sa_j, cf[2 * e]),
-                                                             __fmul_rn(sa_j, cf[2 * e + 1]))
-                                                     : ff;
-                        acc[e] = ptx::ffma2(static_cast<uint64_t>(r[2 * e]) |
-                                                (static_cast<uint64_t>(r[2 * e + 1]) << 32),
-                                            fe, acc[e]);
+                        for (int c = 0; c < NCH; ++c) {
+                            ptx::tmem_ld_32x32b_x32(ta + 32 * c, r);
+                            ptx::tmem_wait_ld();
+                            if (c == NCH - 1) {
+                                ptx::tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0)
+                                    ptx::mbar_arrive_cluster_relaxed(ptx::cluster_addr(&tempty[buf], 0));
+                            }
+                            if (COLSCALE) {
+                                promote_columns(acc + 16 * c, r, fa[j], cf + j * CW + 32 * c);
+                            } else {
+                                const float f = __fmul_rn(fa[j], fb[j]);
+                                promote_uniform(acc + 16 * c, r, pack2(f, f));
+                            }
+                        }
+                    } else {
+                        // two 32-column chunks in flight at a time; the buffer
+                        // goes back once the last pair is in registers
+                        const float f = __fmul_rn(fa[j], fb[j]);
+                        const uint64_t ff = pack2(f, f);
+#pragma unroll
+                        for (int c = 0; c < NCH; c += 2) {
+                            uint32_t r0[32], r1[32];
+                            ptx::tmem_ld_32x32b_x32(ta + 32 * c, r0);
+                            ptx::tmem_ld_32x32b_x32(ta + 32 * c + 32, r1);
+                            ptx::tmem_wait_ld();
+                            if (c + 2 == NCH) {
+                                ptx::tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) ptx::mbar_arrive_cluster_relaxed(ptx::cluster_addr(&tempty[buf], 0));
+                            }
+                            promote_uniform(acc + 16 * c, r0, ff);
+                            promote_uniform(acc + 16 * c + 16, r1, ff);
+                        }
                     }
+                    if (++buf == NBUF) { buf = 0; buf_phase ^= 1u; }
                 }
             }
             if (!ok) break;
-            if (m < p.M) store_block_row(acc, m, n0, p, rmw);
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) emit_block_chunk(slot, acc + 16 * c, m0, n0 + 32 * c, p, &tmD);
         }
+        if (lane == 0) ptx::bulk_wait_group_all();   // every TMA store has completed
+        __syncwarp();
     }
 
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::cluster_sync();   // the pair's MMAs, copies and remote arrivals are all done
     if (warp == 2) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+        ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
     if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_device_status, 1u);
 }
@@ -1428,7 +1597,6 @@ constexpr int kPairStages = 6;
 constexpr int kPairSmemBytes = kPairStages * 2 * 128 * BK + 4 * 2048 + 256 + 1024;
 // Problems with at least this many rows use the CTA-pair kernel.
 constexpr int64_t kPairMinRows = 256;
-constexpr int kBlockStages = 6;
 
 template <typename Kernel>
 int ensure_smem(Kernel k, int bytes, int kernel_id) {
@@ -1451,8 +1619,9 @@ int ensure_smem(Kernel k, int bytes, int kernel_id) {
 // persistent grid size); cached per device.
 int pair_clusters(const void* func, int kernel_id, int threads, int smem) {
     static std::mutex mu;
-    static int cache[64][3] = {};   // [device][kernel id]: 0 single, 1 grouped pair kernel,
-                                    // 2 power-of-two block kernel
+    static int cache[64][5] = {};   // [device][kernel id]: 0 single, 1 grouped pair kernel,
+                                    // 2 power-of-two block kernel, 3 / 4 fp32-factor block
+                                    // kernel (row / column factors on B)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
     int uncached = 0;                            // devices past the table: computed per call
@@ -1537,6 +1706,42 @@ int launch_gemm_mx(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M
     return FP8_OK;
 }
 
+// Block-scaled GEMM with fp32 factors (at least one operand with 1x128 or
+// 128x128 scales; K > 0) on the CTA-pair promotion kernel: 256 x 128 tiles.
+int launch_gemm_block(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
+                      int64_t K, int ga, const float* sa, int gb, const float* sb,
+                      const void* bias, void* D, int out, int accumulate, cudaStream_t stream) {
+    using C = BpNarrow;
+    GemmParams p;
+    p.M = M; p.N = N; p.K = K;
+    p.num_m = static_cast<int>((M + 255) / 256);
+    p.num_n = static_cast<int>((N + C::TN - 1) / C::TN);
+    p.num_kb = static_cast<int>((K + BK - 1) / BK);
+    p.fa = fa; p.fb = fb; p.ga = ga; p.gb = gb; p.sa = sa; p.sb = sb;
+    p.bias = static_cast<const __nv_bfloat16*>(bias);
+    p.D = D; p.out = out; p.accumulate = accumulate;
+    p.a_mn = p.b_mn = 0;
+    CUtensorMap tmA, tmB, tmD;
+    int st = make_kmajor_map(&tmA, A, M, K, 128);
+    if (st != FP8_OK) return st;
+    if ((st = make_kmajor_map(&tmB, B, N, K, C::TN / 2)) != FP8_OK) return st;
+    if ((st = make_store_map(&tmD, D, M, N, out)) != FP8_OK) return st;
+    const bool colscale = gb == FP8_GRAN_1x128;
+    auto k = colscale ? gemm_block_pair_kernel<C, true> : gemm_block_pair_kernel<C, false>;
+    if ((st = ensure_smem(k, C::SMEM, colscale ? 3 : 1)) != FP8_OK) return st;
+    const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
+    const int64_t clusters = pair_clusters(reinterpret_cast<const void*>(k), colscale ? 4 : 3,
+                                           C::THREADS, C::SMEM);
+    const int grid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
+    // factors of four K blocks as one float4: rows of a multiple of 4 floats, aligned arrays
+    const int vec_a = p.num_kb % 4 == 0 && (reinterpret_cast<uintptr_t>(sa) & 15u) == 0;
+    const int vec_b = p.num_kb % 4 == 0 && (reinterpret_cast<uintptr_t>(sb) & 15u) == 0;
+    launch_pdl(k, dim3(grid), dim3(C::THREADS), C::SMEM, stream, tmA, tmB, tmD, p, vec_a, vec_b);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(FP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+    return FP8_OK;
+}
+
 }  // namespace
 
 int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
@@ -1570,11 +1775,14 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
                     (gb == FP8_GRAN_1x128 || gb == FP8_GRAN_128x128);
     if (mx) return launch_gemm_mx(A, fa, B, fb, M, N, K, ga, sa, gb, sb, bias, D, out, accumulate,
                                   stream);
+    if (block)
+        return launch_gemm_block(A, fa, B, fb, M, N, K, ga, sa, gb, sb, bias, D, out, accumulate,
+                                 stream);
     // per-tensor and per-row scales: CTA pairs for every problem of at least
     // 256 rows, and for every MN-major operand (the single-CTA kernel reads
     // K-major tiles only; rows past M are zero-filled and not stored)
-    const bool pair = !block && (M >= kPairMinRows || a_mn || b_mn);
-    const int BN = block ? 128 : kTensorBN;
+    const bool pair = M >= kPairMinRows || a_mn || b_mn;
+    const int BN = kTensorBN;
     const int TM = pair ? 256 : BM;   // rows of C per tile
     GemmParams p;
     p.M = M; p.N = N; p.K = K;
@@ -1604,22 +1812,11 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
         const int pgrid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
         GemmParams none{};
         launch_pdl(k, dim3(pgrid), dim3(256), kPairSmemBytes, stream, tmA, tmB, tmD, p, tmA, tmB, tmD, none);
-    } else if (!block) {
+    } else {
         using L = Layout<kTensorBN, kTensorStages>;
         auto k = gemm_tensor_kernel<kTensorBN, kTensorStages>;
         if ((st = ensure_smem(k, L::SMEM_BYTES, 0)) != FP8_OK) return st;
         launch_pdl(k, dim3(grid), dim3(256), L::SMEM_BYTES, stream, tmA, tmB, p);
-    } else {
-        using L = Layout<128, kBlockStages>;
-        if (gb == FP8_GRAN_1x128) {
-            auto k = gemm_block_kernel<kBlockStages, true>;
-            if ((st = ensure_smem(k, L::SMEM_BYTES, 3)) != FP8_OK) return st;
-            launch_pdl(k, dim3(grid), dim3(kBlockThreads), L::SMEM_BYTES, stream, tmA, tmB, p);
-        } else {
-            auto k = gemm_block_kernel<kBlockStages, false>;
-            if ((st = ensure_smem(k, L::SMEM_BYTES, 1)) != FP8_OK) return st;
-            launch_pdl(k, dim3(grid), dim3(kBlockThreads), L::SMEM_BYTES, stream, tmA, tmB, p);
-        }
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(FP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));

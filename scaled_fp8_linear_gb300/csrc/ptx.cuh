@@ -297,6 +297,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
                  : "memory");
 }
 
+// The same without release ordering: for an arrival that only reports that
+// this thread's earlier reads have completed (e.g. tcgen05.ld results already
+// waited for), where a cluster-scope release -- a fence the thread stalls on
+// -- orders nothing that the waiter needs.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
+}
+
 // TMA tile load into this CTA's shared memory whose completion is counted on
 // an mbarrier of either CTA of the pair (cluster-window address).
 __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map,

@@ -114,15 +114,17 @@ def test_noalloc_matches_workspace_in_every_scratch_layout(mode, transposes):
 def test_noalloc_rejects_shapes_beyond_the_scratch():
     fn = _noalloc()
     rec = F.Recipe(F.SCALING_DELAYED, history_len=16)
-    st = F.LinearStateC()
-    p = ctypes.c_void_p(0x10000)
-    # without transposed copies the scratch holds dY_q alone: 8192 * 8192
-    # bytes > 32 MiB is rejected before any device work
+    fake = 0x10000   # 16-byte aligned, never dereferenced: the calls fail validation
+    p = ctypes.c_void_p(fake)
+    # a state whose arrays are all set, without transposed copies: the
+    # scratch holds dY_q alone, and 8192 * 8192 bytes > 32 MiB is rejected
+    # before any device work
+    st = F.LinearStateC(*([fake] * len(F.LinearStateC._fields_)))
+    st.x_qt = st.w_qt = None
     assert fn(p, 8192, 8192, 4096, ctypes.byref(rec), ctypes.byref(st), p, p, 0, None) == -2
     assert "scratch" in F.fp8_last_error()
     # with them it also holds dY_q^T: 2 * 8192 * 4096 bytes > 32 MiB
-    st_t = F.LinearStateC()
-    st_t.x_qt = st_t.w_qt = 0x10000
+    st_t = F.LinearStateC(*([fake] * len(F.LinearStateC._fields_)))
     assert fn(p, 8192, 4096, 4096, ctypes.byref(rec), ctypes.byref(st_t), p, p, 0, None) == -2
     assert "scratch" in F.fp8_last_error()
 
