@@ -383,7 +383,7 @@ def linear_bwd(dY_bits, recipe: Recipe, st: LinearState, dW_prev=None, rows_dx=N
         return dX, (dW, dWabs)
     sx, sw = st.sinv_fwd
     dy_q, dy_qt, sdy = _per_tensor_operand(st, ROLE_DY, dY_bits, E5M2, recipe)
-    st.dy_q = dy_q
+    st.dy_q, st.dy_qt, st.sinv_bwd = dy_q, dy_qt, sdy
     dX = _gemm_rows(dy_q, E5M2, st.w_qt, E4M3, sdy, sw, rows_dx)
     dW, dWabs = _gemm_rows(dy_qt, E5M2, st.x_qt, E4M3, sdy, sx, rows_dw)
     if dW_prev is not None:

@@ -28,6 +28,7 @@ __all__ = [
     "fp8_quantize_counted", "fp8_quantize_sr", "fp8_gemm", "fp8_gemm_group", "GemmArgsC",
     "fp8_workspace_size",
     "fp8_linear_fwd", "fp8_linear_bwd", "fp8_last_error", "fp8_device_status",
+    "check_device_status", "Fp8NumericsError", "STATUS_TIMEOUT", "STATUS_NONFINITE",
 ]
 
 E4M3, E5M2 = 0, 1
@@ -136,6 +137,11 @@ def lib() -> ctypes.CDLL:
 
 def fp8_last_error() -> str:
     return lib().fp8_last_error().decode()
+
+
+class Fp8NumericsError(RuntimeError):
+    """A scale update met a non-finite amax (a NaN or Inf in a cast tensor,
+    or still in its amax history) and kept the previous scale."""
 
 
 def _check(status: int) -> None:
@@ -379,6 +385,24 @@ def fp8_device_status(clear: bool = True) -> int:
     return st.value
 
 
+STATUS_TIMEOUT = 1     # bit 0 of the device status word: a bounded wait gave up
+STATUS_NONFINITE = 2   # bit 1: a scale update met a non-finite amax
+
+
+def check_device_status() -> None:
+    """Synchronise the device, read and clear the status word, and raise if a
+    kernel reported a problem since the last read: Fp8Error with status
+    FP8_ERR_TIMEOUT when a bounded wait gave up (that call's outputs are
+    incomplete), else Fp8NumericsError when a scale update met a NaN or Inf
+    (the previous scale was kept)."""
+    st = fp8_device_status(clear=True)
+    if st & STATUS_TIMEOUT:
+        raise Fp8Error(-5, "a kernel's bounded wait gave up; its outputs are incomplete")
+    if st & STATUS_NONFINITE:
+        raise Fp8NumericsError("a scale update met a non-finite amax (NaN or Inf in a cast "
+                               "tensor or its amax history); the previous scale was kept")
+
+
 # ------------------------------------------------------------- layer object
 
 class Fp8Linear:
@@ -390,11 +414,15 @@ class Fp8Linear:
     transposes (per-tensor recipes): keep transposed copies of the forward's
     codes for K-major backward GEMMs; by default (False) the backward reads
     the codes as stored (MN-major) and no copy is made.  The block-wise and
-    per-row recipes always keep them (their transposed codes differ)."""
+    per-row recipes always keep them (their transposed codes differ).
+    check_status: after every forward / backward, synchronise and raise
+    (check_device_status) if a kernel timed out or a scale update met a
+    non-finite amax -- off by default, since it waits for the device."""
 
     def __init__(self, M: int, N: int, K: int, recipe: Recipe | None = None, device="cuda",
-                 sr_seed: int = 0, transposes: bool = False):
+                 sr_seed: int = 0, transposes: bool = False, check_status: bool = False):
         self.M, self.N, self.K = M, N, K
+        self.check_status = bool(check_status)
         self.recipe = recipe or Recipe()
         dev = torch.device(device)
         H = self.recipe.history_len if self.recipe.scaling == SCALING_DELAYED else 1
@@ -448,6 +476,8 @@ class Fp8Linear:
         if Y is None:
             Y = torch.empty(self.M, self.N, dtype=torch.bfloat16, device=X.device)
         fp8_linear_fwd(X, W, self.recipe, self.c_state, Y, None, stream, bias=bias)
+        if self.check_status:
+            check_device_status()
         return Y
 
     def backward(self, dY: torch.Tensor, dX=None, dW=None, accumulate_dW: bool = False,
@@ -460,6 +490,8 @@ class Fp8Linear:
             dW = torch.zeros(self.N, self.K, dtype=torch.float32, device=dY.device)
         fp8_linear_bwd(dY, self.M, self.N, self.K, self.recipe, self.c_state, dX, dW,
                        accumulate_dW, self.workspace, stream, dbias=dbias)
+        if self.check_status:
+            check_device_status()
         return dX, dW
 
     def state_dict(self) -> dict:

@@ -620,6 +620,21 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
     return FP8_OK;
 }
 
+// Test hook, not part of the ABI that include/fp8linear.h declares: the
+// time limit of the single-CTA GEMM kernel's epilogue wait for a full
+// accumulator, in nanoseconds (default and maximum 2 s).  A test sets a short
+// limit so that this bounded wait runs out on a long GEMM -- the kernel then
+// returns early with bit 0 of fp8_device_status() set and the output left
+// incomplete -- and restores the default afterwards.  The limit applies to
+// kernels launched after the call on the current device.
+int fp8_test_set_epilogue_wait_ns(uint64_t ns) {
+    if (ns > 2000000000ull)
+        return set_error(FP8_ERR_INVALID_ARG,
+                         "fp8_test_set_epilogue_wait_ns: %llu ns is above the 2 s default",
+                         static_cast<unsigned long long>(ns));
+    return set_epilogue_wait_ns(ns);
+}
+
 int fp8_device_status(int* status, int clear) {
     if (!status) return set_error(FP8_ERR_INVALID_ARG, "fp8_device_status: NULL pointer");
     unsigned v = 0;

@@ -49,6 +49,14 @@ namespace fp8 {
 
 __device__ unsigned int g_device_status = 0;
 
+// Time limit of the single-CTA kernel's epilogue wait for a full accumulator
+// (the wait of the epilogue warps, which have nothing asynchronous in flight
+// behind them: when it gives up, the producer and MMA threads finish or stop
+// at their own bounded waits, drain what they issued, and the kernel returns
+// with bit 0 of the status word set).  The library never changes it; the test
+// hook fp8_test_set_epilogue_wait_ns() shortens it to make that path run.
+__device__ uint64_t g_epilogue_wait_ns = ptx::kWaitTimeoutNs;
+
 namespace {
 
 constexpr int BM = 128;
@@ -85,7 +93,7 @@ __device__ __forceinline__ void load_bias8(float (&b)[8], const __nv_bfloat16* b
 // so that the CTAs resident at one time share A and B panels in L2.  A
 // larger group re-reads each B panel from DRAM fewer times (once per group)
 // at the cost of more A panels resident at once.
-template <int GROUP = 8>
+template <int GROUP = 16>
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk,
                                             int& n_blk) {
     const int per_group = GROUP * num_n;
@@ -418,13 +426,15 @@ __global__ void __launch_bounds__(256, 1)
         const int row = qd * 32 + lane;
         uint32_t acc = 0, acc_phase = 0;
         const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
+        const uint64_t wait_ns = g_epilogue_wait_ns;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             int m_blk, n_blk;
             tile_coords<>(tile, p.num_m, p.num_n, m_blk, n_blk);
             if (rmw)
                 prefetch_row(static_cast<int64_t>(m_blk) * BM + row, static_cast<int64_t>(n_blk) * BN,
                              BN, p);
-            bool ok = (lane == 0) ? ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag) : false;
+            bool ok = (lane == 0) ? ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, wait_ns)
+                                  : false;
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
             __syncwarp();
@@ -1898,6 +1908,13 @@ unsigned* device_status_word() {
     }
     if (dev < 64) ptr[dev] = static_cast<unsigned*>(p);
     return static_cast<unsigned*>(p);
+}
+
+int set_epilogue_wait_ns(uint64_t ns) {
+    const cudaError_t e = cudaMemcpyToSymbol(g_epilogue_wait_ns, &ns, sizeof(ns));
+    if (e != cudaSuccess)
+        return set_error(FP8_ERR_CUDA, "setting the epilogue wait limit: %s", cudaGetErrorString(e));
+    return FP8_OK;
 }
 
 int read_device_status(unsigned* status, bool clear) {

@@ -179,6 +179,10 @@ int launch_gemm_group(const GemmArgs& g1, const GemmArgs& g2, cudaStream_t strea
 // update saw a non-finite amax).
 int read_device_status(unsigned* status, bool clear);
 
+// Sets the epilogue wait limit of the single-CTA GEMM kernel on the current
+// device (g_epilogue_wait_ns; synchronous).
+int set_epilogue_wait_ns(uint64_t ns);
+
 // Device address of the status word on the current device (null if it
 // cannot be looked up), for kernels outside gemm.cu to set bits in.
 unsigned* device_status_word();

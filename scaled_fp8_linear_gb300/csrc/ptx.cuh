@@ -61,16 +61,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Returns false (without waiting further) when `abort_flag` is raised by
 // another role or when the wait exceeds the time limit; in the latter case
 // it raises the flag itself.
+// limit_ns: a shorter limit for a wait with no asynchronous work of its own
+// behind it (see g_epilogue_wait_ns in gemm.cu).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile uint32_t* abort_flag) {
+                                          volatile uint32_t* abort_flag,
+                                          uint64_t limit_ns = kWaitTimeoutNs) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer();
+    const bool short_limit = limit_ns < kWaitTimeoutNs;   // checked at every poll
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((it & 255u) == 0) {
+        if ((it & 255u) == 0 || short_limit) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitTimeoutNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 *abort_flag = 1u;
                 return false;
             }

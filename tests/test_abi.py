@@ -267,3 +267,11 @@ def test_noalloc_checks_arguments_before_touching_the_device():
     assert fn(p, 8192, 8192, 4096, ctypes.byref(F.Recipe()), ctypes.byref(st), p, p, 0,
               None) == -2
     assert "scratch" in F.fp8_last_error()
+
+
+def test_epilogue_wait_hook_refuses_a_longer_limit():
+    fn = F.lib().fp8_test_set_epilogue_wait_ns
+    fn.argtypes = [ctypes.c_uint64]
+    fn.restype = ctypes.c_int
+    assert fn(2_000_000_001) == -1
+    assert "2 s" in F.fp8_last_error()

@@ -142,6 +142,27 @@ def test_block_forward():
     assert_gemm_bound(Y, Yo, Yabs)
 
 
+def _align256(n):
+    return (n + 255) // 256 * 256
+
+
+def _check_block_dy(layer, ost, M, N):
+    """The block-wise backward's dY casts, as the workspace holds them: dY_q
+    [M x N] with its 1x128 scales [M][N/128] along N, and dY_q^T [N x M] with
+    its 1x128 scales [N][M/128] along the tokens -- bit-exact against the
+    oracle's block casts of dY and dY^T."""
+    ws = layer.workspace
+    mn = M * N
+    o_qt, o_s = _align256(mn), 2 * _align256(mn)
+    o_st = o_s + _align256(4 * (mn // 128))
+    assert np.array_equal(u8(ws[:mn]).reshape(M, N), ost.dy_q)
+    assert np.array_equal(u8(ws[o_qt:o_qt + mn]).reshape(N, M), ost.dyt_q)
+    s = ws[o_s:o_s + 4 * (mn // 128)].view(torch.float32).cpu().numpy().reshape(M, N // 128)
+    st = ws[o_st:o_st + 4 * (mn // 128)].view(torch.float32).cpu().numpy().reshape(N, M // 128)
+    assert np.array_equal(f32bits(s), f32bits(ost.dy_s))
+    assert np.array_equal(f32bits(st), f32bits(ost.dyt_s))
+
+
 @pytest.mark.parametrize("M,N,K", [(256, 384, 512), (1024, 768, 1280), (640, 896, 384)])
 @pytest.mark.parametrize("pow2", [False, True], ids=["fp32_scales", "pow2_scales"])
 def test_block_training_steps(M, N, K, pow2):
@@ -170,6 +191,7 @@ def test_block_training_steps(M, N, K, pow2):
         assert np.array_equal(f32bits(layer.x_sinv_t.cpu().numpy()), f32bits(ost.xt_sinv))
         assert np.array_equal(u8(layer.w_qt), ost.wt_q)
         assert np.array_equal(f32bits(layer.w_sinv_t.cpu().numpy()), f32bits(ost.wt_sinv))
+        _check_block_dy(layer, ost, M, N)
         assert_gemm_bound(Y, Yo, Yabs, what=f"Y step {step}")
         assert_gemm_bound(dX, dXo, dXabs, what=f"dX step {step}")
         assert_gemm_bound(dW, dWo, dWabs, prev=prev if acc else None, what=f"dW step {step}")
@@ -234,69 +256,150 @@ def test_checkpoint_restore_gives_identical_next_step():
 
 # ----------------------------------------------------------- full-size shapes
 
-def _sample_rows(n, k, seed):
+LINEARS_7B = [("qkv", 4096, 12288), ("o", 4096, 4096), ("gate", 4096, 11008),
+              ("up", 4096, 11008), ("down", 11008, 4096)]
+LINEARS_70B = [("qkv", 8192, 10240), ("o", 8192, 8192), ("gate", 8192, 28672),
+               ("up", 8192, 28672), ("down", 28672, 8192)]
+SAMPLE = 64   # seeded rows and full columns checked per GEMM output
+
+
+def _sample(n, k, seed):
+    """k distinct sorted indices of 0..n-1 (the first and last included)."""
     rng = np.random.default_rng(seed)
-    return np.sort(np.concatenate([[0, n - 1], rng.choice(n, k, replace=False)]))
+    inner = rng.choice(np.arange(1, n - 1), min(k, n) - 2, replace=False)
+    return np.sort(np.concatenate([[0, n - 1], inner])).astype(np.int64)
 
 
-@pytest.mark.parametrize("name,M,N,K,recipe,transposes", [
-    ("llama2-7b qkv, delayed", 8192, 12288, 4096, F.Recipe(F.SCALING_DELAYED, history_len=16), False),
-    ("llama2-7b qkv, delayed, transposed copies", 8192, 12288, 4096,
-     F.Recipe(F.SCALING_DELAYED, history_len=16), True),
-    ("llama2-7b down, delayed", 8192, 4096, 11008, F.Recipe(F.SCALING_DELAYED, history_len=16), False),
-    ("llama2-70b gate, dynamic", 4096, 28672, 8192, F.Recipe(F.SCALING_DYNAMIC), False),
-    ("llama2-70b down, dynamic", 4096, 8192, 28672, F.Recipe(F.SCALING_DYNAMIC), False)])
-def test_full_size_linear_sampled(name, M, N, K, recipe, transposes):
+def _columns(A, fa, B, fb, sa, sb, nrows, cols, ga=oracle.GRAN_TENSOR, gb=oracle.GRAN_TENSOR):
+    """Full columns `cols` of A . B^T (all nrows rows) from the oracle's
+    codes and factors, as [nrows x len(cols)]."""
+    ii = np.repeat(np.arange(nrows, dtype=np.int64), len(cols))
+    jj = np.tile(cols, nrows)
+    D, Dabs = oracle.gemm_entries(A, fa, B, fb, sa, sb, ii, jj, ga, gb)
+    return D.reshape(nrows, len(cols)), Dabs.reshape(nrows, len(cols))
+
+
+def _outlier_channels(K):
+    return 43 if K == 11008 else max(1, K // 256)
+
+
+FULL_CASES = (
+    [(f"llama2-7b {n}, delayed", 8192, N, K, F.SCALING_DELAYED, False, 1)
+     for n, K, N in LINEARS_7B]
+    + [("llama2-7b qkv, delayed, transposed copies", 8192, 12288, 4096, F.SCALING_DELAYED,
+        True, 1)]
+    + [(f"llama2-70b {n}, dynamic, 2 micro-batches", 4096, N, K, F.SCALING_DYNAMIC, False, 2)
+       for n, K, N in LINEARS_70B])
+
+
+@pytest.mark.parametrize("name,M,N,K,scaling,transposes,micro_batches", FULL_CASES,
+                         ids=[c[0] for c in FULL_CASES])
+def test_full_size_linear_sampled(name, M, N, K, scaling, transposes, micro_batches):
+    """Every linear of the two transformer blocks at full size, with the
+    oracle's own state machine: X, W and dY codes and all scales bit-exact;
+    64 seeded rows and 64 seeded full columns of each of Y, dX and dW within
+    the GEMM bound.  The Llama-2-70B cases accumulate dW over two
+    micro-batches (the second checked against the first's dW plus the
+    oracle's second product)."""
+    recipe = (F.Recipe(F.SCALING_DELAYED, history_len=16) if scaling == F.SCALING_DELAYED
+              else F.Recipe(F.SCALING_DYNAMIC))
     layer = F.Fp8Linear(M, N, K, recipe, device=DEV, transposes=transposes)
-    X = synthetic.with_outlier_channels((M, K), 1.0, max(1, K // 256), 50.0, seed=1, device=DEV)
-    W = synthetic.normal((N, K), 0.02, seed=2, device=DEV)
-    dY = synthetic.normal((M, N), 1e-3, seed=3, device=DEV)
-    Y = layer.forward(X, W)
-    dX, dW = layer.backward(dY)
-    torch.cuda.synchronize()
     orec = _orecipe(recipe)
     ost = oracle.LinearState(orec)
-    bx, bw, bdy = bits(X), bits(W), bits(dY)
-    # scales (whole-tensor amax) and quantised operands, bit-exact
-    rows_y = _sample_rows(M, 6, 1)
-    rows_dw = _sample_rows(N, 6, 2)
-    Yo, Yabs = oracle.linear_fwd(bx, bw, orec, ost, rows=rows_y)
-    (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(bdy, orec, ost, rows_dx=rows_y, rows_dw=rows_dw)
-    assert np.array_equal(u8(layer.x_q), ost.x_q)
-    assert np.array_equal(u8(layer.w_q), ost.w_q)
-    if transposes:
-        assert np.array_equal(u8(layer.w_qt), ost.w_qt)
-    _check_state(layer, ost)
-    ry, rw = torch.as_tensor(rows_y, device=DEV), torch.as_tensor(rows_dw, device=DEV)
-    assert_gemm_bound(Y[ry], Yo, Yabs, what=name + " Y")
-    assert_gemm_bound(dX[ry], dXo, dXabs, what=name + " dX")
-    assert_gemm_bound(dW[rw], dWo, dWabs, what=name + " dW")
+    W = synthetic.normal((N, K), 0.02, seed=2, device=DEV)
+    bw = bits(W)
+    dW = torch.zeros(N, K, dtype=torch.float32, device=DEV)
+    rows_m, cols_n = _sample(M, SAMPLE, 1), _sample(N, SAMPLE, 2)
+    rows_n, cols_k = _sample(N, SAMPLE, 3), _sample(K, SAMPLE, 4)
+    tm, tn, tk = (torch.as_tensor(v, device=DEV) for v in (rows_m, rows_n, cols_k))
+    tcn = torch.as_tensor(cols_n, device=DEV)
+    prev_r = prev_c = None
+    for mb in range(micro_batches):
+        X = synthetic.with_outlier_channels((M, K), 1.0, _outlier_channels(K), 50.0,
+                                            seed=10 + mb, device=DEV)
+        dY = synthetic.normal((M, N), 1e-3, seed=20 + mb, device=DEV)
+        Y = layer.forward(X, W)
+        dX, _ = layer.backward(dY, dW=dW, accumulate_dW=mb > 0)
+        torch.cuda.synchronize()
+        Yo, Yabs = oracle.linear_fwd(bits(X), bw, orec, ost, rows=rows_m)
+        (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(bits(dY), orec, ost, rows_dx=rows_m,
+                                                       rows_dw=rows_n)
+        # the quantised operands (dY's codes live in the workspace) and every scale
+        assert np.array_equal(u8(layer.x_q), ost.x_q)
+        assert np.array_equal(u8(layer.w_q), ost.w_q)
+        assert np.array_equal(u8(layer.workspace[:M * N]).reshape(M, N), ost.dy_q)
+        if transposes:
+            assert np.array_equal(u8(layer.x_qt), ost.x_qt)
+            assert np.array_equal(u8(layer.w_qt), ost.w_qt)
+        _check_state(layer, ost)
+        sx, sw = ost.sinv_fwd
+        sdy = ost.sinv_bwd
+        Yc, Ycabs = _columns(ost.x_q, F.E4M3, ost.w_q, F.E4M3, sx, sw, M, cols_n)
+        dXc, dXcabs = _columns(ost.dy_q, F.E5M2, ost.w_qt, F.E4M3, sdy, sw, M, cols_k)
+        dWc, dWcabs = _columns(ost.dy_qt, F.E5M2, ost.x_qt, F.E4M3, sdy, sx, N, cols_k)
+        what = f"{name}, micro-batch {mb}"
+        assert_gemm_bound(Y[tm], Yo, Yabs, what=what + " Y rows")
+        assert_gemm_bound(Y[:, tcn], Yc, Ycabs, what=what + " Y columns")
+        assert_gemm_bound(dX[tm], dXo, dXabs, what=what + " dX rows")
+        assert_gemm_bound(dX[:, tk], dXc, dXcabs, what=what + " dX columns")
+        if prev_r is None:
+            assert_gemm_bound(dW[tn], dWo, dWabs, what=what + " dW rows")
+            assert_gemm_bound(dW[:, tk], dWc, dWcabs, what=what + " dW columns")
+        else:
+            assert_gemm_bound(dW[tn], dWo + prev_r, dWabs, prev=prev_r, what=what + " dW rows")
+            assert_gemm_bound(dW[:, tk], dWc + prev_c, dWcabs, prev=prev_c,
+                              what=what + " dW columns")
+        prev_r = dW[tn].cpu().numpy().astype(np.float64)
+        prev_c = dW[:, tk].cpu().numpy().astype(np.float64)
+
+
+BLOCK_SAMPLE = 32
 
 
 @pytest.mark.parametrize("M,N,K", [(16384, 18432, 7168), (16384, 7168, 18432)])
 @pytest.mark.parametrize("pow2", [False, True], ids=["fp32_scales", "pow2_scales"])
-def test_full_size_block_gemm_sampled(M, N, K, pow2):
-    """Block-wise scaled forward at the DeepSeek-style shapes."""
-    layer = F.Fp8Linear(M, N, K, F.Recipe(F.SCALING_BLOCK, pow2=pow2), device=DEV)
+def test_full_size_block_layer_sampled(M, N, K, pow2):
+    """The block-wise layer (1x128 activations and gradients, 128x128
+    weights) forward and backward at the DeepSeek-style shapes: every code
+    and block scale of X, X^T, W, W^T, dY and dY^T bit-exact against the
+    oracle's casts; 32 seeded rows and 32 full columns of Y, dX and dW within
+    the GEMM bound."""
+    rec = F.Recipe(F.SCALING_BLOCK, pow2=pow2)
+    layer = F.Fp8Linear(M, N, K, rec, device=DEV)
     X = synthetic.student_t_rows((M, K), 1.0, 3, seed=11, device=DEV)
     W = synthetic.student_t_rows((N, K), 0.02, 3, seed=12, device=DEV)
+    dY = synthetic.normal((M, N), 1e-3, seed=13, device=DEV)
     Y = layer.forward(X, W)
+    dX, dW = layer.backward(dY)
     torch.cuda.synchronize()
-    rows = _sample_rows(M, 8, 3)
-    x_q, x_s = layer.x_q.cpu().numpy(), layer.x_sinv.cpu().numpy()
-    # the quantised rows and their scales against the oracle's block cast of those rows
-    qo, so = oracle.block_quantize(bits(X[torch.as_tensor(rows, device=DEV)]), F.E4M3, 1, pow2)
-    assert np.array_equal(x_q[rows], qo)
-    assert np.array_equal(f32bits(x_s[rows]), f32bits(so))
-    wq, ws = oracle.block_quantize(bits(W), F.E4M3, 128, pow2)
-    assert np.array_equal(u8(layer.w_q), wq)
-    assert np.array_equal(f32bits(layer.w_sinv.cpu().numpy()), f32bits(ws))
-    ii = np.repeat(rows, N)
-    jj = np.tile(np.arange(N), rows.shape[0])
-    D, Dabs = oracle.gemm_entries(x_q, F.E4M3, wq, F.E4M3, x_s, ws, ii, jj, F.GRAN_1x128,
-                                  F.GRAN_128x128)
-    assert_gemm_bound(Y[torch.as_tensor(rows, device=DEV)], D.reshape(len(rows), N),
-                      Dabs.reshape(len(rows), N))
+    orec = _orecipe(rec)
+    ost = oracle.LinearState(orec)
+    rows_m, cols_n = _sample(M, BLOCK_SAMPLE, 5), _sample(N, BLOCK_SAMPLE, 6)
+    rows_n, cols_k = _sample(N, BLOCK_SAMPLE, 7), _sample(K, BLOCK_SAMPLE, 8)
+    Yo, Yabs = oracle.linear_fwd(bits(X), bits(W), orec, ost, rows=rows_m)
+    (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(bits(dY), orec, ost, rows_dx=rows_m,
+                                                   rows_dw=rows_n)
+    for got, want in ((layer.x_q, ost.x_q), (layer.x_qt, ost.xt_q), (layer.w_q, ost.w_q),
+                      (layer.w_qt, ost.wt_q)):
+        assert np.array_equal(u8(got), want)
+    for got, want in ((layer.x_sinv, ost.x_sinv), (layer.x_sinv_t, ost.xt_sinv),
+                      (layer.w_sinv, ost.w_sinv), (layer.w_sinv_t, ost.wt_sinv)):
+        assert np.array_equal(f32bits(got.cpu().numpy()), f32bits(want))
+    _check_block_dy(layer, ost, M, N)
+    G1, G2 = oracle.GRAN_1x128, oracle.GRAN_128x128
+    Yc, Ycabs = _columns(ost.x_q, F.E4M3, ost.w_q, F.E4M3, ost.x_sinv, ost.w_sinv, M, cols_n,
+                         G1, G2)
+    dXc, dXcabs = _columns(ost.dy_q, F.E5M2, ost.wt_q, F.E4M3, ost.dy_s, ost.wt_sinv, M, cols_k,
+                           G1, G2)
+    dWc, dWcabs = _columns(ost.dyt_q, F.E5M2, ost.xt_q, F.E4M3, ost.dyt_s, ost.xt_sinv, N,
+                           cols_k, G1, G1)
+    tm, tn, tk = (torch.as_tensor(v, device=DEV) for v in (rows_m, rows_n, cols_k))
+    assert_gemm_bound(Y[tm], Yo, Yabs, what="Y rows")
+    assert_gemm_bound(Y[:, torch.as_tensor(cols_n, device=DEV)], Yc, Ycabs, what="Y columns")
+    assert_gemm_bound(dX[tm], dXo, dXabs, what="dX rows")
+    assert_gemm_bound(dX[:, tk], dXc, dXcabs, what="dX columns")
+    assert_gemm_bound(dW[tn], dWo, dWabs, what="dW rows")
+    assert_gemm_bound(dW[:, tk], dWc, dWcabs, what="dW columns")
 
 
 def test_step_replays_from_a_cuda_graph():
