@@ -612,12 +612,17 @@ def e2e_pass(F, wl: Workload, dev, args, stream):
     and per micro-batch of its X and dY, from pinned memory;
     fp8_linear_fwd + fp8_linear_bwd; D2H of Y and dX per micro-batch and of
     dW once the last micro-batch has accumulated into it -- all inside the
-    timed region.  Copies run on their own streams so that the next unit's
-    inputs arrive and the previous one's results leave while the current
-    unit computes (two device buffer sets for X, dY, Y, dX; per-linear W and
-    dW buffers; event-ordered and pipelined across steps as a training loop
-    would be)."""
+    timed region.  The copies run on their own streams, ordered by events, so
+    that they overlap the compute and each other as a training loop's would:
+    X and dY of a unit (one micro-batch of one linear) arrive up to two units
+    ahead (three device buffer sets); a linear's W for the next step is
+    uploaded on a stream of its own once the step's last forward of that
+    linear has quantised the current one (the backward reads the codes, not
+    W); Y leaves while the backward runs, dX after it, and dW after the last
+    micro-batch, before the next step's first backward of that linear
+    overwrites it."""
     nl, MB, T = len(wl.linears), wl.micro_batches, wl.tokens
+    NB = 3
     recipe = wl.recipe(F)
     h_w, h_x, h_dy, h_y, h_dx, h_dw, layers = [], [], [], [], [], [], []
     for li, (name, K, N) in enumerate(wl.linears):
@@ -642,33 +647,35 @@ def e2e_pass(F, wl: Workload, dev, args, stream):
                 "Y": torch.empty(T * nmax, dtype=torch.bfloat16, device=dev),
                 "dX": torch.empty(T * kmax, dtype=torch.bfloat16, device=dev)}
 
-    bufs = [dbuf(), dbuf()]
-    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    bufs = [dbuf() for _ in range(NB)]
+    h2d_s, w_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     nbytes = lambda t: t.numel() * t.element_size()
     h2d = sum(nbytes(w) for w in h_w) + sum(nbytes(t) for ts in h_x + h_dy for t in ts)
     d2h = sum(nbytes(t) for ts in h_y + h_dx for t in ts) + sum(nbytes(t) for t in h_dw)
-    # Units g = (step * MB + mb) * nl + li alternate between the two device
-    # buffer sets, so the loads of the next unit (also across a step
-    # boundary) and the drains of the previous one run on the host link while
-    # the current one computes.  Each copy waits only for the last user of
-    # its own buffer.
-    computed, drained, w_used, dw_drained = {}, {}, {}, {}
+    # Units g = (step * MB + mb) * nl + li use device buffer set g % NB; each
+    # copy waits only for the last user of its own buffer.
+    computed, drained, w_loaded, dw_drained = {}, {}, {}, {}
     counter = [0]
+
+    def upload_w(li, after=None):
+        with torch.cuda.stream(w_s):
+            if after is not None:
+                w_s.wait_event(after)
+            d_w[li].copy_(h_w[li], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(w_s)
+            w_loaded[li] = ev
 
     def load_unit():
         g = counter[0]
         counter[0] += 1
         li, mb = g % nl, (g // nl) % MB
         _, K, N = wl.linears[li]
-        b = bufs[g % 2]
+        b = bufs[g % NB]
         loaded = torch.cuda.Event()
         with torch.cuda.stream(h2d_s):
-            if g - 2 in computed:
-                h2d_s.wait_event(computed.pop(g - 2))      # last reader of this set's inputs
-            if mb == 0:
-                if li in w_used:
-                    h2d_s.wait_event(w_used.pop(li))       # last forward that read W[li]
-                d_w[li].copy_(h_w[li], non_blocking=True)
+            if g - NB in computed:
+                h2d_s.wait_event(computed.pop(g - NB))     # last reader of this set's inputs
             b["X"][:T * K].view(T, K).copy_(h_x[li][mb], non_blocking=True)
             b["dY"][:T * N].view(T, N).copy_(h_dy[li][mb], non_blocking=True)
             loaded.record(h2d_s)
@@ -676,8 +683,10 @@ def e2e_pass(F, wl: Workload, dev, args, stream):
 
     def compute_and_drain(g, li, mb, K, N, b, loaded):
         stream.wait_event(loaded)
-        if g - 2 in drained:
-            stream.wait_event(drained.pop(g - 2))          # this set's outputs have left
+        if mb == 0:
+            stream.wait_event(w_loaded.pop(li))            # this step's W[li] has arrived
+        if g - NB in drained:
+            stream.wait_event(drained.pop(g - NB))         # this set's outputs have left
         if mb == 0 and li in dw_drained:
             stream.wait_event(dw_drained.pop(li))          # last step's dW[li] has left
         Y = b["Y"][:T * N].view(T, N)
@@ -687,7 +696,7 @@ def e2e_pass(F, wl: Workload, dev, args, stream):
         fwd_done = torch.cuda.Event()
         fwd_done.record(stream)
         if mb == MB - 1:
-            w_used[li] = fwd_done
+            upload_w(li, after=fwd_done)                   # the next step's W[li]
         with torch.cuda.stream(d2h_s):                     # Y leaves while the backward runs
             d2h_s.wait_event(fwd_done)
             h_y[li][mb].copy_(Y, non_blocking=True)
@@ -707,24 +716,28 @@ def e2e_pass(F, wl: Workload, dev, args, stream):
                 dwd.record(d2h_s)
                 dw_drained[li] = dwd
 
-    def steps(k):
-        """k steps, issued one unit ahead on the load stream."""
-        h2d_s.wait_stream(stream)                          # copies start after the start event
-        d2h_s.wait_stream(stream)
-        pending = load_unit()
-        for i in range(k * MB * nl):
-            nxt = load_unit() if i + 1 < k * MB * nl else None
-            compute_and_drain(*pending)
-            pending = nxt
-        stream.wait_stream(d2h_s)                          # the last results are on the host
-        stream.wait_stream(h2d_s)
+    def steps(k, first):
+        """k steps, loads issued up to NB - 1 units ahead."""
+        for st in (h2d_s, w_s, d2h_s):
+            st.wait_stream(stream)                         # copies start after the start event
+        if first:
+            for li in range(nl):
+                upload_w(li)
+        units = k * MB * nl
+        pending = [load_unit() for _ in range(min(NB - 1, units))]
+        for i in range(units):
+            if i + NB - 1 < units:
+                pending.append(load_unit())
+            compute_and_drain(*pending.pop(0))
+        for st in (h2d_s, w_s, d2h_s):
+            stream.wait_stream(st)                         # the last results are on the host
 
-    steps(max(1, min(args.warmup, 2)))
+    steps(max(1, min(args.warmup, 2)), True)
     torch.cuda.synchronize()
     n = max(1, min(args.steps, 10))
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    steps(n)
+    steps(n, False)
     b.record(stream)
     torch.cuda.synchronize()
     assert F.fp8_device_status() == 0
@@ -734,8 +747,9 @@ def e2e_pass(F, wl: Workload, dev, args, stream):
     return {"value": round(wl.flops_step() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "steps": n, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "copies": "pinned host <-> device on two copy streams, overlapped with compute and "
-                      "with each other across linears, micro-batches and steps",
+            "copies": "pinned host <-> device on three copy streams (inputs, weights, "
+                      "results), overlapped with compute and with each other across linears, "
+                      "micro-batches and steps",
             "host_link": link,
             "link_floor_ms": round(floor_ms, 3),
             "link_floor_note": "the time to move h2d and d2h bytes at the link rates measured "

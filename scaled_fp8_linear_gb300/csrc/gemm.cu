@@ -75,6 +75,7 @@ struct GemmParams {
     int out;          // FP8_OUT_BF16 / FP8_OUT_F32
     int accumulate;
     int a_mn, b_mn;   // operand stored MN-major ([K x M] / [K x N]); CTA-pair kernel only
+    int group;        // CTA-pair kernel: raster group (M-blocks), see pair_group()
 };
 
 // Eight bias values of columns n .. n+7 (n % 8 == 0) as fp32; every lane of
@@ -100,6 +101,18 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
     const int g = tile / per_group;
     const int first_m = g * GROUP;
     const int gsize = min(num_m - first_m, GROUP);
+    const int in_g = tile - g * per_group;
+    m_blk = first_m + in_g % gsize;
+    n_blk = in_g / gsize;
+}
+
+// The same walk with a run-time group size.
+__device__ __forceinline__ void tile_coords_g(int tile, int num_m, int num_n, int group,
+                                              int& m_blk, int& n_blk) {
+    const int per_group = group * num_n;
+    const int g = tile / per_group;
+    const int first_m = g * group;
+    const int gsize = min(num_m - first_m, group);
     const int in_g = tile - g * per_group;
     m_blk = first_m + in_g % gsize;
     n_blk = in_g / gsize;
@@ -561,7 +574,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 const CUtensorMap* ma = second ? &tmA2 : &tmA;
                 const CUtensorMap* mb = second ? &tmB2 : &tmB;
                 int m_blk, n_blk;
-                tile_coords<>(second ? u - t1 : u, q.num_m, q.num_n, m_blk, n_blk);
+                tile_coords_g(second ? u - t1 : u, q.num_m, q.num_n, q.group, m_blk, n_blk);
                 const int ya = m_blk * TILE + static_cast<int>(rank) * HALF;
                 const int yb = n_blk * TILE + static_cast<int>(rank) * HALF;
                 const bool a_mn = q.a_mn != 0, b_mn = q.b_mn != 0;
@@ -653,7 +666,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             const CUtensorMap* map = second ? &tmD2 : &tmD;
             const bool f32 = p.out == FP8_OUT_F32;
             int m_blk, n_blk;
-            tile_coords<>(second ? u - t1 : u, p.num_m, p.num_n, m_blk, n_blk);
+            tile_coords_g(second ? u - t1 : u, p.num_m, p.num_n, p.group, m_blk, n_blk);
             const int64_t m0 = static_cast<int64_t>(m_blk) * TILE + rank * HALF + qd * 32;
             const int64_t m = m0 + lane;
             bool ok = (lane == 0) ? ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag) : false;
@@ -1580,6 +1593,29 @@ int make_mnmajor_map(CUtensorMap* map, const void* ptr, int64_t MN, int64_t K) {
     return FP8_OK;
 }
 
+}  // namespace
+
+int make_bf16_box_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols,
+                      uint32_t box_cols, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return set_error(FP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return set_error(FP8_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for bf16 [%lld x %lld]",
+                         static_cast<int>(r), static_cast<long long>(rows),
+                         static_cast<long long>(cols));
+    return FP8_OK;
+}
+
+namespace {
+
 // Tensor map of the output D [M x N] (bf16 or FP32, row-major) for TMA stores
 // of boxes of 32 rows x 64 bytes (32 bf16 or 16 FP32 columns) with the
 // 64-byte swizzle.
@@ -1683,6 +1719,19 @@ __global__ void bias_rows_kernel(const __nv_bfloat16* __restrict__ bias, int64_t
 
 namespace {
 
+// Raster group of a CTA-pair problem: the group's A panels (GROUP blocks of
+// 256 rows by K bytes) are reused by every N-block of the sweep, so they
+// should stay in L2 (129 MB) next to the B panels in flight: at most 64 MB of
+// them, between 4 and 16 blocks.  Measured on the Llama-2 step GEMMs, 16 beat
+// 8 and 4 where the panels fit; with K = 28672 a group of 16 (117 MB) was
+// re-read from DRAM about once per wave.
+int pair_group(int64_t K) {
+    const int64_t panel = 256 * K;
+    int g = 16;
+    while (g > 4 && g * panel > (int64_t(64) << 20)) g >>= 1;
+    return g;
+}
+
 // Block-scaled GEMM with power-of-two factors on the CTA-pair block-scaled
 // MMA kernel (ga, gb: FP8_GRAN_1x128 / FP8_GRAN_128x128, flag removed; K > 0).
 int launch_gemm_mx(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
@@ -1696,6 +1745,8 @@ int launch_gemm_mx(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M
     p.fa = fa; p.fb = fb; p.ga = ga; p.gb = gb; p.sa = sa; p.sb = sb;
     p.bias = static_cast<const __nv_bfloat16*>(bias);
     p.D = D; p.out = out; p.accumulate = accumulate;
+    p.a_mn = p.b_mn = 0;
+    p.group = 0;   // the block-scaled MMA kernel uses its own raster group
     CUtensorMap tmA, tmB, tmD;
     int st = make_kmajor_map(&tmA, A, M, K, BM);
     if (st != FP8_OK) return st;
@@ -1731,6 +1782,7 @@ int launch_gemm_block(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_
     p.bias = static_cast<const __nv_bfloat16*>(bias);
     p.D = D; p.out = out; p.accumulate = accumulate;
     p.a_mn = p.b_mn = 0;
+    p.group = 0;   // the block kernels use their own raster group
     CUtensorMap tmA, tmB, tmD;
     int st = make_kmajor_map(&tmA, A, M, K, 128);
     if (st != FP8_OK) return st;
@@ -1803,6 +1855,7 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
     p.bias = static_cast<const __nv_bfloat16*>(bias);
     p.D = D; p.out = out; p.accumulate = accumulate;
     p.a_mn = a_mn; p.b_mn = b_mn;
+    p.group = pair_group(K);
 
     CUtensorMap tmA, tmB;
     int st = a_mn ? make_mnmajor_map(&tmA, A, M, K) : make_kmajor_map(&tmA, A, M, K, BM);
@@ -1857,6 +1910,7 @@ int pair_params(const GemmArgs& g, GemmParams& p, CUtensorMap& tmA, CUtensorMap&
     p.D = g.D; p.out = g.out; p.accumulate = g.accumulate;
     p.a_mn = (g.layout & FP8_LAYOUT_A_KM) != 0;
     p.b_mn = (g.layout & FP8_LAYOUT_B_KN) != 0;
+    p.group = pair_group(g.K);
     int st = p.a_mn ? make_mnmajor_map(&tmA, g.A, g.M, g.K) : make_kmajor_map(&tmA, g.A, g.M, g.K, BM);
     if (st != FP8_OK) return st;
     st = p.b_mn ? make_mnmajor_map(&tmB, g.B, g.N, g.K) : make_kmajor_map(&tmB, g.B, g.N, g.K, 128);

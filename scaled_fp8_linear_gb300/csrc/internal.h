@@ -3,6 +3,7 @@
 // functions only configure and enqueue kernels on `stream`.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -31,6 +32,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
+
+// Tensor map of a row-major bf16 matrix [rows x cols] for TMA loads of
+// box_rows x box_cols boxes (no swizzle; zero fill outside the matrix).
+// FP8_OK or a status with its message.
+int make_bf16_box_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols,
+                      uint32_t box_cols, uint32_t box_rows);
 
 // Number of SMs of the current device (cached per device).
 int num_sms();

@@ -17,6 +17,7 @@
 // non-negative floats: the result is exact and independent of order.
 #include <cfloat>
 #include <cstdint>
+#include <mutex>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -892,110 +893,168 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-// Dual 1x128 cast for the block-wise backward: one read of a 128 x 128 bf16
-// tile gives
+// Dual 1x128 cast for the block-wise backward: one read of each 128 x 128
+// bf16 tile gives
 //   q   [R x C]  with one scale per 1x128 row segment   (scale_inv [R][C/128])
 //   q_t [C x R]  with one scale per 1x128 segment of a column of x, i.e. the
 //                1x128 block cast of x^T                  (scale_inv_t [C][R/128]).
-// Phase 1 casts the rows (the 8 threads of a row reduce its amax with
-// shuffles) and stages the bf16 tile in shared memory; phase 2 gives each
-// column to two threads (64 rows each), which reduce the column amax through
-// shared memory and write 64 contiguous codes of q_t each.  R and C are
-// multiples of 128.
+// R and C are multiples of 128.
+//
+// Persistent CTAs (two per SM) walk the tiles; each keeps kDualStages tiles in
+// flight in a ring of shared-memory stages filled by TMA, so that the next
+// tile arrives while the current one is reduced and written (one CTA per tile
+// and plain loads left each tile's load latency exposed: about 0.65 of the
+// HBM bandwidth).  Per tile, thread t holds rows it*32 + t/8 (it = 0..3) and
+// columns 16*(t%8) .. +15:
+//   rows     the 8 threads of a row reduce its 128-element amax with shuffles,
+//            cast and write q (16 bytes each) and the row's scale;
+//   columns  the column maxima are reduced from registers (4 rows per thread,
+//            4 lanes per warp, then the 8 warps through shared memory); each
+//            thread casts its elements with their columns' scales into the
+//            byte staging S, which transpose_tile_out writes to q_t in whole
+//            128-byte row segments.
+constexpr int kDualStages = 2;
+constexpr int kDualTileBytes = 128 * 128 * 2;
+constexpr int kDualSmem = kDualStages * kDualTileBytes + 64 + 1024;
+
 template <int FMT>
-__global__ void __launch_bounds__(kThreads)
-    quantize_1x128_dual_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
-                               int64_t tiles_c, int pow2, uint8_t* __restrict__ q,
+__global__ void __launch_bounds__(kThreads, 2)
+    quantize_1x128_dual_kernel(const __grid_constant__ CUtensorMap tmX, int64_t rows, int64_t cols,
+                               int64_t tiles_c, int64_t tiles, int pow2, uint8_t* __restrict__ q,
                                float* __restrict__ scale_inv, uint8_t* __restrict__ qt,
-                               float* __restrict__ scale_inv_t) {
+                               float* __restrict__ scale_inv_t, unsigned* status) {
     ptx::griddep_launch_dependents();
-    ptx::griddep_wait();   // the previous kernel's results are visible
     __shared__ __align__(16) uint32_t S[128 * 32];          // column-scaled codes, swizzled rows
     __shared__ uint32_t colpart[kThreads / 32][64];         // per warp: 128 column maxima, 2 per word
     __shared__ __align__(16) float colscale[128];
-    const int64_t tile = blockIdx.x;
-    const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
+    __shared__ uint32_t abort_word;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + kDualStages * kDualTileBytes);
     const int t = threadIdx.x, cg = t & 7;
-    uint4 va[4], vb[4];
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int64_t r = r0 + it * 32 + (t >> 3);
-        const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + c0 + cg * 16);
-        va[it] = ldg_stream(src);
-        vb[it] = ldg_stream(src + 1);
-    }
-    // column maxima from registers: this thread's 4 rows of its 16 columns,
-    // then the 4 lanes of the warp with the same columns, then the 8 warps
-    uint32_t cm[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        cm[0] = absmax2(cm[0], va[it].x); cm[1] = absmax2(cm[1], va[it].y);
-        cm[2] = absmax2(cm[2], va[it].z); cm[3] = absmax2(cm[3], va[it].w);
-        cm[4] = absmax2(cm[4], vb[it].x); cm[5] = absmax2(cm[5], vb[it].y);
-        cm[6] = absmax2(cm[6], vb[it].z); cm[7] = absmax2(cm[7], vb[it].w);
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        cm[j] = __vmaxu2(cm[j], __shfl_xor_sync(0xFFFFFFFFu, cm[j], 8));
-        cm[j] = __vmaxu2(cm[j], __shfl_xor_sync(0xFFFFFFFFu, cm[j], 16));
-    }
-    if ((t & 31) < 8) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) colpart[t >> 5][cg * 8 + j] = cm[j];
-    }
-    // row blocks: each 128-element row segment of the tile has its own scale
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const uint4 a = va[it], b = vb[it];
-        const uint32_t m2 = absmax_vec(absmax_vec(0u, a), b);
-        uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-        const float sc = block_scale<FMT>(__uint_as_float(m << 16), pow2);
-        const int64_t r = r0 + it * 32 + (t >> 3);
-        *reinterpret_cast<uint4*>(q + r * cols + c0 + cg * 16) =
-            make_uint4(cvt4<FMT>(a.x, a.y, sc), cvt4<FMT>(a.z, a.w, sc), cvt4<FMT>(b.x, b.y, sc),
-                       cvt4<FMT>(b.z, b.w, sc));
-        if (cg == 0) scale_inv[r * (cols / 128) + c0 / 128] = __fdiv_rn(1.0f, sc);
+    if (t == 0) {
+        for (int st = 0; st < kDualStages; ++st) ptx::mbar_init(&full[st], 1);
+        abort_word = 0;
+        ptx::fence_barrier_init();
     }
     __syncthreads();
-    // column blocks: one scale per column of the tile (thread c < 128), kept in
-    // shared memory; then each thread casts its 4 x 16 elements with them into
-    // S, rows swizzled as in the per-tensor transpose, which then writes q_t
-    // in whole 128-byte row segments
-    if (t < 128) {
-        uint32_t w2 = 0;
+    ptx::griddep_wait();   // the previous kernel's results are visible
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    const int64_t mine = first < tiles ? (tiles - first + step - 1) / step : 0;
+    // the k-th tile of this CTA goes to stage k % kDualStages
+    auto issue = [&](int64_t k) {
+        const int64_t tile = first + k * step;
+        const int st = static_cast<int>(k % kDualStages);
+        ptx::mbar_arrive_expect_tx(&full[st], kDualTileBytes);
+        ptx::tma_load_2d(ring + st * kDualTileBytes, &tmX, &full[st],
+                         static_cast<int32_t>((tile % tiles_c) * 128),
+                         static_cast<int32_t>((tile / tiles_c) * 128));
+    };
+    if (t == 0)
+        for (int64_t k = 0; k < mine && k < kDualStages; ++k) issue(k);
+    int64_t k = 0;
+    for (; k < mine; ++k) {
+        const int st = static_cast<int>(k % kDualStages);
+        const uint32_t par = static_cast<uint32_t>(k / kDualStages) & 1u;
+        const int64_t tile = first + k * step;
+        const int64_t r0 = (tile / tiles_c) * 128, c0 = (tile % tiles_c) * 128;
+        // every thread sees the stage's bytes land; the verdict is the CTA's
+        // (all threads leave together if a wait gave up)
+        const bool ok = ptx::mbar_wait(&full[st], par, &abort_word);
+        if (!__syncthreads_and(ok)) break;
+        const uint8_t* tile_s = ring + st * kDualTileBytes;
+        uint4 va[4], vb[4];
 #pragma unroll
-        for (int g = 0; g < kThreads / 32; ++g) w2 = __vmaxu2(w2, colpart[g][t >> 1]);
-        const uint32_t m = (t & 1) ? (w2 >> 16) : (w2 & 0xFFFFu);
-        const float sc = block_scale<FMT>(__uint_as_float(m << 16), pow2);
-        colscale[t] = sc;
-        scale_inv_t[(c0 + t) * (rows / 128) + r0 / 128] = __fdiv_rn(1.0f, sc);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int rl = it * 32 + (t >> 3);
-        const uint32_t in[8] = {va[it].x, va[it].y, va[it].z, va[it].w,
-                                vb[it].x, vb[it].y, vb[it].z, vb[it].w};
-        uint32_t o[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float4 cs = *reinterpret_cast<const float4*>(&colscale[cg * 16 + 4 * k]);
-            const uint32_t w0 = in[2 * k], w1 = in[2 * k + 1];
-            const float f0 = __fmul_rn(__uint_as_float(w0 << 16), cs.x);
-            const float f1 = __fmul_rn(__uint_as_float(w0 & 0xFFFF0000u), cs.y);
-            const float f2 = __fmul_rn(__uint_as_float(w1 << 16), cs.z);
-            const float f3 = __fmul_rn(__uint_as_float(w1 & 0xFFFF0000u), cs.w);
-            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f0, f1), __NV_SATFINITE, Fp8Traits<FMT>::kind);
-            const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f2, f3), __NV_SATFINITE, Fp8Traits<FMT>::kind);
-            o[k] = lo | (hi << 16);
+        for (int it = 0; it < 4; ++it) {
+            const uint4* src = reinterpret_cast<const uint4*>(tile_s + (it * 32 + (t >> 3)) * 256 + cg * 32);
+            va[it] = src[0];
+            vb[it] = src[1];
         }
-        *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = make_uint4(o[0], o[1], o[2], o[3]);
+        __syncthreads();   // the stage has been read: refill it with tile k + kDualStages
+        if (t == 0 && k + kDualStages < mine) issue(k + kDualStages);
+        // column maxima from registers: this thread's 4 rows of its 16 columns,
+        // then the 4 lanes of the warp with the same columns, then the 8 warps
+        uint32_t cm[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            cm[0] = absmax2(cm[0], va[it].x); cm[1] = absmax2(cm[1], va[it].y);
+            cm[2] = absmax2(cm[2], va[it].z); cm[3] = absmax2(cm[3], va[it].w);
+            cm[4] = absmax2(cm[4], vb[it].x); cm[5] = absmax2(cm[5], vb[it].y);
+            cm[6] = absmax2(cm[6], vb[it].z); cm[7] = absmax2(cm[7], vb[it].w);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            cm[j] = __vmaxu2(cm[j], __shfl_xor_sync(0xFFFFFFFFu, cm[j], 8));
+            cm[j] = __vmaxu2(cm[j], __shfl_xor_sync(0xFFFFFFFFu, cm[j], 16));
+        }
+        if ((t & 31) < 8) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) colpart[t >> 5][cg * 8 + j] = cm[j];
+        }
+        // row blocks: each 128-element row segment of the tile has its own scale
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const uint4 a = va[it], b = vb[it];
+            const uint32_t m2 = absmax_vec(absmax_vec(0u, a), b);
+            uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+            const float sc = block_scale<FMT>(__uint_as_float(m << 16), pow2);
+            const int64_t r = r0 + it * 32 + (t >> 3);
+            *reinterpret_cast<uint4*>(q + r * cols + c0 + cg * 16) =
+                make_uint4(cvt4<FMT>(a.x, a.y, sc), cvt4<FMT>(a.z, a.w, sc), cvt4<FMT>(b.x, b.y, sc),
+                           cvt4<FMT>(b.z, b.w, sc));
+            if (cg == 0) scale_inv[r * (cols / 128) + c0 / 128] = __fdiv_rn(1.0f, sc);
+        }
+        __syncthreads();
+        // column blocks: one scale per column of the tile (thread c < 128)
+        if (t < 128) {
+            uint32_t w2 = 0;
+#pragma unroll
+            for (int g = 0; g < kThreads / 32; ++g) w2 = __vmaxu2(w2, colpart[g][t >> 1]);
+            const uint32_t m = (t & 1) ? (w2 >> 16) : (w2 & 0xFFFFu);
+            const float sc = block_scale<FMT>(__uint_as_float(m << 16), pow2);
+            colscale[t] = sc;
+            scale_inv_t[(c0 + t) * (rows / 128) + r0 / 128] = __fdiv_rn(1.0f, sc);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int rl = it * 32 + (t >> 3);
+            const uint32_t in[8] = {va[it].x, va[it].y, va[it].z, va[it].w,
+                                    vb[it].x, vb[it].y, vb[it].z, vb[it].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 cs = *reinterpret_cast<const float4*>(&colscale[cg * 16 + 4 * j]);
+                const uint32_t w0 = in[2 * j], w1 = in[2 * j + 1];
+                const float f0 = __fmul_rn(__uint_as_float(w0 << 16), cs.x);
+                const float f1 = __fmul_rn(__uint_as_float(w0 & 0xFFFF0000u), cs.y);
+                const float f2 = __fmul_rn(__uint_as_float(w1 << 16), cs.z);
+                const float f3 = __fmul_rn(__uint_as_float(w1 & 0xFFFF0000u), cs.w);
+                const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f0, f1), __NV_SATFINITE, Fp8Traits<FMT>::kind);
+                const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f2, f3), __NV_SATFINITE, Fp8Traits<FMT>::kind);
+                o[j] = lo | (hi << 16);
+            }
+            *reinterpret_cast<uint4*>(&S[rl * 32 + ((cg * 4) ^ tr_swz(rl))]) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        __syncthreads();
+        transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
+        __syncthreads();   // S, colpart and colscale are free for the next tile
     }
-    __syncthreads();
-    transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
+    if (t == 0) {
+        if (k < mine) {
+            // a wait gave up: let the copies already issued into the ring land
+            // (bounded) before the CTA's shared memory is released
+            uint32_t never = 0;
+            for (int64_t j = k; j < mine && j < k + kDualStages; ++j)
+                ptx::mbar_wait(&full[j % kDualStages],
+                               static_cast<uint32_t>(j / kDualStages) & 1u, &never);
+            if (status) atomicOr(status, 1u);   // bit 0: a bounded wait gave up
+        }
+    }
 }
 
 // ------------------------------------------------------ per-row scaling
@@ -1455,6 +1514,21 @@ cudaError_t launch_quantize_rows(const void* x, int64_t rows, int64_t cols, int 
                     : launch_row<1>(xs, rows, cols, pow2, q, scale_inv, q_t, scale_inv_t, stream);
 }
 
+// The dual cast's dynamic shared-memory limit, set once per device and format.
+template <typename Kernel>
+cudaError_t dual_smem_attr(Kernel k, int fmt) {
+    static std::mutex mu;
+    static bool done[64][2] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    const bool cached = dev >= 0 && dev < 64;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached && done[dev][fmt]) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kDualSmem);
+    if (e == cudaSuccess && cached) done[dev][fmt] = true;
+    return e;
+}
+
 cudaError_t launch_quantize_block(const void* x, int64_t rows, int64_t cols, int fmt, int gran,
                                   int pow2, uint8_t* q, float* scale_inv, uint8_t* q_t,
                                   float* scale_inv_t, cudaStream_t stream) {
@@ -1463,10 +1537,16 @@ cudaError_t launch_quantize_block(const void* x, int64_t rows, int64_t cols, int
     if (gran == 1 && q_t) {
         const int64_t tiles_c = cols / 128;
         const unsigned tiles = static_cast<unsigned>((rows / 128) * tiles_c);
-        if (fmt == 0)
-            launch_pdl(quantize_1x128_dual_kernel<0>, dim3(tiles), dim3(kThreads), 0, stream, xs, rows, cols, tiles_c, pow2, q, scale_inv, q_t, scale_inv_t);
-        else
-            launch_pdl(quantize_1x128_dual_kernel<1>, dim3(tiles), dim3(kThreads), 0, stream, xs, rows, cols, tiles_c, pow2, q, scale_inv, q_t, scale_inv_t);
+        CUtensorMap tmX;
+        if (make_bf16_box_map(&tmX, x, rows, cols, 128, 128) != FP8_OK) return cudaErrorInvalidValue;
+        auto k = fmt == 0 ? quantize_1x128_dual_kernel<0> : quantize_1x128_dual_kernel<1>;
+        const cudaError_t e = dual_smem_attr(k, fmt);
+        if (e != cudaSuccess) return e;
+        const int64_t ctas = 2 * static_cast<int64_t>(num_sms());
+        const unsigned grid = static_cast<unsigned>(tiles < ctas ? tiles : ctas);
+        launch_pdl(k, dim3(grid), dim3(kThreads), kDualSmem, stream, tmX, rows, cols, tiles_c,
+                   static_cast<int64_t>(tiles), pow2, q, scale_inv, q_t, scale_inv_t,
+                   device_status_word());
     } else if (gran == 1) {
         const int64_t pairs = (rows * (cols / 128) + 1) / 2;
         const int grid = grid_for(pairs, kThreads / 32);
