@@ -761,7 +761,6 @@ struct BpCfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int SMEM = STAGES * STAGE_BYTES + EPI * (2048 + 4 * CW * 4) + 256 + 1024;
 };
-constexpr int kBpGroup = 16;           // raster group (M-blocks of 256 rows)
 // 256 x 128 tiles, four TMEM buffers (three K blocks of slack for the
 // promotion), 8 promotion warps of 64 columns.  Measured on the 16384 x 18432
 // x 7168 shapes: 256 x 256 tiles with two buffers of 256 columns were slower
@@ -934,7 +933,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
             bool ok = true;
             for (int u = pair; ok && u < num_units; u += npairs) {
                 int m_blk, n_blk;
-                tile_coords<kBpGroup>(u, p.num_m, p.num_n, m_blk, n_blk);
+                tile_coords_g(u, p.num_m, p.num_n, p.group, m_blk, n_blk);
                 const int ya = m_blk * 256 + static_cast<int>(rank) * 128;
                 const int yb = n_blk * TN + static_cast<int>(rank) * (TN / 2);
                 for (int kb = 0; kb < KB; ++kb) {
@@ -1004,7 +1003,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
         bool ok = true;
         for (int u = pair; ok && u < num_units; u += npairs) {
             int m_blk, n_blk;
-            tile_coords<kBpGroup>(u, p.num_m, p.num_n, m_blk, n_blk);
+            tile_coords_g(u, p.num_m, p.num_n, p.group, m_blk, n_blk);
             const int64_t m0 = static_cast<int64_t>(m_blk) * 256 + rank * 128 + qd * 32;
             const int64_t m = m0 + lane;
             const int64_t m_safe = m < p.M ? m : p.M - 1;
@@ -1300,7 +1299,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
             bool ok = true;
             for (int u = pair; ok && u < num_units; u += npairs) {
                 int m_blk, n_blk;
-                tile_coords<>(u, p.num_m, p.num_n, m_blk, n_blk);
+                tile_coords_g(u, p.num_m, p.num_n, p.group, m_blk, n_blk);
                 const int ya = m_blk * TILE + static_cast<int>(rank) * HALF;
                 const int yb = n_blk * TILE + static_cast<int>(rank) * HALF;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -1385,7 +1384,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
         bool live = true;
         for (int u = pair; u < num_units; u += npairs) {
             int m_blk, n_blk;
-            tile_coords<>(u, p.num_m, p.num_n, m_blk, n_blk);
+            tile_coords_g(u, p.num_m, p.num_n, p.group, m_blk, n_blk);
             const int64_t a0 = static_cast<int64_t>(m_blk) * TILE + rank * HALF;
             const int64_t b0 = static_cast<int64_t>(n_blk) * TILE;
             for (int s2 = 0; s2 < num_slots; ++s2) {
@@ -1458,7 +1457,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
         uint32_t acc_phase = 0;
         for (int u = pair; u < num_units; u += npairs) {
             int m_blk, n_blk;
-            tile_coords<>(u, p.num_m, p.num_n, m_blk, n_blk);
+            tile_coords_g(u, p.num_m, p.num_n, p.group, m_blk, n_blk);
             const int64_t m0 = static_cast<int64_t>(m_blk) * TILE + rank * HALF + q * 32;
             const int64_t n0 = static_cast<int64_t>(n_blk) * TILE + h * 128;
             bool ok = (lane == 0) ? ptx::mbar_wait(tfull, acc_phase, abort_flag) : false;
@@ -1746,7 +1745,7 @@ int launch_gemm_mx(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M
     p.bias = static_cast<const __nv_bfloat16*>(bias);
     p.D = D; p.out = out; p.accumulate = accumulate;
     p.a_mn = p.b_mn = 0;
-    p.group = 0;   // the block-scaled MMA kernel uses its own raster group
+    p.group = pair_group(K);
     CUtensorMap tmA, tmB, tmD;
     int st = make_kmajor_map(&tmA, A, M, K, BM);
     if (st != FP8_OK) return st;
@@ -1782,7 +1781,7 @@ int launch_gemm_block(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_
     p.bias = static_cast<const __nv_bfloat16*>(bias);
     p.D = D; p.out = out; p.accumulate = accumulate;
     p.a_mn = p.b_mn = 0;
-    p.group = 0;   // the block kernels use their own raster group
+    p.group = pair_group(K);
     CUtensorMap tmA, tmB, tmD;
     int st = make_kmajor_map(&tmA, A, M, K, 128);
     if (st != FP8_OK) return st;
