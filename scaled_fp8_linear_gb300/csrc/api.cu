@@ -17,8 +17,11 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
+#include <utility>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/fp8linear.h"
@@ -28,7 +31,49 @@ namespace fp8 {
 
 namespace {
 thread_local std::string g_last_error;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The driver's cuCtxGetCurrent and cuCtxGetId, through the runtime's entry
+// point query (null when the driver lacks them).
+std::pair<CtxGetCurrentFn, CtxGetIdFn> ctx_fns() {
+    static CtxGetCurrentFn cur = nullptr;
+    static CtxGetIdFn id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            cur = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    return {cur, id};
 }
+
+// Unique ID of the calling thread's current CUDA context, 0 if there is none
+// (or it cannot be read).  The driver never reuses an ID within a process,
+// so a context made after cudaDeviceReset, or another context made current
+// by the caller, has an ID of its own.
+unsigned long long current_context_id_impl() {
+    const auto fns = ctx_fns();
+    if (!fns.first || !fns.second) return 0;
+    CUcontext ctx = nullptr;
+    if (fns.first(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    if (fns.second(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+}  // namespace
+
+unsigned long long current_context_id() { return current_context_id_impl(); }
 
 int set_error(int code, const char* fmt, ...) {
     char buf[512];

@@ -36,6 +36,8 @@
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -1948,18 +1950,22 @@ int launch_gemm_group(const GemmArgs& g1, const GemmArgs& g2, cudaStream_t strea
 }
 
 unsigned* device_status_word() {
+    // looked up once per CUDA context (the module, and the word, are loaded
+    // per context) and kept under the context's unique ID
     static std::mutex mu;
-    static unsigned* ptr[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
+    static std::vector<std::pair<unsigned long long, unsigned*>> cache;
     std::lock_guard<std::mutex> lock(mu);
-    if (dev < 64 && ptr[dev]) return ptr[dev];
+    const unsigned long long id = current_context_id();
+    if (id != 0)
+        for (const auto& e : cache)
+            if (e.first == id) return e.second;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) {
         (void)cudaGetLastError();
         return nullptr;
     }
-    if (dev < 64) ptr[dev] = static_cast<unsigned*>(p);
+    const unsigned long long id_now = id != 0 ? id : current_context_id();
+    if (id_now != 0) cache.emplace_back(id_now, static_cast<unsigned*>(p));
     return static_cast<unsigned*>(p);
 }
 

@@ -190,7 +190,13 @@ int read_device_status(unsigned* status, bool clear);
 // device (g_epilogue_wait_ns; synchronous).
 int set_epilogue_wait_ns(uint64_t ns);
 
-// Device address of the status word on the current device (null if it
+// Unique ID of the calling thread's current CUDA context (cuCtxGetId), 0 if
+// there is none or it cannot be read.  IDs are never reused within a
+// process, so caches of device addresses keyed by it stay valid across
+// cudaDeviceReset and across contexts a caller makes current.
+unsigned long long current_context_id();
+
+// Device address of the status word in the current context (null if it
 // cannot be looked up), for kernels outside gemm.cu to set bits in.
 unsigned* device_status_word();
 

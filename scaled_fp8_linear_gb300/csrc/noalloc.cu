@@ -24,7 +24,6 @@
 #include <utility>
 #include <vector>
 
-#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/fp8linear.h"
@@ -37,45 +36,6 @@ constexpr size_t kScratchBytes = FP8_NOALLOC_SCRATCH_BYTES;
 // Held by every GPU that loads the library, until the process exits.
 static __device__ __align__(256) uint8_t g_bwd_scratch[kScratchBytes];
 
-using CtxGetCurrentFn = CUresult (*)(CUcontext*);
-using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
-
-// The driver's cuCtxGetCurrent and cuCtxGetId, through the runtime's entry
-// point query (null when the driver lacks them).
-std::pair<CtxGetCurrentFn, CtxGetIdFn> ctx_fns() {
-    static CtxGetCurrentFn cur = nullptr;
-    static CtxGetIdFn id = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            cur = reinterpret_cast<CtxGetCurrentFn>(p);
-        p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            id = reinterpret_cast<CtxGetIdFn>(p);
-    });
-    return {cur, id};
-}
-
-// Unique ID of the calling thread's current CUDA context, 0 if there is none
-// (or it cannot be read).  The driver never reuses an ID within a process,
-// so a context made after cudaDeviceReset, or another context made current
-// by the caller, has an ID of its own.
-unsigned long long current_ctx_id() {
-    const auto fns = ctx_fns();
-    if (!fns.first || !fns.second) return 0;
-    CUcontext ctx = nullptr;
-    if (fns.first(&ctx) != CUDA_SUCCESS || !ctx) return 0;
-    unsigned long long id = 0;
-    if (fns.second(ctx, &id) != CUDA_SUCCESS) return 0;
-    return id;
-}
-
 std::mutex g_mu;
 std::vector<std::pair<unsigned long long, void*>> g_scratch_by_ctx;   // (context ID, address)
 
@@ -86,7 +46,7 @@ std::vector<std::pair<unsigned long long, void*>> g_scratch_by_ctx;   // (contex
 // context's ID.
 int scratch_in_current_context(void** out) {
     std::lock_guard<std::mutex> lock(g_mu);
-    const unsigned long long id = current_ctx_id();
+    const unsigned long long id = fp8::current_context_id();
     if (id != 0) {
         for (const auto& e : g_scratch_by_ctx)
             if (e.first == id) {
@@ -100,7 +60,7 @@ int scratch_in_current_context(void** out) {
         return fp8::set_error(FP8_ERR_CUDA, "fp8_linear_bwd_noalloc: cudaGetSymbolAddress: %s",
                               cudaGetErrorString(e));
     // the lookup made the device's primary context current if none was
-    const unsigned long long id_now = id != 0 ? id : current_ctx_id();
+    const unsigned long long id_now = id != 0 ? id : fp8::current_context_id();
     if (id_now != 0) g_scratch_by_ctx.emplace_back(id_now, p);
     *out = p;
     return FP8_OK;
