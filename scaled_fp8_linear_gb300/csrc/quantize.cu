@@ -992,21 +992,34 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int j = 0; j < 8; ++j) colpart[t >> 5][cg * 8 + j] = cm[j];
         }
-        // row blocks: each 128-element row segment of the tile has its own scale
+        // row blocks: each 128-element row segment of the tile has its own scale.
+        // The 8 threads of a row reduce the amaxes of their 4 rows; then lane
+        // cg = it of each row group computes the scale of row `it` (one
+        // division sequence per warp instead of four) and the others take it
+        // by a shuffle
+        uint32_t mrow[4];
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
-            const uint4 a = va[it], b = vb[it];
-            const uint32_t m2 = absmax_vec(absmax_vec(0u, a), b);
+            const uint32_t m2 = absmax_vec(absmax_vec(0u, va[it]), vb[it]);
             uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
             m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
             m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
             m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-            const float sc = block_scale<FMT>(__uint_as_float(m << 16), pow2);
+            mrow[it] = m;
+        }
+        const uint32_t m_own = cg == 0 ? mrow[0] : cg == 1 ? mrow[1] : cg == 2 ? mrow[2] : mrow[3];
+        const float sc_own = block_scale<FMT>(__uint_as_float(m_own << 16), pow2);
+        if (cg < 4)
+            scale_inv[(r0 + cg * 32 + (t >> 3)) * (cols / 128) + c0 / 128] = __fdiv_rn(1.0f, sc_own);
+        const int group = (t & 31) & ~7;   // first lane of this thread's row group
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const uint4 a = va[it], b = vb[it];
+            const float sc = __shfl_sync(0xFFFFFFFFu, sc_own, group + it);
             const int64_t r = r0 + it * 32 + (t >> 3);
             *reinterpret_cast<uint4*>(q + r * cols + c0 + cg * 16) =
                 make_uint4(cvt4<FMT>(a.x, a.y, sc), cvt4<FMT>(a.z, a.w, sc), cvt4<FMT>(b.x, b.y, sc),
                            cvt4<FMT>(b.z, b.w, sc));
-            if (cg == 0) scale_inv[r * (cols / 128) + c0 / 128] = __fdiv_rn(1.0f, sc);
         }
         __syncthreads();
         // column blocks: one scale per column of the tile (thread c < 128)
