@@ -495,7 +495,9 @@ __global__ void __launch_bounds__(256, 1)
 //     MMA thread issues the pair MMAs; each CTA's TMEM receives its 128 rows
 //     of the 256 x 256 FP32 accumulator (two accumulators, 512 columns);
 //   - MMA completion is multicast to both CTAs' `empty` and `tfull` barriers;
-//     both CTAs' epilogue warps arrive on the even CTA's `tempty` barrier.
+//     both CTAs' epilogue warps arrive on the even CTA's `tempty` barrier, with
+//     a relaxed arrive: it only reports that their tcgen05.ld results are in
+//     registers, and a cluster-scope release would stall them on a fence.
 // GROUPED: a second problem (tmA2, tmB2, p2) shares the launch; without
 // it those parameters are ignored and the kernel is the single-problem one.
 template <int STAGES, bool GROUPED>
@@ -691,7 +693,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive_cluster(ptx::cluster_addr(&tempty[acc], 0));
+            if (lane == 0) ptx::mbar_arrive_cluster_relaxed(ptx::cluster_addr(&tempty[acc], 0));
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -1485,7 +1487,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
                     if (c == 2) {
                         ptx::tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive_cluster(ptx::cluster_addr(tempty, 0));
+                        if (lane == 0) ptx::mbar_arrive_cluster_relaxed(ptx::cluster_addr(tempty, 0));
                     }
                     pack_bf16_chunk(pk[c], r0, n0 + c * 32, p);
                     pack_bf16_chunk(pk[c + 1], r1, n0 + (c + 1) * 32, p);
@@ -1509,7 +1511,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
                     if (c == 2) {
                         ptx::tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive_cluster(ptx::cluster_addr(tempty, 0));
+                        if (lane == 0) ptx::mbar_arrive_cluster_relaxed(ptx::cluster_addr(tempty, 0));
                     }
 #pragma unroll
                     for (int i = 0; i < 2; ++i)
