@@ -720,57 +720,81 @@ __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
 // granularity": every 128-deep partial sum is multiplied by its blocks'
 // factors before it is added to the FP32 accumulator).
 //
-// A cluster of two CTAs (the two SMs of a TPC) computes a 256 x 128 tile with
-// tcgen05.mma.cta_group::2 (M = 256, N = 128, K = 32): CTA r loads rows
-// [r*128, r*128+128) of the tile's A panel and rows [r*64, r*64+64) of its B
-// panel (16 + 8 KiB per stage); both CTAs' copies count on the even CTA's
-// `full` barrier, whose MMA thread issues the MMAs.  Each 128-deep K block
-// goes to its own TMEM buffer -- four buffers of 128 columns, rotated -- so
-// the MMAs of the next three blocks run while the epilogue promotes one.
-// The pair tile halves the operand bytes each SM moves through shared memory
-// per FLOP against a 128 x 128 single-CTA tile, whose shared-memory traffic
-// (TMA writes plus MMA reads) capped the MMA at about half its rate.
+// A cluster of two CTAs (the two SMs of a TPC) computes a 256 x TN tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = TN, K = 32): CTA r loads rows
+// [r*128, r*128+128) of the tile's A panel and rows [r*TN/2, (r+1)*TN/2) of
+// its B panel; both CTAs' copies count on the even CTA's `full` barrier,
+// whose MMA thread issues the MMAs.  Each 128-deep K block goes to its own
+// TMEM buffer (512 / TN buffers of TN columns, rotated), so the MMAs of the
+// next blocks run while the promotion warps promote one.  The pair tile
+// halves the operand bytes each SM moves through shared memory per FLOP
+// against a 128 x TN single-CTA tile.
 //   warp 0      TMA producer (one thread);
 //   warp 1      MMA issuer (one thread of the even CTA): per K block, waits
 //               for a free buffer and a full stage, issues 4 MMAs, commits
 //               the stage (`empty`) and the buffer (`tfull`) to both CTAs;
 //   warp 2      TMEM allocation (512 columns per CTA);
-//   warps 4-11  epilogue, 2 per TMEM lane quarter, 64 columns each: per K
-//               block, read the buffer (tcgen05.ld), hand it back to the MMA
-//               thread (both CTAs' warps arrive on the even CTA's `tempty`),
-//               then add partial * s_a(m, kb) * s_b(n, kb) into FP32
-//               registers with packed fma.rn.f32x2.  The factors of the next
-//               four K blocks are loaded while the current four are promoted.
-//               At the tile's end the accumulator is rounded (plus the bias)
-//               and leaves through 32-row x 64-byte TMA boxes: bf16 stores,
-//               or FP32 stores / reduce-adds (accumulate).
-// Every wait is a blocking try_wait, so that waiting epilogue warps do not
+//   warps 4-    promotion, EPI / 4 per TMEM lane quarter, CW = 4 TN / EPI
+//               columns each: per K block, read the buffer (tcgen05.ld),
+//               hand it back to the MMA thread (both CTAs' warps arrive on
+//               the even CTA's `tempty`), then add partial * s_a(m, kb) *
+//               s_b(n, kb) into FP32 registers with packed fma.rn.f32x2.  The
+//               factors of the next four K blocks are loaded while the
+//               current four are promoted.  At the tile's end the accumulator
+//               is rounded (plus the bias) and leaves through 32-row x
+//               64-byte TMA boxes: bf16 stores, or FP32 stores / reduce-adds
+//               (accumulate).
+// Every wait is a blocking try_wait, so that waiting promotion warps do not
 // take issue slots from the producer and MMA warps on their sub-partitions.
 // COLSCALE: B carries 1x128 scales (one factor per output column and K
-// block, the block-wise wgrad); each epilogue warp stages its 64 columns'
+// block, the block-wise wgrad); each promotion warp stages its columns'
 // factors of four K blocks in shared memory, read back as broadcasts.
-// Shape of one instance: pair tiles of 256 x TN, EPI promotion warps per CTA
-// (at most 4 per TMEM lane quarter), a ring of STAGES operand stages, and
-// TMEM split into 512 / TN partial-sum buffers.
-template <int TN_, int EPI_, int STAGES_>
+//
+// Two instances:
+//  * BpWide (B with one factor per 128 x 128 block, or per tensor): 256 x 256
+//    tiles, so that each MMA is N = 256 (with N = 128 the MMAs alone stop at
+//    0.54-0.60 of the tensor core's rate, against 0.9 with N = 256).  TMEM
+//    then holds two partial-sum buffers, so a K block's promotion has to hand
+//    its buffer back within the next block's MMAs; 16 promotion warps of 64
+//    columns share that work.  The accumulator takes 64 registers a thread,
+//    so the role warpgroup gives registers back with setmaxnreg (32 a thread)
+//    and the promotion warps take them (112): 4 x 32 x 32 + 16 x 32 x 112 =
+//    61440 = 640 threads x the 96 registers of the launch.  One 32-column
+//    TMEM load at a time (two in flight would need 64 more registers; 16-
+//    column loads measured 11% slower).  Three operand stages: four and five
+//    measured 1.5% and about 5% slower -- shared memory comes out of L1,
+//    where the promotion warps' factor reads hit.
+//  * BpNarrow (B with per-column factors): 256 x 128 tiles, four TMEM buffers
+//    (three K blocks of slack for the promotion), 8 promotion warps of 64
+//    columns, no register re-allocation; the per-column factor products do
+//    not fit the wide instance's registers (measured at half the speed).
+template <int TN_, int EPI_, int STAGES_, int RROLE_ = 0, int RPROMO_ = 0, int LD_ = 32>
 struct BpCfg {
     static constexpr int TN = TN_;
     static constexpr int EPI = EPI_;
     static constexpr int STAGES = STAGES_;
+    // registers per thread of the role warpgroup and of the promotion warps
+    // after setmaxnreg (0: no re-allocation)
+    static constexpr int RROLE = RROLE_;
+    static constexpr int RPROMO = RPROMO_;
+    // two 32-column TMEM loads in flight per promotion warp (else one load
+    // of LD columns at a time)
+    static constexpr bool TWO_LD = EPI_ <= 8;
+    static constexpr int LD = LD_;
     static constexpr int NBUF = 512 / TN;
     static constexpr int THREADS = (4 + EPI) * 32;
     static constexpr int CW = 4 * TN / EPI;          // columns of one promotion warp
     static constexpr int A_BYTES = 128 * BK;         // this CTA's 128 rows of A
     static constexpr int B_BYTES = (TN / 2) * BK;    // this CTA's half of the TN rows of B
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + EPI * (2048 + 4 * CW * 4) + 256 + 1024;
+    // shared memory: operand ring, 2 KB of output staging per promotion
+    // warp, per-column factors (COLSCALE only), barriers, alignment slack
+    static constexpr int smem(bool colscale) {
+        return STAGES * STAGE_BYTES + EPI * (2048 + (colscale ? 4 * CW * 4 : 0)) + 256 + 1024;
+    }
 };
-// 256 x 128 tiles, four TMEM buffers (three K blocks of slack for the
-// promotion), 8 promotion warps of 64 columns.  Measured on the 16384 x 18432
-// x 7168 shapes: 256 x 256 tiles with two buffers of 256 columns were slower
-// (each promotion warp then holds 128 accumulator columns and the promotion
-// must finish within one K block), and so were 16 promotion warps.
 using BpNarrow = BpCfg<128, 8, 8>;
+using BpWide = BpCfg<256, 16, 3, 32, 112>;
 
 // Factors of row r of an operand (gran: FP8_GRAN_TENSOR, 1x128 or 128x128;
 // KB blocks per row) for the K blocks kb0 .. kb0+3, 0 past the last block.
@@ -804,12 +828,37 @@ __device__ __forceinline__ void promote_uniform(uint64_t* acc, const uint32_t (&
                             ff, acc[e]);
 }
 
+// The same for 16 columns.
+__device__ __forceinline__ void promote_uniform16(uint64_t* acc, const uint32_t (&r)[16], uint64_t ff) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        acc[e] = ptx::ffma2(static_cast<uint64_t>(r[2 * e]) | (static_cast<uint64_t>(r[2 * e + 1]) << 32),
+                            ff, acc[e]);
+}
+
 // acc[e] += r[2e..2e+1] * fp32(fa * cf[2e..2e+1]): per-column factors cf (32
 // floats in shared memory, read as broadcasts).
 __device__ __forceinline__ void promote_columns(uint64_t* acc, const uint32_t (&r)[32], float fa,
                                                 const float* cf) {
 #pragma unroll
     for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 c = *reinterpret_cast<const float4*>(cf + 4 * e4);
+        const uint64_t f0 = pack2(__fmul_rn(fa, c.x), __fmul_rn(fa, c.y));
+        const uint64_t f1 = pack2(__fmul_rn(fa, c.z), __fmul_rn(fa, c.w));
+        acc[2 * e4] = ptx::ffma2(static_cast<uint64_t>(r[4 * e4]) |
+                                     (static_cast<uint64_t>(r[4 * e4 + 1]) << 32),
+                                 f0, acc[2 * e4]);
+        acc[2 * e4 + 1] = ptx::ffma2(static_cast<uint64_t>(r[4 * e4 + 2]) |
+                                         (static_cast<uint64_t>(r[4 * e4 + 3]) << 32),
+                                     f1, acc[2 * e4 + 1]);
+    }
+}
+
+// The same for 16 columns.
+__device__ __forceinline__ void promote_columns16(uint64_t* acc, const uint32_t (&r)[16], float fa,
+                                                  const float* cf) {
+#pragma unroll
+    for (int e4 = 0; e4 < 4; ++e4) {
         const float4 c = *reinterpret_cast<const float4*>(cf + 4 * e4);
         const uint64_t f0 = pack2(__fmul_rn(fa, c.x), __fmul_rn(fa, c.y));
         const uint64_t f1 = pack2(__fmul_rn(fa, c.z), __fmul_rn(fa, c.w));
@@ -881,14 +930,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
     constexpr int A_BYTES = Cfg::A_BYTES;
     constexpr int STAGE_BYTES = Cfg::STAGE_BYTES;
     constexpr int TN = Cfg::TN;
-    constexpr uint32_t TMEM_COLS = NBUF * TN;
-    static_assert(TMEM_COLS == 512, "the partial-sum buffers fill TMEM");
+    constexpr uint32_t TMEM_COLS = 512;   // allocations are powers of two
+    static_assert(NBUF * TN <= 512, "the partial-sum buffers fit in TMEM");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* epi_stage = ring + STAGES * STAGE_BYTES;   // output boxes: 2 KB per epilogue warp
     float* colf = reinterpret_cast<float*>(epi_stage + EPI * 2048);   // [warp][4][cols]
-    uint64_t* full = reinterpret_cast<uint64_t*>(colf + EPI * 4 * Cfg::CW);
+    uint64_t* full = reinterpret_cast<uint64_t*>(colf + (COLSCALE ? EPI * 4 * Cfg::CW : 0));
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + NBUF;
@@ -930,6 +979,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
     const int num_units = p.num_m * p.num_n;
     const int KB = p.num_kb;
 
+    if (warp < 4) {
+    if constexpr (Cfg::RPROMO != 0) ptx::setmaxnreg_dec<Cfg::RROLE>();
     if (warp == 0) {
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
@@ -995,7 +1046,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
             ptx::mma_commit_pair(done, 0x1);
             ptx::mbar_wait(done, 0, &never);
         }
-    } else if (warp >= 4) {
+    }
+    } else {
+        if constexpr (Cfg::RPROMO != 0) ptx::setmaxnreg_inc<Cfg::RPROMO>();
         constexpr int CW = Cfg::CW;              // columns of this warp
         constexpr int NCH = CW / 32;             // 32-column chunks
         const int qd = warp & 3;                 // TMEM lane quarter of this warp
@@ -1012,6 +1065,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
             const int64_t m = m0 + lane;
             const int64_t m_safe = m < p.M ? m : p.M - 1;
             const int64_t n0 = static_cast<int64_t>(n_blk) * TN + h * CW;
+            // a warp's columns lie all inside or all outside [0, N) (N is a
+            // multiple of 128, CW divides 128); outside, its factors are
+            // read at column N - 1 and its columns are not stored
+            const int64_t nf = n0 < p.N ? n0 : p.N - 1;
             // FP32 accumulator of CW columns, as packed pairs
             uint64_t acc[CW / 2];
 #pragma unroll
@@ -1024,17 +1081,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
             if (COLSCALE) {
 #pragma unroll
                 for (int c = 0; c < NCH; ++c)
-                    block_factors4(fc_n[c], p.sb, p.gb, n0 + 32 * c + lane, 0, KB, vec_b != 0);
+                    block_factors4(fc_n[c], p.sb, p.gb, nf + (n0 < p.N ? 32 * c + lane : 0), 0, KB, vec_b != 0);
             } else {
-                block_factors4(fb_n, p.sb, p.gb, n0, 0, KB, vec_b != 0);
+                block_factors4(fb_n, p.sb, p.gb, nf, 0, KB, vec_b != 0);
             }
             for (int kb0 = 0; ok && kb0 < KB; kb0 += 4) {
-                float fa[4], fb[4];
+                // COLSCALE: the rows' factors; otherwise the products fa * fb
+                float fa[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    fa[j] = fa_n[j];
-                    fb[j] = fb_n[j];
-                }
+                for (int j = 0; j < 4; ++j) fa[j] = COLSCALE ? fa_n[j] : __fmul_rn(fa_n[j], fb_n[j]);
                 if (COLSCALE) {
                     __syncwarp();   // the previous group's factors have been read
 #pragma unroll
@@ -1048,10 +1103,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                 if (COLSCALE) {
 #pragma unroll
                     for (int c = 0; c < NCH; ++c)
-                        block_factors4(fc_n[c], p.sb, p.gb, n0 + 32 * c + lane, kb0 + 4, KB,
+                        block_factors4(fc_n[c], p.sb, p.gb, nf + (n0 < p.N ? 32 * c + lane : 0), kb0 + 4, KB,
                                        vec_b != 0);
                 } else {
-                    block_factors4(fb_n, p.sb, p.gb, n0, kb0 + 4, KB, vec_b != 0);
+                    block_factors4(fb_n, p.sb, p.gb, nf, kb0 + 4, KB, vec_b != 0);
                 }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -1062,7 +1117,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                     __syncwarp();
                     ptx::tc_fence_after();
                     const uint32_t ta = tmem_base + lanes + buf * TN + h * CW;
-                    if (COLSCALE || NCH == 1) {
+                    if (!Cfg::TWO_LD && Cfg::LD == 16) {
+                        // 16-column loads, one at a time (the accumulator
+                        // takes most of the registers): the buffer goes back
+                        // after the last one
+                        const uint64_t ff = pack2(fa[j], fa[j]);
+#pragma unroll
+                        for (int c = 0; c < CW / 16; ++c) {
+                            uint32_t r[16];
+                            ptx::tmem_ld_32x32b_x16(ta + 16 * c, r);
+                            ptx::tmem_wait_ld();
+                            if (c == CW / 16 - 1) {
+                                ptx::tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0)
+                                    ptx::mbar_arrive_cluster_relaxed(ptx::cluster_addr(&tempty[buf], 0));
+                            }
+                            if (COLSCALE)
+                                promote_columns16(acc + 8 * c, r, fa[j], cf + j * CW + 16 * c);
+                            else
+                                promote_uniform16(acc + 8 * c, r, ff);
+                        }
+                    } else if (COLSCALE || NCH == 1 || !Cfg::TWO_LD) {
                         // one 32-column chunk at a time (the per-column factors
                         // need the registers): the buffer goes back after the
                         // last chunk's load
@@ -1080,14 +1156,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                             if (COLSCALE) {
                                 promote_columns(acc + 16 * c, r, fa[j], cf + j * CW + 32 * c);
                             } else {
-                                const float f = __fmul_rn(fa[j], fb[j]);
+                                const float f = fa[j];
                                 promote_uniform(acc + 16 * c, r, pack2(f, f));
                             }
                         }
                     } else {
                         // two 32-column chunks in flight at a time; the buffer
                         // goes back once the last pair is in registers
-                        const float f = __fmul_rn(fa[j], fb[j]);
+                        const float f = fa[j];
                         const uint64_t ff = pack2(f, f);
 #pragma unroll
                         for (int c = 0; c < NCH; c += 2) {
@@ -1109,7 +1185,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
             }
             if (!ok) break;
 #pragma unroll
-            for (int c = 0; c < NCH; ++c) emit_block_chunk(slot, acc + 16 * c, m0, n0 + 32 * c, p, &tmD);
+            for (int c = 0; c < NCH; ++c)
+                if (n0 < p.N) emit_block_chunk(slot, acc + 16 * c, m0, n0 + 32 * c, p, &tmD);
         }
         if (lane == 0) ptx::bulk_wait_group_all();   // every TMA store has completed
         __syncwarp();
@@ -1770,12 +1847,10 @@ int launch_gemm_mx(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M
     return FP8_OK;
 }
 
-// Block-scaled GEMM with fp32 factors (at least one operand with 1x128 or
-// 128x128 scales; K > 0) on the CTA-pair promotion kernel: 256 x 128 tiles.
-int launch_gemm_block(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
-                      int64_t K, int ga, const float* sa, int gb, const float* sb,
-                      const void* bias, void* D, int out, int accumulate, cudaStream_t stream) {
-    using C = BpNarrow;
+template <typename C, bool COLSCALE>
+int launch_block_cfg(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
+                     int64_t K, int ga, const float* sa, int gb, const float* sb,
+                     const void* bias, void* D, int out, int accumulate, cudaStream_t stream) {
     GemmParams p;
     p.M = M; p.N = N; p.K = K;
     p.num_m = static_cast<int>((M + 255) / 256);
@@ -1791,20 +1866,31 @@ int launch_gemm_block(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_
     if (st != FP8_OK) return st;
     if ((st = make_kmajor_map(&tmB, B, N, K, C::TN / 2)) != FP8_OK) return st;
     if ((st = make_store_map(&tmD, D, M, N, out)) != FP8_OK) return st;
-    const bool colscale = gb == FP8_GRAN_1x128;
-    auto k = colscale ? gemm_block_pair_kernel<C, true> : gemm_block_pair_kernel<C, false>;
-    if ((st = ensure_smem(k, C::SMEM, colscale ? 3 : 1)) != FP8_OK) return st;
+    auto k = gemm_block_pair_kernel<C, COLSCALE>;
+    constexpr int SMEM = C::smem(COLSCALE);
+    if ((st = ensure_smem(k, SMEM, COLSCALE ? 3 : 1)) != FP8_OK) return st;
     const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
-    const int64_t clusters = pair_clusters(reinterpret_cast<const void*>(k), colscale ? 4 : 3,
-                                           C::THREADS, C::SMEM);
+    const int64_t clusters = pair_clusters(reinterpret_cast<const void*>(k), COLSCALE ? 4 : 3,
+                                           C::THREADS, SMEM);
     const int grid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
     // factors of four K blocks as one float4: rows of a multiple of 4 floats, aligned arrays
     const int vec_a = p.num_kb % 4 == 0 && (reinterpret_cast<uintptr_t>(sa) & 15u) == 0;
     const int vec_b = p.num_kb % 4 == 0 && (reinterpret_cast<uintptr_t>(sb) & 15u) == 0;
-    launch_pdl(k, dim3(grid), dim3(C::THREADS), C::SMEM, stream, tmA, tmB, tmD, p, vec_a, vec_b);
+    launch_pdl(k, dim3(grid), dim3(C::THREADS), SMEM, stream, tmA, tmB, tmD, p, vec_a, vec_b);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(FP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
     return FP8_OK;
+}
+
+// Block-scaled GEMM with fp32 factors (at least one operand with 1x128 or
+// 128x128 scales; K > 0) on the CTA-pair promotion kernel: 256 x 256 tiles,
+// or 256 x 128 when B has per-column factors.
+int launch_gemm_block(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
+                      int64_t K, int ga, const float* sa, int gb, const float* sb,
+                      const void* bias, void* D, int out, int accumulate, cudaStream_t stream) {
+    const bool colscale = gb == FP8_GRAN_1x128;
+    return colscale ? launch_block_cfg<BpNarrow, true>(A, fa, B, fb, M, N, K, ga, sa, gb, sb, bias, D, out, accumulate, stream)
+                    : launch_block_cfg<BpWide, false>(A, fa, B, fb, M, N, K, ga, sa, gb, sb, bias, D, out, accumulate, stream);
 }
 
 }  // namespace
