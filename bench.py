@@ -499,7 +499,7 @@ def extra_block_scaled(F, dev, flush, stream, bf16_burst, iters=10, warmup=3):
                 res[name] = {"median_ms": round(med, 4), "achieved": round(ach, 1),
                              "unit": "TFLOP/s"}
                 if name == "gemm":
-                    res[name].update({"kernel": "gemm_mx_kernel" if pow2 else "gemm_block_kernel",
+                    res[name].update({"kernel": "gemm_mx_kernel" if pow2 else "gemm_block_pair_kernel",
                                       "peak": round(peak, 1), "frac": round(ach / peak, 4)})
                 else:
                     res[name]["work"] = "6 M N K; casts included"

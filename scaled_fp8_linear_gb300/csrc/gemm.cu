@@ -750,37 +750,34 @@ __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
 // block, the block-wise wgrad); each promotion warp stages its columns'
 // factors of four K blocks in shared memory, read back as broadcasts.
 //
-// Two instances:
-//  * BpWide (B with one factor per 128 x 128 block, or per tensor): 256 x 256
-//    tiles, so that each MMA is N = 256 (with N = 128 the MMAs alone stop at
-//    0.54-0.60 of the tensor core's rate, against 0.9 with N = 256).  TMEM
-//    then holds two partial-sum buffers, so a K block's promotion has to hand
-//    its buffer back within the next block's MMAs; 16 promotion warps of 64
-//    columns share that work.  The accumulator takes 64 registers a thread,
-//    so the role warpgroup gives registers back with setmaxnreg (32 a thread)
-//    and the promotion warps take them (112): 4 x 32 x 32 + 16 x 32 x 112 =
-//    61440 = 640 threads x the 96 registers of the launch.  One 32-column
-//    TMEM load at a time (two in flight would need 64 more registers; 16-
-//    column loads measured 11% slower).  Three operand stages: four and five
-//    measured 1.5% and about 5% slower -- shared memory comes out of L1,
-//    where the promotion warps' factor reads hit.
-//  * BpNarrow (B with per-column factors): 256 x 128 tiles, four TMEM buffers
-//    (three K blocks of slack for the promotion), 8 promotion warps of 64
-//    columns, no register re-allocation; the per-column factor products do
-//    not fit the wide instance's registers (measured at half the speed).
-template <int TN_, int EPI_, int STAGES_, int RROLE_ = 0, int RPROMO_ = 0, int LD_ = 32>
+// The instance (BpWide): 256 x 256 tiles, so that each MMA is N = 256 (with
+// N = 128 the MMAs alone stop at 0.54-0.60 of the tensor core's rate,
+// against 0.9 with N = 256).  TMEM then holds two partial-sum buffers, so a
+// K block's promotion has to hand its buffer back within the next block's
+// MMAs; 16 promotion warps of 64 columns share that work.  The accumulator
+// takes 64 registers a thread, so the role warpgroup gives registers back
+// with setmaxnreg (32 a thread) and the promotion warps take them (112):
+// 4 x 32 x 32 + 16 x 32 x 112 = 61440 = 640 threads x the 96 registers of
+// the launch.  Measured against the alternatives (CUDA events, the C3
+// shapes): one 32-column TMEM load at a time (two in flight need 64 more
+// registers and spill; 16-column loads were 11% slower); three operand
+// stages (four and five were 1.5% and about 5% slower: shared memory comes
+// out of L1, where 97% of the promotion warps' factor reads hit); factors
+// read at the start of each group of four K blocks rather than one group
+// ahead (6% faster: the prefetched values held 8 registers and made the loop
+// spill); per-column factor products by packed mul.rn.f32x2 (scalar
+// multiplies made the COLSCALE loop 38% slower); 256 x 160 tiles with three
+// buffers and 20 promotion warps were 30% slower, and 256 x 128 tiles with
+// four buffers and 8 warps (the earlier form) 24% slower (COLSCALE: 9%).
+template <int TN_, int EPI_, int STAGES_, int RROLE_, int RPROMO_>
 struct BpCfg {
     static constexpr int TN = TN_;
     static constexpr int EPI = EPI_;
     static constexpr int STAGES = STAGES_;
     // registers per thread of the role warpgroup and of the promotion warps
-    // after setmaxnreg (0: no re-allocation)
+    // after setmaxnreg
     static constexpr int RROLE = RROLE_;
     static constexpr int RPROMO = RPROMO_;
-    // two 32-column TMEM loads in flight per promotion warp (else one load
-    // of LD columns at a time)
-    static constexpr bool TWO_LD = EPI_ <= 8;
-    static constexpr int LD = LD_;
     static constexpr int NBUF = 512 / TN;
     static constexpr int THREADS = (4 + EPI) * 32;
     static constexpr int CW = 4 * TN / EPI;          // columns of one promotion warp
@@ -792,8 +789,11 @@ struct BpCfg {
     static constexpr int smem(bool colscale) {
         return STAGES * STAGE_BYTES + EPI * (2048 + (colscale ? 4 * CW * 4 : 0)) + 256 + 1024;
     }
+    static_assert(CW % 32 == 0 && 128 % CW == 0, "a warp's columns: whole 32-column loads "
+                                                 "inside one 128-column factor block");
+    static_assert(4 * 32 * RROLE + EPI * 32 * RPROMO <= THREADS * (65536 / THREADS / 8 * 8),
+                  "the register split fits the launch's registers");
 };
-using BpNarrow = BpCfg<128, 8, 8>;
 using BpWide = BpCfg<256, 16, 3, 32, 112>;
 
 // Factors of row r of an operand (gran: FP8_GRAN_TENSOR, 1x128 or 128x128;
@@ -828,40 +828,16 @@ __device__ __forceinline__ void promote_uniform(uint64_t* acc, const uint32_t (&
                             ff, acc[e]);
 }
 
-// The same for 16 columns.
-__device__ __forceinline__ void promote_uniform16(uint64_t* acc, const uint32_t (&r)[16], uint64_t ff) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-        acc[e] = ptx::ffma2(static_cast<uint64_t>(r[2 * e]) | (static_cast<uint64_t>(r[2 * e + 1]) << 32),
-                            ff, acc[e]);
-}
-
 // acc[e] += r[2e..2e+1] * fp32(fa * cf[2e..2e+1]): per-column factors cf (32
 // floats in shared memory, read as broadcasts).
 __device__ __forceinline__ void promote_columns(uint64_t* acc, const uint32_t (&r)[32], float fa,
                                                 const float* cf) {
+    const uint64_t faa = pack2(fa, fa);
 #pragma unroll
     for (int e4 = 0; e4 < 8; ++e4) {
         const float4 c = *reinterpret_cast<const float4*>(cf + 4 * e4);
-        const uint64_t f0 = pack2(__fmul_rn(fa, c.x), __fmul_rn(fa, c.y));
-        const uint64_t f1 = pack2(__fmul_rn(fa, c.z), __fmul_rn(fa, c.w));
-        acc[2 * e4] = ptx::ffma2(static_cast<uint64_t>(r[4 * e4]) |
-                                     (static_cast<uint64_t>(r[4 * e4 + 1]) << 32),
-                                 f0, acc[2 * e4]);
-        acc[2 * e4 + 1] = ptx::ffma2(static_cast<uint64_t>(r[4 * e4 + 2]) |
-                                         (static_cast<uint64_t>(r[4 * e4 + 3]) << 32),
-                                     f1, acc[2 * e4 + 1]);
-    }
-}
-
-// The same for 16 columns.
-__device__ __forceinline__ void promote_columns16(uint64_t* acc, const uint32_t (&r)[16], float fa,
-                                                  const float* cf) {
-#pragma unroll
-    for (int e4 = 0; e4 < 4; ++e4) {
-        const float4 c = *reinterpret_cast<const float4*>(cf + 4 * e4);
-        const uint64_t f0 = pack2(__fmul_rn(fa, c.x), __fmul_rn(fa, c.y));
-        const uint64_t f1 = pack2(__fmul_rn(fa, c.z), __fmul_rn(fa, c.w));
+        const uint64_t f0 = ptx::fmul2(faa, pack2(c.x, c.y));
+        const uint64_t f1 = ptx::fmul2(faa, pack2(c.z, c.w));
         acc[2 * e4] = ptx::ffma2(static_cast<uint64_t>(r[4 * e4]) |
                                      (static_cast<uint64_t>(r[4 * e4 + 1]) << 32),
                                  f0, acc[2 * e4]);
@@ -980,7 +956,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
     const int KB = p.num_kb;
 
     if (warp < 4) {
-    if constexpr (Cfg::RPROMO != 0) ptx::setmaxnreg_dec<Cfg::RROLE>();
+    ptx::setmaxnreg_dec<Cfg::RROLE>();   // the whole role warpgroup
     if (warp == 0) {
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
@@ -1048,7 +1024,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
         }
     }
     } else {
-        if constexpr (Cfg::RPROMO != 0) ptx::setmaxnreg_inc<Cfg::RPROMO>();
+        ptx::setmaxnreg_inc<Cfg::RPROMO>();   // each promotion warpgroup
         constexpr int CW = Cfg::CW;              // columns of this warp
         constexpr int NCH = CW / 32;             // 32-column chunks
         const int qd = warp & 3;                 // TMEM lane quarter of this warp
@@ -1073,40 +1049,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
             uint64_t acc[CW / 2];
 #pragma unroll
             for (int e = 0; e < CW / 2; ++e) acc[e] = 0ull;
-            // factors of the next group of four K blocks: A per row, B per
-            // 128-column block (or, COLSCALE, per column: lane l holds columns
-            // n0 + 32c + l)
-            float fa_n[4], fb_n[4], fc_n[NCH][4];
-            block_factors4(fa_n, p.sa, p.ga, m_safe, 0, KB, vec_a != 0);
-            if (COLSCALE) {
-#pragma unroll
-                for (int c = 0; c < NCH; ++c)
-                    block_factors4(fc_n[c], p.sb, p.gb, nf + (n0 < p.N ? 32 * c + lane : 0), 0, KB, vec_b != 0);
-            } else {
-                block_factors4(fb_n, p.sb, p.gb, nf, 0, KB, vec_b != 0);
-            }
             for (int kb0 = 0; ok && kb0 < KB; kb0 += 4) {
-                // COLSCALE: the rows' factors; otherwise the products fa * fb
-                float fa[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) fa[j] = COLSCALE ? fa_n[j] : __fmul_rn(fa_n[j], fb_n[j]);
+                // The factors of four K blocks, read at the start of the group
+                // (they hit L1; holding the next group's in registers made the
+                // loop spill): A per row; B per 128-column block, multiplied
+                // into fa here, or (COLSCALE) per column, staged in shared
+                // memory for broadcast reads (lane l writes columns n0+32c+l).
+                float fa[4], fb[4];
+                block_factors4(fa, p.sa, p.ga, m_safe, kb0, KB, vec_a != 0);
                 if (COLSCALE) {
                     __syncwarp();   // the previous group's factors have been read
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int c = 0; c < NCH; ++c) cf[j * CW + 32 * c + lane] = fc_n[c][j];
-                    __syncwarp();
-                }
-                // the next group's factors load while this group is promoted
-                block_factors4(fa_n, p.sa, p.ga, m_safe, kb0 + 4, KB, vec_a != 0);
-                if (COLSCALE) {
-#pragma unroll
-                    for (int c = 0; c < NCH; ++c)
-                        block_factors4(fc_n[c], p.sb, p.gb, nf + (n0 < p.N ? 32 * c + lane : 0), kb0 + 4, KB,
+                    for (int c = 0; c < NCH; ++c) {
+                        block_factors4(fb, p.sb, p.gb, nf + (n0 < p.N ? 32 * c + lane : 0), kb0, KB,
                                        vec_b != 0);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) cf[j * CW + 32 * c + lane] = fb[j];
+                    }
+                    __syncwarp();
                 } else {
-                    block_factors4(fb_n, p.sb, p.gb, nf, kb0 + 4, KB, vec_b != 0);
+                    block_factors4(fb, p.sb, p.gb, nf, kb0, KB, vec_b != 0);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) fa[j] = __fmul_rn(fa[j], fb[j]);
                 }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -1117,68 +1081,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                     __syncwarp();
                     ptx::tc_fence_after();
                     const uint32_t ta = tmem_base + lanes + buf * TN + h * CW;
-                    if (!Cfg::TWO_LD && Cfg::LD == 16) {
-                        // 16-column loads, one at a time (the accumulator
-                        // takes most of the registers): the buffer goes back
-                        // after the last one
-                        const uint64_t ff = pack2(fa[j], fa[j]);
+                    // one 32-column load at a time (the accumulator takes most
+                    // of the registers); the buffer goes back after the last
+                    uint32_t r[32];
 #pragma unroll
-                        for (int c = 0; c < CW / 16; ++c) {
-                            uint32_t r[16];
-                            ptx::tmem_ld_32x32b_x16(ta + 16 * c, r);
-                            ptx::tmem_wait_ld();
-                            if (c == CW / 16 - 1) {
-                                ptx::tc_fence_before();
-                                __syncwarp();
-                                if (lane == 0)
-                                    ptx::mbar_arrive_cluster_relaxed(ptx::cluster_addr(&tempty[buf], 0));
-                            }
-                            if (COLSCALE)
-                                promote_columns16(acc + 8 * c, r, fa[j], cf + j * CW + 16 * c);
-                            else
-                                promote_uniform16(acc + 8 * c, r, ff);
+                    for (int c = 0; c < NCH; ++c) {
+                        ptx::tmem_ld_32x32b_x32(ta + 32 * c, r);
+                        ptx::tmem_wait_ld();
+                        if (c == NCH - 1) {
+                            ptx::tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0)
+                                ptx::mbar_arrive_cluster_relaxed(ptx::cluster_addr(&tempty[buf], 0));
                         }
-                    } else if (COLSCALE || NCH == 1 || !Cfg::TWO_LD) {
-                        // one 32-column chunk at a time (the per-column factors
-                        // need the registers): the buffer goes back after the
-                        // last chunk's load
-                        uint32_t r[32];
-#pragma unroll
-                        for (int c = 0; c < NCH; ++c) {
-                            ptx::tmem_ld_32x32b_x32(ta + 32 * c, r);
-                            ptx::tmem_wait_ld();
-                            if (c == NCH - 1) {
-                                ptx::tc_fence_before();
-                                __syncwarp();
-                                if (lane == 0)
-                                    ptx::mbar_arrive_cluster_relaxed(ptx::cluster_addr(&tempty[buf], 0));
-                            }
-                            if (COLSCALE) {
-                                promote_columns(acc + 16 * c, r, fa[j], cf + j * CW + 32 * c);
-                            } else {
-                                const float f = fa[j];
-                                promote_uniform(acc + 16 * c, r, pack2(f, f));
-                            }
-                        }
-                    } else {
-                        // two 32-column chunks in flight at a time; the buffer
-                        // goes back once the last pair is in registers
-                        const float f = fa[j];
-                        const uint64_t ff = pack2(f, f);
-#pragma unroll
-                        for (int c = 0; c < NCH; c += 2) {
-                            uint32_t r0[32], r1[32];
-                            ptx::tmem_ld_32x32b_x32(ta + 32 * c, r0);
-                            ptx::tmem_ld_32x32b_x32(ta + 32 * c + 32, r1);
-                            ptx::tmem_wait_ld();
-                            if (c + 2 == NCH) {
-                                ptx::tc_fence_before();
-                                __syncwarp();
-                                if (lane == 0) ptx::mbar_arrive_cluster_relaxed(ptx::cluster_addr(&tempty[buf], 0));
-                            }
-                            promote_uniform(acc + 16 * c, r0, ff);
-                            promote_uniform(acc + 16 * c + 16, r1, ff);
-                        }
+                        if (COLSCALE)
+                            promote_columns(acc + 16 * c, r, fa[j], cf + j * CW + 32 * c);
+                        else
+                            promote_uniform(acc + 16 * c, r, pack2(fa[j], fa[j]));
                     }
                     if (++buf == NBUF) { buf = 0; buf_phase ^= 1u; }
                 }
@@ -1889,8 +1808,10 @@ int launch_gemm_block(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_
                       int64_t K, int ga, const float* sa, int gb, const float* sb,
                       const void* bias, void* D, int out, int accumulate, cudaStream_t stream) {
     const bool colscale = gb == FP8_GRAN_1x128;
-    return colscale ? launch_block_cfg<BpNarrow, true>(A, fa, B, fb, M, N, K, ga, sa, gb, sb, bias, D, out, accumulate, stream)
-                    : launch_block_cfg<BpWide, false>(A, fa, B, fb, M, N, K, ga, sa, gb, sb, bias, D, out, accumulate, stream);
+    return colscale ? launch_block_cfg<BpWide, true>(A, fa, B, fb, M, N, K, ga, sa, gb, sb, bias, D,
+                                                     out, accumulate, stream)
+                    : launch_block_cfg<BpWide, false>(A, fa, B, fb, M, N, K, ga, sa, gb, sb, bias, D,
+                                                      out, accumulate, stream);
 }
 
 }  // namespace
