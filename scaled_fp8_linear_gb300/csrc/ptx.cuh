@@ -82,38 +82,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     }
 }
 
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-// Same contract as mbar_wait, but polls with the non-blocking test_wait: the
-// thread never sleeps, so it sees the phase complete within a few cycles.
-// For short, latency-critical handshakes (one per 128-deep K block).
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity,
-                                               volatile uint32_t* abort_flag) {
-    const uint32_t a = smem_u32(bar);
-    if (mbar_test_wait(a, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_test_wait(a, parity)) return true;
-        if ((it & 1023u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitTimeoutNs) {
-                *abort_flag = 1u;
-                return false;
-            }
-        }
-    }
-}
-
 // ------------------------------------------------- programmatic dependent launch
 //
 // Kernels of this library may be launched with programmatic stream

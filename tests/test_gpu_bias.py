@@ -57,6 +57,9 @@ def _scales(gran, rows, K, seed):
     ("pair_f32_acc", 512, 400, 256, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_F32, True, F.LAYOUT_TN),
     ("row", 512, 384, 256, F.GRAN_ROW, F.GRAN_ROW, F.OUT_BF16, False, F.LAYOUT_TN),
     ("block", 256, 256, 384, F.GRAN_1x128, F.GRAN_128x128, F.OUT_BF16, False, F.LAYOUT_TN),
+    # N = 384: the last 256-column tile is half outside the matrix
+    ("block_half_tile", 384, 384, 512, F.GRAN_1x128, F.GRAN_128x128, F.OUT_BF16, False,
+     F.LAYOUT_TN),
     ("block_colscale_f32", 256, 384, 256, F.GRAN_1x128, F.GRAN_1x128, F.OUT_F32, True, F.LAYOUT_TN),
     ("k0", 64, 96, 0, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_BF16, False, F.LAYOUT_TN),
     ("k0_f32_acc", 64, 96, 0, F.GRAN_TENSOR, F.GRAN_TENSOR, F.OUT_F32, True, F.LAYOUT_TN),
