@@ -380,6 +380,7 @@ def run_gpu(args):
     torch.cuda.empty_cache()
 
     e2e = e2e_pass(F, wl, dev, args, stream) if rank == 0 else None
+    e2e_all = e2e_pass(F, wl, dev, args, stream, all_tensors=True) if rank == 0 else None
     extras = {}
     if rank == 0 and not args.no_extras:
         extras["llama2_7b_delayed_step"] = extra_layer_step(F, LLAMA7B, dev, flush, stream,
@@ -419,6 +420,7 @@ def run_gpu(args):
         # grouped dgrad + wgrad GEMM
         "gpu_launches": LAUNCHES_PER_LINEAR * len(wl.linears) * wl.micro_batches * args.steps,
         "e2e": e2e,
+        "e2e_all_tensors": e2e_all,
         "clocks": clk,
         **extras,
     }
@@ -607,24 +609,28 @@ def small_case_pass(F, dev, stream, iters=200):
     return out
 
 
-def e2e_pass(F, wl: Workload, dev, args, stream):
-    """Public API with host buffers.  Per step: H2D of each linear's W once,
-    and per micro-batch of its X and dY, from pinned memory;
-    fp8_linear_fwd + fp8_linear_bwd; D2H of Y and dX per micro-batch and of
-    dW once the last micro-batch has accumulated into it -- all inside the
-    timed region.  The copies run on their own streams, ordered by events, so
-    that they overlap the compute and each other as a training loop's would:
-    X and dY of a unit (one micro-batch of one linear) arrive up to two units
-    ahead (three device buffer sets); a linear's W for the next step is
-    uploaded on a stream of its own once the step's last forward of that
-    linear has quantised the current one (the backward reads the codes, not
-    W); Y leaves while the backward runs, dX after it, and dW after the last
-    micro-batch, before the next step's first backward of that linear
-    overwrites it."""
+def e2e_pass(F, wl: Workload, dev, args, stream, all_tensors=False):
+    """Public API with host buffers, every copy inside the timed region, in the
+    traffic pattern of a training loop: per micro-batch the step's data, X
+    and dY of each linear, goes host -> device from pinned memory; the weights
+    stay on the device (uploaded once before timing, where an optimizer keeps
+    them); Y, dX and dW stay on the device (for the next layer and the
+    optimizer); and after each linear's last micro-batch its scaling metrics
+    (the amax and dequantisation factor of every role) come back to pinned
+    host memory.  fp8_linear_fwd + fp8_linear_bwd per micro-batch and linear.
+    all_tensors: every tensor crosses the host link every step as well -- W
+    in, Y and dX per micro-batch and dW out -- which makes the link the bound.
+    The copies run on their own streams, ordered by events, so that they
+    overlap the compute and each other: X and dY of a unit (one micro-batch
+    of one linear) arrive up to two units ahead (three device buffer sets);
+    a linear's next W (all_tensors) is uploaded on a stream of its own once
+    the step's last forward of that linear has quantised the current one (the
+    backward reads the codes, not W); results leave on a third stream, before
+    the next step's first use of the linear overwrites them."""
     nl, MB, T = len(wl.linears), wl.micro_batches, wl.tokens
     NB = 3
     recipe = wl.recipe(F)
-    h_w, h_x, h_dy, h_y, h_dx, h_dw, layers = [], [], [], [], [], [], []
+    h_w, h_x, h_dy, h_y, h_dx, h_dw, h_met, layers = [], [], [], [], [], [], [], []
     for li, (name, K, N) in enumerate(wl.linears):
         h_w.append(synthetic.normal((N, K), 0.02, seed=1000 + li, device=dev).cpu().pin_memory())
         h_x.append([synthetic.with_outlier_channels((T, K), 1.0, wl.outlier_channels(K), 50.0,
@@ -632,10 +638,12 @@ def e2e_pass(F, wl: Workload, dev, args, stream):
                     for mb in range(MB)])
         h_dy.append([synthetic.normal((T, N), 1e-3, seed=500 + 10 * li + mb,
                                       device=dev).cpu().pin_memory() for mb in range(MB)])
-        h_y.append([torch.empty(T, N, dtype=torch.bfloat16).pin_memory() for _ in range(MB)])
-        h_dx.append([torch.empty(T, K, dtype=torch.bfloat16).pin_memory() for _ in range(MB)])
-        h_dw.append(torch.empty(N, K, dtype=torch.float32).pin_memory())
+        if all_tensors:
+            h_y.append([torch.empty(T, N, dtype=torch.bfloat16).pin_memory() for _ in range(MB)])
+            h_dx.append([torch.empty(T, K, dtype=torch.bfloat16).pin_memory() for _ in range(MB)])
+            h_dw.append(torch.empty(N, K, dtype=torch.float32).pin_memory())
         layers.append(F.Fp8Linear(T, N, K, recipe, device=dev))
+        h_met.append(torch.empty(2, layers[-1].amax.numel(), dtype=torch.float32).pin_memory())
     kmax = max(k for _, k, _ in wl.linears)
     nmax = max(n for _, _, n in wl.linears)
     d_w = [torch.empty(n, k, dtype=torch.bfloat16, device=dev) for _, k, n in wl.linears]
@@ -650,11 +658,14 @@ def e2e_pass(F, wl: Workload, dev, args, stream):
     bufs = [dbuf() for _ in range(NB)]
     h2d_s, w_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     nbytes = lambda t: t.numel() * t.element_size()
-    h2d = sum(nbytes(w) for w in h_w) + sum(nbytes(t) for ts in h_x + h_dy for t in ts)
-    d2h = sum(nbytes(t) for ts in h_y + h_dx for t in ts) + sum(nbytes(t) for t in h_dw)
+    h2d = sum(nbytes(t) for ts in h_x + h_dy for t in ts)
+    d2h = sum(nbytes(t) for t in h_met)
+    if all_tensors:
+        h2d += sum(nbytes(w) for w in h_w)
+        d2h += sum(nbytes(t) for ts in h_y + h_dx for t in ts) + sum(nbytes(t) for t in h_dw)
     # Units g = (step * MB + mb) * nl + li use device buffer set g % NB; each
     # copy waits only for the last user of its own buffer.
-    computed, drained, w_loaded, dw_drained = {}, {}, {}, {}
+    computed, drained, w_loaded, res_drained = {}, {}, {}, {}
     counter = [0]
 
     def upload_w(li, after=None):
@@ -683,38 +694,43 @@ def e2e_pass(F, wl: Workload, dev, args, stream):
 
     def compute_and_drain(g, li, mb, K, N, b, loaded):
         stream.wait_event(loaded)
-        if mb == 0:
+        if mb == 0 and li in w_loaded:
             stream.wait_event(w_loaded.pop(li))            # this step's W[li] has arrived
         if g - NB in drained:
             stream.wait_event(drained.pop(g - NB))         # this set's outputs have left
-        if mb == 0 and li in dw_drained:
-            stream.wait_event(dw_drained.pop(li))          # last step's dW[li] has left
+        if mb == 0 and li in res_drained:
+            stream.wait_event(res_drained.pop(li))         # last step's results of li have left
         Y = b["Y"][:T * N].view(T, N)
         dX = b["dX"][:T * K].view(T, K)
         L = layers[li]
         L.forward(b["X"][:T * K].view(T, K), d_w[li], Y=Y)
         fwd_done = torch.cuda.Event()
         fwd_done.record(stream)
-        if mb == MB - 1:
-            upload_w(li, after=fwd_done)                   # the next step's W[li]
-        with torch.cuda.stream(d2h_s):                     # Y leaves while the backward runs
-            d2h_s.wait_event(fwd_done)
-            h_y[li][mb].copy_(Y, non_blocking=True)
+        if all_tensors:
+            if mb == MB - 1:
+                upload_w(li, after=fwd_done)               # the next step's W[li]
+            with torch.cuda.stream(d2h_s):                 # Y leaves while the backward runs
+                d2h_s.wait_event(fwd_done)
+                h_y[li][mb].copy_(Y, non_blocking=True)
         L.backward(b["dY"][:T * N].view(T, N), dX=dX, dW=d_dw[li], accumulate_dW=mb > 0)
         ev = torch.cuda.Event()
         ev.record(stream)
         computed[g] = ev
         with torch.cuda.stream(d2h_s):
             d2h_s.wait_event(ev)
-            h_dx[li][mb].copy_(dX, non_blocking=True)
-            done = torch.cuda.Event()
-            done.record(d2h_s)
-            drained[g] = done
+            if all_tensors:
+                h_dx[li][mb].copy_(dX, non_blocking=True)
+                done = torch.cuda.Event()
+                done.record(d2h_s)
+                drained[g] = done
             if mb == MB - 1:
-                h_dw[li].copy_(d_dw[li], non_blocking=True)
-                dwd = torch.cuda.Event()
-                dwd.record(d2h_s)
-                dw_drained[li] = dwd
+                h_met[li][0].copy_(L.amax, non_blocking=True)
+                h_met[li][1].copy_(L.scale_inv, non_blocking=True)
+                if all_tensors:
+                    h_dw[li].copy_(d_dw[li], non_blocking=True)
+                rd = torch.cuda.Event()
+                rd.record(d2h_s)
+                res_drained[li] = rd
 
     def steps(k, first):
         """k steps, loads issued up to NB - 1 units ahead."""
@@ -741,20 +757,30 @@ def e2e_pass(F, wl: Workload, dev, args, stream):
     b.record(stream)
     torch.cuda.synchronize()
     assert F.fp8_device_status() == 0
+    assert all(bool(torch.isfinite(m).all()) for m in h_met)
     ms = a.elapsed_time(b) / n
-    link = _host_link(dev)
-    floor_ms = _link_floor_ms(h2d, d2h, link)
-    return {"value": round(wl.flops_step() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-            "ms_per_step": round(ms, 3), "steps": n, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h,
-            "copies": "pinned host <-> device on three copy streams (inputs, weights, "
-                      "results), overlapped with compute and with each other across linears, "
-                      "micro-batches and steps",
+    out = {"value": round(wl.flops_step() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+           "ms_per_step": round(ms, 3), "steps": n, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h}
+    if all_tensors:
+        link = _host_link(dev)
+        out.update({
+            "copies": "W of every linear in, X and dY per micro-batch in, Y and dX per "
+                      "micro-batch and dW per step out, on three copy streams overlapped with "
+                      "compute and with each other",
             "host_link": link,
-            "link_floor_ms": round(floor_ms, 3),
+            "link_floor_ms": round(_link_floor_ms(h2d, d2h, link), 3),
             "link_floor_note": "the time to move h2d and d2h bytes at the link rates measured "
                                "in this run: both directions at their concurrent rates until "
-                               "the smaller finishes, the rest at its one-way rate"}
+                               "the smaller finishes, the rest at its one-way rate"})
+    else:
+        out["copies"] = ("X and dY of every linear and micro-batch in (pinned host memory, up "
+                         "to two units ahead of the compute); after each step the scaling "
+                         "metrics of every linear (amax and dequantisation factor per role) "
+                         "out; weights, outputs and gradients stay on the device, as in a "
+                         "training loop")
+        out["h2d_floor_ms"] = round(h2d / (_host_link(dev)["h2d_gbs"] * 1e9) * 1e3, 3)
+    return out
 
 
 def _link_floor_ms(h2d, d2h, link):
