@@ -789,8 +789,8 @@ struct BpCfg {
     static constexpr int smem(bool colscale) {
         return STAGES * STAGE_BYTES + EPI * (2048 + (colscale ? 4 * CW * 4 : 0)) + 256 + 1024;
     }
-    static_assert(CW % 32 == 0 && 128 % CW == 0, "a warp's columns: whole 32-column loads "
-                                                 "inside one 128-column factor block");
+    static_assert(CW == 64, "a warp's columns: one 64-column slice of a 128-column factor "
+                            "block, loaded as two 32-column chunks");
     static_assert(4 * 32 * RROLE + EPI * 32 * RPROMO <= THREADS * (65536 / THREADS / 8 * 8),
                   "the register split fits the launch's registers");
 };
@@ -820,21 +820,23 @@ __device__ __forceinline__ void block_factors4(float (&f)[4], const float* s, in
     }
 }
 
-// acc[e] += r[2e..2e+1] * f for the 16 packed pairs of a 32-column chunk.
-__device__ __forceinline__ void promote_uniform(uint64_t* acc, const uint32_t (&r)[32], uint64_t ff) {
+// acc[e] += r[2e..2e+1] * f for the NC / 2 packed pairs of NC columns.
+template <int NC>
+__device__ __forceinline__ void promote_uniform(uint64_t* acc, const uint32_t* r, uint64_t ff) {
 #pragma unroll
-    for (int e = 0; e < 16; ++e)
+    for (int e = 0; e < NC / 2; ++e)
         acc[e] = ptx::ffma2(static_cast<uint64_t>(r[2 * e]) | (static_cast<uint64_t>(r[2 * e + 1]) << 32),
                             ff, acc[e]);
 }
 
-// acc[e] += r[2e..2e+1] * fp32(fa * cf[2e..2e+1]): per-column factors cf (32
-// floats in shared memory, read as broadcasts).
-__device__ __forceinline__ void promote_columns(uint64_t* acc, const uint32_t (&r)[32], float fa,
+// acc[e] += r[2e..2e+1] * fp32(fa * cf[2e..2e+1]) for NC columns: per-column
+// factors cf (NC floats in shared memory, read as broadcasts).
+template <int NC>
+__device__ __forceinline__ void promote_columns(uint64_t* acc, const uint32_t* r, float fa,
                                                 const float* cf) {
     const uint64_t faa = pack2(fa, fa);
 #pragma unroll
-    for (int e4 = 0; e4 < 8; ++e4) {
+    for (int e4 = 0; e4 < NC / 4; ++e4) {
         const float4 c = *reinterpret_cast<const float4*>(cf + 4 * e4);
         const uint64_t f0 = ptx::fmul2(faa, pack2(c.x, c.y));
         const uint64_t f1 = ptx::fmul2(faa, pack2(c.z, c.w));
@@ -1081,24 +1083,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                     __syncwarp();
                     ptx::tc_fence_after();
                     const uint32_t ta = tmem_base + lanes + buf * TN + h * CW;
-                    // one 32-column load at a time (the accumulator takes most
-                    // of the registers); the buffer goes back after the last
-                    uint32_t r[32];
-#pragma unroll
-                    for (int c = 0; c < NCH; ++c) {
-                        ptx::tmem_ld_32x32b_x32(ta + 32 * c, r);
-                        ptx::tmem_wait_ld();
-                        if (c == NCH - 1) {
-                            ptx::tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0)
-                                ptx::mbar_arrive_cluster_relaxed(ptx::cluster_addr(&tempty[buf], 0));
-                        }
+                    // The warp's 64 columns as two 32-column loads, one at a
+                    // time (the accumulator takes most of the registers); the
+                    // buffer goes back once the second has landed.  Measured:
+                    // overlapping the second half's loads with the first
+                    // half's promotion (16-column loads) spilled or ran 4-46%
+                    // slower.
+                    const uint64_t ff = pack2(fa[j], fa[j]);
+                    const float* cfj = cf + j * CW;
+                    auto promote32 = [&](int col, const uint32_t* r) {
                         if (COLSCALE)
-                            promote_columns(acc + 16 * c, r, fa[j], cf + j * CW + 32 * c);
+                            promote_columns<32>(acc + col / 2, r, fa[j], cfj + col);
                         else
-                            promote_uniform(acc + 16 * c, r, pack2(fa[j], fa[j]));
-                    }
+                            promote_uniform<32>(acc + col / 2, r, ff);
+                    };
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(ta, r);
+                    ptx::tmem_wait_ld();
+                    promote32(0, r);
+                    ptx::tmem_ld_32x32b_x32(ta + 32, r);
+                    ptx::tmem_wait_ld();
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive_cluster_relaxed(ptx::cluster_addr(&tempty[buf], 0));
+                    promote32(32, r);
                     if (++buf == NBUF) { buf = 0; buf_phase ^= 1u; }
                 }
             }
