@@ -1079,10 +1079,12 @@ def run_kernel(args):
             call = lambda: F.fp8_gemm(A, F.E4M3, B, F.E4M3, sa, sb, F.GRAN_1x128 | F.SCALE_POW2,
                                       F.GRAN_128x128 | F.SCALE_POW2, D=D)
         else:
+            # B per 128 x 128 block, or (--colscale, the block wgrad) per column
+            gb = F.GRAN_1x128 if args.colscale else F.GRAN_128x128
             sa = torch.rand(M, K // 128, generator=g, device=dev) + 0.5
-            sb = torch.rand(N // 128, K // 128, generator=g, device=dev) + 0.5
-            call = lambda: F.fp8_gemm(A, F.E4M3, B, F.E4M3, sa, sb, F.GRAN_1x128,
-                                      F.GRAN_128x128, D=D)
+            sb = torch.rand(N if args.colscale else N // 128, K // 128, generator=g,
+                            device=dev) + 0.5
+            call = lambda: F.fp8_gemm(A, F.E4M3, B, F.E4M3, sa, sb, F.GRAN_1x128, gb, D=D)
         work, unit, peak = 2.0 * M * N * K, "TFLOP/s", 2.0 * bf16_burst
     else:
         R, C = dims
@@ -1133,7 +1135,9 @@ def run_kernel(args):
         extra = {"granularity": args.gran, "transpose": not args.no_transpose}
     if args.kernel == "block_gemm":
         extra = {"factors": "power of two (block-scaled MMA)" if args.pow2
-                 else "fp32 (per-128-K promotion)"}
+                 else "fp32 (per-128-K promotion)",
+                 "b_factors": "per column (1x128)" if args.colscale and not args.pow2
+                 else "per 128 x 128 block"}
     if args.kernel == "gemm":
         extra = {"output": "fp32, accumulated" if args.f32acc else "bf16", "layout": args.layout}
     print(json.dumps({"kernel": args.kernel, "shape": dims, "format": args.fmt, **extra,
@@ -1288,6 +1292,9 @@ def main():
                     help="gemm: FP32 output accumulated into D (the wgrad form)")
     ap.add_argument("--layout", choices=["tn", "b_kn", "a_km", "km_kn"], default="tn",
                     help="gemm: operand storage (b_kn: B as [K x N]; a_km: A as [K x M]; km_kn: both)")
+    ap.add_argument("--colscale", action="store_true",
+                    help="--kernel block_gemm: B with 1x128 factors (one per output column and "
+                         "K block, the block-wise wgrad)")
     ap.add_argument("--pow2", action="store_true",
                     help="block_gemm / block_step: power-of-two block factors (the block-scaled MMA path)")
     ap.add_argument("--no-transpose", action="store_true",

@@ -748,7 +748,8 @@ __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
 // take issue slots from the producer and MMA warps on their sub-partitions.
 // COLSCALE: B carries 1x128 scales (one factor per output column and K
 // block, the block-wise wgrad); each promotion warp stages its columns'
-// factors of four K blocks in shared memory, read back as broadcasts.
+// factors of four K blocks in shared memory, read back as broadcasts, and its
+// rows' factors beside them (the factor products leave no registers for them).
 //
 // The instance (BpWide): 256 x 256 tiles, so that each MMA is N = 256 (with
 // N = 128 the MMAs alone stop at 0.54-0.60 of the tensor core's rate,
@@ -766,7 +767,8 @@ __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
 // read at the start of each group of four K blocks rather than one group
 // ahead (6% faster: the prefetched values held 8 registers and made the loop
 // spill); per-column factor products by packed mul.rn.f32x2 (scalar
-// multiplies made the COLSCALE loop 38% slower); 256 x 160 tiles with three
+// multiplies made the COLSCALE loop 38% slower) and, for COLSCALE, 16-column
+// TMEM loads (3% faster there, with fewer spills); 256 x 160 tiles with three
 // buffers and 20 promotion warps were 30% slower, and 256 x 128 tiles with
 // four buffers and 8 warps (the earlier form) 24% slower (COLSCALE: 9%).
 template <int TN_, int EPI_, int STAGES_, int RROLE_, int RPROMO_>
@@ -785,9 +787,11 @@ struct BpCfg {
     static constexpr int B_BYTES = (TN / 2) * BK;    // this CTA's half of the TN rows of B
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     // shared memory: operand ring, 2 KB of output staging per promotion
-    // warp, per-column factors (COLSCALE only), barriers, alignment slack
+    // warp, per-column and per-row factors (COLSCALE only), barriers,
+    // alignment slack
     static constexpr int smem(bool colscale) {
-        return STAGES * STAGE_BYTES + EPI * (2048 + (colscale ? 4 * CW * 4 : 0)) + 256 + 1024;
+        return STAGES * STAGE_BYTES + EPI * (2048 + (colscale ? 4 * (CW + 32) * 4 : 0)) + 256 +
+               1024;
     }
     static_assert(CW == 64, "a warp's columns: one 64-column slice of a 128-column factor "
                             "block, loaded as two 32-column chunks");
@@ -914,8 +918,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
     uint8_t* ring = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* epi_stage = ring + STAGES * STAGE_BYTES;   // output boxes: 2 KB per epilogue warp
-    float* colf = reinterpret_cast<float*>(epi_stage + EPI * 2048);   // [warp][4][cols]
-    uint64_t* full = reinterpret_cast<uint64_t*>(colf + (COLSCALE ? EPI * 4 * Cfg::CW : 0));
+    float* colf = reinterpret_cast<float*>(epi_stage + EPI * 2048);   // [warp][4][cols + 32]
+    uint64_t* full = reinterpret_cast<uint64_t*>(colf + (COLSCALE ? EPI * 4 * (Cfg::CW + 32) : 0));
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + NBUF;
@@ -1032,7 +1036,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
         const int qd = warp & 3;                 // TMEM lane quarter of this warp
         const int h = (warp - 4) >> 2;           // which CW of the tile's 128 columns
         uint8_t* slot = epi_stage + (warp - 4) * 2048;
-        float* cf = colf + (warp - 4) * 4 * CW;  // COLSCALE: [4 K blocks][CW columns]
+        // COLSCALE: the columns' factors [4 K blocks][CW], then the rows'
+        // [4 K blocks][32 lanes]
+        float* cf = colf + (warp - 4) * 4 * (CW + 32);
+        float* rf = cf + 4 * CW;
         const uint32_t lanes = static_cast<uint32_t>(qd * 32) << 16;
         uint32_t buf = 0, buf_phase = 0;
         bool ok = true;
@@ -1056,11 +1063,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                 // (they hit L1; holding the next group's in registers made the
                 // loop spill): A per row; B per 128-column block, multiplied
                 // into fa here, or (COLSCALE) per column, staged in shared
-                // memory for broadcast reads (lane l writes columns n0+32c+l).
+                // memory for broadcast reads (lane l writes columns n0+32c+l),
+                // with the rows' factors beside them (registers are short).
                 float fa[4], fb[4];
                 block_factors4(fa, p.sa, p.ga, m_safe, kb0, KB, vec_a != 0);
                 if (COLSCALE) {
                     __syncwarp();   // the previous group's factors have been read
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) rf[j * 32 + lane] = fa[j];
 #pragma unroll
                     for (int c = 0; c < NCH; ++c) {
                         block_factors4(fb, p.sb, p.gb, nf + (n0 < p.N ? 32 * c + lane : 0), kb0, KB,
@@ -1085,29 +1095,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t ta = tmem_base + lanes + buf * TN + h * CW;
                     // The warp's 64 columns as two 32-column loads, one at a
                     // time (the accumulator takes most of the registers); the
-                    // buffer goes back once the second has landed.  Measured:
+                    // buffer goes back once the last has landed.  Measured:
                     // overlapping the second half's loads with the first
                     // half's promotion (16-column loads) spilled or ran 4-46%
-                    // slower.
-                    const uint64_t ff = pack2(fa[j], fa[j]);
-                    const float* cfj = cf + j * CW;
-                    auto promote32 = [&](int col, const uint32_t* r) {
-                        if (COLSCALE)
-                            promote_columns<32>(acc + col / 2, r, fa[j], cfj + col);
-                        else
-                            promote_uniform<32>(acc + col / 2, r, ff);
-                    };
-                    uint32_t r[32];
-                    ptx::tmem_ld_32x32b_x32(ta, r);
-                    ptx::tmem_wait_ld();
-                    promote32(0, r);
-                    ptx::tmem_ld_32x32b_x32(ta + 32, r);
-                    ptx::tmem_wait_ld();
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        ptx::mbar_arrive_cluster_relaxed(ptx::cluster_addr(&tempty[buf], 0));
-                    promote32(32, r);
+                    // slower.  COLSCALE, whose factor products need more
+                    // registers, loads 16 columns at a time (3% faster).
+                    if constexpr (COLSCALE) {
+                        const float faj = rf[j * 32 + lane];
+                        const float* cfj = cf + j * CW;
+                        uint32_t r[16];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            ptx::tmem_ld_32x32b_x16(ta + 16 * c, r);
+                            ptx::tmem_wait_ld();
+                            if (c == 3) {
+                                ptx::tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0)
+                                    ptx::mbar_arrive_cluster_relaxed(ptx::cluster_addr(&tempty[buf], 0));
+                            }
+                            promote_columns<16>(acc + 8 * c, r, faj, cfj + 16 * c);
+                        }
+                    } else {
+                        const uint64_t ff = pack2(fa[j], fa[j]);
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32(ta, r);
+                        ptx::tmem_wait_ld();
+                        promote_uniform<32>(acc, r, ff);
+                        ptx::tmem_ld_32x32b_x32(ta + 32, r);
+                        ptx::tmem_wait_ld();
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            ptx::mbar_arrive_cluster_relaxed(ptx::cluster_addr(&tempty[buf], 0));
+                        promote_uniform<32>(acc + 16, r, ff);
+                    }
                     if (++buf == NBUF) { buf = 0; buf_phase ^= 1u; }
                 }
             }
