@@ -1226,19 +1226,19 @@ __global__ void __launch_bounds__(kThreads)
     transpose_tile_out(S, qt, rows, r0, c0, rows, cols);
 }
 
-// scale_inv_t[c] = 1 / s(amax_c), in place over the column amaxes.
+// a[i] = 1 / s(amax_i) for i < na, then b[i] likewise for i < nb, in place
+// over the row and column amaxes: one launch for both.
 template <int FMT>
-__global__ void column_scale_finalize_kernel(float* __restrict__ sinv_t, int64_t cols, int pow2) {
+__global__ void row_col_scale_finalize_kernel(float* __restrict__ a, int64_t na,
+                                              float* __restrict__ b, int64_t nb, int pow2) {
     // (tiny kernel: the next one may launch once the kernel before this one
     // has completed, not earlier, so a chain of launches cannot run ahead of
     // a large kernel)
     ptx::griddep_wait();   // the previous kernel's results are visible
     ptx::griddep_launch_dependents();
-    const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (c < cols) {
-        const float amax = sinv_t[c];
-        sinv_t[c] = __fdiv_rn(1.0f, block_scale<FMT>(amax, pow2));
-    }
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    float* p = i < na ? a + i : (i - na < nb ? b + (i - na) : nullptr);
+    if (p) *p = __fdiv_rn(1.0f, block_scale<FMT>(*p, pow2));
 }
 
 int grid_for(int64_t work_items, int per_cta) {
@@ -1511,10 +1511,8 @@ static cudaError_t launch_row(const uint16_t* xs, int64_t rows, int64_t cols, in
                                                                                rmax, cmax);
     launch_pdl(quantize_row_col_kernel<FMT>, dim3(static_cast<unsigned>(tiles)), dim3(kThreads), 0, stream, 
         xs, rows, cols, tiles_c, pow2, rmax, cmax, q, q_t);
-    launch_pdl(column_scale_finalize_kernel<FMT>, dim3(static_cast<unsigned>((rows + 255) / 256)), dim3(256), 0, stream, 
-        scale_inv, rows, pow2);
-    launch_pdl(column_scale_finalize_kernel<FMT>, dim3(static_cast<unsigned>((cols + 255) / 256)), dim3(256), 0, stream, 
-        scale_inv_t, cols, pow2);
+    launch_pdl(row_col_scale_finalize_kernel<FMT>, dim3(static_cast<unsigned>((rows + cols + 255) / 256)),
+               dim3(256), 0, stream, scale_inv, rows, scale_inv_t, cols, pow2);
     return cudaGetLastError();
 }
 
