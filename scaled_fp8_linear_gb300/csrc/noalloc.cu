@@ -90,3 +90,20 @@ extern "C" int fp8_linear_bwd_noalloc(const void* dY, int64_t M, int64_t N, int6
     return fp8_linear_bwd(dY, M, N, K, recipe, state, dX, dW, accumulate_dW, nullptr, scratch,
                           kScratchBytes, stream);
 }
+
+// Test hook, not part of the ABI that include/fp8linear.h declares: the
+// scratch address that fp8_linear_bwd_noalloc would use in the current
+// context (*cached, from the per-context table) and a fresh lookup of the
+// array's address in that context (*fresh).  The two must agree in every
+// context, also after other contexts have been used.
+extern "C" int fp8_test_noalloc_scratch(void** cached, void** fresh) {
+    if (!cached || !fresh)
+        return fp8::set_error(FP8_ERR_INVALID_ARG, "fp8_test_noalloc_scratch: NULL pointer");
+    const int st = scratch_in_current_context(cached);
+    if (st != FP8_OK) return st;
+    const cudaError_t e = cudaGetSymbolAddress(fresh, g_bwd_scratch);
+    if (e != cudaSuccess)
+        return fp8::set_error(FP8_ERR_CUDA, "fp8_test_noalloc_scratch: cudaGetSymbolAddress: %s",
+                              cudaGetErrorString(e));
+    return FP8_OK;
+}

@@ -153,3 +153,46 @@ def test_noalloc_takes_twice_the_tokens_without_transposed_copies():
     _same_bits(dX_na, dX_ref, "dX")
     _same_bits(dW_na, dW_ref, "dW")
     assert torch.equal(na_layer.scale, ref_layer.scale)
+
+
+def _scratch_addresses():
+    """(address from the per-context table, fresh lookup) in the current context."""
+    fn = F.lib().fp8_test_noalloc_scratch
+    fn.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p)]
+    fn.restype = ctypes.c_int
+    cached, fresh = ctypes.c_void_p(), ctypes.c_void_p()
+    assert fn(ctypes.byref(cached), ctypes.byref(fresh)) == 0, F.fp8_last_error()
+    return cached.value, fresh.value
+
+
+def test_noalloc_scratch_address_belongs_to_the_current_context():
+    """The scratch address is looked up once per CUDA context: in the primary
+    context and in a second context of the same device (made current with the
+    driver API) it equals a fresh lookup, and the primary context's entry is
+    still right after the other context has been used."""
+    F.build()
+    torch.zeros(1, device=DEV)
+    torch.cuda.synchronize()
+    c0, f0 = _scratch_addresses()
+    assert c0 and c0 == f0
+    try:
+        cu = ctypes.CDLL("libcuda.so.1")
+        create, pop, destroy = cu.cuCtxCreate_v2, cu.cuCtxPopCurrent_v2, cu.cuCtxDestroy_v2
+    except (OSError, AttributeError):
+        pytest.skip("the driver API's context calls are not available")
+    create.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_uint, ctypes.c_int]
+    pop.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+    destroy.argtypes = [ctypes.c_void_p]
+    dev = ctypes.c_int()
+    assert cu.cuDeviceGet(ctypes.byref(dev), torch.cuda.current_device()) == 0
+    ctx = ctypes.c_void_p()
+    assert create(ctypes.byref(ctx), 0, dev.value) == 0
+    try:
+        c1, f1 = _scratch_addresses()
+        assert c1 and c1 == f1
+    finally:
+        popped = ctypes.c_void_p()
+        assert pop(ctypes.byref(popped)) == 0 and popped.value == ctx.value
+        assert destroy(ctx) == 0
+    c2, f2 = _scratch_addresses()
+    assert c2 == f2 == c0
