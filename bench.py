@@ -388,6 +388,7 @@ def run_gpu(args):
                                                             peak_kind)
         extras["block_scaled"] = extra_block_scaled(F, dev, flush, stream, bf16_burst)
         extras["quantize_sweep"] = extra_quantize_points(F, dev, flush, stream, hbm_gbs)
+        extras["recipe_casts"] = extra_recipe_casts(F, dev, flush, stream, hbm_gbs)
         extras["small_case"] = small_case_pass(F, dev, stream)
     if world > 1:
         import torch.distributed as dist
@@ -552,6 +553,66 @@ def extra_quantize_points(F, dev, flush, stream, hbm_gbs, iters=10, warmup=3):
     assert F.fp8_device_status() == 0
     return {"mode": "stale scale, fused amax", "iters": iters,
             "l2": "flushed before every launch", "peak_gbs": hbm_gbs, "points": out}
+
+
+def extra_recipe_casts(F, dev, flush, stream, hbm_gbs, iters=10, warmup=3):
+    """The casts of the other recipes, each with its transposed output: the
+    block recipe's dual 1x128 cast (activations and gradients) and 128 x 128
+    cast (weights), the per-row cast with the per-column cast of x^T, the
+    per-tensor cast with the fused underflow / saturation counters, and the
+    stochastically rounded per-tensor cast.  Algorithmic bytes: 2 read + 1
+    per code written (q and q^T) + 4 per scale."""
+    out = []
+
+    def timed(name, shape, fmt_name, work_bytes, call):
+        for _ in range(warmup):
+            call()
+        ev = _events(iters)
+        for i in range(iters):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        med, _ = _median_ms(ev)
+        gbs = work_bytes / (med * 1e-3) / 1e9
+        out.append({"cast": name, "shape": list(shape), "format": fmt_name,
+                    "median_ms": round(med, 4), "achieved_gbs": round(gbs, 1),
+                    "frac": round(gbs / hbm_gbs, 4)})
+
+    R, C = 16384, 7168
+    x = synthetic.student_t_rows((R, C), 1.0, 3, seed=7, device=dev)
+    q = torch.empty(R, C, dtype=torch.uint8, device=dev)
+    qt = torch.empty(C, R, dtype=torch.uint8, device=dev)
+    for name, gran in (("block 1x128, with the 1x128 cast of x^T", F.GRAN_1x128),
+                       ("block 128x128, with x^T", F.GRAN_128x128),
+                       ("per row, with the per-row cast of x^T", F.GRAN_ROW)):
+        s1 = torch.empty(F._scale_shape(gran, R, C), dtype=torch.float32, device=dev)
+        s2 = torch.empty(F._scale_shape_t(gran, R, C), dtype=torch.float32, device=dev)
+        timed(name, (R, C), "e4m3", 4.0 * R * C + 4.0 * (s1.numel() + s2.numel()),
+              lambda: F.fp8_quantize(x, F.E4M3, gran, q=q, q_t=qt, scale_inv_blocks=s1,
+                                     scale_inv_blocks_t=s2))
+    del x, q, qt
+    am = torch.empty(1, dtype=torch.float32, device=dev)
+    one = torch.ones(1, dtype=torch.float32, device=dev)
+    counts = torch.zeros(2, dtype=torch.int64, device=dev)
+    seed = iter(range(1, 1 << 30))
+    for (R, C), name, fmt_name, fmt, call in (
+            ((16384, 8192), "per tensor, fused counters, with x^T", "e4m3", F.E4M3,
+             lambda: F.fp8_quantize_counted(x, F.E4M3, one, counts=counts, q=q, q_t=qt,
+                                            amax_out=am)),
+            ((65536, 8192), "per tensor, stochastic rounding, with x^T", "e5m2", F.E5M2,
+             lambda: F.fp8_quantize_sr(x, F.E5M2, one, next(seed), 0, q=q, q_t=qt,
+                                       amax_out=am))):
+        x = synthetic.student_t((R, C), 3, 1.0, seed=R, device=dev)
+        q = torch.empty(R, C, dtype=torch.uint8, device=dev)
+        qt = torch.empty(C, R, dtype=torch.uint8, device=dev)
+        timed(name, (R, C), fmt_name, 4.0 * R * C, call)
+        del x, q, qt
+    torch.cuda.empty_cache()
+    assert F.fp8_device_status() == 0
+    return {"iters": iters, "l2": "flushed before every launch", "peak_gbs": hbm_gbs,
+            "points": out}
 
 
 def small_case_pass(F, dev, stream, iters=200):
@@ -1102,6 +1163,11 @@ def run_kernel(args):
         if args.kernel == "quantize_sr":
             seed = iter(range(1, 1 << 30))
             call = lambda: F.fp8_quantize_sr(x, fa, one, next(seed), 0, q=q, q_t=qt_arg, amax_out=am)
+        elif gran == F.GRAN_TENSOR and args.counted:
+            # the cast with the fused underflow / saturation counters
+            counts = torch.zeros(2, dtype=torch.int64, device=dev)
+            call = lambda: F.fp8_quantize_counted(x, fa, one, counts=counts, q=q, q_t=qt_arg,
+                                                  amax_out=am)
         elif gran == F.GRAN_TENSOR:
             call = lambda: F.fp8_quantize(x, fa, scale=one, q=q, q_t=qt_arg, amax_out=am)
         else:
@@ -1133,6 +1199,8 @@ def run_kernel(args):
     extra = {}
     if args.kernel in ("quantize", "quantize_sr"):
         extra = {"granularity": args.gran, "transpose": not args.no_transpose}
+        if args.counted and args.gran == "tensor" and args.kernel == "quantize":
+            extra["counters"] = "underflow and saturation, fused"
     if args.kernel == "block_gemm":
         extra = {"factors": "power of two (block-scaled MMA)" if args.pow2
                  else "fp32 (per-128-K promotion)",
@@ -1292,6 +1360,9 @@ def main():
                     help="gemm: FP32 output accumulated into D (the wgrad form)")
     ap.add_argument("--layout", choices=["tn", "b_kn", "a_km", "km_kn"], default="tn",
                     help="gemm: operand storage (b_kn: B as [K x N]; a_km: A as [K x M]; km_kn: both)")
+    ap.add_argument("--counted", action="store_true",
+                    help="--kernel quantize --gran tensor: the cast with the fused underflow / "
+                         "saturation counters (fp8_quantize_counted)")
     ap.add_argument("--colscale", action="store_true",
                     help="--kernel block_gemm: B with 1x128 factors (one per output column and "
                          "K block, the block-wise wgrad)")
