@@ -25,9 +25,9 @@
 //               scale, convert, store to global memory.
 // Per-tensor kernel: BM x BN = 128 x 256, two TMEM accumulators (512
 // columns) so the epilogue of one tile overlaps the mainloop of the next.
-// Block-scaled kernel (fp32 factors): CTA pairs, 256 x 128 tiles, four TMEM
-// partial-sum buffers rotated per 128-deep K block; 8 epilogue warps per CTA
-// promote them into FP32 registers.
+// Block-scaled kernel (fp32 factors): CTA pairs, 256 x 256 tiles, two TMEM
+// partial-sum buffers rotated per 128-deep K block; 16 promotion warps per
+// CTA add them into FP32 registers.
 // Block-scaled kernel (power-of-two factors): CTA pairs, 256 x 256 tiles,
 // tcgen05.mma kind::mxf8f6f4.block_scale with the factors as UE8M0 words in
 // a TMEM ring written by four factor-writer warps.
@@ -1032,7 +1032,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
     } else {
         ptx::setmaxnreg_inc<Cfg::RPROMO>();   // each promotion warpgroup
         constexpr int CW = Cfg::CW;              // columns of this warp
-        constexpr int NCH = CW / 32;             // 32-column chunks
+        constexpr int NCH = CW / 32;             // 32-column chunks (COLSCALE factors, stores)
         const int qd = warp & 3;                 // TMEM lane quarter of this warp
         const int h = (warp - 4) >> 2;           // which CW of the tile's 128 columns
         uint8_t* slot = epi_stage + (warp - 4) * 2048;
@@ -1833,8 +1833,8 @@ int launch_block_cfg(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t
 }
 
 // Block-scaled GEMM with fp32 factors (at least one operand with 1x128 or
-// 128x128 scales; K > 0) on the CTA-pair promotion kernel: 256 x 256 tiles,
-// or 256 x 128 when B has per-column factors.
+// 128x128 scales; K > 0) on the CTA-pair promotion kernel (256 x 256 tiles),
+// with the per-column factor path when B has 1x128 scales.
 int launch_gemm_block(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
                       int64_t K, int ga, const float* sa, int gb, const float* sb,
                       const void* bias, void* D, int out, int accumulate, cudaStream_t stream) {
