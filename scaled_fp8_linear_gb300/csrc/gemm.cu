@@ -1034,7 +1034,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg::THREADS, 1)
         constexpr int CW = Cfg::CW;              // columns of this warp
         constexpr int NCH = CW / 32;             // 32-column chunks (COLSCALE factors, stores)
         const int qd = warp & 3;                 // TMEM lane quarter of this warp
-        const int h = (warp - 4) >> 2;           // which CW of the tile's 128 columns
+        const int h = (warp - 4) >> 2;           // which CW-column slice of the tile
         uint8_t* slot = epi_stage + (warp - 4) * 2048;
         // COLSCALE: the columns' factors [4 K blocks][CW], then the rows'
         // [4 K blocks][32 lanes]
