@@ -109,6 +109,51 @@ def test_random_gemms(case):
         assert_gemm_bound(D, Do, Dabs, what=f"case {case}")
 
 
+@pytest.mark.parametrize("case", range(12))
+def test_random_block_gemms(case):
+    """Random shapes (M ragged against the 256-row tiles, N against the
+    256-column tiles of the fp32-factor kernel), block-scale granularities of
+    both operands (1x128, 128x128, per tensor), fp32 or power-of-two factors,
+    and bf16 or accumulated FP32 outputs of fp8_gemm."""
+    rng = np.random.default_rng(4000 + case)
+    N, K = (128 * int(rng.integers(1, 8)) for _ in range(2))
+    ga = _pick(rng, [F.GRAN_1x128, F.GRAN_128x128, F.GRAN_TENSOR])
+    gb = _pick(rng, [F.GRAN_1x128, F.GRAN_128x128, F.GRAN_TENSOR])
+    if ga == gb == F.GRAN_TENSOR:
+        gb = F.GRAN_128x128
+    M = 128 * int(rng.integers(1, 6)) if ga == F.GRAN_128x128 else 16 * int(rng.integers(1, 40))
+    pow2 = ga != F.GRAN_TENSOR and gb != F.GRAN_TENSOR and bool(rng.integers(2))
+    fa, fb = _pick(rng, [F.E4M3, F.E5M2]), _pick(rng, [F.E4M3, F.E5M2])
+    out = _pick(rng, [F.OUT_BF16, F.OUT_F32])
+    acc = out == F.OUT_F32 and bool(rng.integers(2))
+    g = torch.Generator().manual_seed(100 + case)
+    A = torch.randint(0, 0x7C, (M, K), generator=g, dtype=torch.int32)
+    B = torch.randint(0, 0x7C, (N, K), generator=g, dtype=torch.int32)
+    A = (A | (torch.randint(0, 2, (M, K), generator=g, dtype=torch.int32) << 7)).to(torch.uint8).numpy()
+    B = (B | (torch.randint(0, 2, (N, K), generator=g, dtype=torch.int32) << 7)).to(torch.uint8).numpy()
+
+    def factors(gran, rows):
+        shape = {F.GRAN_TENSOR: (1,), F.GRAN_1x128: (rows, K // 128),
+                 F.GRAN_128x128: ((rows + 127) // 128, K // 128)}[gran]
+        if pow2:
+            return (2.0 ** rng.integers(-8, -3, size=shape)).astype(np.float32)
+        return (rng.random(shape) * 2 ** -4 + 2 ** -6).astype(np.float32)
+
+    sa, sb = factors(ga, M), factors(gb, N)
+    flag = F.SCALE_POW2 if pow2 else 0
+    prev = rng.standard_normal((M, N)).astype(np.float32)
+    D = torch.from_numpy(prev).to(DEV) if out == F.OUT_F32 else None
+    D = F.fp8_gemm(torch.from_numpy(A).to(DEV), fa, torch.from_numpy(B).to(DEV), fb,
+                   torch.from_numpy(sa).to(DEV), torch.from_numpy(sb).to(DEV), ga=ga | flag,
+                   gb=gb | flag, out=out, D=D, accumulate=acc)
+    Do, Dabs = oracle.gemm(A, fa, B, fb, sa, sb, ga, gb)
+    what = f"case {case}: {M}x{N}x{K} ga={ga} gb={gb} pow2={pow2} out={out} acc={acc}"
+    if acc:
+        assert_gemm_bound(D, Do + prev, Dabs, prev=prev, what=what)
+    else:
+        assert_gemm_bound(D, Do, Dabs, what=what)
+
+
 def _orecipe(r):
     return oracle.Recipe(scaling=r.scaling, margin=r.margin, history_len=r.history_len,
                          algo=r.amax_algo, pow2=bool(r.pow2), sr_grad=bool(r.sr_grad))
