@@ -554,6 +554,16 @@ int fp8_linear_fwd(const void* X, const void* W, const void* bias, int64_t M, in
     FP8_CHECK(check_state_scales(s));
     const int H = history_len_of(recipe);
     if (recipe->scaling == FP8_SCALING_DYNAMIC) {
+        if (!s->x_qt && !s->w_qt && M * K <= kSmallDynamicElems && N * K <= kSmallDynamicElems) {
+            // a small layer: amax, scales and casts of X and W in one launch
+            const ScaleUpd ux = dynamic_update(s, 0, recipe, s->qscale_inv + 0);
+            const ScaleUpd uw = dynamic_update(s, 1, recipe, s->qscale_inv + 1);
+            FP8_CHECK(cuda_status(launch_small_dynamic_cast(X, M * K, s->x_q, s->amax + 0, ux, W,
+                                                            N * K, s->w_q, s->amax + 1, &uw, f, st),
+                                  "amax and quantize X, W"));
+            return launch_gemm(s->x_q, f, s->w_q, f, M, N, K, FP8_GRAN_TENSOR, s->scale_inv + 0,
+                               FP8_GRAN_TENSOR, s->scale_inv + 1, bias, Y, FP8_OUT_BF16, 0, st);
+        }
         FP8_CHECK(cuda_status(launch_amax_pair(X, M * K, s->amax + 0, W, N * K, s->amax + 1, st),
                               "amax X, W"));
         if (!s->x_qt && !s->w_qt) {
@@ -623,7 +633,8 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
     // and writes the role's update itself
     const bool fused_upd = recipe->scaling == FP8_SCALING_DYNAMIC && !recipe->sr_grad && !kmajor &&
                            !fused_partial;
-    if (recipe->scaling == FP8_SCALING_DYNAMIC) {
+    const bool small = fused_upd && M * N <= kSmallDynamicElems;
+    if (recipe->scaling == FP8_SCALING_DYNAMIC && !small) {
         FP8_CHECK(cuda_status(launch_amax(dY, M * N, s->amax + 2, st), "amax dY"));
         if (!fused_upd)
             FP8_CHECK(cuda_status(launch_update_scale(s->amax + 2, h2, s->pos + 2, H,
@@ -635,7 +646,12 @@ int fp8_linear_bwd(const void* dY, int64_t M, int64_t N, int64_t K, const fp8_re
     if (recipe->sr_grad)   // "Stochastic rounding": unbiased gradient codes
         FP8_CHECK(cuda_status(launch_quantize_sr(dY, M, N, fb, s->scale + 2, 0, 0, dy_q, dy_qt,
                                                  dy_amax, st, s->sr_key), "quantize dY"));
-    else if (fused_upd) {
+    else if (small) {   // a small layer: amax, scale and cast of dY in one launch
+        const ScaleUpd u = dynamic_update(s, 2, recipe, nullptr);
+        FP8_CHECK(cuda_status(launch_small_dynamic_cast(dY, M * N, dy_q, s->amax + 2, u, nullptr,
+                                                        0, nullptr, nullptr, nullptr, fb, st),
+                              "amax and quantize dY"));
+    } else if (fused_upd) {
         const ScaleUpd u = dynamic_update(s, 2, recipe, nullptr);
         FP8_CHECK(cuda_status(launch_quantize_pair(dY, M, N, s->scale + 2, dy_q, nullptr, nullptr,
                                                    nullptr, 0, 0, nullptr, nullptr, nullptr,

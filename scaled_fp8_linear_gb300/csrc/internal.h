@@ -89,6 +89,17 @@ struct ScaleUpd {
     unsigned* status;
 };
 
+// Dynamic scaling of up to two small tensors (n0, n1 <= kSmallDynamicElems
+// elements; the second optional: upd1 null) in one launch: each tensor's
+// amax (written to amax0 / amax1), its scale and state update per the
+// ScaleUpd (whose amax field is not read), and its codes q0 / q1 -- the same
+// bits as the amax pass followed by the chunked cast with a fused update.
+constexpr int64_t kSmallDynamicElems = int64_t{1} << 20;
+cudaError_t launch_small_dynamic_cast(const void* x0, int64_t n0, uint8_t* q0, float* amax0,
+                                      const ScaleUpd& upd0, const void* x1, int64_t n1,
+                                      uint8_t* q1, float* amax1, const ScaleUpd* upd1, int fmt,
+                                      cudaStream_t stream);
+
 // Per-tensor casts of two tensors in one launch (x0 and x1 each [rows x
 // cols]), both to `fmt`: with transposes (qt0 and qt1 set; rows and cols
 // multiples of 16), or without (both null: the chunked cast, any size).

@@ -286,6 +286,13 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t ran
     return r;
 }
 
+// A 32-bit load from the cluster shared window (own or peer CTA).
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
 // Arrive on an mbarrier given by its cluster-window address (own or peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)

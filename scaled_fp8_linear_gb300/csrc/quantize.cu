@@ -346,10 +346,10 @@ __device__ __forceinline__ float scale_from_amax(float fmax, float a, int margin
     return s;
 }
 
-// The scale a cast with a fused dynamic update uses (every thread), and the
-// role's state update (the thread with `writer` set).
-__device__ __forceinline__ float fused_dynamic_scale(const ScaleUpd& u, float fmax, bool writer) {
-    const float a = *u.amax;
+// The scale a cast with a fused dynamic update uses (every thread), given the
+// role's amax a, and the role's state update (the thread with `writer` set).
+__device__ __forceinline__ float dynamic_scale_of(const ScaleUpd& u, float fmax, float a,
+                                                  bool writer) {
     const bool ok = a > 0.0f && isfinite(a);
     const float s = ok ? scale_from_amax(fmax, a, u.margin, u.pow2) : *u.scale;
     if (writer) {
@@ -363,6 +363,11 @@ __device__ __forceinline__ float fused_dynamic_scale(const ScaleUpd& u, float fm
         if (u.saved) *u.saved = *u.scale_inv;
     }
     return s;
+}
+
+// The same with the amax that an amax pass left in the role's slot.
+__device__ __forceinline__ float fused_dynamic_scale(const ScaleUpd& u, float fmax, bool writer) {
+    return dynamic_scale_of(u, fmax, *u.amax, writer);
 }
 
 // One warp per role.  history[pos] = amax; pos = (pos + 1) % H;
@@ -489,6 +494,7 @@ struct FlatJob {
 };
 
 constexpr int kChunkGroups = 4 * kThreads;   // 16-element groups per CTA
+constexpr int kSmallCtas = 8;                 // CTAs per tensor of the small-tensor cast
 
 template <int FMT, bool AMAX, bool COUNT, bool UPD>
 __global__ void __launch_bounds__(kThreads)
@@ -532,6 +538,61 @@ __global__ void __launch_bounds__(kThreads)
     }
     if (AMAX) cta_amax_commit(m, j.amax_bits);
     if (COUNT) cta_counts_commit(cc, counts);
+}
+
+// Dynamic scaling of small tensors (a small layer's X and W, or its dY):
+// the amax, the scale computed from it and the cast in one launch, one
+// cluster of kSmallCtas CTAs per tensor.  Each CTA reduces its share of the
+// maximum; the cluster combines the CTAs' maxima through distributed shared
+// memory; every thread derives the scale (the first thread of the cluster
+// also writes the role's amax slot and state update) and the CTAs cast their
+// shares.  This replaces the zeroing, amax and cast launches of the chunked
+// path with the same maximum, the same scale function and the same
+// conversion, so the codes and state are the same bits; the second read of
+// the tensor comes from L2.  Job 1 may be empty (n16 = tail_n = 0).
+template <int FMT>
+__global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kThreads)
+    small_dynamic_cast_kernel(FlatJob j0, FlatJob j1, float* amax0, float* amax1) {
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // the previous kernel's results are visible
+    __shared__ uint32_t warp_max[kThreads / 32];
+    __shared__ uint32_t cta_max;
+    const bool second = static_cast<int>(blockIdx.x) >= kSmallCtas;
+    const FlatJob& j = second ? j1 : j0;
+    float* amax_slot = second ? amax1 : amax0;
+    const int r = static_cast<int>(ptx::cluster_ctarank()), t = threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(kSmallCtas) * kThreads;
+    const int64_t g0 = static_cast<int64_t>(r) * kThreads + t;
+    uint32_t m2 = 0;
+    for (int64_t g = g0; g < j.n16; g += stride)
+        m2 = absmax_vec(absmax_vec(m2, ldg_stream(j.x + 2 * g)), ldg_stream(j.x + 2 * g + 1));
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    if (r == 0 && t < j.tail_n) m = max(m, static_cast<uint32_t>(j.xt[t] & 0x7FFFu));
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((t & 31) == 0) warp_max[t >> 5] = m;
+    __syncthreads();
+    if (t < 32) {
+        uint32_t v = t < kThreads / 32 ? warp_max[t] : 0u;
+        v = __reduce_max_sync(0xFFFFFFFFu, v);
+        if (t == 0) cta_max = v;
+    }
+    ptx::cluster_sync();   // every CTA's maximum is in its shared memory
+    uint32_t bits = 0;
+#pragma unroll
+    for (int c = 0; c < kSmallCtas; ++c)
+        bits = max(bits, ptx::ld_shared_cluster_u32(ptx::cluster_addr(&cta_max, c)));
+    ptx::cluster_sync();   // the peers' reads are done before this CTA may exit
+    const float a = __uint_as_float(bits << 16);
+    const bool writer = r == 0 && t == 0;
+    const float s = dynamic_scale_of(j.upd, Fp8Traits<FMT>::max_finite, a, writer);
+    if (writer) *amax_slot = a;
+    CastCounts cc;
+    const SrSched key{};
+    for (int64_t g = g0; g < j.n16; g += stride)
+        j.q[g] = cast16<FMT, false, false>(ldg_stream(j.x + 2 * g), ldg_stream(j.x + 2 * g + 1), s,
+                                           cc, key, 0);
+    if (r == 0 && t < j.tail_n)
+        j.qtail[t] = static_cast<uint8_t>(cvt2<FMT>(j.xt[t], s) & 0xFFu);
 }
 
 // Cast with fused transpose.  One CTA per 128 x 128 tile:
@@ -1412,6 +1473,26 @@ cudaError_t launch_quantize_tensor(const void* x, int64_t rows, int64_t cols, in
                                    float* dbias_partial) {
     return quantize_tensor<false>(x, rows, cols, fmt, scale, q, q_t, amax, counts, SrKey{},
                                   stream, dbias_partial);
+}
+
+cudaError_t launch_small_dynamic_cast(const void* x0, int64_t n0, uint8_t* q0, float* amax0,
+                                      const ScaleUpd& upd0, const void* x1, int64_t n1,
+                                      uint8_t* q1, float* amax1, const ScaleUpd* upd1, int fmt,
+                                      cudaStream_t stream) {
+    if (n0 > kSmallDynamicElems || n1 > kSmallDynamicElems || (n1 && !upd1))
+        return cudaErrorInvalidValue;
+    FlatJob f0 = flat_job(x0, n0, nullptr, q0, nullptr);
+    FlatJob f1 = flat_job(x1, n1, nullptr, q1, nullptr);
+    f0.upd = upd0;
+    if (upd1) f1.upd = *upd1;
+    const unsigned grid = static_cast<unsigned>(kSmallCtas * (upd1 ? 2 : 1));
+    if (fmt == 0)
+        launch_pdl(small_dynamic_cast_kernel<0>, dim3(grid), dim3(kThreads), 0, stream, f0, f1,
+                   amax0, amax1);
+    else
+        launch_pdl(small_dynamic_cast_kernel<1>, dim3(grid), dim3(kThreads), 0, stream, f0, f1,
+                   amax0, amax1);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_pair(const void* x0, int64_t rows0, int64_t cols0, const float* scale0,

@@ -84,6 +84,40 @@ def test_training_steps(recipe, transposes):
         dW_o = dW.cpu().numpy().astype(np.float64)   # next step accumulates onto the GPU buffer
 
 
+@pytest.mark.parametrize("M,N,K", [(1024, 1024, 1024), (1024, 1040, 1024), (1008, 1024, 1040),
+                                   (32, 64, 48)],
+                         ids=["all_at_limit", "w_and_dy_over", "x_under_w_over", "tiny"])
+def test_dynamic_small_tensor_path(M, N, K):
+    """Dynamic scaling of tensors of at most 2^20 elements takes the one-launch
+    small-tensor cast (one cluster per tensor); larger ones the amax pass and
+    the chunked cast.  Either way, at and across the limit: the codes of X, W
+    and dY, every amax, scale and history bit-exact; Y, dX, dW within the
+    bound; 3 steps, the last with an all-zero dY (its scale update skipped)."""
+    rec = F.Recipe(F.SCALING_DYNAMIC)
+    layer = F.Fp8Linear(M, N, K, rec, device=DEV)
+    orec = _orecipe(rec)
+    ost = oracle.LinearState(orec)
+    W = synthetic.normal((N, K), 0.02, seed=51)
+    dW = torch.zeros(N, K, dtype=torch.float32, device=DEV)
+    for step in range(3):
+        X = synthetic.with_outlier_channels((M, K), 1.0, 3, 40.0, seed=60 + step)
+        dY = synthetic.normal((M, N), 1e-3, seed=70 + step)
+        if step == 2:
+            dY.zero_()
+        Y = layer.forward(X.to(DEV), W.to(DEV))
+        dX, _ = layer.backward(dY.to(DEV), dW=dW)
+        Yo, Yabs = oracle.linear_fwd(bits(X), bits(W), orec, ost)
+        (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(bits(dY), orec, ost)
+        assert np.array_equal(u8(layer.x_q), ost.x_q), step
+        assert np.array_equal(u8(layer.w_q), ost.w_q), step
+        assert np.array_equal(u8(layer.workspace[:M * N]).reshape(M, N), ost.dy_q), step
+        assert np.array_equal(f32bits(layer.amax.cpu().numpy()), f32bits(ost.last_amax)), step
+        _check_state(layer, ost)
+        assert_gemm_bound(Y, Yo, Yabs, what=f"Y step {step}")
+        assert_gemm_bound(dX, dXo, dXabs, what=f"dX step {step}")
+        assert_gemm_bound(dW, dWo, dWabs, what=f"dW step {step}")
+
+
 @pytest.mark.parametrize("M,N,K,with_bias,transposes", [
     (656, 272, 400, False, False), (656, 272, 400, True, False), (272, 656, 400, False, False),
     (656, 272, 400, True, True), (48, 272, 400, True, False), (656, 48, 400, False, False)],
