@@ -581,7 +581,7 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kThreads)
 #pragma unroll
     for (int c = 0; c < kSmallCtas; ++c)
         bits = max(bits, ptx::ld_shared_cluster_u32(ptx::cluster_addr(&cta_max, c)));
-    ptx::cluster_sync();   // the peers' reads are done before this CTA may exit
+    ptx::cluster_sync_relaxed();   // the peers' reads are done before this CTA may exit
     const float a = __uint_as_float(bits << 16);
     const bool writer = r == 0 && t == 0;
     const float s = dynamic_scale_of(j.upd, Fp8Traits<FMT>::max_finite, a, writer);
