@@ -218,9 +218,11 @@ def test_cast_counters_sweep_shapes(shape, mag):
     assert tuple(counts.cpu().tolist()) == oracle.cast_counts(bits(x), F.E4M3, 1.0)
 
 
-# (4112, 2064): 33 x 17 tiles with ragged edges, more than one tile per CTA
-# of the persistent passes
-@pytest.mark.parametrize("shape", [(16, 16), (48, 400), (1024, 640), (129, 272), (4112, 2064)])
+# (4112, 2064): 33 x 17 tiles with ragged edges; (4112, 6144): 33 x 48 tiles,
+# enough for the maxima pass to take groups of 4 tiles per CTA, the last
+# group of each column ragged
+@pytest.mark.parametrize("shape", [(16, 16), (48, 400), (1024, 640), (129, 272), (4112, 2064),
+                                   (4112, 6144)])
 @pytest.mark.parametrize("fmt", [F.E4M3, F.E5M2])
 @pytest.mark.parametrize("pow2", [False, True])
 def test_row_cast_and_transposed_column_cast(shape, fmt, pow2):
