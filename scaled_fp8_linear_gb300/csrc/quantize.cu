@@ -1264,14 +1264,21 @@ __global__ void __launch_bounds__(kThreads)
             vb[it] = ldg_stream(src + 1);
         }
     }
+    // the rows' scales: lane cg (< 4) of each row group computes the scale of
+    // the group's row in iteration cg (one division sequence per thread
+    // instead of four) and the others take it by a shuffle
+    const int64_t r_own = r0 + (cg & 3) * 32 + (t >> 3);
+    const float sc_own =
+        block_scale<FMT>(__uint_as_float(r_own < rows ? rowmax[r_own] : 0u), pow2);
+    const int group = (t & 31) & ~7;   // first lane of this thread's row group
     __syncthreads();
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         const int rl = it * 32 + (t >> 3);
         const int64_t r = r0 + rl, c = c0 + cg * 16;
         const uint4 a = va[it], b = vb[it];
+        const float rs = __shfl_sync(0xFFFFFFFFu, sc_own, group + it);
         if (r < rows && c < cols) {
-            const float rs = block_scale<FMT>(__uint_as_float(rowmax[r]), pow2);
             *reinterpret_cast<uint4*>(q + r * cols + c) =
                 make_uint4(cvt4<FMT>(a.x, a.y, rs), cvt4<FMT>(a.z, a.w, rs),
                            cvt4<FMT>(b.x, b.y, rs), cvt4<FMT>(b.z, b.w, rs));
