@@ -889,18 +889,37 @@ __global__ void __launch_bounds__(kThreads)
             v[u] = valid[u] ? ldg_stream(reinterpret_cast<const uint4*>(x + off[u]))
                             : make_uint4(0u, 0u, 0u, 0u);
         }
+        // each half-warp's maxima of its kU segments; lane sub (< kU) of the
+        // half computes the scale of segment sub and writes its factor, the
+        // others take the scale by a shuffle (one division sequence per lane
+        // instead of kU)
+        uint32_t mu[kU];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const uint32_t m2 = absmax_vec(0u, v[u]);
             uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-            const float s = block_scale<FMT>(__uint_as_float(m << 16), pow2);
-            if (valid[u]) {
+            mu[u] = m;
+        }
+        uint32_t m_own = mu[0];
+        int64_t seg_own = seg[0];
+        bool valid_own = valid[0];
+#pragma unroll
+        for (int u = 1; u < kU; ++u)
+            if (sub == u) {
+                m_own = mu[u];
+                seg_own = seg[u];
+                valid_own = valid[u];
+            }
+        const float s_own = block_scale<FMT>(__uint_as_float(m_own << 16), pow2);
+        if (sub < kU && valid_own) scale_inv[seg_own] = __fdiv_rn(1.0f, s_own);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const float s = __shfl_sync(0xFFFFFFFFu, s_own, (lane & 16) + u);
+            if (valid[u])
                 *reinterpret_cast<uint2*>(q + off[u]) =
                     make_uint2(cvt4<FMT>(v[u].x, v[u].y, s), cvt4<FMT>(v[u].z, v[u].w, s));
-                if (sub == 0) scale_inv[seg[u]] = __fdiv_rn(1.0f, s);
-            }
         }
     }
 }
