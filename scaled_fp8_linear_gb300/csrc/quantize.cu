@@ -495,6 +495,7 @@ struct FlatJob {
 
 constexpr int kChunkGroups = 4 * kThreads;   // 16-element groups per CTA
 constexpr int kSmallCtas = 8;                 // CTAs per tensor of the small-tensor cast
+constexpr int kSmallThreads = 256;            // threads per CTA of the small-tensor cast
 
 template <int FMT, bool AMAX, bool COUNT, bool UPD>
 __global__ void __launch_bounds__(kThreads)
@@ -551,18 +552,18 @@ __global__ void __launch_bounds__(kThreads)
 // conversion, so the codes and state are the same bits; the second read of
 // the tensor comes from L2.  Job 1 may be empty (n16 = tail_n = 0).
 template <int FMT>
-__global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kThreads)
+__global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallThreads)
     small_dynamic_cast_kernel(FlatJob j0, FlatJob j1, float* amax0, float* amax1) {
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();   // the previous kernel's results are visible
-    __shared__ uint32_t warp_max[kThreads / 32];
+    __shared__ uint32_t warp_max[kSmallThreads / 32];
     __shared__ uint32_t cta_max;
     const bool second = static_cast<int>(blockIdx.x) >= kSmallCtas;
     const FlatJob& j = second ? j1 : j0;
     float* amax_slot = second ? amax1 : amax0;
     const int r = static_cast<int>(ptx::cluster_ctarank()), t = threadIdx.x;
-    const int64_t stride = static_cast<int64_t>(kSmallCtas) * kThreads;
-    const int64_t g0 = static_cast<int64_t>(r) * kThreads + t;
+    const int64_t stride = static_cast<int64_t>(kSmallCtas) * kSmallThreads;
+    const int64_t g0 = static_cast<int64_t>(r) * kSmallThreads + t;
     uint32_t m2 = 0;
     for (int64_t g = g0; g < j.n16; g += stride)
         m2 = absmax_vec(absmax_vec(m2, ldg_stream(j.x + 2 * g)), ldg_stream(j.x + 2 * g + 1));
@@ -572,7 +573,7 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kThreads)
     if ((t & 31) == 0) warp_max[t >> 5] = m;
     __syncthreads();
     if (t < 32) {
-        uint32_t v = t < kThreads / 32 ? warp_max[t] : 0u;
+        uint32_t v = t < kSmallThreads / 32 ? warp_max[t] : 0u;
         v = __reduce_max_sync(0xFFFFFFFFu, v);
         if (t == 0) cta_max = v;
     }
@@ -1522,10 +1523,10 @@ cudaError_t launch_small_dynamic_cast(const void* x0, int64_t n0, uint8_t* q0, f
     if (upd1) f1.upd = *upd1;
     const unsigned grid = static_cast<unsigned>(kSmallCtas * (upd1 ? 2 : 1));
     if (fmt == 0)
-        launch_pdl(small_dynamic_cast_kernel<0>, dim3(grid), dim3(kThreads), 0, stream, f0, f1,
+        launch_pdl(small_dynamic_cast_kernel<0>, dim3(grid), dim3(kSmallThreads), 0, stream, f0, f1,
                    amax0, amax1);
     else
-        launch_pdl(small_dynamic_cast_kernel<1>, dim3(grid), dim3(kThreads), 0, stream, f0, f1,
+        launch_pdl(small_dynamic_cast_kernel<1>, dim3(grid), dim3(kSmallThreads), 0, stream, f0, f1,
                    amax0, amax1);
     return cudaGetLastError();
 }
