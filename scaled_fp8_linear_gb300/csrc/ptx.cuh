@@ -279,13 +279,6 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// The same barrier without memory ordering: every thread of the cluster has
-// arrived (e.g. its reads of peer shared memory have returned), nothing more.
-__device__ __forceinline__ void cluster_sync_relaxed() {
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
-                 "barrier.cluster.wait.aligned;" ::: "memory");
-}
-
 // Address in the cluster shared window of the same variable in CTA `rank`.
 __device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
     uint32_t r;

@@ -582,7 +582,10 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallThrea
 #pragma unroll
     for (int c = 0; c < kSmallCtas; ++c)
         bits = max(bits, ptx::ld_shared_cluster_u32(ptx::cluster_addr(&cta_max, c)));
-    ptx::cluster_sync_relaxed();   // the peers' reads are done before this CTA may exit
+    // the peers' reads of this CTA's maximum have been performed before it may
+    // exit (release ordering: a load still in flight at a relaxed arrive could
+    // reach a CTA that has already left)
+    ptx::cluster_sync();
     const float a = __uint_as_float(bits << 16);
     const bool writer = r == 0 && t == 0;
     const float s = dynamic_scale_of(j.upd, Fp8Traits<FMT>::max_finite, a, writer);
