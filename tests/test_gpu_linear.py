@@ -118,6 +118,63 @@ def test_dynamic_small_tensor_path(M, N, K):
         assert_gemm_bound(dW, dWo, dWabs, what=f"dW step {step}")
 
 
+@pytest.mark.parametrize("M,N,K,with_bias,fmt", [
+    (256, 512, 512, False, F.E4M3), (128, 128, 128, True, F.E4M3), (1024, 128, 768, False, F.E4M3),
+    (112, 1024, 64, True, F.E4M3), (208, 400, 336, True, F.E5M2), (16, 16, 16, False, F.E5M2)],
+    ids=["small_case_2x4_tiles", "one_tile_bias", "8x1_tiles_k768", "1x8_tiles_ragged_m_bias",
+         "ragged_k336_bias_e5m2", "smallest_e5m2"])
+def test_dynamic_small_forward_shapes(M, N, K, with_bias, fmt):
+    """Small dynamic forwards (the one-launch small-tensor cast, then the
+    GEMM) over 1 to 8 output tiles, ragged M, N and K, with and without bias,
+    E4M3 and E5M2 forward operands.  Over 3 steps, the last with an all-zero
+    X (its scale update skipped): the codes of X and W (which the backward
+    reads), every amax, scale and history bit-exact against the oracle; Y
+    within the bound.  With E4M3 forward operands the backward after each
+    forward stays in parity too."""
+    rec = F.Recipe(F.SCALING_DYNAMIC, fwd_format=fmt)
+    layer = F.Fp8Linear(M, N, K, rec, device=DEV)
+    W = synthetic.normal((N, K), 0.02, seed=81)
+    b = synthetic.normal((N,), 0.1, seed=82) if with_bias else None
+    hybrid = fmt == F.E4M3
+    orec = _orecipe(rec)
+    ost = oracle.LinearState(orec)
+    rx, rw = oracle.ScaleState(1), oracle.ScaleState(1)
+    dW = torch.zeros(N, K, dtype=torch.float32, device=DEV)
+    for step in range(3):
+        X = synthetic.with_outlier_entries((M, K), 1.0, 0.001, 50.0, seed=90 + step)
+        if step == 2:
+            X.zero_()
+        Y = layer.forward(X.to(DEV), W.to(DEV), bias=b.to(DEV) if with_bias else None)
+        ax, aw = oracle.amax(bits(X)), oracle.amax(bits(W))
+        if hybrid:
+            Yo, Yabs = oracle.linear_fwd(bits(X), bits(W), orec, ost,
+                                         bias=bits(b) if with_bias else None)
+            xq, wq = ost.x_q, ost.w_q
+            _check_state(layer, ost, roles=(0, 1))
+        else:
+            oracle.update_scale(rx, ax, oracle.ALGO_MOST_RECENT, fmt)
+            oracle.update_scale(rw, aw, oracle.ALGO_MOST_RECENT, fmt)
+            xq, _ = oracle.quantize(bits(X), fmt, rx.scale[0])
+            wq, _ = oracle.quantize(bits(W), fmt, rw.scale[0])
+            Yo, Yabs = oracle.gemm(xq, fmt, wq, fmt, rx.scale_inv, rw.scale_inv,
+                                   bias=bits(b) if with_bias else None)
+            for r, rs in ((0, rx), (1, rw)):
+                assert f32bits(layer.scale[r].cpu().numpy()) == f32bits(rs.scale[0]), (step, r)
+                assert f32bits(layer.scale_inv[r].cpu().numpy()) == f32bits(rs.scale_inv[0]), (step, r)
+                assert np.array_equal(f32bits(layer.history[r].cpu().numpy()), f32bits(rs.history))
+        assert np.array_equal(u8(layer.x_q), xq), step
+        assert np.array_equal(u8(layer.w_q), wq), step
+        am = layer.amax.cpu().numpy()
+        assert f32bits(am[0]) == f32bits(np.float32(ax)) and f32bits(am[1]) == f32bits(np.float32(aw))
+        assert_gemm_bound(Y, Yo, Yabs, what=f"Y step {step}")
+        if hybrid:
+            dY = synthetic.normal((M, N), 1e-3, seed=95 + step)
+            dX, _ = layer.backward(dY.to(DEV), dW=dW)
+            (dXo, dXabs), (dWo, dWabs) = oracle.linear_bwd(bits(dY), orec, ost)
+            assert_gemm_bound(dX, dXo, dXabs, what=f"dX step {step}")
+            assert_gemm_bound(dW, dWo, dWabs, what=f"dW step {step}")
+
+
 @pytest.mark.parametrize("M,N,K,with_bias,transposes", [
     (656, 272, 400, False, False), (656, 272, 400, True, False), (272, 656, 400, False, False),
     (656, 272, 400, True, True), (48, 272, 400, True, False), (656, 48, 400, False, False)],
