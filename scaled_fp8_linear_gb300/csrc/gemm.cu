@@ -132,7 +132,11 @@ struct Layout {
 
 // Producer role: stream the A / B tiles of every K block of every tile of
 // this CTA through the ring.  On exit, waits for its own copies in flight.
-template <int BN, int STAGES, int GROUP = 8>
+// Raster group of the single-CTA kernel: its producer and its epilogue must
+// walk the tiles in the same order.
+constexpr int kTensorGroup = 8;
+
+template <int BN, int STAGES, int GROUP>
 __device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t* ring,
                          uint64_t* full, uint64_t* empty, const GemmParams& p,
                          volatile uint32_t* abort_flag) {
@@ -403,7 +407,7 @@ __global__ void __launch_bounds__(256, 1)
     const int num_tiles = p.num_m * p.num_n;
 
     if (warp == 0) {
-        if (lane == 0) producer<BN, STAGES>(&tmA, &tmB, ring, full, empty, p, abort_flag);
+        if (lane == 0) producer<BN, STAGES, kTensorGroup>(&tmA, &tmB, ring, full, empty, p, abort_flag);
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = ptx::idesc_f8f6f4(p.fa, p.fb, BM, BN);
@@ -444,7 +448,7 @@ __global__ void __launch_bounds__(256, 1)
         const uint64_t wait_ns = g_epilogue_wait_ns;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             int m_blk, n_blk;
-            tile_coords<>(tile, p.num_m, p.num_n, m_blk, n_blk);
+            tile_coords<kTensorGroup>(tile, p.num_m, p.num_n, m_blk, n_blk);   // as the producer
             if (rmw)
                 prefetch_row(static_cast<int64_t>(m_blk) * BM + row, static_cast<int64_t>(n_blk) * BN,
                              BN, p);

@@ -86,6 +86,27 @@ def test_exact_integer_products(M, N, K):
     assert np.array_equal(D.cpu().numpy().astype(np.float64), want)
 
 
+@pytest.mark.parametrize("M,N,K", [(2048, 256, 256), (1152, 512, 128), (4864, 128, 64),
+                                   (128, 4864, 64), (1040, 1040, 96)])
+def test_one_wave_tile_order(M, N, K):
+    """Problems whose 128 x 128 tiles fit in one wave run on the single-CTA
+    kernel with 128-column tiles, many tiles along M or N: every tile lands
+    where its operand rows came from.  Small-integer codes make the FP32
+    result exact, so a tile written to another tile's place cannot pass."""
+    rng = np.random.default_rng(M + N + K)
+    ai = rng.integers(-4, 5, size=(M, K)).astype(np.float32)
+    bi = rng.integers(-4, 5, size=(N, K)).astype(np.float32)
+    A = oracle.encode(ai, F.E4M3)
+    B = oracle.encode(bi, F.E4M3)
+    want = (ai.astype(np.int64) @ bi.astype(np.int64).T).astype(np.float64) * 0.25
+    D = F.fp8_gemm(_t(A), F.E4M3, _t(B), F.E4M3, _s(0.5), _s(0.5), out=F.OUT_F32)
+    assert np.array_equal(D.cpu().numpy().astype(np.float64), want)
+    # bf16 output: the exact product rounded once (torch's cast rounds to nearest even)
+    Db = F.fp8_gemm(_t(A), F.E4M3, _t(B), F.E4M3, _s(0.5), _s(0.5))
+    wb = torch.from_numpy(want.astype(np.float32)).bfloat16()
+    assert torch.equal(Db.cpu().view(torch.int16), wb.view(torch.int16))
+
+
 def test_degenerate_shapes():
     A = torch.zeros(0, 64, dtype=torch.uint8, device=DEV)
     B = torch.zeros(32, 64, dtype=torch.uint8, device=DEV)
