@@ -322,7 +322,10 @@ size_t fp8_workspace_size(int64_t M, int64_t N, int64_t K, const fp8_recipe_t* r
  *            w_sinv_t) for the backward pass, which needs M % 128 == 0.
  * Writes state->x_q/x_qt/w_q/w_qt (and the block scale arrays) for the
  * backward pass.  Shape rule: M, N, K multiples of 16 (N, K multiples of 128
- * for block). */
+ * for block).  M = 0 (a batch without tokens, e.g. an expert that received
+ * none) is a valid call: X, Y and the state's M-sized arrays (x_q, x_qt,
+ * x_sinv) may then be NULL; W is cast and the scaling state advances as for
+ * any batch, with an amax of 0 for X (so its scale update is skipped). */
 int fp8_linear_fwd(const void* X, const void* W, const void* bias, int64_t M, int64_t N,
                    int64_t K, const fp8_recipe_t* recipe, const fp8_linear_state_t* state,
                    void* Y, void* workspace, size_t workspace_bytes, void* stream);
@@ -338,6 +341,10 @@ int fp8_linear_fwd(const void* X, const void* W, const void* bias, int64_t M, in
  *   w_q and dY_q as stored (FP8_LAYOUT_B_KN for dgrad, FP8_LAYOUT_KM_KN for
  *   wgrad) and no transposed copy is made.  Both give the same codes and
  *   the same GEMM results.
+ * M = 0 (no tokens): dY and dX may be NULL (so may the forward's M-sized
+ *   arrays); dY's amax is 0 (its scale update is skipped), dW and dbias are
+ *   set to zero, or left as they are with accumulate_dW, and the workspace
+ *   may be NULL when fp8_workspace_size gives 0.
  * Block scaling ("DeepSeek FP8 training recipe" > "Block-wise scaling at
  *   128 granularity"): dY is cast once into 1x128 blocks along N (dgrad
  *   operand) and 1x128 blocks along the tokens of dY^T (wgrad operand);

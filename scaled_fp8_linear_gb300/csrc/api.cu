@@ -278,8 +278,8 @@ cudaError_t quantize_x_w(const void* X, const void* W, int64_t M, int64_t N, int
 int check_bwd_workspace(int64_t M, int64_t N, const fp8_recipe_t* recipe,
                         const fp8_linear_state_t* s, const float* dbias, const void* workspace,
                         size_t workspace_bytes) {
-    if (!workspace) return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: NULL pointer");
     const size_t need = bwd_operand_bytes(M, N, recipe, s) + (dbias ? dbias_partial_bytes(M, N) : 0);
+    if (!workspace && need) return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: NULL pointer");
     if (workspace_bytes < need)
         return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: workspace of %zu bytes, %zu needed",
                          workspace_bytes, need);
@@ -358,11 +358,13 @@ int check_linear_bwd_args(const void* dY, int64_t M, int64_t N, int64_t K,
                           const float* dW, const float* dbias) {
     FP8_CHECK(check_recipe(recipe));
     FP8_CHECK(check_linear_shape(M, N, K, recipe));
-    if (!dY || !dX || !dW || !s)
+    // M = 0: dY, dX and the forward's M-sized operands may be NULL; dW (and
+    // dbias) are written (zero) or, with accumulate_dW, left as they are
+    if ((!dY && M) || (!dX && M) || !dW || !s)
         return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: NULL pointer");
     const bool block = recipe->scaling == FP8_SCALING_BLOCK;
     if (block || recipe->scaling == FP8_SCALING_ROW) {
-        if (!s->x_qt || !s->w_qt || !s->x_sinv_t || !s->w_sinv_t)
+        if (M && (!s->x_qt || !s->w_qt || !s->x_sinv_t || !s->w_sinv_t))
             return set_error(FP8_ERR_INVALID_ARG,
                              "fp8_linear_bwd: %s mode needs the forward's x_qt/x_sinv_t and w_qt/w_sinv_t",
                              block ? "block" : "per-row");
@@ -370,7 +372,7 @@ int check_linear_bwd_args(const void* dY, int64_t M, int64_t N, int64_t K,
             return set_error(FP8_ERR_SHAPE, "fp8_linear_bwd: block mode needs M multiple of 128");
     } else {
         FP8_CHECK(check_state_scales(s));
-        if (!s->x_q || !s->w_q)
+        if ((!s->x_q && M) || !s->w_q)
             return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_bwd: state->x_q / w_q must be set");
         if (recipe->sr_grad && (!s->sr_key || (reinterpret_cast<uintptr_t>(s->sr_key) & 7u)))
             return set_error(FP8_ERR_INVALID_ARG,
@@ -504,8 +506,12 @@ int fp8_linear_fwd(const void* X, const void* W, const void* bias, int64_t M, in
     (void)workspace_bytes;
     FP8_CHECK(check_recipe(recipe));
     FP8_CHECK(check_linear_shape(M, N, K, recipe));
-    if (!X || !W || !Y || !s) return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_fwd: NULL pointer");
-    if (!s->x_q || !s->w_q) return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_fwd: state->x_q / w_q must be set");
+    // M = 0 (a batch without tokens): the M-sized buffers X, Y, x_q, x_qt and
+    // x_sinv may be NULL
+    if ((!X && M) || !W || (!Y && M) || !s)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_fwd: NULL pointer");
+    if ((!s->x_q && M) || !s->w_q)
+        return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_fwd: state->x_q / w_q must be set");
     if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(s->x_q) || !aligned16(s->w_q) ||
         (bias && !aligned16(bias)) ||
         (s->x_qt && !aligned16(s->x_qt)) || (s->w_qt && !aligned16(s->w_qt)))
@@ -516,7 +522,7 @@ int fp8_linear_fwd(const void* X, const void* W, const void* bias, int64_t M, in
     if (recipe->scaling == FP8_SCALING_ROW) {
         // per-token X, per-output-channel W; with x_qt and w_qt kept (training)
         // the same launches also cast X^T and W^T per row (per column of X, W)
-        if (!s->x_sinv || !s->w_sinv)
+        if ((!s->x_sinv && M) || !s->w_sinv)
             return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_fwd: per-row mode needs x_sinv and w_sinv");
         const bool keep = s->x_qt && s->w_qt;
         if (keep && (!s->x_sinv_t || !s->w_sinv_t))
@@ -532,7 +538,7 @@ int fp8_linear_fwd(const void* X, const void* W, const void* bias, int64_t M, in
     }
 
     if (recipe->scaling == FP8_SCALING_BLOCK) {
-        if (!s->x_sinv || !s->w_sinv)
+        if ((!s->x_sinv && M) || !s->w_sinv)
             return set_error(FP8_ERR_INVALID_ARG, "fp8_linear_fwd: block mode needs x_sinv and w_sinv");
         // training (x_qt and w_qt kept): the same casts also write the backward operands
         const bool keep = s->x_qt && s->w_qt;

@@ -175,6 +175,52 @@ def test_dynamic_small_forward_shapes(M, N, K, with_bias, fmt):
             assert_gemm_bound(dW, dWo, dWabs, what=f"dW step {step}")
 
 
+@pytest.mark.parametrize("recipe,transposes", [
+    (F.Recipe(F.SCALING_DYNAMIC), False), (F.Recipe(F.SCALING_DYNAMIC), True),
+    (F.Recipe(F.SCALING_DELAYED, history_len=4), False),
+    (F.Recipe(F.SCALING_DYNAMIC, sr_grad=True), False),
+    (F.Recipe(F.SCALING_BLOCK), False), (F.Recipe(F.SCALING_ROW), False)],
+    ids=["dynamic", "dynamic_transposed_copies", "delayed4", "dynamic_sr_grad", "block", "row"])
+def test_empty_token_batch(recipe, transposes):
+    """A batch without tokens (M = 0: an expert that received none): X, Y, dY
+    and dX are empty (NULL pointers), the forward still casts W, the scaling
+    state advances as the oracle's does (X's and dY's amax are 0, so their
+    scale updates are skipped), dW and dbias come out zero, and with
+    accumulation stay as they were; over 2 steps, no device error."""
+    M, N, K = 0, 384, 256
+    layer = F.Fp8Linear(M, N, K, recipe, device=DEV, transposes=transposes)
+    orec = oracle.Recipe(scaling=recipe.scaling, margin=recipe.margin,
+                         history_len=recipe.history_len, algo=recipe.amax_algo,
+                         pow2=bool(recipe.pow2), sr_grad=bool(recipe.sr_grad))
+    ost = oracle.LinearState(orec)
+    per_tensor = recipe.scaling in (F.SCALING_DELAYED, F.SCALING_DYNAMIC)
+    W = synthetic.normal((N, K), 0.02, seed=5)
+    X = torch.empty(M, K, dtype=torch.bfloat16)
+    dY = torch.empty(M, N, dtype=torch.bfloat16)
+    dW = torch.full((N, K), 3.0, dtype=torch.float32, device=DEV)
+    db = torch.full((N,), 2.0, dtype=torch.float32, device=DEV)
+    for step in range(2):
+        acc = step > 0
+        prev_w, prev_b = dW.clone(), db.clone()
+        Y = layer.forward(X.to(DEV), W.to(DEV))
+        dX, _ = layer.backward(dY.to(DEV), dW=dW, dbias=db, accumulate_dW=acc)
+        torch.cuda.synchronize()
+        assert Y.shape == (0, N) and dX.shape == (0, K)
+        oracle.linear_fwd(bits(X), bits(W), orec, ost)
+        oracle.linear_bwd(bits(dY), orec, ost)
+        assert np.array_equal(u8(layer.w_q), ost.w_q), step
+        if per_tensor:
+            _check_state(layer, ost)
+            assert np.array_equal(f32bits(layer.amax.cpu().numpy()), f32bits(ost.last_amax)), step
+        else:
+            assert np.array_equal(f32bits(layer.w_sinv.cpu().numpy().reshape(-1)),
+                                  f32bits(np.asarray(ost.w_sinv).reshape(-1))), step
+        if acc:
+            assert torch.equal(dW, prev_w) and torch.equal(db, prev_b), step
+        else:
+            assert not torch.any(dW) and not torch.any(db), step
+
+
 @pytest.mark.parametrize("M,N,K,with_bias,transposes", [
     (656, 272, 400, False, False), (656, 272, 400, True, False), (272, 656, 400, False, False),
     (656, 272, 400, True, True), (48, 272, 400, True, False), (656, 48, 400, False, False)],
