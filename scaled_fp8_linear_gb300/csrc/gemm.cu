@@ -763,8 +763,8 @@ __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
 // takes 64 registers a thread, so the role warpgroup gives registers back
 // with setmaxnreg (32 a thread) and the promotion warps take them (112):
 // 4 x 32 x 32 + 16 x 32 x 112 = 61440 = 640 threads x the 96 registers of
-// the launch.  Measured against the alternatives (CUDA events, the C3
-// shapes): one 32-column TMEM load at a time (two in flight need 64 more
+// the launch.  Measured against the alternatives (CUDA events, 16384 x
+// 18432 x 7168 and 16384 x 7168 x 18432): one 32-column TMEM load at a time (two in flight need 64 more
 // registers and spill; 16-column loads were 11% slower); three operand
 // stages (four and five were 1.5% and about 5% slower: shared memory comes
 // out of L1, where 97% of the promotion warps' factor reads hit); factors
