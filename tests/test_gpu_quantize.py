@@ -164,6 +164,38 @@ def test_quantizer_sweep_shapes(log2n, width, mag, fmt):
     assert np.array_equal(u8(q2), oracle.quantize(bx, fmt, st.scale[0])[0])
 
 
+@pytest.mark.parametrize("log2n", [28, 30])
+@pytest.mark.parametrize("fmt", [F.E4M3, F.E5M2])
+def test_quantizer_full_size_sampled(log2n, fmt):
+    """The quantizer sweep's largest tensors, [n/8192 x 8192] t_3 values,
+    drawn on the device as the bench draws them: the fused amax bit-exact
+    over the whole tensor, and 16 seeded rows of q and 16 of q^T (columns
+    of x) bit-exact against the oracle's cast of the same rows and columns,
+    with the sweep's stale scale 1 and with the dynamic scale that the
+    oracle derives from the amax."""
+    width = 8192
+    rows = (1 << log2n) // width
+    xd = synthetic.student_t((rows, width), 3, 1.0, seed=log2n, device=torch.device(DEV))
+    bx = bits(xd.cpu())
+    ao = oracle.amax(bx)
+    rng = np.random.default_rng(log2n + fmt)
+    ri = np.sort(rng.choice(rows, 16, replace=False))
+    ci = np.sort(rng.choice(width, 16, replace=False))
+    st = oracle.ScaleState(1)
+    oracle.update_scale(st, ao, oracle.ALGO_MOST_RECENT, fmt)
+    for s in (np.float32(1.0), st.scale[0]):
+        sd = torch.tensor([s], dtype=torch.float32, device=DEV)
+        q, qt, _, am = F.fp8_quantize(xd, fmt, scale=sd, transpose=True, want_amax=True)
+        torch.cuda.synchronize()
+        assert f32bits(am.item()) == f32bits(ao)
+        assert np.array_equal(u8(q[torch.as_tensor(ri, device=DEV)]), oracle.quantize(bx[ri], fmt, s)[0])
+        cols = np.ascontiguousarray(bx[:, ci].T)
+        assert np.array_equal(u8(qt[torch.as_tensor(ci, device=DEV)]), oracle.quantize(cols, fmt, s)[0])
+        del q, qt
+    del xd
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("shape", [(128, 128), (384, 256), (1024, 640)])
 @pytest.mark.parametrize("fmt", [F.E4M3, F.E5M2])
 @pytest.mark.parametrize("pow2", [False, True])
