@@ -196,6 +196,44 @@ def test_quantizer_full_size_sampled(log2n, fmt):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("gran", [F.GRAN_1x128, F.GRAN_128x128, F.GRAN_ROW],
+                         ids=["dual_1x128", "128x128", "row"])
+@pytest.mark.parametrize("fmt", [F.E4M3, F.E5M2])
+def test_recipe_casts_full_size_sampled(gran, fmt):
+    """The other recipes' casts with their transposed outputs at the size the
+    bench times them (16384 x 7168, per-row heavy-tailed values drawn on the
+    device as the bench draws them): seeded sampled rows of q with their
+    scales, and sampled rows of q^T (columns of x, whose scales need the
+    whole column) with theirs, bit-exact against the oracle's cast of the
+    same rows and columns; for 128 x 128 blocks, two sampled 128-row bands."""
+    R, C = 16384, 7168
+    xd = synthetic.student_t_rows((R, C), 1.0, 3, seed=7, device=torch.device(DEV))
+    bx = bits(xd.cpu())
+    q, sc, qt, st = F.fp8_quantize_blocks(xd, fmt, gran, transpose=True)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(gran * 2 + fmt)
+    ri = np.sort(rng.choice(R, 16, replace=False))
+    ci = np.sort(rng.choice(C, 16, replace=False))
+    take = lambda t, idx: t[torch.as_tensor(idx, device=DEV)]
+    if gran == F.GRAN_128x128:
+        for band in np.sort(rng.choice(R // 128, 2, replace=False)):
+            rows = slice(128 * band, 128 * band + 128)
+            qo, so = oracle.block_quantize(bx[rows], fmt, 128)
+            assert np.array_equal(u8(q[rows]), qo)
+            assert np.array_equal(f32bits(sc[band].cpu().numpy()), f32bits(so[0]))
+            assert np.array_equal(u8(qt[:, rows]), qo.T)
+            assert np.array_equal(f32bits(st[:, band].cpu().numpy()), f32bits(so[0]))
+        return
+    cast = (lambda a: oracle.block_quantize(a, fmt, 1)) if gran == F.GRAN_1x128 else \
+        (lambda a: oracle.row_quantize(a, fmt))
+    qo, so = cast(bx[ri])
+    assert np.array_equal(u8(take(q, ri)), qo)
+    assert np.array_equal(f32bits(take(sc, ri).cpu().numpy()), f32bits(so))
+    qto, sto = cast(np.ascontiguousarray(bx[:, ci].T))
+    assert np.array_equal(u8(take(qt, ci)), qto)
+    assert np.array_equal(f32bits(take(st, ci).cpu().numpy()), f32bits(sto))
+
+
 @pytest.mark.parametrize("shape", [(128, 128), (384, 256), (1024, 640)])
 @pytest.mark.parametrize("fmt", [F.E4M3, F.E5M2])
 @pytest.mark.parametrize("pow2", [False, True])
