@@ -278,9 +278,11 @@ def test_cast_counters_every_bf16_pattern(fmt, scale, transpose):
     assert tuple(counts.cpu().tolist()) == tuple(2 * c for c in oracle.cast_counts(bits(x), fmt, scale))
 
 
-@pytest.mark.parametrize("shape,mag", [((4096, 4096), 1e2), ((4096, 4096), 1e-2), ((37, 61), 30.0)])
+@pytest.mark.parametrize("shape,mag", [((4096, 4096), 1e2), ((4096, 4096), 1e-2), ((37, 61), 30.0),
+                                       ((16384, 8192), 1e2), ((16384, 8192), 1e-2)])
 def test_cast_counters_sweep_shapes(shape, mag):
-    """Stale scale 1 on heavy-tailed data: x1e2 saturates, x1e-2 underflows."""
+    """Stale scale 1 on heavy-tailed data: x1e2 saturates, x1e-2 underflows;
+    the last two at the size the bench times the counted cast."""
     x = synthetic.student_t(shape, 3, mag, seed=shape[0] + int(mag))
     one = torch.ones(1, dtype=torch.float32, device=DEV)
     tr = shape[0] % 16 == 0 and shape[1] % 16 == 0
