@@ -494,7 +494,10 @@ struct FlatJob {
 };
 
 constexpr int kChunkGroups = 4 * kThreads;   // 16-element groups per CTA
-constexpr int kSmallCtas = 8;                 // CTAs per tensor of the small-tensor cast
+// CTAs per tensor of the small-tensor cast: one cluster of 16 (a size
+// beyond the portable 8, allowed per kernel; 6% less latency than 8 on a
+// small layer's forward replayed from a CUDA graph)
+constexpr int kSmallCtas = 16;
 constexpr int kSmallThreads = 256;            // threads per CTA of the small-tensor cast
 
 template <int FMT, bool AMAX, bool COUNT, bool UPD>
@@ -1525,6 +1528,24 @@ cudaError_t launch_small_dynamic_cast(const void* x0, int64_t n0, uint8_t* q0, f
     f0.upd = upd0;
     if (upd1) f1.upd = *upd1;
     const unsigned grid = static_cast<unsigned>(kSmallCtas * (upd1 ? 2 : 1));
+    {
+        // clusters beyond 8 CTAs are allowed per kernel, once per device
+        static std::mutex mu;
+        static bool done[64] = {};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+        const bool cached = dev >= 0 && dev < 64;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!cached || !done[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(small_dynamic_cast_kernel<0>,
+                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(small_dynamic_cast_kernel<1>,
+                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+            if (cached) done[dev] = true;
+        }
+    }
     if (fmt == 0)
         launch_pdl(small_dynamic_cast_kernel<0>, dim3(grid), dim3(kSmallThreads), 0, stream, f0, f1,
                    amax0, amax1);
