@@ -149,8 +149,15 @@ def _check(status: int) -> None:
         raise Fp8Error(status, fp8_last_error())
 
 
+# The current stream's handle without building a torch.cuda.Stream object
+# (about 0.1 us against 3 us a call); the public call where it is missing.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> int:
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
