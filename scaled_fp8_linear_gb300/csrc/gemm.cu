@@ -1673,9 +1673,9 @@ int make_store_map(CUtensorMap* map, void* ptr, int64_t M, int64_t N, int out) {
 }
 
 constexpr int kTensorBN = 256, kTensorStages = 4;
-// Column tile of the single-CTA kernel for problems whose 128 x 128 tiles
-// fit in one wave.
-constexpr int kSmallBN = 128;
+// Column tiles of the single-CTA kernel for problems whose 128-row tiles fit
+// in one wave: 64 columns where those fit, else 128.
+constexpr int kSmallBN = 128, kTinyBN = 64;
 constexpr int kPairStages = 6;
 constexpr int kPairSmemBytes = kPairStages * 2 * 128 * BK + 4 * 2048 + 256 + 1024;
 // Problems with at least this many rows use the CTA-pair kernel.
@@ -1891,14 +1891,18 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
     // per-tensor and per-row scales: CTA pairs for every problem of at least
     // 256 rows, and for every MN-major operand (the single-CTA kernel reads
     // K-major tiles only; rows past M are zero-filled and not stored).  A
-    // K-major problem whose 128 x 128 tiles fit in one wave (at most one per
-    // SM) takes the single-CTA kernel with 128-column tiles instead: four
-    // CTAs per 256 x 256 pair tile, each with a quarter of its MMAs and
-    // epilogue (a small layer's forward GEMM, where latency is the cost)
-    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-    const bool one_wave = !a_mn && !b_mn && 4 * pair_tiles <= num_sms();
-    const bool pair = (M >= kPairMinRows && !one_wave) || a_mn || b_mn;
-    const int BN = one_wave ? kSmallBN : kTensorBN;
+    // K-major problem whose 128 x 64 tiles (else 128 x 128 tiles) fit in one
+    // wave (at most one per SM) takes the single-CTA kernel with those tiles
+    // instead: eight (four) CTAs per 256 x 256 pair tile, each with an eighth
+    // (a quarter) of its MMAs and epilogue -- a small layer's forward GEMM,
+    // where latency is the cost
+    const int64_t sms = num_sms(), row_tiles = (M + BM - 1) / BM;
+    const int one_wave_bn = (a_mn || b_mn) ? 0
+                            : row_tiles * ((N + kTinyBN - 1) / kTinyBN) <= sms ? kTinyBN
+                            : row_tiles * ((N + kSmallBN - 1) / kSmallBN) <= sms ? kSmallBN
+                                                                                 : 0;
+    const bool pair = (M >= kPairMinRows && !one_wave_bn) || a_mn || b_mn;
+    const int BN = one_wave_bn ? one_wave_bn : kTensorBN;
     const int TM = pair ? 256 : BM;   // rows of C per tile
     GemmParams p;
     p.M = M; p.N = N; p.K = K;
@@ -1929,6 +1933,11 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
         const int pgrid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
         GemmParams none{};
         launch_pdl(k, dim3(pgrid), dim3(256), kPairSmemBytes, stream, tmA, tmB, tmD, p, tmA, tmB, tmD, none);
+    } else if (BN == kTinyBN) {
+        using L = Layout<kTinyBN, kTensorStages>;
+        auto k = gemm_tensor_kernel<kTinyBN, kTensorStages>;
+        if ((st = ensure_smem(k, L::SMEM_BYTES, 7)) != FP8_OK) return st;
+        launch_pdl(k, dim3(grid), dim3(256), L::SMEM_BYTES, stream, tmA, tmB, p);
     } else if (BN == kSmallBN) {
         using L = Layout<kSmallBN, kTensorStages>;
         auto k = gemm_tensor_kernel<kSmallBN, kTensorStages>;

@@ -90,12 +90,14 @@ def test_exact_integer_products(M, N, K):
                                    (128, 4864, 64), (1040, 1040, 96), (4864, 512, 64),
                                    (5120, 512, 64)])
 def test_one_wave_tile_order(M, N, K):
-    """Problems whose 128 x 128 tiles fit in one wave run on the single-CTA
-    kernel with 128-column tiles, many tiles along M or N: every tile lands
-    where its operand rows came from.  Small-integer codes make the FP32
-    result exact, so a tile written to another tile's place cannot pass.
-    The last two shapes lie just inside (152 tiles) and just outside (160)
-    one wave of a 152-SM GPU, so both kernels run at the boundary."""
+    """Problems whose 128 x 64 (else 128 x 128) tiles fit in one wave run on
+    the single-CTA kernel with those tiles, many tiles along M or N: every
+    tile lands where its operand rows came from.  Small-integer codes make
+    the FP32 result exact, so a tile written to another tile's place cannot
+    pass.  On a 152-SM GPU the first four shapes take 64-column tiles, the
+    next two 128-column tiles (1040 x 1040 just past one wave of 64-column
+    ones, 4864 x 512 exactly one wave of 128-column ones) and the last the
+    CTA pairs (160 tiles of 128 x 128), so every kernel runs at a boundary."""
     rng = np.random.default_rng(M + N + K)
     ai = rng.integers(-4, 5, size=(M, K)).astype(np.float32)
     bi = rng.integers(-4, 5, size=(N, K)).astype(np.float32)
