@@ -76,7 +76,7 @@ struct GemmParams {
     void* D;
     int out;          // FP8_OUT_BF16 / FP8_OUT_F32
     int accumulate;
-    int a_mn, b_mn;   // operand stored MN-major ([K x M] / [K x N]); CTA-pair kernel only
+    int a_mn, b_mn;   // operand stored MN-major ([K x M] / [K x N]); CTA pairs, or 128 x 128 single-CTA tiles
     int group;        // CTA-pair kernel: raster group (M-blocks), see pair_group()
 };
 
@@ -130,42 +130,9 @@ struct Layout {
     static constexpr int SMEM_BYTES = RING_BYTES + BAR_BYTES + 1024;  // + alignment slack
 };
 
-// Producer role: stream the A / B tiles of every K block of every tile of
-// this CTA through the ring.  On exit, waits for its own copies in flight.
-// Raster group of the single-CTA kernel: its producer and its epilogue must
-// walk the tiles in the same order.
+// Raster group of the single-CTA kernel: its producer and its epilogue walk
+// the tiles in the same order.
 constexpr int kTensorGroup = 8;
-
-template <int BN, int STAGES, int GROUP>
-__device__ void producer(const CUtensorMap* tmA, const CUtensorMap* tmB, uint8_t* ring,
-                         uint64_t* full, uint64_t* empty, const GemmParams& p,
-                         volatile uint32_t* abort_flag) {
-    using L = Layout<BN, STAGES>;
-    const int num_tiles = p.num_m * p.num_n;
-    uint32_t stage = 0, phase = 0;
-    int64_t issued = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        int m_blk, n_blk;
-        tile_coords<GROUP>(tile, p.num_m, p.num_n, m_blk, n_blk);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-            if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
-            uint8_t* sa = ring + stage * L::STAGE_BYTES;
-            ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
-            ptx::tma_load_2d(sa, tmA, &full[stage], kb * BK, m_blk * BM);
-            ptx::tma_load_2d(sa + L::A_BYTES, tmB, &full[stage], kb * BK, n_blk * BN);
-            ++issued;
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
-    }
-    // drain: the last copy issued into each slot must have landed
-    uint32_t never = 0;
-    for (int s = 0; s < STAGES; ++s) {
-        if (issued <= s && issued < STAGES) break;
-        const uint32_t par = (static_cast<uint32_t>(s) < stage) ? phase : (phase ^ 1u);
-        ptx::mbar_wait(&full[s], par, &never);
-    }
-}
 
 // Dequantisation factors of one 32-column chunk, f[j] = fp32(fa * sb(n0 + j)):
 // fa is the thread's row factor (sa[m] for per-row A, else sa[0]); sb is per
@@ -359,10 +326,18 @@ __device__ __forceinline__ void emit_bf16_chunk(uint8_t* slot, const uint32_t (&
 
 // --------------------------------------------------------- per-tensor kernel
 
-template <int BN, int STAGES>
+// Single-CTA kernel: 128 x BN tiles, one or (GROUPED) two problems in one
+// launch -- the units are the tiles of p, then those of p2, dealt
+// round-robin to the CTAs.  An operand is read K-major or (a_mn / b_mn, only
+// with BN = 128) MN-major, as the CTA-pair kernel reads it: boxes of
+// (128 K bytes, rows) or (128 M/N elements, 128 k).
+template <int BN, int STAGES, bool GROUPED>
 __global__ void __launch_bounds__(256, 1)
     gemm_tensor_kernel(const __grid_constant__ CUtensorMap tmA,
-                       const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                       const __grid_constant__ CUtensorMap tmB, const __grid_constant__ GemmParams p,
+                       const __grid_constant__ CUtensorMap tmA2,
+                       const __grid_constant__ CUtensorMap tmB2,
+                       const __grid_constant__ GemmParams p2) {
     ptx::griddep_launch_dependents();   // the next kernel may launch now
     using L = Layout<BN, STAGES>;
     constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -378,6 +353,8 @@ __global__ void __launch_bounds__(256, 1)
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t1 = p.num_m * p.num_n;
+    const int num_units = GROUPED ? t1 + p2.num_m * p2.num_n : t1;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&full[s], 1);
@@ -394,6 +371,10 @@ __global__ void __launch_bounds__(256, 1)
     if (warp == 0 && lane == 0) {
         ptx::tma_prefetch_desc(&tmA);
         ptx::tma_prefetch_desc(&tmB);
+        if (GROUPED && num_units > t1) {
+            ptx::tma_prefetch_desc(&tmA2);
+            ptx::tma_prefetch_desc(&tmB2);
+        }
     }
     if (warp == 2) {
         ptx::tmem_alloc(tmem_slot, TMEM_COLS);
@@ -404,29 +385,71 @@ __global__ void __launch_bounds__(256, 1)
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     ptx::griddep_wait();   // the previous kernel's results (operands, factors) are visible
-    const int num_tiles = p.num_m * p.num_n;
 
     if (warp == 0) {
-        if (lane == 0) producer<BN, STAGES, kTensorGroup>(&tmA, &tmB, ring, full, empty, p, abort_flag);
+        if (lane == 0) {
+            // producer: the A / B tiles of every K block of this CTA's units
+            uint32_t stage = 0, phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+                const bool second = GROUPED && u >= t1;
+                const GemmParams& q = second ? p2 : p;
+                const CUtensorMap* ma = second ? &tmA2 : &tmA;
+                const CUtensorMap* mb = second ? &tmB2 : &tmB;
+                int m_blk, n_blk;
+                tile_coords<kTensorGroup>(second ? u - t1 : u, q.num_m, q.num_n, m_blk, n_blk);
+                const int ya = m_blk * BM, yb = n_blk * BN;
+                for (int kb = 0; kb < q.num_kb; ++kb) {
+                    if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+                    uint8_t* sa = ring + stage * L::STAGE_BYTES;
+                    ptx::mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+                    const int kx = kb * BK;
+                    ptx::tma_load_2d(sa, ma, &full[stage], q.a_mn ? ya : kx, q.a_mn ? kx : ya);
+                    ptx::tma_load_2d(sa + L::A_BYTES, mb, &full[stage], q.b_mn ? yb : kx,
+                                     q.b_mn ? kx : yb);
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // drain: the last copy issued into each slot must have landed
+            uint32_t never = 0;
+            for (int s = 0; s < STAGES; ++s) {
+                if (issued <= s && issued < STAGES) break;
+                const uint32_t par = (static_cast<uint32_t>(s) < stage) ? phase : (phase ^ 1u);
+                ptx::mbar_wait(&full[s], par, &never);
+            }
+        }
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc = ptx::idesc_f8f6f4(p.fa, p.fb, BM, BN);
+            const uint32_t idesc1 = ptx::idesc_f8f6f4(p.fa, p.fb, BM, BN, p.a_mn, p.b_mn);
+            const uint32_t idesc2 = ptx::idesc_f8f6f4(p2.fa, p2.fb, BM, BN, p2.a_mn, p2.b_mn);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+                const bool second = GROUPED && u >= t1;
+                const int num_kb = second ? p2.num_kb : p.num_kb;
+                const uint32_t idesc = second ? idesc2 : idesc1;
+                const bool a_mn = (second ? p2.a_mn : p.a_mn) != 0;
+                const bool b_mn = (second ? p2.b_mn : p.b_mn) != 0;
+                // descriptor advance per MMA of K = 32, in 16-byte units: 32
+                // bytes along a K-major row, or 32 rows of 128 bytes MN-major
+                const uint32_t a_step = a_mn ? (UMMA_K * 128) >> 4 : UMMA_K >> 4;
+                const uint32_t b_step = b_mn ? (UMMA_K * 128) >> 4 : UMMA_K >> 4;
+                const uint64_t a_tmpl = a_mn ? ptx::sdesc_mnmajor_sw128(0) : ptx::sdesc_kmajor_sw128(0);
+                const uint64_t b_tmpl = b_mn ? ptx::sdesc_mnmajor_sw128(0) : ptx::sdesc_kmajor_sw128(0);
                 if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) break;
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + acc * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = 0; kb < num_kb; ++kb) {
                     if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
                     ptx::tc_fence_after();
                     uint8_t* sa = ring + stage * L::STAGE_BYTES;
-                    const uint64_t ad = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa));
-                    const uint64_t bd = ptx::sdesc_kmajor_sw128(ptx::smem_u32(sa + L::A_BYTES));
+                    const uint64_t ad = a_tmpl | ((ptx::smem_u32(sa) & 0x3FFFFu) >> 4);
+                    const uint64_t bd = b_tmpl | ((ptx::smem_u32(sa + L::A_BYTES) & 0x3FFFFu) >> 4);
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k)
-                        ptx::mma_f8f6f4(d, ad + (k * UMMA_K >> 4), bd + (k * UMMA_K >> 4), idesc,
-                                        (kb | k) != 0);
+                        ptx::mma_f8f6f4(d, ad + k * a_step, bd + k * b_step, idesc, (kb | k) != 0);
                     ptx::mma_commit(&empty[stage]);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -444,14 +467,16 @@ __global__ void __launch_bounds__(256, 1)
         const int qd = warp & 3;  // TMEM lane quadrant this warp may access
         const int row = qd * 32 + lane;
         uint32_t acc = 0, acc_phase = 0;
-        const bool rmw = p.out == FP8_OUT_F32 && p.accumulate;
         const uint64_t wait_ns = g_epilogue_wait_ns;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+            const bool second = GROUPED && u >= t1;
+            const GemmParams& q = second ? p2 : p;   // this unit's problem
+            const bool rmw = q.out == FP8_OUT_F32 && q.accumulate;
             int m_blk, n_blk;
-            tile_coords<kTensorGroup>(tile, p.num_m, p.num_n, m_blk, n_blk);   // as the producer
+            tile_coords<kTensorGroup>(second ? u - t1 : u, q.num_m, q.num_n, m_blk, n_blk);
             if (rmw)
                 prefetch_row(static_cast<int64_t>(m_blk) * BM + row, static_cast<int64_t>(n_blk) * BN,
-                             BN, p);
+                             BN, q);
             bool ok = (lane == 0) ? ptx::mbar_wait(&tfull[acc], acc_phase, abort_flag, wait_ns)
                                   : false;
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -459,7 +484,7 @@ __global__ void __launch_bounds__(256, 1)
             __syncwarp();
             ptx::tc_fence_after();
             const int64_t m = static_cast<int64_t>(m_blk) * BM + row;
-            const float fa = row_factor(p, m);
+            const float fa = row_factor(q, m);
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + acc * BN;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
@@ -468,8 +493,8 @@ __global__ void __launch_bounds__(256, 1)
                 ptx::tmem_wait_ld();
                 const int64_t n0 = static_cast<int64_t>(n_blk) * BN + c * 32;
                 float f[32];
-                chunk_factors(f, fa, n0, p);
-                if (m < p.M) store_chunk(r, m, n0, p, f, rmw);
+                chunk_factors(f, fa, n0, q);
+                if (m < q.M) store_chunk(r, m, n0, q, f, rmw);
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -1684,7 +1709,7 @@ constexpr int64_t kPairMinRows = 256;
 template <typename Kernel>
 int ensure_smem(Kernel k, int bytes, int kernel_id) {
     static std::mutex mu;
-    static bool done[64][8] = {};   // [device][kernel id]: every GEMM kernel has this one type
+    static bool done[64][16] = {};   // [device][kernel id]: every GEMM kernel has this one type
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
     const bool cached = dev >= 0 && dev < 64;   // other devices: set it on every call
@@ -1854,6 +1879,49 @@ int launch_gemm_block(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_
 
 }  // namespace
 
+namespace {
+
+// Column tile of the single-CTA kernel when an M x N problem's 128-row tiles
+// fit in one wave (at most one CTA per SM): 64 where those fit and both
+// operands are K-major, else 128 (which also reads MN-major operands); 0
+// when neither fits.  Eight or four CTAs per 256 x 256 pair tile, each with
+// an eighth or a quarter of its MMAs and epilogue: a small layer's GEMMs,
+// where latency is the cost.
+int one_wave_bn(int64_t M, int64_t N, bool mn_major) {
+    const int64_t sms = num_sms(), rows = (M + BM - 1) / BM;
+    if (!mn_major && rows * ((N + kTinyBN - 1) / kTinyBN) <= sms) return kTinyBN;
+    if (rows * ((N + kSmallBN - 1) / kSmallBN) <= sms) return kSmallBN;
+    return 0;
+}
+
+// Launch of the single-CTA kernel with BN-column tiles: problem p1 (and,
+// GROUPED, p2 in the same launch; 128-column tiles only).
+template <bool GROUPED>
+int launch_tensor(int BN, int grid, cudaStream_t stream, const CUtensorMap& a1,
+                  const CUtensorMap& b1, const GemmParams& p1, const CUtensorMap& a2,
+                  const CUtensorMap& b2, const GemmParams& p2) {
+    int st;
+    if (GROUPED || BN == kSmallBN) {
+        using L = Layout<kSmallBN, kTensorStages>;
+        auto k = gemm_tensor_kernel<kSmallBN, kTensorStages, GROUPED>;
+        if ((st = ensure_smem(k, L::SMEM_BYTES, GROUPED ? 8 : 6)) != FP8_OK) return st;
+        launch_pdl(k, dim3(grid), dim3(256), L::SMEM_BYTES, stream, a1, b1, p1, a2, b2, p2);
+    } else if (BN == kTinyBN) {
+        using L = Layout<kTinyBN, kTensorStages>;
+        auto k = gemm_tensor_kernel<kTinyBN, kTensorStages, false>;
+        if ((st = ensure_smem(k, L::SMEM_BYTES, 7)) != FP8_OK) return st;
+        launch_pdl(k, dim3(grid), dim3(256), L::SMEM_BYTES, stream, a1, b1, p1, a2, b2, p2);
+    } else {
+        using L = Layout<kTensorBN, kTensorStages>;
+        auto k = gemm_tensor_kernel<kTensorBN, kTensorStages, false>;
+        if ((st = ensure_smem(k, L::SMEM_BYTES, 0)) != FP8_OK) return st;
+        launch_pdl(k, dim3(grid), dim3(256), L::SMEM_BYTES, stream, a1, b1, p1, a2, b2, p2);
+    }
+    return FP8_OK;
+}
+
+}  // namespace
+
 int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, int64_t N,
                 int64_t K, int ga, const float* sa, int gb, const float* sb, const void* bias,
                 void* D, int out, int accumulate, cudaStream_t stream, int layout) {
@@ -1888,21 +1956,15 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
     if (block)
         return launch_gemm_block(A, fa, B, fb, M, N, K, ga, sa, gb, sb, bias, D, out, accumulate,
                                  stream);
-    // per-tensor and per-row scales: CTA pairs for every problem of at least
-    // 256 rows, and for every MN-major operand (the single-CTA kernel reads
-    // K-major tiles only; rows past M are zero-filled and not stored).  A
-    // K-major problem whose 128 x 64 tiles (else 128 x 128 tiles) fit in one
-    // wave (at most one per SM) takes the single-CTA kernel with those tiles
-    // instead: eight (four) CTAs per 256 x 256 pair tile, each with an eighth
-    // (a quarter) of its MMAs and epilogue -- a small layer's forward GEMM,
-    // where latency is the cost
-    const int64_t sms = num_sms(), row_tiles = (M + BM - 1) / BM;
-    const int one_wave_bn = (a_mn || b_mn) ? 0
-                            : row_tiles * ((N + kTinyBN - 1) / kTinyBN) <= sms ? kTinyBN
-                            : row_tiles * ((N + kSmallBN - 1) / kSmallBN) <= sms ? kSmallBN
-                                                                                 : 0;
-    const bool pair = (M >= kPairMinRows && !one_wave_bn) || a_mn || b_mn;
-    const int BN = one_wave_bn ? one_wave_bn : kTensorBN;
+    // per-tensor and per-row scales.  A problem whose 128-row tiles fit in
+    // one wave (at most one CTA per SM) runs on the single-CTA kernel (see
+    // one_wave_bn); otherwise CTA pairs for every problem of at least 256 rows
+    // or with an MN-major operand, and the single-CTA kernel with 128 x 256
+    // tiles for the rest (K-major, M < 256; rows past M are zero-filled and
+    // not stored)
+    const int one_bn = one_wave_bn(M, N, a_mn || b_mn);
+    const bool pair = !one_bn && (M >= kPairMinRows || a_mn || b_mn);
+    const int BN = one_bn ? one_bn : kTensorBN;
     const int TM = pair ? 256 : BM;   // rows of C per tile
     GemmParams p;
     p.M = M; p.N = N; p.K = K;
@@ -1933,21 +1995,8 @@ int launch_gemm(const uint8_t* A, int fa, const uint8_t* B, int fb, int64_t M, i
         const int pgrid = static_cast<int>(2 * (tiles < clusters ? tiles : clusters));
         GemmParams none{};
         launch_pdl(k, dim3(pgrid), dim3(256), kPairSmemBytes, stream, tmA, tmB, tmD, p, tmA, tmB, tmD, none);
-    } else if (BN == kTinyBN) {
-        using L = Layout<kTinyBN, kTensorStages>;
-        auto k = gemm_tensor_kernel<kTinyBN, kTensorStages>;
-        if ((st = ensure_smem(k, L::SMEM_BYTES, 7)) != FP8_OK) return st;
-        launch_pdl(k, dim3(grid), dim3(256), L::SMEM_BYTES, stream, tmA, tmB, p);
-    } else if (BN == kSmallBN) {
-        using L = Layout<kSmallBN, kTensorStages>;
-        auto k = gemm_tensor_kernel<kSmallBN, kTensorStages>;
-        if ((st = ensure_smem(k, L::SMEM_BYTES, 6)) != FP8_OK) return st;
-        launch_pdl(k, dim3(grid), dim3(256), L::SMEM_BYTES, stream, tmA, tmB, p);
-    } else {
-        using L = Layout<kTensorBN, kTensorStages>;
-        auto k = gemm_tensor_kernel<kTensorBN, kTensorStages>;
-        if ((st = ensure_smem(k, L::SMEM_BYTES, 0)) != FP8_OK) return st;
-        launch_pdl(k, dim3(grid), dim3(256), L::SMEM_BYTES, stream, tmA, tmB, p);
+    } else if ((st = launch_tensor<false>(BN, grid, stream, tmA, tmB, p, tmA, tmB, p)) != FP8_OK) {
+        return st;
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(FP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
@@ -1986,9 +2035,56 @@ int pair_params(const GemmArgs& g, GemmParams& p, CUtensorMap& tmA, CUtensorMap&
     return make_store_map(&tmD, g.D, g.M, g.N, g.out);
 }
 
+// Parameters and tensor maps of one problem for the single-CTA kernel with
+// BN-column tiles (MN-major operands need BN = 128).
+int tensor_params(const GemmArgs& g, int BN, GemmParams& p, CUtensorMap& tmA, CUtensorMap& tmB) {
+    p = GemmParams{};
+    p.M = g.M; p.N = g.N; p.K = g.K;
+    p.num_m = static_cast<int>((g.M + BM - 1) / BM);
+    p.num_n = static_cast<int>((g.N + BN - 1) / BN);
+    p.num_kb = static_cast<int>((g.K + BK - 1) / BK);
+    p.fa = g.fa; p.fb = g.fb; p.ga = g.ga; p.gb = g.gb; p.sa = g.sa; p.sb = g.sb;
+    p.bias = static_cast<const __nv_bfloat16*>(g.bias);
+    p.D = g.D; p.out = g.out; p.accumulate = g.accumulate;
+    p.a_mn = (g.layout & FP8_LAYOUT_A_KM) != 0;
+    p.b_mn = (g.layout & FP8_LAYOUT_B_KN) != 0;
+    int st = p.a_mn ? make_mnmajor_map(&tmA, g.A, g.M, g.K) : make_kmajor_map(&tmA, g.A, g.M, g.K, BM);
+    if (st != FP8_OK) return st;
+    return p.b_mn ? make_mnmajor_map(&tmB, g.B, g.N, g.K) : make_kmajor_map(&tmB, g.B, g.N, g.K, BN);
+}
+
+// Two problems that one launch of the single-CTA kernel takes: per-tensor or
+// per-row scales, nonempty, no bias, and their 128 x 128 tiles together in
+// one wave (a small layer's dgrad and wgrad).
+bool one_wave_group(const GemmArgs& g1, const GemmArgs& g2) {
+    auto ok = [](const GemmArgs& g) {
+        const int ga = g.ga & ~FP8_SCALE_POW2, gb = g.gb & ~FP8_SCALE_POW2;
+        const bool block = ga == FP8_GRAN_1x128 || ga == FP8_GRAN_128x128 ||
+                           gb == FP8_GRAN_1x128 || gb == FP8_GRAN_128x128;
+        return !block && g.M > 0 && g.N > 0 && g.K > 0 && !g.bias;
+    };
+    auto tiles = [](const GemmArgs& g) {
+        return ((g.M + BM - 1) / BM) * ((g.N + kSmallBN - 1) / kSmallBN);
+    };
+    return ok(g1) && ok(g2) && tiles(g1) + tiles(g2) <= num_sms();
+}
+
 }  // namespace
 
 int launch_gemm_group(const GemmArgs& g1, const GemmArgs& g2, cudaStream_t stream) {
+    if (one_wave_group(g1, g2)) {
+        GemmParams p1, p2;
+        CUtensorMap a1, b1, a2, b2;
+        int st = tensor_params(g1, kSmallBN, p1, a1, b1);
+        if (st == FP8_OK) st = tensor_params(g2, kSmallBN, p2, a2, b2);
+        if (st != FP8_OK) return st;
+        const int units = p1.num_m * p1.num_n + p2.num_m * p2.num_n;
+        if ((st = launch_tensor<true>(kSmallBN, units, stream, a1, b1, p1, a2, b2, p2)) != FP8_OK)
+            return st;
+        const cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? FP8_OK
+                                : set_error(FP8_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+    }
     if (!pair_eligible(g1) || !pair_eligible(g2)) {
         int st = launch_gemm(g1.A, g1.fa, g1.B, g1.fb, g1.M, g1.N, g1.K, g1.ga, g1.sa, g1.gb,
                              g1.sb, g1.bias, g1.D, g1.out, g1.accumulate, stream, g1.layout);
