@@ -369,11 +369,14 @@ def _rand_codes(shape, seed):
 
 
 @pytest.mark.parametrize("case", ["bwd_like", "ragged", "rowscaled", "fallback_block", "small_m",
-                                  "pow2_block_bwd", "bwd_mn_major", "small_m_mn_major"])
+                                  "pow2_block_bwd", "bwd_mn_major", "small_m_mn_major",
+                                  "bwd_mn_major_large"])
 def test_gemm_group_equals_two_gemms(case):
     """fp8_gemm_group gives, bit for bit, the results of two fp8_gemm calls:
-    the grouped CTA-pair launch computes every tile exactly as the single
-    launch does; problems it does not take fall back to two launches."""
+    a grouped launch -- the single-CTA kernel when both problems' 128 x 128
+    tiles fit in one wave, else CTA pairs (bwd_mn_major_large) -- computes
+    every tile exactly as a single launch does; problems it does not take
+    fall back to two launches."""
     one = torch.ones(1, dtype=torch.float32, device=DEV)
     if case == "bwd_like":        # dgrad (bf16) and wgrad (FP32, accumulated) of a linear
         M, N, K = 1024, 768, 640
@@ -421,7 +424,15 @@ def test_gemm_group_equals_two_gemms(case):
         g2 = dict(A=dy, fa=F.E5M2, B=x, fb=F.E4M3, scale_inv_a=one * 2 ** -7,
                   scale_inv_b=one * 2 ** -6, out=F.OUT_F32, accumulate=True,
                   layout=F.LAYOUT_KM_KN)
-    elif case == "small_m_mn_major":   # fewer than 256 rows: still one CTA-pair launch
+    elif case == "bwd_mn_major_large":   # 192 + 144 tiles of 128 x 128: the grouped CTA pairs
+        M, N, K = 2048, 1536, 1536
+        dy, w, x = _rand_codes((M, N), 32), _rand_codes((N, K), 33), _rand_codes((M, K), 34)
+        g1 = dict(A=dy, fa=F.E5M2, B=w, fb=F.E4M3, scale_inv_a=one * 2 ** -7,
+                  scale_inv_b=one * 2 ** -5, layout=F.LAYOUT_B_KN)
+        g2 = dict(A=dy, fa=F.E5M2, B=x, fb=F.E4M3, scale_inv_a=one * 2 ** -7,
+                  scale_inv_b=one * 2 ** -6, out=F.OUT_F32, accumulate=True,
+                  layout=F.LAYOUT_KM_KN)
+    elif case == "small_m_mn_major":   # fewer than 256 rows, MN-major: one grouped launch
         g1 = dict(A=_rand_codes((640, 96), 28), fa=F.E5M2, B=_rand_codes((640, 512), 29),
                   fb=F.E4M3, scale_inv_a=one, scale_inv_b=one, out=F.OUT_F32,
                   layout=F.LAYOUT_KM_KN)
