@@ -284,11 +284,13 @@ typedef struct {
 
 /* Two independent GEMMs in one launch: the same results, bit for bit, as
  * fp8_gemm(g1) followed by fp8_gemm(g2).  When both are per-tensor / per-row
- * problems of at least 256 rows without bias, one persistent CTA-pair grid
- * deals both problems' 256 x 256 tiles from one list, the deeper problem's
- * first, so that neither leaves a partly filled last wave of its own (the
- * dgrad and wgrad of a backward pass are such a pair); otherwise the two run
- * as two launches.  The problems run concurrently: neither may read or
+ * problems without bias whose 128 x 128 tiles fit together in one wave (at
+ * most one per SM), one single-CTA launch takes both problems' tiles; when
+ * both have at least 256 rows or an MN-major operand, one persistent CTA-pair
+ * grid deals both problems' 256 x 256 tiles from one list, the deeper
+ * problem's first, so that neither leaves a partly filled last wave of its
+ * own (the dgrad and wgrad of a backward pass are such a pair); otherwise
+ * the two run as two launches.  The problems run concurrently: neither may read or
  * write the other's output.  Each is validated as by fp8_gemm; NULL g1 or
  * g2 is FP8_ERR_INVALID_ARG.  (The pages have no counterpart: this is a
  * scheduling property of the library -- the dgrad and wgrad GEMMs of
